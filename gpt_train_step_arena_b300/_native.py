@@ -1,0 +1,65 @@
+"""ctypes binding of include/gpt2.h: loads the in-tree libgpt2_b300.so and declares
+every entry point.  Argument marshalling only; there is no other code path.
+
+Importing this module raises if the library has not been built (run
+``python -m gpt_train_step_arena_b300.build`` or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgpt2_b300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                      "(python -m gpt_train_step_arena_b300.build)")
+
+lib = ct.CDLL(LIB_PATH)
+
+P, I, U64, SZ, F = ct.c_void_p, ct.c_int, ct.c_uint64, ct.c_size_t, ct.c_float
+
+# name: (restype, argtypes) — mirrors include/gpt2.h
+SIGNATURES = {
+    "gpt2_build_ex": (P, [I, I, I, I, I, I, ct.POINTER(I)]),
+    "gpt2_build": (P, [I, I, I, I, I]),
+    "gpt2_free": (None, [P]),
+    "gpt2_num_params": (SZ, [P]),
+    "gpt2_padded_vocab": (I, [P]),
+    "gpt2_set_params": (I, [P, P, SZ]),
+    "gpt2_get_params": (I, [P, P, SZ]),
+    "gpt2_get_grads": (I, [P, P, SZ]),
+    "gpt2_get_opt_state": (I, [P, P, P, SZ]),
+    "gpt2_forward": (F, [P, P, P, I, I]),
+    "gpt2_forward_async": (I, [P, P, P, I, I, I]),
+    "gpt2_read_loss": (I, [P, ct.POINTER(F)]),
+    "gpt2_backward": (I, [P]),
+    "gpt2_zero_grad": (I, [P]),
+    "gpt2_update": (I, [P, F, F, F, F, F, I]),
+    "gpt2_get_losses": (I, [P, P, SZ]),
+    "gpt2_get_logits": (I, [P, P, SZ]),
+    "gpt2_get_ids": (I, [P, P, P, SZ]),
+    "gpt2_set_stream": (I, [P, P]),
+    "gpt2_sync": (I, [P]),
+    "gpt2_last_status": (I, [P]),
+    "gpt2_last_error": (ct.c_char_p, [P]),
+    "gpt2_last_build_error": (ct.c_char_p, []),
+    "gpt2_kernel_launches": (U64, [P]),
+    "gpt2_device_bytes": (SZ, [P]),
+}
+
+for _name, (_res, _args) in SIGNATURES.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+# enum values of include/gpt2.h
+GPT2_OK, GPT2_ERR_ARG, GPT2_ERR_OOM, GPT2_ERR_CUDA = 0, -1, -2, -3
+GPT2_ERR_TOKEN, GPT2_ERR_SHAPE, GPT2_ERR_STATE, GPT2_ERR_NONFINITE, GPT2_ERR_TIMEOUT = -4, -5, -6, -7, -8
+GPT2_FP32, GPT2_BF16 = 0, 2
+GPT2_HOST, GPT2_DEVICE = 0, 1
+
+STATUS_NAMES = {0: "GPT2_OK", -1: "GPT2_ERR_ARG", -2: "GPT2_ERR_OOM", -3: "GPT2_ERR_CUDA",
+                -4: "GPT2_ERR_TOKEN", -5: "GPT2_ERR_SHAPE", -6: "GPT2_ERR_STATE",
+                -7: "GPT2_ERR_NONFINITE", -8: "GPT2_ERR_TIMEOUT"}

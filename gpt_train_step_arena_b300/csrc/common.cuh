@@ -1,0 +1,89 @@
+// Shared device helpers for the GPT-2 train-step kernels (sm_103a).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+typedef __nv_bfloat16 bf16;
+
+#define G2_DEV __device__ __forceinline__
+
+namespace g2 { void count_launches(unsigned n); }
+// Prefix of every kernel launch statement: counts the launch, then launches
+// (comma expression, so it stays one statement under an unbraced if/else).
+#define G2_LAUNCH ::g2::count_launches(1),
+
+G2_DEV float to_f(float x) { return x; }
+G2_DEV float to_f(bf16 x) { return __bfloat162float(x); }
+
+template <typename T> G2_DEV T from_f(float x);
+template <> G2_DEV float from_f<float>(float x) { return x; }
+template <> G2_DEV bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+G2_DEV float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+G2_DEV float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// 8 consecutive elements moved as one 16-byte (bf16) or two 16-byte (fp32) accesses.
+template <typename T> struct Vec8;
+template <> struct Vec8<bf16> {
+    static G2_DEV void load(const bf16* p, float* f) {
+        uint4 u = *reinterpret_cast<const uint4*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float2 t = __bfloat1622float2(h[i]);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+    static G2_DEV void store(bf16* p, const float* f) {
+        uint4 u;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; i++) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        *reinterpret_cast<uint4*>(p) = u;
+    }
+};
+template <> struct Vec8<float> {
+    static G2_DEV void load(const float* p, float* f) {
+        float4 a = *reinterpret_cast<const float4*>(p);
+        float4 b = *reinterpret_cast<const float4*>(p + 4);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+    static G2_DEV void store(float* p, const float* f) {
+        *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<float4*>(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
+    }
+};
+
+// GELU, tanh form (llm.c annotated listing §1.9; picoGPT gelu).
+G2_DEV float gelu_tanh(float x) {
+    const float k = 0.7978845608028654f;  // sqrt(2/pi)
+    float u = k * (x + 0.044715f * x * x * x);
+    return 0.5f * x * (1.0f + tanhf(u));
+}
+// Its derivative (llm.c §1.10) with sech^2(u) written as 1 - tanh^2(u).
+G2_DEV float gelu_tanh_grad(float x) {
+    const float k = 0.7978845608028654f;
+    float u = k * (x + 0.044715f * x * x * x);
+    float th = tanhf(u);
+    float sech2 = 1.0f - th * th;
+    return 0.5f * (1.0f + th) + x * 0.5f * sech2 * k * (1.0f + 3.0f * 0.044715f * x * x);
+}
+
+// Device-side error flags (bitwise OR into one int): never trap, the host reads them.
+enum {
+    G2_FLAG_BAD_TOKEN = 1,
+    G2_FLAG_BAD_TARGET = 2,
+    G2_FLAG_NONFINITE = 4,
+    G2_FLAG_TIMEOUT = 8,
+};

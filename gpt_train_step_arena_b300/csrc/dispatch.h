@@ -1,0 +1,19 @@
+// Choice of kernel for the two contraction-shaped steps (GEMM, attention).
+#pragma once
+#include "kernels.h"
+
+namespace g2 {
+
+// Device workspace the GEMM path needs for a model of this size (split-K partials).
+size_t gemm_workspace_bytes(int M, int C, int Vp, int L);
+// Runs D = epi(A . B^T) on the fastest kernel that takes the shape: the tcgen05
+// tensor-core kernel for bf16 operands it supports, the SIMT kernel otherwise.
+cudaError_t gemm_dispatch(const GemmArgs& a, float* ws, size_t ws_bytes, cudaStream_t s);
+
+cudaError_t attention_forward(ActType at, void* out, float* lse, const void* qkv, int B, int T,
+                              int C, int NH, cudaStream_t s);
+cudaError_t attention_backward(ActType at, void* dqkv, const void* dout, const void* qkv,
+                               const void* out, const float* lse, int B, int T, int C, int NH,
+                               float* scratch_D, cudaStream_t s);
+
+}  // namespace g2

@@ -1,0 +1,726 @@
+// Memory-bound kernels of the GPT-2 train step: ids check, encoder forward and
+// backward, layernorm forward and backward, bias-gradient column sums, fused
+// softmax-cross-entropy, fixed-order mean, AdamW.
+//
+// Determinism: no float atomics anywhere.  Every cross-thread float sum runs in
+// an order fixed by the launch shape (which depends only on the problem size).
+#include "common.cuh"
+#include "kernels.h"
+
+#include <algorithm>
+
+namespace g2 {
+
+static inline unsigned cdiv(size_t a, size_t b) { return (unsigned)((a + b - 1) / b); }
+
+// ------------------------------------------------------------------ ids check
+__global__ void check_ids_k(const int32_t* ids, int M, int V, int* flags, int bit) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < M && (unsigned)ids[i] >= (unsigned)V) atomicOr(flags, bit);
+}
+cudaError_t check_ids(const int32_t* ids, int M, int V, int* flags, int bit, cudaStream_t s) {
+    if (M <= 0) return cudaSuccess;
+    G2_LAUNCH check_ids_k<<<cdiv(M, 256), 256, 0, s>>>(ids, M, V, flags, bit);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ encoder forward
+// llm.c §1.1: out[b,t,:] = wte[tok[b,t],:] + wpe[t,:].  One warp per position.  An id
+// outside [0,V) raises the flag and contributes a zero token row (no read).
+template <typename T>
+__global__ void encoder_fwd_k(T* out, const int32_t* tok, const T* wte, const T* wpe, int M,
+                              int Tn, int C, int V, int* flags) {
+    int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (row >= M) return;
+    int id = tok[row];
+    bool ok = (unsigned)id < (unsigned)V;
+    if (!ok && lane == 0) atomicOr(flags, G2_FLAG_BAD_TOKEN);
+    int t = row % Tn;
+    const T* a = wte + (size_t)(ok ? id : 0) * C;
+    const T* p = wpe + (size_t)t * C;
+    T* o = out + (size_t)row * C;
+    if ((C & 7) == 0) {
+        for (int c = lane * 8; c < C; c += 256) {
+            float x[8], y[8];
+            Vec8<T>::load(p + c, y);
+            if (ok) {
+                Vec8<T>::load(a + c, x);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; i++) x[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; i++) x[i] += y[i];
+            Vec8<T>::store(o + c, x);
+        }
+    } else {
+        for (int c = lane; c < C; c += 32) o[c] = from_f<T>((ok ? to_f(a[c]) : 0.f) + to_f(p[c]));
+    }
+}
+
+cudaError_t encoder_forward(ActType at, void* out, const int32_t* tok, const void* wte,
+                            const void* wpe, int B, int T, int C, int V, int* flags, cudaStream_t s) {
+    int M = B * T;
+    if (M <= 0) return cudaSuccess;
+    if (at == ACT_BF16)
+        G2_LAUNCH encoder_fwd_k<bf16><<<cdiv(M, 8), 256, 0, s>>>((bf16*)out, tok, (const bf16*)wte,
+                                                        (const bf16*)wpe, M, T, C, V, flags);
+    else
+        G2_LAUNCH encoder_fwd_k<float><<<cdiv(M, 8), 256, 0, s>>>((float*)out, tok, (const float*)wte,
+                                                         (const float*)wpe, M, T, C, V, flags);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ encoder backward: dwpe
+// llm.c §1.2, position half: dwpe[t,c] = sum over b (ascending) of dout[b,t,c].
+template <typename T>
+__global__ void encoder_bwd_wpe_k(float* dwpe, const T* dout, int B, int Tn, int C, int maxT) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (size_t)maxT * C) return;
+    int t = (int)(i / C), c = (int)(i % C);
+    float acc = 0.f;
+    if (t < Tn)
+        for (int b = 0; b < B; b++) acc += to_f(dout[((size_t)b * Tn + t) * C + c]);
+    dwpe[i] = acc;
+}
+cudaError_t encoder_backward_wpe(ActType at, float* dwpe, const void* dout, int B, int T, int C,
+                                 int maxT, cudaStream_t s) {
+    size_t n = (size_t)maxT * C;
+    if (at == ACT_BF16)
+        G2_LAUNCH encoder_bwd_wpe_k<bf16><<<cdiv(n, 256), 256, 0, s>>>(dwpe, (const bf16*)dout, B, T, C, maxT);
+    else
+        G2_LAUNCH encoder_bwd_wpe_k<float><<<cdiv(n, 256), 256, 0, s>>>(dwpe, (const float*)dout, B, T, C, maxT);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ encoder backward: dwte
+// llm.c §1.2, token half, made deterministic: positions are bucketed by token id with a
+// stable integer counting sort (integer atomics give exact counts; ranks inside a chunk
+// come from a position-ordered compare, so each bucket lists its positions in ascending
+// order), then each bucket's rows are summed in that order in segments of SEG rows and
+// the segment sums are added in segment order.
+static const int ENC_CHUNK = 1024;  // positions per ranking chunk (one block)
+static const int ENC_SEG = 64;      // positions per summed segment (one warp)
+
+static inline int enc_nchunks(int M) { return (M + ENC_CHUNK - 1) / ENC_CHUNK; }
+static inline int enc_max_items(int M, int V) { return M / ENC_SEG + (M < V ? M : V) + 1; }
+
+size_t encoder_bwd_scratch_bytes(int M, int V, int C) {
+    size_t ints = (size_t)enc_nchunks(M) * V + V + 2 * (V + 1) + enc_max_items(M, V) + M;
+    size_t bytes = ((ints * 4 + 255) / 256) * 256;
+    return bytes + (size_t)enc_max_items(M, V) * C * 4;
+}
+void encoder_bwd_scratch_carve(EncoderBwdScratch* sc, void* base, int M, int V, int C) {
+    int* p = (int*)base;
+    sc->chunk_cnt = p; p += (size_t)enc_nchunks(M) * V;
+    sc->cnt = p; p += V;
+    sc->start = p; p += V + 1;
+    sc->item_start = p; p += V + 1;
+    sc->max_items = enc_max_items(M, V);
+    sc->item_tok = p; p += sc->max_items;
+    sc->perm = p; p += M;
+    size_t ints = (size_t)(p - (int*)base);
+    sc->partial = (float*)((char*)base + ((ints * 4 + 255) / 256) * 256);
+}
+
+__global__ void enc_hist_k(int* chunk_cnt, const int32_t* tok, int M, int V) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= M) return;
+    int id = tok[i];
+    if ((unsigned)id < (unsigned)V) atomicAdd(&chunk_cnt[(size_t)(i / ENC_CHUNK) * V + id], 1);
+}
+
+// Per token: prefix over chunks (in place: chunk_cnt becomes exclusive chunk prefix)
+// and total count.
+__global__ void enc_chunk_prefix_k(int* chunk_cnt, int* cnt, int nchunks, int V) {
+    int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= V) return;
+    int run = 0;
+    for (int c = 0; c < nchunks; c++) {
+        int x = chunk_cnt[(size_t)c * V + k];
+        chunk_cnt[(size_t)c * V + k] = run;
+        run += x;
+    }
+    cnt[k] = run;
+}
+
+// Single block: exclusive scans of cnt (-> start) and of ceil(cnt/SEG) (-> item_start).
+__global__ void enc_scan_k(const int* cnt, int* start, int* item_start, int V) {
+    __shared__ int s_a[1024], s_b[1024];
+    int tid = threadIdx.x, nt = blockDim.x;
+    int per = (V + nt - 1) / nt;
+    int lo = tid * per, hi = min(V, lo + per);
+    int a = 0, b = 0;
+    for (int k = lo; k < hi; k++) {
+        a += cnt[k];
+        b += (cnt[k] + ENC_SEG - 1) / ENC_SEG;
+    }
+    s_a[tid] = a;
+    s_b[tid] = b;
+    __syncthreads();
+    for (int off = 1; off < nt; off <<= 1) {  // Hillis-Steele inclusive scan
+        int ta = tid >= off ? s_a[tid - off] : 0;
+        int tb = tid >= off ? s_b[tid - off] : 0;
+        __syncthreads();
+        s_a[tid] += ta;
+        s_b[tid] += tb;
+        __syncthreads();
+    }
+    int ra = s_a[tid] - a, rb = s_b[tid] - b;
+    for (int k = lo; k < hi; k++) {
+        start[k] = ra;
+        item_start[k] = rb;
+        ra += cnt[k];
+        rb += (cnt[k] + ENC_SEG - 1) / ENC_SEG;
+    }
+    if (tid == nt - 1) {
+        start[V] = s_a[nt - 1];
+        item_start[V] = s_b[nt - 1];
+    }
+}
+
+// One block per chunk: stable destination of every position of the chunk.
+__global__ void enc_rank_k(int* perm, const int32_t* tok, const int* start, const int* chunk_pref,
+                           int M, int V) {
+    __shared__ int s_tok[ENC_CHUNK];
+    int c = blockIdx.x, base = c * ENC_CHUNK, n = min(ENC_CHUNK, M - base);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) s_tok[i] = tok[base + i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        int id = s_tok[i];
+        if ((unsigned)id >= (unsigned)V) continue;
+        int r = 0;
+        for (int j = 0; j < i; j++) r += s_tok[j] == id;
+        perm[start[id] + chunk_pref[(size_t)c * V + id] + r] = base + i;
+    }
+}
+
+__global__ void enc_items_k(int* item_tok, const int* cnt, const int* item_start, int V) {
+    int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= V) return;
+    int n = (cnt[k] + ENC_SEG - 1) / ENC_SEG;
+    for (int j = 0; j < n; j++) item_tok[item_start[k] + j] = k;
+}
+
+// One warp per item (a segment of one bucket).  Single-segment buckets add straight into
+// dwte; longer buckets leave their segment sums for enc_fix_k.
+template <typename T>
+__global__ void enc_seg_k(float* dwte, float* partial, const T* dout, const int* perm,
+                          const int* cnt, const int* start, const int* item_start,
+                          const int* item_tok, const int* n_items, int C) {
+    int item = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (item >= *n_items) return;
+    int k = item_tok[item];
+    int j = item - item_start[k];
+    int lo = start[k] + j * ENC_SEG, hi = min(start[k] + cnt[k], lo + ENC_SEG);
+    bool single = cnt[k] <= ENC_SEG;
+    float* dst = single ? dwte + (size_t)k * C : partial + (size_t)item * C;
+    for (int c0 = 0; c0 < C; c0 += 256) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) acc[i] = 0.f;
+        int c = c0 + lane * 8;
+        if ((C & 7) == 0) {
+            if (c < C) {
+                for (int q = lo; q < hi; q++) {
+                    float x[8];
+                    Vec8<T>::load(dout + (size_t)perm[q] * C + c, x);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) acc[i] += x[i];
+                }
+#pragma unroll
+                for (int i = 0; i < 8; i++) dst[c + i] = single ? dst[c + i] + acc[i] : acc[i];
+            }
+        } else {
+            for (int i = 0; i < 8; i++) {
+                int cc = c0 + lane + 32 * i;
+                if (cc >= C || cc >= c0 + 256) continue;
+                float a = 0.f;
+                for (int q = lo; q < hi; q++) a += to_f(dout[(size_t)perm[q] * C + cc]);
+                dst[cc] = single ? dst[cc] + a : a;
+            }
+        }
+    }
+}
+
+// One warp per token with more than one segment: add the segment sums in order.
+__global__ void enc_fix_k(float* dwte, const float* partial, const int* cnt, const int* item_start,
+                          int V, int C) {
+    int k = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (k >= V || cnt[k] <= ENC_SEG) return;
+    int i0 = item_start[k], i1 = item_start[k + 1];
+    for (int c = lane; c < C; c += 32) {
+        float acc = 0.f;
+        for (int it = i0; it < i1; it++) acc += partial[(size_t)it * C + c];
+        dwte[(size_t)k * C + c] += acc;
+    }
+}
+
+cudaError_t encoder_backward_wte(ActType at, float* dwte, const void* dout, const int32_t* tok,
+                                 int M, int C, int V, const EncoderBwdScratch* sc, cudaStream_t s) {
+    if (M <= 0) return cudaSuccess;
+    int nch = enc_nchunks(M);
+    cudaError_t e = cudaMemsetAsync(sc->chunk_cnt, 0, (size_t)nch * V * sizeof(int), s);
+    if (e != cudaSuccess) return e;
+    G2_LAUNCH enc_hist_k<<<cdiv(M, 256), 256, 0, s>>>(sc->chunk_cnt, tok, M, V);
+    G2_LAUNCH enc_chunk_prefix_k<<<cdiv(V, 256), 256, 0, s>>>(sc->chunk_cnt, sc->cnt, nch, V);
+    G2_LAUNCH enc_scan_k<<<1, 1024, 0, s>>>(sc->cnt, sc->start, sc->item_start, V);
+    G2_LAUNCH enc_rank_k<<<nch, 1024, 0, s>>>(sc->perm, tok, sc->start, sc->chunk_cnt, M, V);
+    G2_LAUNCH enc_items_k<<<cdiv(V, 256), 256, 0, s>>>(sc->item_tok, sc->cnt, sc->item_start, V);
+    // Grid covers the maximum item count; the live count is read on the device.
+    if (at == ACT_BF16)
+        G2_LAUNCH enc_seg_k<bf16><<<cdiv(sc->max_items, 8), 256, 0, s>>>(
+            dwte, sc->partial, (const bf16*)dout, sc->perm, sc->cnt, sc->start, sc->item_start,
+            sc->item_tok, sc->item_start + V, C);
+    else
+        G2_LAUNCH enc_seg_k<float><<<cdiv(sc->max_items, 8), 256, 0, s>>>(
+            dwte, sc->partial, (const float*)dout, sc->perm, sc->cnt, sc->start, sc->item_start,
+            sc->item_tok, sc->item_start + V, C);
+    G2_LAUNCH enc_fix_k<<<cdiv(V, 8), 256, 0, s>>>(dwte, sc->partial, sc->cnt, sc->item_start, V, C);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ layernorm forward
+// llm.c §1.3 / picoGPT layer_norm: one warp per row; mean, biased variance (two passes
+// over the row held in registers), rstd = 1/sqrt(var + 1e-5).
+template <typename T, int NV>
+__global__ void ln_fwd_vec_k(T* out, float* mean, float* rstd, const T* inp, const float* w,
+                             const float* b, int M, int C) {
+    int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (row >= M) return;
+    const T* x = inp + (size_t)row * C;
+    float v[NV][8];
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; j++) {
+        Vec8<T>::load(x + j * 256 + lane * 8, v[j]);
+#pragma unroll
+        for (int i = 0; i < 8; i++) s += v[j][i];
+    }
+    float m = warp_sum(s) / C;
+    float q = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; j++)
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            float d = v[j][i] - m;
+            q += d * d;
+        }
+    float var = warp_sum(q) / C;
+    float r = 1.0f / sqrtf(var + 1e-5f);
+    T* o = out + (size_t)row * C;
+#pragma unroll
+    for (int j = 0; j < NV; j++) {
+        int c = j * 256 + lane * 8;
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) y[i] = (v[j][i] - m) * r * w[c + i] + b[c + i];
+        Vec8<T>::store(o + c, y);
+    }
+    if (lane == 0) {
+        mean[row] = m;
+        rstd[row] = r;
+    }
+}
+
+template <typename T>
+__global__ void ln_fwd_gen_k(T* out, float* mean, float* rstd, const T* inp, const float* w,
+                             const float* b, int M, int C) {
+    int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (row >= M) return;
+    const T* x = inp + (size_t)row * C;
+    float s = 0.f;
+    for (int c = lane; c < C; c += 32) s += to_f(x[c]);
+    float m = warp_sum(s) / C;
+    float q = 0.f;
+    for (int c = lane; c < C; c += 32) {
+        float d = to_f(x[c]) - m;
+        q += d * d;
+    }
+    float var = warp_sum(q) / C;
+    float r = 1.0f / sqrtf(var + 1e-5f);
+    T* o = out + (size_t)row * C;
+    for (int c = lane; c < C; c += 32) o[c] = from_f<T>((to_f(x[c]) - m) * r * w[c] + b[c]);
+    if (lane == 0) {
+        mean[row] = m;
+        rstd[row] = r;
+    }
+}
+
+template <typename T>
+static void ln_fwd_launch(T* out, float* mean, float* rstd, const T* inp, const float* w,
+                          const float* b, int M, int C, cudaStream_t s) {
+    unsigned g = cdiv(M, 8);
+    switch (C % 256 == 0 ? C / 256 : 0) {
+        case 1: count_launches(1); ln_fwd_vec_k<T, 1><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
+        case 2: count_launches(1); ln_fwd_vec_k<T, 2><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
+        case 3: count_launches(1); ln_fwd_vec_k<T, 3><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
+        case 4: count_launches(1); ln_fwd_vec_k<T, 4><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
+        case 5: count_launches(1); ln_fwd_vec_k<T, 5><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
+        case 6: count_launches(1); ln_fwd_vec_k<T, 6><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
+        default: count_launches(1); ln_fwd_gen_k<T><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
+    }
+}
+
+cudaError_t layernorm_forward(ActType at, void* out, float* mean, float* rstd, const void* inp,
+                              const float* w, const float* b, int M, int C, cudaStream_t s) {
+    if (M <= 0) return cudaSuccess;
+    if (at == ACT_BF16)
+        ln_fwd_launch<bf16>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, s);
+    else
+        ln_fwd_launch<float>((float*)out, mean, rstd, (const float*)inp, w, b, M, C, s);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ layernorm backward
+// llm.c §1.4.  One warp per row; dres += dinp (the residual-stream accumulation of
+// llm.c §1.12 fused in).  dw/db: each block sums its rows (warps in fixed order) into
+// part[block][C] and [block][C] of the second half; ln_bwd_final_k adds blocks in order.
+static const int LNB_BLOCKS = 296;  // fixed grid (2 x 148 SMs): fixes the sum order
+
+size_t ln_bwd_partial_floats(int C) { return (size_t)2 * LNB_BLOCKS * C; }
+
+template <typename T>
+__global__ void __launch_bounds__(256) ln_bwd_k(T* dres, float* part, const T* dout, const T* inp,
+                                                const float* w, const float* mean,
+                                                const float* rstd, int M, int C) {
+    extern __shared__ float sh[];  // [8 warps][2][C]
+    int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float* my_dw = sh + (size_t)warp * 2 * C;
+    float* my_db = my_dw + C;
+    for (int c = lane; c < C; c += 32) {
+        my_dw[c] = 0.f;
+        my_db[c] = 0.f;
+    }
+    for (int row = blockIdx.x * 8 + warp; row < M; row += gridDim.x * 8) {
+        const T* d = dout + (size_t)row * C;
+        const T* x = inp + (size_t)row * C;
+        T* dr = dres + (size_t)row * C;
+        float m = mean[row], r = rstd[row];
+        float gm = 0.f, gnm = 0.f;
+        for (int c = lane; c < C; c += 32) {
+            float n = (to_f(x[c]) - m) * r;
+            float g = w[c] * to_f(d[c]);
+            gm += g;
+            gnm += g * n;
+        }
+        gm = warp_sum(gm) / C;
+        gnm = warp_sum(gnm) / C;
+        for (int c = lane; c < C; c += 32) {
+            float dv = to_f(d[c]);
+            float n = (to_f(x[c]) - m) * r;
+            float g = w[c] * dv;
+            my_db[c] += dv;
+            my_dw[c] += n * dv;
+            float val = (g - gm - n * gnm) * r;
+            dr[c] = from_f<T>(to_f(dr[c]) + val);
+        }
+    }
+    __syncthreads();
+    float* pw = part + (size_t)blockIdx.x * C;
+    float* pb = part + (size_t)(gridDim.x + blockIdx.x) * C;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        float a = 0.f, b = 0.f;
+        for (int wi = 0; wi < 8; wi++) {
+            a += sh[(size_t)wi * 2 * C + c];
+            b += sh[(size_t)wi * 2 * C + C + c];
+        }
+        pw[c] = a;
+        pb[c] = b;
+    }
+}
+
+__global__ void ln_bwd_final_k(float* dw, float* db, const float* part, int nblk, int C) {
+    int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    float a = 0.f, b = 0.f;
+    for (int i = 0; i < nblk; i++) {
+        a += part[(size_t)i * C + c];
+        b += part[(size_t)(nblk + i) * C + c];
+    }
+    dw[c] = a;
+    db[c] = b;
+}
+
+cudaError_t layernorm_backward(ActType at, void* dres, float* dw, float* db, const void* dout,
+                               const void* inp, const float* w, const float* mean,
+                               const float* rstd, int M, int C, float* part, cudaStream_t s) {
+    size_t smem = (size_t)8 * 2 * C * sizeof(float);
+    if (smem > 200 * 1024) return cudaErrorInvalidValue;
+    if (at == ACT_BF16) {
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(ln_bwd_k<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        G2_LAUNCH ln_bwd_k<bf16><<<LNB_BLOCKS, 256, smem, s>>>((bf16*)dres, part, (const bf16*)dout,
+                                                     (const bf16*)inp, w, mean, rstd, M, C);
+    } else {
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(ln_bwd_k<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        G2_LAUNCH ln_bwd_k<float><<<LNB_BLOCKS, 256, smem, s>>>((float*)dres, part, (const float*)dout,
+                                                      (const float*)inp, w, mean, rstd, M, C);
+    }
+    G2_LAUNCH ln_bwd_final_k<<<cdiv(C, 256), 256, 0, s>>>(dw, db, part, LNB_BLOCKS, C);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ bias gradient
+// out[n] = sum_m X[m,n]: block (strip of 256 columns, row block) sums its rows with
+// each warp taking every 8th row, warps combined in order; then row blocks in order.
+static const int CS_ROWS = 256;  // rows per row block
+
+size_t colsum_partial_floats(int M, int N) { return (size_t)cdiv(M, CS_ROWS) * N; }
+
+template <typename T>
+__global__ void colsum_part_k(float* part, const T* X, int M, int N) {
+    __shared__ float sh[8][256];
+    int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int col = blockIdx.x * 256 + lane * 8;
+    int r0 = blockIdx.y * CS_ROWS, r1 = min(M, r0 + CS_ROWS);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) acc[i] = 0.f;
+    bool vec = ((N & 7) == 0) && col + 8 <= N;
+    for (int r = r0 + warp; r < r1; r += 8) {
+        const T* x = X + (size_t)r * N;
+        if (vec) {
+            float v[8];
+            Vec8<T>::load(x + col, v);
+#pragma unroll
+            for (int i = 0; i < 8; i++) acc[i] += v[i];
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                if (col + i < N) acc[i] += to_f(x[col + i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i++) sh[warp][lane * 8 + i] = acc[i];
+    __syncthreads();
+    int c = threadIdx.x;
+    if (blockIdx.x * 256 + c < N) {
+        float a = 0.f;
+        for (int wi = 0; wi < 8; wi++) a += sh[wi][c];
+        part[(size_t)blockIdx.y * N + blockIdx.x * 256 + c] = a;
+    }
+}
+
+__global__ void colsum_final_k(float* out, const float* part, int nrb, int N) {
+    int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= N) return;
+    float a = 0.f;
+    for (int i = 0; i < nrb; i++) a += part[(size_t)i * N + c];
+    out[c] = a;
+}
+
+cudaError_t colsum(ActType at, float* out, const void* X, int M, int N, float* part, cudaStream_t s) {
+    if (N <= 0) return cudaSuccess;
+    int nrb = M > 0 ? (int)cdiv(M, CS_ROWS) : 0;
+    if (nrb > 0) {
+        dim3 g(cdiv(N, 256), nrb);
+        if (at == ACT_BF16)
+            G2_LAUNCH colsum_part_k<bf16><<<g, 256, 0, s>>>(part, (const bf16*)X, M, N);
+        else
+            G2_LAUNCH colsum_part_k<float><<<g, 256, 0, s>>>(part, (const float*)X, M, N);
+    }
+    G2_LAUNCH colsum_final_k<<<cdiv(N, 256), 256, 0, s>>>(out, part, nrb, N);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ softmax + cross-entropy
+// llm.c §1.13-§1.15 fused: per row, lse = logsumexp over the V real columns (max then
+// sum of exp, block reductions in a fixed tree), loss = lse - logit[target], and the
+// row is overwritten with (exp(logit - lse) - onehot) * dloss; padding columns get 0.
+// A target outside [0,V) raises the flag; its row gets loss 0 and no one-hot term.
+template <typename T>
+__global__ void __launch_bounds__(1024) softmax_xent_k(T* logits, float* losses,
+                                                       const int32_t* targets, int V, int Vp,
+                                                       float dloss, int* flags) {
+    __shared__ float red[32];
+    __shared__ float bcast;
+    int row = blockIdx.x;
+    T* x = logits + (size_t)row * Vp;
+    int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    bool vec = (Vp & 7) == 0;
+    // pass 1: max
+    float mx = -INFINITY;
+    if (vec) {
+        for (int c = tid * 8; c < V; c += blockDim.x * 8) {
+            float v[8];
+            Vec8<T>::load(x + c, v);
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                if (c + i < V) mx = fmaxf(mx, v[i]);
+        }
+    } else {
+        for (int c = tid; c < V; c += blockDim.x) mx = fmaxf(mx, to_f(x[c]));
+    }
+    mx = warp_max(mx);
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    if (warp == 0) {
+        float t = lane < nw ? red[lane] : -INFINITY;
+        t = warp_max(t);
+        if (lane == 0) bcast = t;
+    }
+    __syncthreads();
+    mx = bcast;
+    // pass 2: sum of exp
+    float sum = 0.f;
+    if (vec) {
+        for (int c = tid * 8; c < V; c += blockDim.x * 8) {
+            float v[8];
+            Vec8<T>::load(x + c, v);
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                if (c + i < V) sum += expf(v[i] - mx);
+        }
+    } else {
+        for (int c = tid; c < V; c += blockDim.x) sum += expf(to_f(x[c]) - mx);
+    }
+    sum = warp_sum(sum);
+    __syncthreads();
+    if (lane == 0) red[warp] = sum;
+    __syncthreads();
+    if (warp == 0) {
+        float t = lane < nw ? red[lane] : 0.f;
+        t = warp_sum(t);
+        if (lane == 0) bcast = t;
+    }
+    __syncthreads();
+    float lse = mx + logf(bcast);
+    int tg = targets[row];
+    bool ok = (unsigned)tg < (unsigned)V;
+    if (tid == 0) {
+        if (!ok) atomicOr(flags, G2_FLAG_BAD_TARGET);
+        losses[row] = ok ? lse - to_f(x[tg]) : 0.f;
+    }
+    __syncthreads();  // every thread has read x[tg] before it is overwritten
+    // pass 3: dlogits in place
+    if (vec) {
+        for (int c = tid * 8; c < Vp; c += blockDim.x * 8) {
+            float v[8];
+            Vec8<T>::load(x + c, v);
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                int cc = c + i;
+                float p = cc < V ? expf(v[i] - lse) : 0.f;
+                float ind = (ok && cc == tg) ? 1.f : 0.f;
+                v[i] = cc < V ? (p - ind) * dloss : 0.f;
+            }
+            Vec8<T>::store(x + c, v);
+        }
+    } else {
+        for (int c = tid; c < Vp; c += blockDim.x) {
+            float p = c < V ? expf(to_f(x[c]) - lse) : 0.f;
+            float ind = (ok && c == tg) ? 1.f : 0.f;
+            x[c] = from_f<T>(c < V ? (p - ind) * dloss : 0.f);
+        }
+    }
+}
+
+cudaError_t softmax_xent(ActType at, void* logits, float* losses, const int32_t* targets, int M,
+                         int V, int Vp, float dloss, int* flags, cudaStream_t s) {
+    if (M <= 0) return cudaSuccess;
+    if (at == ACT_BF16)
+        G2_LAUNCH softmax_xent_k<bf16><<<M, 1024, 0, s>>>((bf16*)logits, losses, targets, V, Vp, dloss, flags);
+    else
+        G2_LAUNCH softmax_xent_k<float><<<M, 1024, 0, s>>>((float*)logits, losses, targets, V, Vp, dloss, flags);
+    return cudaGetLastError();
+}
+
+// Single block; thread i sums x[i], x[i+1024], ... then a fixed tree.  Also flags a
+// non-finite mean.
+__global__ void mean_k(float* out, const float* x, int n) {
+    __shared__ float sh[1024];
+    float a = 0.f;
+    for (int i = threadIdx.x; i < n; i += 1024) a += x[i];
+    sh[threadIdx.x] = a;
+    __syncthreads();
+    for (int off = 512; off > 0; off >>= 1) {
+        if ((int)threadIdx.x < off) sh[threadIdx.x] += sh[threadIdx.x + off];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) out[0] = n > 0 ? sh[0] / (float)n : 0.f;
+}
+cudaError_t mean_fixed_order(float* out, const float* x, int n, cudaStream_t s) {
+    G2_LAUNCH mean_k<<<1, 1024, 0, s>>>(out, x, n);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ AdamW
+// llm.c §1.26, one element per thread-iteration, float4 where aligned.  c1 = 1-b1^t and
+// c2 = 1-b2^t are computed by the caller.
+G2_DEV void adamw_one(float& p, float g, float& m, float& v, float lr, float b1, float b2,
+                      float eps, float wd, float c1, float c2) {
+    float old = p;
+    float mi = b1 * m + (1.0f - b1) * g;
+    float vi = b2 * v + (1.0f - b2) * g * g;
+    float mh = mi / c1;
+    float vh = vi / c2;
+    m = mi;
+    v = vi;
+    p = old - lr * (mh / (sqrtf(vh) + eps) + wd * old);
+}
+
+__global__ void adamw_k(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
+                        float* __restrict__ v, bf16* __restrict__ shadow, size_t n4, float lr,
+                        float b1, float b2, float eps, float wd, float c1, float c2) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (size_t)gridDim.x * blockDim.x) {
+        float4 P = reinterpret_cast<float4*>(p)[i];
+        float4 G = reinterpret_cast<const float4*>(g)[i];
+        float4 Mm = reinterpret_cast<float4*>(m)[i];
+        float4 Vv = reinterpret_cast<float4*>(v)[i];
+        adamw_one(P.x, G.x, Mm.x, Vv.x, lr, b1, b2, eps, wd, c1, c2);
+        adamw_one(P.y, G.y, Mm.y, Vv.y, lr, b1, b2, eps, wd, c1, c2);
+        adamw_one(P.z, G.z, Mm.z, Vv.z, lr, b1, b2, eps, wd, c1, c2);
+        adamw_one(P.w, G.w, Mm.w, Vv.w, lr, b1, b2, eps, wd, c1, c2);
+        reinterpret_cast<float4*>(p)[i] = P;
+        reinterpret_cast<float4*>(m)[i] = Mm;
+        reinterpret_cast<float4*>(v)[i] = Vv;
+        if (shadow) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(P.x, P.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(P.z, P.w);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t*>(&lo);
+            u.y = *reinterpret_cast<uint32_t*>(&hi);
+            reinterpret_cast<uint2*>(shadow)[i] = u;
+        }
+    }
+}
+
+__global__ void adamw_tail_k(float* p, const float* g, float* m, float* v, bf16* shadow,
+                             size_t from, size_t n, float lr, float b1, float b2, float eps,
+                             float wd, float c1, float c2) {
+    size_t i = from + threadIdx.x;
+    if (i >= n) return;
+    adamw_one(p[i], g[i], m[i], v[i], lr, b1, b2, eps, wd, c1, c2);
+    if (shadow) shadow[i] = __float2bfloat16_rn(p[i]);
+}
+
+cudaError_t adamw(float* p, const float* g, float* m, float* v, bf16* shadow, size_t n, float lr,
+                  float b1, float b2, float eps, float wd, float c1, float c2, cudaStream_t s) {
+    size_t n4 = n / 4;
+    if (n4) {
+        int dev = 0, sms = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        unsigned blocks = (unsigned)std::min<size_t>(cdiv(n4, 256), (size_t)sms * 8);
+        G2_LAUNCH adamw_k<<<blocks, 256, 0, s>>>(p, g, m, v, shadow, n4, lr, b1, b2, eps, wd, c1, c2);
+    }
+    if (n4 * 4 < n)
+        G2_LAUNCH adamw_tail_k<<<1, 32, 0, s>>>(p, g, m, v, shadow, n4 * 4, n, lr, b1, b2, eps, wd, c1, c2);
+    return cudaGetLastError();
+}
+
+__global__ void cast_k(bf16* out, const float* in, size_t n) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        out[i] = __float2bfloat16_rn(in[i]);
+}
+cudaError_t cast_f32_to_bf16(bf16* out, const float* in, size_t n, cudaStream_t s) {
+    if (!n) return cudaSuccess;
+    G2_LAUNCH cast_k<<<(unsigned)std::min<size_t>(cdiv(n, 256), 148 * 16), 256, 0, s>>>(out, in, n);
+    return cudaGetLastError();
+}
+
+}  // namespace g2

@@ -1,0 +1,103 @@
+// Host-side launchers of the GPT-2 train-step kernels.  Every launcher is
+// stream-ordered, allocates nothing and returns cudaGetLastError() of its launch(es).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace g2 {
+
+typedef __nv_bfloat16 bf16;
+
+// Activation element type of a launch.
+enum ActType { ACT_F32 = 0, ACT_BF16 = 1 };
+
+// Process-wide count of kernel launches queued by the launchers below.
+void count_launches(unsigned n);
+uint64_t launches_total();
+
+// ---- token ids (llm.c §1.23 validation) --------------------------------------
+cudaError_t check_ids(const int32_t* ids, int M, int V, int* flags, int flag_bit, cudaStream_t s);
+
+// ---- encoder (llm.c §1.1, §1.2) ----------------------------------------------
+cudaError_t encoder_forward(ActType at, void* out, const int32_t* tok, const void* wte,
+                            const void* wpe, int B, int T, int C, int V, int* flags, cudaStream_t s);
+// dwpe (maxT,C) fp32 is overwritten: rows t<T get sum_b dout[b,t,:] (b ascending), rows t>=T get 0.
+cudaError_t encoder_backward_wpe(ActType at, float* dwpe, const void* dout, int B, int T, int C,
+                                 int maxT, cudaStream_t s);
+// Scratch for the deterministic token-bucketed dwte accumulation.
+struct EncoderBwdScratch {
+    int* chunk_cnt;     // nchunks * V ints
+    int* cnt;           // V
+    int* start;         // V + 1
+    int* item_start;    // V + 1
+    int* item_tok;      // max_items
+    int* perm;          // M
+    float* partial;     // max_items * C
+    int max_items;
+};
+size_t encoder_bwd_scratch_bytes(int M, int V, int C);
+void encoder_bwd_scratch_carve(EncoderBwdScratch* sc, void* base, int M, int V, int C);
+// dwte (V,C) fp32 += per-token sums of dout rows, summed in ascending position order.
+cudaError_t encoder_backward_wte(ActType at, float* dwte, const void* dout, const int32_t* tok,
+                                 int M, int C, int V, const EncoderBwdScratch* sc, cudaStream_t s);
+
+// ---- layernorm (llm.c §1.3, §1.4) ----------------------------------------------
+cudaError_t layernorm_forward(ActType at, void* out, float* mean, float* rstd, const void* inp,
+                              const float* w, const float* b, int M, int C, cudaStream_t s);
+// dres (M,C) += LN-backward(dout); dw, db (C) fp32 overwritten.  part: ln_bwd_partial_floats().
+size_t ln_bwd_partial_floats(int C);
+cudaError_t layernorm_backward(ActType at, void* dres, float* dw, float* db, const void* dout,
+                               const void* inp, const float* w, const float* mean,
+                               const float* rstd, int M, int C, float* part, cudaStream_t s);
+
+// ---- bias gradient: out[n] = sum_m X[m,n] (fixed order) --------------------------
+size_t colsum_partial_floats(int M, int N);
+cudaError_t colsum(ActType at, float* out, const void* X, int M, int N, float* part, cudaStream_t s);
+
+// ---- fused softmax + cross-entropy forward and backward (llm.c §1.13-§1.15) -------
+// logits (M,Vp) is overwritten in place by dlogits = (softmax - onehot) * dloss over the
+// first V columns and 0 over the padding; losses[m] = logsumexp - logit[target].
+cudaError_t softmax_xent(ActType at, void* logits, float* losses, const int32_t* targets, int M,
+                         int V, int Vp, float dloss, int* flags, cudaStream_t s);
+// out[0] = mean of x[0..n) in a fixed summation order.
+cudaError_t mean_fixed_order(float* out, const float* x, int n, cudaStream_t s);
+
+// ---- AdamW over a flat fp32 buffer (llm.c §1.26) --------------------------------
+// shadow (optional) receives the bf16 rounding of the updated parameters.
+cudaError_t adamw(float* p, const float* g, float* m, float* v, bf16* shadow, size_t n, float lr,
+                  float b1, float b2, float eps, float wd, float c1, float c2, cudaStream_t s);
+cudaError_t cast_f32_to_bf16(bf16* out, const float* in, size_t n, cudaStream_t s);
+
+// ---- causal multi-head attention (llm.c §1.7, §1.8; flash-style recompute) -------
+// out (B,T,C); lse (B,NH,T) fp32 log-sum-exp of each query row's scores.
+cudaError_t attention_forward_simt(ActType at, void* out, float* lse, const void* qkv, int B,
+                                   int T, int C, int NH, cudaStream_t s);
+// dqkv (B,T,3C) overwritten.  scratch_D: B*NH*T floats.
+cudaError_t attention_backward_simt(ActType at, void* dqkv, const void* dout, const void* qkv,
+                                    const void* out, const float* lse, int B, int T, int C,
+                                    int NH, float* scratch_D, cudaStream_t s);
+
+// ---- GEMM --------------------------------------------------------------------------
+// D[m,n] = epilogue( sum_k A(m,k) * B(n,k) ), A(m,k) = A[m*sAm + k*sAk], B(n,k) = B[n*sBn + k*sBk].
+enum Epilogue {
+    EPI_STORE = 0,      // D = acc (+bias[n]) (+R[m,n])
+    EPI_GELU = 1,       // D = acc + bias (pre-activation), D2 = gelu(acc + bias)
+    EPI_GELU_BWD = 2,   // D = acc * gelu'(P[m,n])
+};
+struct GemmArgs {
+    int M, N, K;
+    ActType in_type;            // A and B element type
+    const void* A; long long sAm, sAk;
+    const void* B; long long sBn, sBk;
+    void* D; long long ldd; int d_f32;   // D element type: fp32 if d_f32 else in_type
+    const float* bias;          // [N] or null
+    const void* R; long long ldr;        // residual added to D (in_type), or null
+    void* D2; long long ldd2;            // EPI_GELU second output (in_type)
+    const void* P; long long ldp;        // EPI_GELU_BWD pre-activation (in_type)
+    int epi;
+};
+cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t s);
+
+}  // namespace g2

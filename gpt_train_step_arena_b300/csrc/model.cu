@@ -1,0 +1,564 @@
+// Host driver of the GPT-2 training step: arenas, the launch sequence of forward,
+// backward and AdamW, and the C ABI of include/gpt2.h.
+//
+// The layer chain is the one of the llm.c annotated listing (gpt2_forward §1.23,
+// gpt2_backward §1.25, gpt2_update §1.26) with these B300 choices:
+//  * one parameter arena (params | grads | m | v | bf16 weight copy), one activation
+//    arena sized at the first forward, nothing allocated afterwards;
+//  * residual additions fused into the epilogue of the projection GEMMs, GELU fused
+//    into the FC GEMM epilogue and its derivative into the FC-proj dgrad epilogue;
+//  * attention keeps only the per-row log-sum-exp (no (T,T) matrices);
+//  * softmax and cross-entropy fused, dlogits written over the logits in place.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/gpt2.h"
+#include "common.cuh"
+#include "dispatch.h"
+#include "kernels.h"
+
+namespace g2 {
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+uint64_t launches_total() { return g_launches.load(std::memory_order_relaxed); }
+}  // namespace g2
+
+using namespace g2;
+
+static std::string g_build_error;
+
+enum { NP = 16 };
+
+struct gpt2 {
+    int L, C, NH, V, Vp, maxT, prec;
+    ActType at;
+    size_t esz;  // bytes per activation element
+    size_t psize[NP], poff[NP];  // padded sizes / offsets (elements)
+    size_t npad, nreal;
+    void* parena;
+    size_t pbytes;
+    float *params, *grads, *mom1, *mom2;
+    bf16* shadow;
+    bool opt_init, have_grads, fwd_targets;
+    // activation arena
+    void* aarena;
+    size_t abytes;
+    int B, T;
+    int32_t *tok, *tgt;
+    int* flags;
+    float *loss, *losses;
+    char *res, *res2, *ln1, *qkv, *atty, *ln2, *fch, *fchg, *lnf, *logits;
+    float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd, *lnf_mean, *lnf_rstd, *lse;
+    char *dres, *dln, *datty, *dqkv, *dfch;
+    float *attD, *ln_part, *cs_part, *gemm_ws;
+    size_t gemm_ws_bytes;
+    EncoderBwdScratch enc;
+    bool logits_valid;
+    cudaStream_t stream;
+    int status;
+    std::string err;
+};
+
+// ------------------------------------------------------------------ helpers
+static int fail(gpt2* m, int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (m) {
+        m->status = code;
+        m->err = buf;
+    }
+    return code;
+}
+
+#define CK(expr)                                                                          \
+    do {                                                                                  \
+        cudaError_t e_ = (expr);                                                          \
+        if (e_ != cudaSuccess)                                                            \
+            return fail(m, GPT2_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_)); \
+    } while (0)
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// pointers into the parameter-shaped buffers
+enum { P_WTE, P_WPE, P_LN1W, P_LN1B, P_QKVW, P_QKVB, P_APW, P_APB, P_LN2W, P_LN2B, P_FCW, P_FCB,
+       P_FPW, P_FPB, P_LNFW, P_LNFB };
+
+static float* pf(const gpt2* m, float* base, int t) { return base + m->poff[t]; }
+// weight operand of a GEMM: bf16 copy in BF16 mode, the fp32 master otherwise
+static const void* pw(const gpt2* m, int t, size_t elem_off) {
+    if (m->at == ACT_BF16) return m->shadow + m->poff[t] + elem_off;
+    return m->params + m->poff[t] + elem_off;
+}
+static char* act(const gpt2* m, char* base, size_t elems) { return base + elems * m->esz; }
+
+// ------------------------------------------------------------------ GEMM dispatch
+// Y[M,N] = X[M,K] . W[N,K]^T (+bias) (+R) with optional GELU epilogue.
+static cudaError_t gemm_fwd(gpt2* m, int M, int N, int K, const void* X, const void* W,
+                            const float* bias, void* Y, const void* R, void* Y2) {
+    GemmArgs a{};
+    a.M = M; a.N = N; a.K = K; a.in_type = m->at;
+    a.A = X; a.sAm = K; a.sAk = 1;
+    a.B = W; a.sBn = K; a.sBk = 1;
+    a.D = Y; a.ldd = N; a.d_f32 = 0;
+    a.bias = bias; a.R = R; a.ldr = N;
+    a.D2 = Y2; a.ldd2 = N;
+    a.epi = Y2 ? EPI_GELU : EPI_STORE;
+    return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
+}
+// dX[M,K] = dY[M,N] . W[N,K]  (optionally times gelu'(P))
+static cudaError_t gemm_dgrad(gpt2* m, int M, int N, int K, const void* dY, const void* W, void* dX,
+                              const void* P) {
+    GemmArgs a{};
+    a.M = M; a.N = K; a.K = N; a.in_type = m->at;
+    a.A = dY; a.sAm = N; a.sAk = 1;
+    a.B = W; a.sBn = 1; a.sBk = K;
+    a.D = dX; a.ldd = K; a.d_f32 = 0;
+    a.P = P; a.ldp = K;
+    a.epi = P ? EPI_GELU_BWD : EPI_STORE;
+    return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
+}
+// dW[N,K] (fp32, overwritten) = dY[M,N]^T . X[M,K]
+static cudaError_t gemm_wgrad(gpt2* m, int M, int N, int K, const void* dY, const void* X, float* dW) {
+    GemmArgs a{};
+    a.M = N; a.N = K; a.K = M; a.in_type = m->at;
+    a.A = dY; a.sAm = 1; a.sAk = N;
+    a.B = X; a.sBn = 1; a.sBk = K;
+    a.D = dW; a.ldd = K; a.d_f32 = 1;
+    a.epi = EPI_STORE;
+    return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
+}
+
+// ------------------------------------------------------------------ build / free
+extern "C" gpt2_t* gpt2_build_ex(int L, int C, int H, int V, int maxT, int precision, int* status) {
+    auto bail = [&](int code, const char* msg) -> gpt2_t* {
+        g_build_error = msg;
+        if (status) *status = code;
+        return nullptr;
+    };
+    if (L <= 0 || C <= 0 || H <= 0 || V <= 0 || maxT <= 0 || C % H)
+        return bail(GPT2_ERR_ARG, "bad shape: need L,C,H,V,maxT > 0 and C % H == 0");
+    if (precision != GPT2_FP32 && precision != GPT2_BF16)
+        return bail(GPT2_ERR_ARG, "precision must be GPT2_FP32 or GPT2_BF16");
+    if (C % 8) return bail(GPT2_ERR_ARG, "C must be a multiple of 8");
+    if (C / H > 256) return bail(GPT2_ERR_ARG, "head size above 256 is not supported");
+    gpt2* m = new (std::nothrow) gpt2();
+    if (!m) return bail(GPT2_ERR_OOM, "host allocation failed");
+    m->L = L; m->C = C; m->NH = H; m->V = V; m->maxT = maxT; m->prec = precision;
+    m->Vp = (V + 127) / 128 * 128;
+    m->at = precision == GPT2_BF16 ? ACT_BF16 : ACT_F32;
+    m->esz = m->at == ACT_BF16 ? 2 : 4;
+    size_t Ls = L, Cs = C;
+    size_t sz[NP] = {(size_t)m->Vp * Cs, (size_t)maxT * Cs, Ls * Cs, Ls * Cs, Ls * 3 * Cs * Cs,
+                     Ls * 3 * Cs, Ls * Cs * Cs, Ls * Cs, Ls * Cs, Ls * Cs, Ls * 4 * Cs * Cs,
+                     Ls * 4 * Cs, Ls * Cs * 4 * Cs, Ls * Cs, Cs, Cs};
+    size_t off = 0;
+    for (int i = 0; i < NP; i++) {
+        m->psize[i] = sz[i];
+        m->poff[i] = off;
+        off += sz[i];
+    }
+    m->npad = off;
+    m->nreal = off - (size_t)(m->Vp - V) * Cs;
+    size_t fbytes = align256(m->npad * 4);
+    m->pbytes = 4 * fbytes + (m->at == ACT_BF16 ? align256(m->npad * 2) : 0);
+    cudaStream_t s0 = nullptr;
+    m->stream = s0;
+    cudaError_t e = cudaMalloc(&m->parena, m->pbytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        char buf[256];
+        snprintf(buf, sizeof buf, "cudaMalloc of %zu bytes failed: %s", m->pbytes, cudaGetErrorString(e));
+        delete m;
+        return bail(e == cudaErrorMemoryAllocation ? GPT2_ERR_OOM : GPT2_ERR_CUDA, buf);
+    }
+    char* p = (char*)m->parena;
+    m->params = (float*)p; p += fbytes;
+    m->grads = (float*)p; p += fbytes;
+    m->mom1 = (float*)p; p += fbytes;
+    m->mom2 = (float*)p; p += fbytes;
+    m->shadow = m->at == ACT_BF16 ? (bf16*)p : nullptr;
+    e = cudaMemset(m->parena, 0, m->pbytes);
+    if (e != cudaSuccess) {
+        cudaFree(m->parena);
+        delete m;
+        return bail(GPT2_ERR_CUDA, cudaGetErrorString(e));
+    }
+    if (status) *status = GPT2_OK;
+    return m;
+}
+
+extern "C" gpt2_t* gpt2_build(int L, int C, int H, int V, int maxT) {
+    return gpt2_build_ex(L, C, H, V, maxT, GPT2_BF16, nullptr);
+}
+
+extern "C" void gpt2_free(gpt2_t* m) {
+    if (!m) return;
+    if (m->parena) cudaFree(m->parena);
+    if (m->aarena) cudaFree(m->aarena);
+    delete m;
+}
+
+extern "C" size_t gpt2_num_params(const gpt2_t* m) { return m ? m->nreal : 0; }
+extern "C" int gpt2_padded_vocab(const gpt2_t* m) { return m ? m->Vp : 0; }
+extern "C" size_t gpt2_device_bytes(const gpt2_t* m) { return m ? m->pbytes + m->abytes : 0; }
+extern "C" uint64_t gpt2_kernel_launches(const gpt2_t*) { return launches_total(); }
+extern "C" int gpt2_last_status(const gpt2_t* m) { return m ? m->status : GPT2_ERR_ARG; }
+extern "C" const char* gpt2_last_error(const gpt2_t* m) { return m ? m->err.c_str() : "null handle"; }
+extern "C" const char* gpt2_last_build_error(void) { return g_build_error.c_str(); }
+
+extern "C" int gpt2_set_stream(gpt2_t* m, void* stream) {
+    if (!m) return GPT2_ERR_ARG;
+    m->stream = (cudaStream_t)stream;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_sync(gpt2_t* m) {
+    if (!m) return GPT2_ERR_ARG;
+    CK(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
+// Host layout (real V rows of wte) <-> device layout (Vp rows): two copies.
+static int copy_params(gpt2* m, float* dev, const float* hin, float* hout) {
+    size_t real_wte = (size_t)m->V * m->C;
+    size_t rest = m->nreal - real_wte;
+    if (hin) {
+        CK(cudaMemcpyAsync(dev, hin, real_wte * 4, cudaMemcpyHostToDevice, m->stream));
+        CK(cudaMemcpyAsync(dev + m->poff[P_WPE], hin + real_wte, rest * 4, cudaMemcpyHostToDevice,
+                           m->stream));
+    } else {
+        CK(cudaMemcpyAsync(hout, dev, real_wte * 4, cudaMemcpyDeviceToHost, m->stream));
+        CK(cudaMemcpyAsync(hout + real_wte, dev + m->poff[P_WPE], rest * 4, cudaMemcpyDeviceToHost,
+                           m->stream));
+    }
+    CK(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_set_params(gpt2_t* m, const float* host, size_t n) {
+    if (!m || !host) return fail(m, GPT2_ERR_ARG, "null argument");
+    if (n != m->nreal) return fail(m, GPT2_ERR_ARG, "expected %zu parameters, got %zu", m->nreal, n);
+    int rc = copy_params(m, m->params, host, nullptr);
+    if (rc) return rc;
+    if (m->shadow) {
+        CK(cast_f32_to_bf16(m->shadow, m->params, m->npad, m->stream));
+        CK(cudaStreamSynchronize(m->stream));
+    }
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_get_params(gpt2_t* m, float* host, size_t n) {
+    if (!m || !host) return fail(m, GPT2_ERR_ARG, "null argument");
+    if (n != m->nreal) return fail(m, GPT2_ERR_ARG, "expected %zu parameters, got %zu", m->nreal, n);
+    return copy_params(m, m->params, nullptr, host);
+}
+
+extern "C" int gpt2_get_grads(gpt2_t* m, float* host, size_t n) {
+    if (!m || !host) return fail(m, GPT2_ERR_ARG, "null argument");
+    if (n != m->nreal) return fail(m, GPT2_ERR_ARG, "expected %zu values, got %zu", m->nreal, n);
+    if (!m->have_grads) return fail(m, GPT2_ERR_STATE, "no backward has run");
+    return copy_params(m, m->grads, nullptr, host);
+}
+
+extern "C" int gpt2_get_opt_state(gpt2_t* m, float* mh, float* vh, size_t n) {
+    if (!m || !mh || !vh) return fail(m, GPT2_ERR_ARG, "null argument");
+    if (n != m->nreal) return fail(m, GPT2_ERR_ARG, "expected %zu values, got %zu", m->nreal, n);
+    int rc = copy_params(m, m->mom1, nullptr, mh);
+    return rc ? rc : copy_params(m, m->mom2, nullptr, vh);
+}
+
+// ------------------------------------------------------------------ activation arena
+static int alloc_acts(gpt2* m, int B, int T) {
+    const size_t M = (size_t)B * T, C = m->C, L = m->L, es = m->esz, NH = m->NH;
+    struct Item { void** slot; size_t bytes; };
+    void *tok, *tgt, *flags, *loss, *losses, *res, *res2, *ln1, *qkv, *atty, *ln2, *fch, *fchg, *lnf,
+        *logits, *ln1m, *ln1r, *ln2m, *ln2r, *lnfm, *lnfr, *lse, *dres, *dln, *datty, *dqkv, *dfch,
+        *attD, *lnp, *csp, *enc, *ws;
+    size_t ln_part = ln_bwd_partial_floats(m->C) * 4;
+    size_t maxN = std::max<size_t>(4 * C, (size_t)m->Vp);
+    size_t cs_part = colsum_partial_floats((int)M, (int)maxN) * 4;
+    size_t enc_bytes = encoder_bwd_scratch_bytes((int)M, m->V, m->C);
+    m->gemm_ws_bytes = gemm_workspace_bytes((int)M, m->C, m->Vp, m->L);
+    Item items[] = {
+        {&tok, M * 4}, {&tgt, M * 4}, {&flags, 64}, {&loss, 64}, {&losses, M * 4},
+        {&res, (L + 1) * M * C * es}, {&res2, L * M * C * es}, {&ln1, L * M * C * es},
+        {&qkv, L * M * 3 * C * es}, {&atty, L * M * C * es}, {&ln2, L * M * C * es},
+        {&fch, L * M * 4 * C * es}, {&fchg, L * M * 4 * C * es}, {&lnf, M * C * es},
+        {&logits, M * (size_t)m->Vp * es}, {&ln1m, L * M * 4}, {&ln1r, L * M * 4},
+        {&ln2m, L * M * 4}, {&ln2r, L * M * 4}, {&lnfm, M * 4}, {&lnfr, M * 4},
+        {&lse, L * M * NH * 4}, {&dres, M * C * es}, {&dln, M * C * es}, {&datty, M * C * es},
+        {&dqkv, M * 3 * C * es}, {&dfch, M * 4 * C * es}, {&attD, M * NH * 4}, {&lnp, ln_part},
+        {&csp, cs_part}, {&enc, enc_bytes}, {&ws, m->gemm_ws_bytes},
+    };
+    size_t total = 0;
+    for (auto& it : items) total += align256(it.bytes);
+    void* base = nullptr;
+    cudaError_t e = cudaMalloc(&base, total);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(m, e == cudaErrorMemoryAllocation ? GPT2_ERR_OOM : GPT2_ERR_CUDA,
+                    "activation arena of %zu bytes: %s", total, cudaGetErrorString(e));
+    }
+    char* p = (char*)base;
+    for (auto& it : items) {
+        *it.slot = p;
+        p += align256(it.bytes);
+    }
+    m->aarena = base;
+    m->abytes = total;
+    m->B = B; m->T = T;
+    m->tok = (int32_t*)tok; m->tgt = (int32_t*)tgt; m->flags = (int*)flags;
+    m->loss = (float*)loss; m->losses = (float*)losses;
+    m->res = (char*)res; m->res2 = (char*)res2; m->ln1 = (char*)ln1; m->qkv = (char*)qkv;
+    m->atty = (char*)atty; m->ln2 = (char*)ln2; m->fch = (char*)fch; m->fchg = (char*)fchg;
+    m->lnf = (char*)lnf; m->logits = (char*)logits;
+    m->ln1_mean = (float*)ln1m; m->ln1_rstd = (float*)ln1r; m->ln2_mean = (float*)ln2m;
+    m->ln2_rstd = (float*)ln2r; m->lnf_mean = (float*)lnfm; m->lnf_rstd = (float*)lnfr;
+    m->lse = (float*)lse;
+    m->dres = (char*)dres; m->dln = (char*)dln; m->datty = (char*)datty; m->dqkv = (char*)dqkv;
+    m->dfch = (char*)dfch; m->attD = (float*)attD; m->ln_part = (float*)lnp;
+    m->cs_part = (float*)csp; m->gemm_ws = (float*)ws;
+    encoder_bwd_scratch_carve(&m->enc, enc, (int)M, m->V, m->C);
+    CK(cudaMemsetAsync(m->flags, 0, 64, m->stream));
+    return GPT2_OK;
+}
+
+// ------------------------------------------------------------------ forward
+static int forward_impl(gpt2* m, const int32_t* tokens, const int32_t* targets, int B, int T,
+                        int where) {
+    if (!m || !tokens) return fail(m, GPT2_ERR_ARG, "null argument");
+    if (B <= 0 || T <= 0) return fail(m, GPT2_ERR_ARG, "B and T must be positive");
+    if (T > m->maxT) return fail(m, GPT2_ERR_SHAPE, "T=%d exceeds maxT=%d", T, m->maxT);
+    if (!m->aarena) {
+        int rc = alloc_acts(m, B, T);
+        if (rc) return rc;
+    } else if (B != m->B || T != m->T) {
+        return fail(m, GPT2_ERR_SHAPE, "activations were allocated for B=%d T=%d, got B=%d T=%d",
+                    m->B, m->T, B, T);
+    }
+    const int L = m->L, C = m->C, NH = m->NH, V = m->V, Vp = m->Vp;
+    const size_t M = (size_t)B * T, MC = M * C;
+    cudaStream_t s = m->stream;
+    cudaMemcpyKind kind = where == GPT2_DEVICE ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+    CK(cudaMemcpyAsync(m->tok, tokens, M * 4, kind, s));
+    if (targets) CK(cudaMemcpyAsync(m->tgt, targets, M * 4, kind, s));
+    CK(cudaMemsetAsync(m->flags, 0, 64, s));
+    CK(check_ids(m->tok, (int)M, V, m->flags, G2_FLAG_BAD_TOKEN, s));
+    if (targets) CK(check_ids(m->tgt, (int)M, V, m->flags, G2_FLAG_BAD_TARGET, s));
+
+    CK(encoder_forward(m->at, m->res, m->tok, pw(m, P_WTE, 0), pw(m, P_WPE, 0), B, T, C, V,
+                       m->flags, s));
+    for (int l = 0; l < L; l++) {
+        char* res_in = act(m, m->res, l * MC);
+        char* res_out = act(m, m->res, (l + 1) * MC);
+        char* res2 = act(m, m->res2, l * MC);
+        char* ln1 = act(m, m->ln1, l * MC);
+        char* qkv = act(m, m->qkv, l * 3 * MC);
+        char* atty = act(m, m->atty, l * MC);
+        char* ln2 = act(m, m->ln2, l * MC);
+        char* fch = act(m, m->fch, l * 4 * MC);
+        char* fchg = act(m, m->fchg, l * 4 * MC);
+        CK(layernorm_forward(m->at, ln1, m->ln1_mean + l * M, m->ln1_rstd + l * M, res_in,
+                             pf(m, m->params, P_LN1W) + l * C, pf(m, m->params, P_LN1B) + l * C,
+                             (int)M, C, s));
+        CK(gemm_fwd(m, (int)M, 3 * C, C, ln1, pw(m, P_QKVW, (size_t)l * 3 * C * C),
+                    pf(m, m->params, P_QKVB) + l * 3 * C, qkv, nullptr, nullptr));
+        CK(attention_forward(m->at, atty, m->lse + l * M * NH, qkv, B, T, C, NH, s));
+        CK(gemm_fwd(m, (int)M, C, C, atty, pw(m, P_APW, (size_t)l * C * C),
+                    pf(m, m->params, P_APB) + l * C, res2, res_in, nullptr));
+        CK(layernorm_forward(m->at, ln2, m->ln2_mean + l * M, m->ln2_rstd + l * M, res2,
+                             pf(m, m->params, P_LN2W) + l * C, pf(m, m->params, P_LN2B) + l * C,
+                             (int)M, C, s));
+        CK(gemm_fwd(m, (int)M, 4 * C, C, ln2, pw(m, P_FCW, (size_t)l * 4 * C * C),
+                    pf(m, m->params, P_FCB) + l * 4 * C, fch, nullptr, fchg));
+        CK(gemm_fwd(m, (int)M, C, 4 * C, fchg, pw(m, P_FPW, (size_t)l * 4 * C * C),
+                    pf(m, m->params, P_FPB) + l * C, res_out, res2, nullptr));
+    }
+    CK(layernorm_forward(m->at, m->lnf, m->lnf_mean, m->lnf_rstd, act(m, m->res, (size_t)L * MC),
+                         pf(m, m->params, P_LNFW), pf(m, m->params, P_LNFB), (int)M, C, s));
+    CK(gemm_fwd(m, (int)M, Vp, C, m->lnf, pw(m, P_WTE, 0), nullptr, m->logits, nullptr, nullptr));
+    if (targets) {
+        CK(softmax_xent(m->at, m->logits, m->losses, m->tgt, (int)M, V, Vp, 1.0f / (float)M,
+                        m->flags, s));
+        CK(mean_fixed_order(m->loss, m->losses, (int)M, s));
+        m->fwd_targets = true;
+        m->logits_valid = false;
+    } else {
+        m->fwd_targets = false;
+        m->logits_valid = true;
+    }
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_forward_async(gpt2_t* m, const int32_t* tokens, const int32_t* targets, int B,
+                                  int T, int where) {
+    if (!m) return GPT2_ERR_ARG;
+    m->status = GPT2_OK;
+    return forward_impl(m, tokens, targets, B, T, where);
+}
+
+extern "C" int gpt2_read_loss(gpt2_t* m, float* out) {
+    if (!m || !out) return fail(m, GPT2_ERR_ARG, "null argument");
+    if (!m->aarena) return fail(m, GPT2_ERR_STATE, "no forward has run");
+    int hflags[2] = {0, 0};
+    float loss = -1.0f;
+    if (m->fwd_targets) CK(cudaMemcpyAsync(&loss, m->loss, 4, cudaMemcpyDeviceToHost, m->stream));
+    CK(cudaMemcpyAsync(hflags, m->flags, 4, cudaMemcpyDeviceToHost, m->stream));
+    CK(cudaStreamSynchronize(m->stream));
+    *out = loss;
+    if (hflags[0] & G2_FLAG_BAD_TOKEN)
+        return fail(m, GPT2_ERR_TOKEN, "an input id is outside [0, %d)", m->V);
+    if (hflags[0] & G2_FLAG_BAD_TARGET)
+        return fail(m, GPT2_ERR_TOKEN, "a target id is outside [0, %d)", m->V);
+    if (m->fwd_targets && !std::isfinite(loss))
+        return fail(m, GPT2_ERR_NONFINITE, "mean loss is not finite (%f)", loss);
+    return GPT2_OK;
+}
+
+extern "C" float gpt2_forward(gpt2_t* m, const int32_t* tokens, const int32_t* targets, int B, int T) {
+    if (!m) return NAN;
+    m->status = GPT2_OK;
+    int rc = forward_impl(m, tokens, targets, B, T, GPT2_HOST);
+    if (rc) return NAN;
+    float loss;
+    rc = gpt2_read_loss(m, &loss);
+    if (rc) {
+        m->fwd_targets = false;  // a failed forward cannot feed a backward
+        return NAN;
+    }
+    return loss;
+}
+
+// ------------------------------------------------------------------ backward
+extern "C" int gpt2_backward(gpt2_t* m) {
+    if (!m) return GPT2_ERR_ARG;
+    if (!m->fwd_targets) return fail(m, GPT2_ERR_STATE, "backward needs a forward with targets first");
+    const int L = m->L, C = m->C, NH = m->NH, V = m->V, Vp = m->Vp, B = m->B, T = m->T;
+    const size_t M = (size_t)B * T, MC = M * C;
+    cudaStream_t s = m->stream;
+    float* g = m->grads;
+    // vocab projection (tied): dlnf = dlogits . wte ; dwte = dlogits^T . lnf (overwrites)
+    CK(gemm_dgrad(m, (int)M, Vp, C, m->logits, pw(m, P_WTE, 0), m->dln, nullptr));
+    CK(gemm_wgrad(m, (int)M, Vp, C, m->logits, m->lnf, pf(m, g, P_WTE)));
+    CK(cudaMemsetAsync(m->dres, 0, MC * m->esz, s));
+    CK(layernorm_backward(m->at, m->dres, pf(m, g, P_LNFW), pf(m, g, P_LNFB), m->dln,
+                          act(m, m->res, (size_t)L * MC), pf(m, m->params, P_LNFW), m->lnf_mean,
+                          m->lnf_rstd, (int)M, C, m->ln_part, s));
+    for (int l = L - 1; l >= 0; l--) {
+        char* res_in = act(m, m->res, l * MC);
+        char* res2 = act(m, m->res2, l * MC);
+        char* ln1 = act(m, m->ln1, l * MC);
+        char* qkv = act(m, m->qkv, l * 3 * MC);
+        char* atty = act(m, m->atty, l * MC);
+        char* ln2 = act(m, m->ln2, l * MC);
+        char* fch = act(m, m->fch, l * 4 * MC);
+        char* fchg = act(m, m->fchg, l * 4 * MC);
+        // fcproj: res_out = fchg . Wfp^T + bfp + res2   (dres = d res_out)
+        CK(gemm_dgrad(m, (int)M, C, 4 * C, m->dres, pw(m, P_FPW, (size_t)l * 4 * C * C), m->dfch, fch));
+        CK(gemm_wgrad(m, (int)M, C, 4 * C, m->dres, fchg, pf(m, g, P_FPW) + (size_t)l * 4 * C * C));
+        CK(colsum(m->at, pf(m, g, P_FPB) + l * C, m->dres, (int)M, C, m->cs_part, s));
+        // fc: fch = ln2 . Wfc^T + bfc   (dfch already multiplied by gelu')
+        CK(gemm_dgrad(m, (int)M, 4 * C, C, m->dfch, pw(m, P_FCW, (size_t)l * 4 * C * C), m->dln, nullptr));
+        CK(gemm_wgrad(m, (int)M, 4 * C, C, m->dfch, ln2, pf(m, g, P_FCW) + (size_t)l * 4 * C * C));
+        CK(colsum(m->at, pf(m, g, P_FCB) + l * 4 * C, m->dfch, (int)M, 4 * C, m->cs_part, s));
+        // ln2 (dres becomes d res2)
+        CK(layernorm_backward(m->at, m->dres, pf(m, g, P_LN2W) + l * C, pf(m, g, P_LN2B) + l * C,
+                              m->dln, res2, pf(m, m->params, P_LN2W) + l * C,
+                              m->ln2_mean + l * M, m->ln2_rstd + l * M, (int)M, C, m->ln_part, s));
+        // attproj: res2 = atty . Wap^T + bap + res_in
+        CK(gemm_dgrad(m, (int)M, C, C, m->dres, pw(m, P_APW, (size_t)l * C * C), m->datty, nullptr));
+        CK(gemm_wgrad(m, (int)M, C, C, m->dres, atty, pf(m, g, P_APW) + (size_t)l * C * C));
+        CK(colsum(m->at, pf(m, g, P_APB) + l * C, m->dres, (int)M, C, m->cs_part, s));
+        // attention
+        CK(attention_backward(m->at, m->dqkv, m->datty, qkv, atty, m->lse + l * M * NH, B, T, C, NH,
+                              m->attD, s));
+        // qkv: qkv = ln1 . Wqkv^T + bqkv
+        CK(gemm_dgrad(m, (int)M, 3 * C, C, m->dqkv, pw(m, P_QKVW, (size_t)l * 3 * C * C), m->dln, nullptr));
+        CK(gemm_wgrad(m, (int)M, 3 * C, C, m->dqkv, ln1, pf(m, g, P_QKVW) + (size_t)l * 3 * C * C));
+        CK(colsum(m->at, pf(m, g, P_QKVB) + l * 3 * C, m->dqkv, (int)M, 3 * C, m->cs_part, s));
+        // ln1 (dres becomes d res_in)
+        CK(layernorm_backward(m->at, m->dres, pf(m, g, P_LN1W) + l * C, pf(m, g, P_LN1B) + l * C,
+                              m->dln, res_in, pf(m, m->params, P_LN1W) + l * C,
+                              m->ln1_mean + l * M, m->ln1_rstd + l * M, (int)M, C, m->ln_part, s));
+    }
+    CK(encoder_backward_wpe(m->at, pf(m, g, P_WPE), m->dres, B, T, C, m->maxT, s));
+    CK(encoder_backward_wte(m->at, pf(m, g, P_WTE), m->dres, m->tok, (int)M, C, V, &m->enc, s));
+    m->fwd_targets = false;
+    m->have_grads = true;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_zero_grad(gpt2_t* m) {
+    if (!m) return GPT2_ERR_ARG;
+    CK(cudaMemsetAsync(m->grads, 0, m->npad * 4, m->stream));
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_update(gpt2_t* m, float lr, float b1, float b2, float eps, float wd, int t) {
+    if (!m) return GPT2_ERR_ARG;
+    if (t < 1) return fail(m, GPT2_ERR_ARG, "t must be >= 1 (got %d)", t);
+    if (!m->have_grads) return fail(m, GPT2_ERR_STATE, "update needs gradients (run backward)");
+    float c1 = 1.0f - powf(b1, (float)t), c2 = 1.0f - powf(b2, (float)t);
+    CK(adamw(m->params, m->grads, m->mom1, m->mom2, m->shadow, m->npad, lr, b1, b2, eps, wd, c1, c2,
+             m->stream));
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_get_losses(gpt2_t* m, float* host, size_t n) {
+    if (!m || !host) return fail(m, GPT2_ERR_ARG, "null argument");
+    if (!m->aarena) return fail(m, GPT2_ERR_STATE, "no forward has run");
+    if (n != (size_t)m->B * m->T) return fail(m, GPT2_ERR_ARG, "expected %d values", m->B * m->T);
+    CK(cudaMemcpyAsync(host, m->losses, n * 4, cudaMemcpyDeviceToHost, m->stream));
+    CK(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_get_logits(gpt2_t* m, float* host, size_t n) {
+    if (!m || !host) return fail(m, GPT2_ERR_ARG, "null argument");
+    if (!m->aarena || !m->logits_valid)
+        return fail(m, GPT2_ERR_STATE, "logits are only kept by a forward without targets");
+    const size_t M = (size_t)m->B * m->T;
+    if (n != M * m->V) return fail(m, GPT2_ERR_ARG, "expected %zu values", M * m->V);
+    if (m->at == ACT_F32) {
+        CK(cudaMemcpy2DAsync(host, (size_t)m->V * 4, m->logits, (size_t)m->Vp * 4, (size_t)m->V * 4, M,
+                             cudaMemcpyDeviceToHost, m->stream));
+        CK(cudaStreamSynchronize(m->stream));
+        return GPT2_OK;
+    }
+    // bf16: widen on the host, row by row, through a small staging buffer
+    const size_t rows_per = 64;
+    std::string stage(rows_per * m->Vp * 2, '\0');
+    for (size_t r0 = 0; r0 < M; r0 += rows_per) {
+        size_t nr = std::min(rows_per, M - r0);
+        CK(cudaMemcpyAsync(&stage[0], m->logits + r0 * m->Vp * 2, nr * m->Vp * 2,
+                           cudaMemcpyDeviceToHost, m->stream));
+        CK(cudaStreamSynchronize(m->stream));
+        const uint16_t* src = (const uint16_t*)stage.data();
+        for (size_t r = 0; r < nr; r++)
+            for (int c = 0; c < m->V; c++) {
+                uint32_t bits = (uint32_t)src[r * m->Vp + c] << 16;
+                float f;
+                memcpy(&f, &bits, 4);
+                host[(r0 + r) * m->V + c] = f;
+            }
+    }
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_get_ids(gpt2_t* m, int32_t* tok, int32_t* tgt, size_t n) {
+    if (!m || !tok) return fail(m, GPT2_ERR_ARG, "null argument");
+    if (!m->aarena) return fail(m, GPT2_ERR_STATE, "no forward has run");
+    if (n != (size_t)m->B * m->T) return fail(m, GPT2_ERR_ARG, "expected %d values", m->B * m->T);
+    CK(cudaMemcpyAsync(tok, m->tok, n * 4, cudaMemcpyDeviceToHost, m->stream));
+    if (tgt) CK(cudaMemcpyAsync(tgt, m->tgt, n * 4, cudaMemcpyDeviceToHost, m->stream));
+    CK(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}

@@ -1,0 +1,152 @@
+/*
+ * gpt2.h — C ABI of the B300 GPT-2 training step (forward, backward, AdamW).
+ *
+ * The operation is the one the llm.c listing defines on the page
+ * "llm.c 的中文注解-20240421" (sections 1.16-1.27: ParameterTensors, GPT2Config,
+ * gpt2_forward, gpt2_zero_grad, gpt2_backward, gpt2_update, gpt2_free) and that the
+ * picoGPT article ("60 行 NumPy 代码 ... 实现一个 GPT": gpt2, transformer_block, mha,
+ * ffn, lm_loss) states a second time: token + position embedding, L pre-LayerNorm
+ * blocks of causal multi-head attention and a tanh-GELU MLP with residuals, a final
+ * LayerNorm, a vocabulary projection tied to the token embedding, and softmax
+ * cross-entropy against the inputs shifted by one; AdamW over one flat buffer.
+ *
+ * Conventions shared by every entry point:
+ *  - A handle owns all of its device memory: one allocation for parameters,
+ *    gradients, AdamW moments (and the bf16 weight copy in GPT2_BF16 mode) made by
+ *    gpt2_build_ex, one for activations made by the first forward.  Nothing else is
+ *    allocated on the hot path.
+ *  - Parameter order and shapes are those of the listing (section 1.16): wte (V,C),
+ *    wpe (maxT,C), ln1w, ln1b (L,C), qkvw (L,3C,C), qkvb (L,3C), attprojw (L,C,C),
+ *    attprojb (L,C), ln2w, ln2b (L,C), fcw (L,4C,C), fcb (L,4C), fcprojw (L,C,4C),
+ *    fcprojb (L,C), lnfw, lnfb (C); weights are (out, in) row-major; fp32.  Host
+ *    buffers exchanged with set/get use exactly that layout with the real vocabulary
+ *    V; internally the vocabulary is padded to Vp (a multiple of 128) with zero rows
+ *    that never receive gradient.
+ *  - All work is ordered on the handle's CUDA stream (gpt2_set_stream; default: the
+ *    legacy default stream).  Only the calls documented as synchronising wait for it.
+ *  - Host pointers are read or written only during the call; the library keeps no
+ *    reference to caller memory.  Device pointers must stay valid until the work
+ *    queued by the call has run.
+ *  - A handle is not thread-safe.  Errors never abort the process: calls return a
+ *    negative gpt2_status and gpt2_last_error() describes the last failure.
+ */
+#ifndef GPT2_B300_H
+#define GPT2_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gpt2 gpt2_t;
+
+/* Status codes.  The listing exits the process on these conditions (bad model
+ * state, ids out of range, B,T changing after the first forward, backward without
+ * a forward with targets); this library returns them instead. */
+enum gpt2_status {
+    GPT2_OK = 0,
+    GPT2_ERR_ARG = -1,       /* bad argument: NULL pointer, size mismatch, t < 1, ... */
+    GPT2_ERR_OOM = -2,       /* device allocation failed; the handle stays freeable */
+    GPT2_ERR_CUDA = -3,      /* a CUDA call failed; see gpt2_last_error */
+    GPT2_ERR_TOKEN = -4,     /* an input id or target outside [0, V) */
+    GPT2_ERR_SHAPE = -5,     /* (B,T) differs from the first forward, or T > maxT */
+    GPT2_ERR_STATE = -6,     /* call order: backward before a forward with targets, ... */
+    GPT2_ERR_NONFINITE = -7, /* the mean loss is NaN or infinite */
+    GPT2_ERR_TIMEOUT = -8    /* a device-side bounded wait gave up (reported, never hangs) */
+};
+
+/* Arithmetic of the step.
+ * GPT2_FP32: every tensor fp32, fp32 arithmetic everywhere (no TF32).
+ * GPT2_BF16: bf16 activations and matrix operands, fp32 accumulation, fp32 master
+ *            parameters, gradients and AdamW moments (mixed precision). */
+enum gpt2_precision { GPT2_FP32 = 0, GPT2_BF16 = 2 };
+
+/* Where the id arrays of gpt2_forward_async live. */
+enum gpt2_memory { GPT2_HOST = 0, GPT2_DEVICE = 1 };
+
+/* Build a model (llm.c §1.20 GPT2Config, §1.22 sizes) and allocate its parameter
+ * arena on the current CUDA device: parameters are zero until gpt2_set_params.
+ * L layers, C channels, H heads (C % H == 0), V real vocabulary size, maxT maximum
+ * sequence length.  Returns NULL on failure; *status (may be NULL) receives the code. */
+gpt2_t* gpt2_build_ex(int L, int C, int H, int V, int maxT, int precision, int* status);
+/* gpt2_build_ex(..., GPT2_BF16, NULL). */
+gpt2_t* gpt2_build(int L, int C, int H, int V, int maxT);
+/* Release everything the handle owns (llm.c §1.27).  NULL is accepted. */
+void gpt2_free(gpt2_t* m);
+
+/* Number of parameters in the listing's layout with the real vocabulary V
+ * (124,439,808 for L=12, C=768, V=50257, maxT=1024). */
+size_t gpt2_num_params(const gpt2_t* m);
+/* Vocabulary rows held on the device (V rounded up to a multiple of 128). */
+int gpt2_padded_vocab(const gpt2_t* m);
+
+/* Copy n = gpt2_num_params() fp32 values in, or out, in the layout above.  set also
+ * refreshes the bf16 weight copy.  Synchronising.  GPT2_ERR_ARG if n differs. */
+int gpt2_set_params(gpt2_t* m, const float* host, size_t n);
+int gpt2_get_params(gpt2_t* m, float* host, size_t n);
+/* Gradients of the last gpt2_backward (same layout).  GPT2_ERR_STATE before any. */
+int gpt2_get_grads(gpt2_t* m, float* host, size_t n);
+/* AdamW first and second moments (same layout; zero before the first update). */
+int gpt2_get_opt_state(gpt2_t* m, float* m_host, float* v_host, size_t n);
+
+/* Forward pass (llm.c §1.23).  tokens and targets are (B,T) int32 row-major host
+ * arrays; targets may be NULL.  The first call fixes (B,T) and allocates the
+ * activation arena; later calls must use the same (B,T) (GPT2_ERR_SHAPE); T <= maxT.
+ * Returns the mean cross-entropy loss over all B*T positions, -1.0f when targets is
+ * NULL (the listing's convention), or NaN on error (gpt2_last_status tells which).
+ * Synchronising (one device-to-host read of the loss).  With targets, the logits
+ * buffer is overwritten by the loss gradient for the following gpt2_backward. */
+float gpt2_forward(gpt2_t* m, const int32_t* tokens, const int32_t* targets, int B, int T);
+/* Same work without waiting: ids are read from host (copied on the stream) or device
+ * memory per `where`.  Id range errors and a non-finite loss are reported by the
+ * next gpt2_read_loss.  Returns a gpt2_status. */
+int gpt2_forward_async(gpt2_t* m, const int32_t* tokens, const int32_t* targets, int B, int T,
+                       int where);
+/* Wait for the stream and read the mean loss of the last forward (-1.0f without
+ * targets).  Returns GPT2_ERR_TOKEN / GPT2_ERR_NONFINITE if the forward saw bad ids
+ * or a non-finite loss. */
+int gpt2_read_loss(gpt2_t* m, float* loss_host);
+
+/* Backward pass (llm.c §1.25).  Needs a forward with targets since the last
+ * backward (GPT2_ERR_STATE otherwise).  Overwrites the gradient buffer (equivalent
+ * to the listing's zero_grad followed by its accumulating backward).  Asynchronous. */
+int gpt2_backward(gpt2_t* m);
+/* Zero the gradient buffer (llm.c §1.24).  Asynchronous. */
+int gpt2_zero_grad(gpt2_t* m);
+/* AdamW (llm.c §1.26) over the whole flat parameter buffer, all tensors alike:
+ * m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2; p -= lr (m/(1-b1^t) / (sqrt(v/(1-b2^t))
+ * + eps) + wd p).  t counts updates from 1 (GPT2_ERR_ARG if t < 1).  Needs
+ * gradients (GPT2_ERR_STATE).  Asynchronous. */
+int gpt2_update(gpt2_t* m, float lr, float b1, float b2, float eps, float wd, int t);
+
+/* Per-position losses (B,T) of the last forward with targets; n = B*T.  Synchronising. */
+int gpt2_get_losses(gpt2_t* m, float* host, size_t n);
+/* Logits (B,T,V) of the last forward WITHOUT targets (real columns, fp32); n = B*T*V.
+ * Synchronising.  GPT2_ERR_STATE if the last forward had targets (its logits were
+ * turned into the loss gradient in place). */
+int gpt2_get_logits(gpt2_t* m, float* host, size_t n);
+
+/* The device copies of the last forward's token ids and targets (B*T each; targets
+ * may be NULL).  Synchronising. */
+int gpt2_get_ids(gpt2_t* m, int32_t* tokens_host, int32_t* targets_host, size_t n);
+
+/* Run subsequent work on `stream` (a cudaStream_t; NULL = legacy default stream). */
+int gpt2_set_stream(gpt2_t* m, void* stream);
+/* Wait for all queued work; returns a gpt2_status for any pending CUDA error. */
+int gpt2_sync(gpt2_t* m);
+/* Last status and a human-readable description of the last failure. */
+int gpt2_last_status(const gpt2_t* m);
+const char* gpt2_last_error(const gpt2_t* m);
+/* Message of the last gpt2_build_ex failure (process-wide). */
+const char* gpt2_last_build_error(void);
+/* Number of kernel launches the handle has queued since it was built. */
+uint64_t gpt2_kernel_launches(const gpt2_t* m);
+/* Device bytes held by the handle (parameter arena + activation arena). */
+size_t gpt2_device_bytes(const gpt2_t* m);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPT2_B300_H */
