@@ -1,0 +1,390 @@
+#!/usr/bin/env python3
+"""Throughput of one GPT-2 training step (forward + backward + AdamW) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gpt2_124m|gpt2_350m|...]
+
+Prints ONE JSON line on rank 0.  The workload is GPT-2 124M (L=12, C=768, H=12,
+V=50257 padded to 50304 on the device) at B=32, T=1024 in bf16 mixed precision, on a
+seeded synthetic Zipf(1.1) token stream with N(0, 0.02) initial weights.
+
+`value` times W warm-up steps and then K steps with the ids already resident in device
+memory (CUDA events on the library's stream, max over ranks).  `e2e` times K more steps
+through the public host-pointer call gpt2_forward (ids copied from pinned host memory,
+the loss read back every step).  With N > 1, each rank trains its own independent
+replica on its own slice of the token stream (the step has no cross-rank exchange in
+this build), so scaling is weak.
+
+--impl reference times the CPU oracle (test infrastructure, plain C, all host cores)
+on bounded samples of the same workload, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "training tokens/sec (fwd+bwd+AdamW) for GPT-2 124M at B=32,T=1024; MFU vs BF16 peak"
+NOMINAL_BF16_TFLOPS = 2250.0  # dense bf16 per GPU, nominal
+DATA = "synthetic: seeded Zipf(s=1.1) token stream (xorshift64*), N(0,0.02) init"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, source="fallback")
+
+
+def flops_per_token(c, Vp):
+    """Algorithmic train FLOPs per token: GEMMs 6*(12*L*C^2 + Vp*C) plus causal attention
+    3 * 2 * C * (T+1) * L (QK^T and PV over t2 <= t; backward = 2x forward)."""
+    L, C, T = c["L"], c["C"], c["T"]
+    return 6.0 * (12 * L * C * C + Vp * C) + 3.0 * 2.0 * C * (T + 1) * L
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.remove(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ traffic from ncu
+def recorded_traffic(kernel_class: str):
+    """dram bytes per launch measured by ncu for this kernel class, if the summary under
+    profiles/ was taken on the current source of that kernel (else None)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_class)
+    if not d:
+        return None
+    h = hashlib.sha256()
+    for f in d.get("sources", []):
+        fp = os.path.join(ROOT, f)
+        if not os.path.exists(fp):
+            return None
+        h.update(open(fp, "rb").read())
+    if h.hexdigest() != d.get("sha256"):
+        return None
+    return d.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def oracle_sample(cfg, T_sample, stream_seed=1337):
+    """Time the CPU oracle on one bounded sample: fwd+bwd+AdamW of the workload's model on
+    B=1, T=T_sample (the first T_sample positions of row 0 of step 0)."""
+    from gpt_train_step_arena_b300 import synth
+    from oracle.oracle import Model, cpu_threads
+    L, C, NH, V, maxT = cfg["L"], cfg["C"], cfg["NH"], cfg["V"], cfg["maxT"]
+    params = synth.init_params(L, C, V, maxT, seed=42)
+    stream = synth.token_stream(cfg, steps=1, seed=stream_seed)
+    inp = stream[:T_sample].reshape(1, T_sample)
+    tgt = stream[1:T_sample + 1].reshape(1, T_sample)
+    m = Model(L, C, NH, V, maxT)
+    m.set_params(params)
+    return m, inp, tgt, cpu_threads()
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the oracle on the host cores, rank 0 only."""
+    if rank != 0:
+        return
+    from gpt_train_step_arena_b300 import synth
+    cfg = dict(synth.WORKLOADS[args.workload])
+    T_s = args.ref_tokens
+    m, inp, tgt, cores = oracle_sample(cfg, T_s)
+    hp = (cfg["lr"], cfg["b1"], cfg["b2"], cfg["eps"], cfg["wd"])
+    for i in range(args.warmup):
+        m.forward(inp, tgt)
+        m.backward()
+        m.update(*hp, i + 1)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        m.forward(inp, tgt)
+        m.backward()
+        m.update(*hp, args.warmup + i + 1)
+    dt = time.perf_counter() - t0
+    value = args.steps * T_s / dt
+    sample = (f"each step: fwd+bwd+AdamW of the full {args.workload} model (all parameters) on "
+              f"B=1,T={T_s} (first {T_s} positions of row 0 of the synthetic stream); f64 oracle, OpenMP")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": DATA, "config": config_block(cfg, args.workload),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(cfg, workload):
+    Vp = (cfg["V"] + 127) // 128 * 128
+    return {"workload": workload, "L": cfg["L"], "C": cfg["C"], "H": cfg["NH"], "V": cfg["V"], "Vp": Vp,
+            "B": cfg["B"], "T": cfg["T"], "precision": "bf16 mixed (fp32 master/AdamW)",
+            "lr": cfg["lr"], "wd": cfg["wd"],
+            "l2": "no flush: every step streams > 10 GB of activations and weights, far above the 126 MB L2"}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+    from gpt_train_step_arena_b300 import synth
+    from gpt_train_step_arena_b300.model import GPT2
+
+    torch.cuda.set_device(local)
+    cfg = dict(synth.WORKLOADS[args.workload])
+    L, C, NH, V, maxT, B, T = (cfg[k] for k in ("L", "C", "NH", "V", "maxT", "B", "T"))
+    hp = (cfg["lr"], cfg["b1"], cfg["b2"], cfg["eps"], cfg["wd"])
+    W, K = args.warmup, args.steps
+    params = synth.init_params(L, C, V, maxT, seed=42)
+    stream = synth.token_stream(cfg, steps=W + 2 * K, seed=1337 + rank)
+    batches = [synth.batch(stream, s, B, T) for s in range(W + 2 * K)]
+
+    g = GPT2(L, C, NH, V, maxT, precision="bf16")
+    g.set_params(params)
+    s = torch.cuda.Stream()
+    g.set_stream(s.cuda_stream)
+    tok_dev = torch.from_numpy(np.stack([b[0] for b in batches])).to(f"cuda:{local}")
+    tgt_dev = torch.from_numpy(np.stack([b[1] for b in batches])).to(f"cuda:{local}")
+    torch.cuda.synchronize()
+
+    step_no = 0
+
+    def dev_step(i):
+        nonlocal step_no
+        step_no += 1
+        g.forward_async(tok_dev[i], tgt_dev[i], B, T, device=True)
+        g.backward()
+        g.update(*hp, step_no)
+
+    for i in range(W):
+        dev_step(i)
+    first_loss = g.read_loss()
+    torch.cuda.synchronize()
+    barrier(world)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    g.profile_reset()
+    g.profile_enable(True)
+    launches0 = g.kernel_launches()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0.record(s)
+    for i in range(W, W + K):
+        dev_step(i)
+    ev1.record(s)
+    torch.cuda.synchronize()
+    launches = g.kernel_launches() - launches0
+    elapsed_ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    g.profile_enable(False)
+    prof = g.profile_read()
+    last_loss = g.read_loss()
+    barrier(world)
+    max_ms = max_over_ranks(elapsed_ms, world)
+
+    # e2e: the public host-pointer call, ids from pinned host memory, loss read back
+    tok_h = torch.from_numpy(np.stack([b[0] for b in batches])).pin_memory()
+    tgt_h = torch.from_numpy(np.stack([b[1] for b in batches])).pin_memory()
+    from gpt_train_step_arena_b300 import _native as N
+    for i in range(W + K, W + K + 2):
+        loss = N.lib.gpt2_forward(g.h, tok_h[i].data_ptr(), tgt_h[i].data_ptr(), B, T)
+        g.backward()
+        step_no += 1
+        g.update(*hp, step_no)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(W + K, W + 2 * K):
+        loss = N.lib.gpt2_forward(g.h, tok_h[i].data_ptr(), tgt_h[i].data_ptr(), B, T)
+        if not math.isfinite(loss):
+            raise RuntimeError(f"e2e forward failed: {N.lib.gpt2_last_error(g.h).decode()}")
+        g.backward()
+        step_no += 1
+        g.update(*hp, step_no)
+    g.sync()
+    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        m, inp, tgt, cores = oracle_sample(cfg, args.cpu_tokens)
+        t1 = time.perf_counter()
+        m.forward(inp, tgt)
+        m.backward()
+        m.update(*hp, 1)
+        dt = time.perf_counter() - t1
+        cpu = {"value": args.cpu_tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": (f"one fwd+bwd+AdamW of the full {args.workload} model on B=1,T={args.cpu_tokens} "
+                          f"(first {args.cpu_tokens} positions of row 0 of step 0), f64 oracle, OpenMP; "
+                          f"{dt:.1f} s; per-token cost at T=1024 is higher (attention grows with T)")}
+        del m
+
+    if rank != 0:
+        return
+    pk = _peaks()
+    Vp = g.Vp
+    fpt = flops_per_token(cfg, Vp)
+    ms_step = max_ms / K
+    tokens = world * K * B * T
+    value = tokens / (max_ms / 1000.0)
+    kernels = {}
+    for name, (ms, work, calls) in prof.items():
+        if calls == 0:
+            continue
+        is_flops = name in ("gemm", "attn_fwd", "attn_bwd")
+        kernels[name] = {"ms_per_step": ms / K, "calls_per_step": calls / K,
+                         ("tflops" if is_flops else "gbs"): (work / (ms / 1e3)) / (1e12 if is_flops else 1e9)}
+    dom = max(prof.items(), key=lambda kv: kv[1][0])
+    dname, (dms, dwork, dcalls) = dom
+    tensor = dname in ("gemm", "attn_fwd", "attn_bwd")
+    if tensor:
+        achieved = dwork / (dms / 1e3) / 1e12
+        peak = pk["bf16_sus"]
+        unit = "TFLOP/s"
+    else:
+        achieved = dwork / (dms / 1e3) / 1e9
+        peak = pk["hbm"]
+        unit = "GB/s"
+    roofline = {"bound": "tensor" if tensor else "hbm", "kernel": dname, "achieved": achieved, "peak": peak,
+                "unit": unit, "frac": achieved / peak, "traffic": recorded_traffic(dname),
+                "peak_source": f"{pk['source']} ({'bf16 sustained' if tensor else 'HBM copy'})",
+                "work_per_launch": dwork / dcalls, "ms_per_launch": dms / dcalls}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": DATA, "config": config_block(cfg, args.workload),
+        "mfu": {"algorithmic_flops_per_token": fpt,
+                "vs_nominal_2250": value / world * fpt / (NOMINAL_BF16_TFLOPS * 1e12),
+                "vs_measured_burst": value / world * fpt / (pk["bf16"] * 1e12)},
+        "roofline": roofline,
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * K * B * T / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 8},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "loss": {"after_warmup": first_loss, "last": last_loss},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gpt2_124m")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=128)
+    ap.add_argument("--ref-tokens", type=int, default=32)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -40,6 +40,9 @@ SIGNATURES = {
     "gpt2_get_losses": (I, [P, P, SZ]),
     "gpt2_get_logits": (I, [P, P, SZ]),
     "gpt2_get_ids": (I, [P, P, P, SZ]),
+    "gpt2_profile_enable": (I, [P, I]),
+    "gpt2_profile_reset": (I, [P]),
+    "gpt2_profile_read": (I, [P, I, ct.POINTER(ct.c_double), ct.POINTER(ct.c_double), ct.POINTER(U64)]),
     "gpt2_set_stream": (I, [P, P]),
     "gpt2_sync": (I, [P]),
     "gpt2_last_status": (I, [P]),
@@ -59,6 +62,7 @@ GPT2_OK, GPT2_ERR_ARG, GPT2_ERR_OOM, GPT2_ERR_CUDA = 0, -1, -2, -3
 GPT2_ERR_TOKEN, GPT2_ERR_SHAPE, GPT2_ERR_STATE, GPT2_ERR_NONFINITE, GPT2_ERR_TIMEOUT = -4, -5, -6, -7, -8
 GPT2_FP32, GPT2_BF16 = 0, 2
 GPT2_HOST, GPT2_DEVICE = 0, 1
+KERNEL_CLASSES = ["gemm", "attn_fwd", "attn_bwd", "layernorm", "xent", "adamw", "encoder", "bias_grad"]
 
 STATUS_NAMES = {0: "GPT2_OK", -1: "GPT2_ERR_ARG", -2: "GPT2_ERR_OOM", -3: "GPT2_ERR_CUDA",
                 -4: "GPT2_ERR_TOKEN", -5: "GPT2_ERR_SHAPE", -6: "GPT2_ERR_STATE",

@@ -16,6 +16,7 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <vector>
 
 #include "../../include/gpt2.h"
 #include "common.cuh"
@@ -44,7 +45,7 @@ struct gpt2 {
     size_t pbytes;
     float *params, *grads, *mom1, *mom2;
     bf16* shadow;
-    bool opt_init, have_grads, fwd_targets;
+    bool opt_init, have_grads, fwd_targets, loss_valid;
     // activation arena
     void* aarena;
     size_t abytes;
@@ -59,6 +60,14 @@ struct gpt2 {
     size_t gemm_ws_bytes;
     EncoderBwdScratch enc;
     bool logits_valid;
+    // per-kernel-class timing (gpt2_profile_*): one event pair per launched op
+    bool prof_on;
+    std::vector<cudaEvent_t> ev_a, ev_b;
+    std::vector<int> ev_cls;
+    std::vector<double> ev_work;
+    size_t ev_used;
+    double prof_ms[GPT2_K_COUNT], prof_work[GPT2_K_COUNT];
+    uint64_t prof_calls[GPT2_K_COUNT];
     cudaStream_t stream;
     int status;
     std::string err;
@@ -83,6 +92,34 @@ static int fail(gpt2* m, int code, const char* fmt, ...) {
         cudaError_t e_ = (expr);                                                          \
         if (e_ != cudaSuccess)                                                            \
             return fail(m, GPT2_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_)); \
+    } while (0)
+
+// Runs one op; with profiling on, brackets it with a CUDA event pair on the stream and
+// books its algorithmic work (FLOPs or bytes) to kernel class `cls`.
+static int prof_begin(gpt2* m, int cls, double work) {
+    if (!m->prof_on) return -1;
+    if (m->ev_used == m->ev_a.size()) {
+        cudaEvent_t a, b;
+        if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return -1;
+        m->ev_a.push_back(a);
+        m->ev_b.push_back(b);
+        m->ev_cls.push_back(0);
+        m->ev_work.push_back(0);
+    }
+    size_t i = m->ev_used++;
+    m->ev_cls[i] = cls;
+    m->ev_work[i] = work;
+    cudaEventRecord(m->ev_a[i], m->stream);
+    return (int)i;
+}
+static void prof_end(gpt2* m, int i) {
+    if (i >= 0) cudaEventRecord(m->ev_b[i], m->stream);
+}
+#define OP(cls, work, expr)                      \
+    do {                                         \
+        int pi_ = prof_begin(m, (cls), (work));  \
+        CK(expr);                                \
+        prof_end(m, pi_);                        \
     } while (0)
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -203,6 +240,10 @@ extern "C" void gpt2_free(gpt2_t* m) {
     if (!m) return;
     if (m->parena) cudaFree(m->parena);
     if (m->aarena) cudaFree(m->aarena);
+    for (size_t i = 0; i < m->ev_a.size(); i++) {
+        cudaEventDestroy(m->ev_a[i]);
+        cudaEventDestroy(m->ev_b[i]);
+    }
     delete m;
 }
 
@@ -332,6 +373,13 @@ static int alloc_acts(gpt2* m, int B, int T) {
 }
 
 // ------------------------------------------------------------------ forward
+// Algorithmic work of one op (booked to its class when profiling).
+static double gemm_flops(size_t M, size_t N, size_t K) { return 2.0 * M * N * K; }
+static double attn_fwd_flops(const gpt2* m) {
+    // QK^T and PV over the causal triangle t2 <= t: 2 * 2 * hs * T(T+1)/2 per (b, h)
+    return 2.0 * m->B * m->NH * (double)(m->C / m->NH) * m->T * (m->T + 1.0);
+}
+
 static int forward_impl(gpt2* m, const int32_t* tokens, const int32_t* targets, int B, int T,
                         int where) {
     if (!m || !tokens) return fail(m, GPT2_ERR_ARG, "null argument");
@@ -346,16 +394,18 @@ static int forward_impl(gpt2* m, const int32_t* tokens, const int32_t* targets, 
     }
     const int L = m->L, C = m->C, NH = m->NH, V = m->V, Vp = m->Vp;
     const size_t M = (size_t)B * T, MC = M * C;
+    const double es = (double)m->esz, actMC = es * MC;
     cudaStream_t s = m->stream;
     cudaMemcpyKind kind = where == GPT2_DEVICE ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
     CK(cudaMemcpyAsync(m->tok, tokens, M * 4, kind, s));
     if (targets) CK(cudaMemcpyAsync(m->tgt, targets, M * 4, kind, s));
     CK(cudaMemsetAsync(m->flags, 0, 64, s));
-    CK(check_ids(m->tok, (int)M, V, m->flags, G2_FLAG_BAD_TOKEN, s));
-    if (targets) CK(check_ids(m->tgt, (int)M, V, m->flags, G2_FLAG_BAD_TARGET, s));
-
-    CK(encoder_forward(m->at, m->res, m->tok, pw(m, P_WTE, 0), pw(m, P_WPE, 0), B, T, C, V,
-                       m->flags, s));
+    OP(GPT2_K_ENCODER, 4.0 * M, check_ids(m->tok, (int)M, V, m->flags, G2_FLAG_BAD_TOKEN, s));
+    if (targets) OP(GPT2_K_ENCODER, 4.0 * M, check_ids(m->tgt, (int)M, V, m->flags, G2_FLAG_BAD_TARGET, s));
+    // gathered token rows + position rows + output
+    OP(GPT2_K_ENCODER, 2 * actMC + es * (double)T * C + 4.0 * M,
+       encoder_forward(m->at, m->res, m->tok, pw(m, P_WTE, 0), pw(m, P_WPE, 0), B, T, C, V, m->flags, s));
+    const double ln_fwd_bytes = 2 * actMC + 8.0 * M + 8.0 * C;
     for (int l = 0; l < L; l++) {
         char* res_in = act(m, m->res, l * MC);
         char* res_out = act(m, m->res, (l + 1) * MC);
@@ -366,33 +416,45 @@ static int forward_impl(gpt2* m, const int32_t* tokens, const int32_t* targets, 
         char* ln2 = act(m, m->ln2, l * MC);
         char* fch = act(m, m->fch, l * 4 * MC);
         char* fchg = act(m, m->fchg, l * 4 * MC);
-        CK(layernorm_forward(m->at, ln1, m->ln1_mean + l * M, m->ln1_rstd + l * M, res_in,
+        OP(GPT2_K_LAYERNORM, ln_fwd_bytes,
+           layernorm_forward(m->at, ln1, m->ln1_mean + l * M, m->ln1_rstd + l * M, res_in,
                              pf(m, m->params, P_LN1W) + l * C, pf(m, m->params, P_LN1B) + l * C,
                              (int)M, C, s));
-        CK(gemm_fwd(m, (int)M, 3 * C, C, ln1, pw(m, P_QKVW, (size_t)l * 3 * C * C),
+        OP(GPT2_K_GEMM, gemm_flops(M, 3 * C, C),
+           gemm_fwd(m, (int)M, 3 * C, C, ln1, pw(m, P_QKVW, (size_t)l * 3 * C * C),
                     pf(m, m->params, P_QKVB) + l * 3 * C, qkv, nullptr, nullptr));
-        CK(attention_forward(m->at, atty, m->lse + l * M * NH, qkv, B, T, C, NH, s));
-        CK(gemm_fwd(m, (int)M, C, C, atty, pw(m, P_APW, (size_t)l * C * C),
+        OP(GPT2_K_ATTN_FWD, attn_fwd_flops(m),
+           attention_forward(m->at, atty, m->lse + l * M * NH, qkv, B, T, C, NH, s));
+        OP(GPT2_K_GEMM, gemm_flops(M, C, C),
+           gemm_fwd(m, (int)M, C, C, atty, pw(m, P_APW, (size_t)l * C * C),
                     pf(m, m->params, P_APB) + l * C, res2, res_in, nullptr));
-        CK(layernorm_forward(m->at, ln2, m->ln2_mean + l * M, m->ln2_rstd + l * M, res2,
+        OP(GPT2_K_LAYERNORM, ln_fwd_bytes,
+           layernorm_forward(m->at, ln2, m->ln2_mean + l * M, m->ln2_rstd + l * M, res2,
                              pf(m, m->params, P_LN2W) + l * C, pf(m, m->params, P_LN2B) + l * C,
                              (int)M, C, s));
-        CK(gemm_fwd(m, (int)M, 4 * C, C, ln2, pw(m, P_FCW, (size_t)l * 4 * C * C),
+        OP(GPT2_K_GEMM, gemm_flops(M, 4 * C, C),
+           gemm_fwd(m, (int)M, 4 * C, C, ln2, pw(m, P_FCW, (size_t)l * 4 * C * C),
                     pf(m, m->params, P_FCB) + l * 4 * C, fch, nullptr, fchg));
-        CK(gemm_fwd(m, (int)M, C, 4 * C, fchg, pw(m, P_FPW, (size_t)l * 4 * C * C),
+        OP(GPT2_K_GEMM, gemm_flops(M, C, 4 * C),
+           gemm_fwd(m, (int)M, C, 4 * C, fchg, pw(m, P_FPW, (size_t)l * 4 * C * C),
                     pf(m, m->params, P_FPB) + l * C, res_out, res2, nullptr));
     }
-    CK(layernorm_forward(m->at, m->lnf, m->lnf_mean, m->lnf_rstd, act(m, m->res, (size_t)L * MC),
+    OP(GPT2_K_LAYERNORM, ln_fwd_bytes,
+       layernorm_forward(m->at, m->lnf, m->lnf_mean, m->lnf_rstd, act(m, m->res, (size_t)L * MC),
                          pf(m, m->params, P_LNFW), pf(m, m->params, P_LNFB), (int)M, C, s));
-    CK(gemm_fwd(m, (int)M, Vp, C, m->lnf, pw(m, P_WTE, 0), nullptr, m->logits, nullptr, nullptr));
+    OP(GPT2_K_GEMM, gemm_flops(M, Vp, C),
+       gemm_fwd(m, (int)M, Vp, C, m->lnf, pw(m, P_WTE, 0), nullptr, m->logits, nullptr, nullptr));
     if (targets) {
-        CK(softmax_xent(m->at, m->logits, m->losses, m->tgt, (int)M, V, Vp, 1.0f / (float)M,
-                        m->flags, s));
-        CK(mean_fixed_order(m->loss, m->losses, (int)M, s));
+        // read the logits once, write the gradient once, targets and per-row losses
+        OP(GPT2_K_XENT, 2.0 * es * M * Vp + 8.0 * M,
+           softmax_xent(m->at, m->logits, m->losses, m->tgt, (int)M, V, Vp, 1.0f / (float)M, m->flags, s));
+        OP(GPT2_K_XENT, 4.0 * M, mean_fixed_order(m->loss, m->losses, (int)M, s));
         m->fwd_targets = true;
+        m->loss_valid = true;
         m->logits_valid = false;
     } else {
         m->fwd_targets = false;
+        m->loss_valid = false;
         m->logits_valid = true;
     }
     return GPT2_OK;
@@ -410,7 +472,7 @@ extern "C" int gpt2_read_loss(gpt2_t* m, float* out) {
     if (!m->aarena) return fail(m, GPT2_ERR_STATE, "no forward has run");
     int hflags[2] = {0, 0};
     float loss = -1.0f;
-    if (m->fwd_targets) CK(cudaMemcpyAsync(&loss, m->loss, 4, cudaMemcpyDeviceToHost, m->stream));
+    if (m->loss_valid) CK(cudaMemcpyAsync(&loss, m->loss, 4, cudaMemcpyDeviceToHost, m->stream));
     CK(cudaMemcpyAsync(hflags, m->flags, 4, cudaMemcpyDeviceToHost, m->stream));
     CK(cudaStreamSynchronize(m->stream));
     *out = loss;
@@ -418,7 +480,7 @@ extern "C" int gpt2_read_loss(gpt2_t* m, float* out) {
         return fail(m, GPT2_ERR_TOKEN, "an input id is outside [0, %d)", m->V);
     if (hflags[0] & G2_FLAG_BAD_TARGET)
         return fail(m, GPT2_ERR_TOKEN, "a target id is outside [0, %d)", m->V);
-    if (m->fwd_targets && !std::isfinite(loss))
+    if (m->loss_valid && !std::isfinite(loss))
         return fail(m, GPT2_ERR_NONFINITE, "mean loss is not finite (%f)", loss);
     return GPT2_OK;
 }
@@ -432,6 +494,7 @@ extern "C" float gpt2_forward(gpt2_t* m, const int32_t* tokens, const int32_t* t
     rc = gpt2_read_loss(m, &loss);
     if (rc) {
         m->fwd_targets = false;  // a failed forward cannot feed a backward
+        m->loss_valid = false;
         return NAN;
     }
     return loss;
@@ -443,13 +506,19 @@ extern "C" int gpt2_backward(gpt2_t* m) {
     if (!m->fwd_targets) return fail(m, GPT2_ERR_STATE, "backward needs a forward with targets first");
     const int L = m->L, C = m->C, NH = m->NH, V = m->V, Vp = m->Vp, B = m->B, T = m->T;
     const size_t M = (size_t)B * T, MC = M * C;
+    const double es = (double)m->esz, actMC = es * MC;
     cudaStream_t s = m->stream;
     float* g = m->grads;
+    // bias gradient: read the (M,N) gradient once, write N floats
+    auto cs_bytes = [&](size_t N) { return es * M * N + 4.0 * N; };
+    // layernorm backward: read dout, x, dres; write dres; stats
+    const double ln_bwd_bytes = 4 * actMC + 8.0 * M + 16.0 * C;
     // vocab projection (tied): dlnf = dlogits . wte ; dwte = dlogits^T . lnf (overwrites)
-    CK(gemm_dgrad(m, (int)M, Vp, C, m->logits, pw(m, P_WTE, 0), m->dln, nullptr));
-    CK(gemm_wgrad(m, (int)M, Vp, C, m->logits, m->lnf, pf(m, g, P_WTE)));
+    OP(GPT2_K_GEMM, gemm_flops(M, C, Vp), gemm_dgrad(m, (int)M, Vp, C, m->logits, pw(m, P_WTE, 0), m->dln, nullptr));
+    OP(GPT2_K_GEMM, gemm_flops(Vp, C, M), gemm_wgrad(m, (int)M, Vp, C, m->logits, m->lnf, pf(m, g, P_WTE)));
     CK(cudaMemsetAsync(m->dres, 0, MC * m->esz, s));
-    CK(layernorm_backward(m->at, m->dres, pf(m, g, P_LNFW), pf(m, g, P_LNFB), m->dln,
+    OP(GPT2_K_LAYERNORM, ln_bwd_bytes,
+       layernorm_backward(m->at, m->dres, pf(m, g, P_LNFW), pf(m, g, P_LNFB), m->dln,
                           act(m, m->res, (size_t)L * MC), pf(m, m->params, P_LNFW), m->lnf_mean,
                           m->lnf_rstd, (int)M, C, m->ln_part, s));
     for (int l = L - 1; l >= 0; l--) {
@@ -462,35 +531,51 @@ extern "C" int gpt2_backward(gpt2_t* m) {
         char* fch = act(m, m->fch, l * 4 * MC);
         char* fchg = act(m, m->fchg, l * 4 * MC);
         // fcproj: res_out = fchg . Wfp^T + bfp + res2   (dres = d res_out)
-        CK(gemm_dgrad(m, (int)M, C, 4 * C, m->dres, pw(m, P_FPW, (size_t)l * 4 * C * C), m->dfch, fch));
-        CK(gemm_wgrad(m, (int)M, C, 4 * C, m->dres, fchg, pf(m, g, P_FPW) + (size_t)l * 4 * C * C));
-        CK(colsum(m->at, pf(m, g, P_FPB) + l * C, m->dres, (int)M, C, m->cs_part, s));
+        OP(GPT2_K_GEMM, gemm_flops(M, 4 * C, C),
+           gemm_dgrad(m, (int)M, C, 4 * C, m->dres, pw(m, P_FPW, (size_t)l * 4 * C * C), m->dfch, fch));
+        OP(GPT2_K_GEMM, gemm_flops(C, 4 * C, M),
+           gemm_wgrad(m, (int)M, C, 4 * C, m->dres, fchg, pf(m, g, P_FPW) + (size_t)l * 4 * C * C));
+        OP(GPT2_K_BIAS_GRAD, cs_bytes(C), colsum(m->at, pf(m, g, P_FPB) + l * C, m->dres, (int)M, C, m->cs_part, s));
         // fc: fch = ln2 . Wfc^T + bfc   (dfch already multiplied by gelu')
-        CK(gemm_dgrad(m, (int)M, 4 * C, C, m->dfch, pw(m, P_FCW, (size_t)l * 4 * C * C), m->dln, nullptr));
-        CK(gemm_wgrad(m, (int)M, 4 * C, C, m->dfch, ln2, pf(m, g, P_FCW) + (size_t)l * 4 * C * C));
-        CK(colsum(m->at, pf(m, g, P_FCB) + l * 4 * C, m->dfch, (int)M, 4 * C, m->cs_part, s));
+        OP(GPT2_K_GEMM, gemm_flops(M, C, 4 * C),
+           gemm_dgrad(m, (int)M, 4 * C, C, m->dfch, pw(m, P_FCW, (size_t)l * 4 * C * C), m->dln, nullptr));
+        OP(GPT2_K_GEMM, gemm_flops(4 * C, C, M),
+           gemm_wgrad(m, (int)M, 4 * C, C, m->dfch, ln2, pf(m, g, P_FCW) + (size_t)l * 4 * C * C));
+        OP(GPT2_K_BIAS_GRAD, cs_bytes(4 * C),
+           colsum(m->at, pf(m, g, P_FCB) + l * 4 * C, m->dfch, (int)M, 4 * C, m->cs_part, s));
         // ln2 (dres becomes d res2)
-        CK(layernorm_backward(m->at, m->dres, pf(m, g, P_LN2W) + l * C, pf(m, g, P_LN2B) + l * C,
+        OP(GPT2_K_LAYERNORM, ln_bwd_bytes,
+           layernorm_backward(m->at, m->dres, pf(m, g, P_LN2W) + l * C, pf(m, g, P_LN2B) + l * C,
                               m->dln, res2, pf(m, m->params, P_LN2W) + l * C,
                               m->ln2_mean + l * M, m->ln2_rstd + l * M, (int)M, C, m->ln_part, s));
         // attproj: res2 = atty . Wap^T + bap + res_in
-        CK(gemm_dgrad(m, (int)M, C, C, m->dres, pw(m, P_APW, (size_t)l * C * C), m->datty, nullptr));
-        CK(gemm_wgrad(m, (int)M, C, C, m->dres, atty, pf(m, g, P_APW) + (size_t)l * C * C));
-        CK(colsum(m->at, pf(m, g, P_APB) + l * C, m->dres, (int)M, C, m->cs_part, s));
+        OP(GPT2_K_GEMM, gemm_flops(M, C, C),
+           gemm_dgrad(m, (int)M, C, C, m->dres, pw(m, P_APW, (size_t)l * C * C), m->datty, nullptr));
+        OP(GPT2_K_GEMM, gemm_flops(C, C, M),
+           gemm_wgrad(m, (int)M, C, C, m->dres, atty, pf(m, g, P_APW) + (size_t)l * C * C));
+        OP(GPT2_K_BIAS_GRAD, cs_bytes(C), colsum(m->at, pf(m, g, P_APB) + l * C, m->dres, (int)M, C, m->cs_part, s));
         // attention
-        CK(attention_backward(m->at, m->dqkv, m->datty, qkv, atty, m->lse + l * M * NH, B, T, C, NH,
+        OP(GPT2_K_ATTN_BWD, 2.0 * attn_fwd_flops(m),
+           attention_backward(m->at, m->dqkv, m->datty, qkv, atty, m->lse + l * M * NH, B, T, C, NH,
                               m->attD, s));
         // qkv: qkv = ln1 . Wqkv^T + bqkv
-        CK(gemm_dgrad(m, (int)M, 3 * C, C, m->dqkv, pw(m, P_QKVW, (size_t)l * 3 * C * C), m->dln, nullptr));
-        CK(gemm_wgrad(m, (int)M, 3 * C, C, m->dqkv, ln1, pf(m, g, P_QKVW) + (size_t)l * 3 * C * C));
-        CK(colsum(m->at, pf(m, g, P_QKVB) + l * 3 * C, m->dqkv, (int)M, 3 * C, m->cs_part, s));
+        OP(GPT2_K_GEMM, gemm_flops(M, C, 3 * C),
+           gemm_dgrad(m, (int)M, 3 * C, C, m->dqkv, pw(m, P_QKVW, (size_t)l * 3 * C * C), m->dln, nullptr));
+        OP(GPT2_K_GEMM, gemm_flops(3 * C, C, M),
+           gemm_wgrad(m, (int)M, 3 * C, C, m->dqkv, ln1, pf(m, g, P_QKVW) + (size_t)l * 3 * C * C));
+        OP(GPT2_K_BIAS_GRAD, cs_bytes(3 * C),
+           colsum(m->at, pf(m, g, P_QKVB) + l * 3 * C, m->dqkv, (int)M, 3 * C, m->cs_part, s));
         // ln1 (dres becomes d res_in)
-        CK(layernorm_backward(m->at, m->dres, pf(m, g, P_LN1W) + l * C, pf(m, g, P_LN1B) + l * C,
+        OP(GPT2_K_LAYERNORM, ln_bwd_bytes,
+           layernorm_backward(m->at, m->dres, pf(m, g, P_LN1W) + l * C, pf(m, g, P_LN1B) + l * C,
                               m->dln, res_in, pf(m, m->params, P_LN1W) + l * C,
                               m->ln1_mean + l * M, m->ln1_rstd + l * M, (int)M, C, m->ln_part, s));
     }
-    CK(encoder_backward_wpe(m->at, pf(m, g, P_WPE), m->dres, B, T, C, m->maxT, s));
-    CK(encoder_backward_wte(m->at, pf(m, g, P_WTE), m->dres, m->tok, (int)M, C, V, &m->enc, s));
+    OP(GPT2_K_ENCODER, actMC + 4.0 * m->maxT * C,
+       encoder_backward_wpe(m->at, pf(m, g, P_WPE), m->dres, B, T, C, m->maxT, s));
+    // read the gradient rows once and the ids; read-modify-write of the touched wte rows
+    OP(GPT2_K_ENCODER, actMC + 4.0 * M,
+       encoder_backward_wte(m->at, pf(m, g, P_WTE), m->dres, m->tok, (int)M, C, V, &m->enc, s));
     m->fwd_targets = false;
     m->have_grads = true;
     return GPT2_OK;
@@ -507,8 +592,46 @@ extern "C" int gpt2_update(gpt2_t* m, float lr, float b1, float b2, float eps, f
     if (t < 1) return fail(m, GPT2_ERR_ARG, "t must be >= 1 (got %d)", t);
     if (!m->have_grads) return fail(m, GPT2_ERR_STATE, "update needs gradients (run backward)");
     float c1 = 1.0f - powf(b1, (float)t), c2 = 1.0f - powf(b2, (float)t);
-    CK(adamw(m->params, m->grads, m->mom1, m->mom2, m->shadow, m->npad, lr, b1, b2, eps, wd, c1, c2,
+    // read p, g, m, v; write p, m, v (fp32) and the bf16 weight copy
+    double bytes = (double)m->npad * (28.0 + (m->shadow ? 2.0 : 0.0));
+    OP(GPT2_K_ADAMW, bytes,
+       adamw(m->params, m->grads, m->mom1, m->mom2, m->shadow, m->npad, lr, b1, b2, eps, wd, c1, c2,
              m->stream));
+    return GPT2_OK;
+}
+
+// ------------------------------------------------------------------ profiling
+extern "C" int gpt2_profile_enable(gpt2_t* m, int on) {
+    if (!m) return GPT2_ERR_ARG;
+    m->prof_on = on != 0;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_profile_reset(gpt2_t* m) {
+    if (!m) return GPT2_ERR_ARG;
+    CK(cudaStreamSynchronize(m->stream));
+    m->ev_used = 0;
+    for (int k = 0; k < GPT2_K_COUNT; k++) {
+        m->prof_ms[k] = m->prof_work[k] = 0;
+        m->prof_calls[k] = 0;
+    }
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_profile_read(gpt2_t* m, int cls, double* ms, double* work, uint64_t* calls) {
+    if (!m || cls < 0 || cls >= GPT2_K_COUNT) return fail(m, GPT2_ERR_ARG, "bad kernel class");
+    CK(cudaStreamSynchronize(m->stream));
+    for (size_t i = 0; i < m->ev_used; i++) {
+        float t = 0;
+        CK(cudaEventElapsedTime(&t, m->ev_a[i], m->ev_b[i]));
+        m->prof_ms[m->ev_cls[i]] += t;
+        m->prof_work[m->ev_cls[i]] += m->ev_work[i];
+        m->prof_calls[m->ev_cls[i]] += 1;
+    }
+    m->ev_used = 0;
+    if (ms) *ms = m->prof_ms[cls];
+    if (work) *work = m->prof_work[cls];
+    if (calls) *calls = m->prof_calls[cls];
     return GPT2_OK;
 }
 

@@ -131,6 +131,21 @@ class GPT2:
     def sync(self):
         self._check(N.lib.gpt2_sync(self.h))
 
+    def profile_enable(self, on: bool = True):
+        self._check(N.lib.gpt2_profile_enable(self.h, 1 if on else 0))
+
+    def profile_reset(self):
+        self._check(N.lib.gpt2_profile_reset(self.h))
+
+    def profile_read(self) -> dict:
+        """{class: (ms, work, calls)} accumulated since the last reset."""
+        out = {}
+        for k, name in enumerate(N.KERNEL_CLASSES):
+            ms, work, calls = ct.c_double(), ct.c_double(), ct.c_uint64()
+            self._check(N.lib.gpt2_profile_read(self.h, k, ct.byref(ms), ct.byref(work), ct.byref(calls)))
+            out[name] = (ms.value, work.value, int(calls.value))
+        return out
+
     def kernel_launches(self) -> int:
         return int(N.lib.gpt2_kernel_launches(self.h))
 

@@ -132,6 +132,27 @@ int gpt2_get_logits(gpt2_t* m, float* host, size_t n);
  * may be NULL).  Synchronising. */
 int gpt2_get_ids(gpt2_t* m, int32_t* tokens_host, int32_t* targets_host, size_t n);
 
+/* Kernel classes of the step, for gpt2_profile_read. */
+enum gpt2_kernel_class {
+    GPT2_K_GEMM = 0,      /* all matrix products (forward, dgrad, wgrad): work = FLOPs */
+    GPT2_K_ATTN_FWD = 1,  /* causal attention forward: work = FLOPs (QK^T and PV, t2 <= t) */
+    GPT2_K_ATTN_BWD = 2,  /* attention backward: work = 2x the forward FLOPs */
+    GPT2_K_LAYERNORM = 3, /* layernorm forward and backward: work = bytes */
+    GPT2_K_XENT = 4,      /* fused softmax + cross-entropy and the loss mean: work = bytes */
+    GPT2_K_ADAMW = 5,     /* AdamW over the flat buffer: work = bytes */
+    GPT2_K_ENCODER = 6,   /* embedding forward and backward, id checks: work = bytes */
+    GPT2_K_BIAS_GRAD = 7, /* bias-gradient column sums: work = bytes */
+    GPT2_K_COUNT = 8
+};
+/* Per-class timing.  While enabled, every op the handle queues is bracketed by a CUDA
+ * event pair on the handle's stream and its algorithmic work (read-once/write-once
+ * bytes, or FLOPs) is booked to its class.  gpt2_profile_read synchronises, adds up
+ * all pairs recorded since the last read or reset into the class totals, and returns
+ * the totals (milliseconds, work units, number of ops).  Reset clears them. */
+int gpt2_profile_enable(gpt2_t* m, int on);
+int gpt2_profile_reset(gpt2_t* m);
+int gpt2_profile_read(gpt2_t* m, int kernel_class, double* ms, double* work, uint64_t* calls);
+
 /* Run subsequent work on `stream` (a cudaStream_t; NULL = legacy default stream). */
 int gpt2_set_stream(gpt2_t* m, void* stream);
 /* Wait for all queued work; returns a gpt2_status for any pending CUDA error. */

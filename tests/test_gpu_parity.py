@@ -86,8 +86,9 @@ def test_tiny_one_step(G, precision):
         lr = synth.WORKLOADS["tiny"]["lr"]
         well = np.abs(g) > 1e-3 * np.sqrt(np.mean(g * g))
         assert np.max(np.abs(d_got - d_ref)[well]) <= 1e-3 * lr
-        zero = g == 0
-        assert np.array_equal(r["params"][zero], r["init"][zero])
+        # |step| <= lr at t=1 with wd = 0, up to the fp32 rounding of the new parameter
+        slack = np.spacing(np.abs(r["init"]).astype(np.float32)).astype(np.float64)
+        assert np.all(np.abs(d_got) <= lr * (1 + 1e-6) + slack)
 
 
 def test_tiny_bf16_logits_close(G):
