@@ -50,6 +50,14 @@ SIGNATURES = {
     "gpt2_last_build_error": (ct.c_char_p, []),
     "gpt2_kernel_launches": (U64, [P]),
     "gpt2_device_bytes": (SZ, [P]),
+    # include/gpt2_ops.h
+    "gpt2_op_last_error": (ct.c_char_p, []),
+    "gpt2_op_bias_grad_workspace": (SZ, [I, I]),
+    "gpt2_op_bias_grad": (I, [I, P, I, I, P, P, SZ, P]),
+    "gpt2_op_matmul": (I, [I, I, I, I, P, ct.c_longlong, I, P, ct.c_longlong, I, P, ct.c_longlong, I, P, P, SZ, P]),
+    "gpt2_op_adamw": (I, [P, P, P, P, P, SZ, F, F, F, F, F, I, P]),
+    "gpt2_op_attention_forward": (I, [I, P, P, P, I, I, I, I, P]),
+    "gpt2_op_attention_backward": (I, [I, P, P, P, P, P, I, I, I, I, P, P]),
 }
 
 for _name, (_res, _args) in SIGNATURES.items():
@@ -61,6 +69,7 @@ for _name, (_res, _args) in SIGNATURES.items():
 GPT2_OK, GPT2_ERR_ARG, GPT2_ERR_OOM, GPT2_ERR_CUDA = 0, -1, -2, -3
 GPT2_ERR_TOKEN, GPT2_ERR_SHAPE, GPT2_ERR_STATE, GPT2_ERR_NONFINITE, GPT2_ERR_TIMEOUT = -4, -5, -6, -7, -8
 GPT2_FP32, GPT2_BF16 = 0, 2
+GPT2_DT_F32, GPT2_DT_BF16 = 0, 1
 GPT2_HOST, GPT2_DEVICE = 0, 1
 KERNEL_CLASSES = ["gemm", "attn_fwd", "attn_bwd", "layernorm", "xent", "adamw", "encoder", "bias_grad"]
 

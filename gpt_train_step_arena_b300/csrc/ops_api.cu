@@ -1,0 +1,120 @@
+// C ABI of include/gpt2_ops.h: argument checks and one launcher call each.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/gpt2.h"
+#include "../../include/gpt2_ops.h"
+#include "dispatch.h"
+#include "kernels.h"
+
+using namespace g2;
+
+static std::mutex g_op_err_mu;
+static std::string g_op_err;
+
+static int op_fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    std::lock_guard<std::mutex> lk(g_op_err_mu);
+    g_op_err = buf;
+    return code;
+}
+
+static int op_cuda(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return GPT2_OK;
+    return op_fail(GPT2_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static bool dtype_ok(int dt) { return dt == GPT2_DT_F32 || dt == GPT2_DT_BF16; }
+static ActType act_of(int dt) { return dt == GPT2_DT_BF16 ? ACT_BF16 : ACT_F32; }
+
+extern "C" const char* gpt2_op_last_error(void) {
+    std::lock_guard<std::mutex> lk(g_op_err_mu);
+    return g_op_err.c_str();
+}
+
+extern "C" size_t gpt2_op_bias_grad_workspace(int M, int N) {
+    if (M < 0 || N <= 0) return 0;
+    return colsum_partial_floats(M, N) * sizeof(float);
+}
+
+extern "C" int gpt2_op_bias_grad(int dtype, const void* dout, int M, int N, float* dbias,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+    if (!dtype_ok(dtype)) return op_fail(GPT2_ERR_ARG, "bias_grad: bad dtype %d", dtype);
+    if (M < 0 || N <= 0) return op_fail(GPT2_ERR_ARG, "bias_grad: bad shape M=%d N=%d", M, N);
+    if (!dbias || (M > 0 && !dout)) return op_fail(GPT2_ERR_ARG, "bias_grad: null pointer");
+    size_t need = gpt2_op_bias_grad_workspace(M, N);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return op_fail(GPT2_ERR_ARG, "bias_grad: workspace of %zu bytes needed, %zu given", need,
+                       workspace_bytes);
+    return op_cuda(colsum(act_of(dtype), dbias, dout, M, N, (float*)workspace, (cudaStream_t)stream),
+                   "bias_grad");
+}
+
+extern "C" int gpt2_op_matmul(int dtype, int M, int N, int K, const void* A, long long lda,
+                              int a_kmajor, const void* B, long long ldb, int b_kmajor, void* D,
+                              long long ldd, int d_f32, const float* bias, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    if (!dtype_ok(dtype)) return op_fail(GPT2_ERR_ARG, "matmul: bad dtype %d", dtype);
+    if (M < 0 || N < 0 || K < 0) return op_fail(GPT2_ERR_ARG, "matmul: negative size");
+    if (M == 0 || N == 0) return GPT2_OK;
+    if (!A || !B || !D) return op_fail(GPT2_ERR_ARG, "matmul: null pointer");
+    GemmArgs a{};
+    a.M = M; a.N = N; a.K = K; a.in_type = act_of(dtype);
+    a.A = A;
+    if (a_kmajor) { a.sAm = lda; a.sAk = 1; } else { a.sAm = 1; a.sAk = lda; }
+    a.B = B;
+    if (b_kmajor) { a.sBn = ldb; a.sBk = 1; } else { a.sBn = 1; a.sBk = ldb; }
+    a.D = D; a.ldd = ldd; a.d_f32 = d_f32 ? 1 : 0;
+    a.bias = bias;
+    a.epi = EPI_STORE;
+    return op_cuda(gemm_dispatch(a, (float*)workspace, workspace ? workspace_bytes : 0,
+                                 (cudaStream_t)stream), "matmul");
+}
+
+extern "C" int gpt2_op_adamw(float* p, const float* g, float* m, float* v, void* shadow, size_t n,
+                             float lr, float b1, float b2, float eps, float wd, int t, void* stream) {
+    if (t < 1) return op_fail(GPT2_ERR_ARG, "adamw: t must be >= 1 (got %d)", t);
+    if (n && (!p || !g || !m || !v)) return op_fail(GPT2_ERR_ARG, "adamw: null pointer");
+    if ((((uintptr_t)p | (uintptr_t)g | (uintptr_t)m | (uintptr_t)v) & 15) != 0)
+        return op_fail(GPT2_ERR_ARG, "adamw: p, g, m, v must be 16-byte aligned");
+    float c1 = 1.0f - powf(b1, (float)t), c2 = 1.0f - powf(b2, (float)t);
+    return op_cuda(adamw(p, g, m, v, (bf16*)shadow, n, lr, b1, b2, eps, wd, c1, c2,
+                         (cudaStream_t)stream), "adamw");
+}
+
+extern "C" int gpt2_op_attention_forward(int dtype, void* out, float* lse, const void* qkv, int B,
+                                         int T, int C, int NH, void* stream) {
+    if (!dtype_ok(dtype)) return op_fail(GPT2_ERR_ARG, "attention: bad dtype %d", dtype);
+    if (B < 0 || T < 0 || C <= 0 || NH <= 0 || C % NH)
+        return op_fail(GPT2_ERR_ARG, "attention: bad shape");
+    if ((size_t)B * T == 0) return GPT2_OK;
+    if (!out || !lse || !qkv) return op_fail(GPT2_ERR_ARG, "attention: null pointer");
+    return op_cuda(attention_forward(act_of(dtype), out, lse, qkv, B, T, C, NH, (cudaStream_t)stream),
+                   "attention_forward");
+}
+
+extern "C" int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv,
+                                          const void* out, const float* lse, int B, int T, int C,
+                                          int NH, float* workspace, void* stream) {
+    if (!dtype_ok(dtype)) return op_fail(GPT2_ERR_ARG, "attention: bad dtype %d", dtype);
+    if (B < 0 || T < 0 || C <= 0 || NH <= 0 || C % NH)
+        return op_fail(GPT2_ERR_ARG, "attention: bad shape");
+    if ((size_t)B * T == 0) return GPT2_OK;
+    if (!dqkv || !dout || !qkv || !out || !lse || !workspace)
+        return op_fail(GPT2_ERR_ARG, "attention: null pointer");
+    return op_cuda(attention_backward(act_of(dtype), dqkv, dout, qkv, out, lse, B, T, C, NH, workspace,
+                                      (cudaStream_t)stream), "attention_backward");
+}
+
+// Sets the message returned by gpt2_op_last_error (for entry points in other files).
+void g2_op_set_error(const char* msg) {
+    std::lock_guard<std::mutex> lk(g_op_err_mu);
+    g_op_err = msg;
+}

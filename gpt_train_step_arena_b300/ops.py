@@ -1,0 +1,79 @@
+"""Per-operation calls of include/gpt2_ops.h on torch device tensors (marshalling only)."""
+from __future__ import annotations
+
+import torch
+
+from . import _native as N
+
+
+class OpError(RuntimeError):
+    pass
+
+
+def _check(rc):
+    if rc != N.GPT2_OK:
+        raise OpError(f"{N.STATUS_NAMES.get(rc, rc)}: {N.lib.gpt2_op_last_error().decode()}")
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return N.GPT2_DT_BF16
+    if t.dtype == torch.float32:
+        return N.GPT2_DT_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def bias_grad(dout: torch.Tensor) -> torch.Tensor:
+    M, Nn = dout.shape
+    out = torch.empty(Nn, dtype=torch.float32, device=dout.device)
+    ws_bytes = N.lib.gpt2_op_bias_grad_workspace(M, Nn)
+    ws = torch.empty(max(ws_bytes, 4), dtype=torch.uint8, device=dout.device)
+    _check(N.lib.gpt2_op_bias_grad(_dt(dout), dout.data_ptr(), M, Nn, out.data_ptr(), ws.data_ptr(),
+                                   ws.numel(), _stream()))
+    return out
+
+
+def matmul(A: torch.Tensor, B: torch.Tensor, a_kmajor=True, b_kmajor=True, out_f32=False,
+           bias=None, workspace_bytes: int = 64 << 20) -> torch.Tensor:
+    """D = A(m,k) B(n,k)^T.  A is (M,K) if a_kmajor else (K,M); B is (N,K) if b_kmajor else (K,N)."""
+    M, K = (A.shape if a_kmajor else A.shape[::-1])
+    Nn, K2 = (B.shape if b_kmajor else B.shape[::-1])
+    assert K == K2 and A.dtype == B.dtype
+    D = torch.empty(M, Nn, dtype=torch.float32 if out_f32 else A.dtype, device=A.device)
+    ws = torch.empty(workspace_bytes, dtype=torch.uint8, device=A.device) if workspace_bytes else None
+    _check(N.lib.gpt2_op_matmul(_dt(A), M, Nn, K, A.data_ptr(), A.stride(0), int(a_kmajor), B.data_ptr(),
+                                B.stride(0), int(b_kmajor), D.data_ptr(), D.stride(0), int(out_f32),
+                                None if bias is None else bias.data_ptr(),
+                                None if ws is None else ws.data_ptr(), workspace_bytes, _stream()))
+    return D
+
+
+def adamw(p, g, m, v, lr, b1, b2, eps, wd, t, shadow=None):
+    _check(N.lib.gpt2_op_adamw(p.data_ptr(), g.data_ptr(), m.data_ptr(), v.data_ptr(),
+                               None if shadow is None else shadow.data_ptr(), p.numel(), lr, b1, b2,
+                               eps, wd, t, _stream()))
+
+
+def attention_forward(qkv: torch.Tensor, NH: int):
+    B, T, C3 = qkv.shape
+    C = C3 // 3
+    out = torch.empty(B, T, C, dtype=qkv.dtype, device=qkv.device)
+    lse = torch.empty(B, NH, T, dtype=torch.float32, device=qkv.device)
+    _check(N.lib.gpt2_op_attention_forward(_dt(qkv), out.data_ptr(), lse.data_ptr(), qkv.data_ptr(),
+                                           B, T, C, NH, _stream()))
+    return out, lse
+
+
+def attention_backward(dout, qkv, out, lse, NH: int):
+    B, T, C3 = qkv.shape
+    C = C3 // 3
+    dqkv = torch.empty_like(qkv)
+    ws = torch.empty(B * NH * T, dtype=torch.float32, device=qkv.device)
+    _check(N.lib.gpt2_op_attention_backward(_dt(qkv), dqkv.data_ptr(), dout.data_ptr(), qkv.data_ptr(),
+                                            out.data_ptr(), lse.data_ptr(), B, T, C, NH, ws.data_ptr(),
+                                            _stream()))
+    return dqkv

@@ -1,0 +1,75 @@
+/*
+ * gpt2_ops.h — single operations of the GPT-2 training step on caller-owned device
+ * memory.  These are the kernels the model in gpt2.h chains, exposed one by one so a
+ * caller (or a test) can run a step of the chain on its own buffers.
+ *
+ * Conventions:
+ *  - Every pointer argument is a device pointer unless its name ends in _host.
+ *    Arrays are dense row-major.  The caller owns all memory; nothing is allocated.
+ *  - `dtype` selects the element type of activation-like arrays: GPT2_DT_F32 (float)
+ *    or GPT2_DT_BF16 (bfloat16).  Parameters, gradients and statistics are fp32.
+ *  - Work is queued on `stream` (a cudaStream_t; NULL = legacy default stream) and the
+ *    call returns without waiting.  The return value is a gpt2_status (gpt2.h);
+ *    gpt2_op_last_error() describes the last failure of any gpt2_op_* call in the
+ *    process.
+ */
+#ifndef GPT2_B300_OPS_H
+#define GPT2_B300_OPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum gpt2_dtype { GPT2_DT_F32 = 0, GPT2_DT_BF16 = 1 };
+
+const char* gpt2_op_last_error(void);
+
+/* Bias gradient of a linear layer (llm.c annotated listing, §1.6 matmul_backward:
+ * dbias[o] accumulates dout[b,t,o] over all positions).  dbias[n] = sum over m of
+ * dout[m,n], for dout (M,N) of `dtype`; dbias (N) fp32 is overwritten.  The sum order is
+ * fixed by (M,N), so results are bitwise reproducible.  `workspace` must hold
+ * gpt2_op_bias_grad_workspace(M,N) bytes (GPT2_ERR_ARG if smaller); its contents on
+ * entry do not matter. */
+size_t gpt2_op_bias_grad_workspace(int M, int N);
+int gpt2_op_bias_grad(int dtype, const void* dout, int M, int N, float* dbias, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Matrix product (llm.c §1.5 matmul_forward, §1.6 matmul_backward):
+ *   D[m,n] = sum_k A(m,k) * B(n,k) (+ bias[n]),  0 <= m < M, 0 <= n < N, 0 <= k < K.
+ * A is stored K-major (A(m,k) at A[m*lda + k]) when a_kmajor != 0, else M-major
+ * (A(m,k) at A[k*lda + m]); likewise B with b_kmajor and ldb.  A and B are `dtype`;
+ * D (row stride ldd) is fp32 when d_f32 != 0, else `dtype`.  bias (N floats) may be
+ * NULL.  The three products of a linear layer map onto this as: forward
+ * (X . W^T: both K-major), input gradient (dY . W: A K-major, B N-major) and weight
+ * gradient (dY^T . X: both M/N-major, fp32 out).  `workspace` (may be NULL when
+ * workspace_bytes is 0) receives split-K partial sums when the kernel uses them. */
+int gpt2_op_matmul(int dtype, int M, int N, int K, const void* A, long long lda, int a_kmajor,
+                   const void* B, long long ldb, int b_kmajor, void* D, long long ldd, int d_f32,
+                   const float* bias, void* workspace, size_t workspace_bytes, void* stream);
+
+/* AdamW over n fp32 elements (llm.c §1.26 gpt2_update), in place on p, m, v; g is read.
+ * shadow_bf16 (n bfloat16, may be NULL) receives the rounded updated parameters.
+ * t >= 1 counts updates. */
+int gpt2_op_adamw(float* p, const float* g, float* m, float* v, void* shadow_bf16, size_t n,
+                  float lr, float b1, float b2, float eps, float wd, int t, void* stream);
+
+/* Causal multi-head attention forward (llm.c §1.7; picoGPT attention with its causal
+ * mask).  qkv (B,T,3C) holds query | key | value, head h at channels [h*hs,(h+1)*hs)
+ * of each, hs = C/NH.  out (B,T,C) is overwritten with softmax(q k^T / sqrt(hs)) v
+ * over keys t2 <= t; lse (B,NH,T) fp32 with each row's log-sum-exp of the scaled
+ * scores (kept for the backward instead of the (T,T) probabilities). */
+int gpt2_op_attention_forward(int dtype, void* out, float* lse, const void* qkv, int B, int T,
+                              int C, int NH, void* stream);
+/* Its backward (llm.c §1.8): dqkv (B,T,3C) is overwritten with the gradients of q, k
+ * and v given dout (B,T,C), the forward's qkv, out and lse.  workspace: B*NH*T floats. */
+int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv,
+                               const void* out, const float* lse, int B, int T, int C, int NH,
+                               float* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPT2_B300_OPS_H */

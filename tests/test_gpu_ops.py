@@ -1,0 +1,146 @@
+"""GPU parity of single operations (include/gpt2_ops.h) against the CPU oracle's layer
+functions on the same seeded inputs.  Shapes span several tiles and a ragged tail."""
+import numpy as np
+import pytest
+
+from oracle.oracle import Ops
+
+pytestmark = pytest.mark.gpu
+
+o64 = Ops("f64")
+o32 = Ops("f32")
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    assert torch.cuda.is_available()
+    return torch
+
+
+def _to(torch, a, dtype):
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda").to(dtype)
+
+
+def _np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+# ---------------------------------------------------------------- bias gradient
+@pytest.mark.parametrize("M,N", [(1000, 300), (32768 // 16, 3072), (1, 8), (0, 64), (257, 27)])
+def test_bias_grad(torch_cuda, M, N):
+    torch = torch_cuda
+    from gpt_train_step_arena_b300 import ops
+    rng = np.random.default_rng(M * 7 + N)
+    x = rng.normal(size=(M, N)).astype(np.float32)
+    want = x.astype(np.float64).sum(0) if M else np.zeros(N)
+    got = _np(ops.bias_grad(_to(torch, x, torch.float32)))
+    assert np.allclose(got, want, rtol=1e-5, atol=1e-4 * max(1.0, np.sqrt(M)))
+    xb = _to(torch, x, torch.bfloat16)
+    want_b = _np(xb).sum(0) if M else np.zeros(N)
+    got_b = _np(ops.bias_grad(xb))
+    assert np.allclose(got_b, want_b, rtol=1e-5, atol=1e-4 * max(1.0, np.sqrt(M)))
+    assert np.array_equal(got_b, _np(ops.bias_grad(xb)))  # fixed summation order
+
+
+# ---------------------------------------------------------------- matmul
+SHAPES = [(300, 200, 104), (256, 256, 128), (128, 768, 768), (1, 8, 16), (129, 136, 72), (512, 2304, 768)]
+
+
+def _ref_mm(A, B):
+    return A.astype(np.float64) @ B.astype(np.float64).T
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("layout", ["fwd", "dgrad", "wgrad"])
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+def test_matmul_layouts(torch_cuda, M, N, K, layout, dt):
+    torch = torch_cuda
+    from gpt_train_step_arena_b300 import ops
+    rng = np.random.default_rng(M + 3 * N + 7 * K)
+    A = rng.normal(size=(M, K)).astype(np.float32)
+    B = rng.normal(size=(N, K)).astype(np.float32)
+    tdt = torch.float32 if dt == "fp32" else torch.bfloat16
+    Ad, Bd = _to(torch, A, tdt), _to(torch, B, tdt)
+    A_eff, B_eff = _np(Ad), _np(Bd)  # the values the kernel sees
+    if layout == "fwd":        # X . W^T: both K-major
+        D = ops.matmul(Ad, Bd, True, True)
+    elif layout == "dgrad":    # dY . W: A K-major, B stored (K, N)
+        D = ops.matmul(Ad, Bd.t().contiguous(), True, False)
+    else:                      # dY^T . X: A stored (K, M), B stored (K, N), fp32 out
+        D = ops.matmul(Ad.t().contiguous(), Bd.t().contiguous(), False, False, out_f32=True)
+    want = _ref_mm(A_eff, B_eff)
+    got = _np(D)
+    # fp32 accumulation over K terms; bf16 output adds one rounding (2^-9 relative)
+    out_bf16 = dt == "bf16" and layout != "wgrad"
+    tol = 8e-3 if out_bf16 else 1e-5
+    assert _rel(got, want) <= tol, _rel(got, want)
+
+
+def test_matmul_bias(torch_cuda):
+    torch = torch_cuda
+    from gpt_train_step_arena_b300 import ops
+    rng = np.random.default_rng(1)
+    A = rng.normal(size=(200, 64)).astype(np.float32)
+    B = rng.normal(size=(96, 64)).astype(np.float32)
+    b = rng.normal(size=96).astype(np.float32)
+    D = ops.matmul(_to(torch, A, torch.float32), _to(torch, B, torch.float32), bias=_to(torch, b, torch.float32))
+    assert _rel(_np(D), _ref_mm(A, B) + b) <= 1e-5
+
+
+# ---------------------------------------------------------------- AdamW
+def test_adamw_matches_float_oracle_to_ulp(torch_cuda):
+    torch = torch_cuda
+    from gpt_train_step_arena_b300 import ops
+    n = 1_000_003  # not a multiple of 4: exercises the scalar tail
+    rng = np.random.default_rng(2)
+    p = rng.normal(size=n).astype(np.float32)
+    g = (rng.normal(size=n) * 1e-2).astype(np.float32)
+    m = (rng.normal(size=n) * 1e-3).astype(np.float32)
+    v = np.abs(rng.normal(size=n) * 1e-5).astype(np.float32)
+    hp = (6e-4, 0.9, 0.999, 1e-8, 0.1, 7)
+    pd, gd, md, vd = (_to(torch, a, torch.float32) for a in (p, g, m, v))
+    sh = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    ops.adamw(pd, gd, md, vd, *hp, shadow=sh)
+    rp, rm, rv = o32.adamw(p, g, m, v, *hp)
+    got = pd.cpu().numpy()
+    # p' = p - lr*u: each side rounds p' once (half an ulp of p') and u's few operations
+    # (a few ulps of lr*|u| = |p - p'|); fused multiply-adds may differ between the sides.
+    step = np.abs(p.astype(np.float64) - rp)
+    assert np.all(np.abs(got - rp) <= 2.0 ** -22 * (np.abs(rp) + 4 * step) + 1e-30)
+    assert np.all(np.abs(md.cpu().numpy() - rm) <= 2.0 ** -22 * np.abs(rm) + 1e-20)
+    assert np.all(np.abs(vd.cpu().numpy() - rv) <= 2.0 ** -22 * np.abs(rv) + 1e-24)
+    assert torch.equal(sh, pd.to(torch.bfloat16))
+
+
+# ---------------------------------------------------------------- attention
+@pytest.mark.parametrize("B,T,C,NH", [(2, 77, 64, 4), (1, 1, 32, 2), (2, 130, 128, 2), (1, 256, 768, 12)])
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+def test_attention_fwd_bwd(torch_cuda, B, T, C, NH, dt):
+    torch = torch_cuda
+    from gpt_train_step_arena_b300 import ops
+    rng = np.random.default_rng(B * 1000 + T)
+    qkv = rng.normal(size=(B, T, 3 * C)).astype(np.float32)
+    dy = rng.normal(size=(B, T, C)).astype(np.float32)
+    tdt = torch.float32 if dt == "fp32" else torch.bfloat16
+    qd, dyd = _to(torch, qkv, tdt), _to(torch, dy, tdt)
+    out, lse = ops.attention_forward(qd, NH)
+    dq = ops.attention_backward(dyd, qd, out, lse, NH)
+    q_eff, dy_eff = _np(qd), _np(dyd)
+    ref_out, _, ref_att = o64.attention(q_eff, NH)
+    ref_dq = o64.attention_backward(dy_eff, q_eff, ref_att, NH)
+    tol_o, tol_g = (1e-5, 1e-4) if dt == "fp32" else (1e-2, 3e-2)
+    assert _rel(_np(out), ref_out) <= tol_o
+    assert _rel(_np(dq), ref_dq) <= tol_g
+    # lse: log of the softmax normaliser of the scaled scores
+    hs = C // NH
+    q = q_eff[..., :C].reshape(B, T, NH, hs).transpose(0, 2, 1, 3)
+    k = q_eff[..., C:2 * C].reshape(B, T, NH, hs).transpose(0, 2, 1, 3)
+    s = q @ k.transpose(0, 1, 3, 2) / np.sqrt(hs) + (1 - np.tri(T)) * -1e30
+    mx = s.max(-1, keepdims=True)
+    ref_lse = (mx + np.log(np.exp(s - mx).sum(-1, keepdims=True)))[..., 0]
+    assert np.max(np.abs(_np(lse) - ref_lse)) <= (1e-4 if dt == "fp32" else 2e-2)
