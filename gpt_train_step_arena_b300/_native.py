@@ -54,6 +54,8 @@ SIGNATURES = {
     "gpt2_op_last_error": (ct.c_char_p, []),
     "gpt2_op_bias_grad_workspace": (SZ, [I, I]),
     "gpt2_op_bias_grad": (I, [I, P, I, I, P, P, SZ, P]),
+    "gpt2_op_bias_grad_noalloc": (I, [I, P, I, I, P, P]),
+    "gpt2_op_bias_grad_noalloc_max_floats": (SZ, []),
     "gpt2_op_matmul": (I, [I, I, I, I, P, ct.c_longlong, I, P, ct.c_longlong, I, P, ct.c_longlong, I, P, P, SZ, P]),
     "gpt2_op_adamw": (I, [P, P, P, P, P, SZ, F, F, F, F, F, I, P]),
     "gpt2_op_attention_forward": (I, [I, P, P, P, I, I, I, I, P]),

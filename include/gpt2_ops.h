@@ -37,6 +37,23 @@ size_t gpt2_op_bias_grad_workspace(int M, int N);
 int gpt2_op_bias_grad(int dtype, const void* dout, int M, int N, float* dbias, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/* Bias gradient without a caller workspace.  The paper has no counterpart: this is an
+ * interface for callers that cannot allocate device memory, for example a plugin
+ * running inside a host framework whose caching allocator already holds the device's
+ * memory, or a deployment that forbids device allocation after start-up.  Same result
+ * as gpt2_op_bias_grad (same kernels, same summation order), but the partial sums live
+ * in a fixed array inside the library: 2^20 floats (4 MiB), which every device that
+ * loads the library keeps until the process exits.  It requires ceil(M/256) * N <=
+ * gpt2_op_bias_grad_noalloc_max_floats() and returns GPT2_ERR_ARG (with a message in
+ * gpt2_op_last_error) beyond that.  It allocates nothing.  The first call on a device
+ * looks up the array's device address with that device current; make that first call
+ * before any stream capture.  All calls share the one array: calls whose work overlaps
+ * on the GPU (different streams, or different host threads) race on it and must be
+ * serialised by the caller. */
+int gpt2_op_bias_grad_noalloc(int dtype, const void* dout, int M, int N, float* dbias,
+                              void* stream);
+size_t gpt2_op_bias_grad_noalloc_max_floats(void);
+
 /* Matrix product (llm.c §1.5 matmul_forward, §1.6 matmul_backward):
  *   D[m,n] = sum_k A(m,k) * B(n,k) (+ bias[n]),  0 <= m < M, 0 <= n < N, 0 <= k < K.
  * A is stored K-major (A(m,k) at A[m*lda + k]) when a_kmajor != 0, else M-major
