@@ -1,11 +1,22 @@
 // Kernel selection for GEMM and attention.
 #include "dispatch.h"
 
+#include <algorithm>
+
+#include "gemm_tc.h"
+
 namespace g2 {
 
-size_t gemm_workspace_bytes(int, int, int, int) { return 256; }
+// The largest split-K workspace of the weight-gradient products of one model.
+size_t gemm_workspace_bytes(int M, int C, int Vp, int) {
+    size_t b = 256;
+    const int shapes[][2] = {{3 * C, C}, {C, C}, {4 * C, C}, {C, 4 * C}, {Vp, C}};
+    for (auto& sh : shapes) b = std::max(b, gemm_tc_workspace_bytes(sh[0], sh[1], M));
+    return b;
+}
 
-cudaError_t gemm_dispatch(const GemmArgs& a, float*, size_t, cudaStream_t s) {
+cudaError_t gemm_dispatch(const GemmArgs& a, float* ws, size_t ws_bytes, cudaStream_t s) {
+    if (gemm_tc_supported(a)) return gemm_tc(a, ws, ws_bytes, a.flags, s);
     return gemm_simt(a, s);
 }
 

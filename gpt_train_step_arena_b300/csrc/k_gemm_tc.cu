@@ -1,0 +1,686 @@
+// Tensor-core GEMM for sm_103a: D = epi(A . B^T) with bf16 operands and fp32
+// accumulation in tensor memory (tcgen05), operands staged by TMA.
+//
+// The three products of a linear layer (llm.c annotated listing §1.5 matmul_forward,
+// §1.6 matmul_backward) all run here:
+//   forward  X.W^T   A K-major, B K-major      (+bias, +residual, or GELU epilogue)
+//   dgrad    dY.W    A K-major, B N-major      (optionally times GELU'(pre-activation))
+//   wgrad    dY^T.X  A M-major, B N-major      (fp32 out; split-K with a fixed-order sum)
+//
+// Structure (one persistent CTA per SM, 192 threads):
+//   warp 0    TMA producer: one elected lane streams 128 x 64 (A) and BN x 64 (B)
+//             bf16 tiles into a ring of shared-memory stages (128-byte swizzle).
+//   warp 1    allocates tensor memory; one lane issues tcgen05.mma (M=128, N=BN, K=16)
+//             into one of two fp32 accumulators (2 x BN columns) and commits to
+//             mbarriers that free the stage / publish the accumulator.
+//   warps 2-5 epilogue: tcgen05.ld of their 32 accumulator lanes, fused epilogue
+//             math, bf16/fp32 stores; then release the accumulator.
+// The two accumulators let the epilogue of one tile overlap the main loop of the
+// next.  Every mbarrier wait is bounded (about 2 s): on expiry the kernel raises a
+// flag, drains what it issued and returns instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm_tc.h"
+
+namespace g2 {
+namespace tc {
+
+constexpr int BM = 128, BK = 64, UMMA_K = 16;
+constexpr int NTHREADS = 192;
+constexpr int GROUP_M = 16;  // tile order: m fastest within groups of GROUP_M row tiles
+constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
+
+enum { E_STORE = 0, E_GELU = 1, E_GELU_BWD = 2, E_PARTIAL = 3 };
+
+struct Params {
+    int M, N, K;
+    int tiles_m, tiles_n, splits, kb_per_split, num_kb, num_units;
+    void* D;
+    long long ldd;
+    int d_f32;
+    const float* bias;
+    const bf16* R;
+    long long ldr;
+    bf16* D2;
+    long long ldd2;
+    const bf16* P;
+    long long ldp;
+    float* ws;  // split-K partials: [splits][M][N] fp32
+    int* flags;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+G2_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+G2_DEV unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+G2_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+G2_DEV void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+G2_DEV void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+G2_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait on phase `parity`.  Returns false (and raises the CTA-wide abort and
+// the global timeout flag) if it does not complete within TIMEOUT_NS, or if another
+// role of the CTA has already aborted.
+G2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* flags) {
+    if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 64; i++)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > TIMEOUT_NS) {
+            *abort_flag = 1;
+            if (flags) atomicOr(flags, G2_FLAG_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+G2_DEV void tma_load_2d(const CUtensorMap* tm, uint64_t* bar, void* dst, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            smem_u32(dst)),
+        "l"((uint64_t)tm), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+G2_DEV void tma_prefetch_desc(const CUtensorMap* tm) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tm) : "memory");
+}
+
+G2_DEV void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+G2_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+G2_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+G2_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+G2_DEV void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+G2_DEV void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's accumulator lane.
+G2_DEV void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, Blackwell descriptor version 1.
+G2_DEV uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo & 0x3FFFFu) >> 4) << 16;
+    d |= (uint64_t)((sbo & 0x3FFFFu) >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, operand majors,
+// N and M.
+__host__ __device__ constexpr uint32_t make_idesc(int bn, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+template <int BN>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+G2_DEV void unit_coords(const Params& p, int u, int& m_blk, int& n_blk, int& split) {
+    int per = p.tiles_m * p.tiles_n;
+    split = u / per;
+    int t = u % per;
+    int group_size = GROUP_M * p.tiles_n;
+    int group = t / group_size;
+    int first_m = group * GROUP_M;
+    int gsz = min(p.tiles_m - first_m, GROUP_M);
+    int r = t % group_size;
+    m_blk = first_m + r % gsz;
+    n_blk = r / gsz;
+}
+
+// ------------------------------------------------------------------ epilogue
+template <int EPI>
+G2_DEV void epilogue_chunk(const Params& p, const float* acc, int gm, int gn0, int split) {
+    const int N = p.N;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = acc[i];
+    const bool full = gn0 + 32 <= N;
+    if (EPI == E_PARTIAL) {
+        float* dst = p.ws + ((size_t)split * p.M + gm) * N + gn0;
+        if (full && (N & 3) == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+            for (int i = 0; i < 32; i++)
+                if (gn0 + i < N) dst[i] = v[i];
+        }
+        return;
+    }
+    if (EPI == E_GELU_BWD) {
+        const bf16* pre = p.P + (size_t)gm * p.ldp + gn0;
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                float x[8];
+                Vec8<bf16>::load(pre + i, x);
+#pragma unroll
+                for (int j = 0; j < 8; j++) v[i + j] *= gelu_tanh_grad(x[j]);
+            }
+        } else {
+            for (int i = 0; i < 32; i++)
+                if (gn0 + i < N) v[i] *= gelu_tanh_grad(__bfloat162float(pre[i]));
+        }
+    } else {
+        if (p.bias) {
+            if (full) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    float4 b = *reinterpret_cast<const float4*>(p.bias + gn0 + i);
+                    v[i] += b.x; v[i + 1] += b.y; v[i + 2] += b.z; v[i + 3] += b.w;
+                }
+            } else {
+                for (int i = 0; i < 32; i++)
+                    if (gn0 + i < N) v[i] += p.bias[gn0 + i];
+            }
+        }
+        if (p.R) {
+            const bf16* r = p.R + (size_t)gm * p.ldr + gn0;
+            if (full) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    float x[8];
+                    Vec8<bf16>::load(r + i, x);
+#pragma unroll
+                    for (int j = 0; j < 8; j++) v[i + j] += x[j];
+                }
+            } else {
+                for (int i = 0; i < 32; i++)
+                    if (gn0 + i < N) v[i] += __bfloat162float(r[i]);
+            }
+        }
+    }
+    if (p.d_f32) {
+        float* dst = (float*)p.D + (size_t)gm * p.ldd + gn0;
+        if (full && (p.ldd & 3) == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+            for (int i = 0; i < 32; i++)
+                if (gn0 + i < N) dst[i] = v[i];
+        }
+    } else {
+        bf16* dst = (bf16*)p.D + (size_t)gm * p.ldd + gn0;
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) Vec8<bf16>::store(dst + i, v + i);
+        } else {
+            for (int i = 0; i < 32; i++)
+                if (gn0 + i < N) dst[i] = __float2bfloat16_rn(v[i]);
+        }
+    }
+    if (EPI == E_GELU) {
+        float gv[32];
+#pragma unroll
+        for (int i = 0; i < 32; i++) gv[i] = gelu_tanh(v[i]);
+        bf16* dst = p.D2 + (size_t)gm * p.ldd2 + gn0;
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) Vec8<bf16>::store(dst + i, gv + i);
+        } else {
+            for (int i = 0; i < 32; i++)
+                if (gn0 + i < N) dst[i] = __float2bfloat16_rn(gv[i]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int BN, bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const Params p) {
+    using CF = Cfg<BN>;
+    constexpr int S = CF::STAGES;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = (uint64_t*)(smem + S * CF::STAGE_BYTES);
+    uint64_t* full_bar = bars;            // [S]
+    uint64_t* empty_bar = bars + S;       // [S]
+    uint64_t* tfull_bar = bars + 2 * S;   // [2]
+    uint64_t* tempty_bar = bars + 2 * S + 2;  // [2]
+    uint64_t* drain_bar = bars + 2 * S + 4;   // [1]
+    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * S + 5);
+    __shared__ int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int i = 0; i < S; i++) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&tfull_bar[i], 1);
+            mbar_init(&tempty_bar[i], 4);
+        }
+        mbar_init(drain_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, CF::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    volatile int* abort_flag = &s_abort;
+
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued_phase[S];
+            for (int i = 0; i < S; i++) issued_phase[i] = -1;
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+                int mb, nb, sp;
+                unit_coords(p, u, mb, nb, sp);
+                int kb0 = sp * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+                for (int kb = kb0; kb < kb1; kb++) {
+                    if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, p.flags)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * CF::STAGE_BYTES;
+                    uint8_t* sb = sa + CF::A_BYTES;
+                    mbar_expect_tx(&full_bar[stage], CF::STAGE_BYTES);
+                    const int k0 = kb * BK;
+                    if (!A_MN) {
+                        tma_load_2d(&tmA, &full_bar[stage], sa, k0, mb * BM);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / 64; j++)
+                            tma_load_2d(&tmA, &full_bar[stage], sa + j * 64 * BK * 2, mb * BM + 64 * j, k0);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d(&tmB, &full_bar[stage], sb, k0, nb * BN);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; j++)
+                            tma_load_2d(&tmB, &full_bar[stage], sb + j * 64 * BK * 2, nb * BN + 64 * j, k0);
+                    }
+                    issued_phase[stage] = (int)phase;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                // drain: wait (bounded) for every load still in flight before returning
+                for (int i = 0; i < S; i++) {
+                    if (issued_phase[i] < 0) continue;
+                    unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(&full_bar[i], (uint32_t)issued_phase[i]) &&
+                           globaltimer() - t0 < TIMEOUT_NS) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = make_idesc(BN, A_MN, B_MN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            bool issued_any = false;
+            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+                int mb, nb, sp;
+                unit_coords(p, u, mb, nb, sp);
+                int kb0 = sp * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+                if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, abort_flag, p.flags)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = kb0; kb < kb1; kb++) {
+                    if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.flags)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * CF::STAGE_BYTES);
+                    const uint32_t sb = sa + CF::A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; k++) {
+                        uint64_t ad, bd;
+                        if (!A_MN)
+                            ad = sdesc(sa + k * UMMA_K * 2, 16, 1024);
+                        else
+                            ad = sdesc(sa + k * UMMA_K * 128, 64 * BK * 2, 1024);
+                        if (!B_MN)
+                            bd = sdesc(sb + k * UMMA_K * 2, 16, 1024);
+                        else
+                            bd = sdesc(sb + k * UMMA_K * 128, 64 * BK * 2, 1024);
+                        umma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                    }
+                    issued_any = true;
+                    umma_commit(&empty_bar[stage]);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&tfull_bar[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+            if (!ok && issued_any) {
+                // drain: all MMAs issued so far complete before this commit arrives
+                umma_commit(drain_bar);
+                unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue warps 2..5
+        const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+        const int row_in_tile = quarter * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            int mb, nb, sp;
+            unit_coords(p, u, mb, nb, sp);
+            bool ok = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.flags);
+            if (!__all_sync(0xffffffffu, ok)) break;  // the warp leaves together
+            tc_fence_after();
+            const int gm = mb * BM + row_in_tile;
+            const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                tmem_ld32(trow + c0, v);
+                const int gn0 = nb * BN + c0;
+                if (gm < p.M && gn0 < p.N) epilogue_chunk<EPI>(p, v, gm, gn0, sp);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, CF::TMEM_COLS);
+}
+
+// Fixed-order sum of the split-K partials: out[i] = sum_s ws[s][i].
+__global__ void splitk_reduce_k(float* out, long long ldo, const float* ws, int M, int N, int splits) {
+    size_t n = (size_t)M * N;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        float a = 0.f;
+        for (int s = 0; s < splits; s++) a += ws[(size_t)s * n + i];
+        int m = (int)(i / N), c = (int)(i % N);
+        out[(size_t)m * ldo + c] = a;
+    }
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    });
+    return fn;
+}
+
+// bf16 2-D map: `inner` contiguous elements per row, `outer` rows `ld` elements apart.
+static bool make_map(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                     uint32_t box_inner, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static int num_sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+template <int BN, bool A_MN, bool B_MN, int EPI>
+static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, cudaStream_t s) {
+    auto kern = gemm_tc_kernel<BN, A_MN, B_MN, EPI>;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    int grid = std::min(p.num_units, num_sms());
+    G2_LAUNCH kern<<<grid, NTHREADS, Cfg<BN>::SMEM_BYTES, s>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+template <int BN, int EPI>
+static cudaError_t launch_layout(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+                                 const Params& p, cudaStream_t s) {
+    if (!a_mn && !b_mn) return launch_t<BN, false, false, EPI>(ta, tb, p, s);
+    if (!a_mn && b_mn) return launch_t<BN, false, true, EPI>(ta, tb, p, s);
+    if (a_mn && b_mn) return launch_t<BN, true, true, EPI>(ta, tb, p, s);
+    return launch_t<BN, true, false, EPI>(ta, tb, p, s);
+}
+
+}  // namespace tc
+
+using namespace tc;
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+// Timeout flag used when the caller passes none.
+__device__ int g_gemm_tc_timeout_flag;
+static int* fallback_flag() {
+    static int* ptr = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_gemm_tc_timeout_flag) == cudaSuccess) ptr = (int*)p;
+    });
+    return ptr;
+}
+
+// Split-K plan for a product with few output tiles and a long K.
+static void plan(int M, int N, int K, int BN, int& splits, int& kb_per) {
+    int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    int num_kb = (K + BK - 1) / BK;
+    int sms = num_sms();
+    splits = 1;
+    if (tiles < sms && num_kb >= 8) {
+        splits = std::min(std::max(1, (2 * sms) / tiles), num_kb / 4);
+        splits = std::max(splits, 1);
+    }
+    kb_per = (num_kb + splits - 1) / splits;
+    splits = (num_kb + kb_per - 1) / kb_per;
+}
+
+size_t gemm_tc_workspace_bytes(int M, int N, int K) {
+    int BN = N > 128 ? 256 : 128, splits, kb_per;
+    plan(M, N, K, BN, splits, kb_per);
+    return splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+}
+
+bool gemm_tc_supported(const GemmArgs& a) {
+    if (a.in_type != ACT_BF16 || !encode_fn()) return false;
+    if (a.M < 1 || a.N < 1 || a.K < 16) return false;
+    bool a_k = a.sAk == 1, b_k = a.sBk == 1;
+    long long lda = a_k ? a.sAm : a.sAk, ldb = b_k ? a.sBn : a.sBk;
+    if (!a_k && a.sAm != 1) return false;
+    if (!b_k && a.sBn != 1) return false;
+    if ((lda % 8) || (ldb % 8) || !aligned16(a.A) || !aligned16(a.B)) return false;
+    // inner extents of the tensor maps must reach one 128-byte swizzle row
+    if (a_k ? a.K < 64 : a.M < 64) return false;
+    if (b_k ? a.K < 64 : a.N < 64) return false;
+    if (!aligned16(a.D) || (a.ldd % 8)) return false;
+    if (a.epi == EPI_GELU && (!a.D2 || (a.ldd2 % 8) || !aligned16(a.D2))) return false;
+    if (a.epi == EPI_GELU_BWD && (!a.P || (a.ldp % 8) || !aligned16(a.P))) return false;
+    if (a.R && ((a.ldr % 8) || !aligned16(a.R))) return false;
+    if (a.bias && !aligned16(a.bias)) return false;
+    return true;
+}
+
+cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, cudaStream_t s) {
+    const bool a_mn = a.sAk != 1, b_mn = a.sBk != 1;
+    const int BN = a.N > 128 ? 256 : 128;
+    CUtensorMap ta, tb;
+    bool ok;
+    if (!a_mn)
+        ok = make_map(&ta, a.A, a.K, a.M, a.sAm, BK, BM);
+    else
+        ok = make_map(&ta, a.A, a.M, a.K, a.sAk, 64, BK);
+    if (!ok) return cudaErrorInvalidValue;
+    if (!b_mn)
+        ok = make_map(&tb, a.B, a.K, a.N, a.sBn, BK, BN);
+    else
+        ok = make_map(&tb, a.B, a.N, a.K, a.sBk, 64, BK);
+    if (!ok) return cudaErrorInvalidValue;
+
+    Params p{};
+    p.M = a.M; p.N = a.N; p.K = a.K;
+    p.tiles_m = (a.M + BM - 1) / BM;
+    p.tiles_n = (a.N + BN - 1) / BN;
+    p.num_kb = (a.K + BK - 1) / BK;
+    int splits = 1, kb_per = p.num_kb;
+    if (a.epi == EPI_STORE && a.d_f32 && !a.bias && !a.R) plan(a.M, a.N, a.K, BN, splits, kb_per);
+    if (splits > 1 && (!ws || ws_bytes < (size_t)splits * a.M * a.N * sizeof(float))) {
+        splits = 1;
+        kb_per = p.num_kb;
+    }
+    p.splits = splits;
+    p.kb_per_split = kb_per;
+    p.num_units = p.tiles_m * p.tiles_n * splits;
+    p.D = a.D; p.ldd = a.ldd; p.d_f32 = a.d_f32;
+    p.bias = a.bias;
+    p.R = (const bf16*)a.R; p.ldr = a.ldr;
+    p.D2 = (bf16*)a.D2; p.ldd2 = a.ldd2;
+    p.P = (const bf16*)a.P; p.ldp = a.ldp;
+    p.ws = ws;
+    p.flags = flags ? flags : fallback_flag();
+
+    cudaError_t e;
+    if (splits > 1) {
+        e = BN == 256 ? launch_layout<256, E_PARTIAL>(a_mn, b_mn, ta, tb, p, s)
+                      : launch_layout<128, E_PARTIAL>(a_mn, b_mn, ta, tb, p, s);
+        if (e != cudaSuccess) return e;
+        size_t n = (size_t)a.M * a.N;
+        unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
+        G2_LAUNCH splitk_reduce_k<<<blocks, 256, 0, s>>>((float*)a.D, a.ldd, ws, a.M, a.N, splits);
+        return cudaGetLastError();
+    }
+    switch (a.epi) {
+        case EPI_GELU:
+            return BN == 256 ? launch_layout<256, E_GELU>(a_mn, b_mn, ta, tb, p, s)
+                             : launch_layout<128, E_GELU>(a_mn, b_mn, ta, tb, p, s);
+        case EPI_GELU_BWD:
+            return BN == 256 ? launch_layout<256, E_GELU_BWD>(a_mn, b_mn, ta, tb, p, s)
+                             : launch_layout<128, E_GELU_BWD>(a_mn, b_mn, ta, tb, p, s);
+        default:
+            return BN == 256 ? launch_layout<256, E_STORE>(a_mn, b_mn, ta, tb, p, s)
+                             : launch_layout<128, E_STORE>(a_mn, b_mn, ta, tb, p, s);
+    }
+}
+
+}  // namespace g2

@@ -97,6 +97,7 @@ struct GemmArgs {
     void* D2; long long ldd2;            // EPI_GELU second output (in_type)
     const void* P; long long ldp;        // EPI_GELU_BWD pre-activation (in_type)
     int epi;
+    int* flags;                 // device error flags (G2_FLAG_TIMEOUT), or null
 };
 cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t s);
 

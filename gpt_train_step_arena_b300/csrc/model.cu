@@ -148,6 +148,7 @@ static cudaError_t gemm_fwd(gpt2* m, int M, int N, int K, const void* X, const v
     a.bias = bias; a.R = R; a.ldr = N;
     a.D2 = Y2; a.ldd2 = N;
     a.epi = Y2 ? EPI_GELU : EPI_STORE;
+    a.flags = m->flags;
     return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
 }
 // dX[M,K] = dY[M,N] . W[N,K]  (optionally times gelu'(P))
@@ -160,6 +161,7 @@ static cudaError_t gemm_dgrad(gpt2* m, int M, int N, int K, const void* dY, cons
     a.D = dX; a.ldd = K; a.d_f32 = 0;
     a.P = P; a.ldp = K;
     a.epi = P ? EPI_GELU_BWD : EPI_STORE;
+    a.flags = m->flags;
     return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
 }
 // dW[N,K] (fp32, overwritten) = dY[M,N]^T . X[M,K]
@@ -170,6 +172,7 @@ static cudaError_t gemm_wgrad(gpt2* m, int M, int N, int K, const void* dY, cons
     a.B = X; a.sBn = 1; a.sBk = K;
     a.D = dW; a.ldd = K; a.d_f32 = 1;
     a.epi = EPI_STORE;
+    a.flags = m->flags;
     return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
 }
 
@@ -476,6 +479,8 @@ extern "C" int gpt2_read_loss(gpt2_t* m, float* out) {
     CK(cudaMemcpyAsync(hflags, m->flags, 4, cudaMemcpyDeviceToHost, m->stream));
     CK(cudaStreamSynchronize(m->stream));
     *out = loss;
+    if (hflags[0] & G2_FLAG_TIMEOUT)
+        return fail(m, GPT2_ERR_TIMEOUT, "a device-side wait gave up (kernel reported a timeout)");
     if (hflags[0] & G2_FLAG_BAD_TOKEN)
         return fail(m, GPT2_ERR_TOKEN, "an input id is outside [0, %d)", m->V);
     if (hflags[0] & G2_FLAG_BAD_TARGET)

@@ -112,7 +112,9 @@ def test_adamw_matches_float_oracle_to_ulp(torch_cuda):
     # (a few ulps of lr*|u| = |p - p'|); fused multiply-adds may differ between the sides.
     step = np.abs(p.astype(np.float64) - rp)
     assert np.all(np.abs(got - rp) <= 2.0 ** -22 * (np.abs(rp) + 4 * step) + 1e-30)
-    assert np.all(np.abs(md.cpu().numpy() - rm) <= 2.0 ** -22 * np.abs(rm) + 1e-20)
+    # m = b1*m + (1-b1)*g can cancel: its rounding error scales with the two terms
+    terms = 0.9 * np.abs(m.astype(np.float64)) + 0.1 * np.abs(g.astype(np.float64))
+    assert np.all(np.abs(md.cpu().numpy() - rm) <= 2.0 ** -22 * terms + 1e-30)
     assert np.all(np.abs(vd.cpu().numpy() - rv) <= 2.0 ** -22 * np.abs(rv) + 1e-24)
     assert torch.equal(sh, pd.to(torch.bfloat16))
 
