@@ -22,12 +22,15 @@ cudaError_t gemm_dispatch(const GemmArgs& a, float* ws, size_t ws_bytes, cudaStr
 
 cudaError_t attention_forward(ActType at, void* out, float* lse, const void* qkv, int B, int T,
                               int C, int NH, cudaStream_t s) {
+    if (attention_mma_supported(at, C, NH)) return attention_forward_mma(out, lse, qkv, B, T, C, NH, s);
     return attention_forward_simt(at, out, lse, qkv, B, T, C, NH, s);
 }
 
 cudaError_t attention_backward(ActType at, void* dqkv, const void* dout, const void* qkv,
                                const void* out, const float* lse, int B, int T, int C, int NH,
                                float* scratch_D, cudaStream_t s) {
+    if (attention_mma_supported(at, C, NH))
+        return attention_backward_mma(dqkv, dout, qkv, out, lse, B, T, C, NH, scratch_D, s);
     return attention_backward_simt(at, dqkv, dout, qkv, out, lse, B, T, C, NH, scratch_D, s);
 }
 

@@ -227,6 +227,17 @@ cudaError_t attention_forward_simt(ActType at, void* out, float* lse, const void
     return cudaGetLastError();
 }
 
+cudaError_t attention_bwd_dot(ActType at, float* D, const void* dout, const void* out, int B, int T,
+                              int C, int NH, cudaStream_t s) {
+    long long n = (long long)B * NH * T;
+    if (n <= 0) return cudaSuccess;
+    if (at == ACT_BF16)
+        G2_LAUNCH attn_bwd_dot_k<bf16><<<rows8(n), 256, 0, s>>>(D, (const bf16*)dout, (const bf16*)out, B, T, C, NH);
+    else
+        G2_LAUNCH attn_bwd_dot_k<float><<<rows8(n), 256, 0, s>>>(D, (const float*)dout, (const float*)out, B, T, C, NH);
+    return cudaGetLastError();
+}
+
 cudaError_t attention_backward_simt(ActType at, void* dqkv, const void* dout, const void* qkv,
                                     const void* out, const float* lse, int B, int T, int C, int NH,
                                     float* Dbuf, cudaStream_t s) {

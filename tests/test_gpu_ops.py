@@ -120,7 +120,8 @@ def test_adamw_matches_float_oracle_to_ulp(torch_cuda):
 
 
 # ---------------------------------------------------------------- attention
-@pytest.mark.parametrize("B,T,C,NH", [(2, 77, 64, 4), (1, 1, 32, 2), (2, 130, 128, 2), (1, 256, 768, 12)])
+@pytest.mark.parametrize("B,T,C,NH", [(2, 77, 64, 4), (1, 1, 32, 2), (2, 130, 128, 2), (1, 256, 768, 12),
+                                        (1, 1, 64, 1), (2, 64, 128, 2), (1, 200, 192, 3), (2, 1024, 64, 1)])
 @pytest.mark.parametrize("dt", ["fp32", "bf16"])
 def test_attention_fwd_bwd(torch_cuda, B, T, C, NH, dt):
     torch = torch_cuda
