@@ -374,11 +374,83 @@ cudaError_t layernorm_forward(ActType at, void* out, float* mean, float* rstd, c
 
 // ------------------------------------------------------------------ layernorm backward
 // llm.c §1.4.  One warp per row; dres += dinp (the residual-stream accumulation of
-// llm.c §1.12 fused in).  dw/db: each block sums its rows (warps in fixed order) into
-// part[block][C] and [block][C] of the second half; ln_bwd_final_k adds blocks in order.
-static const int LNB_BLOCKS = 296;  // fixed grid (2 x 148 SMs): fixes the sum order
+// llm.c §1.12 fused in).  dw/db: each warp sums its rows, the block adds its warps in
+// order into part[block][C] (dw) and part[nblk + block][C] (db); ln_bwd_final_k adds
+// the blocks in order.  The grid size is a constant, so the summation order depends on
+// the problem size only.
+static const int LNB_BLOCKS = 296;      // generic kernel: 8 warps per block
+static const int LNB_VEC_BLOCKS = 888;  // vector kernel: 4 warps per block (6 per SM)
 
-size_t ln_bwd_partial_floats(int C) { return (size_t)2 * LNB_BLOCKS * C; }
+size_t ln_bwd_partial_floats(int C) { return (size_t)2 * LNB_VEC_BLOCKS * C; }
+
+// C = 256 * NV: each lane owns 8 consecutive columns in each of NV 256-column slabs;
+// the row's dout and x stay in registers, the row sums are warp reductions.
+template <typename T, int NV>
+__global__ void __launch_bounds__(128) ln_bwd_vec_k(T* dres, float* part, const T* dout, const T* inp,
+                                                    const float* w, const float* mean,
+                                                    const float* rstd, int M, int C) {
+    __shared__ float sh[4][2][NV * 256];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float aw[NV][8], ab[NV][8];
+#pragma unroll
+    for (int j = 0; j < NV; j++)
+#pragma unroll
+        for (int i = 0; i < 8; i++) aw[j][i] = ab[j][i] = 0.f;
+    for (int row = blockIdx.x * 4 + warp; row < M; row += gridDim.x * 4) {
+        const T* d = dout + (size_t)row * C;
+        const T* x = inp + (size_t)row * C;
+        T* dr = dres + (size_t)row * C;
+        float dv[NV][8], xv[NV][8];
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            Vec8<T>::load(d + j * 256 + lane * 8, dv[j]);
+            Vec8<T>::load(x + j * 256 + lane * 8, xv[j]);
+        }
+        const float m = mean[row], r = rstd[row];
+        float gm = 0.f, gnm = 0.f;
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            const float4 w0 = *reinterpret_cast<const float4*>(w + j * 256 + lane * 8);
+            const float4 w1 = *reinterpret_cast<const float4*>(w + j * 256 + lane * 8 + 4);
+            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                float n = (xv[j][i] - m) * r;
+                xv[j][i] = n;                 // keep the normalised value
+                float g = wv[i] * dv[j][i];
+                gm += g;
+                gnm += g * n;
+                ab[j][i] += dv[j][i];
+                aw[j][i] += n * dv[j][i];
+                dv[j][i] = g;                 // keep w*dout
+            }
+        }
+        gm = warp_sum(gm) / C;
+        gnm = warp_sum(gnm) / C;
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            float o[8];
+            Vec8<T>::load(dr + j * 256 + lane * 8, o);
+#pragma unroll
+            for (int i = 0; i < 8; i++) o[i] += (dv[j][i] - gm - xv[j][i] * gnm) * r;
+            Vec8<T>::store(dr + j * 256 + lane * 8, o);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NV; j++)
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            sh[warp][0][j * 256 + lane * 8 + i] = aw[j][i];
+            sh[warp][1][j * 256 + lane * 8 + i] = ab[j][i];
+        }
+    __syncthreads();
+    float* pw = part + (size_t)blockIdx.x * C;
+    float* pb = part + (size_t)(gridDim.x + blockIdx.x) * C;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        pw[c] = ((sh[0][0][c] + sh[1][0][c]) + sh[2][0][c]) + sh[3][0][c];
+        pb[c] = ((sh[0][1][c] + sh[1][1][c]) + sh[2][1][c]) + sh[3][1][c];
+    }
+}
 
 template <typename T>
 __global__ void __launch_bounds__(256) ln_bwd_k(T* dres, float* part, const T* dout, const T* inp,
@@ -442,24 +514,38 @@ __global__ void ln_bwd_final_k(float* dw, float* db, const float* part, int nblk
     db[c] = b;
 }
 
+template <typename T>
+static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, const T* dout, const T* inp,
+                                 const float* w, const float* mean, const float* rstd, int M, int C,
+                                 float* part, cudaStream_t s) {
+    const int nv = (C % 256 == 0) ? C / 256 : 0;
+    if (nv >= 1 && nv <= 4) {
+        switch (nv) {
+            case 1: G2_LAUNCH ln_bwd_vec_k<T, 1><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, rstd, M, C); break;
+            case 2: G2_LAUNCH ln_bwd_vec_k<T, 2><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, rstd, M, C); break;
+            case 3: G2_LAUNCH ln_bwd_vec_k<T, 3><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, rstd, M, C); break;
+            default: G2_LAUNCH ln_bwd_vec_k<T, 4><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, rstd, M, C); break;
+        }
+        G2_LAUNCH ln_bwd_final_k<<<cdiv(C, 256), 256, 0, s>>>(dw, db, part, LNB_VEC_BLOCKS, C);
+        return cudaGetLastError();
+    }
+    size_t smem = (size_t)8 * 2 * C * sizeof(float);
+    if (smem > 200 * 1024) return cudaErrorInvalidValue;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(ln_bwd_k<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    G2_LAUNCH ln_bwd_k<T><<<LNB_BLOCKS, 256, smem, s>>>(dres, part, dout, inp, w, mean, rstd, M, C);
+    G2_LAUNCH ln_bwd_final_k<<<cdiv(C, 256), 256, 0, s>>>(dw, db, part, LNB_BLOCKS, C);
+    return cudaGetLastError();
+}
+
 cudaError_t layernorm_backward(ActType at, void* dres, float* dw, float* db, const void* dout,
                                const void* inp, const float* w, const float* mean,
                                const float* rstd, int M, int C, float* part, cudaStream_t s) {
-    size_t smem = (size_t)8 * 2 * C * sizeof(float);
-    if (smem > 200 * 1024) return cudaErrorInvalidValue;
-    if (at == ACT_BF16) {
-        if (smem > 48 * 1024)
-            cudaFuncSetAttribute(ln_bwd_k<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        G2_LAUNCH ln_bwd_k<bf16><<<LNB_BLOCKS, 256, smem, s>>>((bf16*)dres, part, (const bf16*)dout,
-                                                     (const bf16*)inp, w, mean, rstd, M, C);
-    } else {
-        if (smem > 48 * 1024)
-            cudaFuncSetAttribute(ln_bwd_k<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        G2_LAUNCH ln_bwd_k<float><<<LNB_BLOCKS, 256, smem, s>>>((float*)dres, part, (const float*)dout,
-                                                      (const float*)inp, w, mean, rstd, M, C);
-    }
-    G2_LAUNCH ln_bwd_final_k<<<cdiv(C, 256), 256, 0, s>>>(dw, db, part, LNB_BLOCKS, C);
-    return cudaGetLastError();
+    if (at == ACT_BF16)
+        return ln_bwd_launch<bf16>((bf16*)dres, dw, db, (const bf16*)dout, (const bf16*)inp, w, mean, rstd,
+                                   M, C, part, s);
+    return ln_bwd_launch<float>((float*)dres, dw, db, (const float*)dout, (const float*)inp, w, mean, rstd,
+                                M, C, part, s);
 }
 
 // ------------------------------------------------------------------ bias gradient
@@ -617,9 +703,122 @@ __global__ void __launch_bounds__(1024) softmax_xent_k(T* logits, float* losses,
     }
 }
 
+// bf16 rows held in registers: each of the 1024 threads keeps its NCH chunks of 8
+// columns (chunk tid + 1024 k) as packed bf16 (4 registers per chunk), so the row is
+// read from memory once and written once.  Each thread keeps a running max m_t and sum
+// of exp(x - m_t); one block reduction merges the (max, sum) pairs in a fixed tree.
+G2_DEV void merge_ms(float& m, float& s, float m2, float s2) {
+    float mn = fmaxf(m, m2);
+    if (mn == -INFINITY) return;  // both empty
+    s = s * expf(m - mn) + s2 * expf(m2 - mn);
+    m = mn;
+}
+
+template <int NCH>
+__global__ void __launch_bounds__(1024) softmax_xent_reg_k(bf16* logits, float* losses, const int32_t* targets,
+                                                           int V, int Vp, float dloss, int* flags) {
+    __shared__ float red_m[32], red_s[32];
+    __shared__ float bcast;
+    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    bf16* x = logits + (size_t)row * Vp;
+    const int tg = targets[row];
+    const bool ok = (unsigned)tg < (unsigned)V;
+    // the target column lives in chunk k_t of thread t_t, element e_t
+    const int t_t = (tg >> 3) & 1023, k_t = (tg >> 3) >> 10, e_t = tg & 7;
+    const bool own = ok && tid == t_t;
+    const float x_tg = own ? __bfloat162float(x[tg]) : 0.f;
+    uint4 raw[NCH];
+#pragma unroll
+    for (int k = 0; k < NCH; k++) {
+        const int c = (tid + k * 1024) * 8;
+        raw[k] = c < Vp ? *reinterpret_cast<const uint4*>(x + c) : make_uint4(0, 0, 0, 0);
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < NCH; k++) {
+        const int c = (tid + k * 1024) * 8;
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float2 v = __bfloat1622float2(h[i]);
+            m = fmaxf(m, c + 2 * i < V ? v.x : -INFINITY);
+            m = fmaxf(m, c + 2 * i + 1 < V ? v.y : -INFINITY);
+        }
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < NCH; k++) {
+        const int c = (tid + k * 1024) * 8;
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float2 v = __bfloat1622float2(h[i]);
+            sum += c + 2 * i < V ? expf(v.x - m) : 0.f;
+            sum += c + 2 * i + 1 < V ? expf(v.y - m) : 0.f;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+        merge_ms(m, sum, m2, s2);
+    }
+    if (lane == 0) {
+        red_m[warp] = m;
+        red_s[warp] = sum;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float mm = red_m[lane], ss = red_s[lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float m2 = __shfl_xor_sync(0xffffffffu, mm, o), s2 = __shfl_xor_sync(0xffffffffu, ss, o);
+            merge_ms(mm, ss, m2, s2);
+        }
+        if (lane == 0) bcast = mm + logf(ss);
+    }
+    __syncthreads();
+    const float lse = bcast;
+#pragma unroll
+    for (int k = 0; k < NCH; k++) {
+        const int c = (tid + k * 1024) * 8;
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+        uint4 outv;
+        __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&outv);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float2 v = __bfloat1622float2(h[i]);
+            float g0 = c + 2 * i < V ? expf(v.x - lse) * dloss : 0.f;
+            float g1 = c + 2 * i + 1 < V ? expf(v.y - lse) * dloss : 0.f;
+            if (own && k == k_t) {
+                g0 -= e_t == 2 * i ? dloss : 0.f;
+                g1 -= e_t == 2 * i + 1 ? dloss : 0.f;
+            }
+            oh[i] = __floats2bfloat162_rn(g0, g1);
+        }
+        if (c < Vp) *reinterpret_cast<uint4*>(x + c) = outv;
+    }
+    if (own) losses[row] = lse - x_tg;
+    if (tid == 0 && !ok) {
+        atomicOr(flags, G2_FLAG_BAD_TARGET);
+        losses[row] = 0.f;
+    }
+}
+
 cudaError_t softmax_xent(ActType at, void* logits, float* losses, const int32_t* targets, int M,
                          int V, int Vp, float dloss, int* flags, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
+    const int nch = (Vp % 8 == 0) ? (Vp / 8 + 1023) / 1024 : 0;
+    if (at == ACT_BF16 && nch >= 1 && nch <= 8) {
+#define G2_XENT_CASE(N)                                                                               \
+    case N:                                                                                           \
+        G2_LAUNCH softmax_xent_reg_k<N><<<M, 1024, 0, s>>>((bf16*)logits, losses, targets, V, Vp, dloss, flags); \
+        return cudaGetLastError();
+        switch (nch) {
+            G2_XENT_CASE(1) G2_XENT_CASE(2) G2_XENT_CASE(3) G2_XENT_CASE(4)
+            G2_XENT_CASE(5) G2_XENT_CASE(6) G2_XENT_CASE(7) G2_XENT_CASE(8)
+        }
+#undef G2_XENT_CASE
+    }
     if (at == ACT_BF16)
         G2_LAUNCH softmax_xent_k<bf16><<<M, 1024, 0, s>>>((bf16*)logits, losses, targets, V, Vp, dloss, flags);
     else

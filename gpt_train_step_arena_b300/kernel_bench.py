@@ -1,0 +1,100 @@
+"""Run one operation of the training step on its own, at the shapes of a GPT-2 workload.
+
+    python -m gpt_train_step_arena_b300.kernel_bench --op fc_fwd [--reps 20] [--workload gpt2_124m]
+
+Ops: the matrix products of a layer (qkv_fwd, attproj_fwd, fc_fwd, fcproj_fwd,
+lmhead_fwd, fc_dgrad, fc_wgrad, qkv_wgrad, lmhead_dgrad, lmhead_wgrad), attention
+(attn_fwd, attn_bwd) and AdamW over the full parameter count.  Inputs are seeded random
+device tensors; each op runs --reps times after --warmup runs, timed with CUDA events,
+and prints one JSON line (ms per run, TFLOP/s or GB/s).  Used for per-kernel timing and
+as the small, self-contained program that Nsight Compute captures.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import torch
+
+from . import ops, synth
+
+
+def _gemm_case(name, c):
+    M, C, Vp = c["B"] * c["T"], c["C"], (c["V"] + 127) // 128 * 128
+    shapes = {  # (M, N, K, layout)
+        "qkv_fwd": (M, 3 * C, C, "fwd"), "attproj_fwd": (M, C, C, "fwd"), "fc_fwd": (M, 4 * C, C, "fwd"),
+        "fcproj_fwd": (M, C, 4 * C, "fwd"), "lmhead_fwd": (M, Vp, C, "fwd"),
+        "fc_dgrad": (M, C, 4 * C, "dgrad"), "fcproj_dgrad": (M, 4 * C, C, "dgrad"),
+        "lmhead_dgrad": (M, C, Vp, "dgrad"),
+        "fc_wgrad": (4 * C, C, M, "wgrad"), "qkv_wgrad": (3 * C, C, M, "wgrad"),
+        "attproj_wgrad": (C, C, M, "wgrad"), "lmhead_wgrad": (Vp, C, M, "wgrad"),
+    }
+    return shapes[name]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--op", required=True)
+    ap.add_argument("--workload", default="gpt2_124m")
+    ap.add_argument("--batch", type=int, default=None, help="override B (smaller device footprint)")
+    ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    args = ap.parse_args()
+    c = dict(synth.WORKLOADS[args.workload])
+    if args.batch:
+        c["B"] = args.batch
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(0)
+    bf = torch.bfloat16
+
+    def rnd(*shape, dtype=bf):
+        return (torch.randn(*shape, device=dev, generator=g) * 0.5).to(dtype)
+
+    if args.op.startswith("attn"):
+        B, T, C, NH = c["B"], c["T"], c["C"], c["NH"]
+        qkv = rnd(B, T, 3 * C)
+        out, lse = ops.attention_forward(qkv, NH)
+        dout = rnd(B, T, C)
+        flops = 2.0 * B * NH * (C // NH) * T * (T + 1)
+        if args.op == "attn_fwd":
+            fn = lambda: ops.attention_forward(qkv, NH)
+        else:
+            fn = lambda: ops.attention_backward(dout, qkv, out, lse, NH)
+            flops *= 2
+        unit, work = "TFLOP/s", flops
+    elif args.op == "adamw":
+        n = sum(synth.param_sizes(c["L"], c["C"], (c["V"] + 127) // 128 * 128, c["maxT"]))
+        p, gr, m, v = (rnd(n, dtype=torch.float32) for _ in range(4))
+        v.abs_()
+        sh = torch.empty(n, dtype=bf, device=dev)
+        fn = lambda: ops.adamw(p, gr, m, v, 6e-4, 0.9, 0.999, 1e-8, 0.1, 1, shadow=sh)
+        unit, work = "GB/s", 30.0 * n
+    else:
+        M, N, K, layout = _gemm_case(args.op, c)
+        if layout == "fwd":
+            A, Bm = rnd(M, K), rnd(N, K)
+            fn = lambda: ops.matmul(A, Bm, True, True)
+        elif layout == "dgrad":
+            A, Bm = rnd(M, K), rnd(K, N)
+            fn = lambda: ops.matmul(A, Bm, True, False)
+        else:
+            A, Bm = rnd(K, M), rnd(K, N)
+            ws = 1 << 28
+            fn = lambda: ops.matmul(A, Bm, False, False, out_f32=True, workspace_bytes=ws)
+        unit, work = "TFLOP/s", 2.0 * M * N * K
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.reps
+    rate = work / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    print(json.dumps({"op": args.op, "workload": args.workload, "B": c["B"], "ms": ms, unit: rate}))
+
+
+if __name__ == "__main__":
+    main()
