@@ -60,6 +60,10 @@ SIGNATURES = {
     "gpt2_op_adamw": (I, [P, P, P, P, P, SZ, F, F, F, F, F, I, P]),
     "gpt2_op_attention_forward": (I, [I, P, P, P, I, I, I, I, P]),
     "gpt2_op_attention_backward": (I, [I, P, P, P, P, P, I, I, I, I, P, P]),
+    "gpt2_op_layernorm_forward": (I, [I, P, P, P, P, P, P, I, I, P]),
+    "gpt2_op_layernorm_backward_workspace": (SZ, [I]),
+    "gpt2_op_layernorm_backward": (I, [I, P, P, P, P, P, P, P, P, I, I, P, SZ, P]),
+    "gpt2_op_softmax_xent": (I, [I, P, P, P, I, I, I, F, P, P]),
 }
 
 for _name, (_res, _args) in SIGNATURES.items():

@@ -312,9 +312,11 @@ __global__ void ln_fwd_vec_k(T* out, float* mean, float* rstd, const T* inp, con
 #pragma unroll
     for (int j = 0; j < NV; j++) {
         int c = j * 256 + lane * 8;
-        float y[8];
+        float wv[8], bv[8], y[8];
+        Vec8<float>::load(w + c, wv);
+        Vec8<float>::load(b + c, bv);
 #pragma unroll
-        for (int i = 0; i < 8; i++) y[i] = (v[j][i] - m) * r * w[c + i] + b[c + i];
+        for (int i = 0; i < 8; i++) y[i] = (v[j][i] - m) * r * wv[i] + bv[i];
         Vec8<T>::store(o + c, y);
     }
     if (lane == 0) {
@@ -351,7 +353,8 @@ template <typename T>
 static void ln_fwd_launch(T* out, float* mean, float* rstd, const T* inp, const float* w,
                           const float* b, int M, int C, cudaStream_t s) {
     unsigned g = cdiv(M, 8);
-    switch (C % 256 == 0 ? C / 256 : 0) {
+    const bool aligned = (((uintptr_t)w | (uintptr_t)b) & 15) == 0;
+    switch (C % 256 == 0 && aligned ? C / 256 : 0) {
         case 1: count_launches(1); ln_fwd_vec_k<T, 1><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
         case 2: count_launches(1); ln_fwd_vec_k<T, 2><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
         case 3: count_launches(1); ln_fwd_vec_k<T, 3><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
@@ -375,11 +378,11 @@ cudaError_t layernorm_forward(ActType at, void* out, float* mean, float* rstd, c
 // ------------------------------------------------------------------ layernorm backward
 // llm.c §1.4.  One warp per row; dres += dinp (the residual-stream accumulation of
 // llm.c §1.12 fused in).  dw/db: each warp sums its rows, the block adds its warps in
-// order into part[block][C] (dw) and part[nblk + block][C] (db); ln_bwd_final_k adds
+// order into part[block][C] (dw) and part[nblk + block][C] (db); colreduce_k adds
 // the blocks in order.  The grid size is a constant, so the summation order depends on
 // the problem size only.
 static const int LNB_BLOCKS = 296;      // generic kernel: 8 warps per block
-static const int LNB_VEC_BLOCKS = 888;  // vector kernel: 4 warps per block (6 per SM)
+static const int LNB_VEC_BLOCKS = 592;  // vector kernel: 4 warps per block, 4 blocks per SM
 
 size_t ln_bwd_partial_floats(int C) { return (size_t)2 * LNB_VEC_BLOCKS * C; }
 
@@ -502,23 +505,48 @@ __global__ void __launch_bounds__(256) ln_bwd_k(T* dres, float* part, const T* d
     }
 }
 
-__global__ void ln_bwd_final_k(float* dw, float* db, const float* part, int nblk, int C) {
-    int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= C) return;
-    float a = 0.f, b = 0.f;
-    for (int i = 0; i < nblk; i++) {
-        a += part[(size_t)i * C + c];
-        b += part[(size_t)(nblk + i) * C + c];
+// out_j[c] = sum over i < n of part[(j*n + i)*N + c] for j = blockIdx.y (out_0 = dw, out_1 =
+// db), in a fixed order: warp w adds rows w, w+32, ... into four interleaved accumulators,
+// then the 32 warp totals are added in warp order.  One block per 32 columns.
+__global__ void __launch_bounds__(1024) colreduce_k(float* out0, float* out1, const float* part, int n,
+                                                    int N) {
+    __shared__ float sh[32][33];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + lane;
+    const float* p = part + (size_t)blockIdx.y * n * N;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    if (c < N) {
+        int i = warp;
+        for (; i + 96 < n; i += 128) {
+            a0 += p[(size_t)i * N + c];
+            a1 += p[(size_t)(i + 32) * N + c];
+            a2 += p[(size_t)(i + 64) * N + c];
+            a3 += p[(size_t)(i + 96) * N + c];
+        }
+        for (; i < n; i += 32) a0 += p[(size_t)i * N + c];
     }
-    dw[c] = a;
-    db[c] = b;
+    sh[warp][lane] = (a0 + a1) + (a2 + a3);
+    __syncthreads();
+    if (warp == 0 && c < N) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < 32; w++) t += sh[w][lane];
+        (blockIdx.y ? out1 : out0)[c] = t;
+    }
+}
+
+static cudaError_t colreduce(float* out0, float* out1, const float* part, int n, int N, cudaStream_t s) {
+    dim3 g(cdiv(N, 32), out1 ? 2 : 1);
+    G2_LAUNCH colreduce_k<<<g, 1024, 0, s>>>(out0, out1, part, n, N);
+    return cudaGetLastError();
 }
 
 template <typename T>
 static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, const T* dout, const T* inp,
                                  const float* w, const float* mean, const float* rstd, int M, int C,
                                  float* part, cudaStream_t s) {
-    const int nv = (C % 256 == 0) ? C / 256 : 0;
+    const bool aligned = ((uintptr_t)w & 15) == 0;
+    const int nv = (C % 256 == 0 && aligned) ? C / 256 : 0;
     if (nv >= 1 && nv <= 4) {
         switch (nv) {
             case 1: G2_LAUNCH ln_bwd_vec_k<T, 1><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, rstd, M, C); break;
@@ -526,16 +554,14 @@ static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, const T* dout, c
             case 3: G2_LAUNCH ln_bwd_vec_k<T, 3><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, rstd, M, C); break;
             default: G2_LAUNCH ln_bwd_vec_k<T, 4><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, rstd, M, C); break;
         }
-        G2_LAUNCH ln_bwd_final_k<<<cdiv(C, 256), 256, 0, s>>>(dw, db, part, LNB_VEC_BLOCKS, C);
-        return cudaGetLastError();
+        return colreduce(dw, db, part, LNB_VEC_BLOCKS, C, s);
     }
     size_t smem = (size_t)8 * 2 * C * sizeof(float);
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(ln_bwd_k<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     G2_LAUNCH ln_bwd_k<T><<<LNB_BLOCKS, 256, smem, s>>>(dres, part, dout, inp, w, mean, rstd, M, C);
-    G2_LAUNCH ln_bwd_final_k<<<cdiv(C, 256), 256, 0, s>>>(dw, db, part, LNB_BLOCKS, C);
-    return cudaGetLastError();
+    return colreduce(dw, db, part, LNB_BLOCKS, C, s);
 }
 
 cudaError_t layernorm_backward(ActType at, void* dres, float* dw, float* db, const void* dout,
@@ -556,7 +582,7 @@ static const int CS_ROWS = 256;  // rows per row block
 size_t colsum_partial_floats(int M, int N) { return (size_t)cdiv(M, CS_ROWS) * N; }
 
 template <typename T>
-__global__ void colsum_part_k(float* part, const T* X, int M, int N) {
+__global__ void __launch_bounds__(256) colsum_part_k(float* part, const T* X, int M, int N) {
     __shared__ float sh[8][256];
     int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int col = blockIdx.x * 256 + lane * 8;
@@ -565,7 +591,20 @@ __global__ void colsum_part_k(float* part, const T* X, int M, int N) {
 #pragma unroll
     for (int i = 0; i < 8; i++) acc[i] = 0.f;
     bool vec = ((N & 7) == 0) && col + 8 <= N;
-    for (int r = r0 + warp; r < r1; r += 8) {
+    int r = r0 + warp;
+    if (vec) {
+        // rows r, r+8, r+16, r+24 loaded together, added in row order
+        for (; r + 24 < r1; r += 32) {
+            float v[4][8];
+#pragma unroll
+            for (int j = 0; j < 4; j++) Vec8<T>::load(X + (size_t)(r + 8 * j) * N + col, v[j]);
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+#pragma unroll
+                for (int i = 0; i < 8; i++) acc[i] += v[j][i];
+        }
+    }
+    for (; r < r1; r += 8) {
         const T* x = X + (size_t)r * N;
         if (vec) {
             float v[8];
@@ -589,14 +628,6 @@ __global__ void colsum_part_k(float* part, const T* X, int M, int N) {
     }
 }
 
-__global__ void colsum_final_k(float* out, const float* part, int nrb, int N) {
-    int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= N) return;
-    float a = 0.f;
-    for (int i = 0; i < nrb; i++) a += part[(size_t)i * N + c];
-    out[c] = a;
-}
-
 cudaError_t colsum(ActType at, float* out, const void* X, int M, int N, float* part, cudaStream_t s) {
     if (N <= 0) return cudaSuccess;
     int nrb = M > 0 ? (int)cdiv(M, CS_ROWS) : 0;
@@ -607,8 +638,8 @@ cudaError_t colsum(ActType at, float* out, const void* X, int M, int N, float* p
         else
             G2_LAUNCH colsum_part_k<float><<<g, 256, 0, s>>>(part, (const float*)X, M, N);
     }
-    G2_LAUNCH colsum_final_k<<<cdiv(N, 256), 256, 0, s>>>(out, part, nrb, N);
-    return cudaGetLastError();
+    if (nrb == 0) return cudaMemsetAsync(out, 0, (size_t)N * sizeof(float), s);
+    return colreduce(out, nullptr, part, nrb, N, s);
 }
 
 // ------------------------------------------------------------------ softmax + cross-entropy
@@ -676,7 +707,7 @@ __global__ void __launch_bounds__(1024) softmax_xent_k(T* logits, float* losses,
     int tg = targets[row];
     bool ok = (unsigned)tg < (unsigned)V;
     if (tid == 0) {
-        if (!ok) atomicOr(flags, G2_FLAG_BAD_TARGET);
+        if (!ok && flags) atomicOr(flags, G2_FLAG_BAD_TARGET);
         losses[row] = ok ? lse - to_f(x[tg]) : 0.f;
     }
     __syncthreads();  // every thread has read x[tg] before it is overwritten
@@ -703,121 +734,138 @@ __global__ void __launch_bounds__(1024) softmax_xent_k(T* logits, float* losses,
     }
 }
 
-// bf16 rows held in registers: each of the 1024 threads keeps its NCH chunks of 8
-// columns (chunk tid + 1024 k) as packed bf16 (4 registers per chunk), so the row is
-// read from memory once and written once.  Each thread keeps a running max m_t and sum
-// of exp(x - m_t); one block reduction merges the (max, sum) pairs in a fixed tree.
+// bf16 rows, Vp a multiple of 8, in two passes over the row with one block per row.
+// Pass 1 streams the row from memory; each thread keeps a running maximum m of its
+// columns and the sum s of 2^((x - m) log2 e), rescaling s when a chunk of 8 columns
+// raises m; the block then merges the (m, s) pairs in a fixed tree.  Pass 2 reads the
+// row again -- an L2 hit, it was read microseconds earlier -- and overwrites it with
+// (softmax - onehot) * dloss.  Exponentials are exp2f of pre-scaled arguments.
+constexpr int XE_THREADS = 512;
+constexpr float XE_LOG2E = 1.4426950408889634f;
+constexpr float XE_LN2 = 0.6931471805599453f;
+
+G2_DEV void unpack8(const uint4& u, float* v) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        float2 t = __bfloat1622float2(h[i]);
+        v[2 * i] = t.x;
+        v[2 * i + 1] = t.y;
+    }
+}
+
+// fold 8 columns (the first nvalid real) into the running (m, s)
+template <bool FULL>
+G2_DEV void xe_fold(const uint4& u, int nvalid, float& m, float& s) {
+    float v[8];
+    unpack8(u, v);
+    float cm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        if (FULL || i < nvalid) cm = fmaxf(cm, v[i]);
+    if (cm > m) {
+        s *= exp2f((m - cm) * XE_LOG2E);  // m = -inf at the start: s stays 0
+        m = cm;
+    }
+    const float ml = m * XE_LOG2E;
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        if (FULL || i < nvalid) s += exp2f(fmaf(v[i], XE_LOG2E, -ml));
+}
+
 G2_DEV void merge_ms(float& m, float& s, float m2, float s2) {
     float mn = fmaxf(m, m2);
     if (mn == -INFINITY) return;  // both empty
-    s = s * expf(m - mn) + s2 * expf(m2 - mn);
+    s = s * exp2f((m - mn) * XE_LOG2E) + s2 * exp2f((m2 - mn) * XE_LOG2E);
     m = mn;
 }
 
-template <int NCH>
-__global__ void __launch_bounds__(1024) softmax_xent_reg_k(bf16* logits, float* losses, const int32_t* targets,
-                                                           int V, int Vp, float dloss, int* flags) {
-    __shared__ float red_m[32], red_s[32];
+__global__ void __launch_bounds__(XE_THREADS) softmax_xent_bf16_k(bf16* logits, float* losses,
+                                                                  const int32_t* targets, int V, int Vp,
+                                                                  float dloss, int* flags) {
+    __shared__ float red_m[XE_THREADS / 32], red_s[XE_THREADS / 32];
     __shared__ float bcast;
     const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     bf16* x = logits + (size_t)row * Vp;
     const int tg = targets[row];
     const bool ok = (unsigned)tg < (unsigned)V;
-    // the target column lives in chunk k_t of thread t_t, element e_t
-    const int t_t = (tg >> 3) & 1023, k_t = (tg >> 3) >> 10, e_t = tg & 7;
-    const bool own = ok && tid == t_t;
-    const float x_tg = own ? __bfloat162float(x[tg]) : 0.f;
-    uint4 raw[NCH];
+    const int nfull = V >> 3, nreal = (V + 7) >> 3, nch = Vp >> 3;
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    float x_tg = 0.f;
+    if (tid == 0 && ok) x_tg = __bfloat162float(x[tg]);
+
+    float m = -INFINITY, s = 0.f;
+    int k = tid;
+    for (; k + 3 * XE_THREADS < nfull; k += 4 * XE_THREADS) {
+        uint4 u[4];
 #pragma unroll
-    for (int k = 0; k < NCH; k++) {
-        const int c = (tid + k * 1024) * 8;
-        raw[k] = c < Vp ? *reinterpret_cast<const uint4*>(x + c) : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < 4; j++) u[j] = xv[k + j * XE_THREADS];
+#pragma unroll
+        for (int j = 0; j < 4; j++) xe_fold<true>(u[j], 8, m, s);
     }
-    float m = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < NCH; k++) {
-        const int c = (tid + k * 1024) * 8;
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            float2 v = __bfloat1622float2(h[i]);
-            m = fmaxf(m, c + 2 * i < V ? v.x : -INFINITY);
-            m = fmaxf(m, c + 2 * i + 1 < V ? v.y : -INFINITY);
-        }
-    }
-    float sum = 0.f;
-#pragma unroll
-    for (int k = 0; k < NCH; k++) {
-        const int c = (tid + k * 1024) * 8;
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            float2 v = __bfloat1622float2(h[i]);
-            sum += c + 2 * i < V ? expf(v.x - m) : 0.f;
-            sum += c + 2 * i + 1 < V ? expf(v.y - m) : 0.f;
-        }
+    for (; k < nreal; k += XE_THREADS) {
+        uint4 u = xv[k];
+        if (k < nfull)
+            xe_fold<true>(u, 8, m, s);
+        else
+            xe_fold<false>(u, V - k * 8, m, s);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-        merge_ms(m, sum, m2, s2);
+        float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        merge_ms(m, s, m2, s2);
     }
     if (lane == 0) {
         red_m[warp] = m;
-        red_s[warp] = sum;
+        red_s[warp] = s;
     }
     __syncthreads();
     if (warp == 0) {
-        float mm = red_m[lane], ss = red_s[lane];
+        float mm = lane < XE_THREADS / 32 ? red_m[lane] : -INFINITY;
+        float ss = lane < XE_THREADS / 32 ? red_s[lane] : 0.f;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             float m2 = __shfl_xor_sync(0xffffffffu, mm, o), s2 = __shfl_xor_sync(0xffffffffu, ss, o);
             merge_ms(mm, ss, m2, s2);
         }
-        if (lane == 0) bcast = mm + logf(ss);
+        if (lane == 0) bcast = mm * XE_LOG2E + log2f(ss);  // log2 of the row's sum of exp
     }
-    __syncthreads();
-    const float lse = bcast;
-#pragma unroll
-    for (int k = 0; k < NCH; k++) {
-        const int c = (tid + k * 1024) * 8;
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
-        uint4 outv;
-        __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&outv);
+    __syncthreads();  // also orders the read of x[tg] before pass 2 overwrites it
+    const float lse2 = bcast;
+    if (tid == 0) {
+        if (!ok && flags) atomicOr(flags, G2_FLAG_BAD_TARGET);
+        losses[row] = ok ? lse2 * XE_LN2 - x_tg : 0.f;
+    }
+    const int k_t = ok ? tg >> 3 : -1, e_t = tg & 7;
+    uint4* xo = reinterpret_cast<uint4*>(x);
+    for (k = tid; k < nch; k += XE_THREADS) {
+        uint4 u = __ldcs(xv + k);
+        float v[8];
+        unpack8(u, v);
+        uint4 o;
+        __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            float2 v = __bfloat1622float2(h[i]);
-            float g0 = c + 2 * i < V ? expf(v.x - lse) * dloss : 0.f;
-            float g1 = c + 2 * i + 1 < V ? expf(v.y - lse) * dloss : 0.f;
-            if (own && k == k_t) {
+            const int c0 = k * 8 + 2 * i;
+            float g0 = c0 < V ? exp2f(fmaf(v[2 * i], XE_LOG2E, -lse2)) * dloss : 0.f;
+            float g1 = c0 + 1 < V ? exp2f(fmaf(v[2 * i + 1], XE_LOG2E, -lse2)) * dloss : 0.f;
+            if (k == k_t) {
                 g0 -= e_t == 2 * i ? dloss : 0.f;
                 g1 -= e_t == 2 * i + 1 ? dloss : 0.f;
             }
             oh[i] = __floats2bfloat162_rn(g0, g1);
         }
-        if (c < Vp) *reinterpret_cast<uint4*>(x + c) = outv;
-    }
-    if (own) losses[row] = lse - x_tg;
-    if (tid == 0 && !ok) {
-        atomicOr(flags, G2_FLAG_BAD_TARGET);
-        losses[row] = 0.f;
+        __stcs(xo + k, o);
     }
 }
 
 cudaError_t softmax_xent(ActType at, void* logits, float* losses, const int32_t* targets, int M,
                          int V, int Vp, float dloss, int* flags, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
-    const int nch = (Vp % 8 == 0) ? (Vp / 8 + 1023) / 1024 : 0;
-    if (at == ACT_BF16 && nch >= 1 && nch <= 8) {
-#define G2_XENT_CASE(N)                                                                               \
-    case N:                                                                                           \
-        G2_LAUNCH softmax_xent_reg_k<N><<<M, 1024, 0, s>>>((bf16*)logits, losses, targets, V, Vp, dloss, flags); \
+    if (at == ACT_BF16 && Vp % 8 == 0 && (((uintptr_t)logits) & 15) == 0) {
+        G2_LAUNCH softmax_xent_bf16_k<<<M, XE_THREADS, 0, s>>>((bf16*)logits, losses, targets, V, Vp, dloss,
+                                                               flags);
         return cudaGetLastError();
-        switch (nch) {
-            G2_XENT_CASE(1) G2_XENT_CASE(2) G2_XENT_CASE(3) G2_XENT_CASE(4)
-            G2_XENT_CASE(5) G2_XENT_CASE(6) G2_XENT_CASE(7) G2_XENT_CASE(8)
-        }
-#undef G2_XENT_CASE
     }
     if (at == ACT_BF16)
         G2_LAUNCH softmax_xent_k<bf16><<<M, 1024, 0, s>>>((bf16*)logits, losses, targets, V, Vp, dloss, flags);

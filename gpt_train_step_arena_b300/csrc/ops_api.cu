@@ -113,6 +113,61 @@ extern "C" int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dou
                                       (cudaStream_t)stream), "attention_backward");
 }
 
+extern "C" int gpt2_op_layernorm_forward(int dtype, void* out, float* mean, float* rstd, const void* inp,
+                                         const float* w, const float* b, int M, int C, void* stream) {
+    if (!dtype_ok(dtype)) return op_fail(GPT2_ERR_ARG, "layernorm: bad dtype %d", dtype);
+    if (M < 0 || C <= 0) return op_fail(GPT2_ERR_ARG, "layernorm: bad shape M=%d C=%d", M, C);
+    if (M == 0) return GPT2_OK;
+    if (!out || !mean || !rstd || !inp || !w || !b) return op_fail(GPT2_ERR_ARG, "layernorm: null pointer");
+    return op_cuda(layernorm_forward(act_of(dtype), out, mean, rstd, inp, w, b, M, C, (cudaStream_t)stream),
+                   "layernorm_forward");
+}
+
+extern "C" size_t gpt2_op_layernorm_backward_workspace(int C) {
+    return C > 0 ? ln_bwd_partial_floats(C) * sizeof(float) : 0;
+}
+
+extern "C" int gpt2_op_layernorm_backward(int dtype, void* dinp, float* dw, float* db, const void* dout,
+                                          const void* inp, const float* w, const float* mean,
+                                          const float* rstd, int M, int C, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+    if (!dtype_ok(dtype)) return op_fail(GPT2_ERR_ARG, "layernorm_backward: bad dtype %d", dtype);
+    if (M < 0 || C <= 0) return op_fail(GPT2_ERR_ARG, "layernorm_backward: bad shape M=%d C=%d", M, C);
+    if (!dw || !db || !w || (M > 0 && (!dinp || !dout || !inp || !mean || !rstd)))
+        return op_fail(GPT2_ERR_ARG, "layernorm_backward: null pointer");
+    size_t need = gpt2_op_layernorm_backward_workspace(C);
+    if (!workspace || workspace_bytes < need)
+        return op_fail(GPT2_ERR_ARG, "layernorm_backward: workspace of %zu bytes needed, %zu given", need,
+                       workspace_bytes);
+    return op_cuda(layernorm_backward(act_of(dtype), dinp, dw, db, dout, inp, w, mean, rstd, M, C,
+                                      (float*)workspace, (cudaStream_t)stream),
+                   "layernorm_backward");
+}
+
+extern "C" int gpt2_op_softmax_xent(int dtype, void* logits, float* losses, const int32_t* targets, int M,
+                                    int V, int Vp, float dloss, int* flags, void* stream) {
+    if (!dtype_ok(dtype)) return op_fail(GPT2_ERR_ARG, "softmax_xent: bad dtype %d", dtype);
+    if (M < 0 || V <= 0 || Vp < V) return op_fail(GPT2_ERR_ARG, "softmax_xent: bad shape M=%d V=%d Vp=%d", M, V, Vp);
+    if (M == 0) return GPT2_OK;
+    if (!logits || !losses || !targets) return op_fail(GPT2_ERR_ARG, "softmax_xent: null pointer");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (flags) {
+        int rc = op_cuda(cudaMemsetAsync(flags, 0, sizeof(int), s), "softmax_xent");
+        if (rc) return rc;
+    }
+    int scratch = 0;
+    int rc = op_cuda(softmax_xent(act_of(dtype), logits, losses, targets, M, V, Vp, dloss,
+                                  flags ? flags : nullptr, s),
+                     "softmax_xent");
+    if (rc || !flags) return rc;
+    rc = op_cuda(cudaMemcpyAsync(&scratch, flags, sizeof(int), cudaMemcpyDeviceToHost, s), "softmax_xent");
+    if (rc) return rc;
+    rc = op_cuda(cudaStreamSynchronize(s), "softmax_xent");
+    if (rc) return rc;
+    if (scratch) return op_fail(GPT2_ERR_TOKEN, "softmax_xent: a target id is outside [0, %d)", V);
+    return GPT2_OK;
+}
+
 // Sets the message returned by gpt2_op_last_error (for entry points in other files).
 void g2_op_set_error(const char* msg) {
     std::lock_guard<std::mutex> lk(g_op_err_mu);

@@ -4,7 +4,9 @@
 
 Ops: the matrix products of a layer (qkv_fwd, attproj_fwd, fc_fwd, fcproj_fwd,
 lmhead_fwd, fc_dgrad, fc_wgrad, qkv_wgrad, lmhead_dgrad, lmhead_wgrad), attention
-(attn_fwd, attn_bwd) and AdamW over the full parameter count.  Inputs are seeded random
+(attn_fwd, attn_bwd), layernorm (ln_fwd, ln_bwd), softmax + cross-entropy (xent), bias
+gradients (bias_grad, bias_grad_fc, bias_grad_qkv) and AdamW over the full parameter
+count.  Inputs are seeded random
 device tensors; each op runs --reps times after --warmup runs, timed with CUDA events,
 and prints one JSON line (ms per run, TFLOP/s or GB/s).  Used for per-kernel timing and
 as the small, self-contained program that Nsight Compute captures.
@@ -62,6 +64,32 @@ def main():
             fn = lambda: ops.attention_backward(dout, qkv, out, lse, NH)
             flops *= 2
         unit, work = "TFLOP/s", flops
+    elif args.op in ("ln_fwd", "ln_bwd"):
+        M, C = c["B"] * c["T"], c["C"]
+        x, dy, acc = rnd(M, C), rnd(M, C), rnd(M, C)
+        w = torch.ones(C, device=dev) + 0.1 * torch.randn(C, device=dev, generator=g)
+        b = 0.1 * torch.randn(C, device=dev, generator=g)
+        _, mean, rstd = ops.layernorm_forward(x, w, b)
+        if args.op == "ln_fwd":
+            fn = lambda: ops.layernorm_forward(x, w, b)
+            work = 2.0 * M * C * 2 + 8.0 * M
+        else:
+            fn = lambda: ops.layernorm_backward(acc, dy, x, w, mean, rstd)
+            work = 4.0 * M * C * 2 + 8.0 * M
+        unit = "GB/s"
+    elif args.op == "xent":
+        M, V = c["B"] * c["T"], c["V"]
+        Vp = (V + 127) // 128 * 128
+        logits = rnd(M, Vp)
+        tg = torch.randint(0, V, (M,), device=dev, dtype=torch.int32, generator=g)
+        fn = lambda: ops.softmax_xent(logits, tg, V, 1.0 / M, check=False)
+        unit, work = "GB/s", 2.0 * M * Vp * 2 + 8.0 * M
+    elif args.op.startswith("bias_grad"):
+        M = c["B"] * c["T"]
+        Nn = {"bias_grad": c["C"], "bias_grad_fc": 4 * c["C"], "bias_grad_qkv": 3 * c["C"]}[args.op]
+        x = rnd(M, Nn)
+        fn = lambda: ops.bias_grad(x)
+        unit, work = "GB/s", 2.0 * M * Nn + 4.0 * Nn
     elif args.op == "adamw":
         n = sum(synth.param_sizes(c["L"], c["C"], (c["V"] + 127) // 128 * 128, c["maxT"]))
         p, gr, m, v = (rnd(n, dtype=torch.float32) for _ in range(4))

@@ -77,3 +77,38 @@ def attention_backward(dout, qkv, out, lse, NH: int):
                                             out.data_ptr(), lse.data_ptr(), B, T, C, NH, ws.data_ptr(),
                                             _stream()))
     return dqkv
+
+
+def layernorm_forward(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor):
+    """x (M,C) -> (out (M,C) like x, mean (M) fp32, rstd (M) fp32)."""
+    M, C = x.shape
+    out = torch.empty_like(x)
+    mean = torch.empty(M, dtype=torch.float32, device=x.device)
+    rstd = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(N.lib.gpt2_op_layernorm_forward(_dt(x), out.data_ptr(), mean.data_ptr(), rstd.data_ptr(),
+                                           x.data_ptr(), w.data_ptr(), b.data_ptr(), M, C, _stream()))
+    return out, mean, rstd
+
+
+def layernorm_backward(dinp: torch.Tensor, dout, x, w, mean, rstd):
+    """dinp (M,C) is accumulated into in place; returns (dw, db) fp32 (C)."""
+    M, C = x.shape
+    dw = torch.empty(C, dtype=torch.float32, device=x.device)
+    db = torch.empty(C, dtype=torch.float32, device=x.device)
+    ws_bytes = N.lib.gpt2_op_layernorm_backward_workspace(C)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    _check(N.lib.gpt2_op_layernorm_backward(_dt(x), dinp.data_ptr(), dw.data_ptr(), db.data_ptr(),
+                                            dout.data_ptr(), x.data_ptr(), w.data_ptr(), mean.data_ptr(),
+                                            rstd.data_ptr(), M, C, ws.data_ptr(), ws_bytes, _stream()))
+    return dw, db
+
+
+def softmax_xent(logits: torch.Tensor, targets: torch.Tensor, V: int, dloss: float, check: bool = True):
+    """logits (M,Vp) is overwritten with dlogits; returns the per-row losses (M) fp32."""
+    M, Vp = logits.shape
+    losses = torch.empty(M, dtype=torch.float32, device=logits.device)
+    flags = torch.zeros(1, dtype=torch.int32, device=logits.device) if check else None
+    _check(N.lib.gpt2_op_softmax_xent(_dt(logits), logits.data_ptr(), losses.data_ptr(), targets.data_ptr(),
+                                      M, V, Vp, dloss, None if flags is None else flags.data_ptr(),
+                                      _stream()))
+    return losses

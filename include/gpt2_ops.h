@@ -86,6 +86,38 @@ int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const vo
                                const void* out, const float* lse, int B, int T, int C, int NH,
                                float* workspace, void* stream);
 
+/* LayerNorm forward (llm.c annotated listing §1.3 layernorm_forward; picoGPT
+ * layer_norm): for each of the M rows of inp (M,C) of `dtype`, out = (x - mean) * rstd
+ * * w + b with the row mean, the biased variance and rstd = 1/sqrt(var + 1e-5).
+ * out (M,C) `dtype` is overwritten; mean and rstd (M floats each) receive the row
+ * statistics; w and b are C floats.  M may be 0. */
+int gpt2_op_layernorm_forward(int dtype, void* out, float* mean, float* rstd, const void* inp,
+                              const float* w, const float* b, int M, int C, void* stream);
+
+/* Its backward (llm.c §1.4 layernorm_backward).  dinp (M,C) `dtype` is ACCUMULATED into
+ * (dinp += d loss / d inp, as in the listing, which is how the residual stream's
+ * gradient is carried); dw and db (C floats) are OVERWRITTEN with the weight and bias
+ * gradients summed over the rows in a fixed order (the listing accumulates into zeroed
+ * buffers: the same values).  mean and rstd are the forward's statistics.  workspace
+ * must hold gpt2_op_layernorm_backward_workspace(C) bytes. */
+size_t gpt2_op_layernorm_backward_workspace(int C);
+int gpt2_op_layernorm_backward(int dtype, void* dinp, float* dw, float* db, const void* dout,
+                               const void* inp, const float* w, const float* mean,
+                               const float* rstd, int M, int C, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* Fused softmax + cross-entropy forward and backward (llm.c §1.13 softmax_forward,
+ * §1.14 crossentropy_forward, §1.15 crossentropy_softmax_backward; picoGPT lm_loss).
+ * logits (M,Vp) of `dtype` with V <= Vp real columns: for each row, lse = logsumexp of
+ * the V real logits, losses[m] = lse - logit[targets[m]], and the row is OVERWRITTEN
+ * in place with (softmax - onehot(target)) * dloss over the V real columns and 0 over
+ * the Vp - V padding columns.  targets: M int32 device ids; one outside [0, V) gives
+ * that row loss 0 and no one-hot term, and the call returns GPT2_ERR_TOKEN after
+ * waiting for the stream (flags, 4 bytes of device memory, must be given for that
+ * check; pass NULL to skip it and return without waiting). */
+int gpt2_op_softmax_xent(int dtype, void* logits, float* losses, const int32_t* targets, int M,
+                         int V, int Vp, float dloss, int* flags, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -147,3 +147,75 @@ def test_attention_fwd_bwd(torch_cuda, B, T, C, NH, dt):
     mx = s.max(-1, keepdims=True)
     ref_lse = (mx + np.log(np.exp(s - mx).sum(-1, keepdims=True)))[..., 0]
     assert np.max(np.abs(_np(lse) - ref_lse)) <= (1e-4 if dt == "fp32" else 2e-2)
+
+
+# ---------------------------------------------------------------- layernorm
+@pytest.mark.parametrize("M,C", [(1000, 768), (37, 768), (300, 100), (1, 256), (513, 1024), (0, 768)])
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+def test_layernorm_fwd_bwd(torch_cuda, M, C, dt):
+    torch = torch_cuda
+    from gpt_train_step_arena_b300 import ops
+    rng = np.random.default_rng(M * 11 + C)
+    x = (rng.normal(size=(M, C)) * 2 + 0.5).astype(np.float32)
+    w = (1 + 0.1 * rng.normal(size=C)).astype(np.float32)
+    b = (0.1 * rng.normal(size=C)).astype(np.float32)
+    dy = rng.normal(size=(M, C)).astype(np.float32)
+    acc = rng.normal(size=(M, C)).astype(np.float32)
+    tdt = torch.float32 if dt == "fp32" else torch.bfloat16
+    xd, dyd, accd = _to(torch, x, tdt), _to(torch, dy, tdt), _to(torch, acc, tdt)
+    wd, bd = _to(torch, w, torch.float32), _to(torch, b, torch.float32)
+    out, mean, rstd = ops.layernorm_forward(xd, wd, bd)
+    acc_before = _np(accd)
+    dw, db = ops.layernorm_backward(accd, dyd, xd, wd, mean, rstd)
+    torch.cuda.synchronize()
+    if M == 0:
+        assert np.all(_np(dw) == 0) and np.all(_np(db) == 0)
+        return
+    x_eff, dy_eff = _np(xd), _np(dyd)
+    r_out, r_mean, r_rstd = o64.layernorm(x_eff, w, b)
+    r_dx, r_dw, r_db = o64.layernorm_backward(dy_eff, x_eff, w, r_mean, r_rstd)
+    assert np.max(np.abs(_np(mean) - r_mean)) <= 1e-5 * (1 + np.max(np.abs(r_mean)))
+    assert np.max(np.abs(_np(rstd) / r_rstd - 1)) <= 1e-5
+    # fp32: a few roundings per element; bf16: one output rounding (2^-9 relative)
+    tol = 1e-5 if dt == "fp32" else 4e-3
+    assert _rel(_np(out), r_out) <= tol
+    assert _rel(_np(accd) - acc_before, r_dx) <= (1e-5 if dt == "fp32" else 8e-3)
+    assert _rel(_np(dw), r_dw) <= 1e-5 and _rel(_np(db), r_db) <= 1e-5
+    dw2, db2 = ops.layernorm_backward(_to(torch, acc, tdt), dyd, xd, wd, mean, rstd)
+    assert torch.equal(dw, dw2) and torch.equal(db, db2)  # fixed summation order
+
+
+# ---------------------------------------------------------------- softmax + cross-entropy
+@pytest.mark.parametrize("M,V,Vp", [(64, 50257, 50304), (300, 27, 32), (129, 1000, 1000), (5, 1, 8),
+                                    (40, 4101, 4104), (3, 9000, 9001)])
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+def test_softmax_xent(torch_cuda, M, V, Vp, dt):
+    torch = torch_cuda
+    from gpt_train_step_arena_b300 import ops
+    rng = np.random.default_rng(M + V)
+    logits = (rng.normal(size=(M, Vp)) * 3).astype(np.float32)
+    logits[:, V:] = 1e4   # padding columns must be ignored whatever they hold
+    tg = rng.integers(0, V, size=M).astype(np.int32)
+    tdt = torch.float32 if dt == "fp32" else torch.bfloat16
+    ld = _to(torch, logits, tdt)
+    l_eff = _np(ld)[:, :V]
+    dloss = 1.0 / M
+    losses = ops.softmax_xent(ld, torch.from_numpy(tg).to("cuda"), V, dloss)
+    _, r_losses, r_dl = o64.cross_entropy(l_eff, tg)
+    got_l = _np(losses)
+    assert np.max(np.abs(got_l - r_losses)) <= (2e-5 if dt == "fp32" else 1e-4) * max(1.0, np.max(r_losses))
+    got_d = _np(ld)
+    assert np.all(got_d[:, V:] == 0)
+    # relative to the gradient's natural scale (dloss per row): with V = 1 the exact
+    # gradient is 0 and the kernel leaves a rounding residue of order 2^-22 * dloss
+    scale = max(np.linalg.norm(r_dl), dloss * np.sqrt(M))
+    assert np.linalg.norm(got_d[:, :V] - r_dl) <= (1e-5 if dt == "fp32" else 8e-3) * scale
+
+
+def test_softmax_xent_bad_target(torch_cuda):
+    torch = torch_cuda
+    from gpt_train_step_arena_b300 import ops
+    logits = torch.zeros(4, 64, dtype=torch.bfloat16, device="cuda")
+    tg = torch.tensor([0, 1, 64, 3], dtype=torch.int32, device="cuda")
+    with pytest.raises(ops.OpError, match="TOKEN"):
+        ops.softmax_xent(logits, tg, 64, 0.25)
