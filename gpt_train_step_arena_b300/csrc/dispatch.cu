@@ -21,7 +21,11 @@ cudaError_t gemm_dispatch(const GemmArgs& a, float* ws, size_t ws_bytes, cudaStr
 }
 
 cudaError_t attention_forward(ActType at, void* out, float* lse, const void* qkv, int B, int T,
-                              int C, int NH, cudaStream_t s) {
+                              int C, int NH, cudaStream_t s, int* flags) {
+    if (attention_tc_supported(at, C, NH, qkv)) {
+        cudaError_t e = attention_forward_tc(out, lse, qkv, B, T, C, NH, flags, s);
+        if (e != cudaErrorNotSupported) return e;  // else: no tensor map for this shape
+    }
     if (attention_mma_supported(at, C, NH)) return attention_forward_mma(out, lse, qkv, B, T, C, NH, s);
     return attention_forward_simt(at, out, lse, qkv, B, T, C, NH, s);
 }

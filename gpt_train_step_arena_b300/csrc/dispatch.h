@@ -10,8 +10,10 @@ size_t gemm_workspace_bytes(int M, int C, int Vp, int L);
 // tensor-core kernel for bf16 operands it supports, the SIMT kernel otherwise.
 cudaError_t gemm_dispatch(const GemmArgs& a, float* ws, size_t ws_bytes, cudaStream_t s);
 
+// flags (may be null): device error flags, G2_FLAG_TIMEOUT is OR-ed in if a bounded
+// wait of the tensor-core kernel expires.
 cudaError_t attention_forward(ActType at, void* out, float* lse, const void* qkv, int B, int T,
-                              int C, int NH, cudaStream_t s);
+                              int C, int NH, cudaStream_t s, int* flags = nullptr);
 cudaError_t attention_backward(ActType at, void* dqkv, const void* dout, const void* qkv,
                                const void* out, const float* lse, int B, int T, int C, int NH,
                                float* scratch_D, cudaStream_t s);

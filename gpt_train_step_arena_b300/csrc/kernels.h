@@ -90,6 +90,12 @@ cudaError_t attention_backward_mma(void* dqkv, const void* dout, const void* qkv
                                    const float* lse, int B, int T, int C, int NH, float* scratch_D,
                                    cudaStream_t s);
 
+// tcgen05 forward (bf16, head size 64, 16-byte aligned qkv).  flags (may be null):
+// G2_FLAG_TIMEOUT is OR-ed in if a bounded wait expires.
+bool attention_tc_supported(ActType at, int C, int NH, const void* qkv);
+cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, int T, int C, int NH, int* flags,
+                                 cudaStream_t s);
+
 // ---- GEMM --------------------------------------------------------------------------
 // D[m,n] = epilogue( sum_k A(m,k) * B(n,k) ), A(m,k) = A[m*sAm + k*sAk], B(n,k) = B[n*sBn + k*sBk].
 enum Epilogue {

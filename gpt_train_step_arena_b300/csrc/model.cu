@@ -427,7 +427,7 @@ static int forward_impl(gpt2* m, const int32_t* tokens, const int32_t* targets, 
            gemm_fwd(m, (int)M, 3 * C, C, ln1, pw(m, P_QKVW, (size_t)l * 3 * C * C),
                     pf(m, m->params, P_QKVB) + l * 3 * C, qkv, nullptr, nullptr));
         OP(GPT2_K_ATTN_FWD, attn_fwd_flops(m),
-           attention_forward(m->at, atty, m->lse + l * M * NH, qkv, B, T, C, NH, s));
+           attention_forward(m->at, atty, m->lse + l * M * NH, qkv, B, T, C, NH, s, m->flags));
         OP(GPT2_K_GEMM, gemm_flops(M, C, C),
            gemm_fwd(m, (int)M, C, C, atty, pw(m, P_APW, (size_t)l * C * C),
                     pf(m, m->params, P_APB) + l * C, res2, res_in, nullptr));
