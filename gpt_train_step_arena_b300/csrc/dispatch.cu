@@ -32,7 +32,11 @@ cudaError_t attention_forward(ActType at, void* out, float* lse, const void* qkv
 
 cudaError_t attention_backward(ActType at, void* dqkv, const void* dout, const void* qkv,
                                const void* out, const float* lse, int B, int T, int C, int NH,
-                               float* scratch_D, cudaStream_t s) {
+                               float* scratch_D, cudaStream_t s, int* flags) {
+    if (attention_tc_supported(at, C, NH, qkv)) {
+        cudaError_t e = attention_backward_tc(dqkv, dout, qkv, out, lse, B, T, C, NH, scratch_D, flags, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
     if (attention_mma_supported(at, C, NH))
         return attention_backward_mma(dqkv, dout, qkv, out, lse, B, T, C, NH, scratch_D, s);
     return attention_backward_simt(at, dqkv, dout, qkv, out, lse, B, T, C, NH, scratch_D, s);

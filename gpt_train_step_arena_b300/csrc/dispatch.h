@@ -16,6 +16,6 @@ cudaError_t attention_forward(ActType at, void* out, float* lse, const void* qkv
                               int C, int NH, cudaStream_t s, int* flags = nullptr);
 cudaError_t attention_backward(ActType at, void* dqkv, const void* dout, const void* qkv,
                                const void* out, const float* lse, int B, int T, int C, int NH,
-                               float* scratch_D, cudaStream_t s);
+                               float* scratch_D, cudaStream_t s, int* flags = nullptr);
 
 }  // namespace g2

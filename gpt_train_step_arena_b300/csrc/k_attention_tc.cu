@@ -328,6 +328,375 @@ __global__ void __launch_bounds__(NTH, 2)
     if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+
+// ------------------------------------------------------------------ backward
+// llm.c §1.8 attention_backward, without atomics and without the (T, T) buffers: P is
+// rebuilt from the forward's log-sum-exp L and D = rowsum(dO * O), dS = P * (dP - D).
+// Two kernels of one template, 192 threads, one CTA per SM:
+//   DQ = true   (query-major, runs first): the CTA owns 128 queries of one head, keeps
+//               Q and dO, and streams K_j and V_j for j <= the query tile.  Its softmax
+//               threads first compute D for their own rows (and store it for the other
+//               kernel); then S = Q K^T, dP = dO V^T, dS = P (dP - D), dQ += dS K.
+//   DQ = false  (key-major): the CTA owns 128 keys, keeps K and V, and streams Q_i and
+//               dO_i for i >= the key tile; S^T = K Q^T, dP^T = V dO^T, P^T and
+//               dS^T = P^T (dP^T - D) with L and D of the query columns staged in
+//               shared memory; dV += P^T dO, dK += dS^T Q.
+// Each streamed 128-row tile is processed in two 64-column halves: the two halves' S and
+// dP sit in separate tensor-memory buffers (64 + 64 columns each) and their bf16 P / dS
+// in separate shared-memory buffers, so the products of one half overlap the softmax of
+// the other.  Accumulators (dQ, or dV and dK) stay in tensor memory until the end.
+struct BwdBars {
+    uint64_t row_full, st_full[2], st_empty[2], sdp_full[2], sdp_free[2], pds_full[2], pds_free[2], stats[2],
+        acc_done, drain;
+    uint32_t tmem_slot;
+    int abort;
+};
+constexpr int HALF = 64 * 128 * 2;  // 16 KB: 128 rows x 64 bf16
+constexpr int B_ROWA = 0, B_ROWB = TILE, B_ST = 2 * TILE;  // stream stages: 2 x (A 16 KB + B 16 KB)
+constexpr int B_PDS = B_ST + 4 * TILE;                     // P / dS half buffers
+template <bool DQ>
+struct BwdCfg {
+    static constexpr int NPDS = DQ ? 1 : 2;               // dS only, or P^T and dS^T
+    static constexpr int OFF_STATS = B_PDS + 2 * NPDS * HALF;  // key-major: L, D of 2 x 128 queries
+    static constexpr int OFF_BAR = OFF_STATS + (DQ ? 0 : 2 * 2 * 128 * 4);
+    static constexpr int SMEM = OFF_BAR + (int)sizeof(BwdBars);
+};
+// tensor memory: S / dP of half h at 128 h (+64), accumulators at 256 (dQ or dV), 320 (dK)
+constexpr uint32_t TB_COLS = 512, TB_ACC1 = 256, TB_ACC2 = 320;
+
+// one 128-byte row of 64 bf16 (packed pairs) into a K-major, 128-byte-swizzled buffer
+G2_DEV void store_row64(uint8_t* buf, int r, const uint32_t* pk) {
+    uint8_t* row = buf + r * 128;
+#pragma unroll
+    for (int ch = 0; ch < 8; ch++)
+        *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+}
+
+template <bool DQ>
+__global__ void __launch_bounds__(NTH, 1)
+    attn_bwd_tc_k(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
+                  bf16* dqkv, const bf16* dout, const bf16* outp, const float* lse, float* Dbuf, int T, int C,
+                  int NH, int* flags) {
+    using CF = BwdCfg<DQ>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    BwdBars* bar = reinterpret_cast<BwdBars*>(smem + CF::OFF_BAR);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (smem_u32(smem) & 1023) {
+        if (threadIdx.x == 0 && flags) atomicOr(flags, G2_FLAG_TIMEOUT);
+        return;
+    }
+    const int ntiles_t = gridDim.x;
+    // the row tile: queries (heaviest = last first) or keys (heaviest = first first)
+    const int rt = DQ ? ntiles_t - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
+    const int row0 = b * T, r0 = rt * 128;
+    // streamed tiles: keys 0..rt (DQ) or queries rt..ntiles_t-1 (key-major)
+    const int st0 = DQ ? 0 : rt, nst = DQ ? rt + 1 : ntiles_t - rt;
+    // x coordinates in the tensor maps: the row operands and the streamed operands
+    const int xa_row = DQ ? h * HS : C + h * HS;      // Q or K
+    const int xb_row = DQ ? h * HS : 2 * C + h * HS;  // dO (its own map) or V
+    const int xa_st = DQ ? C + h * HS : h * HS;       // K or Q
+    const int xb_st = DQ ? 2 * C + h * HS : h * HS;   // V or dO (its own map)
+    const CUtensorMap* map_b_row = DQ ? &tm_do : &tm_qkv;
+    const CUtensorMap* map_b_st = DQ ? &tm_qkv : &tm_do;
+
+    if (threadIdx.x == 0) {
+        bar->abort = 0;
+        mbar_init(&bar->row_full, 1);
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&bar->st_full[i], 1);
+            mbar_init(&bar->st_empty[i], 1);
+            mbar_init(&bar->sdp_full[i], 1);
+            mbar_init(&bar->sdp_free[i], 4);
+            mbar_init(&bar->pds_full[i], 4);
+            mbar_init(&bar->pds_free[i], 1);
+            mbar_init(&bar->stats[i], 128);
+        }
+        mbar_init(&bar->acc_done, 1);
+        mbar_init(&bar->drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_async_smem();
+        tma_prefetch_desc(&tm_qkv);
+        tma_prefetch_desc(&tm_do);
+    }
+    if (warp == 1) tmem_alloc(&bar->tmem_slot, TB_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar->tmem_slot;
+    volatile int* abort_flag = &bar->abort;
+
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            mbar_expect_tx(&bar->row_full, 2 * TILE);
+            tma_load_2d(&tm_qkv, &bar->row_full, smem + B_ROWA, xa_row, row0 + r0);
+            tma_load_2d(map_b_row, &bar->row_full, smem + B_ROWB, xb_row, row0 + r0);
+            for (int n = 2; n < nst; n++) {
+                tma_prefetch_l2(&tm_qkv, xa_st, row0 + (st0 + n) * 128);
+                tma_prefetch_l2(map_b_st, xb_st, row0 + (st0 + n) * 128);
+            }
+            int issued[2] = {-1, -1};
+            bool ok = true;
+            for (int n = 0; n < nst; n++) {
+                const int s = n & 1;
+                const uint32_t ph = (n >> 1) & 1;
+                if (!mbar_wait(&bar->st_empty[s], ph ^ 1, abort_flag, flags)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(&bar->st_full[s], 2 * TILE);
+                uint8_t* st = smem + B_ST + s * 2 * TILE;
+                tma_load_2d(&tm_qkv, &bar->st_full[s], st, xa_st, row0 + (st0 + n) * 128);
+                tma_load_2d(map_b_st, &bar->st_full[s], st + TILE, xb_st, row0 + (st0 + n) * 128);
+                issued[s] = (int)ph;
+            }
+            if (!ok) {
+                unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(&bar->row_full, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+                }
+                for (int s = 0; s < 2; s++) {
+                    if (issued[s] < 0) continue;
+                    t0 = globaltimer();
+                    while (!mbar_try_wait(&bar->st_full[s], (uint32_t)issued[s]) && globaltimer() - t0 < TIMEOUT_NS) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t ID_SDP = make_idesc(64, false, false);  // N = 64 streamed rows
+            constexpr uint32_t ID_ACC = make_idesc(HS, false, true);   // N = 64, streamed operand MN-major
+            const uint32_t sRA = smem_u32(smem + B_ROWA), sRB = smem_u32(smem + B_ROWB);
+            const uint32_t sPDS = smem_u32(smem + B_PDS);
+            bool ok = mbar_wait(&bar->row_full, 0, abort_flag, flags);
+            bool issued_any = false;
+            // half g = 2n + hh; its accumulation step runs one half behind its S / dP step
+            const int nhalves = 2 * nst;
+            for (int g = 0; ok && g <= nhalves; g++) {
+                if (g < nhalves) {
+                    const int n = g >> 1, hh = g & 1, s = n & 1;
+                    if ((hh == 0 && !mbar_wait(&bar->st_full[s], (n >> 1) & 1, abort_flag, flags)) ||
+                        !mbar_wait(&bar->sdp_free[hh], (n & 1) ^ 1, abort_flag, flags)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sA = smem_u32(smem + B_ST + s * 2 * TILE) + hh * 8192, sB = sA + TILE;
+                    const uint32_t tS = tmem + hh * 128, tP = tS + 64;
+#pragma unroll
+                    for (int k = 0; k < HS / 16; k++)
+                        umma_bf16(tS, sdesc(sRA + k * 32, 16, 1024), sdesc(sA + k * 32, 16, 1024), ID_SDP,
+                                  k > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < HS / 16; k++)
+                        umma_bf16(tP, sdesc(sRB + k * 32, 16, 1024), sdesc(sB + k * 32, 16, 1024), ID_SDP,
+                                  k > 0 ? 1u : 0u);
+                    umma_commit(&bar->sdp_full[hh]);
+                    issued_any = true;
+                }
+                if (g > 0) {
+                    const int pg = g - 1, n = pg >> 1, hh = pg & 1, s = n & 1;
+                    if (!mbar_wait(&bar->pds_full[hh], n & 1, abort_flag, flags)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // the streamed operands' rows of this half, read N-major (64 hs wide)
+                    const uint32_t sA = smem_u32(smem + B_ST + s * 2 * TILE) + hh * 8192, sB = sA + TILE;
+                    const uint32_t sDS = sPDS + (DQ ? hh : 2 + hh) * HALF;
+#pragma unroll
+                    for (int k = 0; k < 64 / 16; k++) {
+                        const uint32_t acc = (pg > 0 || k > 0) ? 1u : 0u;
+                        const uint64_t bA = sdesc(sA + k * 2048, 8192, 1024);
+                        if (DQ) {
+                            umma_bf16(tmem + TB_ACC1, sdesc(sDS + k * 32, 16, 1024), bA, ID_ACC, acc);  // dQ += dS K
+                        } else {
+                            const uint32_t sPT = sPDS + hh * HALF;
+                            const uint64_t bB = sdesc(sB + k * 2048, 8192, 1024);
+                            umma_bf16(tmem + TB_ACC1, sdesc(sPT + k * 32, 16, 1024), bB, ID_ACC, acc);  // dV += P^T dO
+                            umma_bf16(tmem + TB_ACC2, sdesc(sDS + k * 32, 16, 1024), bA, ID_ACC, acc);  // dK += dS^T Q
+                        }
+                    }
+                    umma_commit(&bar->pds_free[hh]);
+                    if (hh == 1) umma_commit(&bar->st_empty[s]);
+                    if (pg == nhalves - 1) umma_commit(&bar->acc_done);
+                    issued_any = true;
+                }
+            }
+            if (!ok && issued_any) {
+                umma_commit(&bar->drain);
+                unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(&bar->drain, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+                }
+            }
+        }
+    } else {
+        // ---------------- softmax warps 2..5: thread = row of the CTA's tile
+        const int quarter = warp & 3, r = quarter * 32 + lane;
+        const int grow = r0 + r;  // query (DQ) or key position of this thread's row
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const float sl2 = LOG2E / sqrtf((float)HS);
+        float L2_row = 0.f, D_row = 0.f;
+        float* Ls = reinterpret_cast<float*>(smem + CF::OFF_STATS);  // [2][128] (key-major only)
+        float* Dsm = Ls + 2 * 128;
+        float nL = 0.f, nD = 0.f;  // key-major: this thread's query column of the next tile
+        if (DQ) {
+            // D = rowsum(dO * O) for this row; stored for the key-major kernel
+            if (grow < T) {
+                const bf16* dor = dout + (size_t)(row0 + grow) * C + h * HS;
+                const bf16* orr = outp + (size_t)(row0 + grow) * C + h * HS;
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < HS; i += 8) {
+                    float a[8], c8[8];
+                    Vec8<bf16>::load(dor + i, a);
+                    Vec8<bf16>::load(orr + i, c8);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) acc += a[e] * c8[e];
+                }
+                D_row = acc;
+                Dbuf[(size_t)bh * T + grow] = acc;
+                L2_row = lse[(size_t)bh * T + grow] * LOG2E;
+            }
+        } else {
+            const int q = st0 * 128 + r;
+            nL = q < T ? lse[(size_t)bh * T + q] * LOG2E : INFINITY;  // absent queries: P = 0
+            nD = q < T ? Dbuf[(size_t)bh * T + q] : 0.f;
+        }
+        bool ok = true;
+        for (int n = 0; n < nst && ok; n++) {
+            const int slot = n & 1;
+            if (!DQ) {
+                // every softmax thread writes one query column's L and D, then waits
+                // (bounded) until all 128 have: slot n&1 was last read in tile n-2, which
+                // every thread finished before arriving for tile n-1
+                Ls[slot * 128 + r] = nL;
+                Dsm[slot * 128 + r] = nD;
+                mbar_arrive(&bar->stats[slot]);
+                ok = mbar_wait(&bar->stats[slot], (n >> 1) & 1, abort_flag, flags);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                if (n + 1 < nst) {
+                    const int q = (st0 + n + 1) * 128 + r;
+                    nL = q < T ? lse[(size_t)bh * T + q] * LOG2E : INFINITY;
+                    nD = q < T ? Dbuf[(size_t)bh * T + q] : 0.f;
+                }
+            }
+            const bool diag = (st0 + n) == rt;
+            for (int hh = 0; hh < 2; hh++) {
+                ok = mbar_wait(&bar->sdp_full[hh], n & 1, abort_flag, flags);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t sv[64], dv[64];
+                const uint32_t tS = tmem + lane_off + hh * 128;
+                tmem_ld32_raw(tS, sv);
+                tmem_ld32_raw(tS + 32, sv + 32);
+                tmem_ld32_raw(tS + 64, dv);
+                tmem_ld32_raw(tS + 96, dv + 32);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->sdp_free[hh]);
+                uint32_t pk[32], dk[32];
+                const int cbase = hh * 64;  // column offset of this half within the streamed tile
+#pragma unroll
+                for (int c4 = 0; c4 < 64; c4 += 4) {
+                    float Lc[4], Dc[4];
+                    if (DQ) {
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            Lc[e] = L2_row;
+                            Dc[e] = D_row;
+                        }
+                    } else {
+                        const float4 l4 = *reinterpret_cast<const float4*>(Ls + slot * 128 + cbase + c4);
+                        const float4 d4 = *reinterpret_cast<const float4*>(Dsm + slot * 128 + cbase + c4);
+                        Lc[0] = l4.x; Lc[1] = l4.y; Lc[2] = l4.z; Lc[3] = l4.w;
+                        Dc[0] = d4.x; Dc[1] = d4.y; Dc[2] = d4.z; Dc[3] = d4.w;
+                    }
+                    float pv[4], dsv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int c = cbase + c4 + e;
+                        // causal: key <= query; DQ rows are queries, key-major rows are keys
+                        const bool vis = !diag || (DQ ? c <= r : r <= c);
+                        const float p = vis ? ex2(fmaf(__uint_as_float(sv[c4 + e]), sl2, -Lc[e])) : 0.f;
+                        pv[e] = p;
+                        dsv[e] = p * (__uint_as_float(dv[c4 + e]) - Dc[e]);
+                    }
+                    pk[c4 >> 1] = pack_bf16x2(pv[0], pv[1]);
+                    pk[(c4 >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
+                    dk[c4 >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                    dk[(c4 >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
+                }
+                // the accumulation step of this buffer's previous half has read it
+                ok = mbar_wait(&bar->pds_free[hh], (n & 1) ^ 1, abort_flag, flags);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                if (DQ) {
+                    store_row64(smem + B_PDS + hh * HALF, r, dk);
+                } else {
+                    store_row64(smem + B_PDS + hh * HALF, r, pk);
+                    store_row64(smem + B_PDS + (2 + hh) * HALF, r, dk);
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->pds_full[hh]);
+            }
+        }
+        if (ok) {
+            ok = mbar_wait(&bar->acc_done, 0, abort_flag, flags);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+                const float scale = 1.0f / sqrtf((float)HS);
+                float a[64];
+                tmem_ld32(tmem + lane_off + TB_ACC1, a);
+                tmem_ld32(tmem + lane_off + TB_ACC1 + 32, a + 32);
+                bf16* base = dqkv + (size_t)(row0 + grow) * 3 * C + h * HS;
+                if (grow < T) {
+                    bf16* dst = DQ ? base : base + 2 * C;  // dQ (scaled) or dV
+                    const float mul = DQ ? scale : 1.0f;
+#pragma unroll
+                    for (int i = 0; i < HS; i += 8) {
+                        float y[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e++) y[e] = a[i + e] * mul;
+                        Vec8<bf16>::store(dst + i, y);
+                    }
+                }
+                if (!DQ) {
+                    tmem_ld32(tmem + lane_off + TB_ACC2, a);
+                    tmem_ld32(tmem + lane_off + TB_ACC2 + 32, a + 32);
+                    if (grow < T) {
+#pragma unroll
+                        for (int i = 0; i < HS; i += 8) {
+                            float y[8];
+#pragma unroll
+                            for (int e = 0; e < 8; e++) y[e] = a[i + e] * scale;
+                            Vec8<bf16>::store(base + C + i, y);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TB_COLS);
+}
+
 }  // namespace atc
 
 bool attention_tc_supported(ActType at, int C, int NH, const void* qkv) {
@@ -349,6 +718,33 @@ cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, 
     dim3 grid((T + atc::BQ - 1) / atc::BQ, B * NH);
     if (grid.y > 65535) return cudaErrorInvalidValue;
     G2_LAUNCH atc::attn_fwd_tc_k<<<grid, atc::NTH, atc::FWD_SMEM, s>>>(tm, (bf16*)out, lse, T, C, NH, flags);
+    return cudaGetLastError();
+}
+
+cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv, const void* out, const float* lse,
+                                  int B, int T, int C, int NH, float* Dbuf, int* flags, cudaStream_t s) {
+    CUtensorMap tq, td;
+    if (((uintptr_t)dout & 15) || (C % 8)) return cudaErrorNotSupported;
+    if (!tc::make_map(&tq, qkv, 3ull * C, (uint64_t)B * T, 3ull * C, 64, 128) ||
+        !tc::make_map(&td, dout, (uint64_t)C, (uint64_t)B * T, (uint64_t)C, 64, 128))
+        return cudaErrorNotSupported;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(atc::attn_bwd_tc_k<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             atc::BwdCfg<true>::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(atc::attn_bwd_tc_k<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     atc::BwdCfg<false>::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    dim3 grid((T + 127) / 128, B * NH);
+    if (grid.y > 65535) return cudaErrorInvalidValue;
+    // the query-major kernel also writes D = rowsum(dO * O), which the key-major one reads
+    G2_LAUNCH atc::attn_bwd_tc_k<true><<<grid, atc::NTH, atc::BwdCfg<true>::SMEM, s>>>(
+        tq, td, (bf16*)dqkv, (const bf16*)dout, (const bf16*)out, lse, Dbuf, T, C, NH, flags);
+    G2_LAUNCH atc::attn_bwd_tc_k<false><<<grid, atc::NTH, atc::BwdCfg<false>::SMEM, s>>>(
+        tq, td, (bf16*)dqkv, (const bf16*)dout, (const bf16*)out, lse, Dbuf, T, C, NH, flags);
     return cudaGetLastError();
 }
 

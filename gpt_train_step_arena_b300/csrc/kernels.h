@@ -95,6 +95,10 @@ cudaError_t attention_backward_mma(void* dqkv, const void* dout, const void* qkv
 bool attention_tc_supported(ActType at, int C, int NH, const void* qkv);
 cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, int T, int C, int NH, int* flags,
                                  cudaStream_t s);
+// Its backward: dqkv (B,T,3C) overwritten; Dbuf (B*NH*T floats) receives rowsum(dout * out).
+// cudaErrorNotSupported when the tensor maps cannot be built (caller falls back).
+cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv, const void* out, const float* lse,
+                                  int B, int T, int C, int NH, float* Dbuf, int* flags, cudaStream_t s);
 
 // ---- GEMM --------------------------------------------------------------------------
 // D[m,n] = epilogue( sum_k A(m,k) * B(n,k) ), A(m,k) = A[m*sAm + k*sAk], B(n,k) = B[n*sBn + k*sBk].

@@ -562,7 +562,7 @@ extern "C" int gpt2_backward(gpt2_t* m) {
         // attention
         OP(GPT2_K_ATTN_BWD, 2.0 * attn_fwd_flops(m),
            attention_backward(m->at, m->dqkv, m->datty, qkv, atty, m->lse + l * M * NH, B, T, C, NH,
-                              m->attD, s));
+                              m->attD, s, m->flags));
         // qkv: qkv = ln1 . Wqkv^T + bqkv
         OP(GPT2_K_GEMM, gemm_flops(M, C, 3 * C),
            gemm_dgrad(m, (int)M, 3 * C, C, m->dqkv, pw(m, P_QKVW, (size_t)l * 3 * C * C), m->dln, nullptr));
