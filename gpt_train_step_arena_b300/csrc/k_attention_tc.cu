@@ -34,6 +34,7 @@ namespace atc {
 using namespace tc;
 
 constexpr int HS = 64, BQ = 128, BKV = 128, NTH = 192;
+constexpr int NTH_BWD = 320;  // backward: TMA warp, MMA warp, 8 softmax warps
 constexpr int TILE = 128 * 64 * 2;  // 16 KB: 128 rows of one head, 128-byte rows
 constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 3 * TILE, OFF_P = 5 * TILE, OFF_BAR = 7 * TILE;
 constexpr uint32_t TMEM_COLS = 256, TM_S = 0, TM_O = 128;
@@ -332,55 +333,45 @@ __global__ void __launch_bounds__(NTH, 2)
 // ------------------------------------------------------------------ backward
 // llm.c §1.8 attention_backward, without atomics and without the (T, T) buffers: P is
 // rebuilt from the forward's log-sum-exp L and D = rowsum(dO * O), dS = P * (dP - D).
-// Two kernels of one template, 192 threads, one CTA per SM:
-//   DQ = true   (query-major, runs first): the CTA owns 128 queries of one head, keeps
-//               Q and dO, and streams K_j and V_j for j <= the query tile.  Its softmax
-//               threads first compute D for their own rows (and store it for the other
-//               kernel); then S = Q K^T, dP = dO V^T, dS = P (dP - D), dQ += dS K.
-//   DQ = false  (key-major): the CTA owns 128 keys, keeps K and V, and streams Q_i and
-//               dO_i for i >= the key tile; S^T = K Q^T, dP^T = V dO^T, P^T and
-//               dS^T = P^T (dP^T - D) with L and D of the query columns staged in
-//               shared memory; dV += P^T dO, dK += dS^T Q.
-// Each streamed 128-row tile is processed in two 64-column halves: the two halves' S and
-// dP sit in separate tensor-memory buffers (64 + 64 columns each) and their bf16 P / dS
-// in separate shared-memory buffers, so the products of one half overlap the softmax of
-// the other.  Accumulators (dQ, or dV and dK) stay in tensor memory until the end.
+// Two kernels of one template, 320 threads (TMA warp, MMA warp, 8 softmax warps: two
+// per tensor-memory lane quarter, each taking 32 of a half's 64 columns), one CTA per SM:
+//   DQ = true   (query-major, runs first): the CTA owns 128 queries of one head and
+//               streams K_j and V_j for j <= the query tile.  Its softmax threads first
+//               compute D for their own rows (and store it for the other kernel); then
+//               S = Q K^T, dP = dO V^T, dS = P (dP - D), dQ += dS K.
+//   DQ = false  (key-major): the CTA owns 128 keys and streams Q_i and dO_i for i >= the
+//               key tile; S^T = K Q^T, dP^T = V dO^T, P^T and dS^T = P^T (dP^T - D) with
+//               L and D of the query columns staged in shared memory; dV += P^T dO,
+//               dK += dS^T Q.
+// Operand placement keeps shared-memory traffic to the streamed tiles (the B operands):
+// the CTA's own rows (Q and dO, or K and V) are written into tensor memory once and used
+// as the A operand of the S and dP products; P and dS are written back (bf16) over the
+// S and dP columns each thread has read and used as the A operand of the accumulation
+// products.  Each streamed 128-row tile is processed in two 64-column halves with their
+// own tensor-memory buffers, so one half's products overlap the other half's softmax;
+// the tensor core runs each buffer's accumulation before its next S and dP in issue
+// order.
 struct BwdBars {
-    uint64_t row_full, st_full[2], st_empty[2], sdp_full[2], sdp_free[2], pds_full[2], pds_free[2], stats[2],
-        acc_done, drain;
+    uint64_t row_full, st_full[3], st_empty[3], sdp_full[2], pds_full[2], stats[2], acc_done, drain;
     uint32_t tmem_slot;
     int abort;
 };
-constexpr int HALF = 64 * 128 * 2;  // 16 KB: 128 rows x 64 bf16
-constexpr int B_ROWA = 0, B_ROWB = TILE, B_ST = 2 * TILE;  // stream stages: 2 x (A 16 KB + B 16 KB)
-constexpr int B_PDS = B_ST + 4 * TILE;                     // P / dS half buffers
-template <bool DQ>
-struct BwdCfg {
-    static constexpr int NPDS = DQ ? 1 : 2;               // dS only, or P^T and dS^T
-    static constexpr int OFF_STATS = B_PDS + 2 * NPDS * HALF;  // key-major: L, D of 2 x 128 queries
-    static constexpr int OFF_BAR = OFF_STATS + (DQ ? 0 : 2 * 2 * 128 * 4);
-    static constexpr int SMEM = OFF_BAR + (int)sizeof(BwdBars);
-};
-// tensor memory: S / dP of half h at 128 h (+64), accumulators at 256 (dQ or dV), 320 (dK)
-constexpr uint32_t TB_COLS = 512, TB_ACC1 = 256, TB_ACC2 = 320;
-
-// one 128-byte row of 64 bf16 (packed pairs) into a K-major, 128-byte-swizzled buffer
-G2_DEV void store_row64(uint8_t* buf, int r, const uint32_t* pk) {
-    uint8_t* row = buf + r * 128;
-#pragma unroll
-    for (int ch = 0; ch < 8; ch++)
-        *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-}
+constexpr int NSTAGE = 3;  // streamed 128-row tiles in flight: A (16 KB) + B (16 KB) each
+constexpr int B_STATS = NSTAGE * 2 * TILE;  // key-major: L, D of 2 x 128 query columns
+constexpr int B_BAR = B_STATS + 2 * 2 * 128 * 4;
+constexpr int BWD_SMEM = B_BAR + (int)sizeof(BwdBars);
+// tensor memory: half h's S at 128h, dP at 128h + 64 (P and dS written back over their
+// first 16 + 16 columns per column group); accumulators dQ or dV at 256, dK at 320; the
+// CTA's rows (A operands of S and dP) at 384 and 416
+constexpr uint32_t TB_COLS = 512, TB_ACC1 = 256, TB_ACC2 = 320, TB_RA = 384, TB_RB = 416;
 
 template <bool DQ>
-__global__ void __launch_bounds__(NTH, 1)
+__global__ void __launch_bounds__(NTH_BWD, 1)
     attn_bwd_tc_k(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-                  bf16* dqkv, const bf16* dout, const bf16* outp, const float* lse, float* Dbuf, int T, int C,
-                  int NH, int* flags) {
-    using CF = BwdCfg<DQ>;
+                  bf16* dqkv, const bf16* qkv, const bf16* dout, const bf16* outp, const float* lse, float* Dbuf,
+                  int T, int C, int NH, int* flags) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    BwdBars* bar = reinterpret_cast<BwdBars*>(smem + CF::OFF_BAR);
+    BwdBars* bar = reinterpret_cast<BwdBars*>(smem + B_BAR);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (smem_u32(smem) & 1023) {
         if (threadIdx.x == 0 && flags) atomicOr(flags, G2_FLAG_TIMEOUT);
@@ -393,25 +384,21 @@ __global__ void __launch_bounds__(NTH, 1)
     const int row0 = b * T, r0 = rt * 128;
     // streamed tiles: keys 0..rt (DQ) or queries rt..ntiles_t-1 (key-major)
     const int st0 = DQ ? 0 : rt, nst = DQ ? rt + 1 : ntiles_t - rt;
-    // x coordinates in the tensor maps: the row operands and the streamed operands
-    const int xa_row = DQ ? h * HS : C + h * HS;      // Q or K
-    const int xb_row = DQ ? h * HS : 2 * C + h * HS;  // dO (its own map) or V
-    const int xa_st = DQ ? C + h * HS : h * HS;       // K or Q
-    const int xb_st = DQ ? 2 * C + h * HS : h * HS;   // V or dO (its own map)
-    const CUtensorMap* map_b_row = DQ ? &tm_do : &tm_qkv;
+    const int xa_st = DQ ? C + h * HS : h * HS;      // K or Q (qkv map)
+    const int xb_st = DQ ? 2 * C + h * HS : h * HS;  // V (qkv map) or dO (its own map)
     const CUtensorMap* map_b_st = DQ ? &tm_qkv : &tm_do;
 
     if (threadIdx.x == 0) {
         bar->abort = 0;
-        mbar_init(&bar->row_full, 1);
-        for (int i = 0; i < 2; i++) {
+        mbar_init(&bar->row_full, 8);
+        for (int i = 0; i < NSTAGE; i++) {
             mbar_init(&bar->st_full[i], 1);
             mbar_init(&bar->st_empty[i], 1);
+        }
+        for (int i = 0; i < 2; i++) {
             mbar_init(&bar->sdp_full[i], 1);
-            mbar_init(&bar->sdp_free[i], 4);
-            mbar_init(&bar->pds_full[i], 4);
-            mbar_init(&bar->pds_free[i], 1);
-            mbar_init(&bar->stats[i], 128);
+            mbar_init(&bar->pds_full[i], 8);
+            mbar_init(&bar->stats[i], 256);
         }
         mbar_init(&bar->acc_done, 1);
         mbar_init(&bar->drain, 1);
@@ -428,37 +415,32 @@ __global__ void __launch_bounds__(NTH, 1)
     volatile int* abort_flag = &bar->abort;
 
     if (warp == 0) {
-        // ---------------- TMA producer
+        // ---------------- TMA producer: the streamed tiles
         if (lane == 0) {
-            mbar_expect_tx(&bar->row_full, 2 * TILE);
-            tma_load_2d(&tm_qkv, &bar->row_full, smem + B_ROWA, xa_row, row0 + r0);
-            tma_load_2d(map_b_row, &bar->row_full, smem + B_ROWB, xb_row, row0 + r0);
-            for (int n = 2; n < nst; n++) {
+            for (int n = NSTAGE; n < nst; n++) {
                 tma_prefetch_l2(&tm_qkv, xa_st, row0 + (st0 + n) * 128);
                 tma_prefetch_l2(map_b_st, xb_st, row0 + (st0 + n) * 128);
             }
-            int issued[2] = {-1, -1};
+            int issued[NSTAGE];
+            for (int i = 0; i < NSTAGE; i++) issued[i] = -1;
             bool ok = true;
             for (int n = 0; n < nst; n++) {
-                const int s = n & 1;
-                const uint32_t ph = (n >> 1) & 1;
+                const int s = n % NSTAGE;
+                const uint32_t ph = (n / NSTAGE) & 1;
                 if (!mbar_wait(&bar->st_empty[s], ph ^ 1, abort_flag, flags)) {
                     ok = false;
                     break;
                 }
                 mbar_expect_tx(&bar->st_full[s], 2 * TILE);
-                uint8_t* st = smem + B_ST + s * 2 * TILE;
+                uint8_t* st = smem + s * 2 * TILE;
                 tma_load_2d(&tm_qkv, &bar->st_full[s], st, xa_st, row0 + (st0 + n) * 128);
                 tma_load_2d(map_b_st, &bar->st_full[s], st + TILE, xb_st, row0 + (st0 + n) * 128);
                 issued[s] = (int)ph;
             }
             if (!ok) {
-                unsigned long long t0 = globaltimer();
-                while (!mbar_try_wait(&bar->row_full, 0) && globaltimer() - t0 < TIMEOUT_NS) {
-                }
-                for (int s = 0; s < 2; s++) {
+                for (int s = 0; s < NSTAGE; s++) {
                     if (issued[s] < 0) continue;
-                    t0 = globaltimer();
+                    unsigned long long t0 = globaltimer();
                     while (!mbar_try_wait(&bar->st_full[s], (uint32_t)issued[s]) && globaltimer() - t0 < TIMEOUT_NS) {
                     }
                 }
@@ -469,62 +451,61 @@ __global__ void __launch_bounds__(NTH, 1)
         if (lane == 0) {
             constexpr uint32_t ID_SDP = make_idesc(64, false, false);  // N = 64 streamed rows
             constexpr uint32_t ID_ACC = make_idesc(HS, false, true);   // N = 64, streamed operand MN-major
-            const uint32_t sRA = smem_u32(smem + B_ROWA), sRB = smem_u32(smem + B_ROWB);
-            const uint32_t sPDS = smem_u32(smem + B_PDS);
+            const uint32_t sbase = smem_u32(smem);
+            const int nhalves = 2 * nst;
             bool ok = mbar_wait(&bar->row_full, 0, abort_flag, flags);
             bool issued_any = false;
-            // half g = 2n + hh; its accumulation step runs one half behind its S / dP step
-            const int nhalves = 2 * nst;
-            for (int g = 0; ok && g <= nhalves; g++) {
-                if (g < nhalves) {
-                    const int n = g >> 1, hh = g & 1, s = n & 1;
-                    if ((hh == 0 && !mbar_wait(&bar->st_full[s], (n >> 1) & 1, abort_flag, flags)) ||
-                        !mbar_wait(&bar->sdp_free[hh], (n & 1) ^ 1, abort_flag, flags)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sA = smem_u32(smem + B_ST + s * 2 * TILE) + hh * 8192, sB = sA + TILE;
-                    const uint32_t tS = tmem + hh * 128, tP = tS + 64;
+            // S and dP of half g (tile g/2, columns 64 (g%2) ..): A = the CTA's rows in
+            // tensor memory, B = the streamed rows of the half (K-major)
+            auto issue_sdp = [&](int g) -> bool {
+                const int n = g >> 1, hh = g & 1, s = n % NSTAGE;
+                if (hh == 0 && !mbar_wait(&bar->st_full[s], (n / NSTAGE) & 1, abort_flag, flags)) return false;
+                tc_fence_after();
+                const uint32_t sA = sbase + s * 2 * TILE + hh * 8192, sB = sA + TILE;
+                const uint32_t tS = tmem + hh * 128;
 #pragma unroll
-                    for (int k = 0; k < HS / 16; k++)
-                        umma_bf16(tS, sdesc(sRA + k * 32, 16, 1024), sdesc(sA + k * 32, 16, 1024), ID_SDP,
-                                  k > 0 ? 1u : 0u);
+                for (int k = 0; k < HS / 16; k++)
+                    umma_bf16_ts(tS, tmem + TB_RA + k * 8, sdesc(sA + k * 32, 16, 1024), ID_SDP, k > 0 ? 1u : 0u);
 #pragma unroll
-                    for (int k = 0; k < HS / 16; k++)
-                        umma_bf16(tP, sdesc(sRB + k * 32, 16, 1024), sdesc(sB + k * 32, 16, 1024), ID_SDP,
-                                  k > 0 ? 1u : 0u);
-                    umma_commit(&bar->sdp_full[hh]);
-                    issued_any = true;
+                for (int k = 0; k < HS / 16; k++)
+                    umma_bf16_ts(tS + 64, tmem + TB_RB + k * 8, sdesc(sB + k * 32, 16, 1024), ID_SDP,
+                                 k > 0 ? 1u : 0u);
+                umma_commit(&bar->sdp_full[hh]);
+                issued_any = true;
+                return true;
+            };
+            if (ok) ok = issue_sdp(0);
+            if (ok && nhalves > 1) ok = issue_sdp(1);
+            for (int g = 0; ok && g < nhalves; g++) {
+                const int n = g >> 1, hh = g & 1, s = n % NSTAGE;
+                if (!mbar_wait(&bar->pds_full[hh], n & 1, abort_flag, flags)) {
+                    ok = false;
+                    break;
                 }
-                if (g > 0) {
-                    const int pg = g - 1, n = pg >> 1, hh = pg & 1, s = n & 1;
-                    if (!mbar_wait(&bar->pds_full[hh], n & 1, abort_flag, flags)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // the streamed operands' rows of this half, read N-major (64 hs wide)
-                    const uint32_t sA = smem_u32(smem + B_ST + s * 2 * TILE) + hh * 8192, sB = sA + TILE;
-                    const uint32_t sDS = sPDS + (DQ ? hh : 2 + hh) * HALF;
+                tc_fence_after();
+                // accumulation of half g: A = P or dS in tensor memory (column group c of the
+                // half at 32c, 16 columns = 32 rows of the contraction each), B = the
+                // streamed rows of the half read N-major (64 hs wide)
+                const uint32_t sA = sbase + s * 2 * TILE + hh * 8192, sB = sA + TILE;
+                const uint32_t tH = tmem + hh * 128;
 #pragma unroll
-                    for (int k = 0; k < 64 / 16; k++) {
-                        const uint32_t acc = (pg > 0 || k > 0) ? 1u : 0u;
-                        const uint64_t bA = sdesc(sA + k * 2048, 8192, 1024);
-                        if (DQ) {
-                            umma_bf16(tmem + TB_ACC1, sdesc(sDS + k * 32, 16, 1024), bA, ID_ACC, acc);  // dQ += dS K
-                        } else {
-                            const uint32_t sPT = sPDS + hh * HALF;
-                            const uint64_t bB = sdesc(sB + k * 2048, 8192, 1024);
-                            umma_bf16(tmem + TB_ACC1, sdesc(sPT + k * 32, 16, 1024), bB, ID_ACC, acc);  // dV += P^T dO
-                            umma_bf16(tmem + TB_ACC2, sdesc(sDS + k * 32, 16, 1024), bA, ID_ACC, acc);  // dK += dS^T Q
-                        }
+                for (int k = 0; k < 64 / 16; k++) {
+                    const uint32_t acc = (g > 0 || k > 0) ? 1u : 0u;
+                    const uint32_t a_off = (k >> 1) * 32 + (k & 1) * 8;
+                    const uint64_t bA = sdesc(sA + k * 2048, 8192, 1024);
+                    if (DQ) {
+                        umma_bf16_ts(tmem + TB_ACC1, tH + 64 + a_off, bA, ID_ACC, acc);  // dQ += dS K
+                    } else {
+                        const uint64_t bB = sdesc(sB + k * 2048, 8192, 1024);
+                        umma_bf16_ts(tmem + TB_ACC1, tH + a_off, bB, ID_ACC, acc);       // dV += P^T dO
+                        umma_bf16_ts(tmem + TB_ACC2, tH + 64 + a_off, bA, ID_ACC, acc);  // dK += dS^T Q
                     }
-                    umma_commit(&bar->pds_free[hh]);
-                    if (hh == 1) umma_commit(&bar->st_empty[s]);
-                    if (pg == nhalves - 1) umma_commit(&bar->acc_done);
-                    issued_any = true;
                 }
+                issued_any = true;
+                if (hh == 1) umma_commit(&bar->st_empty[s]);
+                if (g == nhalves - 1) umma_commit(&bar->acc_done);
+                // the same buffer's next S and dP follow this accumulation on the tensor core
+                if (g + 2 < nhalves && !issue_sdp(g + 2)) ok = false;
             }
             if (!ok && issued_any) {
                 umma_commit(&bar->drain);
@@ -534,34 +515,59 @@ __global__ void __launch_bounds__(NTH, 1)
             }
         }
     } else {
-        // ---------------- softmax warps 2..5: thread = row of the CTA's tile
-        const int quarter = warp & 3, r = quarter * 32 + lane;
+        // ---------------- softmax warps 2..9: thread = row of the CTA's tile; warps 2-5
+        // take columns 0-31 of each half, warps 6-9 columns 32-63
+        const int quarter = warp & 3, r = quarter * 32 + lane, sub = (warp - 2) >> 2;
         const int grow = r0 + r;  // query (DQ) or key position of this thread's row
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = LOG2E / sqrtf((float)HS);
         float L2_row = 0.f, D_row = 0.f;
-        float* Ls = reinterpret_cast<float*>(smem + CF::OFF_STATS);  // [2][128] (key-major only)
+        float* Ls = reinterpret_cast<float*>(smem + B_STATS);  // [2][128] (key-major only)
         float* Dsm = Ls + 2 * 128;
         float nL = 0.f, nD = 0.f;  // key-major: this thread's query column of the next tile
+        {
+            // this row of the CTA's two A operands into tensor memory: group 0 writes Q (DQ)
+            // or K, group 1 dO or V; 64 bf16 = 32 packed columns
+            uint32_t rv[32];
+            const bf16* src;
+            if (DQ)
+                src = sub == 0 ? qkv + (size_t)(row0 + grow) * 3 * C + h * HS : dout + (size_t)(row0 + grow) * C + h * HS;
+            else
+                src = qkv + (size_t)(row0 + grow) * 3 * C + (sub == 0 ? C : 2 * C) + h * HS;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const uint4 u = grow < T ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0, 0, 0, 0);
+                rv[4 * i] = u.x;
+                rv[4 * i + 1] = u.y;
+                rv[4 * i + 2] = u.z;
+                rv[4 * i + 3] = u.w;
+            }
+            tmem_st32u(tmem + lane_off + (sub == 0 ? TB_RA : TB_RB), rv);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->row_full);
+        }
         if (DQ) {
-            // D = rowsum(dO * O) for this row; stored for the key-major kernel
+            // D = rowsum(dO * O) for this row (both column groups need it; group 0 stores
+            // it for the key-major kernel)
             if (grow < T) {
                 const bf16* dor = dout + (size_t)(row0 + grow) * C + h * HS;
                 const bf16* orr = outp + (size_t)(row0 + grow) * C + h * HS;
                 float acc = 0.f;
 #pragma unroll
                 for (int i = 0; i < HS; i += 8) {
-                    float a[8], c8[8];
-                    Vec8<bf16>::load(dor + i, a);
+                    float a8[8], c8[8];
+                    Vec8<bf16>::load(dor + i, a8);
                     Vec8<bf16>::load(orr + i, c8);
 #pragma unroll
-                    for (int e = 0; e < 8; e++) acc += a[e] * c8[e];
+                    for (int e = 0; e < 8; e++) acc += a8[e] * c8[e];
                 }
                 D_row = acc;
-                Dbuf[(size_t)bh * T + grow] = acc;
+                if (sub == 0) Dbuf[(size_t)bh * T + grow] = acc;
                 L2_row = lse[(size_t)bh * T + grow] * LOG2E;
             }
-        } else {
+        } else if (sub == 0) {
             const int q = st0 * 128 + r;
             nL = q < T ? lse[(size_t)bh * T + q] * LOG2E : INFINITY;  // absent queries: P = 0
             nD = q < T ? Dbuf[(size_t)bh * T + q] : 0.f;
@@ -570,18 +576,20 @@ __global__ void __launch_bounds__(NTH, 1)
         for (int n = 0; n < nst && ok; n++) {
             const int slot = n & 1;
             if (!DQ) {
-                // every softmax thread writes one query column's L and D, then waits
-                // (bounded) until all 128 have: slot n&1 was last read in tile n-2, which
-                // every thread finished before arriving for tile n-1
-                Ls[slot * 128 + r] = nL;
-                Dsm[slot * 128 + r] = nD;
+                // column group 0 writes one query column's L and D each; everyone waits
+                // (bounded) until all have: slot n&1 was last read in tile n-2, which every
+                // thread finished before arriving for tile n-1
+                if (sub == 0) {
+                    Ls[slot * 128 + r] = nL;
+                    Dsm[slot * 128 + r] = nD;
+                }
                 mbar_arrive(&bar->stats[slot]);
                 ok = mbar_wait(&bar->stats[slot], (n >> 1) & 1, abort_flag, flags);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
-                if (n + 1 < nst) {
+                if (sub == 0 && n + 1 < nst) {
                     const int q = (st0 + n + 1) * 128 + r;
                     nL = q < T ? lse[(size_t)bh * T + q] * LOG2E : INFINITY;
                     nD = q < T ? Dbuf[(size_t)bh * T + q] : 0.f;
@@ -595,20 +603,15 @@ __global__ void __launch_bounds__(NTH, 1)
                     break;
                 }
                 tc_fence_after();
-                uint32_t sv[64], dv[64];
-                const uint32_t tS = tmem + lane_off + hh * 128;
+                uint32_t sv[32], dv[32];
+                const uint32_t tS = tmem + lane_off + hh * 128 + sub * 32;
                 tmem_ld32_raw(tS, sv);
-                tmem_ld32_raw(tS + 32, sv + 32);
                 tmem_ld32_raw(tS + 64, dv);
-                tmem_ld32_raw(tS + 96, dv + 32);
                 tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar->sdp_free[hh]);
-                uint32_t pk[32], dk[32];
-                const int cbase = hh * 64;  // column offset of this half within the streamed tile
+                uint32_t pk[16], dk[16];
+                const int cbase = hh * 64 + sub * 32;  // column offset within the streamed tile
 #pragma unroll
-                for (int c4 = 0; c4 < 64; c4 += 4) {
+                for (int c4 = 0; c4 < 32; c4 += 4) {
                     float Lc[4], Dc[4];
                     if (DQ) {
 #pragma unroll
@@ -628,28 +631,19 @@ __global__ void __launch_bounds__(NTH, 1)
                         const int c = cbase + c4 + e;
                         // causal: key <= query; DQ rows are queries, key-major rows are keys
                         const bool vis = !diag || (DQ ? c <= r : r <= c);
-                        const float p = vis ? ex2(fmaf(__uint_as_float(sv[c4 + e]), sl2, -Lc[e])) : 0.f;
-                        pv[e] = p;
-                        dsv[e] = p * (__uint_as_float(dv[c4 + e]) - Dc[e]);
+                        const float pr = vis ? ex2(fmaf(__uint_as_float(sv[c4 + e]), sl2, -Lc[e])) : 0.f;
+                        pv[e] = pr;
+                        dsv[e] = pr * (__uint_as_float(dv[c4 + e]) - Dc[e]);
                     }
                     pk[c4 >> 1] = pack_bf16x2(pv[0], pv[1]);
                     pk[(c4 >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
                     dk[c4 >> 1] = pack_bf16x2(dsv[0], dsv[1]);
                     dk[(c4 >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
                 }
-                // the accumulation step of this buffer's previous half has read it
-                ok = mbar_wait(&bar->pds_free[hh], (n & 1) ^ 1, abort_flag, flags);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                if (DQ) {
-                    store_row64(smem + B_PDS + hh * HALF, r, dk);
-                } else {
-                    store_row64(smem + B_PDS + hh * HALF, r, pk);
-                    store_row64(smem + B_PDS + (2 + hh) * HALF, r, dk);
-                }
-                fence_async_smem();
+                // P (key-major only) and dS over the first 16 of the 32 columns just read
+                if (!DQ) tmem_st16(tS, pk);
+                tmem_st16(tS + 64, dk);
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar->pds_full[hh]);
@@ -660,31 +654,27 @@ __global__ void __launch_bounds__(NTH, 1)
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 const float scale = 1.0f / sqrtf((float)HS);
-                float a[64];
-                tmem_ld32(tmem + lane_off + TB_ACC1, a);
-                tmem_ld32(tmem + lane_off + TB_ACC1 + 32, a + 32);
                 bf16* base = dqkv + (size_t)(row0 + grow) * 3 * C + h * HS;
-                if (grow < T) {
-                    bf16* dst = DQ ? base : base + 2 * C;  // dQ (scaled) or dV
-                    const float mul = DQ ? scale : 1.0f;
-#pragma unroll
-                    for (int i = 0; i < HS; i += 8) {
-                        float y[8];
-#pragma unroll
-                        for (int e = 0; e < 8; e++) y[e] = a[i + e] * mul;
-                        Vec8<bf16>::store(dst + i, y);
-                    }
+                // DQ: group g stores dQ columns 32g..32g+31; key-major: group 0 dV, group 1 dK
+                float a[64];
+                if (DQ) {
+                    tmem_ld32(tmem + lane_off + TB_ACC1 + sub * 32, a);
+                } else {
+                    const uint32_t t0 = tmem + lane_off + (sub ? TB_ACC2 : TB_ACC1);
+                    tmem_ld32(t0, a);
+                    tmem_ld32(t0 + 32, a + 32);
                 }
-                if (!DQ) {
-                    tmem_ld32(tmem + lane_off + TB_ACC2, a);
-                    tmem_ld32(tmem + lane_off + TB_ACC2 + 32, a + 32);
-                    if (grow < T) {
+                if (grow < T) {
+                    const int ncol = DQ ? 32 : 64;
+                    bf16* dst = DQ ? base + sub * 32 : (sub ? base + C : base + 2 * C);
+                    const float mul = (DQ || sub) ? scale : 1.0f;
 #pragma unroll
-                        for (int i = 0; i < HS; i += 8) {
+                    for (int i = 0; i < 64; i += 8) {
+                        if (i < ncol) {
                             float y[8];
 #pragma unroll
-                            for (int e = 0; e < 8; e++) y[e] = a[i + e] * scale;
-                            Vec8<bf16>::store(base + C + i, y);
+                            for (int e = 0; e < 8; e++) y[e] = a[i + e] * mul;
+                            Vec8<bf16>::store(dst + i, y);
                         }
                     }
                 }
@@ -724,27 +714,28 @@ cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, 
 cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv, const void* out, const float* lse,
                                   int B, int T, int C, int NH, float* Dbuf, int* flags, cudaStream_t s) {
     CUtensorMap tq, td;
-    if (((uintptr_t)dout & 15) || (C % 8)) return cudaErrorNotSupported;
+    if (((uintptr_t)dout & 15) || ((uintptr_t)out & 15) || ((uintptr_t)dqkv & 15) || (C % 8))
+        return cudaErrorNotSupported;
     if (!tc::make_map(&tq, qkv, 3ull * C, (uint64_t)B * T, 3ull * C, 64, 128) ||
         !tc::make_map(&td, dout, (uint64_t)C, (uint64_t)B * T, (uint64_t)C, 64, 128))
         return cudaErrorNotSupported;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(atc::attn_bwd_tc_k<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             atc::BwdCfg<true>::SMEM);
+                                             atc::BWD_SMEM);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(atc::attn_bwd_tc_k<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     atc::BwdCfg<false>::SMEM);
+                                     atc::BWD_SMEM);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
     dim3 grid((T + 127) / 128, B * NH);
     if (grid.y > 65535) return cudaErrorInvalidValue;
     // the query-major kernel also writes D = rowsum(dO * O), which the key-major one reads
-    G2_LAUNCH atc::attn_bwd_tc_k<true><<<grid, atc::NTH, atc::BwdCfg<true>::SMEM, s>>>(
-        tq, td, (bf16*)dqkv, (const bf16*)dout, (const bf16*)out, lse, Dbuf, T, C, NH, flags);
-    G2_LAUNCH atc::attn_bwd_tc_k<false><<<grid, atc::NTH, atc::BwdCfg<false>::SMEM, s>>>(
-        tq, td, (bf16*)dqkv, (const bf16*)dout, (const bf16*)out, lse, Dbuf, T, C, NH, flags);
+    G2_LAUNCH atc::attn_bwd_tc_k<true><<<grid, atc::NTH_BWD, atc::BWD_SMEM, s>>>(
+        tq, td, (bf16*)dqkv, (const bf16*)qkv, (const bf16*)dout, (const bf16*)out, lse, Dbuf, T, C, NH, flags);
+    G2_LAUNCH atc::attn_bwd_tc_k<false><<<grid, atc::NTH_BWD, atc::BWD_SMEM, s>>>(
+        tq, td, (bf16*)dqkv, (const bf16*)qkv, (const bf16*)dout, (const bf16*)out, lse, Dbuf, T, C, NH, flags);
     return cudaGetLastError();
 }
 

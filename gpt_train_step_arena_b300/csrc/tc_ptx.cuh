@@ -48,12 +48,26 @@ G2_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait on phase `parity`.  Returns false (and raises the CTA-wide abort and
 // the global timeout flag) if it does not complete within TIMEOUT_NS, or if another
 // role of the CTA has already aborted.
+// As mbar_try_wait, but the thread may be suspended (no issue slots used) until the
+// phase completes or about `ns` nanoseconds pass.
+G2_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 G2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* flags) {
     if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = globaltimer();
     while (true) {
-        for (int i = 0; i < 64; i++)
-            if (mbar_try_wait(bar, parity)) return true;
+        for (int i = 0; i < 16; i++)
+            if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
         if (*abort_flag) return false;
         if (globaltimer() - t0 > TIMEOUT_NS) {
             *abort_flag = 1;
@@ -157,6 +171,39 @@ G2_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "
 // Makes this thread's generic-proxy shared-memory writes visible to the async proxy
 // (the tensor core reads operands through it).
 G2_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// D (tensor memory) (+)= A (tensor memory) . B (shared-memory descriptor), kind::f16.
+// A occupies 128 lanes (row m in lane m) and K/2 columns, two 16-bit elements per column.
+G2_DEV void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's lane from registers.
+G2_DEV void tmem_st16(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+// 32 consecutive 32-bit columns of this thread's lane from registers (raw bits).
+G2_DEV void tmem_st32u(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
 
 // Shared-memory matrix descriptor: 128-byte swizzle, Blackwell descriptor version 1.
 G2_DEV uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
