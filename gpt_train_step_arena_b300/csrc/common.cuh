@@ -80,6 +80,29 @@ G2_DEV float gelu_tanh_grad(float x) {
     return 0.5f * (1.0f + th) + x * 0.5f * sech2 * k * (1.0f + 3.0f * 0.044715f * x * x);
 }
 
+// tanh through the identity tanh(u) = 1 - 2 / (e^{2u} + 1), with the hardware base-2
+// exponential and reciprocal approximations: absolute error a few 1e-7, far below a bf16
+// rounding; used where the result is rounded to bf16 (the tensor-core GEMM epilogues).
+// Saturates correctly: e^{2u} -> inf gives 1, e^{2u} -> 0 gives -1.
+G2_DEV float tanh_via_exp2(float u) {
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(u * 2.8853900817779268f));  // 2 log2(e) u
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(e + 1.0f));
+    return fmaf(-2.0f, r, 1.0f);
+}
+G2_DEV float gelu_tanh_fast(float x) {
+    const float k = 0.7978845608028654f;
+    float u = k * (x + 0.044715f * x * x * x);
+    return 0.5f * x * (1.0f + tanh_via_exp2(u));
+}
+G2_DEV float gelu_tanh_grad_fast(float x) {
+    const float k = 0.7978845608028654f;
+    float u = k * (x + 0.044715f * x * x * x);
+    float th = tanh_via_exp2(u);
+    float sech2 = 1.0f - th * th;
+    return 0.5f * (1.0f + th) + x * 0.5f * sech2 * k * (1.0f + 3.0f * 0.044715f * x * x);
+}
+
 // Device-side error flags (bitwise OR into one int): never trap, the host reads them.
 enum {
     G2_FLAG_BAD_TOKEN = 1,

@@ -7,17 +7,22 @@
 //   dgrad    dY.W    A K-major, B N-major      (optionally times GELU'(pre-activation))
 //   wgrad    dY^T.X  A M-major, B N-major      (fp32 out; split-K with a fixed-order sum)
 //
-// Structure (one persistent CTA per SM, 192 threads):
-//   warp 0    TMA producer: one elected lane streams 128 x 64 (A) and BN x 64 (B)
-//             bf16 tiles into a ring of shared-memory stages (128-byte swizzle).
-//   warp 1    allocates tensor memory; one lane issues tcgen05.mma (M=128, N=BN, K=16)
-//             into one of two fp32 accumulators (2 x BN columns) and commits to
+// Structure (one persistent CTA per SM, 320 threads).  A tile is 256 rows x BN columns:
+// two 128-row halves that share every B stage, so each SM receives 64 KB of operands per
+// 1024 clocks of BN = 256 tensor work -- the rate its TMA ingress sustains (about 64
+// bytes per clock); 128-row tiles would need 1.5 x that.
+//   warp 0    TMA producer: one elected lane streams the 256 x 64 (A) and BN x 64 (B)
+//             bf16 tiles of each K block into a ring of shared-memory stages (128-byte
+//             swizzle).
+//   warp 1    allocates all 512 tensor-memory columns; one lane issues tcgen05.mma
+//             (M = 128 per half, N = BN, K = 16) into the tile's two fp32 accumulator
+//             halves (2 x BN columns; two such buffers when BN = 128) and commits to
 //             mbarriers that free the stage / publish the accumulator.
-//   warps 2-5 epilogue: tcgen05.ld of their 32 accumulator lanes, fused epilogue
-//             math, bf16/fp32 stores; then release the accumulator.
-// The two accumulators let the epilogue of one tile overlap the main loop of the
-// next.  Every mbarrier wait is bounded (about 2 s): on expiry the kernel raises a
-// flag, drains what it issued and returns instead of hanging.
+//   warps 2-9 epilogue, warps 2-5 for the first half and 6-9 for the second (each warp one
+//             32-lane quarter): tcgen05.ld, fused epilogue math, bf16/fp32 stores; then
+//             release the accumulator.
+// Every mbarrier wait is bounded (about 2 s): on expiry the kernel raises a flag, drains
+// what it issued and returns instead of hanging.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -31,15 +36,14 @@
 namespace g2 {
 namespace tc {
 
-constexpr int BM = 128, BK = 64, UMMA_K = 16;
-constexpr int NTHREADS = 192;
-constexpr int GROUP_M = 16;  // tile order: m fastest within groups of GROUP_M row tiles
+constexpr int BM = 128, BK = 64, UMMA_K = 16;  // rows per MMA (one accumulator half)
+constexpr int GROUP_M = 8;     // tile order: m fastest within groups of GROUP_M row tiles
 
 enum { E_STORE = 0, E_GELU = 1, E_GELU_BWD = 2, E_PARTIAL = 3 };
 
 struct Params {
     int M, N, K;
-    int tiles_m, tiles_n, splits, kb_per_split, num_kb, num_units;
+    int tiles_m, tiles_n, splits, kb_per_split, num_kb, num_units;  // units: (row tile, col tile, split)
     void* D;
     long long ldd;
     int d_f32;
@@ -54,16 +58,23 @@ struct Params {
     int* flags;
 };
 
-template <int BN>
+template <int BN, int BMT>
 struct Cfg {
-    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int HALVES = BMT / BM;                 // 128-row accumulator halves per tile
+    static constexpr int EPI_WARPS = 4 * HALVES;            // one per 32-lane quarter per half
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;     // + TMA warp + MMA warp
+    static constexpr int A_BYTES = BMT * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
-    static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;  // 3 to 6 stages, 192 KB
+    static constexpr int ACC_COLS = HALVES * BN;
+    static constexpr int ACC_BUFS = (512 / ACC_COLS) >= 2 ? 2 : 1;
+    static constexpr int TMEM_COLS = 512;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
 
+// Work unit u: row tile m_blk (BMT rows), column tile n_blk, K split `split`.  Row tiles
+// run fastest within groups of GROUP_M, so concurrently running CTAs share B tiles in L2.
 G2_DEV void unit_coords(const Params& p, int u, int& m_blk, int& n_blk, int& split) {
     int per = p.tiles_m * p.tiles_n;
     split = u / per;
@@ -105,11 +116,11 @@ G2_DEV void epilogue_chunk(const Params& p, const float* acc, int gm, int gn0, i
                 float x[8];
                 Vec8<bf16>::load(pre + i, x);
 #pragma unroll
-                for (int j = 0; j < 8; j++) v[i + j] *= gelu_tanh_grad(x[j]);
+                for (int j = 0; j < 8; j++) v[i + j] *= gelu_tanh_grad_fast(x[j]);
             }
         } else {
             for (int i = 0; i < 32; i++)
-                if (gn0 + i < N) v[i] *= gelu_tanh_grad(__bfloat162float(pre[i]));
+                if (gn0 + i < N) v[i] *= gelu_tanh_grad_fast(__bfloat162float(pre[i]));
         }
     } else {
         if (p.bias) {
@@ -163,7 +174,7 @@ G2_DEV void epilogue_chunk(const Params& p, const float* acc, int gm, int gn0, i
     if (EPI == E_GELU) {
         float gv[32];
 #pragma unroll
-        for (int i = 0; i < 32; i++) gv[i] = gelu_tanh(v[i]);
+        for (int i = 0; i < 32; i++) gv[i] = gelu_tanh_fast(v[i]);
         bf16* dst = p.D2 + (size_t)gm * p.ldd2 + gn0;
         if (full) {
 #pragma unroll
@@ -176,21 +187,21 @@ G2_DEV void epilogue_chunk(const Params& p, const float* acc, int gm, int gn0, i
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int BN, bool A_MN, bool B_MN, int EPI>
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <int BN, int BMT, bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(Cfg<BN, BMT>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const Params p) {
-    using CF = Cfg<BN>;
-    constexpr int S = CF::STAGES;
+    using CF = Cfg<BN, BMT>;
+    constexpr int S = CF::STAGES, NB = CF::ACC_BUFS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(smem + S * CF::STAGE_BYTES);
-    uint64_t* full_bar = bars;            // [S]
-    uint64_t* empty_bar = bars + S;       // [S]
-    uint64_t* tfull_bar = bars + 2 * S;   // [2]
-    uint64_t* tempty_bar = bars + 2 * S + 2;  // [2]
-    uint64_t* drain_bar = bars + 2 * S + 4;   // [1]
-    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * S + 5);
+    uint64_t* full_bar = bars;                  // [S]
+    uint64_t* empty_bar = bars + S;             // [S]
+    uint64_t* tfull_bar = bars + 2 * S;         // [NB]
+    uint64_t* tempty_bar = bars + 2 * S + NB;   // [NB]
+    uint64_t* drain_bar = bars + 2 * S + 2 * NB;
+    uint32_t* tmem_slot = (uint32_t*)(drain_bar + 1);
     __shared__ int s_abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -200,9 +211,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&full_bar[i], 1);
             mbar_init(&empty_bar[i], 1);
         }
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < NB; i++) {
             mbar_init(&tfull_bar[i], 1);
-            mbar_init(&tempty_bar[i], 4);
+            mbar_init(&tempty_bar[i], CF::EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -239,11 +250,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     mbar_expect_tx(&full_bar[stage], CF::STAGE_BYTES);
                     const int k0 = kb * BK;
                     if (!A_MN) {
-                        tma_load_2d(&tmA, &full_bar[stage], sa, k0, mb * BM);
+                        tma_load_2d(&tmA, &full_bar[stage], sa, k0, mb * BMT);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BM / 64; j++)
-                            tma_load_2d(&tmA, &full_bar[stage], sa + j * 64 * BK * 2, mb * BM + 64 * j, k0);
+                        for (int j = 0; j < BMT / 64; j++)
+                            tma_load_2d(&tmA, &full_bar[stage], sa + j * 64 * BK * 2, mb * BMT + 64 * j, k0);
                     }
                     if (!B_MN) {
                         tma_load_2d(&tmB, &full_bar[stage], sb, k0, nb * BN);
@@ -289,7 +300,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * CF::ACC_COLS);
                 for (int kb = kb0; kb < kb1; kb++) {
                     if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.flags)) {
                         ok = false;
@@ -299,17 +310,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t sa = smem_u32(smem + stage * CF::STAGE_BYTES);
                     const uint32_t sb = sa + CF::A_BYTES;
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; k++) {
-                        uint64_t ad, bd;
-                        if (!A_MN)
-                            ad = sdesc(sa + k * UMMA_K * 2, 16, 1024);
-                        else
-                            ad = sdesc(sa + k * UMMA_K * 128, 64 * BK * 2, 1024);
-                        if (!B_MN)
-                            bd = sdesc(sb + k * UMMA_K * 2, 16, 1024);
-                        else
-                            bd = sdesc(sb + k * UMMA_K * 128, 64 * BK * 2, 1024);
-                        umma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                    for (int hh = 0; hh < CF::HALVES; hh++) {
+                        // rows 128 hh.. of the tile: 16 KB into the A stage in either layout
+                        const uint32_t sah = sa + hh * (BM * BK * 2);
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; k++) {
+                            uint64_t ad, bd;
+                            if (!A_MN)
+                                ad = sdesc(sah + k * UMMA_K * 2, 16, 1024);
+                            else
+                                ad = sdesc(sah + k * UMMA_K * 128, 64 * BK * 2, 1024);
+                            if (!B_MN)
+                                bd = sdesc(sb + k * UMMA_K * 2, 16, 1024);
+                            else
+                                bd = sdesc(sb + k * UMMA_K * 128, 64 * BK * 2, 1024);
+                            umma_bf16(d_tmem + hh * BN, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     issued_any = true;
                     umma_commit(&empty_bar[stage]);
@@ -320,7 +336,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 if (!ok) break;
                 umma_commit(&tfull_bar[acc]);
-                if (++acc == 2) {
+                if (++acc == NB) {
                     acc = 0;
                     acc_phase ^= 1;
                 }
@@ -334,9 +350,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
     } else {
-        // ---------------- epilogue warps 2..5
+        // ---------------- epilogue warps: warps 2-5 drain the first 128-row half of the tile,
+        // warps 6-9 (256-row tiles) the second; each warp its 32-lane quarter, all BN columns
         const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
-        const int row_in_tile = quarter * 32 + lane;
+        const int hh = (warp - 2) >> 2;
+        const int row_in_tile = hh * BM + quarter * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
@@ -345,8 +363,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             bool ok = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.flags);
             if (!__all_sync(0xffffffffu, ok)) break;  // the warp leaves together
             tc_fence_after();
-            const int gm = mb * BM + row_in_tile;
-            const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+            const int gm = mb * BMT + row_in_tile;
+            const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * CF::ACC_COLS + hh * BN);
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 float v[32];
@@ -357,7 +375,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty_bar[acc]);
-            if (++acc == 2) {
+            if (++acc == NB) {
                 acc = 0;
                 acc_phase ^= 1;
             }
@@ -392,27 +410,34 @@ static int num_sms() {
     return n;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
+template <int BN, int BMT, bool A_MN, bool B_MN, int EPI>
 static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, cudaStream_t s) {
-    auto kern = gemm_tc_kernel<BN, A_MN, B_MN, EPI>;
+    using CF = Cfg<BN, BMT>;
+    auto kern = gemm_tc_kernel<BN, BMT, A_MN, B_MN, EPI>;
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
     int grid = std::min(p.num_units, num_sms());
-    G2_LAUNCH kern<<<grid, NTHREADS, Cfg<BN>::SMEM_BYTES, s>>>(ta, tb, p);
+    G2_LAUNCH kern<<<grid, CF::THREADS, CF::SMEM_BYTES, s>>>(ta, tb, p);
     return cudaGetLastError();
 }
 
 template <int BN, int EPI>
-static cudaError_t launch_layout(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+static cudaError_t launch_layout(int bmt, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                                  const Params& p, cudaStream_t s) {
-    if (!a_mn && !b_mn) return launch_t<BN, false, false, EPI>(ta, tb, p, s);
-    if (!a_mn && b_mn) return launch_t<BN, false, true, EPI>(ta, tb, p, s);
-    if (a_mn && b_mn) return launch_t<BN, true, true, EPI>(ta, tb, p, s);
-    return launch_t<BN, true, false, EPI>(ta, tb, p, s);
+    if (bmt == 256) {
+        if (!a_mn && !b_mn) return launch_t<BN, 256, false, false, EPI>(ta, tb, p, s);
+        if (!a_mn && b_mn) return launch_t<BN, 256, false, true, EPI>(ta, tb, p, s);
+        if (a_mn && b_mn) return launch_t<BN, 256, true, true, EPI>(ta, tb, p, s);
+        return launch_t<BN, 256, true, false, EPI>(ta, tb, p, s);
+    }
+    if (!a_mn && !b_mn) return launch_t<BN, 128, false, false, EPI>(ta, tb, p, s);
+    if (!a_mn && b_mn) return launch_t<BN, 128, false, true, EPI>(ta, tb, p, s);
+    if (a_mn && b_mn) return launch_t<BN, 128, true, true, EPI>(ta, tb, p, s);
+    return launch_t<BN, 128, true, false, EPI>(ta, tb, p, s);
 }
 
 }  // namespace tc
@@ -433,9 +458,19 @@ static int* fallback_flag() {
     return ptr;
 }
 
+// Tile height: 256-row tiles halve the operand bytes each SM receives per FLOP for B but
+// leave no room in tensor memory for a second accumulator, so their epilogue does not
+// overlap the next tile; they pay off for long K (many K blocks per tile) when there are
+// plenty of tiles.  Otherwise 128-row tiles with double-buffered accumulators.
+static int tile_rows(int M, int N, int K, int BN) {
+    const long long tiles128 = (long long)((M + 127) / 128) * ((N + BN - 1) / BN);
+    return (K >= 2048 && tiles128 >= 4LL * num_sms()) ? 256 : 128;
+}
+
 // Split-K plan for a product with few output tiles and a long K.
 static void plan(int M, int N, int K, int BN, int& splits, int& kb_per) {
-    int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int bmt = tile_rows(M, N, K, BN);
+    int tiles = ((M + bmt - 1) / bmt) * ((N + BN - 1) / BN);
     int num_kb = (K + BK - 1) / BK;
     int sms = num_sms();
     splits = 1;
@@ -475,10 +510,11 @@ bool gemm_tc_supported(const GemmArgs& a) {
 cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, cudaStream_t s) {
     const bool a_mn = a.sAk != 1, b_mn = a.sBk != 1;
     const int BN = a.N > 128 ? 256 : 128;
+    const int bmt = tile_rows(a.M, a.N, a.K, BN);
     CUtensorMap ta, tb;
     bool ok;
     if (!a_mn)
-        ok = make_map(&ta, a.A, a.K, a.M, a.sAm, BK, BM);
+        ok = make_map(&ta, a.A, a.K, a.M, a.sAm, BK, bmt);
     else
         ok = make_map(&ta, a.A, a.M, a.K, a.sAk, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
@@ -490,7 +526,7 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
 
     Params p{};
     p.M = a.M; p.N = a.N; p.K = a.K;
-    p.tiles_m = (a.M + BM - 1) / BM;
+    p.tiles_m = (a.M + bmt - 1) / bmt;
     p.tiles_n = (a.N + BN - 1) / BN;
     p.num_kb = (a.K + BK - 1) / BK;
     int splits = 1, kb_per = p.num_kb;
@@ -512,8 +548,8 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
 
     cudaError_t e;
     if (splits > 1) {
-        e = BN == 256 ? launch_layout<256, E_PARTIAL>(a_mn, b_mn, ta, tb, p, s)
-                      : launch_layout<128, E_PARTIAL>(a_mn, b_mn, ta, tb, p, s);
+        e = BN == 256 ? launch_layout<256, E_PARTIAL>(bmt, a_mn, b_mn, ta, tb, p, s)
+                      : launch_layout<128, E_PARTIAL>(bmt, a_mn, b_mn, ta, tb, p, s);
         if (e != cudaSuccess) return e;
         size_t n = (size_t)a.M * a.N;
         unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
@@ -522,14 +558,14 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
     }
     switch (a.epi) {
         case EPI_GELU:
-            return BN == 256 ? launch_layout<256, E_GELU>(a_mn, b_mn, ta, tb, p, s)
-                             : launch_layout<128, E_GELU>(a_mn, b_mn, ta, tb, p, s);
+            return BN == 256 ? launch_layout<256, E_GELU>(bmt, a_mn, b_mn, ta, tb, p, s)
+                             : launch_layout<128, E_GELU>(bmt, a_mn, b_mn, ta, tb, p, s);
         case EPI_GELU_BWD:
-            return BN == 256 ? launch_layout<256, E_GELU_BWD>(a_mn, b_mn, ta, tb, p, s)
-                             : launch_layout<128, E_GELU_BWD>(a_mn, b_mn, ta, tb, p, s);
+            return BN == 256 ? launch_layout<256, E_GELU_BWD>(bmt, a_mn, b_mn, ta, tb, p, s)
+                             : launch_layout<128, E_GELU_BWD>(bmt, a_mn, b_mn, ta, tb, p, s);
         default:
-            return BN == 256 ? launch_layout<256, E_STORE>(a_mn, b_mn, ta, tb, p, s)
-                             : launch_layout<128, E_STORE>(a_mn, b_mn, ta, tb, p, s);
+            return BN == 256 ? launch_layout<256, E_STORE>(bmt, a_mn, b_mn, ta, tb, p, s)
+                             : launch_layout<128, E_STORE>(bmt, a_mn, b_mn, ta, tb, p, s);
     }
 }
 
