@@ -8,6 +8,7 @@
 #include "kernels.h"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace g2 {
 
@@ -375,30 +376,39 @@ cudaError_t layernorm_forward(ActType at, void* out, float* mean, float* rstd, c
     return cudaGetLastError();
 }
 
+cudaError_t colsum(ActType at, float* out, const void* X, int M, int N, float* part, cudaStream_t s);
+
 // ------------------------------------------------------------------ layernorm backward
 // llm.c §1.4.  One warp per row; dres += dinp (the residual-stream accumulation of
 // llm.c §1.12 fused in).  dw/db: each warp sums its rows, the block adds its warps in
 // order into part[block][C] (dw) and part[nblk + block][C] (db); colreduce_k adds
 // the blocks in order.  The grid size is a constant, so the summation order depends on
-// the problem size only.
+// the problem size only.  Optionally (OUTSUM) a third set part[2 nblk + block][C] sums
+// the updated dres rows as stored: that column sum is the bias gradient of the linear
+// layer whose output gradient dres is (llm.c §1.6), so it needs no pass of its own.
 static const int LNB_BLOCKS = 296;      // generic kernel: 8 warps per block
-static const int LNB_VEC_BLOCKS = 592;  // vector kernel: 4 warps per block, 4 blocks per SM
+static const int LNB_VEC_BLOCKS = 592;      // vector kernel: 4 warps per block, 4 blocks per SM
+static const int LNB_VEC_SUM_BLOCKS = 444;  // with the third sum: 3 blocks per SM
 
-size_t ln_bwd_partial_floats(int C) { return (size_t)2 * LNB_VEC_BLOCKS * C; }
+size_t ln_bwd_partial_floats(int C) { return (size_t)3 * LNB_VEC_BLOCKS * C; }
 
 // C = 256 * NV: each lane owns 8 consecutive columns in each of NV 256-column slabs;
 // the row's dout and x stay in registers, the row sums are warp reductions.
-template <typename T, int NV>
+template <typename T, int NV, bool OUTSUM>
 __global__ void __launch_bounds__(128) ln_bwd_vec_k(T* dres, float* part, const T* dout, const T* inp,
                                                     const float* w, const float* mean,
                                                     const float* rstd, int M, int C) {
-    __shared__ float sh[4][2][NV * 256];
+    constexpr int NS = OUTSUM ? 3 : 2;
+    __shared__ float sh[4][NS][NV * 256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float aw[NV][8], ab[NV][8];
+    float aw[NV][8], ab[NV][8], ar[OUTSUM ? NV : 1][8];
 #pragma unroll
     for (int j = 0; j < NV; j++)
 #pragma unroll
-        for (int i = 0; i < 8; i++) aw[j][i] = ab[j][i] = 0.f;
+        for (int i = 0; i < 8; i++) {
+            aw[j][i] = ab[j][i] = 0.f;
+            if (OUTSUM) ar[OUTSUM ? j : 0][i] = 0.f;
+        }
     for (int row = blockIdx.x * 4 + warp; row < M; row += gridDim.x * 4) {
         const T* d = dout + (size_t)row * C;
         const T* x = inp + (size_t)row * C;
@@ -437,6 +447,10 @@ __global__ void __launch_bounds__(128) ln_bwd_vec_k(T* dres, float* part, const 
 #pragma unroll
             for (int i = 0; i < 8; i++) o[i] += (dv[j][i] - gm - xv[j][i] * gnm) * r;
             Vec8<T>::store(dr + j * 256 + lane * 8, o);
+            if (OUTSUM) {
+#pragma unroll
+                for (int i = 0; i < 8; i++) ar[OUTSUM ? j : 0][i] += to_f(from_f<T>(o[i]));  // as stored
+            }
         }
     }
 #pragma unroll
@@ -445,13 +459,13 @@ __global__ void __launch_bounds__(128) ln_bwd_vec_k(T* dres, float* part, const 
         for (int i = 0; i < 8; i++) {
             sh[warp][0][j * 256 + lane * 8 + i] = aw[j][i];
             sh[warp][1][j * 256 + lane * 8 + i] = ab[j][i];
+            if (OUTSUM) sh[warp][NS - 1][j * 256 + lane * 8 + i] = ar[OUTSUM ? j : 0][i];
         }
     __syncthreads();
-    float* pw = part + (size_t)blockIdx.x * C;
-    float* pb = part + (size_t)(gridDim.x + blockIdx.x) * C;
-    for (int c = threadIdx.x; c < C; c += blockDim.x) {
-        pw[c] = ((sh[0][0][c] + sh[1][0][c]) + sh[2][0][c]) + sh[3][0][c];
-        pb[c] = ((sh[0][1][c] + sh[1][1][c]) + sh[2][1][c]) + sh[3][1][c];
+    for (int k = 0; k < NS; k++) {
+        float* pk = part + (size_t)(k * gridDim.x + blockIdx.x) * C;
+        for (int c = threadIdx.x; c < C; c += blockDim.x)
+            pk[c] = ((sh[0][k][c] + sh[1][k][c]) + sh[2][k][c]) + sh[3][k][c];
     }
 }
 
@@ -505,11 +519,12 @@ __global__ void __launch_bounds__(256) ln_bwd_k(T* dres, float* part, const T* d
     }
 }
 
-// out_j[c] = sum over i < n of part[(j*n + i)*N + c] for j = blockIdx.y (out_0 = dw, out_1 =
-// db), in a fixed order: warp w adds rows w, w+32, ... into four interleaved accumulators,
-// then the 32 warp totals are added in warp order.  One block per 32 columns.
-__global__ void __launch_bounds__(1024) colreduce_k(float* out0, float* out1, const float* part, int n,
-                                                    int N) {
+// out_j[c] = sum over i < n of part[(j*n + i)*N + c] for j = blockIdx.y (out_0 = dw,
+// out_1 = db, out_2 = the optional output column sum), in a fixed order: warp w adds rows
+// w, w+32, ... into four interleaved accumulators, then the 32 warp totals are added in
+// warp order.  One block per 32 columns.
+__global__ void __launch_bounds__(1024) colreduce_k(float* out0, float* out1, float* out2, const float* part,
+                                                    int n, int N) {
     __shared__ float sh[32][33];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + lane;
@@ -531,47 +546,59 @@ __global__ void __launch_bounds__(1024) colreduce_k(float* out0, float* out1, co
         float t = 0.f;
 #pragma unroll
         for (int w = 0; w < 32; w++) t += sh[w][lane];
-        (blockIdx.y ? out1 : out0)[c] = t;
+        (blockIdx.y == 0 ? out0 : blockIdx.y == 1 ? out1 : out2)[c] = t;
     }
 }
 
-static cudaError_t colreduce(float* out0, float* out1, const float* part, int n, int N, cudaStream_t s) {
-    dim3 g(cdiv(N, 32), out1 ? 2 : 1);
-    G2_LAUNCH colreduce_k<<<g, 1024, 0, s>>>(out0, out1, part, n, N);
+static cudaError_t colreduce(float* out0, float* out1, float* out2, const float* part, int n, int N,
+                             cudaStream_t s) {
+    dim3 g(cdiv(N, 32), out2 ? 3 : out1 ? 2 : 1);
+    G2_LAUNCH colreduce_k<<<g, 1024, 0, s>>>(out0, out1, out2, part, n, N);
     return cudaGetLastError();
 }
 
 template <typename T>
-static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, const T* dout, const T* inp,
+static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, float* dres_sum, const T* dout, const T* inp,
                                  const float* w, const float* mean, const float* rstd, int M, int C,
-                                 float* part, cudaStream_t s) {
+                                 float* part, float* cs_part, cudaStream_t s) {
     const bool aligned = ((uintptr_t)w & 15) == 0;
     const int nv = (C % 256 == 0 && aligned) ? C / 256 : 0;
     if (nv >= 1 && nv <= 4) {
+#define G2_LNB_CASE(NVV)                                                                                  \
+    case NVV:                                                                                             \
+        if (dres_sum)                                                                                     \
+            G2_LAUNCH ln_bwd_vec_k<T, NVV, true><<<LNB_VEC_SUM_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, \
+                                                                                   rstd, M, C);           \
+        else                                                                                              \
+            G2_LAUNCH ln_bwd_vec_k<T, NVV, false><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, \
+                                                                                rstd, M, C);              \
+        break;
         switch (nv) {
-            case 1: G2_LAUNCH ln_bwd_vec_k<T, 1><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, rstd, M, C); break;
-            case 2: G2_LAUNCH ln_bwd_vec_k<T, 2><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, rstd, M, C); break;
-            case 3: G2_LAUNCH ln_bwd_vec_k<T, 3><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, rstd, M, C); break;
-            default: G2_LAUNCH ln_bwd_vec_k<T, 4><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, rstd, M, C); break;
+            G2_LNB_CASE(1) G2_LNB_CASE(2) G2_LNB_CASE(3) G2_LNB_CASE(4)
         }
-        return colreduce(dw, db, part, LNB_VEC_BLOCKS, C, s);
+#undef G2_LNB_CASE
+        return colreduce(dw, db, dres_sum, part, dres_sum ? LNB_VEC_SUM_BLOCKS : LNB_VEC_BLOCKS, C, s);
     }
     size_t smem = (size_t)8 * 2 * C * sizeof(float);
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(ln_bwd_k<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     G2_LAUNCH ln_bwd_k<T><<<LNB_BLOCKS, 256, smem, s>>>(dres, part, dout, inp, w, mean, rstd, M, C);
-    return colreduce(dw, db, part, LNB_BLOCKS, C, s);
+    cudaError_t e = colreduce(dw, db, nullptr, part, LNB_BLOCKS, C, s);
+    if (e != cudaSuccess || !dres_sum) return e;
+    // the generic kernel keeps no third sum: column-sum the updated rows separately
+    return colsum(std::is_same<T, bf16>::value ? ACT_BF16 : ACT_F32, dres_sum, dres, M, C, cs_part, s);
 }
 
-cudaError_t layernorm_backward(ActType at, void* dres, float* dw, float* db, const void* dout,
-                               const void* inp, const float* w, const float* mean,
-                               const float* rstd, int M, int C, float* part, cudaStream_t s) {
+cudaError_t layernorm_backward(ActType at, void* dres, float* dw, float* db, float* dres_sum, const void* dout,
+                               const void* inp, const float* w, const float* mean, const float* rstd, int M,
+                               int C, float* part, float* cs_part, cudaStream_t s) {
+    if (dres_sum && !cs_part) return cudaErrorInvalidValue;
     if (at == ACT_BF16)
-        return ln_bwd_launch<bf16>((bf16*)dres, dw, db, (const bf16*)dout, (const bf16*)inp, w, mean, rstd,
-                                   M, C, part, s);
-    return ln_bwd_launch<float>((float*)dres, dw, db, (const float*)dout, (const float*)inp, w, mean, rstd,
-                                M, C, part, s);
+        return ln_bwd_launch<bf16>((bf16*)dres, dw, db, dres_sum, (const bf16*)dout, (const bf16*)inp, w, mean,
+                                   rstd, M, C, part, cs_part, s);
+    return ln_bwd_launch<float>((float*)dres, dw, db, dres_sum, (const float*)dout, (const float*)inp, w, mean,
+                                rstd, M, C, part, cs_part, s);
 }
 
 // ------------------------------------------------------------------ bias gradient
@@ -639,7 +666,7 @@ cudaError_t colsum(ActType at, float* out, const void* X, int M, int N, float* p
             G2_LAUNCH colsum_part_k<float><<<g, 256, 0, s>>>(part, (const float*)X, M, N);
     }
     if (nrb == 0) return cudaMemsetAsync(out, 0, (size_t)N * sizeof(float), s);
-    return colreduce(out, nullptr, part, nrb, N, s);
+    return colreduce(out, nullptr, nullptr, part, nrb, N, s);
 }
 
 // ------------------------------------------------------------------ softmax + cross-entropy

@@ -47,10 +47,13 @@ cudaError_t encoder_backward_wte(ActType at, float* dwte, const void* dout, cons
 cudaError_t layernorm_forward(ActType at, void* out, float* mean, float* rstd, const void* inp,
                               const float* w, const float* b, int M, int C, cudaStream_t s);
 // dres (M,C) += LN-backward(dout); dw, db (C) fp32 overwritten.  part: ln_bwd_partial_floats().
+// dres_sum (C floats, may be null) receives the column sums of the updated dres as stored
+// (the bias gradient of the layer whose output gradient dres is); cs_part (colsum
+// partials) is then required.
 size_t ln_bwd_partial_floats(int C);
-cudaError_t layernorm_backward(ActType at, void* dres, float* dw, float* db, const void* dout,
-                               const void* inp, const float* w, const float* mean,
-                               const float* rstd, int M, int C, float* part, cudaStream_t s);
+cudaError_t layernorm_backward(ActType at, void* dres, float* dw, float* db, float* dres_sum, const void* dout,
+                               const void* inp, const float* w, const float* mean, const float* rstd, int M,
+                               int C, float* part, float* cs_part, cudaStream_t s);
 
 // ---- bias gradient: out[n] = sum_m X[m,n] (fixed order) --------------------------
 size_t colsum_partial_floats(int M, int N);

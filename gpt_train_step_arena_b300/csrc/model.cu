@@ -523,9 +523,10 @@ extern "C" int gpt2_backward(gpt2_t* m) {
     OP(GPT2_K_GEMM, gemm_flops(Vp, C, M), gemm_wgrad(m, (int)M, Vp, C, m->logits, m->lnf, pf(m, g, P_WTE)));
     CK(cudaMemsetAsync(m->dres, 0, MC * m->esz, s));
     OP(GPT2_K_LAYERNORM, ln_bwd_bytes,
-       layernorm_backward(m->at, m->dres, pf(m, g, P_LNFW), pf(m, g, P_LNFB), m->dln,
-                          act(m, m->res, (size_t)L * MC), pf(m, m->params, P_LNFW), m->lnf_mean,
-                          m->lnf_rstd, (int)M, C, m->ln_part, s));
+       layernorm_backward(m->at, m->dres, pf(m, g, P_LNFW), pf(m, g, P_LNFB),
+                          pf(m, g, P_FPB) + (size_t)(L - 1) * C,  // d res_out(L-1): fcproj bias
+                          m->dln, act(m, m->res, (size_t)L * MC), pf(m, m->params, P_LNFW), m->lnf_mean,
+                          m->lnf_rstd, (int)M, C, m->ln_part, m->cs_part, s));
     for (int l = L - 1; l >= 0; l--) {
         char* res_in = act(m, m->res, l * MC);
         char* res2 = act(m, m->res2, l * MC);
@@ -540,7 +541,8 @@ extern "C" int gpt2_backward(gpt2_t* m) {
            gemm_dgrad(m, (int)M, C, 4 * C, m->dres, pw(m, P_FPW, (size_t)l * 4 * C * C), m->dfch, fch));
         OP(GPT2_K_GEMM, gemm_flops(C, 4 * C, M),
            gemm_wgrad(m, (int)M, C, 4 * C, m->dres, fchg, pf(m, g, P_FPW) + (size_t)l * 4 * C * C));
-        OP(GPT2_K_BIAS_GRAD, cs_bytes(C), colsum(m->at, pf(m, g, P_FPB) + l * C, m->dres, (int)M, C, m->cs_part, s));
+        // (the fcproj bias gradient, the column sum of dres, came out of the layernorm
+        // backward that produced dres)
         // fc: fch = ln2 . Wfc^T + bfc   (dfch already multiplied by gelu')
         OP(GPT2_K_GEMM, gemm_flops(M, C, 4 * C),
            gemm_dgrad(m, (int)M, 4 * C, C, m->dfch, pw(m, P_FCW, (size_t)l * 4 * C * C), m->dln, nullptr));
@@ -551,14 +553,14 @@ extern "C" int gpt2_backward(gpt2_t* m) {
         // ln2 (dres becomes d res2)
         OP(GPT2_K_LAYERNORM, ln_bwd_bytes,
            layernorm_backward(m->at, m->dres, pf(m, g, P_LN2W) + l * C, pf(m, g, P_LN2B) + l * C,
+                              pf(m, g, P_APB) + l * C,  // d res2: attproj bias
                               m->dln, res2, pf(m, m->params, P_LN2W) + l * C,
-                              m->ln2_mean + l * M, m->ln2_rstd + l * M, (int)M, C, m->ln_part, s));
+                              m->ln2_mean + l * M, m->ln2_rstd + l * M, (int)M, C, m->ln_part, m->cs_part, s));
         // attproj: res2 = atty . Wap^T + bap + res_in
         OP(GPT2_K_GEMM, gemm_flops(M, C, C),
            gemm_dgrad(m, (int)M, C, C, m->dres, pw(m, P_APW, (size_t)l * C * C), m->datty, nullptr));
         OP(GPT2_K_GEMM, gemm_flops(C, C, M),
            gemm_wgrad(m, (int)M, C, C, m->dres, atty, pf(m, g, P_APW) + (size_t)l * C * C));
-        OP(GPT2_K_BIAS_GRAD, cs_bytes(C), colsum(m->at, pf(m, g, P_APB) + l * C, m->dres, (int)M, C, m->cs_part, s));
         // attention
         OP(GPT2_K_ATTN_BWD, 2.0 * attn_fwd_flops(m),
            attention_backward(m->at, m->dqkv, m->datty, qkv, atty, m->lse + l * M * NH, B, T, C, NH,
@@ -573,8 +575,9 @@ extern "C" int gpt2_backward(gpt2_t* m) {
         // ln1 (dres becomes d res_in)
         OP(GPT2_K_LAYERNORM, ln_bwd_bytes,
            layernorm_backward(m->at, m->dres, pf(m, g, P_LN1W) + l * C, pf(m, g, P_LN1B) + l * C,
+                              l > 0 ? pf(m, g, P_FPB) + (size_t)(l - 1) * C : nullptr,  // d res_out(l-1)
                               m->dln, res_in, pf(m, m->params, P_LN1W) + l * C,
-                              m->ln1_mean + l * M, m->ln1_rstd + l * M, (int)M, C, m->ln_part, s));
+                              m->ln1_mean + l * M, m->ln1_rstd + l * M, (int)M, C, m->ln_part, m->cs_part, s));
     }
     OP(GPT2_K_ENCODER, actMC + 4.0 * m->maxT * C,
        encoder_backward_wpe(m->at, pf(m, g, P_WPE), m->dres, B, T, C, m->maxT, s));

@@ -139,8 +139,8 @@ extern "C" int gpt2_op_layernorm_backward(int dtype, void* dinp, float* dw, floa
     if (!workspace || workspace_bytes < need)
         return op_fail(GPT2_ERR_ARG, "layernorm_backward: workspace of %zu bytes needed, %zu given", need,
                        workspace_bytes);
-    return op_cuda(layernorm_backward(act_of(dtype), dinp, dw, db, dout, inp, w, mean, rstd, M, C,
-                                      (float*)workspace, (cudaStream_t)stream),
+    return op_cuda(layernorm_backward(act_of(dtype), dinp, dw, db, nullptr, dout, inp, w, mean, rstd, M, C,
+                                      (float*)workspace, nullptr, (cudaStream_t)stream),
                    "layernorm_backward");
 }
 
