@@ -57,6 +57,8 @@ SIGNATURES = {
     "gpt2_op_bias_grad_noalloc": (I, [I, P, I, I, P, P]),
     "gpt2_op_bias_grad_noalloc_max_floats": (SZ, []),
     "gpt2_op_matmul": (I, [I, I, I, I, P, ct.c_longlong, I, P, ct.c_longlong, I, P, ct.c_longlong, I, P, P, SZ, P]),
+    "gpt2_op_matmul_ex": (I, [I, I, I, I, P, ct.c_longlong, I, P, ct.c_longlong, I, P, ct.c_longlong, P, P,
+                              ct.c_longlong, P, ct.c_longlong, P, ct.c_longlong, I, P, SZ, P]),
     "gpt2_op_adamw": (I, [P, P, P, P, P, SZ, F, F, F, F, F, I, P]),
     "gpt2_op_attention_forward": (I, [I, P, P, P, I, I, I, I, P]),
     "gpt2_op_attention_backward": (I, [I, P, P, P, P, P, I, I, I, I, P, P]),
@@ -77,6 +79,7 @@ GPT2_ERR_TOKEN, GPT2_ERR_SHAPE, GPT2_ERR_STATE, GPT2_ERR_NONFINITE, GPT2_ERR_TIM
 GPT2_FP32, GPT2_BF16 = 0, 2
 GPT2_DT_F32, GPT2_DT_BF16 = 0, 1
 GPT2_HOST, GPT2_DEVICE = 0, 1
+GPT2_EPI_STORE, GPT2_EPI_GELU, GPT2_EPI_GELU_BWD = 0, 1, 2
 KERNEL_CLASSES = ["gemm", "attn_fwd", "attn_bwd", "layernorm", "xent", "adamw", "encoder", "bias_grad"]
 
 STATUS_NAMES = {0: "GPT2_OK", -1: "GPT2_ERR_ARG", -2: "GPT2_ERR_OOM", -3: "GPT2_ERR_CUDA",

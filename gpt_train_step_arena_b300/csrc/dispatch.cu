@@ -15,6 +15,8 @@ size_t gemm_workspace_bytes(int M, int C, int Vp, int) {
     return b;
 }
 
+bool gemm_tc_path(const GemmArgs& a) { return gemm_tc_supported(a); }
+
 cudaError_t gemm_dispatch(const GemmArgs& a, float* ws, size_t ws_bytes, cudaStream_t s) {
     if (gemm_tc_supported(a)) return gemm_tc(a, ws, ws_bytes, a.flags, s);
     return gemm_simt(a, s);

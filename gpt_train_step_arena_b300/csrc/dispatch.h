@@ -9,6 +9,8 @@ size_t gemm_workspace_bytes(int M, int C, int Vp, int L);
 // Runs D = epi(A . B^T) on the fastest kernel that takes the shape: the tcgen05
 // tensor-core kernel for bf16 operands it supports, the SIMT kernel otherwise.
 cudaError_t gemm_dispatch(const GemmArgs& a, float* ws, size_t ws_bytes, cudaStream_t s);
+// True when the tensor-core kernel takes this product (else the SIMT kernel would).
+bool gemm_tc_path(const GemmArgs& a);
 
 // flags (may be null): device error flags, G2_FLAG_TIMEOUT is OR-ed in if a bounded
 // wait of the tensor-core kernel expires.

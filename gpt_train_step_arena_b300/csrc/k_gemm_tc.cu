@@ -39,7 +39,14 @@ namespace tc {
 constexpr int BM = 128, BK = 64, UMMA_K = 16;  // rows per MMA (one accumulator half)
 constexpr int GROUP_M = 8;     // tile order: m fastest within groups of GROUP_M row tiles
 
-enum { E_STORE = 0, E_GELU = 1, E_GELU_BWD = 2, E_PARTIAL = 3 };
+// epilogues: bf16 store (+bias, +residual), GELU (two bf16 outputs), times GELU' of the
+// pre-activation, fp32 split-K partial, fp32 store
+enum { E_STORE = 0, E_GELU = 1, E_GELU_BWD = 2, E_PARTIAL = 3, E_STORE_F32 = 4 };
+template <int EPI> struct EpiOut {
+    static constexpr bool F32 = EPI == E_PARTIAL || EPI == E_STORE_F32;
+    static constexpr int CW = F32 ? 32 : 64;           // columns per 128-byte staged row
+    static constexpr int NOUT = EPI == E_GELU ? 2 : 1;  // staged outputs per chunk
+};
 
 struct Params {
     int M, N, K;
@@ -58,7 +65,7 @@ struct Params {
     int* flags;
 };
 
-template <int BN, int BMT>
+template <int BN, int BMT, int EPI>
 struct Cfg {
     static constexpr int HALVES = BMT / BM;                 // 128-row accumulator halves per tile
     static constexpr int EPI_WARPS = 4 * HALVES;            // one per 32-lane quarter per half
@@ -66,11 +73,17 @@ struct Cfg {
     static constexpr int A_BYTES = BMT * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;  // 3 to 6 stages, 192 KB
+    // each epilogue warp stages 32 rows x 128 bytes per output for the TMA store
+    static constexpr int EPI_WARP_BYTES = EpiOut<EPI>::NOUT * 4096;
+    static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
+    static constexpr int SMEM_LIMIT = 227 * 1024 - 1024 /*align*/ - 256 /*barriers*/;
+    static constexpr int STAGES_FIT = (SMEM_LIMIT - EPI_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
     static constexpr int ACC_COLS = HALVES * BN;
     static constexpr int ACC_BUFS = (512 / ACC_COLS) >= 2 ? 2 : 1;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+    static_assert(STAGES >= 2, "shared memory too small for the pipeline");
 };
 
 // Work unit u: row tile m_blk (BMT rows), column tile n_blk, K split `split`.  Row tiles
@@ -89,113 +102,98 @@ G2_DEV void unit_coords(const Params& p, int u, int& m_blk, int& n_blk, int& spl
 }
 
 // ------------------------------------------------------------------ epilogue
+// One chunk of CW columns of this thread's row (gm): the fused math on the fp32
+// accumulator values, then the row written into the warp's staging buffer (32 rows x 128
+// bytes, the 128-byte swizzle a TMA store expects).  Columns past N carry garbage the
+// store does not write.
 template <int EPI>
-G2_DEV void epilogue_chunk(const Params& p, const float* acc, int gm, int gn0, int split) {
+G2_DEV void epilogue_math(const Params& p, float* v, int gm, int gn0) {
+    constexpr int CW = EpiOut<EPI>::CW;
     const int N = p.N;
-    float v[32];
+    const bool full = gn0 + CW <= N;
+    if (EPI == E_GELU_BWD) {
+        if (gm < p.M) {
+            const bf16* pre = p.P + (size_t)gm * p.ldp + gn0;
+            if (full) {
 #pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = acc[i];
-    const bool full = gn0 + 32 <= N;
-    if (EPI == E_PARTIAL) {
-        float* dst = p.ws + ((size_t)split * p.M + gm) * N + gn0;
-        if (full && (N & 3) == 0) {
+                for (int i = 0; i < CW; i += 8) {
+                    float x[8];
+                    Vec8<bf16>::load(pre + i, x);
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-        } else {
-            for (int i = 0; i < 32; i++)
-                if (gn0 + i < N) dst[i] = v[i];
+                    for (int j = 0; j < 8; j++) v[i + j] *= gelu_tanh_grad_fast(x[j]);
+                }
+            } else {
+                for (int i = 0; i < CW; i++)
+                    if (gn0 + i < N) v[i] *= gelu_tanh_grad_fast(__bfloat162float(pre[i]));
+            }
         }
         return;
     }
-    if (EPI == E_GELU_BWD) {
-        const bf16* pre = p.P + (size_t)gm * p.ldp + gn0;
+    if (EPI == E_PARTIAL) return;
+    if (p.bias) {
         if (full) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
+            for (int i = 0; i < CW; i += 4) {
+                float4 b = *reinterpret_cast<const float4*>(p.bias + gn0 + i);
+                v[i] += b.x; v[i + 1] += b.y; v[i + 2] += b.z; v[i + 3] += b.w;
+            }
+        } else {
+            for (int i = 0; i < CW; i++)
+                if (gn0 + i < N) v[i] += p.bias[gn0 + i];
+        }
+    }
+    if (p.R && gm < p.M) {
+        const bf16* r = p.R + (size_t)gm * p.ldr + gn0;
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < CW; i += 8) {
                 float x[8];
-                Vec8<bf16>::load(pre + i, x);
+                Vec8<bf16>::load(r + i, x);
 #pragma unroll
-                for (int j = 0; j < 8; j++) v[i + j] *= gelu_tanh_grad_fast(x[j]);
+                for (int j = 0; j < 8; j++) v[i + j] += x[j];
             }
         } else {
-            for (int i = 0; i < 32; i++)
-                if (gn0 + i < N) v[i] *= gelu_tanh_grad_fast(__bfloat162float(pre[i]));
-        }
-    } else {
-        if (p.bias) {
-            if (full) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    float4 b = *reinterpret_cast<const float4*>(p.bias + gn0 + i);
-                    v[i] += b.x; v[i + 1] += b.y; v[i + 2] += b.z; v[i + 3] += b.w;
-                }
-            } else {
-                for (int i = 0; i < 32; i++)
-                    if (gn0 + i < N) v[i] += p.bias[gn0 + i];
-            }
-        }
-        if (p.R) {
-            const bf16* r = p.R + (size_t)gm * p.ldr + gn0;
-            if (full) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    float x[8];
-                    Vec8<bf16>::load(r + i, x);
-#pragma unroll
-                    for (int j = 0; j < 8; j++) v[i + j] += x[j];
-                }
-            } else {
-                for (int i = 0; i < 32; i++)
-                    if (gn0 + i < N) v[i] += __bfloat162float(r[i]);
-            }
+            for (int i = 0; i < CW; i++)
+                if (gn0 + i < N) v[i] += __bfloat162float(r[i]);
         }
     }
-    if (p.d_f32) {
-        float* dst = (float*)p.D + (size_t)gm * p.ldd + gn0;
-        if (full && (p.ldd & 3) == 0) {
+}
+
+// this thread's row of a staging buffer: 8 chunks of 16 bytes, chunk c at (c ^ (row & 7))
+template <bool F32>
+G2_DEV void stage_row(uint8_t* buf, int lane, const float* v) {
+    uint8_t* row = buf + lane * 128;
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    for (int c = 0; c < 8; c++) {
+        uint4 u;
+        if (F32) {
+            u = make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]), __float_as_uint(v[4 * c + 2]),
+                           __float_as_uint(v[4 * c + 3]));
         } else {
-            for (int i = 0; i < 32; i++)
-                if (gn0 + i < N) dst[i] = v[i];
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * c], v[8 * c + 1]);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * c + 2], v[8 * c + 3]);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * c + 4], v[8 * c + 5]);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * c + 6], v[8 * c + 7]);
+            u = make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
+                           *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
         }
-    } else {
-        bf16* dst = (bf16*)p.D + (size_t)gm * p.ldd + gn0;
-        if (full) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) Vec8<bf16>::store(dst + i, v + i);
-        } else {
-            for (int i = 0; i < 32; i++)
-                if (gn0 + i < N) dst[i] = __float2bfloat16_rn(v[i]);
-        }
-    }
-    if (EPI == E_GELU) {
-        float gv[32];
-#pragma unroll
-        for (int i = 0; i < 32; i++) gv[i] = gelu_tanh_fast(v[i]);
-        bf16* dst = p.D2 + (size_t)gm * p.ldd2 + gn0;
-        if (full) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) Vec8<bf16>::store(dst + i, gv + i);
-        } else {
-            for (int i = 0; i < 32; i++)
-                if (gn0 + i < N) dst[i] = __float2bfloat16_rn(gv[i]);
-        }
+        *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) = u;
     }
 }
 
 // ------------------------------------------------------------------ the kernel
 template <int BN, int BMT, bool A_MN, bool B_MN, int EPI>
-__global__ void __launch_bounds__(Cfg<BN, BMT>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                    const Params p) {
-    using CF = Cfg<BN, BMT>;
+    using CF = Cfg<BN, BMT, EPI>;
+    using EO = EpiOut<EPI>;
     constexpr int S = CF::STAGES, NB = CF::ACC_BUFS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t* bars = (uint64_t*)(smem + S * CF::STAGE_BYTES);
+    uint8_t* epi_smem = smem + S * CF::STAGE_BYTES;  // staging for the TMA stores
+    uint64_t* bars = (uint64_t*)(epi_smem + CF::EPI_BYTES);
     uint64_t* full_bar = bars;                  // [S]
     uint64_t* empty_bar = bars + S;             // [S]
     uint64_t* tfull_bar = bars + 2 * S;         // [NB]
@@ -220,6 +218,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMT>::THREADS, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmD);
     }
     if (warp == 1) tmem_alloc(tmem_slot, CF::TMEM_COLS);
     tc_fence_before();
@@ -355,6 +354,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMT>::THREADS, 1)
         const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
         const int hh = (warp - 2) >> 2;
         const int row_in_tile = hh * BM + quarter * 32 + lane;
+        uint8_t* stg = epi_smem + (warp - 2) * CF::EPI_WARP_BYTES;  // this warp's staging
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
@@ -364,13 +364,34 @@ __global__ void __launch_bounds__(Cfg<BN, BMT>::THREADS, 1)
             if (!__all_sync(0xffffffffu, ok)) break;  // the warp leaves together
             tc_fence_after();
             const int gm = mb * BMT + row_in_tile;
+            const int gm0 = gm - lane;  // first row of this warp's 32
             const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * CF::ACC_COLS + hh * BN);
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                float v[32];
+            for (int c0 = 0; c0 < BN; c0 += EO::CW) {
+                float v[EO::CW];
                 tmem_ld32(trow + c0, v);
+                if (EO::CW == 64) tmem_ld32(trow + c0 + 32, v + 32);
                 const int gn0 = nb * BN + c0;
-                if (gm < p.M && gn0 < p.N) epilogue_chunk<EPI>(p, v, gm, gn0, sp);
+                epilogue_math<EPI>(p, v, gm, gn0);
+                // the previous chunk's stores have finished reading the staging buffers
+                if (lane == 0) bulk_wait_read0();
+                __syncwarp();
+                stage_row<EO::F32>(stg, lane, v);
+                if (EPI == E_GELU) {
+#pragma unroll
+                    for (int i = 0; i < EO::CW; i++) v[i] = gelu_tanh_fast(v[i]);
+                    stage_row<false>(stg + 4096, lane, v);
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0 && gm0 < p.M && gn0 < p.N) {
+                    if (EPI == E_PARTIAL)
+                        tma_store_3d(&tmD, stg, gn0, gm0, sp);
+                    else
+                        tma_store_2d(&tmD, stg, gn0, gm0);
+                    if (EPI == E_GELU) tma_store_2d(&tmD2, stg + 4096, gn0, gm0);
+                    bulk_commit();
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -380,6 +401,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMT>::THREADS, 1)
                 acc_phase ^= 1;
             }
         }
+        if (lane == 0) bulk_wait0();  // this warp's stores are complete before the CTA ends
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -411,8 +434,9 @@ static int num_sms() {
 }
 
 template <int BN, int BMT, bool A_MN, bool B_MN, int EPI>
-static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, cudaStream_t s) {
-    using CF = Cfg<BN, BMT>;
+static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                            const CUtensorMap& td2, const Params& p, cudaStream_t s) {
+    using CF = Cfg<BN, BMT, EPI>;
     auto kern = gemm_tc_kernel<BN, BMT, A_MN, B_MN, EPI>;
     static bool attr_done = false;
     if (!attr_done) {
@@ -421,23 +445,26 @@ static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const 
         attr_done = true;
     }
     int grid = std::min(p.num_units, num_sms());
-    G2_LAUNCH kern<<<grid, CF::THREADS, CF::SMEM_BYTES, s>>>(ta, tb, p);
+    G2_LAUNCH kern<<<grid, CF::THREADS, CF::SMEM_BYTES, s>>>(ta, tb, td, td2, p);
     return cudaGetLastError();
 }
 
+struct Maps {
+    CUtensorMap a, b, d, d2;
+};
+
 template <int BN, int EPI>
-static cudaError_t launch_layout(int bmt, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
-                                 const Params& p, cudaStream_t s) {
+static cudaError_t launch_layout(int bmt, bool a_mn, bool b_mn, const Maps& m, const Params& p, cudaStream_t s) {
     if (bmt == 256) {
-        if (!a_mn && !b_mn) return launch_t<BN, 256, false, false, EPI>(ta, tb, p, s);
-        if (!a_mn && b_mn) return launch_t<BN, 256, false, true, EPI>(ta, tb, p, s);
-        if (a_mn && b_mn) return launch_t<BN, 256, true, true, EPI>(ta, tb, p, s);
-        return launch_t<BN, 256, true, false, EPI>(ta, tb, p, s);
+        if (!a_mn && !b_mn) return launch_t<BN, 256, false, false, EPI>(m.a, m.b, m.d, m.d2, p, s);
+        if (!a_mn && b_mn) return launch_t<BN, 256, false, true, EPI>(m.a, m.b, m.d, m.d2, p, s);
+        if (a_mn && b_mn) return launch_t<BN, 256, true, true, EPI>(m.a, m.b, m.d, m.d2, p, s);
+        return launch_t<BN, 256, true, false, EPI>(m.a, m.b, m.d, m.d2, p, s);
     }
-    if (!a_mn && !b_mn) return launch_t<BN, 128, false, false, EPI>(ta, tb, p, s);
-    if (!a_mn && b_mn) return launch_t<BN, 128, false, true, EPI>(ta, tb, p, s);
-    if (a_mn && b_mn) return launch_t<BN, 128, true, true, EPI>(ta, tb, p, s);
-    return launch_t<BN, 128, true, false, EPI>(ta, tb, p, s);
+    if (!a_mn && !b_mn) return launch_t<BN, 128, false, false, EPI>(m.a, m.b, m.d, m.d2, p, s);
+    if (!a_mn && b_mn) return launch_t<BN, 128, false, true, EPI>(m.a, m.b, m.d, m.d2, p, s);
+    if (a_mn && b_mn) return launch_t<BN, 128, true, true, EPI>(m.a, m.b, m.d, m.d2, p, s);
+    return launch_t<BN, 128, true, false, EPI>(m.a, m.b, m.d, m.d2, p, s);
 }
 
 }  // namespace tc
@@ -511,17 +538,17 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
     const bool a_mn = a.sAk != 1, b_mn = a.sBk != 1;
     const int BN = a.N > 128 ? 256 : 128;
     const int bmt = tile_rows(a.M, a.N, a.K, BN);
-    CUtensorMap ta, tb;
+    Maps mp;
     bool ok;
     if (!a_mn)
-        ok = make_map(&ta, a.A, a.K, a.M, a.sAm, BK, bmt);
+        ok = make_map(&mp.a, a.A, a.K, a.M, a.sAm, BK, bmt);
     else
-        ok = make_map(&ta, a.A, a.M, a.K, a.sAk, 64, BK);
+        ok = make_map(&mp.a, a.A, a.M, a.K, a.sAk, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
     if (!b_mn)
-        ok = make_map(&tb, a.B, a.K, a.N, a.sBn, BK, BN);
+        ok = make_map(&mp.b, a.B, a.K, a.N, a.sBn, BK, BN);
     else
-        ok = make_map(&tb, a.B, a.N, a.K, a.sBk, 64, BK);
+        ok = make_map(&mp.b, a.B, a.N, a.K, a.sBk, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
 
     Params p{};
@@ -546,10 +573,30 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
     p.ws = ws;
     p.flags = flags ? flags : fallback_flag();
 
+    // output maps for the TMA stores: 32-row boxes of 128 bytes (64 bf16 or 32 fp32)
+    const uint32_t box_bf16[2] = {64, 32}, box_f32[2] = {32, 32};
+    if (splits > 1) {
+        const uint64_t dims[3] = {(uint64_t)a.N, (uint64_t)a.M, (uint64_t)splits};
+        const uint64_t st[2] = {(uint64_t)a.N * 4, (uint64_t)a.M * a.N * 4};
+        const uint32_t box3[3] = {32, 32, 1};
+        ok = (a.N % 4 == 0) && make_map_nd(&mp.d, ws, true, 3, dims, st, box3);
+    } else {
+        const uint64_t dims[2] = {(uint64_t)a.N, (uint64_t)a.M};
+        const uint64_t st[1] = {(uint64_t)a.ldd * (a.d_f32 ? 4 : 2)};
+        ok = make_map_nd(&mp.d, a.D, a.d_f32 != 0, 2, dims, st, a.d_f32 ? box_f32 : box_bf16);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    mp.d2 = mp.d;
+    if (a.epi == EPI_GELU) {
+        const uint64_t dims[2] = {(uint64_t)a.N, (uint64_t)a.M};
+        const uint64_t st[1] = {(uint64_t)a.ldd2 * 2};
+        if (!make_map_nd(&mp.d2, a.D2, false, 2, dims, st, box_bf16)) return cudaErrorInvalidValue;
+    }
+
     cudaError_t e;
     if (splits > 1) {
-        e = BN == 256 ? launch_layout<256, E_PARTIAL>(bmt, a_mn, b_mn, ta, tb, p, s)
-                      : launch_layout<128, E_PARTIAL>(bmt, a_mn, b_mn, ta, tb, p, s);
+        e = BN == 256 ? launch_layout<256, E_PARTIAL>(bmt, a_mn, b_mn, mp, p, s)
+                      : launch_layout<128, E_PARTIAL>(bmt, a_mn, b_mn, mp, p, s);
         if (e != cudaSuccess) return e;
         size_t n = (size_t)a.M * a.N;
         unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
@@ -558,14 +605,17 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
     }
     switch (a.epi) {
         case EPI_GELU:
-            return BN == 256 ? launch_layout<256, E_GELU>(bmt, a_mn, b_mn, ta, tb, p, s)
-                             : launch_layout<128, E_GELU>(bmt, a_mn, b_mn, ta, tb, p, s);
+            return BN == 256 ? launch_layout<256, E_GELU>(bmt, a_mn, b_mn, mp, p, s)
+                             : launch_layout<128, E_GELU>(bmt, a_mn, b_mn, mp, p, s);
         case EPI_GELU_BWD:
-            return BN == 256 ? launch_layout<256, E_GELU_BWD>(bmt, a_mn, b_mn, ta, tb, p, s)
-                             : launch_layout<128, E_GELU_BWD>(bmt, a_mn, b_mn, ta, tb, p, s);
+            return BN == 256 ? launch_layout<256, E_GELU_BWD>(bmt, a_mn, b_mn, mp, p, s)
+                             : launch_layout<128, E_GELU_BWD>(bmt, a_mn, b_mn, mp, p, s);
         default:
-            return BN == 256 ? launch_layout<256, E_STORE>(bmt, a_mn, b_mn, ta, tb, p, s)
-                             : launch_layout<128, E_STORE>(bmt, a_mn, b_mn, ta, tb, p, s);
+            if (a.d_f32)
+                return BN == 256 ? launch_layout<256, E_STORE_F32>(bmt, a_mn, b_mn, mp, p, s)
+                                 : launch_layout<128, E_STORE_F32>(bmt, a_mn, b_mn, mp, p, s);
+            return BN == 256 ? launch_layout<256, E_STORE>(bmt, a_mn, b_mn, mp, p, s)
+                             : launch_layout<128, E_STORE>(bmt, a_mn, b_mn, mp, p, s);
     }
 }
 

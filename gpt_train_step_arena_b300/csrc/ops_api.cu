@@ -78,6 +78,36 @@ extern "C" int gpt2_op_matmul(int dtype, int M, int N, int K, const void* A, lon
                                  (cudaStream_t)stream), "matmul");
 }
 
+extern "C" int gpt2_op_matmul_ex(int dtype, int M, int N, int K, const void* A, long long lda, int a_kmajor,
+                                 const void* B, long long ldb, int b_kmajor, void* D, long long ldd,
+                                 const float* bias, const void* R, long long ldr, void* D2, long long ldd2,
+                                 const void* P, long long ldp, int epilogue, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    if (dtype != GPT2_DT_BF16) return op_fail(GPT2_ERR_ARG, "matmul_ex: the fused epilogues take bf16 only");
+    if (epilogue < GPT2_EPI_STORE || epilogue > GPT2_EPI_GELU_BWD)
+        return op_fail(GPT2_ERR_ARG, "matmul_ex: bad epilogue %d", epilogue);
+    if (M < 0 || N < 0 || K < 0) return op_fail(GPT2_ERR_ARG, "matmul_ex: negative size");
+    if (M == 0 || N == 0) return GPT2_OK;
+    if (!A || !B || !D) return op_fail(GPT2_ERR_ARG, "matmul_ex: null pointer");
+    if (epilogue == GPT2_EPI_GELU && (!D2 || !bias)) return op_fail(GPT2_ERR_ARG, "matmul_ex: GELU needs bias and D2");
+    if (epilogue == GPT2_EPI_GELU_BWD && !P) return op_fail(GPT2_ERR_ARG, "matmul_ex: GELU_BWD needs P");
+    GemmArgs a{};
+    a.M = M; a.N = N; a.K = K; a.in_type = ACT_BF16;
+    a.A = A;
+    if (a_kmajor) { a.sAm = lda; a.sAk = 1; } else { a.sAm = 1; a.sAk = lda; }
+    a.B = B;
+    if (b_kmajor) { a.sBn = ldb; a.sBk = 1; } else { a.sBn = 1; a.sBk = ldb; }
+    a.D = D; a.ldd = ldd; a.d_f32 = 0;
+    a.bias = epilogue == GPT2_EPI_GELU_BWD ? nullptr : bias;
+    a.R = epilogue == GPT2_EPI_STORE ? R : nullptr; a.ldr = ldr;
+    a.D2 = D2; a.ldd2 = ldd2;
+    a.P = P; a.ldp = ldp;
+    a.epi = epilogue == GPT2_EPI_GELU ? EPI_GELU : epilogue == GPT2_EPI_GELU_BWD ? EPI_GELU_BWD : EPI_STORE;
+    if (!gemm_tc_path(a)) return op_fail(GPT2_ERR_ARG, "matmul_ex: layout or alignment outside the fused path");
+    return op_cuda(gemm_dispatch(a, (float*)workspace, workspace ? workspace_bytes : 0, (cudaStream_t)stream),
+                   "matmul_ex");
+}
+
 extern "C" int gpt2_op_adamw(float* p, const float* g, float* m, float* v, void* shadow, size_t n,
                              float lr, float b1, float b2, float eps, float wd, int t, void* stream) {
     if (t < 1) return op_fail(GPT2_ERR_ARG, "adamw: t must be >= 1 (got %d)", t);

@@ -118,6 +118,25 @@ G2_DEV uint32_t num_clusters_x() {
 G2_DEV void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Shared memory -> global tensor tile stores (bulk-group completion).  The source must be
+// made visible to the async proxy first (fence_async_smem); coordinates are never
+// negative here; parts of the box outside the tensor are not written.
+G2_DEV void tma_store_2d(const CUtensorMap* tm, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"((uint64_t)tm),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+G2_DEV void tma_store_3d(const CUtensorMap* tm, const void* src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     (uint64_t)tm),
+                 "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+G2_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the committed stores have finished reading their shared-memory sources
+G2_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// the committed stores have completed
+G2_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 G2_DEV void tma_prefetch_desc(const CUtensorMap* tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tm) : "memory");
 }
@@ -272,6 +291,25 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
             fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
     });
     return fn;
+}
+
+// General tiled map with the 128-byte swizzle: rank 2 or 3, dims[0] contiguous, strides in
+// bytes for dims 1.., element type bf16 or fp32.
+inline bool make_map_nd(CUtensorMap* tm, const void* base, bool f32, int rank, const uint64_t* dims,
+                        const uint64_t* strides_bytes, const uint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[3], st[2];
+    cuuint32_t bx[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; i++) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; i++) st[i] = strides_bytes[i];
+    CUresult r = fn(tm, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+                    const_cast<void*>(base), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 // bf16 2-D map: `inner` contiguous elements per row, `outer` rows `ld` elements apart.

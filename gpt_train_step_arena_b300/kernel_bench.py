@@ -4,7 +4,8 @@
 
 Ops: the matrix products of a layer (qkv_fwd, attproj_fwd, fc_fwd, fcproj_fwd,
 lmhead_fwd, fc_dgrad, fc_wgrad, qkv_wgrad, lmhead_dgrad, lmhead_wgrad), attention
-(attn_fwd, attn_bwd), layernorm (ln_fwd, ln_bwd), softmax + cross-entropy (xent), bias
+(attn_fwd, attn_bwd), the fused-epilogue products (fc_fwd_gelu, fcproj_dgrad_gelu,
+attproj_fwd_res, qkv_fwd_bias), layernorm (ln_fwd, ln_bwd), softmax + cross-entropy (xent), bias
 gradients (bias_grad, bias_grad_fc, bias_grad_qkv) and AdamW over the full parameter
 count.  Inputs are seeded random
 device tensors; each op runs --reps times after --warmup runs, timed with CUDA events,
@@ -97,6 +98,28 @@ def main():
         sh = torch.empty(n, dtype=bf, device=dev)
         fn = lambda: ops.adamw(p, gr, m, v, 6e-4, 0.9, 0.999, 1e-8, 0.1, 1, shadow=sh)
         unit, work = "GB/s", 30.0 * n
+    elif args.op in ("fc_fwd_gelu", "fcproj_dgrad_gelu", "attproj_fwd_res", "qkv_fwd_bias"):
+        # the products with the epilogues the training step fuses into them
+        from . import _native as N_
+        M, C = c["B"] * c["T"], c["C"]
+        bias = lambda n: 0.1 * torch.randn(n, device=dev, generator=g)
+        if args.op == "fc_fwd_gelu":
+            A, W, b = rnd(M, C), rnd(4 * C, C), bias(4 * C)
+            fn = lambda: ops.linear_fused(A, W, N_.GPT2_EPI_GELU, bias=b)
+            Nn, K = 4 * C, C
+        elif args.op == "fcproj_dgrad_gelu":
+            A, W, P = rnd(M, C), rnd(C, 4 * C), rnd(M, 4 * C)
+            fn = lambda: ops.linear_fused(A, W, N_.GPT2_EPI_GELU_BWD, P=P, b_kmajor=False)
+            Nn, K = 4 * C, C
+        elif args.op == "attproj_fwd_res":
+            A, W, b, R = rnd(M, C), rnd(C, C), bias(C), rnd(M, C)
+            fn = lambda: ops.linear_fused(A, W, N_.GPT2_EPI_STORE, bias=b, R=R)
+            Nn, K = C, C
+        else:
+            A, W, b = rnd(M, C), rnd(3 * C, C), bias(3 * C)
+            fn = lambda: ops.linear_fused(A, W, N_.GPT2_EPI_STORE, bias=b)
+            Nn, K = 3 * C, C
+        unit, work = "TFLOP/s", 2.0 * M * Nn * K
     else:
         M, N, K, layout = _gemm_case(args.op, c)
         if layout == "fwd":

@@ -112,3 +112,22 @@ def softmax_xent(logits: torch.Tensor, targets: torch.Tensor, V: int, dloss: flo
                                       M, V, Vp, dloss, None if flags is None else flags.data_ptr(),
                                       _stream()))
     return losses
+
+
+def linear_fused(A: torch.Tensor, W: torch.Tensor, epilogue: int, bias=None, R=None, P=None, b_kmajor=True,
+                 workspace_bytes: int = 0):
+    """bf16 D = A . W^T (W (N,K), b_kmajor) or A . W (W (K,N), not b_kmajor) with a fused epilogue
+    (N.GPT2_EPI_*).  Returns D, or (D, gelu(D)) for GPT2_EPI_GELU."""
+    M, K = A.shape
+    Nn = W.shape[0] if b_kmajor else W.shape[1]
+    D = torch.empty(M, Nn, dtype=A.dtype, device=A.device)
+    D2 = torch.empty_like(D) if epilogue == N.GPT2_EPI_GELU else None
+    ws = torch.empty(workspace_bytes, dtype=torch.uint8, device=A.device) if workspace_bytes else None
+    _check(N.lib.gpt2_op_matmul_ex(_dt(A), M, Nn, K, A.data_ptr(), A.stride(0), 1, W.data_ptr(), W.stride(0),
+                                   int(b_kmajor), D.data_ptr(), D.stride(0),
+                                   None if bias is None else bias.data_ptr(),
+                                   None if R is None else R.data_ptr(), 0 if R is None else R.stride(0),
+                                   None if D2 is None else D2.data_ptr(), 0 if D2 is None else D2.stride(0),
+                                   None if P is None else P.data_ptr(), 0 if P is None else P.stride(0),
+                                   epilogue, None if ws is None else ws.data_ptr(), workspace_bytes, _stream()))
+    return (D, D2) if D2 is not None else D

@@ -67,6 +67,21 @@ int gpt2_op_matmul(int dtype, int M, int N, int K, const void* A, long long lda,
                    const void* B, long long ldb, int b_kmajor, void* D, long long ldd, int d_f32,
                    const float* bias, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same product with the epilogues the training step fuses into it (llm.c §1.5
+ * matmul_forward with §1.11 residual_forward or §1.9 gelu_forward; §1.6 with §1.10
+ * gelu_backward), bf16 tensor-core path only (GPT2_DT_BF16, D bf16):
+ *   GPT2_EPI_STORE     D = A.B^T (+ bias[n]) (+ R[m,n])           R: (M,N) bf16, row stride ldr
+ *   GPT2_EPI_GELU      D = A.B^T + bias[n]; D2 = gelu_tanh(D)      D2: (M,N) bf16, row stride ldd2
+ *   GPT2_EPI_GELU_BWD  D = (A.B^T) * gelu_tanh'(P[m,n])            P: (M,N) bf16, row stride ldp
+ * Unused pointers may be NULL.  Returns GPT2_ERR_ARG for an epilogue the layout or dtype
+ * cannot take (the fused path needs 16-byte aligned operands and strides that are
+ * multiples of 8 elements). */
+enum gpt2_epilogue { GPT2_EPI_STORE = 0, GPT2_EPI_GELU = 1, GPT2_EPI_GELU_BWD = 2 };
+int gpt2_op_matmul_ex(int dtype, int M, int N, int K, const void* A, long long lda, int a_kmajor,
+                      const void* B, long long ldb, int b_kmajor, void* D, long long ldd, const float* bias,
+                      const void* R, long long ldr, void* D2, long long ldd2, const void* P, long long ldp,
+                      int epilogue, void* workspace, size_t workspace_bytes, void* stream);
+
 /* AdamW over n fp32 elements (llm.c §1.26 gpt2_update), in place on p, m, v; g is read.
  * shadow_bf16 (n bfloat16, may be NULL) receives the rounded updated parameters.
  * t >= 1 counts updates. */

@@ -219,3 +219,33 @@ def test_softmax_xent_bad_target(torch_cuda):
     tg = torch.tensor([0, 1, 64, 3], dtype=torch.int32, device="cuda")
     with pytest.raises(ops.OpError, match="TOKEN"):
         ops.softmax_xent(logits, tg, 64, 0.25)
+
+
+# ---------------------------------------------------------------- fused linear-layer epilogues
+@pytest.mark.parametrize("M,N,K", [(300, 256, 128), (1024, 3072, 768), (257, 768, 3072)])
+def test_matmul_fused_epilogues(torch_cuda, M, N, K):
+    """The residual, bias+GELU and GELU-backward epilogues of the tensor-core GEMM against the
+    oracle's gelu_forward / gelu_backward (llm.c §1.9, §1.10) on the same bf16 operands."""
+    torch = torch_cuda
+    from gpt_train_step_arena_b300 import ops, _native as N_
+    rng = np.random.default_rng(M + N + K)
+    bf = torch.bfloat16
+    A = _to(torch, rng.normal(size=(M, K)).astype(np.float32) * 0.5, bf)
+    W = _to(torch, rng.normal(size=(N, K)).astype(np.float32) / np.sqrt(K), bf)
+    bias = _to(torch, rng.normal(size=N).astype(np.float32) * 0.1, torch.float32)
+    R = _to(torch, rng.normal(size=(M, N)).astype(np.float32), bf)
+    P = _to(torch, rng.normal(size=(M, N)).astype(np.float32) * 2, bf)
+    a, w, b, r, pp = _np(A), _np(W), _np(bias), _np(R), _np(P)
+    acc = a @ w.T
+    # bias + residual
+    D = ops.linear_fused(A, W, N_.GPT2_EPI_STORE, bias=bias, R=R)
+    assert _rel(_np(D), acc + b + r) <= 8e-3
+    # bias + GELU: the pre-activation and its GELU, both rounded once to bf16
+    D, G = ops.linear_fused(A, W, N_.GPT2_EPI_GELU, bias=bias)
+    pre = acc + b
+    assert _rel(_np(D), pre) <= 8e-3
+    assert _rel(_np(G), o64.gelu(pre)) <= 8e-3
+    # GELU backward in the input-gradient layout (W stored (K, N)): (A . W) * gelu'(P)
+    Wt = W.t().contiguous()
+    D = ops.linear_fused(A, Wt, N_.GPT2_EPI_GELU_BWD, P=P, b_kmajor=False)
+    assert _rel(_np(D), o64.gelu_backward(pp, acc)) <= 8e-3
