@@ -39,13 +39,16 @@ namespace tc {
 constexpr int BM = 128, BK = 64, UMMA_K = 16;  // rows per MMA (one accumulator half)
 constexpr int GROUP_M = 8;     // tile order: m fastest within groups of GROUP_M row tiles
 
-// epilogues: bf16 store (+bias, +residual), GELU (two bf16 outputs), times GELU' of the
-// pre-activation, fp32 split-K partial, fp32 store
-enum { E_STORE = 0, E_GELU = 1, E_GELU_BWD = 2, E_PARTIAL = 3, E_STORE_F32 = 4 };
+// epilogues: bf16 store (+bias), GELU (two bf16 outputs), times GELU' of the pre-activation,
+// fp32 split-K partial, fp32 store, bf16 store of + bias + residual
+enum { E_STORE = 0, E_GELU = 1, E_GELU_BWD = 2, E_PARTIAL = 3, E_STORE_F32 = 4, E_STORE_RES = 5 };
 template <int EPI> struct EpiOut {
     static constexpr bool F32 = EPI == E_PARTIAL || EPI == E_STORE_F32;
     static constexpr int CW = F32 ? 32 : 64;           // columns per 128-byte staged row
     static constexpr int NOUT = EPI == E_GELU ? 2 : 1;  // staged outputs per chunk
+    // a bf16 (M,N) input read per chunk (pre-activation or residual): TMA-loaded one chunk
+    // ahead into two staging buffers
+    static constexpr bool IN = EPI == E_GELU_BWD || EPI == E_STORE_RES;
 };
 
 struct Params {
@@ -74,15 +77,15 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     // each epilogue warp stages 32 rows x 128 bytes per output for the TMA store
-    static constexpr int EPI_WARP_BYTES = EpiOut<EPI>::NOUT * 4096;
+    static constexpr int EPI_WARP_BYTES = (EpiOut<EPI>::NOUT + (EpiOut<EPI>::IN ? 2 : 0)) * 4096;
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
-    static constexpr int SMEM_LIMIT = 227 * 1024 - 1024 /*align*/ - 256 /*barriers*/;
+    static constexpr int SMEM_LIMIT = 227 * 1024 - 1024 /*align*/ - 512 /*barriers*/;
     static constexpr int STAGES_FIT = (SMEM_LIMIT - EPI_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
     static constexpr int ACC_COLS = HALVES * BN;
     static constexpr int ACC_BUFS = (512 / ACC_COLS) >= 2 ? 2 : 1;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 /*align*/ + 512 /*barriers*/;
     static_assert(STAGES >= 2, "shared memory too small for the pipeline");
 };
 
@@ -106,30 +109,35 @@ G2_DEV void unit_coords(const Params& p, int u, int& m_blk, int& n_blk, int& spl
 // accumulator values, then the row written into the warp's staging buffer (32 rows x 128
 // bytes, the 128-byte swizzle a TMA store expects).  Columns past N carry garbage the
 // store does not write.
+// this thread's row (64 bf16) of a staged input buffer, unswizzled
+G2_DEV void unstage_row_bf16(const uint8_t* buf, int lane, float* x) {
+    const uint8_t* row = buf + lane * 128;
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+        const uint4 u = *reinterpret_cast<const uint4*>(row + ((c ^ (lane & 7)) << 4));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float2 f = __bfloat1622float2(h[i]);
+            x[8 * c + 2 * i] = f.x;
+            x[8 * c + 2 * i + 1] = f.y;
+        }
+    }
+}
+
 template <int EPI>
-G2_DEV void epilogue_math(const Params& p, float* v, int gm, int gn0) {
+G2_DEV void epilogue_math(const Params& p, float* v, const uint8_t* in_row_buf, int lane, int gn0) {
     constexpr int CW = EpiOut<EPI>::CW;
     const int N = p.N;
     const bool full = gn0 + CW <= N;
+    if (EPI == E_PARTIAL) return;
     if (EPI == E_GELU_BWD) {
-        if (gm < p.M) {
-            const bf16* pre = p.P + (size_t)gm * p.ldp + gn0;
-            if (full) {
+        float x[CW];
+        unstage_row_bf16(in_row_buf, lane, x);
 #pragma unroll
-                for (int i = 0; i < CW; i += 8) {
-                    float x[8];
-                    Vec8<bf16>::load(pre + i, x);
-#pragma unroll
-                    for (int j = 0; j < 8; j++) v[i + j] *= gelu_tanh_grad_fast(x[j]);
-                }
-            } else {
-                for (int i = 0; i < CW; i++)
-                    if (gn0 + i < N) v[i] *= gelu_tanh_grad_fast(__bfloat162float(pre[i]));
-            }
-        }
+        for (int i = 0; i < CW; i++) v[i] *= gelu_tanh_grad_fast(x[i]);
         return;
     }
-    if (EPI == E_PARTIAL) return;
     if (p.bias) {
         if (full) {
 #pragma unroll
@@ -142,20 +150,11 @@ G2_DEV void epilogue_math(const Params& p, float* v, int gm, int gn0) {
                 if (gn0 + i < N) v[i] += p.bias[gn0 + i];
         }
     }
-    if (p.R && gm < p.M) {
-        const bf16* r = p.R + (size_t)gm * p.ldr + gn0;
-        if (full) {
+    if (EPI == E_STORE_RES) {
+        float x[CW];
+        unstage_row_bf16(in_row_buf, lane, x);
 #pragma unroll
-            for (int i = 0; i < CW; i += 8) {
-                float x[8];
-                Vec8<bf16>::load(r + i, x);
-#pragma unroll
-                for (int j = 0; j < 8; j++) v[i + j] += x[j];
-            }
-        } else {
-            for (int i = 0; i < CW; i++)
-                if (gn0 + i < N) v[i] += __bfloat162float(r[i]);
-        }
+        for (int i = 0; i < CW; i++) v[i] += x[i];
     }
 }
 
@@ -186,7 +185,7 @@ template <int BN, int BMT, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
-                   const Params p) {
+                   const __grid_constant__ CUtensorMap tmX, const Params p) {
     using CF = Cfg<BN, BMT, EPI>;
     using EO = EpiOut<EPI>;
     constexpr int S = CF::STAGES, NB = CF::ACC_BUFS;
@@ -199,7 +198,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
     uint64_t* tfull_bar = bars + 2 * S;         // [NB]
     uint64_t* tempty_bar = bars + 2 * S + NB;   // [NB]
     uint64_t* drain_bar = bars + 2 * S + 2 * NB;
-    uint32_t* tmem_slot = (uint32_t*)(drain_bar + 1);
+    uint64_t* in_bar = drain_bar + 1;  // [EPI_WARPS][2]: staged epilogue inputs
+    uint32_t* tmem_slot = (uint32_t*)(in_bar + 2 * CF::EPI_WARPS);
     __shared__ int s_abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
             mbar_init(&tempty_bar[i], CF::EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
+        for (int i = 0; i < 2 * CF::EPI_WARPS; i++) mbar_init(&in_bar[i], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tma_prefetch_desc(&tmA);
@@ -355,6 +356,9 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
         const int hh = (warp - 2) >> 2;
         const int row_in_tile = hh * BM + quarter * 32 + lane;
         uint8_t* stg = epi_smem + (warp - 2) * CF::EPI_WARP_BYTES;  // this warp's staging
+        uint8_t* inb = stg + EO::NOUT * 4096;                       // its two input buffers
+        uint64_t* ibar = in_bar + 2 * (warp - 2);
+        uint32_t in_par = 0;  // bit b: parity of input buffer b's next completion
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
@@ -366,13 +370,34 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
             const int gm = mb * BMT + row_in_tile;
             const int gm0 = gm - lane;  // first row of this warp's 32
             const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * CF::ACC_COLS + hh * BN);
+            constexpr int NCH = BN / EO::CW;
+            if (EO::IN && lane == 0) {  // the first chunk's input
+                mbar_expect_tx(&ibar[0], 4096);
+                tma_load_2d(&tmX, &ibar[0], inb, nb * BN, gm0);
+            }
+            bool in_ok = true;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += EO::CW) {
+            for (int ch = 0; ch < NCH; ch++) {
+                const int c0 = ch * EO::CW;
+                const int gn0 = nb * BN + c0;
+                const int ib = ch & 1;
+                if (EO::IN) {
+                    // the next chunk's input into the other buffer (read one chunk ago)
+                    __syncwarp();
+                    if (lane == 0 && ch + 1 < NCH) {
+                        mbar_expect_tx(&ibar[ib ^ 1], 4096);
+                        tma_load_2d(&tmX, &ibar[ib ^ 1], inb + (ib ^ 1) * 4096, gn0 + EO::CW, gm0);
+                    }
+                }
                 float v[EO::CW];
                 tmem_ld32(trow + c0, v);
                 if (EO::CW == 64) tmem_ld32(trow + c0 + 32, v + 32);
-                const int gn0 = nb * BN + c0;
-                epilogue_math<EPI>(p, v, gm, gn0);
+                if (EO::IN) {
+                    const bool ok_in = mbar_wait(&ibar[ib], (in_par >> ib) & 1, abort_flag, p.flags);
+                    in_par ^= 1u << ib;
+                    if (!__all_sync(0xffffffffu, ok_in)) in_ok = false;
+                }
+                epilogue_math<EPI>(p, v, inb + ib * 4096, lane, gn0);
                 // the previous chunk's stores have finished reading the staging buffers
                 if (lane == 0) bulk_wait_read0();
                 __syncwarp();
@@ -384,13 +409,23 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
                 }
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0 && gm0 < p.M && gn0 < p.N) {
+                if (lane == 0 && gm0 < p.M && gn0 < p.N && in_ok) {
                     if (EPI == E_PARTIAL)
                         tma_store_3d(&tmD, stg, gn0, gm0, sp);
                     else
                         tma_store_2d(&tmD, stg, gn0, gm0);
                     if (EPI == E_GELU) tma_store_2d(&tmD2, stg + 4096, gn0, gm0);
                     bulk_commit();
+                }
+                if (!in_ok) {
+                    // a wait gave up: let the next chunk's load (if issued) land before leaving
+                    if (lane == 0 && ch + 1 < NCH) {
+                        unsigned long long t0 = globaltimer();
+                        while (!mbar_try_wait(&ibar[ib ^ 1], (in_par >> (ib ^ 1)) & 1) && globaltimer() - t0 < TIMEOUT_NS) {
+                        }
+                    }
+                    __syncwarp();
+                    break;
                 }
             }
             tc_fence_before();
@@ -435,7 +470,7 @@ static int num_sms() {
 
 template <int BN, int BMT, bool A_MN, bool B_MN, int EPI>
 static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
-                            const CUtensorMap& td2, const Params& p, cudaStream_t s) {
+                            const CUtensorMap& td2, const CUtensorMap& tx, const Params& p, cudaStream_t s) {
     using CF = Cfg<BN, BMT, EPI>;
     auto kern = gemm_tc_kernel<BN, BMT, A_MN, B_MN, EPI>;
     static bool attr_done = false;
@@ -445,26 +480,26 @@ static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const 
         attr_done = true;
     }
     int grid = std::min(p.num_units, num_sms());
-    G2_LAUNCH kern<<<grid, CF::THREADS, CF::SMEM_BYTES, s>>>(ta, tb, td, td2, p);
+    G2_LAUNCH kern<<<grid, CF::THREADS, CF::SMEM_BYTES, s>>>(ta, tb, td, td2, tx, p);
     return cudaGetLastError();
 }
 
 struct Maps {
-    CUtensorMap a, b, d, d2;
+    CUtensorMap a, b, d, d2, x;
 };
 
 template <int BN, int EPI>
 static cudaError_t launch_layout(int bmt, bool a_mn, bool b_mn, const Maps& m, const Params& p, cudaStream_t s) {
     if (bmt == 256) {
-        if (!a_mn && !b_mn) return launch_t<BN, 256, false, false, EPI>(m.a, m.b, m.d, m.d2, p, s);
-        if (!a_mn && b_mn) return launch_t<BN, 256, false, true, EPI>(m.a, m.b, m.d, m.d2, p, s);
-        if (a_mn && b_mn) return launch_t<BN, 256, true, true, EPI>(m.a, m.b, m.d, m.d2, p, s);
-        return launch_t<BN, 256, true, false, EPI>(m.a, m.b, m.d, m.d2, p, s);
+        if (!a_mn && !b_mn) return launch_t<BN, 256, false, false, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
+        if (!a_mn && b_mn) return launch_t<BN, 256, false, true, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
+        if (a_mn && b_mn) return launch_t<BN, 256, true, true, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
+        return launch_t<BN, 256, true, false, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
     }
-    if (!a_mn && !b_mn) return launch_t<BN, 128, false, false, EPI>(m.a, m.b, m.d, m.d2, p, s);
-    if (!a_mn && b_mn) return launch_t<BN, 128, false, true, EPI>(m.a, m.b, m.d, m.d2, p, s);
-    if (a_mn && b_mn) return launch_t<BN, 128, true, true, EPI>(m.a, m.b, m.d, m.d2, p, s);
-    return launch_t<BN, 128, true, false, EPI>(m.a, m.b, m.d, m.d2, p, s);
+    if (!a_mn && !b_mn) return launch_t<BN, 128, false, false, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
+    if (!a_mn && b_mn) return launch_t<BN, 128, false, true, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
+    if (a_mn && b_mn) return launch_t<BN, 128, true, true, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
+    return launch_t<BN, 128, true, false, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
 }
 
 }  // namespace tc
@@ -489,9 +524,9 @@ static int* fallback_flag() {
 // leave no room in tensor memory for a second accumulator, so their epilogue does not
 // overlap the next tile; they pay off for long K (many K blocks per tile) when there are
 // plenty of tiles.  Otherwise 128-row tiles with double-buffered accumulators.
-static int tile_rows(int M, int N, int K, int BN) {
+static int tile_rows(int M, int N, int K, int BN, bool staged_input = false) {
     const long long tiles128 = (long long)((M + 127) / 128) * ((N + BN - 1) / BN);
-    return (K >= 2048 && tiles128 >= 4LL * num_sms()) ? 256 : 128;
+    return (!staged_input && K >= 2048 && tiles128 >= 4LL * num_sms()) ? 256 : 128;
 }
 
 // Split-K plan for a product with few output tiles and a long K.
@@ -530,6 +565,7 @@ bool gemm_tc_supported(const GemmArgs& a) {
     if (a.epi == EPI_GELU && (!a.D2 || (a.ldd2 % 8) || !aligned16(a.D2))) return false;
     if (a.epi == EPI_GELU_BWD && (!a.P || (a.ldp % 8) || !aligned16(a.P))) return false;
     if (a.R && ((a.ldr % 8) || !aligned16(a.R))) return false;
+    if (a.R && a.d_f32) return false;  // the residual epilogue writes bf16 only
     if (a.bias && !aligned16(a.bias)) return false;
     return true;
 }
@@ -537,7 +573,8 @@ bool gemm_tc_supported(const GemmArgs& a) {
 cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, cudaStream_t s) {
     const bool a_mn = a.sAk != 1, b_mn = a.sBk != 1;
     const int BN = a.N > 128 ? 256 : 128;
-    const int bmt = tile_rows(a.M, a.N, a.K, BN);
+    const bool staged_in = a.epi == EPI_GELU_BWD || (a.epi == EPI_STORE && a.R && !a.d_f32);
+    const int bmt = tile_rows(a.M, a.N, a.K, BN, staged_in);
     Maps mp;
     bool ok;
     if (!a_mn)
@@ -587,6 +624,15 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
     }
     if (!ok) return cudaErrorInvalidValue;
     mp.d2 = mp.d;
+    mp.x = mp.d;
+    const bool has_in = staged_in;
+    if (has_in) {
+        const void* xb = a.epi == EPI_GELU_BWD ? a.P : a.R;
+        const long long ldx = a.epi == EPI_GELU_BWD ? a.ldp : a.ldr;
+        const uint64_t dims[2] = {(uint64_t)a.N, (uint64_t)a.M};
+        const uint64_t st[1] = {(uint64_t)ldx * 2};
+        if (!make_map_nd(&mp.x, xb, false, 2, dims, st, box_bf16)) return cudaErrorInvalidValue;
+    }
     if (a.epi == EPI_GELU) {
         const uint64_t dims[2] = {(uint64_t)a.N, (uint64_t)a.M};
         const uint64_t st[1] = {(uint64_t)a.ldd2 * 2};
@@ -614,6 +660,9 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
             if (a.d_f32)
                 return BN == 256 ? launch_layout<256, E_STORE_F32>(bmt, a_mn, b_mn, mp, p, s)
                                  : launch_layout<128, E_STORE_F32>(bmt, a_mn, b_mn, mp, p, s);
+            if (has_in)
+                return BN == 256 ? launch_layout<256, E_STORE_RES>(bmt, a_mn, b_mn, mp, p, s)
+                                 : launch_layout<128, E_STORE_RES>(bmt, a_mn, b_mn, mp, p, s);
             return BN == 256 ? launch_layout<256, E_STORE>(bmt, a_mn, b_mn, mp, p, s)
                              : launch_layout<128, E_STORE>(bmt, a_mn, b_mn, mp, p, s);
     }
