@@ -333,8 +333,8 @@ __global__ void __launch_bounds__(NTH, 2)
 // ------------------------------------------------------------------ backward
 // llm.c §1.8 attention_backward, without atomics and without the (T, T) buffers: P is
 // rebuilt from the forward's log-sum-exp L and D = rowsum(dO * O), dS = P * (dP - D).
-// Two kernels of one template, 320 threads (TMA warp, MMA warp, 8 softmax warps: two
-// per tensor-memory lane quarter, each taking 32 of a half's 64 columns), one CTA per SM:
+// Two kernels of one template, 320 threads (TMA warp, MMA warp, 8 softmax warps: two per
+// tensor-memory lane quarter, each taking 32 of a half's 64 columns), two CTAs per SM:
 //   DQ = true   (query-major, runs first): the CTA owns 128 queries of one head and
 //               streams K_j and V_j for j <= the query tile.  Its softmax threads first
 //               compute D for their own rows (and store it for the other kernel); then
@@ -343,30 +343,30 @@ __global__ void __launch_bounds__(NTH, 2)
 //               key tile; S^T = K Q^T, dP^T = V dO^T, P^T and dS^T = P^T (dP^T - D) with
 //               L and D of the query columns staged in shared memory; dV += P^T dO,
 //               dK += dS^T Q.
-// Operand placement keeps shared-memory traffic to the streamed tiles (the B operands):
-// the CTA's own rows (Q and dO, or K and V) are written into tensor memory once and used
-// as the A operand of the S and dP products; P and dS are written back (bf16) over the
-// S and dP columns each thread has read and used as the A operand of the accumulation
-// products.  Each streamed 128-row tile is processed in two 64-column halves with their
-// own tensor-memory buffers, so one half's products overlap the other half's softmax;
-// the tensor core runs each buffer's accumulation before its next S and dP in issue
-// order.
+// Each streamed 128-row tile is processed in two 64-column halves through one tensor-
+// memory buffer (S at column 0, dP at 64); P and dS are written back (bf16) over the
+// columns each thread read and are the A operand of the accumulation products, which the
+// tensor core runs before the next half's S and dP overwrite the buffer.  A CTA's chain
+// (products -> softmax -> products) is serial; the second CTA on the SM fills the gaps:
+// one CTA per SM issues these 64-column products at about 85 clocks each, two reach
+// about 58 (the tensor core's own rate is 45-48).
+// Tensor memory (256 columns): the half buffer at 0-127, dQ (or dV) at 128, dK at 192; the
+// query-major CTA's own rows Q and dO (A operands of S and dP) at 192 and 224.  The key-
+// major CTA keeps K and V in shared memory instead.
 struct BwdBars {
-    uint64_t row_full, st_full[3], st_empty[3], sdp_full[2], pds_full[2], stats[2], acc_done, drain;
+    uint64_t row_full, st_full[2], st_empty[2], sdp_full, pds_full, stats[2], acc_done, drain;
     uint32_t tmem_slot;
     int abort;
 };
-constexpr int NSTAGE = 3;  // streamed 128-row tiles in flight: A (16 KB) + B (16 KB) each
-constexpr int B_STATS = NSTAGE * 2 * TILE;  // key-major: L, D of 2 x 128 query columns
+constexpr int B_ROWS = 0;                 // key-major: K, V tiles (32 KB)
+constexpr int B_ST = 2 * TILE;            // streamed stages: 2 x (A 16 KB + B 16 KB)
+constexpr int B_STATS = B_ST + 4 * TILE;  // key-major: L, D of 2 x 128 query columns
 constexpr int B_BAR = B_STATS + 2 * 2 * 128 * 4;
 constexpr int BWD_SMEM = B_BAR + (int)sizeof(BwdBars);
-// tensor memory: half h's S at 128h, dP at 128h + 64 (P and dS written back over their
-// first 16 + 16 columns per column group); accumulators dQ or dV at 256, dK at 320; the
-// CTA's rows (A operands of S and dP) at 384 and 416
-constexpr uint32_t TB_COLS = 512, TB_ACC1 = 256, TB_ACC2 = 320, TB_RA = 384, TB_RB = 416;
+constexpr uint32_t TB_COLS = 256, TB_ACC1 = 128, TB_ACC2 = 192, TB_RA = 192, TB_RB = 224;
 
 template <bool DQ>
-__global__ void __launch_bounds__(NTH_BWD, 1)
+__global__ void __launch_bounds__(NTH_BWD, 2)
     attn_bwd_tc_k(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                   bf16* dqkv, const bf16* qkv, const bf16* dout, const bf16* outp, const float* lse, float* Dbuf,
                   int T, int C, int NH, int* flags) {
@@ -390,16 +390,14 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
 
     if (threadIdx.x == 0) {
         bar->abort = 0;
-        mbar_init(&bar->row_full, 8);
-        for (int i = 0; i < NSTAGE; i++) {
+        mbar_init(&bar->row_full, DQ ? 8 : 1);  // softmax warps' tensor-memory rows, or TMA
+        for (int i = 0; i < 2; i++) {
             mbar_init(&bar->st_full[i], 1);
             mbar_init(&bar->st_empty[i], 1);
-        }
-        for (int i = 0; i < 2; i++) {
-            mbar_init(&bar->sdp_full[i], 1);
-            mbar_init(&bar->pds_full[i], 8);
             mbar_init(&bar->stats[i], 256);
         }
+        mbar_init(&bar->sdp_full, 1);
+        mbar_init(&bar->pds_full, 8);
         mbar_init(&bar->acc_done, 1);
         mbar_init(&bar->drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -415,32 +413,41 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
     volatile int* abort_flag = &bar->abort;
 
     if (warp == 0) {
-        // ---------------- TMA producer: the streamed tiles
+        // ---------------- TMA producer: the key-major CTA's K and V, then the streamed tiles
         if (lane == 0) {
-            for (int n = NSTAGE; n < nst; n++) {
+            if (!DQ) {
+                mbar_expect_tx(&bar->row_full, 2 * TILE);
+                tma_load_2d(&tm_qkv, &bar->row_full, smem + B_ROWS, C + h * HS, row0 + r0);
+                tma_load_2d(&tm_qkv, &bar->row_full, smem + B_ROWS + TILE, 2 * C + h * HS, row0 + r0);
+            }
+            for (int n = 2; n < nst; n++) {
                 tma_prefetch_l2(&tm_qkv, xa_st, row0 + (st0 + n) * 128);
                 tma_prefetch_l2(map_b_st, xb_st, row0 + (st0 + n) * 128);
             }
-            int issued[NSTAGE];
-            for (int i = 0; i < NSTAGE; i++) issued[i] = -1;
+            int issued[2] = {-1, -1};
             bool ok = true;
             for (int n = 0; n < nst; n++) {
-                const int s = n % NSTAGE;
-                const uint32_t ph = (n / NSTAGE) & 1;
+                const int s = n & 1;
+                const uint32_t ph = (n >> 1) & 1;
                 if (!mbar_wait(&bar->st_empty[s], ph ^ 1, abort_flag, flags)) {
                     ok = false;
                     break;
                 }
                 mbar_expect_tx(&bar->st_full[s], 2 * TILE);
-                uint8_t* st = smem + s * 2 * TILE;
+                uint8_t* st = smem + B_ST + s * 2 * TILE;
                 tma_load_2d(&tm_qkv, &bar->st_full[s], st, xa_st, row0 + (st0 + n) * 128);
                 tma_load_2d(map_b_st, &bar->st_full[s], st + TILE, xb_st, row0 + (st0 + n) * 128);
                 issued[s] = (int)ph;
             }
             if (!ok) {
-                for (int s = 0; s < NSTAGE; s++) {
+                unsigned long long t0 = globaltimer();
+                if (!DQ) {
+                    while (!mbar_try_wait(&bar->row_full, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+                    }
+                }
+                for (int s = 0; s < 2; s++) {
                     if (issued[s] < 0) continue;
-                    unsigned long long t0 = globaltimer();
+                    t0 = globaltimer();
                     while (!mbar_try_wait(&bar->st_full[s], (uint32_t)issued[s]) && globaltimer() - t0 < TIMEOUT_NS) {
                     }
                 }
@@ -455,30 +462,38 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
             const int nhalves = 2 * nst;
             bool ok = mbar_wait(&bar->row_full, 0, abort_flag, flags);
             bool issued_any = false;
-            // S and dP of half g (tile g/2, columns 64 (g%2) ..): A = the CTA's rows in
-            // tensor memory, B = the streamed rows of the half (K-major)
+            // S and dP of half g (tile g/2, columns 64 (g%2) ..): A = the CTA's rows (tensor
+            // memory, or shared memory for K and V), B = the streamed rows of the half
             auto issue_sdp = [&](int g) -> bool {
-                const int n = g >> 1, hh = g & 1, s = n % NSTAGE;
-                if (hh == 0 && !mbar_wait(&bar->st_full[s], (n / NSTAGE) & 1, abort_flag, flags)) return false;
+                const int n = g >> 1, hh = g & 1, s = n & 1;
+                if (hh == 0 && !mbar_wait(&bar->st_full[s], (n >> 1) & 1, abort_flag, flags)) return false;
                 tc_fence_after();
-                const uint32_t sA = sbase + s * 2 * TILE + hh * 8192, sB = sA + TILE;
-                const uint32_t tS = tmem + hh * 128;
+                const uint32_t sA = sbase + B_ST + s * 2 * TILE + hh * 8192, sB = sA + TILE;
 #pragma unroll
-                for (int k = 0; k < HS / 16; k++)
-                    umma_bf16_ts(tS, tmem + TB_RA + k * 8, sdesc(sA + k * 32, 16, 1024), ID_SDP, k > 0 ? 1u : 0u);
+                for (int k = 0; k < HS / 16; k++) {
+                    const uint64_t bd = sdesc(sA + k * 32, 16, 1024);
+                    if (DQ)
+                        umma_bf16_ts(tmem, tmem + TB_RA + k * 8, bd, ID_SDP, k > 0 ? 1u : 0u);
+                    else
+                        umma_bf16(tmem, sdesc(sbase + B_ROWS + k * 32, 16, 1024), bd, ID_SDP, k > 0 ? 1u : 0u);
+                }
 #pragma unroll
-                for (int k = 0; k < HS / 16; k++)
-                    umma_bf16_ts(tS + 64, tmem + TB_RB + k * 8, sdesc(sB + k * 32, 16, 1024), ID_SDP,
-                                 k > 0 ? 1u : 0u);
-                umma_commit(&bar->sdp_full[hh]);
+                for (int k = 0; k < HS / 16; k++) {
+                    const uint64_t bd = sdesc(sB + k * 32, 16, 1024);
+                    if (DQ)
+                        umma_bf16_ts(tmem + 64, tmem + TB_RB + k * 8, bd, ID_SDP, k > 0 ? 1u : 0u);
+                    else
+                        umma_bf16(tmem + 64, sdesc(sbase + B_ROWS + TILE + k * 32, 16, 1024), bd, ID_SDP,
+                                  k > 0 ? 1u : 0u);
+                }
+                umma_commit(&bar->sdp_full);
                 issued_any = true;
                 return true;
             };
             if (ok) ok = issue_sdp(0);
-            if (ok && nhalves > 1) ok = issue_sdp(1);
             for (int g = 0; ok && g < nhalves; g++) {
-                const int n = g >> 1, hh = g & 1, s = n % NSTAGE;
-                if (!mbar_wait(&bar->pds_full[hh], n & 1, abort_flag, flags)) {
+                const int n = g >> 1, hh = g & 1, s = n & 1;
+                if (!mbar_wait(&bar->pds_full, g & 1, abort_flag, flags)) {
                     ok = false;
                     break;
                 }
@@ -486,26 +501,25 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
                 // accumulation of half g: A = P or dS in tensor memory (column group c of the
                 // half at 32c, 16 columns = 32 rows of the contraction each), B = the
                 // streamed rows of the half read N-major (64 hs wide)
-                const uint32_t sA = sbase + s * 2 * TILE + hh * 8192, sB = sA + TILE;
-                const uint32_t tH = tmem + hh * 128;
+                const uint32_t sA = sbase + B_ST + s * 2 * TILE + hh * 8192, sB = sA + TILE;
 #pragma unroll
                 for (int k = 0; k < 64 / 16; k++) {
                     const uint32_t acc = (g > 0 || k > 0) ? 1u : 0u;
                     const uint32_t a_off = (k >> 1) * 32 + (k & 1) * 8;
                     const uint64_t bA = sdesc(sA + k * 2048, 8192, 1024);
                     if (DQ) {
-                        umma_bf16_ts(tmem + TB_ACC1, tH + 64 + a_off, bA, ID_ACC, acc);  // dQ += dS K
+                        umma_bf16_ts(tmem + TB_ACC1, tmem + 64 + a_off, bA, ID_ACC, acc);  // dQ += dS K
                     } else {
                         const uint64_t bB = sdesc(sB + k * 2048, 8192, 1024);
-                        umma_bf16_ts(tmem + TB_ACC1, tH + a_off, bB, ID_ACC, acc);       // dV += P^T dO
-                        umma_bf16_ts(tmem + TB_ACC2, tH + 64 + a_off, bA, ID_ACC, acc);  // dK += dS^T Q
+                        umma_bf16_ts(tmem + TB_ACC1, tmem + a_off, bB, ID_ACC, acc);       // dV += P^T dO
+                        umma_bf16_ts(tmem + TB_ACC2, tmem + 64 + a_off, bA, ID_ACC, acc);  // dK += dS^T Q
                     }
                 }
                 issued_any = true;
                 if (hh == 1) umma_commit(&bar->st_empty[s]);
                 if (g == nhalves - 1) umma_commit(&bar->acc_done);
-                // the same buffer's next S and dP follow this accumulation on the tensor core
-                if (g + 2 < nhalves && !issue_sdp(g + 2)) ok = false;
+                // the next half's S and dP follow this accumulation on the tensor core
+                if (g + 1 < nhalves && !issue_sdp(g + 1)) ok = false;
             }
             if (!ok && issued_any) {
                 umma_commit(&bar->drain);
@@ -525,30 +539,27 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
         float* Ls = reinterpret_cast<float*>(smem + B_STATS);  // [2][128] (key-major only)
         float* Dsm = Ls + 2 * 128;
         float nL = 0.f, nD = 0.f;  // key-major: this thread's query column of the next tile
-        {
-            // this row of the CTA's two A operands into tensor memory: group 0 writes Q (DQ)
-            // or K, group 1 dO or V; 64 bf16 = 32 packed columns
-            uint32_t rv[32];
-            const bf16* src;
-            if (DQ)
-                src = sub == 0 ? qkv + (size_t)(row0 + grow) * 3 * C + h * HS : dout + (size_t)(row0 + grow) * C + h * HS;
-            else
-                src = qkv + (size_t)(row0 + grow) * 3 * C + (sub == 0 ? C : 2 * C) + h * HS;
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                const uint4 u = grow < T ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0, 0, 0, 0);
-                rv[4 * i] = u.x;
-                rv[4 * i + 1] = u.y;
-                rv[4 * i + 2] = u.z;
-                rv[4 * i + 3] = u.w;
-            }
-            tmem_st32u(tmem + lane_off + (sub == 0 ? TB_RA : TB_RB), rv);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->row_full);
-        }
         if (DQ) {
+            // this row's Q (group 0) or dO (group 1) into tensor memory: the A operands of S
+            // and dP, 64 bf16 = 32 packed columns
+            {
+                uint32_t rv[32];
+                const bf16* src = sub == 0 ? qkv + (size_t)(row0 + grow) * 3 * C + h * HS
+                                           : dout + (size_t)(row0 + grow) * C + h * HS;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const uint4 u = grow < T ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0, 0, 0, 0);
+                    rv[4 * i] = u.x;
+                    rv[4 * i + 1] = u.y;
+                    rv[4 * i + 2] = u.z;
+                    rv[4 * i + 3] = u.w;
+                }
+                tmem_st32u(tmem + lane_off + (sub == 0 ? TB_RA : TB_RB), rv);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->row_full);
+            }
             // D = rowsum(dO * O) for this row (both column groups need it; group 0 stores
             // it for the key-major kernel)
             if (grow < T) {
@@ -597,56 +608,63 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
             }
             const bool diag = (st0 + n) == rt;
             for (int hh = 0; hh < 2; hh++) {
-                ok = mbar_wait(&bar->sdp_full[hh], n & 1, abort_flag, flags);
+                const int g = 2 * n + hh;
+                ok = mbar_wait(&bar->sdp_full, g & 1, abort_flag, flags);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t sv[32], dv[32];
-                const uint32_t tS = tmem + lane_off + hh * 128 + sub * 32;
-                tmem_ld32_raw(tS, sv);
-                tmem_ld32_raw(tS + 64, dv);
-                tmem_wait_ld();
-                uint32_t pk[16], dk[16];
-                const int cbase = hh * 64 + sub * 32;  // column offset within the streamed tile
+                // 32 columns in two rounds of 16: S and dP in, P and dS (8 packed columns
+                // each) written back over the first half of what this thread read
 #pragma unroll
-                for (int c4 = 0; c4 < 32; c4 += 4) {
-                    float Lc[4], Dc[4];
-                    if (DQ) {
+                for (int rd = 0; rd < 2; rd++) {
+                    uint32_t sv[16], dv[16];
+                    const uint32_t tS = tmem + lane_off + sub * 32 + rd * 16;
+                    tmem_ld16_raw(tS, sv);
+                    tmem_ld16_raw(tS + 64, dv);
+                    tmem_wait_ld();
+                    uint32_t pk[8], dk[8];
+                    const int cbase = hh * 64 + sub * 32 + rd * 16;  // column within the streamed tile
+#pragma unroll
+                    for (int c4 = 0; c4 < 16; c4 += 4) {
+                        float Lc[4], Dc[4];
+                        if (DQ) {
+#pragma unroll
+                            for (int e = 0; e < 4; e++) {
+                                Lc[e] = L2_row;
+                                Dc[e] = D_row;
+                            }
+                        } else {
+                            const float4 l4 = *reinterpret_cast<const float4*>(Ls + slot * 128 + cbase + c4);
+                            const float4 d4 = *reinterpret_cast<const float4*>(Dsm + slot * 128 + cbase + c4);
+                            Lc[0] = l4.x; Lc[1] = l4.y; Lc[2] = l4.z; Lc[3] = l4.w;
+                            Dc[0] = d4.x; Dc[1] = d4.y; Dc[2] = d4.z; Dc[3] = d4.w;
+                        }
+                        float pv[4], dsv[4];
 #pragma unroll
                         for (int e = 0; e < 4; e++) {
-                            Lc[e] = L2_row;
-                            Dc[e] = D_row;
+                            const int c = cbase + c4 + e;
+                            // causal: key <= query; DQ rows are queries, key-major rows are keys
+                            const bool vis = !diag || (DQ ? c <= r : r <= c);
+                            const float pr = vis ? ex2(fmaf(__uint_as_float(sv[c4 + e]), sl2, -Lc[e])) : 0.f;
+                            pv[e] = pr;
+                            dsv[e] = pr * (__uint_as_float(dv[c4 + e]) - Dc[e]);
                         }
-                    } else {
-                        const float4 l4 = *reinterpret_cast<const float4*>(Ls + slot * 128 + cbase + c4);
-                        const float4 d4 = *reinterpret_cast<const float4*>(Dsm + slot * 128 + cbase + c4);
-                        Lc[0] = l4.x; Lc[1] = l4.y; Lc[2] = l4.z; Lc[3] = l4.w;
-                        Dc[0] = d4.x; Dc[1] = d4.y; Dc[2] = d4.z; Dc[3] = d4.w;
+                        pk[c4 >> 1] = pack_bf16x2(pv[0], pv[1]);
+                        pk[(c4 >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
+                        dk[c4 >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                        dk[(c4 >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
                     }
-                    float pv[4], dsv[4];
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const int c = cbase + c4 + e;
-                        // causal: key <= query; DQ rows are queries, key-major rows are keys
-                        const bool vis = !diag || (DQ ? c <= r : r <= c);
-                        const float pr = vis ? ex2(fmaf(__uint_as_float(sv[c4 + e]), sl2, -Lc[e])) : 0.f;
-                        pv[e] = pr;
-                        dsv[e] = pr * (__uint_as_float(dv[c4 + e]) - Dc[e]);
-                    }
-                    pk[c4 >> 1] = pack_bf16x2(pv[0], pv[1]);
-                    pk[(c4 >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
-                    dk[c4 >> 1] = pack_bf16x2(dsv[0], dsv[1]);
-                    dk[(c4 >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
+                    // packed columns 8 rd .. 8 rd + 7 of this group's 16 (all already read)
+                    const uint32_t tP = tmem + lane_off + sub * 32 + rd * 8;
+                    if (!DQ) tmem_st8(tP, pk);
+                    tmem_st8(tP + 64, dk);
                 }
-                // P (key-major only) and dS over the first 16 of the 32 columns just read
-                if (!DQ) tmem_st16(tS, pk);
-                tmem_st16(tS + 64, dk);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar->pds_full[hh]);
+                if (lane == 0) mbar_arrive(&bar->pds_full);
             }
         }
         if (ok) {
@@ -656,25 +674,20 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
                 const float scale = 1.0f / sqrtf((float)HS);
                 bf16* base = dqkv + (size_t)(row0 + grow) * 3 * C + h * HS;
                 // DQ: group g stores dQ columns 32g..32g+31; key-major: group 0 dV, group 1 dK
-                float a[64];
-                if (DQ) {
-                    tmem_ld32(tmem + lane_off + TB_ACC1 + sub * 32, a);
-                } else {
-                    const uint32_t t0 = tmem + lane_off + (sub ? TB_ACC2 : TB_ACC1);
-                    tmem_ld32(t0, a);
-                    tmem_ld32(t0 + 32, a + 32);
-                }
-                if (grow < T) {
-                    const int ncol = DQ ? 32 : 64;
-                    bf16* dst = DQ ? base + sub * 32 : (sub ? base + C : base + 2 * C);
-                    const float mul = (DQ || sub) ? scale : 1.0f;
+                const int ncol = DQ ? 32 : 64;
+                bf16* dst = DQ ? base + sub * 32 : (sub ? base + C : base + 2 * C);
+                const float mul = (DQ || sub) ? scale : 1.0f;
+                const uint32_t t0 = tmem + lane_off + (DQ ? TB_ACC1 + sub * 32 : (sub ? TB_ACC2 : TB_ACC1));
+                for (int c0 = 0; c0 < ncol; c0 += 32) {
+                    float a[32];
+                    tmem_ld32(t0 + c0, a);
+                    if (grow < T) {
 #pragma unroll
-                    for (int i = 0; i < 64; i += 8) {
-                        if (i < ncol) {
+                        for (int i = 0; i < 32; i += 8) {
                             float y[8];
 #pragma unroll
                             for (int e = 0; e < 8; e++) y[e] = a[i + e] * mul;
-                            Vec8<bf16>::store(dst + i, y);
+                            Vec8<bf16>::store(dst + c0 + i, y);
                         }
                     }
                 }

@@ -526,7 +526,9 @@ static int* fallback_flag() {
 // plenty of tiles.  Otherwise 128-row tiles with double-buffered accumulators.
 static int tile_rows(int M, int N, int K, int BN, bool staged_input = false) {
     const long long tiles128 = (long long)((M + 127) / 128) * ((N + BN - 1) / BN);
-    return (!staged_input && K >= 2048 && tiles128 >= 4LL * num_sms()) ? 256 : 128;
+    const bool long_k = K >= 2048 && tiles128 >= 4LL * num_sms();
+    const bool very_many_tiles = tiles128 >= 64LL * num_sms();  // e.g. the LM head forward
+    return (!staged_input && (long_k || very_many_tiles)) ? 256 : 128;
 }
 
 // Split-K plan for a product with few output tiles and a long K.
