@@ -6,6 +6,7 @@
 // an order fixed by the launch shape (which depends only on the problem size).
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 #include <algorithm>
 #include <type_traits>
@@ -326,6 +327,127 @@ __global__ void ln_fwd_vec_k(T* out, float* mean, float* rstd, const T* inp, con
     }
 }
 
+// bf16 rows streamed through shared memory: one CTA per SM; warp 0 copies tiles of 32
+// consecutive rows (one contiguous bulk copy each) into a 3-stage ring, warps 1-8
+// normalise 4 rows of each tile from shared memory and store them.  Keeps up to three
+// tiles (3 x 32 rows) in flight per SM without holding them in registers.
+constexpr int LNT_ROWS = 32, LNT_STAGES = 3, LNT_THREADS = 288;
+
+template <int NV>
+__global__ void __launch_bounds__(LNT_THREADS, 1) ln_fwd_tma_k(bf16* out, float* mean, float* rstd, const bf16* inp,
+                                                               const float* w, const float* b, int M, int C) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tile_bytes = LNT_ROWS * C * 2;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + LNT_STAGES * tile_bytes);
+    uint64_t* empty = full + LNT_STAGES;
+    int* abort_p = reinterpret_cast<int*>(empty + LNT_STAGES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < LNT_STAGES; i++) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], 8);
+        }
+        *abort_p = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    volatile int* abort_flag = abort_p;
+    const int ntiles = (M + LNT_ROWS - 1) / LNT_ROWS;
+    if (warp == 0) {
+        if (lane == 0) {
+            int it = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, it++) {
+                const int s = it % LNT_STAGES;
+                if (!tc::mbar_wait(&empty[s], ((it / LNT_STAGES) & 1) ^ 1, abort_flag, nullptr)) break;
+                const int rows = min(LNT_ROWS, M - t * LNT_ROWS);
+                const uint32_t bytes = (uint32_t)rows * C * 2;
+                tc::mbar_expect_tx(&full[s], bytes);
+                tc::bulk_load_1d(smem + s * tile_bytes, inp + (size_t)t * LNT_ROWS * C, bytes, &full[s]);
+            }
+        }
+    } else {
+        // warps 1..8: rows (warp - 1) + 8 i of each tile
+        float wv[NV][8], bv[NV][8];
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            Vec8<float>::load(w + j * 256 + lane * 8, wv[j]);
+            Vec8<float>::load(b + j * 256 + lane * 8, bv[j]);
+        }
+        int it = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, it++) {
+            const int s = it % LNT_STAGES;
+            const bool ok = tc::mbar_wait(&full[s], (it / LNT_STAGES) & 1, abort_flag, nullptr);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const int rows = min(LNT_ROWS, M - t * LNT_ROWS);
+            const bf16* tile = reinterpret_cast<const bf16*>(smem + s * tile_bytes);
+            for (int r = warp - 1; r < rows; r += 8) {
+                const bf16* x = tile + (size_t)r * C;
+                float v[NV][8];
+                float sum = 0.f;
+#pragma unroll
+                for (int j = 0; j < NV; j++) {
+                    Vec8<bf16>::load(x + j * 256 + lane * 8, v[j]);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) sum += v[j][i];
+                }
+                const float m = warp_sum(sum) / C;
+                float q = 0.f;
+#pragma unroll
+                for (int j = 0; j < NV; j++)
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        float d = v[j][i] - m;
+                        q += d * d;
+                    }
+                const float rs = 1.0f / sqrtf(warp_sum(q) / C + 1e-5f);
+                const int row = t * LNT_ROWS + r;
+                bf16* o = out + (size_t)row * C;
+#pragma unroll
+                for (int j = 0; j < NV; j++) {
+                    float y[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i++) y[i] = (v[j][i] - m) * rs * wv[j][i] + bv[j][i];
+                    Vec8<bf16>::store(o + j * 256 + lane * 8, y);
+                }
+                if (lane == 0) {
+                    mean[row] = m;
+                    rstd[row] = rs;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&empty[s]);
+        }
+    }
+}
+
+static int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+template <int NV>
+static cudaError_t ln_fwd_tma_launch(bf16* out, float* mean, float* rstd, const bf16* inp, const float* w,
+                                     const float* b, int M, int C, cudaStream_t s) {
+    const int smem = LNT_STAGES * LNT_ROWS * C * 2 + 256;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(ln_fwd_tma_k<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             LNT_STAGES * LNT_ROWS * (NV * 256) * 2 + 256);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const int ntiles = (M + LNT_ROWS - 1) / LNT_ROWS;
+    G2_LAUNCH ln_fwd_tma_k<NV><<<std::min(ntiles, sm_count()), LNT_THREADS, smem, s>>>(out, mean, rstd, inp, w, b,
+                                                                                      M, C);
+    return cudaGetLastError();
+}
+
 template <typename T>
 __global__ void ln_fwd_gen_k(T* out, float* mean, float* rstd, const T* inp, const float* w,
                              const float* b, int M, int C) {
@@ -369,6 +491,15 @@ static void ln_fwd_launch(T* out, float* mean, float* rstd, const T* inp, const 
 cudaError_t layernorm_forward(ActType at, void* out, float* mean, float* rstd, const void* inp,
                               const float* w, const float* b, int M, int C, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
+    const bool al = ((((uintptr_t)out | (uintptr_t)inp | (uintptr_t)w | (uintptr_t)b)) & 15) == 0;
+    if (at == ACT_BF16 && al && C % 256 == 0 && C / 256 >= 1 && C / 256 <= 4) {
+        switch (C / 256) {
+            case 1: return ln_fwd_tma_launch<1>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, s);
+            case 2: return ln_fwd_tma_launch<2>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, s);
+            case 3: return ln_fwd_tma_launch<3>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, s);
+            default: return ln_fwd_tma_launch<4>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, s);
+        }
+    }
     if (at == ACT_BF16)
         ln_fwd_launch<bf16>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, s);
     else
@@ -469,6 +600,145 @@ __global__ void __launch_bounds__(128) ln_bwd_vec_k(T* dres, float* part, const 
     }
 }
 
+// bf16 backward with the rows streamed through shared memory: one CTA per SM; warp 0
+// copies tiles of 16 consecutive rows of dout, x and dres (three contiguous bulk copies)
+// into a 3-stage ring; warps 1-8 take 2 rows of each tile, update dres in global memory
+// and keep per-column sums of n*dout (dw), dout (db) and, with OUTSUM, of the stored new
+// dres in registers.  At the end each CTA writes one partial row per sum
+// (part[k][blockIdx][C]), which colreduce_k adds in block order: the summation order
+// depends on (M, C, grid) only.
+constexpr int LNB_ROWS = 16, LNB_STAGES = 3;
+
+template <int NV, bool OUTSUM>
+__global__ void __launch_bounds__(LNT_THREADS, 1)
+    ln_bwd_tma_k(bf16* dres, float* part, const bf16* dout, const bf16* inp, const float* w, const float* mean,
+                 const float* rstd, int M, int C) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int sub_bytes = LNB_ROWS * C * 2;  // one tensor's rows of a tile
+    const int stage_bytes = 3 * sub_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + LNB_STAGES * stage_bytes);
+    uint64_t* empty = full + LNB_STAGES;
+    int* abort_p = reinterpret_cast<int*>(empty + LNB_STAGES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < LNB_STAGES; i++) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], 8);
+        }
+        *abort_p = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    volatile int* abort_flag = abort_p;
+    const int ntiles = (M + LNB_ROWS - 1) / LNB_ROWS;
+    constexpr int NS = OUTSUM ? 3 : 2;
+    float aw[NV][8], ab[NV][8], ar[OUTSUM ? NV : 1][8];
+#pragma unroll
+    for (int j = 0; j < NV; j++)
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            aw[j][i] = ab[j][i] = 0.f;
+            if (OUTSUM) ar[OUTSUM ? j : 0][i] = 0.f;
+        }
+    if (warp == 0) {
+        if (lane == 0) {
+            int it = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, it++) {
+                const int s = it % LNB_STAGES;
+                if (!tc::mbar_wait(&empty[s], ((it / LNB_STAGES) & 1) ^ 1, abort_flag, nullptr)) break;
+                const int rows = min(LNB_ROWS, M - t * LNB_ROWS);
+                const uint32_t bytes = (uint32_t)rows * C * 2;
+                const size_t off = (size_t)t * LNB_ROWS * C;
+                uint8_t* st = smem + s * stage_bytes;
+                tc::mbar_expect_tx(&full[s], 3 * bytes);
+                tc::bulk_load_1d(st, dout + off, bytes, &full[s]);
+                tc::bulk_load_1d(st + sub_bytes, inp + off, bytes, &full[s]);
+                tc::bulk_load_1d(st + 2 * sub_bytes, dres + off, bytes, &full[s]);
+            }
+        }
+    } else {
+        float wv[NV][8];
+#pragma unroll
+        for (int j = 0; j < NV; j++) Vec8<float>::load(w + j * 256 + lane * 8, wv[j]);
+        int it = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, it++) {
+            const int s = it % LNB_STAGES;
+            const bool ok = tc::mbar_wait(&full[s], (it / LNB_STAGES) & 1, abort_flag, nullptr);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const int rows = min(LNB_ROWS, M - t * LNB_ROWS);
+            const uint8_t* st = smem + s * stage_bytes;
+            for (int r = warp - 1; r < rows; r += 8) {
+                const int row = t * LNB_ROWS + r;
+                const bf16* d = reinterpret_cast<const bf16*>(st) + (size_t)r * C;
+                const bf16* x = reinterpret_cast<const bf16*>(st + sub_bytes) + (size_t)r * C;
+                const bf16* dr_in = reinterpret_cast<const bf16*>(st + 2 * sub_bytes) + (size_t)r * C;
+                float dv[NV][8], xv[NV][8];
+#pragma unroll
+                for (int j = 0; j < NV; j++) {
+                    Vec8<bf16>::load(d + j * 256 + lane * 8, dv[j]);
+                    Vec8<bf16>::load(x + j * 256 + lane * 8, xv[j]);
+                }
+                const float m = mean[row], rs = rstd[row];
+                float gm = 0.f, gnm = 0.f;
+#pragma unroll
+                for (int j = 0; j < NV; j++)
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        const float n = (xv[j][i] - m) * rs;
+                        xv[j][i] = n;
+                        const float g = wv[j][i] * dv[j][i];
+                        gm += g;
+                        gnm += g * n;
+                        ab[j][i] += dv[j][i];
+                        aw[j][i] += n * dv[j][i];
+                        dv[j][i] = g;
+                    }
+                gm = warp_sum(gm) / C;
+                gnm = warp_sum(gnm) / C;
+                bf16* dr_out = dres + (size_t)row * C;
+#pragma unroll
+                for (int j = 0; j < NV; j++) {
+                    float o[8];
+                    Vec8<bf16>::load(dr_in + j * 256 + lane * 8, o);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) o[i] += (dv[j][i] - gm - xv[j][i] * gnm) * rs;
+                    Vec8<bf16>::store(dr_out + j * 256 + lane * 8, o);
+                    if (OUTSUM) {
+#pragma unroll
+                        for (int i = 0; i < 8; i++) ar[OUTSUM ? j : 0][i] += to_f(from_f<bf16>(o[i]));
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&empty[s]);
+        }
+    }
+    // every stage is consumed (or the loop gave up): reuse the ring for the block's sums
+    __syncthreads();
+    float* sh = reinterpret_cast<float*>(smem);  // [8 warps][NS][C]
+    if (warp >= 1) {
+#pragma unroll
+        for (int j = 0; j < NV; j++)
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int c = j * 256 + lane * 8 + i;
+                sh[((warp - 1) * NS + 0) * C + c] = aw[j][i];
+                sh[((warp - 1) * NS + 1) * C + c] = ab[j][i];
+                if (OUTSUM) sh[((warp - 1) * NS + 2) * C + c] = ar[OUTSUM ? j : 0][i];
+            }
+    }
+    __syncthreads();
+    for (int k = 0; k < NS; k++) {
+        float* pk = part + (size_t)(k * gridDim.x + blockIdx.x) * C;
+        for (int c = threadIdx.x; c < C; c += blockDim.x) {
+            float a = 0.f;
+#pragma unroll
+            for (int wi = 0; wi < 8; wi++) a += sh[(wi * NS + k) * C + c];
+            pk[c] = a;
+        }
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) ln_bwd_k(T* dres, float* part, const T* dout, const T* inp,
                                                 const float* w, const float* mean,
@@ -557,11 +827,46 @@ static cudaError_t colreduce(float* out0, float* out1, float* out2, const float*
     return cudaGetLastError();
 }
 
+template <int NV, bool OUTSUM>
+static cudaError_t ln_bwd_tma_launch(bf16* dres, float* part, const bf16* dout, const bf16* inp, const float* w,
+                                     const float* mean, const float* rstd, int M, int C, int grid, cudaStream_t s) {
+    const int smem = LNB_STAGES * 3 * LNB_ROWS * C * 2 + 256;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(ln_bwd_tma_k<NV, OUTSUM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             LNB_STAGES * 3 * LNB_ROWS * (NV * 256) * 2 + 256);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    G2_LAUNCH ln_bwd_tma_k<NV, OUTSUM><<<grid, LNT_THREADS, smem, s>>>(dres, part, dout, inp, w, mean, rstd, M, C);
+    return cudaGetLastError();
+}
+
 template <typename T>
 static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, float* dres_sum, const T* dout, const T* inp,
                                  const float* w, const float* mean, const float* rstd, int M, int C,
                                  float* part, float* cs_part, cudaStream_t s) {
     const bool aligned = ((uintptr_t)w & 15) == 0;
+    const bool al_all = ((((uintptr_t)dres | (uintptr_t)dout | (uintptr_t)inp | (uintptr_t)w)) & 15) == 0;
+    if (std::is_same<T, bf16>::value && al_all && M > 0 && C % 256 == 0 && C / 256 >= 1 && C / 256 <= 3) {
+        // grid: one CTA per SM, at most LNB_VEC_SUM_BLOCKS partial rows (the buffer's size)
+        const int ntiles = (M + LNB_ROWS - 1) / LNB_ROWS;
+        const int grid = std::min(std::min(ntiles, sm_count()), LNB_VEC_SUM_BLOCKS);
+        cudaError_t e;
+        bf16* dr = (bf16*)dres;
+        const bf16 *dd = (const bf16*)dout, *xx = (const bf16*)inp;
+#define G2_LNBT(NVV)                                                                                        \
+    case NVV:                                                                                               \
+        e = dres_sum ? ln_bwd_tma_launch<NVV, true>(dr, part, dd, xx, w, mean, rstd, M, C, grid, s)          \
+                     : ln_bwd_tma_launch<NVV, false>(dr, part, dd, xx, w, mean, rstd, M, C, grid, s);        \
+        break;
+        switch (C / 256) {
+            G2_LNBT(1) G2_LNBT(2) default: G2_LNBT(3)
+        }
+#undef G2_LNBT
+        if (e != cudaSuccess) return e;
+        return colreduce(dw, db, dres_sum, part, grid, C, s);
+    }
     const int nv = (C % 256 == 0 && aligned) ? C / 256 : 0;
     if (nv >= 1 && nv <= 4) {
 #define G2_LNB_CASE(NVV)                                                                                  \
