@@ -9,7 +9,8 @@
  * (sections 1.1-1.27, cited below as "llm.c §x.y"), with picoGPT's NumPy
  * statement ("60 行 NumPy 代码 ... 实现一个 GPT", functions gelu, softmax,
  * layer_norm, attention, mha, gpt2, lm_loss) as the second statement of the
- * forward and the loss.  Every function below restates what the listing
+ * forward and the loss.  The microGPT variant (page "microGPT 3D", lesson 04)
+ * swaps every LayerNorm for RMSNorm (or_rmsnorm_forward/backward, or_build_ex).  Every function below restates what the listing
  * computes, loop by loop, in the order the listing uses; nothing is blocked,
  * fused or reordered, except that loops over independent (b, h) pairs run under
  * OpenMP where the sum order of every output element is unchanged.
@@ -148,6 +149,50 @@ OR_EXPORT void or_layernorm_backward(real* dinp, real* dw, real* db, const real*
             val -= n * gn_mean;
             val *= s;
             dx[c] += val;
+        }
+    }
+}
+
+/* RMSNorm, the normalisation of the microGPT page's transformer block ("microGPT 3D",
+ * lesson 04: embedding -> RMSNorm -> attention -> residual -> MLP -> residual ->
+ * logits).  The page names the operation only; this is its standard definition
+ * (root-mean-square normalisation, no mean subtraction) with the same eps as the
+ * LayerNorm above and a per-channel gain w, no shift:
+ *   ms = sum_c x[c]^2 / C,  rstd = 1/sqrt(ms + 1e-5),  out = x*rstd*w.
+ * rstd is kept for the backward. */
+OR_EXPORT void or_rmsnorm_forward(real* out, real* rstd, const real* inp, const real* w, int B, int T,
+                                  int C) {
+    const real eps = (real)1e-5;
+    for (int bt = 0; bt < B * T; bt++) {
+        const real* x = inp + (size_t)bt * C;
+        real ms = 0;
+        for (int c = 0; c < C; c++) ms += x[c] * x[c];
+        ms = ms / C;
+        real s = (real)1 / R_SQRT(ms + eps);
+        real* o = out + (size_t)bt * C;
+        for (int c = 0; c < C; c++) o[c] = (s * x[c]) * w[c];
+        rstd[bt] = s;
+    }
+}
+
+/* Backward of or_rmsnorm_forward.  With n = x*rstd and g = w*dout (the chain rule
+ * through ms, which depends on every x[c]):
+ *   dw += n*dout,
+ *   dinp += (g - n*mean(g*n)) * rstd. */
+OR_EXPORT void or_rmsnorm_backward(real* dinp, real* dw, const real* dout, const real* inp, const real* w,
+                                   const real* rstd, int B, int T, int C) {
+    for (int bt = 0; bt < B * T; bt++) {
+        const real* d = dout + (size_t)bt * C;
+        const real* x = inp + (size_t)bt * C;
+        real* dx = dinp + (size_t)bt * C;
+        real s = rstd[bt];
+        real gn_mean = 0;
+        for (int c = 0; c < C; c++) gn_mean += (w[c] * d[c]) * (x[c] * s);
+        gn_mean = gn_mean / C;
+        for (int c = 0; c < C; c++) {
+            real n = x[c] * s;
+            dw[c] += n * d[c];
+            dx[c] += (w[c] * d[c] - n * gn_mean) * s;
         }
     }
 }
@@ -404,8 +449,13 @@ typedef struct {
         *lnf_rstd, *logits, *probs, *losses;
 } Acts;
 
+/* Normalisation of the model: GPT-2's LayerNorm (llm.c) or the microGPT variant's
+ * RMSNorm.  The RMSNorm model keeps the GPT-2 parameter layout; the LayerNorm
+ * shift tensors (ln1b, ln2b, lnfb) are carried but unused, so their gradients are 0. */
+enum { OR_LAYERNORM = 0, OR_RMSNORM = 1 };
+
 typedef struct {
-    int L, C, NH, V, maxT;
+    int L, C, NH, V, maxT, norm;
     size_t psize[NP], nparams;
     Params p, g;
     real *pmem, *gmem, *mmem, *vmem;
@@ -450,11 +500,12 @@ static real* carve_acts(Acts* a, const size_t* sizes) {
 
 /* llm.c §1.22 (sizes) without the checkpoint file: the caller uploads the
  * parameters with or_set_params. */
-OR_EXPORT OracleModel* or_build(int L, int C, int NH, int V, int maxT) {
+OR_EXPORT OracleModel* or_build_ex(int L, int C, int NH, int V, int maxT, int norm) {
     if (L <= 0 || C <= 0 || NH <= 0 || V <= 0 || maxT <= 0 || C % NH) return NULL;
+    if (norm != OR_LAYERNORM && norm != OR_RMSNORM) return NULL;
     OracleModel* m = (OracleModel*)calloc(1, sizeof(OracleModel));
     if (!m) return NULL;
-    m->L = L; m->C = C; m->NH = NH; m->V = V; m->maxT = maxT;
+    m->L = L; m->C = C; m->NH = NH; m->V = V; m->maxT = maxT; m->norm = norm;
     size_t Ls = L, Cs = C;
     size_t sz[NP] = {(size_t)V * Cs, (size_t)maxT * Cs, Ls * Cs, Ls * Cs, Ls * 3 * Cs * Cs,
                      Ls * 3 * Cs, Ls * Cs * Cs, Ls * Cs, Ls * Cs, Ls * Cs, Ls * 4 * Cs * Cs,
@@ -465,6 +516,10 @@ OR_EXPORT OracleModel* or_build(int L, int C, int NH, int V, int maxT) {
     if (!m->pmem) { free(m); return NULL; }
     m->mean_loss = -1;
     return m;
+}
+
+OR_EXPORT OracleModel* or_build(int L, int C, int NH, int V, int maxT) {
+    return or_build_ex(L, C, NH, V, maxT, OR_LAYERNORM);
 }
 
 OR_EXPORT size_t or_num_params(const OracleModel* m) { return m->nparams; }
@@ -507,6 +562,27 @@ OR_EXPORT int or_get_dencoded(const OracleModel* m, real* dst) {
     if (!m->gamem) return -1;
     memcpy(dst, m->ga.encoded, (size_t)m->B * m->T * m->C * sizeof(real));
     return 0;
+}
+
+/* The model's normalisation (LayerNorm, or RMSNorm for the microGPT variant, whose
+ * mean slot is set to 0 and whose shift is not read). */
+static void norm_forward(const OracleModel* m, real* out, real* mean, real* rstd, const real* inp,
+                         const real* w, const real* b, int B, int T, int C) {
+    if (m->norm == OR_RMSNORM) {
+        or_rmsnorm_forward(out, rstd, inp, w, B, T, C);
+        for (int i = 0; i < B * T; i++) mean[i] = 0;
+    } else {
+        or_layernorm_forward(out, mean, rstd, inp, w, b, B, T, C);
+    }
+}
+
+static void norm_backward(const OracleModel* m, real* dinp, real* dw, real* db, const real* dout,
+                          const real* inp, const real* w, const real* mean, const real* rstd, int B,
+                          int T, int C) {
+    if (m->norm == OR_RMSNORM)
+        or_rmsnorm_backward(dinp, dw, dout, inp, w, rstd, B, T, C);
+    else
+        or_layernorm_backward(dinp, dw, db, dout, inp, w, mean, rstd, B, T, C);
 }
 
 /* llm.c §1.23 gpt2_forward.  Returns 0, -1 on out-of-range ids, -2 if (B,T)
@@ -556,13 +632,13 @@ OR_EXPORT int or_forward(OracleModel* m, const int* inputs, const int* targets, 
         real* fchg = a.fch_gelu + l * 4 * BTC;
         real* fcproj = a.fcproj + l * BTC;
         real* res3 = a.residual3 + l * BTC;
-        or_layernorm_forward(ln1, a.ln1_mean + l * BT, a.ln1_rstd + l * BT, res, p.ln1w + l * C,
+        norm_forward(m, ln1, a.ln1_mean + l * BT, a.ln1_rstd + l * BT, res, p.ln1w + l * C,
                              p.ln1b + l * C, B, T, C);
         or_matmul_forward(qkv, ln1, p.qkvw + (size_t)l * 3 * C * C, p.qkvb + l * 3 * C, B, T, C, 3 * C);
         or_attention_forward(atty, a.preatt + l * BNTT, a.att + l * BNTT, qkv, B, T, C, NH);
         or_matmul_forward(attproj, atty, p.attprojw + (size_t)l * C * C, p.attprojb + l * C, B, T, C, C);
         or_residual_forward(res2, res, attproj, BTC);
-        or_layernorm_forward(ln2, a.ln2_mean + l * BT, a.ln2_rstd + l * BT, res2, p.ln2w + l * C,
+        norm_forward(m, ln2, a.ln2_mean + l * BT, a.ln2_rstd + l * BT, res2, p.ln2w + l * C,
                              p.ln2b + l * C, B, T, C);
         or_matmul_forward(fch, ln2, p.fcw + (size_t)l * 4 * C * C, p.fcb + l * 4 * C, B, T, C, 4 * C);
         or_gelu_forward(fchg, fch, 4 * BTC);
@@ -571,7 +647,7 @@ OR_EXPORT int or_forward(OracleModel* m, const int* inputs, const int* targets, 
         or_residual_forward(res3, res2, fcproj, BTC);
     }
     real* last = a.residual3 + (size_t)(L - 1) * BTC;
-    or_layernorm_forward(a.lnf, a.lnf_mean, a.lnf_rstd, last, p.lnfw, p.lnfb, B, T, C);
+    norm_forward(m, a.lnf, a.lnf_mean, a.lnf_rstd, last, p.lnfw, p.lnfb, B, T, C);
     or_matmul_forward(a.logits, a.lnf, p.wte, NULL, B, T, C, V);
     or_softmax_forward(a.probs, a.logits, B, T, V);
     if (targets) {
@@ -616,7 +692,7 @@ OR_EXPORT int or_backward(OracleModel* m) {
     or_matmul_backward(ga.lnf, g.wte, NULL, ga.logits, a.lnf, p.wte, B, T, C, V);
     real* res = a.residual3 + (size_t)(L - 1) * BTC;
     real* dres = ga.residual3 + (size_t)(L - 1) * BTC;
-    or_layernorm_backward(dres, g.lnfw, g.lnfb, ga.lnf, res, p.lnfw, a.lnf_mean, a.lnf_rstd, B, T, C);
+    norm_backward(m, dres, g.lnfw, g.lnfb, ga.lnf, res, p.lnfw, a.lnf_mean, a.lnf_rstd, B, T, C);
     for (int l = L - 1; l >= 0; l--) {
         res = l == 0 ? a.encoded : a.residual3 + (size_t)(l - 1) * BTC;
         dres = l == 0 ? ga.encoded : ga.residual3 + (size_t)(l - 1) * BTC;
@@ -628,7 +704,7 @@ OR_EXPORT int or_backward(OracleModel* m) {
         or_matmul_backward(ga.ln2 + l * BTC, g.fcw + (size_t)l * 4 * C * C, g.fcb + l * 4 * C,
                            ga.fch + l * 4 * BTC, a.ln2 + l * BTC, p.fcw + (size_t)l * 4 * C * C, B,
                            T, C, 4 * C);
-        or_layernorm_backward(ga.residual2 + l * BTC, g.ln2w + l * C, g.ln2b + l * C, ga.ln2 + l * BTC,
+        norm_backward(m, ga.residual2 + l * BTC, g.ln2w + l * C, g.ln2b + l * C, ga.ln2 + l * BTC,
                               a.residual2 + l * BTC, p.ln2w + l * C, a.ln2_mean + l * BT,
                               a.ln2_rstd + l * BT, B, T, C);
         or_residual_backward(dres, ga.attproj + l * BTC, ga.residual2 + l * BTC, BTC);
@@ -640,7 +716,7 @@ OR_EXPORT int or_backward(OracleModel* m) {
         or_matmul_backward(ga.ln1 + l * BTC, g.qkvw + (size_t)l * 3 * C * C, g.qkvb + l * 3 * C,
                            ga.qkv + l * 3 * BTC, a.ln1 + l * BTC, p.qkvw + (size_t)l * 3 * C * C,
                            B, T, C, 3 * C);
-        or_layernorm_backward(dres, g.ln1w + l * C, g.ln1b + l * C, ga.ln1 + l * BTC, res,
+        norm_backward(m, dres, g.ln1w + l * C, g.ln1b + l * C, ga.ln1 + l * BTC, res,
                               p.ln1w + l * C, a.ln1_mean + l * BT, a.ln1_rstd + l * BT, B, T, C);
     }
     or_encoder_backward(g.wte, g.wpe, ga.encoded, m->inputs, B, T, C);

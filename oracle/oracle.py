@@ -27,6 +27,8 @@ def _lib(variant: str):
             "or_encoder_backward": (None, [P, P, P, P, i, i, i]),
             "or_layernorm_forward": (None, [P, P, P, P, P, P, i, i, i]),
             "or_layernorm_backward": (None, [P, P, P, P, P, P, P, P, i, i, i]),
+            "or_rmsnorm_forward": (None, [P, P, P, P, i, i, i]),
+            "or_rmsnorm_backward": (None, [P, P, P, P, P, P, i, i, i]),
             "or_matmul_forward": (None, [P, P, P, P, i, i, i, i]),
             "or_matmul_backward": (None, [P, P, P, P, P, P, i, i, i, i]),
             "or_attention_forward": (None, [P, P, P, P, i, i, i, i]),
@@ -40,6 +42,7 @@ def _lib(variant: str):
             "or_crossentropy_softmax_backward": (None, [P, P, P, P, i, i, i]),
             "or_adamw": (i, [P, P, P, P, z, R, R, R, R, R, i]),
             "or_build": (P, [i, i, i, i, i]),
+            "or_build_ex": (P, [i, i, i, i, i, i]),
             "or_num_params": (z, [P]),
             "or_num_acts": (z, [P]),
             "or_param_sizes": (None, [P, P]),
@@ -123,6 +126,25 @@ class Ops:
         self.lib.or_layernorm_backward(_p(dx), _p(dw), _p(db), _p(dout), _p(x), _p(w),
                                        _p(self._c(mean)), _p(self._c(rstd)), 1, rows, C)
         return dx, dw, db
+
+    def rmsnorm(self, x, w):
+        """microGPT's RMSNorm: out = x / sqrt(mean(x^2) + 1e-5) * w; returns (out, rstd)."""
+        x, w = self._c(x), self._c(w)
+        C = x.shape[-1]
+        rows = x.size // C
+        out = np.empty_like(x)
+        rstd = np.empty(rows, self.dt)
+        self.lib.or_rmsnorm_forward(_p(out), _p(rstd), _p(x), _p(w), 1, rows, C)
+        return out, rstd
+
+    def rmsnorm_backward(self, dout, x, w, rstd):
+        dout, x, w = self._c(dout), self._c(x), self._c(w)
+        C = x.shape[-1]
+        rows = x.size // C
+        dx = np.zeros_like(x)
+        dw = np.zeros(C, self.dt)
+        self.lib.or_rmsnorm_backward(_p(dx), _p(dw), _p(dout), _p(x), _p(w), _p(self._c(rstd)), 1, rows, C)
+        return dx, dw
 
     def matmul(self, x, W, bias=None):
         x, W = self._c(x), self._c(W)
@@ -209,13 +231,19 @@ class Ops:
 
 
 class Model:
-    """The oracle's whole-model step (llm.c sections 1.22-1.27)."""
+    """The oracle's whole-model step (llm.c sections 1.22-1.27).
 
-    def __init__(self, L, C, NH, V, maxT, variant: str = "f64"):
+    norm: "layernorm" (GPT-2) or "rmsnorm" (the microGPT variant: every LayerNorm
+    replaced by RMSNorm with gain, the shift tensors carried unused)."""
+
+    NORMS = {"layernorm": 0, "rmsnorm": 1}
+
+    def __init__(self, L, C, NH, V, maxT, variant: str = "f64", norm: str = "layernorm"):
         self.lib = _lib(variant)
         self.dt = dtype_of(variant)
         self.L, self.C, self.NH, self.V, self.maxT = L, C, NH, V, maxT
-        self.h = self.lib.or_build(L, C, NH, V, maxT)
+        self.norm = norm
+        self.h = self.lib.or_build_ex(L, C, NH, V, maxT, self.NORMS[norm])
         if not self.h:
             raise ValueError("or_build failed")
         self.n = self.lib.or_num_params(self.h)

@@ -8,7 +8,8 @@ Neither helper shares code with the oracle or with the CUDA library:
   i.e. the transposes of the llm.c (out, in) layout.
 * ``torch_loss_and_grads`` states the same model with PyTorch library routines
   (layer_norm, the tanh GELU, masked softmax, cross_entropy) in float64 and
-  lets autograd produce the gradients.
+  lets autograd produce the gradients; with norm="rmsnorm" it states the microGPT
+  variant with torch's rms_norm.
 """
 from __future__ import annotations
 
@@ -86,9 +87,16 @@ def picogpt_logits(flat, tokens, L, C, NH, V, maxT):
 
 # ---- PyTorch library routines + autograd, float64 ---------------------------
 
-def torch_loss_and_grads(flat, tokens, targets, L, C, NH, V, maxT):
+def torch_loss_and_grads(flat, tokens, targets, L, C, NH, V, maxT, norm="layernorm"):
+    """norm="rmsnorm" states the microGPT variant: torch's rms_norm (eps 1e-5, gain =
+    the ln*w tensors) in place of every layer_norm; the ln*b tensors are not used."""
     import torch
     import torch.nn.functional as F
+
+    def normalise(x, w, b):
+        if norm == "rmsnorm":
+            return F.rms_norm(x, (C,), w, eps=1e-5)
+        return F.layer_norm(x, (C,), w, b, eps=1e-5)
 
     p = torch.tensor(np.asarray(flat, np.float64), requires_grad=True)
     P = unflatten(p, L, C, V, maxT)
@@ -99,7 +107,7 @@ def torch_loss_and_grads(flat, tokens, targets, L, C, NH, V, maxT):
     x = P["wte"][tok] + P["wpe"][:T].unsqueeze(0)
     causal = torch.ones(T, T, dtype=torch.bool).tril()
     for l in range(L):
-        h = F.layer_norm(x, (C,), P["ln1w"][l], P["ln1b"][l], eps=1e-5)
+        h = normalise(x, P["ln1w"][l], P["ln1b"][l])
         qkv = F.linear(h, P["qkvw"][l], P["qkvb"][l])
         q, k, v = qkv.split(C, dim=-1)
         q = q.view(B, T, NH, hs).transpose(1, 2)
@@ -109,10 +117,10 @@ def torch_loss_and_grads(flat, tokens, targets, L, C, NH, V, maxT):
         s = s.masked_fill(~causal, float("-inf"))
         y = (torch.softmax(s, dim=-1) @ v).transpose(1, 2).reshape(B, T, C)
         x = x + F.linear(y, P["attprojw"][l], P["attprojb"][l])
-        h = F.layer_norm(x, (C,), P["ln2w"][l], P["ln2b"][l], eps=1e-5)
+        h = normalise(x, P["ln2w"][l], P["ln2b"][l])
         a = F.gelu(F.linear(h, P["fcw"][l], P["fcb"][l]), approximate="tanh")
         x = x + F.linear(a, P["fcprojw"][l], P["fcprojb"][l])
-    x = F.layer_norm(x, (C,), P["lnfw"], P["lnfb"], eps=1e-5)
+    x = normalise(x, P["lnfw"], P["lnfb"])
     logits = x @ P["wte"].T
     loss = F.cross_entropy(logits.reshape(B * T, V), tgt.reshape(B * T))
     loss.backward()

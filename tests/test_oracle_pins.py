@@ -415,3 +415,94 @@ def test_oracle_error_codes():
         m.backward()                                       # no targets in the last forward
     with pytest.raises(ValueError):
         m.forward(np.zeros((3, 4), np.int32))              # B differs from the first call
+
+
+# ---------------------------------------------------------------- microGPT variant: RMSNorm
+# The page "microGPT 3D" (lesson 04) puts RMSNorm where GPT-2 has LayerNorm.  Read as
+# root-mean-square normalisation with eps 1e-5 and a per-channel gain, no shift.
+
+def test_rmsnorm_zero_mean_rows_equal_layernorm():
+    """On rows with mean exactly 0 the two normalisations coincide (LayerNorm is pinned
+    to the picoGPT worked values above)."""
+    rng = np.random.default_rng(71)
+    half = rng.normal(size=(16, 24)) * 2.0
+    x = np.concatenate([half, -half], axis=1)          # every row sums to exactly 0
+    w = rng.normal(size=48)
+    ln, _, ln_rstd = ops.layernorm(x, w, np.zeros(48))
+    rms, rstd = ops.rmsnorm(x, w)
+    assert np.allclose(rms, ln, rtol=1e-13, atol=1e-14)
+    assert np.allclose(rstd, ln_rstd, rtol=1e-13)
+
+
+def test_rmsnorm_moments_and_worked_value():
+    rng = np.random.default_rng(72)
+    z = rng.normal(size=(32, 97)) * 3 + 1              # non-zero mean: differs from LayerNorm
+    o, r = ops.rmsnorm(z, np.ones(97))
+    ms = (z * z).mean(-1)
+    # unit gain: every output row has mean square ms / (ms + eps), and o / z is one
+    # positive constant per row (no shift, no mean subtraction)
+    assert np.allclose((o * o).mean(-1), ms / (ms + 1e-5), rtol=1e-12)
+    ratio = o / z
+    assert np.allclose(ratio, ratio[:, :1], rtol=1e-12) and np.all(ratio > 0)
+    ln, _, _ = ops.layernorm(z, np.ones(97), np.zeros(97))
+    assert np.max(np.abs(o - ln)) > 0.1
+    # by hand: x = (3, 4): mean square 12.5, out = x / sqrt(12.5 + 1e-5)
+    o2, _ = ops.rmsnorm(np.array([[3.0, 4.0]]), np.array([1.0, 2.0]))
+    assert np.allclose(o2, [[0.848528137423857 * (12.5 / 12.50001) ** 0.5,
+                             2 * 1.131370849898476 * (12.5 / 12.50001) ** 0.5]], rtol=1e-14)
+
+
+def test_rmsnorm_backward_finite_difference():
+    rng = np.random.default_rng(73)
+    x = rng.normal(size=(3, 10)) + 0.5
+    w = rng.normal(size=10)
+    dy = rng.normal(size=(3, 10))
+    out, rstd = ops.rmsnorm(x, w)
+    dx, dw = ops.rmsnorm_backward(dy, x, w, rstd)
+    f = lambda: float((ops.rmsnorm(x, w)[0] * dy).sum())
+    assert np.allclose(dx, _fd(f, x), atol=1e-8)
+    assert np.allclose(dw, _fd(f, w), atol=1e-8)
+
+
+def test_rmsnorm_model_matches_torch_autograd():
+    """The whole microGPT-variant step against torch's rms_norm + autograd (float64)."""
+    L, C, NH, V, maxT = _cfg("tiny")
+    params = synth.init_params(L, C, V, maxT, seed=74)
+    rng = np.random.default_rng(75)
+    params = params + rng.normal(scale=0.02, size=params.size).astype(np.float32)
+    stream = synth.zipf_stream(V, 4 * 32 + 1, seed=76)
+    inp, tgt = synth.batch(stream, 0, 4, 32)
+    m = Model(L, C, NH, V, maxT, norm="rmsnorm")
+    m.set_params(params)
+    loss = m.forward(inp, tgt)
+    m.backward()
+    tl, tg, tlog = torch_loss_and_grads(params, inp, tgt, L, C, NH, V, maxT, norm="rmsnorm")
+    assert abs(loss - tl) <= 1e-12 * abs(tl)
+    assert np.allclose(m.logits(), tlog, rtol=1e-10, atol=1e-12)
+    g = m.grads()
+    sizes = synth.param_sizes(L, C, V, maxT)
+    for name, a, b in zip(synth.PARAM_NAMES, np.split(g, np.cumsum(sizes)[:-1]), np.split(tg, np.cumsum(sizes)[:-1])):
+        if name in ("ln1b", "ln2b", "lnfb"):
+            assert not a.any() and not b.any(), name    # the shifts are carried, unused
+            continue
+        err = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
+        assert err < 1e-10, (name, err)
+    # and it is a different model from the LayerNorm one on the same weights
+    ml = Model(L, C, NH, V, maxT)
+    ml.set_params(params)
+    assert abs(ml.forward(inp, tgt) - loss) > 1e-6
+
+
+def test_rmsnorm_model_finite_difference_char_all_params():
+    L, C, NH, V, maxT = _cfg("char")
+    params = synth.init_params(L, C, V, maxT, seed=77).astype(np.float64)
+    params += np.random.default_rng(78).normal(scale=0.05, size=params.size)
+    stream = synth.uniform_stream(V, 4 * 16 + 1, seed=79)
+    inp, tgt = synth.batch(stream, 0, 4, 16)
+    m = Model(L, C, NH, V, maxT, norm="rmsnorm")
+    f = _loss_fn(m, params, inp, tgt)
+    f()
+    m.backward()
+    g = m.grads()
+    fd = _fd(f, params, h=1e-6)
+    assert np.all(np.abs(fd - g) <= 1e-6 * np.abs(g) + 2e-9), np.max(np.abs(fd - g))
