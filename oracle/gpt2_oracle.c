@@ -735,6 +735,84 @@ OR_EXPORT int or_update(OracleModel* m, real lr, real b1, real b2, real eps, rea
     return or_adamw(m->pmem, m->gmem, m->mmem, m->vmem, m->nparams, lr, b1, b2, eps, wd, t);
 }
 
+/* ------------------------------------------------------------------------- */
+/* generation (picoGPT "generate"; llm.c §1.35 sample_mult)                    */
+/* ------------------------------------------------------------------------- */
+
+/* Drop the activation buffers (and their gradients) so the next or_forward may use
+ * a different (B,T).  Parameters, gradients and AdamW moments are kept. */
+OR_EXPORT void or_release_acts(OracleModel* m) {
+    free(m->amem); free(m->gamem); free(m->inputs); free(m->targets);
+    m->amem = m->gamem = NULL;
+    m->inputs = m->targets = NULL;
+    m->nacts = 0;
+    m->have_targets = 0;
+    m->mean_loss = -1;
+}
+
+/* llm.c §1.35 sample_mult: walk the cumulative distribution of the n probabilities and
+ * return the first index whose cumulative value exceeds coin (in [0,1)); the last index
+ * if rounding leaves coin above every cumulative value. */
+OR_EXPORT int or_sample_mult(const real* probs, int n, real coin) {
+    real cdf = 0;
+    for (int i = 0; i < n; i++) {
+        cdf += probs[i];
+        if (coin < cdf) return i;
+    }
+    return n - 1;
+}
+
+/* picoGPT "generate", the autoregressive decode loop: n_new times, run the whole
+ * forward over the sequence so far and pick the next id from the logits of its last
+ * position, then append it.  temperature <= 0: greedy, argmax of the logits (the first
+ * index among equal maxima, as numpy's argmax); temperature > 0: sample_mult over
+ * softmax(logits / temperature) with coins[b * n_new + step] (drawn by the caller).
+ * prompt (B,T0) int32; out (B,n_new) receives the new ids.  No cache: every step
+ * recomputes every position.  Returns 0, or or_forward's code (T0 + n_new - 1 > maxT
+ * gives -2, an id outside [0,V) -1), -3 on allocation failure. */
+OR_EXPORT int or_generate(OracleModel* m, const int* prompt, int B, int T0, int n_new, real temperature,
+                          const real* coins, int* out) {
+    if (B <= 0 || T0 <= 0 || n_new < 0) return -2;
+    const int V = m->V, Tmax = T0 + n_new;
+    int* seq = (int*)malloc((size_t)B * Tmax * sizeof(int));
+    int* cur = (int*)malloc((size_t)B * Tmax * sizeof(int));
+    real* probs = (real*)malloc((size_t)V * sizeof(real));
+    if (!seq || !cur || !probs) { free(seq); free(cur); free(probs); return -3; }
+    for (int b = 0; b < B; b++)
+        for (int t = 0; t < T0; t++) seq[b * Tmax + t] = prompt[b * T0 + t];
+    int rc = 0;
+    for (int step = 0; step < n_new && rc == 0; step++) {
+        const int T = T0 + step;
+        for (int b = 0; b < B; b++)
+            for (int t = 0; t < T; t++) cur[b * T + t] = seq[b * Tmax + t];
+        or_release_acts(m);
+        rc = or_forward(m, cur, NULL, B, T, NULL);
+        if (rc) break;
+        for (int b = 0; b < B; b++) {
+            const real* l = m->a.logits + ((size_t)b * T + (T - 1)) * V;
+            int next = 0;
+            if (temperature <= 0) {
+                for (int i = 1; i < V; i++)
+                    if (l[i] > l[next]) next = i;
+            } else {
+                real mx = -INFINITY;
+                for (int i = 0; i < V; i++) if (l[i] / temperature > mx) mx = l[i] / temperature;
+                real sum = 0;
+                for (int i = 0; i < V; i++) {
+                    probs[i] = R_EXP(l[i] / temperature - mx);
+                    sum += probs[i];
+                }
+                for (int i = 0; i < V; i++) probs[i] /= sum;
+                next = or_sample_mult(probs, V, coins[(size_t)b * n_new + step]);
+            }
+            seq[b * Tmax + T] = next;
+            out[(size_t)b * n_new + step] = next;
+        }
+    }
+    free(seq); free(cur); free(probs);
+    return rc;
+}
+
 /* llm.c §1.27 gpt2_free. */
 OR_EXPORT void or_free(OracleModel* m) {
     if (!m) return;

@@ -59,6 +59,9 @@ def _lib(variant: str):
             "or_update": (i, [P, R, R, R, R, R, i]),
             "or_free": (None, [P]),
             "or_real_bytes": (i, []),
+            "or_release_acts": (None, [P]),
+            "or_sample_mult": (i, [P, i, R]),
+            "or_generate": (i, [P, P, i, i, i, R, P, P]),
         }
         for name, (res, args) in sigs.items():
             f = getattr(lib, name)
@@ -221,6 +224,11 @@ class Ops:
         self.lib.or_crossentropy_softmax_backward(_p(dlogits), _p(dl), _p(probs), _p(targets), 1, rows, V)
         return losses.mean(), losses, dlogits
 
+    def sample_mult(self, probs, coin):
+        """llm.c section 1.35: first index whose cumulative probability exceeds coin."""
+        probs = self._c(probs)
+        return int(self.lib.or_sample_mult(_p(probs), probs.size, float(coin)))
+
     def adamw(self, p, g, m, v, lr, b1, b2, eps, wd, t):
         """Returns updated (p, m, v); inputs are not modified."""
         p, g, m, v = (self._c(a).copy() for a in (p, g, m, v))
@@ -320,6 +328,26 @@ class Model:
         rc = self.lib.or_update(self.h, lr, b1, b2, eps, wd, t)
         if rc != 0:
             raise RuntimeError(f"or_update failed with code {rc}")
+
+    def release_acts(self):
+        """Forget the activation shape so the next forward may use another (B, T)."""
+        self.lib.or_release_acts(self.h)
+        self.B = self.T = None
+
+    def generate(self, prompt, n_new, temperature=0.0, coins=None):
+        """picoGPT's generate: (B, n_new) new ids; greedy when temperature <= 0, else
+        sample_mult over softmax(logits / temperature) with coins (B, n_new) in [0, 1)."""
+        prompt = np.ascontiguousarray(prompt, np.int32)
+        B, T0 = prompt.shape
+        out = np.zeros((B, n_new), np.int32)
+        c = None if coins is None else np.ascontiguousarray(coins, self.dt).reshape(B, n_new)
+        if temperature > 0 and c is None:
+            raise ValueError("sampling needs coins")
+        rc = self.lib.or_generate(self.h, _p(prompt), B, T0, n_new, float(temperature), _p(c), _p(out))
+        if rc != 0:
+            raise ValueError(f"or_generate failed with code {rc}")
+        self.B = self.T = None
+        return out
 
 
 def cpu_threads() -> int:

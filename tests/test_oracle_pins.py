@@ -506,3 +506,77 @@ def test_rmsnorm_model_finite_difference_char_all_params():
     g = m.grads()
     fd = _fd(f, params, h=1e-6)
     assert np.all(np.abs(fd - g) <= 1e-6 * np.abs(g) + 2e-9), np.max(np.abs(fd - g))
+
+
+# ---------------------------------------------------------------- generation
+# picoGPT's "generate" (greedy decode loop; sampling with np.random.choice over the
+# last position's distribution, temperature as the article's knob) and llm.c §1.35
+# sample_mult.
+
+def test_sample_mult_matches_searchsorted_and_edges():
+    rng = np.random.default_rng(81)
+    p = rng.random(37)
+    p /= p.sum()
+    cdf = np.cumsum(p)
+    for coin in rng.random(500):
+        assert ops.sample_mult(p, coin) == int(np.searchsorted(cdf, coin, side="right"))
+    assert ops.sample_mult(np.array([0.0, 0.0, 1.0]), 0.0) == 2     # zero-mass ids are never drawn
+    assert ops.sample_mult(np.array([0.25, 0.25, 0.25, 0.25]), 0.5) == 2
+    assert ops.sample_mult(np.array([0.3, 0.3, 0.3]), 0.95) == 2    # rounding slack: last id
+    # frequencies over a fine grid of coins reproduce the distribution exactly
+    coins = (np.arange(100000) + 0.5) / 100000
+    counts = np.bincount([ops.sample_mult(p, c) for c in coins[::10]], minlength=37)
+    assert np.allclose(counts / counts.sum(), p, atol=2e-4)
+
+
+def _pico_generate(params, prompt, n_new, cfg, temperature=0.0, coins=None):
+    L, C, NH, V, maxT = cfg
+    seq = np.array(prompt)
+    out = []
+    for s in range(n_new):
+        logits = picogpt_logits(params, seq, L, C, NH, V, maxT)[:, -1]
+        if temperature <= 0:
+            nxt = np.argmax(logits, axis=-1)
+        else:
+            z = logits / temperature
+            e = np.exp(z - z.max(-1, keepdims=True))
+            p = e / e.sum(-1, keepdims=True)
+            nxt = np.array([int(np.searchsorted(np.cumsum(p[b]), coins[b, s], side="right"))
+                            for b in range(seq.shape[0])])
+        out.append(nxt)
+        seq = np.concatenate([seq, nxt[:, None]], axis=1)
+    return np.stack(out, axis=1)
+
+
+def test_generate_greedy_matches_picogpt_loop():
+    cfg = _cfg("tiny")
+    L, C, NH, V, maxT = cfg
+    params = synth.init_params(L, C, V, maxT, seed=82).astype(np.float64)
+    params += np.random.default_rng(83).normal(scale=0.05, size=params.size)   # non-flat logits
+    prompt = synth.zipf_stream(V, 3 * 5, seed=84).reshape(3, 5)
+    m = Model(*cfg)
+    m.set_params(params)
+    got = m.generate(prompt, 6)
+    want = _pico_generate(params, prompt, 6, cfg)
+    assert np.array_equal(got, want)
+    # each row's continuation depends on that row only
+    got1 = m.generate(prompt[1:2], 6)
+    assert np.array_equal(got1[0], got[1])
+
+
+def test_generate_sampling_matches_picogpt_loop_and_low_temperature_is_greedy():
+    cfg = _cfg("tiny")
+    L, C, NH, V, maxT = cfg
+    params = synth.init_params(L, C, V, maxT, seed=85).astype(np.float64)
+    params += np.random.default_rng(86).normal(scale=0.05, size=params.size)
+    prompt = synth.zipf_stream(V, 2 * 4, seed=87).reshape(2, 4)
+    coins = np.random.default_rng(88).random((2, 5))
+    m = Model(*cfg)
+    m.set_params(params)
+    for tau in (1.0, 0.7):
+        got = m.generate(prompt, 5, temperature=tau, coins=coins)
+        want = _pico_generate(params, prompt, 5, cfg, temperature=tau, coins=coins)
+        assert np.array_equal(got, want), tau
+    # as the temperature goes to 0 the distribution collapses onto the argmax
+    cold = m.generate(prompt, 5, temperature=1e-4, coins=coins)
+    assert np.array_equal(cold, m.generate(prompt, 5))
