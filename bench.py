@@ -2,7 +2,7 @@
 """Throughput of one GPT-2 training step (forward + backward + AdamW) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload gpt2_124m|gpt2_350m|...]
+                    [--workload gpt2_124m|gpt2_350m|...] [--norm layernorm|rmsnorm]
 
 Prints ONE JSON line on rank 0.  The workload is GPT-2 124M (L=12, C=768, H=12,
 V=50257 padded to 50304 on the device) at B=32, T=1024 in bf16 mixed precision, on a
@@ -14,6 +14,9 @@ through the public host-pointer call gpt2_forward (ids copied from pinned host m
 the loss read back every step).  With N > 1, each rank trains its own independent
 replica on its own slice of the token stream (the step has no cross-rank exchange in
 this build), so scaling is weak.
+
+--norm rmsnorm runs the microGPT variant of the same shapes (every LayerNorm replaced
+by RMSNorm, page "microGPT 3D", lesson 04).
 
 --impl reference times the CPU oracle (test infrastructure, plain C, all host cores)
 on bounded samples of the same workload, rank 0 only.
@@ -159,7 +162,7 @@ def recorded_traffic(kernel_class: str):
 
 
 # ------------------------------------------------------------------ oracle (CPU) timing
-def oracle_sample(cfg, T_sample, stream_seed=1337):
+def oracle_sample(cfg, T_sample, stream_seed=1337, norm="layernorm"):
     """Time the CPU oracle on one bounded sample: fwd+bwd+AdamW of the workload's model on
     B=1, T=T_sample (the first T_sample positions of row 0 of step 0)."""
     from gpt_train_step_arena_b300 import synth
@@ -169,7 +172,7 @@ def oracle_sample(cfg, T_sample, stream_seed=1337):
     stream = synth.token_stream(cfg, steps=1, seed=stream_seed)
     inp = stream[:T_sample].reshape(1, T_sample)
     tgt = stream[1:T_sample + 1].reshape(1, T_sample)
-    m = Model(L, C, NH, V, maxT)
+    m = Model(L, C, NH, V, maxT, norm=norm)
     m.set_params(params)
     return m, inp, tgt, cpu_threads()
 
@@ -181,7 +184,7 @@ def run_reference(args, rank, world):
     from gpt_train_step_arena_b300 import synth
     cfg = dict(synth.WORKLOADS[args.workload])
     T_s = args.ref_tokens
-    m, inp, tgt, cores = oracle_sample(cfg, T_s)
+    m, inp, tgt, cores = oracle_sample(cfg, T_s, norm=args.norm)
     hp = (cfg["lr"], cfg["b1"], cfg["b2"], cfg["eps"], cfg["wd"])
     for i in range(args.warmup):
         m.forward(inp, tgt)
@@ -200,7 +203,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": DATA, "config": config_block(cfg, args.workload),
+        "data": DATA, "config": config_block(cfg, args.workload, args.norm),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -208,9 +211,11 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def config_block(cfg, workload):
+def config_block(cfg, workload, norm="layernorm"):
     Vp = (cfg["V"] + 127) // 128 * 128
-    return {"workload": workload, "L": cfg["L"], "C": cfg["C"], "H": cfg["NH"], "V": cfg["V"], "Vp": Vp,
+    if norm != "layernorm":
+        workload = f"{workload}_{norm}"   # the microGPT variant of the same shapes
+    return {"workload": workload, "norm": norm, "L": cfg["L"], "C": cfg["C"], "H": cfg["NH"], "V": cfg["V"], "Vp": Vp,
             "B": cfg["B"], "T": cfg["T"], "precision": "bf16 mixed (fp32 master/AdamW)",
             "lr": cfg["lr"], "wd": cfg["wd"],
             "l2": "no flush: every step streams > 10 GB of activations and weights, far above the 126 MB L2"}
@@ -232,7 +237,7 @@ def run_ours(args, rank, world, local):
     stream = synth.token_stream(cfg, steps=W + 2 * K, seed=1337 + rank)
     batches = [synth.batch(stream, s, B, T) for s in range(W + 2 * K)]
 
-    g = GPT2(L, C, NH, V, maxT, precision="bf16")
+    g = GPT2(L, C, NH, V, maxT, precision="bf16", norm=args.norm)
     g.set_params(params)
     s = torch.cuda.Stream()
     g.set_stream(s.cuda_stream)
@@ -309,7 +314,7 @@ def run_ours(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        m, inp, tgt, cores = oracle_sample(cfg, args.cpu_tokens)
+        m, inp, tgt, cores = oracle_sample(cfg, args.cpu_tokens, norm=args.norm)
         t1 = time.perf_counter()
         m.forward(inp, tgt)
         m.backward()
@@ -354,7 +359,7 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": DATA, "config": config_block(cfg, args.workload),
+        "dtype": "bf16", "data": DATA, "config": config_block(cfg, args.workload, args.norm),
         "mfu": {"algorithmic_flops_per_token": fpt,
                 "vs_nominal_2250": value / world * fpt / (NOMINAL_BF16_TFLOPS * 1e12),
                 "vs_measured_burst": value / world * fpt / (pk["bf16"] * 1e12)},
@@ -370,6 +375,91 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ generation
+GEN_METRIC = "generated tokens/sec (greedy decode with a key/value cache) for GPT-2 124M"
+
+
+def gen_bytes_per_step(cfg, Vp, B, t):
+    """Algorithmic HBM bytes of one one-token decode step at cache length t (positions
+    0..t): every bf16 weight once (the 12*L*C^2 block matrices and the Vp*C tied head),
+    plus the cached keys and values of B sequences read once, plus the new row's
+    key/value written."""
+    L, C = cfg["L"], cfg["C"]
+    weights = 2 * (12 * L * C * C + Vp * C)
+    kv = 2 * L * B * (t + 1) * 2 * C
+    return weights + kv
+
+
+def run_generate(args, rank, world, local):
+    import numpy as np
+    import torch
+    from gpt_train_step_arena_b300 import synth
+    from gpt_train_step_arena_b300.model import GPT2
+
+    torch.cuda.set_device(local)
+    cfg = dict(synth.WORKLOADS[args.workload])
+    L, C, NH, V, maxT = (cfg[k] for k in ("L", "C", "NH", "V", "maxT"))
+    B, T0, n_new = args.gen_batch, args.gen_prompt, args.gen_tokens
+    params = synth.init_params(L, C, V, maxT, seed=42)
+    stream = synth.token_stream(cfg, steps=1, seed=1337 + rank)
+    prompt = stream[:B * T0].reshape(B, T0).astype(np.int32)
+    g = GPT2(L, C, NH, V, maxT, precision="bf16", norm=args.norm)
+    g.set_params(params)
+    s = torch.cuda.Stream()
+    g.set_stream(s.cuda_stream)
+    for _ in range(args.warmup):
+        g.generate(prompt, n_new)
+    # the prompt pass alone, to separate it from the decode steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev[0].record(s)
+    for _ in range(args.steps):
+        g.generate(prompt, 1)
+    ev[1].record(s)
+    clocks = ClockSampler(local)
+    clocks.start()
+    launches0 = g.kernel_launches()
+    barrier(world)
+    t_host = time.perf_counter()
+    ev[2].record(s)
+    for _ in range(args.steps):
+        out = g.generate(prompt, n_new)
+    ev[3].record(s)
+    torch.cuda.synchronize()
+    t_host = time.perf_counter() - t_host
+    clk = clocks.stop()
+    launches = g.kernel_launches() - launches0
+    prefill_ms = ev[0].elapsed_time(ev[1]) / args.steps
+    total_ms = max_over_ranks(ev[2].elapsed_time(ev[3]) / args.steps, world)
+    decode_ms = (total_ms - prefill_ms) / max(1, n_new - 1)
+    if rank != 0:
+        return
+    pk = _peaks()
+    Vp = g.Vp
+    t_mid = T0 + (n_new - 1) // 2
+    bytes_step = gen_bytes_per_step(cfg, Vp, B, t_mid)
+    achieved = bytes_step / (decode_ms / 1e3) / 1e9
+    value = world * B * n_new / (total_ms / 1e3)
+    line = {
+        "mode": "generate", "metric": GEN_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": DATA,
+        "config": {"workload": f"{args.workload}_generate" + ("" if args.norm == "layernorm" else f"_{args.norm}"),
+                   "B": B, "prompt": T0, "new_tokens": n_new, "sampling": "greedy",
+                   "step": "one gpt2_generate call: prompt pass + (new_tokens - 1) one-token decode steps",
+                   "l2": "no flush: every decode step streams the 0.25 GB of bf16 weights, twice the L2"},
+        "prefill_ms": prefill_ms, "decode_ms_per_token": decode_ms,
+        "roofline": {"bound": "hbm", "kernel": "decode step (all kernels)", "achieved": achieved,
+                     "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"], "traffic": None,
+                     "peak_source": f"{pk['source']} (HBM copy)", "bytes_per_decode_step": bytes_step},
+        "e2e": {"value": world * B * n_new / (t_host / args.steps), "unit": "tokens/s",
+                "h2d_bytes_per_step": B * T0 * 4, "d2h_bytes_per_step": B * n_new * 4},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "sample_ids": out[0, :8].tolist(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -377,6 +467,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gpt2_124m")
+    ap.add_argument("--mode", choices=["train", "generate"], default="train",
+                    help="generate: greedy decode throughput with the key/value cache")
+    ap.add_argument("--gen-batch", type=int, default=16)
+    ap.add_argument("--gen-prompt", type=int, default=64)
+    ap.add_argument("--gen-tokens", type=int, default=40)
+    ap.add_argument("--norm", choices=["layernorm", "rmsnorm"], default="layernorm",
+                    help="rmsnorm: the microGPT variant (every LayerNorm replaced by RMSNorm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=128)
     ap.add_argument("--ref-tokens", type=int, default=32)
@@ -386,6 +483,8 @@ def main():
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.mode == "generate":
+        run_generate(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

@@ -23,6 +23,7 @@ P, I, U64, SZ, F = ct.c_void_p, ct.c_int, ct.c_uint64, ct.c_size_t, ct.c_float
 # name: (restype, argtypes) — mirrors include/gpt2.h
 SIGNATURES = {
     "gpt2_build_ex": (P, [I, I, I, I, I, I, ct.POINTER(I)]),
+    "gpt2_build_norm": (P, [I, I, I, I, I, I, I, ct.POINTER(I)]),
     "gpt2_build": (P, [I, I, I, I, I]),
     "gpt2_free": (None, [P]),
     "gpt2_num_params": (SZ, [P]),
@@ -39,6 +40,8 @@ SIGNATURES = {
     "gpt2_update": (I, [P, F, F, F, F, F, I]),
     "gpt2_get_losses": (I, [P, P, SZ]),
     "gpt2_get_logits": (I, [P, P, SZ]),
+    "gpt2_generate": (I, [P, P, I, I, I, F, P, P]),
+    "gpt2_get_gen_logits": (I, [P, P, SZ]),
     "gpt2_get_ids": (I, [P, P, P, SZ]),
     "gpt2_profile_enable": (I, [P, I]),
     "gpt2_profile_reset": (I, [P]),
@@ -65,6 +68,9 @@ SIGNATURES = {
     "gpt2_op_layernorm_forward": (I, [I, P, P, P, P, P, P, I, I, P]),
     "gpt2_op_layernorm_backward_workspace": (SZ, [I]),
     "gpt2_op_layernorm_backward": (I, [I, P, P, P, P, P, P, P, P, I, I, P, SZ, P]),
+    "gpt2_op_rmsnorm_forward": (I, [I, P, P, P, P, I, I, P]),
+    "gpt2_op_rmsnorm_backward_workspace": (SZ, [I]),
+    "gpt2_op_rmsnorm_backward": (I, [I, P, P, P, P, P, P, I, I, P, SZ, P]),
     "gpt2_op_softmax_xent": (I, [I, P, P, P, I, I, I, F, P, P]),
 }
 
@@ -77,6 +83,7 @@ for _name, (_res, _args) in SIGNATURES.items():
 GPT2_OK, GPT2_ERR_ARG, GPT2_ERR_OOM, GPT2_ERR_CUDA = 0, -1, -2, -3
 GPT2_ERR_TOKEN, GPT2_ERR_SHAPE, GPT2_ERR_STATE, GPT2_ERR_NONFINITE, GPT2_ERR_TIMEOUT = -4, -5, -6, -7, -8
 GPT2_FP32, GPT2_BF16 = 0, 2
+GPT2_LAYERNORM, GPT2_RMSNORM = 0, 1
 GPT2_DT_F32, GPT2_DT_BF16 = 0, 1
 GPT2_HOST, GPT2_DEVICE = 0, 1
 GPT2_EPI_STORE, GPT2_EPI_GELU, GPT2_EPI_GELU_BWD = 0, 1, 2

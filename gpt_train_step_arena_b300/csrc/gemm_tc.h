@@ -8,6 +8,8 @@ namespace g2 {
 bool gemm_tc_supported(const GemmArgs& a);
 // Workspace the kernel wants for split-K partial sums of an fp32-output product.
 size_t gemm_tc_workspace_bytes(int M, int N, int K);
+// Workspace of a product with one row tile (M <= 128) launched with skinny_split set.
+size_t gemm_tc_skinny_workspace_bytes(int M, int N, int K);
 // flags (may be null): G2_FLAG_TIMEOUT is OR-ed in if a bounded wait expires.
 cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, cudaStream_t s);
 

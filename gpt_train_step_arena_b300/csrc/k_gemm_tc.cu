@@ -456,6 +456,26 @@ __global__ void splitk_reduce_k(float* out, long long ldo, const float* ws, int 
     }
 }
 
+// The same sum with the forward epilogue of a split product: v = sum_s ws[s][m][n]
+// (+ bias[n]) (+ R[m,n]); D = v (bf16, or fp32 with d_f32); with D2, D2 = gelu(v) from the
+// unrounded v (as the fused GELU epilogue does).
+__global__ void splitk_epilogue_k(void* D, long long ldd, int d_f32, const float* ws, int M, int N, int splits,
+                                  const float* bias, const bf16* R, long long ldr, bf16* D2, long long ldd2) {
+    size_t n = (size_t)M * N;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        float a = 0.f;
+        for (int s = 0; s < splits; s++) a += ws[(size_t)s * n + i];
+        const int m = (int)(i / N), c = (int)(i % N);
+        if (bias) a += bias[c];
+        if (R) a += __bfloat162float(R[(size_t)m * ldr + c]);
+        if (d_f32)
+            ((float*)D)[(size_t)m * ldd + c] = a;
+        else
+            ((bf16*)D)[(size_t)m * ldd + c] = __float2bfloat16_rn(a);
+        if (D2) D2[(size_t)m * ldd2 + c] = __float2bfloat16_rn(gelu_tanh_fast(a));
+    }
+}
+
 // ------------------------------------------------------------------ host side
 static int num_sms() {
     static int n = 0;
@@ -546,6 +566,32 @@ static void plan(int M, int N, int K, int BN, int& splits, int& kb_per) {
     splits = (num_kb + kb_per - 1) / kb_per;
 }
 
+// Split-K plan for a product with a single row tile (a few rows: the one-token steps of
+// generation), where the time goes into streaming B: enough (column tile, split) units
+// to keep every SM loading, while the fp32 partials (splits*M*N*4 bytes) stay within
+// half of B's own bytes (N*K*2).
+static int skinny_bn(int M, int N) {
+    const int tiles256 = (N + 255) / 256;
+    return (N <= 128 || (M <= 128 && tiles256 < num_sms())) ? 128 : 256;
+}
+static void plan_skinny(int M, int N, int K, int BN, int& splits, int& kb_per) {
+    const int tiles = (N + BN - 1) / BN;
+    const int num_kb = (K + BK - 1) / BK;
+    const int want = (2 * num_sms() + tiles - 1) / tiles;
+    const int cap = std::max(1, K / (4 * std::max(M, 1)));
+    splits = std::max(1, std::min(std::min(want, num_kb), cap));
+    kb_per = (num_kb + splits - 1) / splits;
+    splits = (num_kb + kb_per - 1) / kb_per;
+}
+
+size_t gemm_tc_skinny_workspace_bytes(int M, int N, int K) {
+    if (M > 128) return 0;
+    const int BN = skinny_bn(M, N);
+    int splits, kb_per;
+    plan_skinny(M, N, K, BN, splits, kb_per);
+    return splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+}
+
 size_t gemm_tc_workspace_bytes(int M, int N, int K) {
     int BN = N > 128 ? 256 : 128, splits, kb_per;
     plan(M, N, K, BN, splits, kb_per);
@@ -574,7 +620,8 @@ bool gemm_tc_supported(const GemmArgs& a) {
 
 cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, cudaStream_t s) {
     const bool a_mn = a.sAk != 1, b_mn = a.sBk != 1;
-    const int BN = a.N > 128 ? 256 : 128;
+    const bool skinny = a.skinny_split && a.M <= 128 && a.epi != EPI_GELU_BWD;
+    const int BN = skinny ? skinny_bn(a.M, a.N) : (a.N > 128 ? 256 : 128);
     const bool staged_in = a.epi == EPI_GELU_BWD || (a.epi == EPI_STORE && a.R && !a.d_f32);
     const int bmt = tile_rows(a.M, a.N, a.K, BN, staged_in);
     Maps mp;
@@ -596,7 +643,10 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
     p.tiles_n = (a.N + BN - 1) / BN;
     p.num_kb = (a.K + BK - 1) / BK;
     int splits = 1, kb_per = p.num_kb;
-    if (a.epi == EPI_STORE && a.d_f32 && !a.bias && !a.R) plan(a.M, a.N, a.K, BN, splits, kb_per);
+    if (skinny)
+        plan_skinny(a.M, a.N, a.K, BN, splits, kb_per);
+    else if (a.epi == EPI_STORE && a.d_f32 && !a.bias && !a.R)
+        plan(a.M, a.N, a.K, BN, splits, kb_per);
     if (splits > 1 && (!ws || ws_bytes < (size_t)splits * a.M * a.N * sizeof(float))) {
         splits = 1;
         kb_per = p.num_kb;
@@ -648,7 +698,12 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
         if (e != cudaSuccess) return e;
         size_t n = (size_t)a.M * a.N;
         unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
-        G2_LAUNCH splitk_reduce_k<<<blocks, 256, 0, s>>>((float*)a.D, a.ldd, ws, a.M, a.N, splits);
+        if (skinny)
+            G2_LAUNCH splitk_epilogue_k<<<blocks, 256, 0, s>>>(
+                a.D, a.ldd, a.d_f32, ws, a.M, a.N, splits, a.bias, (const bf16*)a.R, a.ldr,
+                a.epi == EPI_GELU ? (bf16*)a.D2 : nullptr, a.ldd2);
+        else
+            G2_LAUNCH splitk_reduce_k<<<blocks, 256, 0, s>>>((float*)a.D, a.ldd, ws, a.M, a.N, splits);
         return cudaGetLastError();
     }
     switch (a.epi) {

@@ -285,9 +285,12 @@ cudaError_t encoder_backward_wte(ActType at, float* dwte, const void* dout, cons
 // ------------------------------------------------------------------ layernorm forward
 // llm.c §1.3 / picoGPT layer_norm: one warp per row; mean, biased variance (two passes
 // over the row held in registers), rstd = 1/sqrt(var + 1e-5).
+// rms != 0 gives the RMSNorm of the microGPT variant ("microGPT 3D", lesson 04): the
+// mean is taken as 0 (so the "variance" is the mean square), the shift b is not read
+// (may be null) and mean[] receives 0.
 template <typename T, int NV>
 __global__ void ln_fwd_vec_k(T* out, float* mean, float* rstd, const T* inp, const float* w,
-                             const float* b, int M, int C) {
+                             const float* b, int M, int C, int rms) {
     int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (row >= M) return;
     const T* x = inp + (size_t)row * C;
@@ -299,7 +302,7 @@ __global__ void ln_fwd_vec_k(T* out, float* mean, float* rstd, const T* inp, con
 #pragma unroll
         for (int i = 0; i < 8; i++) s += v[j][i];
     }
-    float m = warp_sum(s) / C;
+    float m = rms ? 0.f : warp_sum(s) / C;
     float q = 0.f;
 #pragma unroll
     for (int j = 0; j < NV; j++)
@@ -314,15 +317,15 @@ __global__ void ln_fwd_vec_k(T* out, float* mean, float* rstd, const T* inp, con
 #pragma unroll
     for (int j = 0; j < NV; j++) {
         int c = j * 256 + lane * 8;
-        float wv[8], bv[8], y[8];
+        float wv[8], bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, y[8];
         Vec8<float>::load(w + c, wv);
-        Vec8<float>::load(b + c, bv);
+        if (!rms) Vec8<float>::load(b + c, bv);
 #pragma unroll
         for (int i = 0; i < 8; i++) y[i] = (v[j][i] - m) * r * wv[i] + bv[i];
         Vec8<T>::store(o + c, y);
     }
     if (lane == 0) {
-        mean[row] = m;
+        if (mean) mean[row] = m;
         rstd[row] = r;
     }
 }
@@ -333,7 +336,7 @@ __global__ void ln_fwd_vec_k(T* out, float* mean, float* rstd, const T* inp, con
 // tiles (3 x 32 rows) in flight per SM without holding them in registers.
 constexpr int LNT_ROWS = 32, LNT_STAGES = 3, LNT_THREADS = 288;
 
-template <int NV>
+template <int NV, bool RMS>
 __global__ void __launch_bounds__(LNT_THREADS, 1) ln_fwd_tma_k(bf16* out, float* mean, float* rstd, const bf16* inp,
                                                                const float* w, const float* b, int M, int C) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -371,7 +374,12 @@ __global__ void __launch_bounds__(LNT_THREADS, 1) ln_fwd_tma_k(bf16* out, float*
 #pragma unroll
         for (int j = 0; j < NV; j++) {
             Vec8<float>::load(w + j * 256 + lane * 8, wv[j]);
-            Vec8<float>::load(b + j * 256 + lane * 8, bv[j]);
+            if (RMS) {
+#pragma unroll
+                for (int i = 0; i < 8; i++) bv[j][i] = 0.f;
+            } else {
+                Vec8<float>::load(b + j * 256 + lane * 8, bv[j]);
+            }
         }
         int it = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, it++) {
@@ -390,7 +398,7 @@ __global__ void __launch_bounds__(LNT_THREADS, 1) ln_fwd_tma_k(bf16* out, float*
 #pragma unroll
                     for (int i = 0; i < 8; i++) sum += v[j][i];
                 }
-                const float m = warp_sum(sum) / C;
+                const float m = RMS ? 0.f : warp_sum(sum) / C;
                 float q = 0.f;
 #pragma unroll
                 for (int j = 0; j < NV; j++)
@@ -410,7 +418,7 @@ __global__ void __launch_bounds__(LNT_THREADS, 1) ln_fwd_tma_k(bf16* out, float*
                     Vec8<bf16>::store(o + j * 256 + lane * 8, y);
                 }
                 if (lane == 0) {
-                    mean[row] = m;
+                    if (mean) mean[row] = m;
                     rstd[row] = rs;
                 }
             }
@@ -431,32 +439,39 @@ static int sm_count() {
     return n;
 }
 
-template <int NV>
-static cudaError_t ln_fwd_tma_launch(bf16* out, float* mean, float* rstd, const bf16* inp, const float* w,
-                                     const float* b, int M, int C, cudaStream_t s) {
+template <int NV, bool RMS>
+static cudaError_t ln_fwd_tma_launch_t(bf16* out, float* mean, float* rstd, const bf16* inp, const float* w,
+                                       const float* b, int M, int C, cudaStream_t s) {
     const int smem = LNT_STAGES * LNT_ROWS * C * 2 + 256;
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(ln_fwd_tma_k<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(ln_fwd_tma_k<NV, RMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              LNT_STAGES * LNT_ROWS * (NV * 256) * 2 + 256);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
     const int ntiles = (M + LNT_ROWS - 1) / LNT_ROWS;
-    G2_LAUNCH ln_fwd_tma_k<NV><<<std::min(ntiles, sm_count()), LNT_THREADS, smem, s>>>(out, mean, rstd, inp, w, b,
-                                                                                      M, C);
+    G2_LAUNCH ln_fwd_tma_k<NV, RMS><<<std::min(ntiles, sm_count()), LNT_THREADS, smem, s>>>(out, mean, rstd, inp, w,
+                                                                                           b, M, C);
     return cudaGetLastError();
+}
+
+template <int NV>
+static cudaError_t ln_fwd_tma_launch(bf16* out, float* mean, float* rstd, const bf16* inp, const float* w,
+                                     const float* b, int M, int C, int rms, cudaStream_t s) {
+    return rms ? ln_fwd_tma_launch_t<NV, true>(out, mean, rstd, inp, w, b, M, C, s)
+               : ln_fwd_tma_launch_t<NV, false>(out, mean, rstd, inp, w, b, M, C, s);
 }
 
 template <typename T>
 __global__ void ln_fwd_gen_k(T* out, float* mean, float* rstd, const T* inp, const float* w,
-                             const float* b, int M, int C) {
+                             const float* b, int M, int C, int rms) {
     int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (row >= M) return;
     const T* x = inp + (size_t)row * C;
     float s = 0.f;
     for (int c = lane; c < C; c += 32) s += to_f(x[c]);
-    float m = warp_sum(s) / C;
+    float m = rms ? 0.f : warp_sum(s) / C;
     float q = 0.f;
     for (int c = lane; c < C; c += 32) {
         float d = to_f(x[c]) - m;
@@ -465,45 +480,47 @@ __global__ void ln_fwd_gen_k(T* out, float* mean, float* rstd, const T* inp, con
     float var = warp_sum(q) / C;
     float r = 1.0f / sqrtf(var + 1e-5f);
     T* o = out + (size_t)row * C;
-    for (int c = lane; c < C; c += 32) o[c] = from_f<T>((to_f(x[c]) - m) * r * w[c] + b[c]);
+    for (int c = lane; c < C; c += 32) o[c] = from_f<T>((to_f(x[c]) - m) * r * w[c] + (rms ? 0.f : b[c]));
     if (lane == 0) {
-        mean[row] = m;
+        if (mean) mean[row] = m;
         rstd[row] = r;
     }
 }
 
 template <typename T>
 static void ln_fwd_launch(T* out, float* mean, float* rstd, const T* inp, const float* w,
-                          const float* b, int M, int C, cudaStream_t s) {
+                          const float* b, int M, int C, int rms, cudaStream_t s) {
     unsigned g = cdiv(M, 8);
     const bool aligned = (((uintptr_t)w | (uintptr_t)b) & 15) == 0;
     switch (C % 256 == 0 && aligned ? C / 256 : 0) {
-        case 1: count_launches(1); ln_fwd_vec_k<T, 1><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
-        case 2: count_launches(1); ln_fwd_vec_k<T, 2><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
-        case 3: count_launches(1); ln_fwd_vec_k<T, 3><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
-        case 4: count_launches(1); ln_fwd_vec_k<T, 4><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
-        case 5: count_launches(1); ln_fwd_vec_k<T, 5><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
-        case 6: count_launches(1); ln_fwd_vec_k<T, 6><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
-        default: count_launches(1); ln_fwd_gen_k<T><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C); break;
+        case 1: count_launches(1); ln_fwd_vec_k<T, 1><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
+        case 2: count_launches(1); ln_fwd_vec_k<T, 2><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
+        case 3: count_launches(1); ln_fwd_vec_k<T, 3><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
+        case 4: count_launches(1); ln_fwd_vec_k<T, 4><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
+        case 5: count_launches(1); ln_fwd_vec_k<T, 5><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
+        case 6: count_launches(1); ln_fwd_vec_k<T, 6><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
+        default: count_launches(1); ln_fwd_gen_k<T><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
     }
 }
 
 cudaError_t layernorm_forward(ActType at, void* out, float* mean, float* rstd, const void* inp,
-                              const float* w, const float* b, int M, int C, cudaStream_t s) {
+                              const float* w, const float* b, int M, int C, NormKind nk, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
+    const int rms = nk == NORM_RMS;
+    if (rms) b = w;  // not read; keeps the alignment test below meaningful
     const bool al = ((((uintptr_t)out | (uintptr_t)inp | (uintptr_t)w | (uintptr_t)b)) & 15) == 0;
     if (at == ACT_BF16 && al && C % 256 == 0 && C / 256 >= 1 && C / 256 <= 4) {
         switch (C / 256) {
-            case 1: return ln_fwd_tma_launch<1>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, s);
-            case 2: return ln_fwd_tma_launch<2>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, s);
-            case 3: return ln_fwd_tma_launch<3>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, s);
-            default: return ln_fwd_tma_launch<4>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, s);
+            case 1: return ln_fwd_tma_launch<1>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, rms, s);
+            case 2: return ln_fwd_tma_launch<2>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, rms, s);
+            case 3: return ln_fwd_tma_launch<3>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, rms, s);
+            default: return ln_fwd_tma_launch<4>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, rms, s);
         }
     }
     if (at == ACT_BF16)
-        ln_fwd_launch<bf16>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, s);
+        ln_fwd_launch<bf16>((bf16*)out, mean, rstd, (const bf16*)inp, w, b, M, C, rms, s);
     else
-        ln_fwd_launch<float>((float*)out, mean, rstd, (const float*)inp, w, b, M, C, s);
+        ln_fwd_launch<float>((float*)out, mean, rstd, (const float*)inp, w, b, M, C, rms, s);
     return cudaGetLastError();
 }
 
@@ -517,6 +534,8 @@ cudaError_t colsum(ActType at, float* out, const void* X, int M, int N, float* p
 // the problem size only.  Optionally (OUTSUM) a third set part[2 nblk + block][C] sums
 // the updated dres rows as stored: that column sum is the bias gradient of the linear
 // layer whose output gradient dres is (llm.c §1.6), so it needs no pass of its own.
+// rms != 0: the RMSNorm backward (mean taken as 0, no mean(w*dout) term, mean[] not
+// read, db comes out exactly 0 since the shift is not part of the RMSNorm).
 static const int LNB_BLOCKS = 296;      // generic kernel: 8 warps per block
 static const int LNB_VEC_BLOCKS = 592;      // vector kernel: 4 warps per block, 4 blocks per SM
 static const int LNB_VEC_SUM_BLOCKS = 444;  // with the third sum: 3 blocks per SM
@@ -528,7 +547,7 @@ size_t ln_bwd_partial_floats(int C) { return (size_t)3 * LNB_VEC_BLOCKS * C; }
 template <typename T, int NV, bool OUTSUM>
 __global__ void __launch_bounds__(128) ln_bwd_vec_k(T* dres, float* part, const T* dout, const T* inp,
                                                     const float* w, const float* mean,
-                                                    const float* rstd, int M, int C) {
+                                                    const float* rstd, int M, int C, int rms) {
     constexpr int NS = OUTSUM ? 3 : 2;
     __shared__ float sh[4][NS][NV * 256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -550,7 +569,7 @@ __global__ void __launch_bounds__(128) ln_bwd_vec_k(T* dres, float* part, const 
             Vec8<T>::load(d + j * 256 + lane * 8, dv[j]);
             Vec8<T>::load(x + j * 256 + lane * 8, xv[j]);
         }
-        const float m = mean[row], r = rstd[row];
+        const float m = rms ? 0.f : mean[row], r = rstd[row];
         float gm = 0.f, gnm = 0.f;
 #pragma unroll
         for (int j = 0; j < NV; j++) {
@@ -564,12 +583,12 @@ __global__ void __launch_bounds__(128) ln_bwd_vec_k(T* dres, float* part, const 
                 float g = wv[i] * dv[j][i];
                 gm += g;
                 gnm += g * n;
-                ab[j][i] += dv[j][i];
+                ab[j][i] += rms ? 0.f : dv[j][i];
                 aw[j][i] += n * dv[j][i];
                 dv[j][i] = g;                 // keep w*dout
             }
         }
-        gm = warp_sum(gm) / C;
+        gm = rms ? 0.f : warp_sum(gm) / C;
         gnm = warp_sum(gnm) / C;
 #pragma unroll
         for (int j = 0; j < NV; j++) {
@@ -609,7 +628,7 @@ __global__ void __launch_bounds__(128) ln_bwd_vec_k(T* dres, float* part, const 
 // depends on (M, C, grid) only.
 constexpr int LNB_ROWS = 16, LNB_STAGES = 3;
 
-template <int NV, bool OUTSUM>
+template <int NV, bool OUTSUM, bool RMS>
 __global__ void __launch_bounds__(LNT_THREADS, 1)
     ln_bwd_tma_k(bf16* dres, float* part, const bf16* dout, const bf16* inp, const float* w, const float* mean,
                  const float* rstd, int M, int C) {
@@ -678,7 +697,7 @@ __global__ void __launch_bounds__(LNT_THREADS, 1)
                     Vec8<bf16>::load(d + j * 256 + lane * 8, dv[j]);
                     Vec8<bf16>::load(x + j * 256 + lane * 8, xv[j]);
                 }
-                const float m = mean[row], rs = rstd[row];
+                const float m = RMS ? 0.f : mean[row], rs = rstd[row];
                 float gm = 0.f, gnm = 0.f;
 #pragma unroll
                 for (int j = 0; j < NV; j++)
@@ -689,11 +708,11 @@ __global__ void __launch_bounds__(LNT_THREADS, 1)
                         const float g = wv[j][i] * dv[j][i];
                         gm += g;
                         gnm += g * n;
-                        ab[j][i] += dv[j][i];
+                        if (!RMS) ab[j][i] += dv[j][i];
                         aw[j][i] += n * dv[j][i];
                         dv[j][i] = g;
                     }
-                gm = warp_sum(gm) / C;
+                gm = RMS ? 0.f : warp_sum(gm) / C;
                 gnm = warp_sum(gnm) / C;
                 bf16* dr_out = dres + (size_t)row * C;
 #pragma unroll
@@ -742,7 +761,7 @@ __global__ void __launch_bounds__(LNT_THREADS, 1)
 template <typename T>
 __global__ void __launch_bounds__(256) ln_bwd_k(T* dres, float* part, const T* dout, const T* inp,
                                                 const float* w, const float* mean,
-                                                const float* rstd, int M, int C) {
+                                                const float* rstd, int M, int C, int rms) {
     extern __shared__ float sh[];  // [8 warps][2][C]
     int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float* my_dw = sh + (size_t)warp * 2 * C;
@@ -755,7 +774,7 @@ __global__ void __launch_bounds__(256) ln_bwd_k(T* dres, float* part, const T* d
         const T* d = dout + (size_t)row * C;
         const T* x = inp + (size_t)row * C;
         T* dr = dres + (size_t)row * C;
-        float m = mean[row], r = rstd[row];
+        float m = rms ? 0.f : mean[row], r = rstd[row];
         float gm = 0.f, gnm = 0.f;
         for (int c = lane; c < C; c += 32) {
             float n = (to_f(x[c]) - m) * r;
@@ -763,13 +782,13 @@ __global__ void __launch_bounds__(256) ln_bwd_k(T* dres, float* part, const T* d
             gm += g;
             gnm += g * n;
         }
-        gm = warp_sum(gm) / C;
+        gm = rms ? 0.f : warp_sum(gm) / C;
         gnm = warp_sum(gnm) / C;
         for (int c = lane; c < C; c += 32) {
             float dv = to_f(d[c]);
             float n = (to_f(x[c]) - m) * r;
             float g = w[c] * dv;
-            my_db[c] += dv;
+            my_db[c] += rms ? 0.f : dv;
             my_dw[c] += n * dv;
             float val = (g - gm - n * gnm) * r;
             dr[c] = from_f<T>(to_f(dr[c]) + val);
@@ -827,25 +846,35 @@ static cudaError_t colreduce(float* out0, float* out1, float* out2, const float*
     return cudaGetLastError();
 }
 
-template <int NV, bool OUTSUM>
-static cudaError_t ln_bwd_tma_launch(bf16* dres, float* part, const bf16* dout, const bf16* inp, const float* w,
-                                     const float* mean, const float* rstd, int M, int C, int grid, cudaStream_t s) {
+template <int NV, bool OUTSUM, bool RMS>
+static cudaError_t ln_bwd_tma_launch_t(bf16* dres, float* part, const bf16* dout, const bf16* inp, const float* w,
+                                       const float* mean, const float* rstd, int M, int C, int grid, cudaStream_t s) {
     const int smem = LNB_STAGES * 3 * LNB_ROWS * C * 2 + 256;
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(ln_bwd_tma_k<NV, OUTSUM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(ln_bwd_tma_k<NV, OUTSUM, RMS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              LNB_STAGES * 3 * LNB_ROWS * (NV * 256) * 2 + 256);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    G2_LAUNCH ln_bwd_tma_k<NV, OUTSUM><<<grid, LNT_THREADS, smem, s>>>(dres, part, dout, inp, w, mean, rstd, M, C);
+    G2_LAUNCH ln_bwd_tma_k<NV, OUTSUM, RMS><<<grid, LNT_THREADS, smem, s>>>(dres, part, dout, inp, w, mean, rstd, M,
+                                                                             C);
     return cudaGetLastError();
+}
+
+template <int NV, bool OUTSUM>
+static cudaError_t ln_bwd_tma_launch(bf16* dres, float* part, const bf16* dout, const bf16* inp, const float* w,
+                                     const float* mean, const float* rstd, int M, int C, int grid, int rms,
+                                     cudaStream_t s) {
+    return rms ? ln_bwd_tma_launch_t<NV, OUTSUM, true>(dres, part, dout, inp, w, mean, rstd, M, C, grid, s)
+               : ln_bwd_tma_launch_t<NV, OUTSUM, false>(dres, part, dout, inp, w, mean, rstd, M, C, grid, s);
 }
 
 template <typename T>
 static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, float* dres_sum, const T* dout, const T* inp,
                                  const float* w, const float* mean, const float* rstd, int M, int C,
-                                 float* part, float* cs_part, cudaStream_t s) {
+                                 float* part, float* cs_part, int rms, cudaStream_t s) {
     const bool aligned = ((uintptr_t)w & 15) == 0;
     const bool al_all = ((((uintptr_t)dres | (uintptr_t)dout | (uintptr_t)inp | (uintptr_t)w)) & 15) == 0;
     if (std::is_same<T, bf16>::value && al_all && M > 0 && C % 256 == 0 && C / 256 >= 1 && C / 256 <= 3) {
@@ -857,8 +886,8 @@ static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, float* dres_sum,
         const bf16 *dd = (const bf16*)dout, *xx = (const bf16*)inp;
 #define G2_LNBT(NVV)                                                                                        \
     case NVV:                                                                                               \
-        e = dres_sum ? ln_bwd_tma_launch<NVV, true>(dr, part, dd, xx, w, mean, rstd, M, C, grid, s)          \
-                     : ln_bwd_tma_launch<NVV, false>(dr, part, dd, xx, w, mean, rstd, M, C, grid, s);        \
+        e = dres_sum ? ln_bwd_tma_launch<NVV, true>(dr, part, dd, xx, w, mean, rstd, M, C, grid, rms, s)     \
+                     : ln_bwd_tma_launch<NVV, false>(dr, part, dd, xx, w, mean, rstd, M, C, grid, rms, s);   \
         break;
         switch (C / 256) {
             G2_LNBT(1) G2_LNBT(2) default: G2_LNBT(3)
@@ -873,10 +902,10 @@ static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, float* dres_sum,
     case NVV:                                                                                             \
         if (dres_sum)                                                                                     \
             G2_LAUNCH ln_bwd_vec_k<T, NVV, true><<<LNB_VEC_SUM_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, \
-                                                                                   rstd, M, C);           \
+                                                                                   rstd, M, C, rms);      \
         else                                                                                              \
             G2_LAUNCH ln_bwd_vec_k<T, NVV, false><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, \
-                                                                                rstd, M, C);              \
+                                                                                rstd, M, C, rms);         \
         break;
         switch (nv) {
             G2_LNB_CASE(1) G2_LNB_CASE(2) G2_LNB_CASE(3) G2_LNB_CASE(4)
@@ -888,7 +917,7 @@ static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, float* dres_sum,
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(ln_bwd_k<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    G2_LAUNCH ln_bwd_k<T><<<LNB_BLOCKS, 256, smem, s>>>(dres, part, dout, inp, w, mean, rstd, M, C);
+    G2_LAUNCH ln_bwd_k<T><<<LNB_BLOCKS, 256, smem, s>>>(dres, part, dout, inp, w, mean, rstd, M, C, rms);
     cudaError_t e = colreduce(dw, db, nullptr, part, LNB_BLOCKS, C, s);
     if (e != cudaSuccess || !dres_sum) return e;
     // the generic kernel keeps no third sum: column-sum the updated rows separately
@@ -897,13 +926,14 @@ static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, float* dres_sum,
 
 cudaError_t layernorm_backward(ActType at, void* dres, float* dw, float* db, float* dres_sum, const void* dout,
                                const void* inp, const float* w, const float* mean, const float* rstd, int M,
-                               int C, float* part, float* cs_part, cudaStream_t s) {
+                               int C, float* part, float* cs_part, NormKind nk, cudaStream_t s) {
     if (dres_sum && !cs_part) return cudaErrorInvalidValue;
+    const int rms = nk == NORM_RMS;
     if (at == ACT_BF16)
         return ln_bwd_launch<bf16>((bf16*)dres, dw, db, dres_sum, (const bf16*)dout, (const bf16*)inp, w, mean,
-                                   rstd, M, C, part, cs_part, s);
+                                   rstd, M, C, part, cs_part, rms, s);
     return ln_bwd_launch<float>((float*)dres, dw, db, dres_sum, (const float*)dout, (const float*)inp, w, mean,
-                                rstd, M, C, part, cs_part, s);
+                                rstd, M, C, part, cs_part, rms, s);
 }
 
 // ------------------------------------------------------------------ bias gradient

@@ -43,9 +43,12 @@ void encoder_bwd_scratch_carve(EncoderBwdScratch* sc, void* base, int M, int V, 
 cudaError_t encoder_backward_wte(ActType at, float* dwte, const void* dout, const int32_t* tok,
                                  int M, int C, int V, const EncoderBwdScratch* sc, cudaStream_t s);
 
-// ---- layernorm (llm.c §1.3, §1.4) ----------------------------------------------
+// ---- layernorm (llm.c §1.3, §1.4) and RMSNorm ("microGPT 3D", lesson 04) ---------
+// NORM_RMS: out = x * rstd * w with rstd = 1/sqrt(mean(x^2) + 1e-5); b is not read (may be
+// null), mean (may be null) receives 0; the backward leaves db = 0 and ignores mean.
+enum NormKind { NORM_LAYER = 0, NORM_RMS = 1 };
 cudaError_t layernorm_forward(ActType at, void* out, float* mean, float* rstd, const void* inp,
-                              const float* w, const float* b, int M, int C, cudaStream_t s);
+                              const float* w, const float* b, int M, int C, NormKind nk, cudaStream_t s);
 // dres (M,C) += LN-backward(dout); dw, db (C) fp32 overwritten.  part: ln_bwd_partial_floats().
 // dres_sum (C floats, may be null) receives the column sums of the updated dres as stored
 // (the bias gradient of the layer whose output gradient dres is); cs_part (colsum
@@ -53,7 +56,7 @@ cudaError_t layernorm_forward(ActType at, void* out, float* mean, float* rstd, c
 size_t ln_bwd_partial_floats(int C);
 cudaError_t layernorm_backward(ActType at, void* dres, float* dw, float* db, float* dres_sum, const void* dout,
                                const void* inp, const float* w, const float* mean, const float* rstd, int M,
-                               int C, float* part, float* cs_part, cudaStream_t s);
+                               int C, float* part, float* cs_part, NormKind nk, cudaStream_t s);
 
 // ---- bias gradient: out[n] = sum_m X[m,n] (fixed order) --------------------------
 size_t colsum_partial_floats(int M, int N);
@@ -103,6 +106,29 @@ cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, 
 cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv, const void* out, const float* lse,
                                   int B, int T, int C, int NH, float* Dbuf, int* flags, cudaStream_t s);
 
+// ---- generation with a key/value cache (picoGPT generate; llm.c §1.35 sample_mult) ----
+// Rows r = b*n + i are the new positions t0+i of sequence b; ids is (B, maxT) int32 and
+// kv (B, maxT, 2C) holds [key | value] of every position computed so far.  dstate (may
+// be null): 4 ints in device memory {t0, step, n_new, temperature bits} that replace the
+// corresponding arguments (one-token steps replayed from a CUDA graph).
+cudaError_t gen_embed(ActType at, void* x, const int32_t* ids, const void* wte, const void* wpe, int B, int n, int t0,
+                      int maxT, int C, const int* dstate, cudaStream_t s);
+cudaError_t gen_kv_append(ActType at, void* kv, const void* qkv, int B, int n, int t0, int maxT, int C,
+                          const int* dstate, cudaStream_t s);
+// out (B*n, C) = attention of each new query over the cached positions 0..t0+i.
+size_t gen_attn_smem_bytes(int C, int NH, int maxT);
+cudaError_t gen_attention(ActType at, void* out, const void* qkv, const void* kv, int B, int n, int t0, int maxT,
+                          int C, int NH, const int* dstate, cudaStream_t s);
+cudaError_t gen_last_rows(ActType at, void* last, const void* x, int B, int n, int C, cudaStream_t s);
+// Next id per sequence from logits (B, Vp): argmax (temperature <= 0) or sample_mult over
+// softmax(logits / temperature) with coins[b*n_new + step]; written to ids[b, t_next]
+// (if t_next < maxT) and out[b*n_new + step].  With dstate: t_next = t0 + 1.
+cudaError_t gen_sample(ActType at, int32_t* ids, int32_t* out, const void* logits, int B, int V, int Vp,
+                       float temperature, const float* coins, int step, int n_new, int t_next, int maxT,
+                       const int* dstate, cudaStream_t s);
+// dstate t0 and step += 1.
+cudaError_t gen_advance(int* dstate, cudaStream_t s);
+
 // ---- GEMM --------------------------------------------------------------------------
 // D[m,n] = epilogue( sum_k A(m,k) * B(n,k) ), A(m,k) = A[m*sAm + k*sAk], B(n,k) = B[n*sBn + k*sBk].
 enum Epilogue {
@@ -122,6 +148,7 @@ struct GemmArgs {
     const void* P; long long ldp;        // EPI_GELU_BWD pre-activation (in_type)
     int epi;
     int* flags;                 // device error flags (G2_FLAG_TIMEOUT), or null
+    int skinny_split;           // one row tile (M <= 128): split K, epilogue in the fixed-order reduce
 };
 cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t s);
 

@@ -21,6 +21,7 @@
 #include "../../include/gpt2.h"
 #include "common.cuh"
 #include "dispatch.h"
+#include "gemm_tc.h"
 #include "kernels.h"
 
 namespace g2 {
@@ -38,6 +39,7 @@ enum { NP = 16 };
 struct gpt2 {
     int L, C, NH, V, Vp, maxT, prec;
     ActType at;
+    NormKind nk;  // LayerNorm (GPT-2) or RMSNorm (the microGPT variant)
     size_t esz;  // bytes per activation element
     size_t psize[NP], poff[NP];  // padded sizes / offsets (elements)
     size_t npad, nreal;
@@ -68,6 +70,21 @@ struct gpt2 {
     size_t ev_used;
     double prof_ms[GPT2_K_COUNT], prof_work[GPT2_K_COUNT];
     uint64_t prof_calls[GPT2_K_COUNT];
+    // generation (gpt2_generate): key/value cache of gB sequences of up to maxT positions
+    // and the working rows of one extend step (up to gB*maxT rows for a prompt)
+    void* garena;
+    size_t gbytes;
+    int gB;
+    char *g_kv, *g_x, *g_x2, *g_ln, *g_qkv, *g_atty, *g_fch, *g_fchg, *g_last, *g_lnl, *g_logits;
+    float *g_mean, *g_rstd, *g_coins, *g_ws;
+    size_t g_ws_bytes;
+    int32_t *g_ids, *g_out;
+    int *g_flags, *g_state;
+    bool gen_logits_valid;
+    cudaStream_t g_stream;       // generation runs here (graph capture needs a non-legacy stream)
+    cudaEvent_t g_ev;
+    cudaGraphExec_t g_step;      // captured one-token step (position read from g_state)
+    unsigned g_step_launches;    // kernels in it
     cudaStream_t stream;
     int status;
     std::string err;
@@ -177,7 +194,7 @@ static cudaError_t gemm_wgrad(gpt2* m, int M, int N, int K, const void* dY, cons
 }
 
 // ------------------------------------------------------------------ build / free
-extern "C" gpt2_t* gpt2_build_ex(int L, int C, int H, int V, int maxT, int precision, int* status) {
+extern "C" gpt2_t* gpt2_build_norm(int L, int C, int H, int V, int maxT, int precision, int norm, int* status) {
     auto bail = [&](int code, const char* msg) -> gpt2_t* {
         g_build_error = msg;
         if (status) *status = code;
@@ -187,11 +204,14 @@ extern "C" gpt2_t* gpt2_build_ex(int L, int C, int H, int V, int maxT, int preci
         return bail(GPT2_ERR_ARG, "bad shape: need L,C,H,V,maxT > 0 and C % H == 0");
     if (precision != GPT2_FP32 && precision != GPT2_BF16)
         return bail(GPT2_ERR_ARG, "precision must be GPT2_FP32 or GPT2_BF16");
+    if (norm != GPT2_LAYERNORM && norm != GPT2_RMSNORM)
+        return bail(GPT2_ERR_ARG, "norm must be GPT2_LAYERNORM or GPT2_RMSNORM");
     if (C % 8) return bail(GPT2_ERR_ARG, "C must be a multiple of 8");
     if (C / H > 256) return bail(GPT2_ERR_ARG, "head size above 256 is not supported");
     gpt2* m = new (std::nothrow) gpt2();
     if (!m) return bail(GPT2_ERR_OOM, "host allocation failed");
     m->L = L; m->C = C; m->NH = H; m->V = V; m->maxT = maxT; m->prec = precision;
+    m->nk = norm == GPT2_RMSNORM ? NORM_RMS : NORM_LAYER;
     m->Vp = (V + 127) / 128 * 128;
     m->at = precision == GPT2_BF16 ? ACT_BF16 : ACT_F32;
     m->esz = m->at == ACT_BF16 ? 2 : 4;
@@ -235,6 +255,10 @@ extern "C" gpt2_t* gpt2_build_ex(int L, int C, int H, int V, int maxT, int preci
     return m;
 }
 
+extern "C" gpt2_t* gpt2_build_ex(int L, int C, int H, int V, int maxT, int precision, int* status) {
+    return gpt2_build_norm(L, C, H, V, maxT, precision, GPT2_LAYERNORM, status);
+}
+
 extern "C" gpt2_t* gpt2_build(int L, int C, int H, int V, int maxT) {
     return gpt2_build_ex(L, C, H, V, maxT, GPT2_BF16, nullptr);
 }
@@ -243,6 +267,10 @@ extern "C" void gpt2_free(gpt2_t* m) {
     if (!m) return;
     if (m->parena) cudaFree(m->parena);
     if (m->aarena) cudaFree(m->aarena);
+    if (m->garena) cudaFree(m->garena);
+    if (m->g_step) cudaGraphExecDestroy(m->g_step);
+    if (m->g_ev) cudaEventDestroy(m->g_ev);
+    if (m->g_stream) cudaStreamDestroy(m->g_stream);
     for (size_t i = 0; i < m->ev_a.size(); i++) {
         cudaEventDestroy(m->ev_a[i]);
         cudaEventDestroy(m->ev_b[i]);
@@ -252,7 +280,7 @@ extern "C" void gpt2_free(gpt2_t* m) {
 
 extern "C" size_t gpt2_num_params(const gpt2_t* m) { return m ? m->nreal : 0; }
 extern "C" int gpt2_padded_vocab(const gpt2_t* m) { return m ? m->Vp : 0; }
-extern "C" size_t gpt2_device_bytes(const gpt2_t* m) { return m ? m->pbytes + m->abytes : 0; }
+extern "C" size_t gpt2_device_bytes(const gpt2_t* m) { return m ? m->pbytes + m->abytes + m->gbytes : 0; }
 extern "C" uint64_t gpt2_kernel_launches(const gpt2_t*) { return launches_total(); }
 extern "C" int gpt2_last_status(const gpt2_t* m) { return m ? m->status : GPT2_ERR_ARG; }
 extern "C" const char* gpt2_last_error(const gpt2_t* m) { return m ? m->err.c_str() : "null handle"; }
@@ -422,7 +450,7 @@ static int forward_impl(gpt2* m, const int32_t* tokens, const int32_t* targets, 
         OP(GPT2_K_LAYERNORM, ln_fwd_bytes,
            layernorm_forward(m->at, ln1, m->ln1_mean + l * M, m->ln1_rstd + l * M, res_in,
                              pf(m, m->params, P_LN1W) + l * C, pf(m, m->params, P_LN1B) + l * C,
-                             (int)M, C, s));
+                             (int)M, C, m->nk, s));
         OP(GPT2_K_GEMM, gemm_flops(M, 3 * C, C),
            gemm_fwd(m, (int)M, 3 * C, C, ln1, pw(m, P_QKVW, (size_t)l * 3 * C * C),
                     pf(m, m->params, P_QKVB) + l * 3 * C, qkv, nullptr, nullptr));
@@ -434,7 +462,7 @@ static int forward_impl(gpt2* m, const int32_t* tokens, const int32_t* targets, 
         OP(GPT2_K_LAYERNORM, ln_fwd_bytes,
            layernorm_forward(m->at, ln2, m->ln2_mean + l * M, m->ln2_rstd + l * M, res2,
                              pf(m, m->params, P_LN2W) + l * C, pf(m, m->params, P_LN2B) + l * C,
-                             (int)M, C, s));
+                             (int)M, C, m->nk, s));
         OP(GPT2_K_GEMM, gemm_flops(M, 4 * C, C),
            gemm_fwd(m, (int)M, 4 * C, C, ln2, pw(m, P_FCW, (size_t)l * 4 * C * C),
                     pf(m, m->params, P_FCB) + l * 4 * C, fch, nullptr, fchg));
@@ -444,7 +472,7 @@ static int forward_impl(gpt2* m, const int32_t* tokens, const int32_t* targets, 
     }
     OP(GPT2_K_LAYERNORM, ln_fwd_bytes,
        layernorm_forward(m->at, m->lnf, m->lnf_mean, m->lnf_rstd, act(m, m->res, (size_t)L * MC),
-                         pf(m, m->params, P_LNFW), pf(m, m->params, P_LNFB), (int)M, C, s));
+                         pf(m, m->params, P_LNFW), pf(m, m->params, P_LNFB), (int)M, C, m->nk, s));
     OP(GPT2_K_GEMM, gemm_flops(M, Vp, C),
        gemm_fwd(m, (int)M, Vp, C, m->lnf, pw(m, P_WTE, 0), nullptr, m->logits, nullptr, nullptr));
     if (targets) {
@@ -526,7 +554,7 @@ extern "C" int gpt2_backward(gpt2_t* m) {
        layernorm_backward(m->at, m->dres, pf(m, g, P_LNFW), pf(m, g, P_LNFB),
                           pf(m, g, P_FPB) + (size_t)(L - 1) * C,  // d res_out(L-1): fcproj bias
                           m->dln, act(m, m->res, (size_t)L * MC), pf(m, m->params, P_LNFW), m->lnf_mean,
-                          m->lnf_rstd, (int)M, C, m->ln_part, m->cs_part, s));
+                          m->lnf_rstd, (int)M, C, m->ln_part, m->cs_part, m->nk, s));
     for (int l = L - 1; l >= 0; l--) {
         char* res_in = act(m, m->res, l * MC);
         char* res2 = act(m, m->res2, l * MC);
@@ -555,7 +583,7 @@ extern "C" int gpt2_backward(gpt2_t* m) {
            layernorm_backward(m->at, m->dres, pf(m, g, P_LN2W) + l * C, pf(m, g, P_LN2B) + l * C,
                               pf(m, g, P_APB) + l * C,  // d res2: attproj bias
                               m->dln, res2, pf(m, m->params, P_LN2W) + l * C,
-                              m->ln2_mean + l * M, m->ln2_rstd + l * M, (int)M, C, m->ln_part, m->cs_part, s));
+                              m->ln2_mean + l * M, m->ln2_rstd + l * M, (int)M, C, m->ln_part, m->cs_part, m->nk, s));
         // attproj: res2 = atty . Wap^T + bap + res_in
         OP(GPT2_K_GEMM, gemm_flops(M, C, C),
            gemm_dgrad(m, (int)M, C, C, m->dres, pw(m, P_APW, (size_t)l * C * C), m->datty, nullptr));
@@ -577,7 +605,7 @@ extern "C" int gpt2_backward(gpt2_t* m) {
            layernorm_backward(m->at, m->dres, pf(m, g, P_LN1W) + l * C, pf(m, g, P_LN1B) + l * C,
                               l > 0 ? pf(m, g, P_FPB) + (size_t)(l - 1) * C : nullptr,  // d res_out(l-1)
                               m->dln, res_in, pf(m, m->params, P_LN1W) + l * C,
-                              m->ln1_mean + l * M, m->ln1_rstd + l * M, (int)M, C, m->ln_part, m->cs_part, s));
+                              m->ln1_mean + l * M, m->ln1_rstd + l * M, (int)M, C, m->ln_part, m->cs_part, m->nk, s));
     }
     OP(GPT2_K_ENCODER, actMC + 4.0 * m->maxT * C,
        encoder_backward_wpe(m->at, pf(m, g, P_WPE), m->dres, B, T, C, m->maxT, s));
@@ -691,5 +719,241 @@ extern "C" int gpt2_get_ids(gpt2_t* m, int32_t* tok, int32_t* tgt, size_t n) {
     CK(cudaMemcpyAsync(tok, m->tok, n * 4, cudaMemcpyDeviceToHost, m->stream));
     if (tgt) CK(cudaMemcpyAsync(tgt, m->tgt, n * 4, cudaMemcpyDeviceToHost, m->stream));
     CK(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
+// ------------------------------------------------------------------ generation
+// picoGPT "generate" with a key/value cache: the prompt runs as one extend step over
+// positions 0..T0-1, every further token as an extend of one position; each step ends
+// with the LM head on the last position of every sequence and the choice of the next id.
+static int alloc_gen(gpt2* m, int B) {
+    if (m->g_step) {
+        cudaGraphExecDestroy(m->g_step);
+        m->g_step = nullptr;
+    }
+    if (m->garena) {
+        cudaFree(m->garena);
+        m->garena = nullptr;
+        m->gB = 0;
+    }
+    if (!m->g_stream) {
+        CK(cudaStreamCreateWithFlags(&m->g_stream, cudaStreamNonBlocking));
+        CK(cudaEventCreateWithFlags(&m->g_ev, cudaEventDisableTiming));
+    }
+    const size_t R = (size_t)B * m->maxT, C = m->C, L = m->L, es = m->esz;
+    struct Item { void** slot; size_t bytes; };
+    void *kv, *x, *x2, *ln, *qkv, *atty, *fch, *fchg, *last, *lnl, *logits, *mean, *rstd, *coins, *ids, *out, *flags,
+        *ws, *state;
+    // split-K partials of the one-token steps' products (B rows)
+    size_t wsb = 256;
+    const size_t shapes[][2] = {{3 * C, C}, {C, C}, {4 * C, C}, {C, 4 * C}, {(size_t)m->Vp, C}};
+    for (auto& sh : shapes) wsb = std::max(wsb, gemm_tc_skinny_workspace_bytes(B, (int)sh[0], (int)sh[1]));
+    Item items[] = {
+        {&kv, L * R * 2 * C * es}, {&x, R * C * es}, {&x2, R * C * es}, {&ln, R * C * es}, {&qkv, R * 3 * C * es},
+        {&atty, R * C * es}, {&fch, R * 4 * C * es}, {&fchg, R * 4 * C * es}, {&last, (size_t)B * C * es},
+        {&lnl, (size_t)B * C * es}, {&logits, (size_t)B * m->Vp * es}, {&mean, R * 4}, {&rstd, R * 4},
+        {&coins, (size_t)B * (m->maxT + 1) * 4}, {&ids, R * 4}, {&out, (size_t)B * (m->maxT + 1) * 4},
+        {&flags, 64}, {&ws, wsb}, {&state, 64},
+    };
+    size_t total = 0;
+    for (auto& it : items) total += align256(it.bytes);
+    void* base = nullptr;
+    cudaError_t e = cudaMalloc(&base, total);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(m, e == cudaErrorMemoryAllocation ? GPT2_ERR_OOM : GPT2_ERR_CUDA,
+                    "generation arena of %zu bytes: %s", total, cudaGetErrorString(e));
+    }
+    char* p = (char*)base;
+    for (auto& it : items) {
+        *it.slot = p;
+        p += align256(it.bytes);
+    }
+    m->garena = base;
+    m->gbytes = total;
+    m->gB = B;
+    m->g_kv = (char*)kv; m->g_x = (char*)x; m->g_x2 = (char*)x2; m->g_ln = (char*)ln; m->g_qkv = (char*)qkv;
+    m->g_atty = (char*)atty; m->g_fch = (char*)fch; m->g_fchg = (char*)fchg; m->g_last = (char*)last;
+    m->g_lnl = (char*)lnl; m->g_logits = (char*)logits;
+    m->g_mean = (float*)mean; m->g_rstd = (float*)rstd; m->g_coins = (float*)coins;
+    m->g_ids = (int32_t*)ids; m->g_out = (int32_t*)out; m->g_flags = (int*)flags;
+    m->g_ws = (float*)ws; m->g_ws_bytes = wsb;
+    m->g_state = (int*)state;
+    return GPT2_OK;
+}
+
+// Y[M,N] = X[M,K] . W[N,K]^T (+bias) (+R) (GELU epilogue with Y2), timeouts into the
+// generation flags.  Products of at most one 128-row tile (the one-token steps) split K
+// over the SMs and apply their epilogue in the fixed-order reduce.
+static cudaError_t gen_gemm(gpt2* m, int M, int N, int K, const void* X, const void* W, const float* bias, void* Y,
+                            const void* R, void* Y2, cudaStream_t s) {
+    GemmArgs a{};
+    a.M = M; a.N = N; a.K = K; a.in_type = m->at;
+    a.A = X; a.sAm = K; a.sAk = 1;
+    a.B = W; a.sBn = K; a.sBk = 1;
+    a.D = Y; a.ldd = N; a.d_f32 = 0;
+    a.bias = bias; a.R = R; a.ldr = N;
+    a.D2 = Y2; a.ldd2 = N;
+    a.epi = Y2 ? EPI_GELU : EPI_STORE;
+    a.flags = m->g_flags;
+    a.skinny_split = 1;
+    return gemm_dispatch(a, m->g_ws, m->g_ws_bytes, s);
+}
+
+// Forward of positions t0..t0+n-1 of the gB sequences (ids already in g_ids); leaves
+// the logits of each sequence's last new position in g_logits.  dstate: the position
+// comes from device memory instead (one-token steps, n = 1).
+static int gen_extend(gpt2* m, int t0, int n, const int* dstate, cudaStream_t s) {
+    const int B = m->gB, L = m->L, C = m->C, NH = m->NH, maxT = m->maxT;
+    const int rows = B * n;
+    float* P = m->params;
+    CK(gen_embed(m->at, m->g_x, m->g_ids, pw(m, P_WTE, 0), pw(m, P_WPE, 0), B, n, t0, maxT, C, dstate, s));
+    for (int l = 0; l < L; l++) {
+        char* kv = act(m, m->g_kv, (size_t)l * B * maxT * 2 * C);
+        CK(layernorm_forward(m->at, m->g_ln, m->g_mean, m->g_rstd, m->g_x, pf(m, P, P_LN1W) + l * C,
+                             pf(m, P, P_LN1B) + l * C, rows, C, m->nk, s));
+        CK(gen_gemm(m, rows, 3 * C, C, m->g_ln, pw(m, P_QKVW, (size_t)l * 3 * C * C), pf(m, P, P_QKVB) + l * 3 * C,
+                    m->g_qkv, nullptr, nullptr, s));
+        CK(gen_kv_append(m->at, kv, m->g_qkv, B, n, t0, maxT, C, dstate, s));
+        CK(gen_attention(m->at, m->g_atty, m->g_qkv, kv, B, n, t0, maxT, C, NH, dstate, s));
+        CK(gen_gemm(m, rows, C, C, m->g_atty, pw(m, P_APW, (size_t)l * C * C), pf(m, P, P_APB) + l * C, m->g_x2,
+                    m->g_x, nullptr, s));
+        CK(layernorm_forward(m->at, m->g_ln, m->g_mean, m->g_rstd, m->g_x2, pf(m, P, P_LN2W) + l * C,
+                             pf(m, P, P_LN2B) + l * C, rows, C, m->nk, s));
+        CK(gen_gemm(m, rows, 4 * C, C, m->g_ln, pw(m, P_FCW, (size_t)l * 4 * C * C), pf(m, P, P_FCB) + l * 4 * C,
+                    m->g_fch, nullptr, m->g_fchg, s));
+        CK(gen_gemm(m, rows, C, 4 * C, m->g_fchg, pw(m, P_FPW, (size_t)l * 4 * C * C), pf(m, P, P_FPB) + l * C,
+                    m->g_x, m->g_x2, nullptr, s));
+    }
+    CK(gen_last_rows(m->at, m->g_last, m->g_x, B, n, C, s));
+    CK(layernorm_forward(m->at, m->g_lnl, m->g_mean, m->g_rstd, m->g_last, pf(m, P, P_LNFW), pf(m, P, P_LNFB), B, C,
+                         m->nk, s));
+    CK(gen_gemm(m, B, m->Vp, C, m->g_lnl, pw(m, P_WTE, 0), nullptr, m->g_logits, nullptr, nullptr, s));
+    return GPT2_OK;
+}
+
+// One one-token step with its position in g_state: extend, choose, advance.
+static int gen_token_step(gpt2* m, cudaStream_t s) {
+    int rc = gen_extend(m, 0, 1, m->g_state, s);
+    if (rc) return rc;
+    CK(gen_sample(m->at, m->g_ids, m->g_out, m->g_logits, m->gB, m->V, m->Vp, 0.f, m->g_coins, 0, 0, 0, m->maxT,
+                  m->g_state, s));
+    CK(gen_advance(m->g_state, s));
+    return GPT2_OK;
+}
+
+// Capture one one-token step into a CUDA graph (kept until the arena changes).
+static int gen_capture(gpt2* m) {
+    cudaStream_t s = m->g_stream;
+    const uint64_t l0 = launches_total();
+    CK(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+    int rc = gen_token_step(m, s);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(s, &graph);
+    if (rc) {
+        if (graph) cudaGraphDestroy(graph);
+        return rc;
+    }
+    CK(e);
+    e = cudaGraphInstantiate(&m->g_step, graph, 0);
+    cudaGraphDestroy(graph);
+    CK(e);
+    m->g_step_launches = (unsigned)(launches_total() - l0);
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_generate(gpt2_t* m, const int32_t* prompt, int B, int T0, int n_new, float temperature,
+                             const float* coins, int32_t* out) {
+    if (!m || !prompt || !out) return fail(m, GPT2_ERR_ARG, "null argument");
+    if (B <= 0 || T0 <= 0 || n_new < 0) return fail(m, GPT2_ERR_ARG, "need B > 0, T0 > 0, n_new >= 0");
+    if (!(temperature == temperature)) return fail(m, GPT2_ERR_ARG, "temperature is NaN");
+    if ((long long)T0 + n_new - 1 > m->maxT)
+        return fail(m, GPT2_ERR_SHAPE, "T0 + n_new - 1 = %lld exceeds maxT = %d", (long long)T0 + n_new - 1,
+                    m->maxT);
+    if (gen_attn_smem_bytes(m->C, m->NH, m->maxT) > 227 * 1024)
+        return fail(m, GPT2_ERR_SHAPE, "maxT = %d is too long for the cached attention", m->maxT);
+    for (size_t i = 0; i < (size_t)B * T0; i++)
+        if (prompt[i] < 0 || prompt[i] >= m->V) return fail(m, GPT2_ERR_TOKEN, "prompt id %d outside [0, V)", prompt[i]);
+    if (temperature > 0.f) {
+        if (!coins) return fail(m, GPT2_ERR_ARG, "sampling (temperature > 0) needs coins");
+        for (size_t i = 0; i < (size_t)B * n_new; i++)
+            if (!(coins[i] >= 0.f && coins[i] < 1.f)) return fail(m, GPT2_ERR_ARG, "coins must lie in [0, 1)");
+    }
+    if (n_new == 0) return GPT2_OK;
+    if (!m->garena || m->gB != B) {
+        int rc = alloc_gen(m, B);
+        if (rc) return rc;
+    }
+    const int maxT = m->maxT;
+    cudaStream_t s = m->g_stream;
+    m->gen_logits_valid = false;
+    // after the work already queued on the handle's stream
+    CK(cudaEventRecord(m->g_ev, m->stream));
+    CK(cudaStreamWaitEvent(s, m->g_ev, 0));
+    CK(cudaMemsetAsync(m->g_flags, 0, 64, s));
+    CK(cudaMemcpy2DAsync(m->g_ids, (size_t)maxT * 4, prompt, (size_t)T0 * 4, (size_t)T0 * 4, B,
+                         cudaMemcpyHostToDevice, s));
+    if (temperature > 0.f)
+        CK(cudaMemcpyAsync(m->g_coins, coins, (size_t)B * n_new * 4, cudaMemcpyHostToDevice, s));
+    // the prompt: all T0 positions at once, then the first new id
+    int rc = gen_extend(m, 0, T0, nullptr, s);
+    if (rc) return rc;
+    CK(gen_sample(m->at, m->g_ids, m->g_out, m->g_logits, B, m->V, m->Vp, temperature, m->g_coins, 0, n_new, T0, maxT,
+                  nullptr, s));
+    if (n_new > 1) {
+        float tbits = temperature;
+        int st[4] = {T0, 1, n_new, 0};
+        memcpy(&st[3], &tbits, 4);
+        CK(cudaMemcpyAsync(m->g_state, st, sizeof st, cudaMemcpyHostToDevice, s));
+        CK(cudaStreamSynchronize(s));  // st leaves scope; also keeps capture off a busy stream
+        int step = 1;
+        if (!m->g_step) {
+            // first time for this arena: one step launched directly (sets every kernel's
+            // attributes), then the step captured for the rest
+            rc = gen_token_step(m, s);
+            if (rc) return rc;
+            step++;
+            if (step < n_new) {
+                rc = gen_capture(m);
+                if (rc) return rc;
+            }
+        }
+        for (; step < n_new; step++) {
+            CK(cudaGraphLaunch(m->g_step, s));
+            count_launches(m->g_step_launches);
+        }
+    }
+    int hflags[2] = {0, 0};
+    CK(cudaMemcpyAsync(out, m->g_out, (size_t)B * n_new * 4, cudaMemcpyDeviceToHost, s));
+    CK(cudaMemcpyAsync(hflags, m->g_flags, 4, cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    if (hflags[0] & G2_FLAG_TIMEOUT)
+        return fail(m, GPT2_ERR_TIMEOUT, "a device-side wait gave up (kernel reported a timeout)");
+    m->gen_logits_valid = true;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_get_gen_logits(gpt2_t* m, float* host, size_t n) {
+    if (!m || !host) return fail(m, GPT2_ERR_ARG, "null argument");
+    if (!m->garena || !m->gen_logits_valid) return fail(m, GPT2_ERR_STATE, "no generation has run");
+    const size_t B = m->gB;
+    if (n != B * m->V) return fail(m, GPT2_ERR_ARG, "expected %zu values", B * m->V);
+    if (m->at == ACT_F32) {
+        CK(cudaMemcpy2DAsync(host, (size_t)m->V * 4, m->g_logits, (size_t)m->Vp * 4, (size_t)m->V * 4, B,
+                             cudaMemcpyDeviceToHost, m->g_stream));
+        CK(cudaStreamSynchronize(m->g_stream));
+        return GPT2_OK;
+    }
+    std::string stage(B * m->Vp * 2, '\0');
+    CK(cudaMemcpyAsync(&stage[0], m->g_logits, B * m->Vp * 2, cudaMemcpyDeviceToHost, m->g_stream));
+    CK(cudaStreamSynchronize(m->g_stream));
+    const uint16_t* src = (const uint16_t*)stage.data();
+    for (size_t r = 0; r < B; r++)
+        for (int c = 0; c < m->V; c++) {
+            uint32_t bits = (uint32_t)src[r * m->Vp + c] << 16;
+            float f;
+            memcpy(&f, &bits, 4);
+            host[r * m->V + c] = f;
+        }
     return GPT2_OK;
 }

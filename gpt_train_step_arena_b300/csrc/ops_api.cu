@@ -149,12 +149,28 @@ extern "C" int gpt2_op_layernorm_forward(int dtype, void* out, float* mean, floa
     if (M < 0 || C <= 0) return op_fail(GPT2_ERR_ARG, "layernorm: bad shape M=%d C=%d", M, C);
     if (M == 0) return GPT2_OK;
     if (!out || !mean || !rstd || !inp || !w || !b) return op_fail(GPT2_ERR_ARG, "layernorm: null pointer");
-    return op_cuda(layernorm_forward(act_of(dtype), out, mean, rstd, inp, w, b, M, C, (cudaStream_t)stream),
+    return op_cuda(layernorm_forward(act_of(dtype), out, mean, rstd, inp, w, b, M, C, NORM_LAYER,
+                                     (cudaStream_t)stream),
                    "layernorm_forward");
+}
+
+extern "C" int gpt2_op_rmsnorm_forward(int dtype, void* out, float* rstd, const void* inp, const float* w, int M,
+                                       int C, void* stream) {
+    if (!dtype_ok(dtype)) return op_fail(GPT2_ERR_ARG, "rmsnorm: bad dtype %d", dtype);
+    if (M < 0 || C <= 0) return op_fail(GPT2_ERR_ARG, "rmsnorm: bad shape M=%d C=%d", M, C);
+    if (M == 0) return GPT2_OK;
+    if (!out || !rstd || !inp || !w) return op_fail(GPT2_ERR_ARG, "rmsnorm: null pointer");
+    return op_cuda(layernorm_forward(act_of(dtype), out, nullptr, rstd, inp, w, nullptr, M, C, NORM_RMS,
+                                     (cudaStream_t)stream),
+                   "rmsnorm_forward");
 }
 
 extern "C" size_t gpt2_op_layernorm_backward_workspace(int C) {
     return C > 0 ? ln_bwd_partial_floats(C) * sizeof(float) : 0;
+}
+
+extern "C" size_t gpt2_op_rmsnorm_backward_workspace(int C) {
+    return C > 0 ? (ln_bwd_partial_floats(C) + (size_t)C) * sizeof(float) : 0;
 }
 
 extern "C" int gpt2_op_layernorm_backward(int dtype, void* dinp, float* dw, float* db, const void* dout,
@@ -170,8 +186,27 @@ extern "C" int gpt2_op_layernorm_backward(int dtype, void* dinp, float* dw, floa
         return op_fail(GPT2_ERR_ARG, "layernorm_backward: workspace of %zu bytes needed, %zu given", need,
                        workspace_bytes);
     return op_cuda(layernorm_backward(act_of(dtype), dinp, dw, db, nullptr, dout, inp, w, mean, rstd, M, C,
-                                      (float*)workspace, nullptr, (cudaStream_t)stream),
+                                      (float*)workspace, nullptr, NORM_LAYER, (cudaStream_t)stream),
                    "layernorm_backward");
+}
+
+extern "C" int gpt2_op_rmsnorm_backward(int dtype, void* dinp, float* dw, const void* dout, const void* inp,
+                                        const float* w, const float* rstd, int M, int C, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    if (!dtype_ok(dtype)) return op_fail(GPT2_ERR_ARG, "rmsnorm_backward: bad dtype %d", dtype);
+    if (M < 0 || C <= 0) return op_fail(GPT2_ERR_ARG, "rmsnorm_backward: bad shape M=%d C=%d", M, C);
+    if (!dw || !w || (M > 0 && (!dinp || !dout || !inp || !rstd)))
+        return op_fail(GPT2_ERR_ARG, "rmsnorm_backward: null pointer");
+    // the shift's sums (all 0 for RMSNorm) land in the workspace tail, after the partials
+    size_t need = gpt2_op_rmsnorm_backward_workspace(C);
+    if (!workspace || workspace_bytes < need)
+        return op_fail(GPT2_ERR_ARG, "rmsnorm_backward: workspace of %zu bytes needed, %zu given", need,
+                       workspace_bytes);
+    float* part = (float*)workspace;
+    float* db_sink = part + ln_bwd_partial_floats(C);
+    return op_cuda(layernorm_backward(act_of(dtype), dinp, dw, db_sink, nullptr, dout, inp, w, nullptr, rstd, M, C,
+                                      part, nullptr, NORM_RMS, (cudaStream_t)stream),
+                   "rmsnorm_backward");
 }
 
 extern "C" int gpt2_op_softmax_xent(int dtype, void* logits, float* losses, const int32_t* targets, int M,

@@ -27,16 +27,21 @@ def _ptr(a):
 
 
 class GPT2:
-    """One model on the current CUDA device (gpt2_build_ex)."""
+    """One model on the current CUDA device (gpt2_build_norm).
 
-    def __init__(self, L: int, C: int, H: int, V: int, maxT: int, precision: str = "bf16"):
+    norm: "layernorm" (GPT-2) or "rmsnorm" (the microGPT variant)."""
+
+    def __init__(self, L: int, C: int, H: int, V: int, maxT: int, precision: str = "bf16",
+                 norm: str = "layernorm"):
         prec = {"bf16": N.GPT2_BF16, "fp32": N.GPT2_FP32}[precision]
+        nk = {"layernorm": N.GPT2_LAYERNORM, "rmsnorm": N.GPT2_RMSNORM}[norm]
         st = ct.c_int(0)
-        h = N.lib.gpt2_build_ex(L, C, H, V, maxT, prec, ct.byref(st))
+        h = N.lib.gpt2_build_norm(L, C, H, V, maxT, prec, nk, ct.byref(st))
         if not h:
             raise GPT2Error(st.value, N.lib.gpt2_last_build_error().decode())
         self.h = h
         self.L, self.C, self.H, self.V, self.maxT, self.precision = L, C, H, V, maxT, precision
+        self.norm = norm
         self.n = N.lib.gpt2_num_params(h)
         self.Vp = N.lib.gpt2_padded_vocab(h)
 
@@ -117,6 +122,24 @@ class GPT2:
     def logits(self, B: int, T: int) -> np.ndarray:
         out = np.empty((B, T, self.V), np.float32)
         self._check(N.lib.gpt2_get_logits(self.h, _ptr(out), out.size))
+        return out
+
+    # -- generation
+    def generate(self, prompt, n_new: int, temperature: float = 0.0, coins=None) -> np.ndarray:
+        """(B, n_new) new ids after the (B, T0) int32 prompt: greedy when temperature <= 0,
+        else sampled with the caller's coins (B, n_new) in [0, 1)."""
+        prompt = np.ascontiguousarray(prompt, np.int32)
+        B, T0 = prompt.shape
+        out = np.zeros((B, n_new), np.int32)
+        c = None if coins is None else np.ascontiguousarray(coins, np.float32).reshape(B, n_new)
+        self._check(N.lib.gpt2_generate(self.h, _ptr(prompt), B, T0, n_new, float(temperature),
+                                        None if c is None else _ptr(c), _ptr(out)))
+        return out
+
+    def gen_logits(self, B: int) -> np.ndarray:
+        """(B, V) logits of the last generation step."""
+        out = np.empty((B, self.V), np.float32)
+        self._check(N.lib.gpt2_get_gen_logits(self.h, _ptr(out), out.size))
         return out
 
     def ids(self, B: int, T: int):

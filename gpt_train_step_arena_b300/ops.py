@@ -103,6 +103,28 @@ def layernorm_backward(dinp: torch.Tensor, dout, x, w, mean, rstd):
     return dw, db
 
 
+def rmsnorm_forward(x: torch.Tensor, w: torch.Tensor):
+    """x (M,C) -> (out (M,C) like x, rstd (M) fp32): the microGPT RMSNorm."""
+    M, C = x.shape
+    out = torch.empty_like(x)
+    rstd = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(N.lib.gpt2_op_rmsnorm_forward(_dt(x), out.data_ptr(), rstd.data_ptr(), x.data_ptr(), w.data_ptr(),
+                                         M, C, _stream()))
+    return out, rstd
+
+
+def rmsnorm_backward(dinp: torch.Tensor, dout, x, w, rstd):
+    """dinp (M,C) is accumulated into in place; returns dw fp32 (C)."""
+    M, C = x.shape
+    dw = torch.empty(C, dtype=torch.float32, device=x.device)
+    ws_bytes = N.lib.gpt2_op_rmsnorm_backward_workspace(C)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    _check(N.lib.gpt2_op_rmsnorm_backward(_dt(x), dinp.data_ptr(), dw.data_ptr(), dout.data_ptr(), x.data_ptr(),
+                                          w.data_ptr(), rstd.data_ptr(), M, C, ws.data_ptr(), ws_bytes,
+                                          _stream()))
+    return dw
+
+
 def softmax_xent(logits: torch.Tensor, targets: torch.Tensor, V: int, dloss: float, check: bool = True):
     """logits (M,Vp) is overwritten with dlogits; returns the per-row losses (M) fp32."""
     M, Vp = logits.shape

@@ -73,6 +73,17 @@ enum gpt2_memory { GPT2_HOST = 0, GPT2_DEVICE = 1 };
 gpt2_t* gpt2_build_ex(int L, int C, int H, int V, int maxT, int precision, int* status);
 /* gpt2_build_ex(..., GPT2_BF16, NULL). */
 gpt2_t* gpt2_build(int L, int C, int H, int V, int maxT);
+
+/* Normalisation of the block.  GPT2_LAYERNORM: GPT-2's LayerNorm (llm.c §1.3, §1.4).
+ * GPT2_RMSNORM: the microGPT variant (page "microGPT 3D", lesson 04: embedding ->
+ * RMSNorm -> attention -> residual -> MLP -> residual -> logits): every LayerNorm
+ * (ln1, ln2, lnf) becomes out = x / sqrt(mean(x^2) + 1e-5) * w with the same gains w;
+ * the parameter layout is unchanged and the shift tensors (ln1b, ln2b, lnfb) are
+ * carried but unused, so their gradients are 0. */
+enum gpt2_norm { GPT2_LAYERNORM = 0, GPT2_RMSNORM = 1 };
+/* gpt2_build_ex with a choice of normalisation; GPT2_ERR_ARG for another norm value.
+ * gpt2_build_ex(...) = gpt2_build_norm(..., GPT2_LAYERNORM, status). */
+gpt2_t* gpt2_build_norm(int L, int C, int H, int V, int maxT, int precision, int norm, int* status);
 /* Release everything the handle owns (llm.c §1.27).  NULL is accepted. */
 void gpt2_free(gpt2_t* m);
 
@@ -128,6 +139,25 @@ int gpt2_get_losses(gpt2_t* m, float* host, size_t n);
  * turned into the loss gradient in place). */
 int gpt2_get_logits(gpt2_t* m, float* host, size_t n);
 
+/* Autoregressive generation (picoGPT's "generate" decode loop; llm.c §1.35
+ * sample_mult), with a key/value cache: the prompt's positions run through the model
+ * once, then each new token only its own position, attending over the cached keys
+ * and values of all earlier positions.  prompt: B*T0 host int32 ids (row-major
+ * (B,T0), each in [0,V)); out: B*n_new host int32, receives the new ids (B,n_new).
+ * temperature <= 0: greedy, the argmax of the last position's logits (the first
+ * index among equal maxima); temperature > 0: the first id whose cumulative
+ * softmax(logits / temperature) exceeds coins[b*n_new + step] (B*n_new host floats
+ * in [0,1), drawn by the caller; NULL allowed when greedy).  Requires
+ * T0 + n_new - 1 <= maxT (GPT2_ERR_SHAPE).  The first call for a batch size B
+ * allocates the cache and working buffers for (B, maxT) in a separate device arena
+ * (kept until gpt2_free or a call with another B); training buffers are untouched.
+ * Stream-ordered on the handle's stream; synchronises once at the end. */
+int gpt2_generate(gpt2_t* m, const int32_t* prompt, int B, int T0, int n_new, float temperature,
+                  const float* coins, int32_t* out);
+/* Logits (B,V) fp32 (real columns) from which the last gpt2_generate chose its last
+ * ids; n = B*V.  GPT2_ERR_STATE before any generation.  Synchronising. */
+int gpt2_get_gen_logits(gpt2_t* m, float* host, size_t n);
+
 /* The device copies of the last forward's token ids and targets (B*T each; targets
  * may be NULL).  Synchronising. */
 int gpt2_get_ids(gpt2_t* m, int32_t* tokens_host, int32_t* targets_host, size_t n);
@@ -164,7 +194,7 @@ const char* gpt2_last_error(const gpt2_t* m);
 const char* gpt2_last_build_error(void);
 /* Number of kernel launches the handle has queued since it was built. */
 uint64_t gpt2_kernel_launches(const gpt2_t* m);
-/* Device bytes held by the handle (parameter arena + activation arena). */
+/* Device bytes held by the handle (parameter, activation and generation arenas). */
 size_t gpt2_device_bytes(const gpt2_t* m);
 
 #ifdef __cplusplus

@@ -121,6 +121,24 @@ int gpt2_op_layernorm_backward(int dtype, void* dinp, float* dw, float* db, cons
                                const float* rstd, int M, int C, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/* RMSNorm forward, the normalisation of the microGPT block (page "microGPT 3D",
+ * lesson 04; the page names the operation only, this is its standard definition with
+ * LayerNorm's eps and gain and no shift): for each of the M rows of inp (M,C) of
+ * `dtype`, out = x * rstd * w with rstd = 1/sqrt(mean(x^2) + 1e-5).  out (M,C) `dtype`
+ * is overwritten; rstd (M floats) receives the row statistic; w is C floats.  M may
+ * be 0. */
+int gpt2_op_rmsnorm_forward(int dtype, void* out, float* rstd, const void* inp, const float* w, int M,
+                            int C, void* stream);
+
+/* Its backward: with n = x * rstd and g = w * dout, dinp += (g - n * mean(g * n)) * rstd
+ * (ACCUMULATED, like gpt2_op_layernorm_backward) and dw (C floats) is OVERWRITTEN with
+ * sum over rows of n * dout in a fixed order.  rstd is the forward's statistic.
+ * workspace must hold gpt2_op_rmsnorm_backward_workspace(C) bytes. */
+size_t gpt2_op_rmsnorm_backward_workspace(int C);
+int gpt2_op_rmsnorm_backward(int dtype, void* dinp, float* dw, const void* dout, const void* inp,
+                             const float* w, const float* rstd, int M, int C, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 /* Fused softmax + cross-entropy forward and backward (llm.c §1.13 softmax_forward,
  * §1.14 crossentropy_forward, §1.15 crossentropy_softmax_backward; picoGPT lm_loss).
  * logits (M,Vp) of `dtype` with V <= Vp real columns: for each row, lse = logsumexp of

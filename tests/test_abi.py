@@ -48,3 +48,17 @@ def test_product_path_does_not_reference_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not re.search(r"^\s*(import|from)\s+oracle|liboracle|gpt2_oracle", text, re.M), f
+
+
+def test_build_rejects_bad_arguments_before_touching_the_device():
+    """Argument checks of gpt2_build_norm run on the host: no CUDA call is made, so this
+    needs no GPU."""
+    import ctypes as ct
+    from gpt_train_step_arena_b300 import _native as N
+    st = ct.c_int(0)
+    assert not N.lib.gpt2_build_norm(1, 16, 4, 27, 16, N.GPT2_FP32, 7, ct.byref(st))   # unknown norm
+    assert st.value == N.GPT2_ERR_ARG and b"norm" in N.lib.gpt2_last_build_error()
+    assert not N.lib.gpt2_build_norm(1, 16, 5, 27, 16, N.GPT2_FP32, N.GPT2_RMSNORM, ct.byref(st))  # C % H
+    assert st.value == N.GPT2_ERR_ARG
+    assert not N.lib.gpt2_build_ex(1, 16, 4, 27, 16, 1, ct.byref(st))                 # unknown precision
+    assert st.value == N.GPT2_ERR_ARG

@@ -185,6 +185,40 @@ def test_layernorm_fwd_bwd(torch_cuda, M, C, dt):
     assert torch.equal(dw, dw2) and torch.equal(db, db2)  # fixed summation order
 
 
+# ---------------------------------------------------------------- RMSNorm (microGPT variant)
+@pytest.mark.parametrize("M,C", [(1000, 768), (37, 768), (300, 100), (1, 256), (513, 1024), (0, 768),
+                                 (20000, 768), (5003, 512)])
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+def test_rmsnorm_fwd_bwd(torch_cuda, M, C, dt):
+    torch = torch_cuda
+    from gpt_train_step_arena_b300 import ops
+    rng = np.random.default_rng(M * 13 + C)
+    x = (rng.normal(size=(M, C)) * 2 + 0.5).astype(np.float32)   # non-zero mean: not a LayerNorm
+    w = (1 + 0.1 * rng.normal(size=C)).astype(np.float32)
+    dy = rng.normal(size=(M, C)).astype(np.float32)
+    acc = rng.normal(size=(M, C)).astype(np.float32)
+    tdt = torch.float32 if dt == "fp32" else torch.bfloat16
+    xd, dyd, accd = _to(torch, x, tdt), _to(torch, dy, tdt), _to(torch, acc, tdt)
+    wd = _to(torch, w, torch.float32)
+    out, rstd = ops.rmsnorm_forward(xd, wd)
+    acc_before = _np(accd)
+    dw = ops.rmsnorm_backward(accd, dyd, xd, wd, rstd)
+    torch.cuda.synchronize()
+    if M == 0:
+        assert np.all(_np(dw) == 0)
+        return
+    x_eff, dy_eff = _np(xd), _np(dyd)
+    r_out, r_rstd = o64.rmsnorm(x_eff, w)
+    r_dx, r_dw = o64.rmsnorm_backward(dy_eff, x_eff, w, r_rstd)
+    assert np.max(np.abs(_np(rstd) / r_rstd - 1)) <= 1e-5
+    tol = 1e-5 if dt == "fp32" else 4e-3
+    assert _rel(_np(out), r_out) <= tol
+    assert _rel(_np(accd) - acc_before, r_dx) <= (1e-5 if dt == "fp32" else 8e-3)
+    assert _rel(_np(dw), r_dw) <= 1e-5
+    dw2 = ops.rmsnorm_backward(_to(torch, acc, tdt), dyd, xd, wd, rstd)
+    assert torch.equal(dw, dw2)  # fixed summation order
+
+
 # ---------------------------------------------------------------- softmax + cross-entropy
 @pytest.mark.parametrize("M,V,Vp", [(64, 50257, 50304), (300, 27, 32), (129, 1000, 1000), (5, 1, 8),
                                     (40, 4101, 4104), (3, 9000, 9001)])

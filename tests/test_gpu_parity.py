@@ -20,7 +20,7 @@ def G():
     return GPT2
 
 
-def _run_one_step(G, name, precision, B=None, T=None, seed=42, variant="f64"):
+def _run_one_step(G, name, precision, B=None, T=None, seed=42, variant="f64", norm="layernorm"):
     c = synth.WORKLOADS[name]
     L, C, NH, V, maxT = cfg_shape(name)
     B = B or c["B"]
@@ -32,7 +32,7 @@ def _run_one_step(G, name, precision, B=None, T=None, seed=42, variant="f64"):
     inp, tgt = synth.batch(stream, 0, B, T)
     hp = (c["lr"], c["b1"], c["b2"], c["eps"], c["wd"])
 
-    o = Oracle(L, C, NH, V, maxT, variant=variant)
+    o = Oracle(L, C, NH, V, maxT, variant=variant, norm=norm)
     o.set_params(params)
     o.forward(inp)
     ref_logits = o.logits().copy()
@@ -44,12 +44,12 @@ def _run_one_step(G, name, precision, B=None, T=None, seed=42, variant="f64"):
     ref_params = o.params().copy()
 
     # a fresh handle per pass so the logits of a forward without targets are kept
-    g = G(L, C, NH, V, maxT, precision=precision)
+    g = G(L, C, NH, V, maxT, precision=precision, norm=norm)
     g.set_params(params)
     assert g.forward(inp) == -1.0
     logits = g.logits(B, T)
     g.close()
-    g = G(L, C, NH, V, maxT, precision=precision)
+    g = G(L, C, NH, V, maxT, precision=precision, norm=norm)
     g.set_params(params)
     loss = g.forward(inp, tgt)
     tok_back, tgt_back = g.ids(B, T)
@@ -250,3 +250,33 @@ def test_error_paths_never_fault(G):
         g.forward(np.zeros((1, 9), np.int32))              # T > maxT
     assert e.value.code == N.GPT2_ERR_SHAPE
     g.close()
+
+
+# ---------------------------------------------------------------- microGPT variant (RMSNorm)
+@pytest.mark.parametrize("precision", ["fp32", "bf16"])
+def test_rmsnorm_variant_tiny_one_step(G, precision):
+    r = _run_one_step(G, "tiny", precision, norm="rmsnorm")
+    tol = TOL[precision]
+    L, C, V, maxT = r["shape"]
+    assert abs(r["loss"] - r["ref_loss"]) <= tol["loss"] * abs(r["ref_loss"]), (r["loss"], r["ref_loss"])
+    if tol["logits"]:
+        assert rel_l2(r["logits"], r["ref_logits"]) <= tol["logits"]
+    assert_grads_close(r["grads"], r["ref_grads"], L, C, V, maxT, tol["grads"])
+    # the shift tensors are unused: their gradients are exactly zero on the device too
+    sizes = synth.param_sizes(L, C, V, maxT)
+    for name, gpart in zip(synth.PARAM_NAMES, np.split(r["grads"], np.cumsum(sizes)[:-1])):
+        if name in ("ln1b", "ln2b", "lnfb"):
+            assert not gpart.any(), name
+
+
+@pytest.mark.parametrize("precision", ["fp32", "bf16"])
+def test_rmsnorm_variant_gpt2_124m_small(G, precision):
+    """124M shapes at B=4, T=64 with RMSNorm, against the double oracle's RMSNorm model."""
+    r = _run_one_step(G, "gpt2_124m_small", precision, norm="rmsnorm")
+    L, C, V, maxT = r["shape"]
+    tol = TOL[precision]
+    assert abs(r["loss"] - r["ref_loss"]) <= tol["loss"] * r["ref_loss"]
+    if tol["logits"]:
+        assert rel_l2(r["logits"], r["ref_logits"]) <= tol["logits"]
+    assert_grads_close(r["grads"], r["ref_grads"], L, C, V, maxT, tol["grads"])
+
