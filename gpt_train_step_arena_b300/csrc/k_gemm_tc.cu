@@ -71,13 +71,24 @@ struct Params {
 template <int BN, int BMT, int EPI>
 struct Cfg {
     static constexpr int HALVES = BMT / BM;                 // 128-row accumulator halves per tile
-    static constexpr int EPI_WARPS = 4 * HALVES;            // one per 32-lane quarter per half
+    // The GELU' epilogue (FC-projection input gradient) is latency-bound with one epilogue
+    // warp per SM sub-partition: on 128-row tiles it gets two warps per 32-lane quarter,
+    // each draining half of the tile's columns, with one staged-input buffer each so the
+    // pipeline keeps three stages (measured: 186 -> 162 us per layer at B=32, T=1024;
+    // two input buffers and two stages: 189 us).  The residual epilogue gains nothing.
+    static constexpr int COLSPLIT = (HALVES == 1 && EPI == E_GELU_BWD) ? 2 : 1;
+    static constexpr int EPI_WARPS = 4 * HALVES * COLSPLIT;  // per 32-lane quarter, per half, per column part
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;     // + TMA warp + MMA warp
+    static constexpr int NIN = COLSPLIT == 2 ? 1 : 2;       // staged-input buffers per warp
     static constexpr int A_BYTES = BMT * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     // each epilogue warp stages 32 rows x 128 bytes per output for the TMA store
-    static constexpr int EPI_WARP_BYTES = (EpiOut<EPI>::NOUT + (EpiOut<EPI>::IN ? 2 : 0)) * 4096;
+    // output staging: two sets on 128-row tiles (a chunk's stores need not have finished
+    // reading before the next chunk is staged), one set on 256-row tiles (their 8
+    // epilogue warps would otherwise take the shared memory of a pipeline stage)
+    static constexpr int STG_BUFS = (HALVES == 1 && COLSPLIT == 1) ? 2 : 1;
+    static constexpr int EPI_WARP_BYTES = (EpiOut<EPI>::NOUT * STG_BUFS + (EpiOut<EPI>::IN ? NIN : 0)) * 4096;
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
     static constexpr int SMEM_LIMIT = 227 * 1024 - 1024 /*align*/ - 512 /*barriers*/;
     static constexpr int STAGES_FIT = (SMEM_LIMIT - EPI_BYTES) / STAGE_BYTES;
@@ -351,55 +362,101 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
         }
     } else {
         // ---------------- epilogue warps: warps 2-5 drain the first 128-row half of the tile,
-        // warps 6-9 (256-row tiles) the second; each warp its 32-lane quarter, all BN columns
+        // warps 6-9 the second (256-row tiles) or the second half of the columns (split
+        // columns); each warp its 32-lane quarter
+        const int ew = warp - 2;
         const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
-        const int hh = (warp - 2) >> 2;
+        const int hh = CF::COLSPLIT == 1 ? (ew >> 2) : 0;
+        const int col0 = CF::COLSPLIT == 1 ? 0 : (ew >> 2) * (BN / CF::COLSPLIT);  // first column of this warp
         const int row_in_tile = hh * BM + quarter * 32 + lane;
-        uint8_t* stg = epi_smem + (warp - 2) * CF::EPI_WARP_BYTES;  // this warp's staging
-        uint8_t* inb = stg + EO::NOUT * 4096;                       // its two input buffers
-        uint64_t* ibar = in_bar + 2 * (warp - 2);
+        uint8_t* stg0 = epi_smem + ew * CF::EPI_WARP_BYTES;            // this warp's staging sets
+        uint8_t* inb = stg0 + EO::NOUT * CF::STG_BUFS * 4096;          // its input buffers
+        int sbuf = 0;       // staging set of the next chunk
+        int newest_set = -1;  // (lane 0) set read by the most recently committed store group
+        uint64_t* ibar = in_bar + 2 * ew;
         uint32_t in_par = 0;  // bit b: parity of input buffer b's next completion
         int acc = 0;
         uint32_t acc_phase = 0;
+        // staged inputs: with NIN buffers, buffer b holds chunks b, b+NIN, ... of a tile; a
+        // chunk's load is issued NIN chunks ahead (the first NIN before the accumulator is ready)
+        constexpr int NIN = CF::NIN;
+        int pend = 0;  // bit b: a load into input buffer b is in flight, not yet consumed
+        auto issue_in = [&](int b, int gcol, int grow) {
+            if (lane == 0) {
+                mbar_expect_tx(&ibar[b], 4096);
+                tma_load_2d(&tmX, &ibar[b], inb + b * 4096, gcol, grow);
+            }
+            pend |= 1 << b;
+        };
+        auto drain_in = [&]() {  // let issued loads land before the warp leaves (bounded)
+            if (lane == 0) {
+                for (int b = 0; b < NIN; b++) {
+                    if (!((pend >> b) & 1)) continue;
+                    unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(&ibar[b], (in_par >> b) & 1) && globaltimer() - t0 < TIMEOUT_NS) {
+                    }
+                }
+            }
+            __syncwarp();
+        };
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
             int mb, nb, sp;
             unit_coords(p, u, mb, nb, sp);
-            bool ok = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.flags);
-            if (!__all_sync(0xffffffffu, ok)) break;  // the warp leaves together
-            tc_fence_after();
             const int gm = mb * BMT + row_in_tile;
             const int gm0 = gm - lane;  // first row of this warp's 32
-            const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * CF::ACC_COLS + hh * BN);
-            constexpr int NCH = BN / EO::CW;
-            if (EO::IN && lane == 0) {  // the first chunk's input
-                mbar_expect_tx(&ibar[0], 4096);
-                tma_load_2d(&tmX, &ibar[0], inb, nb * BN, gm0);
+            constexpr int NCH = BN / EO::CW / CF::COLSPLIT;  // chunks of this warp
+            if (EO::IN) {
+                __syncwarp();  // the input buffers were read by the previous tile's chunks
+#pragma unroll
+                for (int b = 0; b < NIN && b < NCH; b++) issue_in(b, nb * BN + col0 + b * EO::CW, gm0);
             }
+            bool ok = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.flags);
+            if (!__all_sync(0xffffffffu, ok)) {  // the warp leaves together
+                if (EO::IN) drain_in();
+                break;
+            }
+            tc_fence_after();
+            const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * CF::ACC_COLS + hh * BN);
             bool in_ok = true;
 #pragma unroll 1
             for (int ch = 0; ch < NCH; ch++) {
-                const int c0 = ch * EO::CW;
+                const int c0 = col0 + ch * EO::CW;
                 const int gn0 = nb * BN + c0;
-                const int ib = ch & 1;
-                if (EO::IN) {
-                    // the next chunk's input into the other buffer (read one chunk ago)
-                    __syncwarp();
-                    if (lane == 0 && ch + 1 < NCH) {
-                        mbar_expect_tx(&ibar[ib ^ 1], 4096);
-                        tma_load_2d(&tmX, &ibar[ib ^ 1], inb + (ib ^ 1) * 4096, gn0 + EO::CW, gm0);
-                    }
-                }
+                const int ib = ch % NIN;
                 float v[EO::CW];
-                tmem_ld32(trow + c0, v);
-                if (EO::CW == 64) tmem_ld32(trow + c0 + 32, v + 32);
+                {  // both halves of the chunk in flight, one wait
+                    uint32_t r[EO::CW];
+                    tmem_ld32_raw(trow + c0, r);
+                    if (EO::CW == 64) tmem_ld32_raw(trow + c0 + 32, r + 32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < EO::CW; i++) v[i] = __uint_as_float(r[i]);
+                }
                 if (EO::IN) {
                     const bool ok_in = mbar_wait(&ibar[ib], (in_par >> ib) & 1, abort_flag, p.flags);
-                    in_par ^= 1u << ib;
-                    if (!__all_sync(0xffffffffu, ok_in)) in_ok = false;
+                    if (__all_sync(0xffffffffu, ok_in)) {
+                        in_par ^= 1u << ib;
+                        pend &= ~(1 << ib);
+                    } else {
+                        in_ok = false;  // the load stays pending: drained below
+                    }
                 }
                 epilogue_math<EPI>(p, v, inb + ib * 4096, lane, gn0);
-                // the previous chunk's stores have finished reading the staging buffers
-                if (lane == 0) bulk_wait_read0();
+                if (EO::IN && in_ok && ch + NIN < NCH) {
+                    __syncwarp();  // every lane has read buffer ib
+                    issue_in(ib, gn0 + NIN * EO::CW, gm0);
+                }
+                // the stores that last read this staging set have finished reading it: every
+                // group but the newest has; the newest too unless it reads the other set
+                const int set = sbuf;
+                uint8_t* stg = stg0 + set * (EO::NOUT * 4096);
+                if (CF::STG_BUFS == 2) sbuf ^= 1;
+                if (lane == 0) {
+                    if (CF::STG_BUFS == 2 && newest_set != set)
+                        bulk_wait_read1();
+                    else
+                        bulk_wait_read0();
+                }
                 __syncwarp();
                 stage_row<EO::F32>(stg, lane, v);
                 if (EPI == E_GELU) {
@@ -416,15 +473,11 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
                         tma_store_2d(&tmD, stg, gn0, gm0);
                     if (EPI == E_GELU) tma_store_2d(&tmD2, stg + 4096, gn0, gm0);
                     bulk_commit();
+                    newest_set = set;
                 }
                 if (!in_ok) {
-                    // a wait gave up: let the next chunk's load (if issued) land before leaving
-                    if (lane == 0 && ch + 1 < NCH) {
-                        unsigned long long t0 = globaltimer();
-                        while (!mbar_try_wait(&ibar[ib ^ 1], (in_par >> (ib ^ 1)) & 1) && globaltimer() - t0 < TIMEOUT_NS) {
-                        }
-                    }
-                    __syncwarp();
+                    // a wait gave up: let the loads already issued land before leaving
+                    drain_in();
                     break;
                 }
             }

@@ -138,46 +138,95 @@ __global__ void enc_chunk_prefix_k(int* chunk_cnt, int* cnt, int nchunks, int V)
     int k = blockIdx.x * blockDim.x + threadIdx.x;
     if (k >= V) return;
     int run = 0;
-    for (int c = 0; c < nchunks; c++) {
-        int x = chunk_cnt[(size_t)c * V + k];
-        chunk_cnt[(size_t)c * V + k] = run;
-        run += x;
+    for (int c0 = 0; c0 < nchunks; c0 += 8) {  // 8 independent loads in flight, then the stores
+        int x[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) x[j] = c0 + j < nchunks ? chunk_cnt[(size_t)(c0 + j) * V + k] : 0;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            if (c0 + j < nchunks) chunk_cnt[(size_t)(c0 + j) * V + k] = run;
+            run += x[j];
+        }
     }
     cnt[k] = run;
 }
 
-// Single block: exclusive scans of cnt (-> start) and of ceil(cnt/SEG) (-> item_start).
-__global__ void enc_scan_k(const int* cnt, int* start, int* item_start, int V) {
-    __shared__ int s_a[1024], s_b[1024];
-    int tid = threadIdx.x, nt = blockDim.x;
-    int per = (V + nt - 1) / nt;
-    int lo = tid * per, hi = min(V, lo + per);
-    int a = 0, b = 0;
-    for (int k = lo; k < hi; k++) {
-        a += cnt[k];
-        b += (cnt[k] + ENC_SEG - 1) / ENC_SEG;
-    }
-    s_a[tid] = a;
-    s_b[tid] = b;
-    __syncthreads();
-    for (int off = 1; off < nt; off <<= 1) {  // Hillis-Steele inclusive scan
-        int ta = tid >= off ? s_a[tid - off] : 0;
-        int tb = tid >= off ? s_b[tid - off] : 0;
+// Single block of ENC_SCAN_T threads: exclusive scans of cnt (-> start) and of
+// ceil(cnt/SEG) (-> item_start), over tiles of ENC_SCAN_T * 8 ids staged in shared memory
+// with coalesced loads (thread t scans ids 8t..8t+7 of the tile, the block scans the
+// thread totals, a running offset carries from tile to tile).  Integer sums: exact.
+constexpr int ENC_SCAN_T = 1024, ENC_SCAN_PER = 8;
+__global__ void __launch_bounds__(ENC_SCAN_T) enc_scan_k(const int* cnt, int* start, int* item_start, int V) {
+    __shared__ int s_cnt[ENC_SCAN_T * ENC_SCAN_PER];
+    __shared__ int s_a[32], s_b[32];
+    static_assert(ENC_SCAN_T == 1024, "one warp scans the 32 warp totals");
+    const int tid = threadIdx.x;
+    int off_a = 0, off_b = 0;  // totals of the earlier tiles
+    for (int t0 = 0; t0 < V; t0 += ENC_SCAN_T * ENC_SCAN_PER) {
+        for (int i = tid; i < ENC_SCAN_T * ENC_SCAN_PER; i += ENC_SCAN_T)
+            s_cnt[i] = t0 + i < V ? cnt[t0 + i] : 0;
         __syncthreads();
-        s_a[tid] += ta;
-        s_b[tid] += tb;
+        int a = 0, b = 0;
+#pragma unroll
+        for (int j = 0; j < ENC_SCAN_PER; j++) {
+            const int x = s_cnt[tid * ENC_SCAN_PER + j];
+            a += x;
+            b += (x + ENC_SEG - 1) / ENC_SEG;
+        }
+        // inclusive scan of the thread totals: within each warp by shuffles, then the
+        // warp totals by warp 0, then each warp adds the totals of the warps before it
+        const int lane = tid & 31, wid = tid >> 5;
+        int ia = a, ib = b;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ta = __shfl_up_sync(0xffffffffu, ia, o), tb = __shfl_up_sync(0xffffffffu, ib, o);
+            if (lane >= o) {
+                ia += ta;
+                ib += tb;
+            }
+        }
+        if (lane == 31) {
+            s_a[wid] = ia;
+            s_b[wid] = ib;
+        }
         __syncthreads();
+        if (wid == 0) {
+            int wa = s_a[lane], wb = s_b[lane];  // ENC_SCAN_T / 32 == 32 warp totals
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int ta = __shfl_up_sync(0xffffffffu, wa, o), tb = __shfl_up_sync(0xffffffffu, wb, o);
+                if (lane >= o) {
+                    wa += ta;
+                    wb += tb;
+                }
+            }
+            s_a[lane] = wa;
+            s_b[lane] = wb;
+        }
+        __syncthreads();
+        if (wid > 0) {
+            ia += s_a[wid - 1];
+            ib += s_b[wid - 1];
+        }
+        int ra = off_a + ia - a, rb = off_b + ib - b;
+#pragma unroll
+        for (int j = 0; j < ENC_SCAN_PER; j++) {
+            const int k = t0 + tid * ENC_SCAN_PER + j;
+            const int x = s_cnt[tid * ENC_SCAN_PER + j];
+            if (k < V) {
+                start[k] = ra;
+                item_start[k] = rb;
+            }
+            ra += x;
+            rb += (x + ENC_SEG - 1) / ENC_SEG;
+        }
+        off_a += s_a[ENC_SCAN_T / 32 - 1];
+        off_b += s_b[ENC_SCAN_T / 32 - 1];
+        __syncthreads();  // s_cnt and the totals are reused by the next tile
     }
-    int ra = s_a[tid] - a, rb = s_b[tid] - b;
-    for (int k = lo; k < hi; k++) {
-        start[k] = ra;
-        item_start[k] = rb;
-        ra += cnt[k];
-        rb += (cnt[k] + ENC_SEG - 1) / ENC_SEG;
-    }
-    if (tid == nt - 1) {
-        start[V] = s_a[nt - 1];
-        item_start[V] = s_b[nt - 1];
+    if (tid == 0) {
+        start[V] = off_a;
+        item_start[V] = off_b;
     }
 }
 
@@ -224,14 +273,20 @@ __global__ void enc_seg_k(float* dwte, float* partial, const T* dout, const int*
         int c = c0 + lane * 8;
         if ((C & 7) == 0) {
             if (c < C) {
+#pragma unroll 4
                 for (int q = lo; q < hi; q++) {
                     float x[8];
                     Vec8<T>::load(dout + (size_t)perm[q] * C + c, x);
 #pragma unroll
                     for (int i = 0; i < 8; i++) acc[i] += x[i];
                 }
+                if (single) {
+                    float d[8];
+                    Vec8<float>::load(dst + c, d);
 #pragma unroll
-                for (int i = 0; i < 8; i++) dst[c + i] = single ? dst[c + i] + acc[i] : acc[i];
+                    for (int i = 0; i < 8; i++) acc[i] = d[i] + acc[i];
+                }
+                Vec8<float>::store(dst + c, acc);
             }
         } else {
             for (int i = 0; i < 8; i++) {
@@ -245,13 +300,93 @@ __global__ void enc_seg_k(float* dwte, float* partial, const T* dout, const int*
     }
 }
 
-// One warp per token with more than one segment: add the segment sums in order.
+// The same for C % 8 == 0, C <= 256 * NJ: the warp reads its segment's row indices once
+// (32 at a time, one per lane, broadcast by shuffles) and, per row, loads all NJ
+// 256-column groups (8 columns per lane each) before adding them, so one row costs one
+// dependent step instead of NJ.  Rows are added in the same order as above.
+template <typename T, int NJ>
+__global__ void enc_seg_vec_k(float* dwte, float* partial, const T* dout, const int* perm, const int* cnt,
+                              const int* start, const int* item_start, const int* item_tok, const int* n_items,
+                              int C) {
+    int item = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (item >= *n_items) return;
+    int k = item_tok[item];
+    int j = item - item_start[k];
+    int lo = start[k] + j * ENC_SEG, hi = min(start[k] + cnt[k], lo + ENC_SEG);
+    bool single = cnt[k] <= ENC_SEG;
+    float* dst = single ? dwte + (size_t)k * C : partial + (size_t)item * C;
+    float acc[NJ][8];
+#pragma unroll
+    for (int g = 0; g < NJ; g++)
+#pragma unroll
+        for (int i = 0; i < 8; i++) acc[g][i] = 0.f;
+    for (int q0 = lo; q0 < hi; q0 += 32) {
+        const int nq = min(32, hi - q0);
+        const int my_row = lane < nq ? perm[q0 + lane] : 0;
+#pragma unroll 2
+        for (int q = 0; q < nq; q++) {
+            const int row = __shfl_sync(0xffffffffu, my_row, q);
+            float x[NJ][8];
+#pragma unroll
+            for (int g = 0; g < NJ; g++) {
+                const int c = g * 256 + lane * 8;
+                if (c < C) {
+                    Vec8<T>::load(dout + (size_t)row * C + c, x[g]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; i++) x[g][i] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < NJ; g++)
+#pragma unroll
+                for (int i = 0; i < 8; i++) acc[g][i] += x[g][i];
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < NJ; g++) {
+        const int c = g * 256 + lane * 8;
+        if (c >= C) continue;
+        if (single) {
+            float d[8];
+            Vec8<float>::load(dst + c, d);
+#pragma unroll
+            for (int i = 0; i < 8; i++) acc[g][i] = d[i] + acc[g][i];
+        }
+        Vec8<float>::store(dst + c, acc[g]);
+    }
+}
+
+// Tokens with more than one segment: add the segment sums in segment order.  One warp
+// per (token, 256-column group, blockIdx.y); 8 consecutive columns per lane (C % 8 == 0),
+// else one column per lane in steps of 32.
 __global__ void enc_fix_k(float* dwte, const float* partial, const int* cnt, const int* item_start,
                           int V, int C) {
     int k = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (k >= V || cnt[k] <= ENC_SEG) return;
     int i0 = item_start[k], i1 = item_start[k + 1];
-    for (int c = lane; c < C; c += 32) {
+    const int c0 = blockIdx.y * 256;
+    if ((C & 7) == 0) {
+        const int c = c0 + lane * 8;
+        if (c >= C) return;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) acc[i] = 0.f;
+#pragma unroll 4
+        for (int it = i0; it < i1; it++) {
+            float x[8];
+            Vec8<float>::load(partial + (size_t)it * C + c, x);
+#pragma unroll
+            for (int i = 0; i < 8; i++) acc[i] += x[i];
+        }
+        float d[8];
+        Vec8<float>::load(dwte + (size_t)k * C + c, d);
+#pragma unroll
+        for (int i = 0; i < 8; i++) d[i] += acc[i];
+        Vec8<float>::store(dwte + (size_t)k * C + c, d);
+        return;
+    }
+    for (int c = c0 + lane; c < min(C, c0 + 256); c += 32) {
         float acc = 0.f;
         for (int it = i0; it < i1; it++) acc += partial[(size_t)it * C + c];
         dwte[(size_t)k * C + c] += acc;
@@ -266,11 +401,21 @@ cudaError_t encoder_backward_wte(ActType at, float* dwte, const void* dout, cons
     if (e != cudaSuccess) return e;
     G2_LAUNCH enc_hist_k<<<cdiv(M, 256), 256, 0, s>>>(sc->chunk_cnt, tok, M, V);
     G2_LAUNCH enc_chunk_prefix_k<<<cdiv(V, 256), 256, 0, s>>>(sc->chunk_cnt, sc->cnt, nch, V);
-    G2_LAUNCH enc_scan_k<<<1, 1024, 0, s>>>(sc->cnt, sc->start, sc->item_start, V);
+    G2_LAUNCH enc_scan_k<<<1, ENC_SCAN_T, 0, s>>>(sc->cnt, sc->start, sc->item_start, V);
     G2_LAUNCH enc_rank_k<<<nch, 1024, 0, s>>>(sc->perm, tok, sc->start, sc->chunk_cnt, M, V);
     G2_LAUNCH enc_items_k<<<cdiv(V, 256), 256, 0, s>>>(sc->item_tok, sc->cnt, sc->item_start, V);
     // Grid covers the maximum item count; the live count is read on the device.
-    if (at == ACT_BF16)
+    const int nj = (C % 8 == 0) ? (C + 255) / 256 : 0;
+    if (at == ACT_BF16 && nj >= 1 && nj <= 4) {
+#define G2_SEGV(NJ)                                                                                          \
+    case NJ:                                                                                                 \
+        G2_LAUNCH enc_seg_vec_k<bf16, NJ><<<cdiv(sc->max_items, 8), 256, 0, s>>>(                            \
+            dwte, sc->partial, (const bf16*)dout, sc->perm, sc->cnt, sc->start, sc->item_start, sc->item_tok, \
+            sc->item_start + V, C);                                                                          \
+        break;
+        switch (nj) { G2_SEGV(1) G2_SEGV(2) G2_SEGV(3) G2_SEGV(4) }
+#undef G2_SEGV
+    } else if (at == ACT_BF16)
         G2_LAUNCH enc_seg_k<bf16><<<cdiv(sc->max_items, 8), 256, 0, s>>>(
             dwte, sc->partial, (const bf16*)dout, sc->perm, sc->cnt, sc->start, sc->item_start,
             sc->item_tok, sc->item_start + V, C);
@@ -278,7 +423,8 @@ cudaError_t encoder_backward_wte(ActType at, float* dwte, const void* dout, cons
         G2_LAUNCH enc_seg_k<float><<<cdiv(sc->max_items, 8), 256, 0, s>>>(
             dwte, sc->partial, (const float*)dout, sc->perm, sc->cnt, sc->start, sc->item_start,
             sc->item_tok, sc->item_start + V, C);
-    G2_LAUNCH enc_fix_k<<<cdiv(V, 8), 256, 0, s>>>(dwte, sc->partial, sc->cnt, sc->item_start, V, C);
+    G2_LAUNCH enc_fix_k<<<dim3(cdiv(V, 8), cdiv(C, 256)), 256, 0, s>>>(dwte, sc->partial, sc->cnt, sc->item_start,
+                                                                        V, C);
     return cudaGetLastError();
 }
 

@@ -135,6 +135,8 @@ G2_DEV void tma_store_3d(const CUtensorMap* tm, const void* src, int x, int y, i
 G2_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the committed stores have finished reading their shared-memory sources
 G2_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// all but the most recently committed group have finished reading their sources
+G2_DEV void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // the committed stores have completed
 G2_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte
