@@ -460,6 +460,74 @@ def run_generate(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ forward only
+FWD_METRIC = "forward-only tokens/sec (logits of every position, no targets)"
+
+
+def run_forward(args, rank, world, local):
+    """The forward pass without targets (logits of every position, no loss): the
+    inference half of the step, 1/3 of its algorithmic FLOPs."""
+    import numpy as np
+    import torch
+    from gpt_train_step_arena_b300 import synth
+    from gpt_train_step_arena_b300.model import GPT2
+
+    torch.cuda.set_device(local)
+    cfg = dict(synth.WORKLOADS[args.workload])
+    L, C, NH, V, maxT, T = (cfg[k] for k in ("L", "C", "NH", "V", "maxT", "T"))
+    B = args.fwd_batch or cfg["B"]
+    W, K = args.warmup, args.steps
+    params = synth.init_params(L, C, V, maxT, seed=42)
+    stream = synth.token_stream(dict(cfg, B=B), steps=W + K, seed=1337 + rank)
+    tok = np.stack([synth.batch(stream, i, B, T)[0] for i in range(W + K)])
+    g = GPT2(L, C, NH, V, maxT, precision="bf16", norm=args.norm)
+    g.set_params(params)
+    s = torch.cuda.Stream()
+    g.set_stream(s.cuda_stream)
+    tok_dev = torch.from_numpy(tok).to(f"cuda:{local}")
+    for i in range(W):
+        g.forward_async(tok_dev[i], None, B, T, device=True)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    launches0 = g.kernel_launches()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(s)
+    for i in range(W, W + K):
+        g.forward_async(tok_dev[i], None, B, T, device=True)
+    ev1.record(s)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    launches = g.kernel_launches() - launches0
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / K, world)
+    # e2e: the public host-pointer call with ids from pinned host memory
+    tok_h = torch.from_numpy(tok).pin_memory()
+    from gpt_train_step_arena_b300 import _native as N
+    t0 = time.perf_counter()
+    for i in range(W, W + K):
+        N.lib.gpt2_forward(g.h, tok_h[i].data_ptr(), None, B, T)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / K, world)
+    if rank != 0:
+        return
+    pk = _peaks()
+    fpt = flops_per_token(cfg, g.Vp) / 3.0
+    value = world * B * T / (ms / 1e3)
+    line = {
+        "mode": "forward", "metric": FWD_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": DATA,
+        "config": dict(config_block(cfg, args.workload, args.norm), B=B, workload=f"{args.workload}_forward_b{B}"),
+        "mfu": {"algorithmic_flops_per_token": fpt, "vs_measured_burst": value / world * fpt / (pk["bf16"] * 1e12)},
+        "e2e": {"value": world * B * T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": B * T * 4,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -467,8 +535,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gpt2_124m")
-    ap.add_argument("--mode", choices=["train", "generate"], default="train",
-                    help="generate: greedy decode throughput with the key/value cache")
+    ap.add_argument("--mode", choices=["train", "generate", "forward"], default="train",
+                    help="generate: greedy decode throughput with the key/value cache; "
+                         "forward: logits of every position without targets")
+    ap.add_argument("--fwd-batch", type=int, default=0, help="forward mode batch (default: the workload's B)")
     ap.add_argument("--gen-batch", type=int, default=16)
     ap.add_argument("--gen-prompt", type=int, default=64)
     ap.add_argument("--gen-tokens", type=int, default=40)
@@ -485,6 +555,8 @@ def main():
         run_reference(args, rank, world)
     elif args.mode == "generate":
         run_generate(args, rank, world, local)
+    elif args.mode == "forward":
+        run_forward(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:
