@@ -825,14 +825,37 @@ __global__ void __launch_bounds__(LNT_THREADS, 1)
         float wv[NV][8];
 #pragma unroll
         for (int j = 0; j < NV; j++) Vec8<float>::load(w + j * 256 + lane * 8, wv[j]);
+        // the row statistics of this warp's rows (warp - 1 and warp + 7) are loaded one
+        // tile ahead, so no row starts with a dependent global load
+        constexpr int RPW = LNB_ROWS / 8;
+        float nm[RPW], nr[RPW];
+        auto load_stats = [&](int t) {
+#pragma unroll
+            for (int i = 0; i < RPW; i++) {
+                const int row = t * LNB_ROWS + warp - 1 + 8 * i;
+                nm[i] = (RMS || t >= ntiles || row >= M) ? 0.f : mean[row];
+                nr[i] = (t >= ntiles || row >= M) ? 0.f : rstd[row];
+            }
+        };
+        load_stats(blockIdx.x);
         int it = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, it++) {
+            float cm[RPW], cr[RPW];
+#pragma unroll
+            for (int i = 0; i < RPW; i++) {
+                cm[i] = nm[i];
+                cr[i] = nr[i];
+            }
+            load_stats(t + gridDim.x);
             const int s = it % LNB_STAGES;
             const bool ok = tc::mbar_wait(&full[s], (it / LNB_STAGES) & 1, abort_flag, nullptr);
             if (!__all_sync(0xffffffffu, ok)) break;
             const int rows = min(LNB_ROWS, M - t * LNB_ROWS);
             const uint8_t* st = smem + s * stage_bytes;
-            for (int r = warp - 1; r < rows; r += 8) {
+#pragma unroll
+            for (int ri = 0; ri < RPW; ri++) {
+                const int r = warp - 1 + 8 * ri;
+                if (r >= rows) break;
                 const int row = t * LNB_ROWS + r;
                 const bf16* d = reinterpret_cast<const bf16*>(st) + (size_t)r * C;
                 const bf16* x = reinterpret_cast<const bf16*>(st + sub_bytes) + (size_t)r * C;
@@ -843,7 +866,7 @@ __global__ void __launch_bounds__(LNT_THREADS, 1)
                     Vec8<bf16>::load(d + j * 256 + lane * 8, dv[j]);
                     Vec8<bf16>::load(x + j * 256 + lane * 8, xv[j]);
                 }
-                const float m = RMS ? 0.f : mean[row], rs = rstd[row];
+                const float m = cm[ri], rs = cr[ri];
                 float gm = 0.f, gnm = 0.f;
 #pragma unroll
                 for (int j = 0; j < NV; j++)
