@@ -68,19 +68,25 @@ def _mha(x, w_attn, b_attn, w_proj, b_proj, n_head):
     return _linear(np.hstack(outs), w_proj, b_proj)
 
 
-def picogpt_logits(flat, tokens, L, C, NH, V, maxT):
-    """(B, T, V) logits from the picoGPT formulation, one sequence at a time."""
+def _rms_norm(x, g, b, eps=1e-5):  # b unused: RMSNorm has no shift
+    return g * x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+
+
+def picogpt_logits(flat, tokens, L, C, NH, V, maxT, norm="layernorm"):
+    """(B, T, V) logits from the picoGPT formulation, one sequence at a time; norm="rmsnorm"
+    puts root-mean-square normalisation (gain, no shift) in place of every layer_norm."""
+    nf = _rms_norm if norm == "rmsnorm" else _layer_norm
     P = unflatten(np.asarray(flat, np.float64), L, C, V, maxT)
     res = []
     for seq in np.asarray(tokens):
         x = P["wte"][seq] + P["wpe"][np.arange(len(seq))]
         for l in range(L):
-            h = _layer_norm(x, P["ln1w"][l], P["ln1b"][l])
+            h = nf(x, P["ln1w"][l], P["ln1b"][l])
             x = x + _mha(h, P["qkvw"][l].T, P["qkvb"][l], P["attprojw"][l].T, P["attprojb"][l], NH)
-            h = _layer_norm(x, P["ln2w"][l], P["ln2b"][l])
+            h = nf(x, P["ln2w"][l], P["ln2b"][l])
             a = _gelu(_linear(h, P["fcw"][l].T, P["fcb"][l]))
             x = x + _linear(a, P["fcprojw"][l].T, P["fcprojb"][l])
-        x = _layer_norm(x, P["lnfw"], P["lnfb"])
+        x = nf(x, P["lnfw"], P["lnfb"])
         res.append(x @ P["wte"].T)
     return np.stack(res)
 

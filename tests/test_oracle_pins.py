@@ -580,3 +580,17 @@ def test_generate_sampling_matches_picogpt_loop_and_low_temperature_is_greedy():
     # as the temperature goes to 0 the distribution collapses onto the argmax
     cold = m.generate(prompt, 5, temperature=1e-4, coins=coins)
     assert np.array_equal(cold, m.generate(prompt, 5))
+
+
+def test_rmsnorm_model_forward_matches_numpy_statement():
+    """The RMSNorm model's logits against a numpy restatement of the same forward."""
+    L, C, NH, V, maxT = _cfg("tiny")
+    params = synth.init_params(L, C, V, maxT, seed=89).astype(np.float64)
+    params += np.random.default_rng(90).normal(scale=0.05, size=params.size)
+    inp = synth.zipf_stream(V, 2 * 12, seed=91).reshape(2, 12)
+    m = Model(L, C, NH, V, maxT, norm="rmsnorm")
+    m.set_params(params)
+    m.forward(inp)
+    want = picogpt_logits(params, inp, L, C, NH, V, maxT, norm="rmsnorm")
+    assert np.allclose(m.logits(), want, rtol=1e-11, atol=1e-12)
+    assert not np.allclose(want, picogpt_logits(params, inp, L, C, NH, V, maxT), atol=1e-3)
