@@ -72,6 +72,11 @@ SIGNATURES = {
     "gpt2_op_rmsnorm_backward_workspace": (SZ, [I]),
     "gpt2_op_rmsnorm_backward": (I, [I, P, P, P, P, P, P, I, I, P, SZ, P]),
     "gpt2_op_softmax_xent": (I, [I, P, P, P, I, I, I, F, P, P]),
+    "gpt2_op_encoder_forward": (I, [I, P, P, P, P, I, I, I, I, P, P]),
+    "gpt2_op_encoder_backward_workspace": (SZ, [I, I, I]),
+    "gpt2_op_encoder_backward": (I, [I, P, P, P, P, I, I, I, I, I, P, SZ, P]),
+    "gpt2_op_gemm_force_tile_rows": (I, [I]),
+    "gpt2_op_gemm_last_variant": (ct.c_char_p, []),
 }
 
 for _name, (_res, _args) in SIGNATURES.items():

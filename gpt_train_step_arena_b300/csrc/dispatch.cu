@@ -19,6 +19,7 @@ bool gemm_tc_path(const GemmArgs& a) { return gemm_tc_supported(a); }
 
 cudaError_t gemm_dispatch(const GemmArgs& a, float* ws, size_t ws_bytes, cudaStream_t s) {
     if (gemm_tc_supported(a)) return gemm_tc(a, ws, ws_bytes, a.flags, s);
+    gemm_tc_note_variant("simt");
     return gemm_simt(a, s);
 }
 
@@ -28,7 +29,6 @@ cudaError_t attention_forward(ActType at, void* out, float* lse, const void* qkv
         cudaError_t e = attention_forward_tc(out, lse, qkv, B, T, C, NH, flags, s);
         if (e != cudaErrorNotSupported) return e;  // else: no tensor map for this shape
     }
-    if (attention_mma_supported(at, C, NH)) return attention_forward_mma(out, lse, qkv, B, T, C, NH, s);
     return attention_forward_simt(at, out, lse, qkv, B, T, C, NH, s);
 }
 
@@ -39,8 +39,6 @@ cudaError_t attention_backward(ActType at, void* dqkv, const void* dout, const v
         cudaError_t e = attention_backward_tc(dqkv, dout, qkv, out, lse, B, T, C, NH, scratch_D, flags, s);
         if (e != cudaErrorNotSupported) return e;
     }
-    if (attention_mma_supported(at, C, NH))
-        return attention_backward_mma(dqkv, dout, qkv, out, lse, B, T, C, NH, scratch_D, s);
     return attention_backward_simt(at, dqkv, dout, qkv, out, lse, B, T, C, NH, scratch_D, s);
 }
 

@@ -27,6 +27,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
+#include <cstdio>
 #include <mutex>
 
 #include "common.cuh"
@@ -593,15 +595,37 @@ static int* fallback_flag() {
     return ptr;
 }
 
+// Tile-height override (0: chosen per shape) and a description of the last launch, so
+// that the variants large shapes pick can be run, and identified, on small ones.
+static std::atomic<int> g_force_rows{0};
+static std::mutex g_variant_mu;
+static char g_variant[128] = "none";
+
 // Tile height: 256-row tiles halve the operand bytes each SM receives per FLOP for B but
 // leave no room in tensor memory for a second accumulator, so their epilogue does not
 // overlap the next tile; they pay off for long K (many K blocks per tile) when there are
-// plenty of tiles.  Otherwise 128-row tiles with double-buffered accumulators.
+// plenty of tiles.  Otherwise 128-row tiles with double-buffered accumulators.  Products
+// with a staged epilogue input always take 128-row tiles, whatever the override.
 static int tile_rows(int M, int N, int K, int BN, bool staged_input = false) {
+    if (staged_input) return 128;
+    const int forced = g_force_rows.load(std::memory_order_relaxed);
+    if (forced) return forced;
     const long long tiles128 = (long long)((M + 127) / 128) * ((N + BN - 1) / BN);
     const bool long_k = K >= 2048 && tiles128 >= 4LL * num_sms();
     const bool very_many_tiles = tiles128 >= 64LL * num_sms();  // e.g. the LM head forward
-    return (!staged_input && (long_k || very_many_tiles)) ? 256 : 128;
+    return (long_k || very_many_tiles) ? 256 : 128;
+}
+
+int gemm_tc_force_tile_rows(int rows) { return g_force_rows.exchange(rows == 128 || rows == 256 ? rows : 0); }
+
+void gemm_tc_note_variant(const char* v) {
+    std::lock_guard<std::mutex> lk(g_variant_mu);
+    snprintf(g_variant, sizeof g_variant, "%s", v);
+}
+
+void gemm_tc_last_variant(char* out, size_t n) {
+    std::lock_guard<std::mutex> lk(g_variant_mu);
+    snprintf(out, n, "%s", g_variant);
 }
 
 // Split-K plan for a product with few output tiles and a long K.
@@ -744,6 +768,13 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
         if (!make_map_nd(&mp.d2, a.D2, false, 2, dims, st, box_bf16)) return cudaErrorInvalidValue;
     }
 
+    {
+        static const char* epi_names[] = {"store", "gelu", "gelu_bwd"};
+        std::lock_guard<std::mutex> lk(g_variant_mu);
+        snprintf(g_variant, sizeof g_variant, "rows=%d cols=%d splits=%d a=%s b=%s epi=%s%s%s", bmt, BN, splits,
+                 a_mn ? "mn" : "k", b_mn ? "mn" : "k", epi_names[a.epi], a.d_f32 ? " f32" : "",
+                 staged_in && a.epi == EPI_STORE ? " residual" : "");
+    }
     cudaError_t e;
     if (splits > 1) {
         e = BN == 256 ? launch_layout<256, E_PARTIAL>(bmt, a_mn, b_mn, mp, p, s)

@@ -1121,7 +1121,9 @@ __global__ void __launch_bounds__(256) colsum_part_k(float* part, const T* X, in
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; i++) acc[i] = 0.f;
-    bool vec = ((N & 7) == 0) && col + 8 <= N;
+    // 16-byte loads need a 16-byte aligned base (a column-offset view may not be); both
+    // paths add the same rows in the same order, so the sums are bitwise the same
+    bool vec = ((N & 7) == 0) && (((uintptr_t)X & 15) == 0) && col + 8 <= N;
     int r = r0 + warp;
     if (vec) {
         // rows r, r+8, r+16, r+24 loaded together, added in row order

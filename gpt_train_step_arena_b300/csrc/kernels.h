@@ -88,14 +88,6 @@ cudaError_t attention_backward_simt(ActType at, void* dqkv, const void* dout, co
 // D[b,h,t] = sum_d dout[b,t,h,d] * out[b,t,h,d]  (B*NH*T floats)
 cudaError_t attention_bwd_dot(ActType at, float* D, const void* dout, const void* out, int B, int T,
                               int C, int NH, cudaStream_t s);
-// Tensor-core (mma.sync, bf16, head size 64) forward and backward.
-bool attention_mma_supported(ActType at, int C, int NH);
-cudaError_t attention_forward_mma(void* out, float* lse, const void* qkv, int B, int T, int C, int NH,
-                                  cudaStream_t s);
-cudaError_t attention_backward_mma(void* dqkv, const void* dout, const void* qkv, const void* out,
-                                   const float* lse, int B, int T, int C, int NH, float* scratch_D,
-                                   cudaStream_t s);
-
 // tcgen05 forward (bf16, head size 64, 16-byte aligned qkv).  flags (may be null):
 // G2_FLAG_TIMEOUT is OR-ed in if a bounded wait expires.
 bool attention_tc_supported(ActType at, int C, int NH, const void* qkv);

@@ -8,6 +8,7 @@
 #include "../../include/gpt2.h"
 #include "../../include/gpt2_ops.h"
 #include "dispatch.h"
+#include "gemm_tc.h"
 #include "kernels.h"
 
 using namespace g2;
@@ -231,6 +232,51 @@ extern "C" int gpt2_op_softmax_xent(int dtype, void* logits, float* losses, cons
     if (rc) return rc;
     if (scratch) return op_fail(GPT2_ERR_TOKEN, "softmax_xent: a target id is outside [0, %d)", V);
     return GPT2_OK;
+}
+
+extern "C" int gpt2_op_encoder_forward(int dtype, void* out, const int32_t* tokens, const void* wte, const void* wpe,
+                                       int B, int T, int C, int V, int* flags, void* stream) {
+    if (!dtype_ok(dtype)) return op_fail(GPT2_ERR_ARG, "encoder_forward: bad dtype %d", dtype);
+    if (B < 0 || T < 0 || C <= 0 || V <= 0) return op_fail(GPT2_ERR_ARG, "encoder_forward: bad shape");
+    if ((size_t)B * T == 0) return GPT2_OK;
+    if (!out || !tokens || !wte || !wpe || !flags) return op_fail(GPT2_ERR_ARG, "encoder_forward: null pointer");
+    return op_cuda(encoder_forward(act_of(dtype), out, tokens, wte, wpe, B, T, C, V, flags, (cudaStream_t)stream),
+                   "encoder_forward");
+}
+
+extern "C" size_t gpt2_op_encoder_backward_workspace(int M, int V, int C) {
+    if (M < 0 || V <= 0 || C <= 0) return 0;
+    return encoder_bwd_scratch_bytes(M, V, C);
+}
+
+extern "C" int gpt2_op_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dout, const int32_t* tokens,
+                                        int B, int T, int C, int V, int maxT, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    if (!dtype_ok(dtype)) return op_fail(GPT2_ERR_ARG, "encoder_backward: bad dtype %d", dtype);
+    if (B < 0 || T < 0 || C <= 0 || V <= 0 || T > maxT)
+        return op_fail(GPT2_ERR_ARG, "encoder_backward: bad shape");
+    if (!dwte || !dwpe) return op_fail(GPT2_ERR_ARG, "encoder_backward: null pointer");
+    const int M = B * T;
+    if (M > 0 && (!dout || !tokens)) return op_fail(GPT2_ERR_ARG, "encoder_backward: null pointer");
+    const size_t need = gpt2_op_encoder_backward_workspace(M, V, C);
+    if (!workspace || workspace_bytes < need)
+        return op_fail(GPT2_ERR_ARG, "encoder_backward: workspace of %zu bytes needed, %zu given", need,
+                       workspace_bytes);
+    if ((uintptr_t)workspace & 255) return op_fail(GPT2_ERR_ARG, "encoder_backward: workspace must be 256-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    int rc = op_cuda(encoder_backward_wpe(act_of(dtype), dwpe, dout, B, T, C, maxT, s), "encoder_backward");
+    if (rc) return rc;
+    EncoderBwdScratch sc;
+    encoder_bwd_scratch_carve(&sc, workspace, M, V, C);
+    return op_cuda(encoder_backward_wte(act_of(dtype), dwte, dout, tokens, M, C, V, &sc, s), "encoder_backward");
+}
+
+extern "C" int gpt2_op_gemm_force_tile_rows(int rows) { return gemm_tc_force_tile_rows(rows); }
+
+extern "C" const char* gpt2_op_gemm_last_variant(void) {
+    static thread_local char buf[128];
+    gemm_tc_last_variant(buf, sizeof buf);
+    return buf;
 }
 
 // Sets the message returned by gpt2_op_last_error (for entry points in other files).

@@ -6,6 +6,9 @@
 // cudaMalloc of its own would fail or fragment that pool), or a deployment that
 // forbids device allocation once it has started.  gpt2_op_bias_grad_noalloc keeps the
 // partial sums in a fixed array that lives in the library's own device image instead.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdio>
 #include <mutex>
 
@@ -25,6 +28,37 @@ __device__ __align__(256) float g_bias_grad_scratch[kNoAllocScratchFloats];
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 float* g_scratch_ptr[kMaxDevices] = {};
+// Id of the context the cached address belongs to.  A cudaDeviceReset destroys the
+// device's primary context; the next one loads the library's device image afresh, so
+// the array may sit at another address and the cache must be refreshed.  Context ids
+// are unique for the life of the process (a new context never reuses an old id).
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
+
+// Id of the calling thread's current context (0 if it cannot be read: the address is
+// then looked up on every call, which is always correct).
+unsigned long long current_ctx_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = (GetCurrent)f;
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = (GetId)f;
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 int set_error(int code, const char* msg) {
     g2_op_set_error(msg);
@@ -54,10 +88,13 @@ extern "C" int gpt2_op_bias_grad_noalloc(int dtype, const void* dout, int M, int
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return set_error(GPT2_ERR_CUDA, cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return set_error(GPT2_ERR_ARG, "bias_grad_noalloc: device id too large");
+    // (before the runtime has made a context current this is 0 and the lookup below,
+    // which creates the context, runs again on the next call)
+    const unsigned long long ctx = current_ctx_id();
     float* scratch;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        if (!g_scratch_ptr[dev]) {
+        if (!g_scratch_ptr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
             // the device address of the array on the current device (host code cannot
             // use the symbol itself)
             void* p = nullptr;
@@ -67,6 +104,7 @@ extern "C" int gpt2_op_bias_grad_noalloc(int dtype, const void* dout, int M, int
                 return set_error(GPT2_ERR_CUDA, msg);
             }
             g_scratch_ptr[dev] = (float*)p;
+            g_scratch_ctx[dev] = ctx;
         }
         scratch = g_scratch_ptr[dev];
     }

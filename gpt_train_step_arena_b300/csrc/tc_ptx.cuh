@@ -45,9 +45,6 @@ G2_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait on phase `parity`.  Returns false (and raises the CTA-wide abort and
-// the global timeout flag) if it does not complete within TIMEOUT_NS, or if another
-// role of the CTA has already aborted.
 // As mbar_try_wait, but the thread may be suspended (no issue slots used) until the
 // phase completes or about `ns` nanoseconds pass.
 G2_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
@@ -62,6 +59,9 @@ G2_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
     return ok != 0;
 }
 
+// Bounded wait on phase `parity`.  Returns false (and raises the CTA-wide abort and
+// the global timeout flag) if it does not complete within TIMEOUT_NS, or if another
+// role of the CTA has already aborted.
 G2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* flags) {
     if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = globaltimer();
@@ -89,15 +89,6 @@ G2_DEV void tma_prefetch_l2(const CUtensorMap* tm, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"((uint64_t)tm), "r"(x),
                  "r"(y)
                  : "memory");
-}
-// As tma_load_2d, but the tile lands at the same shared-memory offset in every CTA of
-// the cluster named in cta_mask, each of whose mbarrier (same offset) receives the bytes.
-G2_DEV void tma_load_2d_mc(const CUtensorMap* tm, uint64_t* bar, void* dst, int x, int y, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"((uint64_t)tm), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
 }
 G2_DEV uint32_t cluster_rank() {
     uint32_t r;
@@ -169,15 +160,6 @@ G2_DEV void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t 
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-        : "memory");
-}
-// Arrive on the mbarrier at this offset in every CTA of cta_mask once all prior MMAs of
-// this thread complete.
-G2_DEV void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
         : "memory");
 }
 G2_DEV void umma_commit(uint64_t* bar) {

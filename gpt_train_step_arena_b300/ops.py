@@ -153,3 +153,46 @@ def linear_fused(A: torch.Tensor, W: torch.Tensor, epilogue: int, bias=None, R=N
                                    None if P is None else P.data_ptr(), 0 if P is None else P.stride(0),
                                    epilogue, None if ws is None else ws.data_ptr(), workspace_bytes, _stream()))
     return (D, D2) if D2 is not None else D
+
+
+def encoder_forward(tokens: torch.Tensor, wte: torch.Tensor, wpe: torch.Tensor, flags=None):
+    """tokens (B,T) int32, wte (V,C), wpe (>=T,C) -> out (B,T,C) like wte."""
+    B, T = tokens.shape
+    V, C = wte.shape
+    out = torch.empty(B, T, C, dtype=wte.dtype, device=wte.device)
+    if flags is None:
+        flags = torch.zeros(1, dtype=torch.int32, device=wte.device)
+    _check(N.lib.gpt2_op_encoder_forward(_dt(wte), out.data_ptr(), tokens.data_ptr(), wte.data_ptr(),
+                                         wpe.data_ptr(), B, T, C, V, flags.data_ptr(), _stream()))
+    return out
+
+
+def encoder_backward(dwte: torch.Tensor, dout: torch.Tensor, tokens: torch.Tensor, maxT: int):
+    """dwte (V,C) fp32 is accumulated into in place; returns dwpe (maxT,C) fp32."""
+    B, T, C = dout.shape
+    V = dwte.shape[0]
+    dwpe = torch.empty(maxT, C, dtype=torch.float32, device=dout.device)
+    ws_bytes = N.lib.gpt2_op_encoder_backward_workspace(B * T, V, C)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dout.device)
+    _check(N.lib.gpt2_op_encoder_backward(_dt(dout), dwte.data_ptr(), dwpe.data_ptr(), dout.data_ptr(),
+                                          tokens.data_ptr(), B, T, C, V, maxT, ws.data_ptr(), ws.numel(),
+                                          _stream()))
+    return dwpe
+
+
+class gemm_tile_rows:
+    """Context manager: force the tensor-core GEMM's tile height (128 or 256) inside."""
+
+    def __init__(self, rows: int):
+        self.rows = rows
+
+    def __enter__(self):
+        self.prev = N.lib.gpt2_op_gemm_force_tile_rows(self.rows)
+        return self
+
+    def __exit__(self, *exc):
+        N.lib.gpt2_op_gemm_force_tile_rows(self.prev)
+
+
+def gemm_last_variant() -> str:
+    return N.lib.gpt2_op_gemm_last_variant().decode()

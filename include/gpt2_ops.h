@@ -47,9 +47,13 @@ int gpt2_op_bias_grad(int dtype, const void* dout, int M, int N, float* dbias, v
  * gpt2_op_bias_grad_noalloc_max_floats() and returns GPT2_ERR_ARG (with a message in
  * gpt2_op_last_error) beyond that.  It allocates nothing.  The first call on a device
  * looks up the array's device address with that device current; make that first call
- * before any stream capture.  All calls share the one array: calls whose work overlaps
- * on the GPU (different streams, or different host threads) race on it and must be
- * serialised by the caller. */
+ * before any stream capture.  After a cudaDeviceReset the device gets a new context
+ * (and the array a possibly new address): the first call in that context looks the
+ * address up again, so it too belongs before any capture.  All calls share the one
+ * array, which keeps the last call's partial sums (every partial is written before it
+ * is read, so nothing needs clearing): calls whose work overlaps on the GPU (different
+ * streams, or different host threads) race on it and must be serialised by the
+ * caller.  dout needs no particular alignment. */
 int gpt2_op_bias_grad_noalloc(int dtype, const void* dout, int M, int N, float* dbias,
                               void* stream);
 size_t gpt2_op_bias_grad_noalloc_max_floats(void);
@@ -150,6 +154,40 @@ int gpt2_op_rmsnorm_backward(int dtype, void* dinp, float* dw, const void* dout,
  * check; pass NULL to skip it and return without waiting). */
 int gpt2_op_softmax_xent(int dtype, void* logits, float* losses, const int32_t* targets, int M,
                          int V, int Vp, float dloss, int* flags, void* stream);
+
+/* Token + position embedding (llm.c §1.1 encoder_forward; picoGPT gpt2's
+ * wte[inputs] + wpe[range(len(inputs))]): out[b,t,:] = wte[tokens[b,t],:] + wpe[t,:] for
+ * tokens (B,T) int32 device ids, wte (V,C) and wpe (>= T rows, C) of `dtype`, out (B,T,C)
+ * of `dtype` overwritten.  An id outside [0,V) ORs 1 into *flags (4 bytes of device
+ * memory, required; never cleared here) and gives that row wpe[t] alone. */
+int gpt2_op_encoder_forward(int dtype, void* out, const int32_t* tokens, const void* wte, const void* wpe, int B,
+                            int T, int C, int V, int* flags, void* stream);
+
+/* Its backward (llm.c §1.2 encoder_backward), deterministic: dwpe (maxT,C) fp32 is
+ * OVERWRITTEN (rows t < T get the sum over b, in ascending b, of dout[b,t,:]; rows
+ * t >= T get 0) and dwte (V,C) fp32 is ACCUMULATED into (row k += the sum of the dout
+ * rows whose id is k, in ascending position order; the listing's += into the gradient
+ * the tied LM head already wrote).  Positions are bucketed by id with a stable integer
+ * counting sort, so no float atomics are used and the result is bitwise reproducible.
+ * Ids outside [0,V) are skipped.  workspace: gpt2_op_encoder_backward_workspace(B*T, V,
+ * C) bytes, 256-byte aligned; its contents on entry do not matter. */
+size_t gpt2_op_encoder_backward_workspace(int M, int V, int C);
+int gpt2_op_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dout, const int32_t* tokens, int B,
+                             int T, int C, int V, int maxT, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Tile height of the tensor-core matrix product, a test and tuning hook: rows = 128 or
+ * 256 makes every later bf16 tensor-core product of the process use tiles of that many
+ * rows, any other value restores the choice per shape (the default); returns the
+ * previous setting.  Products whose epilogue reads a staged input (residual, GELU')
+ * always use 128-row tiles.  Not synchronised with work in flight: set it between
+ * launches. */
+int gpt2_op_gemm_force_tile_rows(int rows);
+/* The kernel variant of the last matrix product launched by this process, as
+ * "rows=R cols=N splits=S a=k|mn b=k|mn epi=...", or "simt" when the last product took
+ * the CUDA-core kernel (fp32, or a layout the tensor-core path does not take; "none"
+ * before any).  The string
+ * belongs to the calling thread and stays valid until its next call. */
+const char* gpt2_op_gemm_last_variant(void);
 
 #ifdef __cplusplus
 }

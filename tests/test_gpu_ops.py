@@ -47,6 +47,25 @@ def test_bias_grad(torch_cuda, M, N):
     assert np.array_equal(got_b, _np(ops.bias_grad(xb)))  # fixed summation order
 
 
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+def test_bias_grad_unaligned_view(torch_cuda, dt):
+    """N % 8 == 0 but dout starts one element off a 16-byte boundary (a column-offset
+    view): the kernel must not issue 16-byte loads there, and the sums stay bitwise the
+    same as on an aligned copy (same rows in the same order)."""
+    torch = torch_cuda
+    from gpt_train_step_arena_b300 import ops
+    M, N = 777, 512
+    tdt = torch.float32 if dt == "fp32" else torch.bfloat16
+    rng = np.random.default_rng(77)
+    flat = _to(torch, rng.normal(size=M * N + 8).astype(np.float32), tdt)
+    view = flat[1:1 + M * N].view(M, N)
+    assert view.data_ptr() % 16 != 0
+    got = ops.bias_grad(view)
+    aligned = ops.bias_grad(view.clone())
+    assert torch.equal(got, aligned)
+    assert np.allclose(_np(got), _np(view).sum(0), rtol=1e-5, atol=1e-4 * np.sqrt(M))
+
+
 # ---------------------------------------------------------------- matmul
 SHAPES = [(300, 200, 104), (256, 256, 128), (128, 768, 768), (1, 8, 16), (129, 136, 72), (512, 2304, 768)]
 
@@ -150,7 +169,8 @@ def test_attention_fwd_bwd(torch_cuda, B, T, C, NH, dt):
 
 
 # ---------------------------------------------------------------- layernorm
-@pytest.mark.parametrize("M,C", [(1000, 768), (37, 768), (300, 100), (1, 256), (513, 1024), (0, 768)])
+@pytest.mark.parametrize("M,C", [(1000, 768), (37, 768), (300, 100), (1, 256), (513, 1024), (0, 768),
+                                 (20000, 768), (5003, 1024)])
 @pytest.mark.parametrize("dt", ["fp32", "bf16"])
 def test_layernorm_fwd_bwd(torch_cuda, M, C, dt):
     torch = torch_cuda

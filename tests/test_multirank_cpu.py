@@ -46,7 +46,7 @@ def test_reference_arm_two_ranks_prints_one_line():
     port = _free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--gpus", "2",
-           "--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3", "--ref-tokens", "8"]
+           "--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3", "--cpu-tokens", "8"]
     env = dict(os.environ, OMP_NUM_THREADS="2")
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
