@@ -28,6 +28,7 @@ SIGNATURES = {
     "gpt2_free": (None, [P]),
     "gpt2_num_params": (SZ, [P]),
     "gpt2_padded_vocab": (I, [P]),
+    "gpt2_init_params": (I, [P, U64]),
     "gpt2_set_params": (I, [P, P, SZ]),
     "gpt2_get_params": (I, [P, P, SZ]),
     "gpt2_get_grads": (I, [P, P, SZ]),
@@ -60,6 +61,7 @@ SIGNATURES = {
     "gpt2_op_bias_grad_noalloc": (I, [I, P, I, I, P, P]),
     "gpt2_op_bias_grad_noalloc_max_floats": (SZ, []),
     "gpt2_op_matmul": (I, [I, I, I, I, P, ct.c_longlong, I, P, ct.c_longlong, I, P, ct.c_longlong, I, P, P, SZ, P]),
+    "gpt2_op_matmul_workspace": (SZ, [I, I, I, I, I, I]),
     "gpt2_op_matmul_ex": (I, [I, I, I, I, P, ct.c_longlong, I, P, ct.c_longlong, I, P, ct.c_longlong, P, P,
                               ct.c_longlong, P, ct.c_longlong, P, ct.c_longlong, I, P, SZ, P]),
     "gpt2_op_adamw": (I, [P, P, P, P, P, SZ, F, F, F, F, F, I, P]),
@@ -87,9 +89,9 @@ for _name, (_res, _args) in SIGNATURES.items():
 # enum values of include/gpt2.h
 GPT2_OK, GPT2_ERR_ARG, GPT2_ERR_OOM, GPT2_ERR_CUDA = 0, -1, -2, -3
 GPT2_ERR_TOKEN, GPT2_ERR_SHAPE, GPT2_ERR_STATE, GPT2_ERR_NONFINITE, GPT2_ERR_TIMEOUT = -4, -5, -6, -7, -8
-GPT2_FP32, GPT2_BF16 = 0, 2
+GPT2_FP32, GPT2_TF32, GPT2_BF16 = 0, 1, 2
 GPT2_LAYERNORM, GPT2_RMSNORM = 0, 1
-GPT2_DT_F32, GPT2_DT_BF16 = 0, 1
+GPT2_DT_F32, GPT2_DT_BF16, GPT2_DT_TF32 = 0, 1, 2
 GPT2_HOST, GPT2_DEVICE = 0, 1
 GPT2_EPI_STORE, GPT2_EPI_GELU, GPT2_EPI_GELU_BWD = 0, 1, 2
 KERNEL_CLASSES = ["gemm", "attn_fwd", "attn_bwd", "layernorm", "xent", "adamw", "encoder", "bias_grad"]

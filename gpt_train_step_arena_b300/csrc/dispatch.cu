@@ -18,6 +18,7 @@ size_t gemm_workspace_bytes(int M, int C, int Vp, int) {
 bool gemm_tc_path(const GemmArgs& a) { return gemm_tc_supported(a); }
 
 cudaError_t gemm_dispatch(const GemmArgs& a, float* ws, size_t ws_bytes, cudaStream_t s) {
+    if (a.in_type == ACT_F32 && a.tf32) return gemm_dispatch_tf32(a, ws, ws_bytes, s);
     if (gemm_tc_supported(a)) return gemm_tc(a, ws, ws_bytes, a.flags, s);
     gemm_tc_note_variant("simt");
     return gemm_simt(a, s);

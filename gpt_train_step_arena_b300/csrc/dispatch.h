@@ -11,6 +11,11 @@ size_t gemm_workspace_bytes(int M, int C, int Vp, int L);
 cudaError_t gemm_dispatch(const GemmArgs& a, float* ws, size_t ws_bytes, cudaStream_t s);
 // True when the tensor-core kernel takes this product (else the SIMT kernel would).
 bool gemm_tc_path(const GemmArgs& a);
+// TF32 products (fp32 operands, a.tf32 set): bytes of a.tws that K-major copies of the
+// M/N-major operands need, and the product itself (tensor cores on K-major copies, then
+// the residual / GELU / GELU' epilogue as an fp32 pass; exact fp32 SIMT if it cannot).
+size_t gemm_tf32_pack_bytes(int M, int N, int K, bool a_kmajor, bool b_kmajor);
+cudaError_t gemm_dispatch_tf32(const GemmArgs& a, float* ws, size_t ws_bytes, cudaStream_t s);
 
 // flags (may be null): device error flags, G2_FLAG_TIMEOUT is OR-ed in if a bounded
 // wait of the tensor-core kernel expires.

@@ -4,7 +4,9 @@
 
 namespace g2 {
 
-// True when the product's layout, alignment and sizes fit the tensor-core kernel.
+// True when the product's layout, alignment and sizes fit the tensor-core kernel: bf16
+// operands, or fp32 operands with tf32 set (then K-major only, fp32 output, store or bias
+// epilogue).
 bool gemm_tc_supported(const GemmArgs& a);
 // Workspace the kernel wants for split-K partial sums of an fp32-output product.
 size_t gemm_tc_workspace_bytes(int M, int N, int K);

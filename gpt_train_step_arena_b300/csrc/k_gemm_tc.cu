@@ -39,6 +39,12 @@ namespace g2 {
 namespace tc {
 
 constexpr int BM = 128, BK = 64, UMMA_K = 16;  // rows per MMA (one accumulator half)
+// With fp32 operands (TF32 products) a K block is the same 128 bytes per row: 32
+// elements, four MMAs of K = 8.
+template <bool TF> struct OperandT {
+    static constexpr int BKE = TF ? 32 : 64;   // elements per K block
+    static constexpr int UK = TF ? 8 : 16;     // K per MMA instruction
+};
 constexpr int GROUP_M = 8;     // tile order: m fastest within groups of GROUP_M row tiles
 
 // epilogues: bf16 store (+bias), GELU (two bf16 outputs), times GELU' of the pre-activation,
@@ -194,13 +200,15 @@ G2_DEV void stage_row(uint8_t* buf, int lane, const float* v) {
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int BN, int BMT, bool A_MN, bool B_MN, int EPI>
+template <int BN, int BMT, bool A_MN, bool B_MN, int EPI, bool TF = false>
 __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                    const __grid_constant__ CUtensorMap tmX, const Params p) {
     using CF = Cfg<BN, BMT, EPI>;
     using EO = EpiOut<EPI>;
+    using OT = OperandT<TF>;
+    static_assert(!TF || (!A_MN && !B_MN), "TF32 products take K-major operands only");
     constexpr int S = CF::STAGES, NB = CF::ACC_BUFS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -261,7 +269,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
                     uint8_t* sa = smem + stage * CF::STAGE_BYTES;
                     uint8_t* sb = sa + CF::A_BYTES;
                     mbar_expect_tx(&full_bar[stage], CF::STAGE_BYTES);
-                    const int k0 = kb * BK;
+                    const int k0 = kb * OT::BKE;
                     if (!A_MN) {
                         tma_load_2d(&tmA, &full_bar[stage], sa, k0, mb * BMT);
                     } else {
@@ -297,7 +305,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t IDESC = make_idesc(BN, A_MN, B_MN);
+            constexpr uint32_t IDESC = TF ? make_idesc_tf32(BN) : make_idesc(BN, A_MN, B_MN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -337,7 +345,12 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
                                 bd = sdesc(sb + k * UMMA_K * 2, 16, 1024);
                             else
                                 bd = sdesc(sb + k * UMMA_K * 128, 64 * BK * 2, 1024);
-                            umma_bf16(d_tmem + hh * BN, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                            // K-major: the k-th MMA's operands start 32 bytes further along the
+                            // 128-byte row (16 bf16 or 8 fp32)
+                            if (TF)
+                                umma_tf32(d_tmem + hh * BN, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                            else
+                                umma_bf16(d_tmem + hh * BN, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
                         }
                     }
                     issued_any = true;
@@ -543,11 +556,11 @@ static int num_sms() {
     return n;
 }
 
-template <int BN, int BMT, bool A_MN, bool B_MN, int EPI>
+template <int BN, int BMT, bool A_MN, bool B_MN, int EPI, bool TF = false>
 static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
                             const CUtensorMap& td2, const CUtensorMap& tx, const Params& p, cudaStream_t s) {
     using CF = Cfg<BN, BMT, EPI>;
-    auto kern = gemm_tc_kernel<BN, BMT, A_MN, B_MN, EPI>;
+    auto kern = gemm_tc_kernel<BN, BMT, A_MN, B_MN, EPI, TF>;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES);
@@ -575,6 +588,13 @@ static cudaError_t launch_layout(int bmt, bool a_mn, bool b_mn, const Maps& m, c
     if (!a_mn && b_mn) return launch_t<BN, 128, false, true, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
     if (a_mn && b_mn) return launch_t<BN, 128, true, true, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
     return launch_t<BN, 128, true, false, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
+}
+
+// TF32 products: K-major operands only, fp32 output (plain store or split-K partial).
+template <int BN, int EPI>
+static cudaError_t launch_tf32(int bmt, const Maps& m, const Params& p, cudaStream_t s) {
+    if (bmt == 256) return launch_t<BN, 256, false, false, EPI, true>(m.a, m.b, m.d, m.d2, m.x, p, s);
+    return launch_t<BN, 128, false, false, EPI, true>(m.a, m.b, m.d, m.d2, m.x, p, s);
 }
 
 }  // namespace tc
@@ -628,11 +648,12 @@ void gemm_tc_last_variant(char* out, size_t n) {
     snprintf(out, n, "%s", g_variant);
 }
 
-// Split-K plan for a product with few output tiles and a long K.
-static void plan(int M, int N, int K, int BN, int& splits, int& kb_per) {
+// Split-K plan for a product with few output tiles and a long K (bke: elements per K
+// block, 64 for bf16 operands, 32 for fp32 ones).
+static void plan(int M, int N, int K, int BN, int& splits, int& kb_per, int bke = BK) {
     const int bmt = tile_rows(M, N, K, BN);
     int tiles = ((M + bmt - 1) / bmt) * ((N + BN - 1) / BN);
-    int num_kb = (K + BK - 1) / BK;
+    int num_kb = (K + bke - 1) / bke;
     int sms = num_sms();
     splits = 1;
     if (tiles < sms && num_kb >= 8) {
@@ -672,10 +693,27 @@ size_t gemm_tc_skinny_workspace_bytes(int M, int N, int K) {
 size_t gemm_tc_workspace_bytes(int M, int N, int K) {
     int BN = N > 128 ? 256 : 128, splits, kb_per;
     plan(M, N, K, BN, splits, kb_per);
-    return splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+    size_t b = splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+    plan(M, N, K, BN, splits, kb_per, 32);  // the same product with fp32 (TF32) operands
+    return std::max(b, splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0);
+}
+
+// TF32 products (fp32 operands): both operands K-major, rows 16-byte aligned, fp32
+// output with a plain or bias epilogue (the dispatcher transposes operands and applies
+// the other epilogues around this kernel).
+bool gemm_tc_tf32_supported(const GemmArgs& a) {
+    if (a.in_type != ACT_F32 || !encode_fn()) return false;
+    if (a.M < 1 || a.N < 1 || a.K < 32) return false;
+    if (a.sAk != 1 || a.sBk != 1) return false;
+    if ((a.sAm % 4) || (a.sBn % 4) || !aligned16(a.A) || !aligned16(a.B)) return false;
+    if (!aligned16(a.D) || (a.ldd % 4)) return false;
+    if (a.epi != EPI_STORE || a.R || a.D2 || a.P) return false;
+    if (a.bias && !aligned16(a.bias)) return false;
+    return true;
 }
 
 bool gemm_tc_supported(const GemmArgs& a) {
+    if (a.in_type == ACT_F32) return a.tf32 && gemm_tc_tf32_supported(a);
     if (a.in_type != ACT_BF16 || !encode_fn()) return false;
     if (a.M < 1 || a.N < 1 || a.K < 16) return false;
     bool a_k = a.sAk == 1, b_k = a.sBk == 1;
@@ -695,7 +733,71 @@ bool gemm_tc_supported(const GemmArgs& a) {
     return true;
 }
 
+// D (fp32) = A . B^T (+ bias) with fp32 operands read as TF32.
+static cudaError_t gemm_tc_tf32(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, cudaStream_t s) {
+    const int BN = a.N > 128 ? 256 : 128;
+    const int bmt = tile_rows(a.M, a.N, a.K, BN);
+    constexpr int BKE = OperandT<true>::BKE;
+    Maps mp;
+    {
+        const uint64_t da[2] = {(uint64_t)a.K, (uint64_t)a.M}, sa[1] = {(uint64_t)a.sAm * 4};
+        const uint32_t ba[2] = {(uint32_t)BKE, (uint32_t)bmt};
+        const uint64_t db[2] = {(uint64_t)a.K, (uint64_t)a.N}, sb[1] = {(uint64_t)a.sBn * 4};
+        const uint32_t bb[2] = {(uint32_t)BKE, (uint32_t)BN};
+        if (!make_map_nd(&mp.a, a.A, true, 2, da, sa, ba) || !make_map_nd(&mp.b, a.B, true, 2, db, sb, bb))
+            return cudaErrorInvalidValue;
+    }
+    Params p{};
+    p.M = a.M; p.N = a.N; p.K = a.K;
+    p.tiles_m = (a.M + bmt - 1) / bmt;
+    p.tiles_n = (a.N + BN - 1) / BN;
+    p.num_kb = (a.K + BKE - 1) / BKE;
+    int splits = 1, kb_per = p.num_kb;
+    if (!a.bias) plan(a.M, a.N, a.K, BN, splits, kb_per, BKE);
+    if (splits > 1 && (!ws || ws_bytes < (size_t)splits * a.M * a.N * sizeof(float) || a.N % 4)) {
+        splits = 1;
+        kb_per = p.num_kb;
+    }
+    p.splits = splits;
+    p.kb_per_split = kb_per;
+    p.num_units = p.tiles_m * p.tiles_n * splits;
+    p.D = a.D; p.ldd = a.ldd; p.d_f32 = 1;
+    p.bias = a.bias;
+    p.ws = ws;
+    p.flags = flags ? flags : fallback_flag();
+    bool ok;
+    const uint32_t box_f32[2] = {32, 32};
+    if (splits > 1) {
+        const uint64_t dims[3] = {(uint64_t)a.N, (uint64_t)a.M, (uint64_t)splits};
+        const uint64_t st[2] = {(uint64_t)a.N * 4, (uint64_t)a.M * a.N * 4};
+        const uint32_t box3[3] = {32, 32, 1};
+        ok = make_map_nd(&mp.d, ws, true, 3, dims, st, box3);
+    } else {
+        const uint64_t dims[2] = {(uint64_t)a.N, (uint64_t)a.M};
+        const uint64_t st[1] = {(uint64_t)a.ldd * 4};
+        ok = make_map_nd(&mp.d, a.D, true, 2, dims, st, box_f32);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    mp.d2 = mp.d;
+    mp.x = mp.d;
+    {
+        std::lock_guard<std::mutex> lk(g_variant_mu);
+        snprintf(g_variant, sizeof g_variant, "rows=%d cols=%d splits=%d a=k b=k epi=store f32 tf32", bmt, BN,
+                 splits);
+    }
+    if (splits > 1) {
+        cudaError_t e = BN == 256 ? launch_tf32<256, E_PARTIAL>(bmt, mp, p, s) : launch_tf32<128, E_PARTIAL>(bmt, mp, p, s);
+        if (e != cudaSuccess) return e;
+        size_t n = (size_t)a.M * a.N;
+        unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
+        G2_LAUNCH splitk_reduce_k<<<blocks, 256, 0, s>>>((float*)a.D, a.ldd, ws, a.M, a.N, splits);
+        return cudaGetLastError();
+    }
+    return BN == 256 ? launch_tf32<256, E_STORE_F32>(bmt, mp, p, s) : launch_tf32<128, E_STORE_F32>(bmt, mp, p, s);
+}
+
 cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, cudaStream_t s) {
+    if (a.in_type == ACT_F32) return gemm_tc_tf32(a, ws, ws_bytes, flags, s);
     const bool a_mn = a.sAk != 1, b_mn = a.sBk != 1;
     const bool skinny = a.skinny_split && a.M <= 128 && a.epi != EPI_GELU_BWD;
     const int BN = skinny ? skinny_bn(a.M, a.N) : (a.N > 128 ? 256 : 128);

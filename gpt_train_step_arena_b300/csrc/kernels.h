@@ -121,6 +121,19 @@ cudaError_t gen_sample(ActType at, int32_t* ids, int32_t* out, const void* logit
 // dstate t0 and step += 1.
 cudaError_t gen_advance(int* dstate, cudaStream_t s);
 
+// ---- seeded initial parameters (llm.c §1.33 random_u32, §1.34 random_f32) ----------
+// Normal tensors in draw order: params + offset[k] receives n[k] values N(0, std[k]).
+struct InitPlan {
+    int count;
+    size_t offset[8];
+    size_t n[8];
+    double std[8];
+};
+// Fills the n_ones arrays ones[i] (ones_n[i] floats) with 1 and draws the plan's normal
+// tensors; everything else is left as it is (the caller zeroes it first).
+cudaError_t init_params_device(float* params, const InitPlan& plan, const float* const* ones, const size_t* ones_n,
+                               int n_ones, uint64_t seed, cudaStream_t s);
+
 // ---- GEMM --------------------------------------------------------------------------
 // D[m,n] = epilogue( sum_k A(m,k) * B(n,k) ), A(m,k) = A[m*sAm + k*sAk], B(n,k) = B[n*sBn + k*sBk].
 enum Epilogue {
@@ -141,6 +154,9 @@ struct GemmArgs {
     int epi;
     int* flags;                 // device error flags (G2_FLAG_TIMEOUT), or null
     int skinny_split;           // one row tile (M <= 128): split K, epilogue in the fixed-order reduce
+    int tf32;                   // fp32 operands: contract on the tensor cores as TF32 (else exact fp32)
+    float* tws;                 // TF32: workspace for K-major copies of M/N-major operands, or null
+    size_t tws_bytes;
 };
 cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t s);
 

@@ -60,6 +60,8 @@ struct gpt2 {
     char *dres, *dln, *datty, *dqkv, *dfch;
     float *attD, *ln_part, *cs_part, *gemm_ws;
     size_t gemm_ws_bytes;
+    float* tf32_ws;  // GPT2_TF32: K-major copies of the products' M/N-major operands
+    size_t tf32_ws_bytes;
     EncoderBwdScratch enc;
     bool logits_valid;
     // per-kernel-class timing (gpt2_profile_*): one event pair per launched op
@@ -154,6 +156,13 @@ static const void* pw(const gpt2* m, int t, size_t elem_off) {
 static char* act(const gpt2* m, char* base, size_t elems) { return base + elems * m->esz; }
 
 // ------------------------------------------------------------------ GEMM dispatch
+// TF32 mode: fp32 operands contracted on the tensor cores as TF32.
+static void tf32_args(const gpt2* m, GemmArgs& a) {
+    if (m->prec != GPT2_TF32) return;
+    a.tf32 = 1;
+    a.tws = m->tf32_ws;
+    a.tws_bytes = m->tf32_ws_bytes;
+}
 // Y[M,N] = X[M,K] . W[N,K]^T (+bias) (+R) with optional GELU epilogue.
 static cudaError_t gemm_fwd(gpt2* m, int M, int N, int K, const void* X, const void* W,
                             const float* bias, void* Y, const void* R, void* Y2) {
@@ -166,6 +175,7 @@ static cudaError_t gemm_fwd(gpt2* m, int M, int N, int K, const void* X, const v
     a.D2 = Y2; a.ldd2 = N;
     a.epi = Y2 ? EPI_GELU : EPI_STORE;
     a.flags = m->flags;
+    tf32_args(m, a);
     return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
 }
 // dX[M,K] = dY[M,N] . W[N,K]  (optionally times gelu'(P))
@@ -179,6 +189,7 @@ static cudaError_t gemm_dgrad(gpt2* m, int M, int N, int K, const void* dY, cons
     a.P = P; a.ldp = K;
     a.epi = P ? EPI_GELU_BWD : EPI_STORE;
     a.flags = m->flags;
+    tf32_args(m, a);
     return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
 }
 // dW[N,K] (fp32, overwritten) = dY[M,N]^T . X[M,K]
@@ -190,6 +201,7 @@ static cudaError_t gemm_wgrad(gpt2* m, int M, int N, int K, const void* dY, cons
     a.D = dW; a.ldd = K; a.d_f32 = 1;
     a.epi = EPI_STORE;
     a.flags = m->flags;
+    tf32_args(m, a);
     return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
 }
 
@@ -202,8 +214,8 @@ extern "C" gpt2_t* gpt2_build_norm(int L, int C, int H, int V, int maxT, int pre
     };
     if (L <= 0 || C <= 0 || H <= 0 || V <= 0 || maxT <= 0 || C % H)
         return bail(GPT2_ERR_ARG, "bad shape: need L,C,H,V,maxT > 0 and C % H == 0");
-    if (precision != GPT2_FP32 && precision != GPT2_BF16)
-        return bail(GPT2_ERR_ARG, "precision must be GPT2_FP32 or GPT2_BF16");
+    if (precision != GPT2_FP32 && precision != GPT2_TF32 && precision != GPT2_BF16)
+        return bail(GPT2_ERR_ARG, "precision must be GPT2_FP32, GPT2_TF32 or GPT2_BF16");
     if (norm != GPT2_LAYERNORM && norm != GPT2_RMSNORM)
         return bail(GPT2_ERR_ARG, "norm must be GPT2_LAYERNORM or GPT2_RMSNORM");
     if (C % 8) return bail(GPT2_ERR_ARG, "C must be a multiple of 8");
@@ -327,6 +339,26 @@ extern "C" int gpt2_set_params(gpt2_t* m, const float* host, size_t n) {
     return GPT2_OK;
 }
 
+extern "C" int gpt2_init_params(gpt2_t* m, uint64_t seed) {
+    if (!m) return GPT2_ERR_ARG;
+    const size_t L = m->L, C = m->C;
+    const double std = 0.02, proj_std = 0.02 / std::sqrt(2.0 * (double)L);
+    CK(cudaMemsetAsync(m->params, 0, m->npad * 4, m->stream));
+    InitPlan plan{};
+    const int normal[] = {P_WTE, P_WPE, P_QKVW, P_APW, P_FCW, P_FPW};
+    for (int t : normal) {
+        const int k = plan.count++;
+        plan.offset[k] = m->poff[t];
+        plan.n[k] = t == P_WTE ? (size_t)m->V * C : m->psize[t];   // real rows only: the padding stays 0
+        plan.std[k] = (t == P_APW || t == P_FPW) ? proj_std : std;
+    }
+    const float* ones[3] = {pf(m, m->params, P_LN1W), pf(m, m->params, P_LN2W), pf(m, m->params, P_LNFW)};
+    const size_t ones_n[3] = {L * C, L * C, C};
+    CK(init_params_device(m->params, plan, ones, ones_n, 3, seed, m->stream));
+    if (m->shadow) CK(cast_f32_to_bf16(m->shadow, m->params, m->npad, m->stream));
+    return GPT2_OK;
+}
+
 extern "C" int gpt2_get_params(gpt2_t* m, float* host, size_t n) {
     if (!m || !host) return fail(m, GPT2_ERR_ARG, "null argument");
     if (n != m->nreal) return fail(m, GPT2_ERR_ARG, "expected %zu parameters, got %zu", m->nreal, n);
@@ -353,12 +385,23 @@ static int alloc_acts(gpt2* m, int B, int T) {
     struct Item { void** slot; size_t bytes; };
     void *tok, *tgt, *flags, *loss, *losses, *res, *res2, *ln1, *qkv, *atty, *ln2, *fch, *fchg, *lnf,
         *logits, *ln1m, *ln1r, *ln2m, *ln2r, *lnfm, *lnfr, *lse, *dres, *dln, *datty, *dqkv, *dfch,
-        *attD, *lnp, *csp, *enc, *ws;
+        *attD, *lnp, *csp, *enc, *ws, *tws;
     size_t ln_part = ln_bwd_partial_floats(m->C) * 4;
     size_t maxN = std::max<size_t>(4 * C, (size_t)m->Vp);
     size_t cs_part = colsum_partial_floats((int)M, (int)maxN) * 4;
     size_t enc_bytes = encoder_bwd_scratch_bytes((int)M, m->V, m->C);
     m->gemm_ws_bytes = gemm_workspace_bytes((int)M, m->C, m->Vp, m->L);
+    // TF32: the largest set of operand copies of one product (the LM-head weight gradient
+    // packs dlogits^T and lnf^T; the input gradients pack a weight matrix)
+    m->tf32_ws_bytes = 0;
+    if (m->prec == GPT2_TF32) {
+        const int Mi = (int)M, Ci = m->C;
+        const int shapes[][2] = {{3 * Ci, Ci}, {Ci, Ci}, {4 * Ci, Ci}, {Ci, 4 * Ci}, {m->Vp, Ci}};
+        for (auto& sh : shapes) {  // (out, in) of a linear layer
+            m->tf32_ws_bytes = std::max(m->tf32_ws_bytes, gemm_tf32_pack_bytes(Mi, sh[1], sh[0], true, false));
+            m->tf32_ws_bytes = std::max(m->tf32_ws_bytes, gemm_tf32_pack_bytes(sh[0], sh[1], Mi, false, false));
+        }
+    }
     Item items[] = {
         {&tok, M * 4}, {&tgt, M * 4}, {&flags, 64}, {&loss, 64}, {&losses, M * 4},
         {&res, (L + 1) * M * C * es}, {&res2, L * M * C * es}, {&ln1, L * M * C * es},
@@ -368,7 +411,7 @@ static int alloc_acts(gpt2* m, int B, int T) {
         {&ln2m, L * M * 4}, {&ln2r, L * M * 4}, {&lnfm, M * 4}, {&lnfr, M * 4},
         {&lse, L * M * NH * 4}, {&dres, M * C * es}, {&dln, M * C * es}, {&datty, M * C * es},
         {&dqkv, M * 3 * C * es}, {&dfch, M * 4 * C * es}, {&attD, M * NH * 4}, {&lnp, ln_part},
-        {&csp, cs_part}, {&enc, enc_bytes}, {&ws, m->gemm_ws_bytes},
+        {&csp, cs_part}, {&enc, enc_bytes}, {&ws, m->gemm_ws_bytes}, {&tws, m->tf32_ws_bytes},
     };
     size_t total = 0;
     for (auto& it : items) total += align256(it.bytes);
@@ -398,6 +441,7 @@ static int alloc_acts(gpt2* m, int B, int T) {
     m->dres = (char*)dres; m->dln = (char*)dln; m->datty = (char*)datty; m->dqkv = (char*)dqkv;
     m->dfch = (char*)dfch; m->attD = (float*)attD; m->ln_part = (float*)lnp;
     m->cs_part = (float*)csp; m->gemm_ws = (float*)ws;
+    m->tf32_ws = m->tf32_ws_bytes ? (float*)tws : nullptr;
     encoder_bwd_scratch_carve(&m->enc, enc, (int)M, m->V, m->C);
     CK(cudaMemsetAsync(m->flags, 0, 64, m->stream));
     return GPT2_OK;

@@ -58,16 +58,37 @@ extern "C" int gpt2_op_bias_grad(int dtype, const void* dout, int M, int N, floa
                    "bias_grad");
 }
 
+extern "C" size_t gpt2_op_matmul_workspace(int dtype, int M, int N, int K, int a_kmajor, int b_kmajor) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    size_t b = gemm_tc_workspace_bytes(M, N, K);
+    if (dtype == GPT2_DT_TF32) b += gemm_tf32_pack_bytes(M, N, K, a_kmajor != 0, b_kmajor != 0);
+    return b;
+}
+
 extern "C" int gpt2_op_matmul(int dtype, int M, int N, int K, const void* A, long long lda,
                               int a_kmajor, const void* B, long long ldb, int b_kmajor, void* D,
                               long long ldd, int d_f32, const float* bias, void* workspace,
                               size_t workspace_bytes, void* stream) {
-    if (!dtype_ok(dtype)) return op_fail(GPT2_ERR_ARG, "matmul: bad dtype %d", dtype);
+    const bool tf32 = dtype == GPT2_DT_TF32;
+    if (!dtype_ok(dtype) && !tf32) return op_fail(GPT2_ERR_ARG, "matmul: bad dtype %d", dtype);
     if (M < 0 || N < 0 || K < 0) return op_fail(GPT2_ERR_ARG, "matmul: negative size");
     if (M == 0 || N == 0) return GPT2_OK;
     if (!A || !B || !D) return op_fail(GPT2_ERR_ARG, "matmul: null pointer");
     GemmArgs a{};
-    a.M = M; a.N = N; a.K = K; a.in_type = act_of(dtype);
+    a.M = M; a.N = N; a.K = K; a.in_type = tf32 ? ACT_F32 : act_of(dtype);
+    if (tf32) {
+        // the operand copies first, the split-K partials after them
+        const size_t pk = gemm_tf32_pack_bytes(M, N, K, a_kmajor != 0, b_kmajor != 0);
+        if (pk && (!workspace || workspace_bytes < pk))
+            return op_fail(GPT2_ERR_ARG, "matmul: TF32 needs %zu workspace bytes for operand copies", pk);
+        if ((uintptr_t)workspace & 255) return op_fail(GPT2_ERR_ARG, "matmul: workspace must be 256-byte aligned");
+        a.tf32 = 1;
+        a.tws = (float*)workspace;
+        a.tws_bytes = pk;
+        workspace = pk ? (void*)((char*)workspace + pk) : workspace;
+        workspace_bytes = workspace ? workspace_bytes - pk : 0;
+        d_f32 = 1;
+    }
     a.A = A;
     if (a_kmajor) { a.sAm = lda; a.sAk = 1; } else { a.sAm = 1; a.sAk = lda; }
     a.B = B;

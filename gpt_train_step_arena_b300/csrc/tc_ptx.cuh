@@ -162,6 +162,15 @@ G2_DEV void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t 
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
         : "memory");
 }
+// The same with fp32 operands read as TF32 (kind::tf32: K = 8 per instruction).
+G2_DEV void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
 G2_DEV void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
@@ -285,6 +294,11 @@ G2_DEV uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
 __host__ __device__ constexpr uint32_t make_idesc(int bn, bool a_mn, bool b_mn, int bm = 128) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
            ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(bm >> 4) << 24);
+}
+// Instruction descriptor of kind::tf32: fp32 accumulator, TF32 A and B (format 2), both
+// K-major, N and M.
+__host__ __device__ constexpr uint32_t make_idesc_tf32(int bn, int bm = 128) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(bm >> 4) << 24);
 }
 
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

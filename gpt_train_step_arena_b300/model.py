@@ -33,7 +33,7 @@ class GPT2:
 
     def __init__(self, L: int, C: int, H: int, V: int, maxT: int, precision: str = "bf16",
                  norm: str = "layernorm"):
-        prec = {"bf16": N.GPT2_BF16, "fp32": N.GPT2_FP32}[precision]
+        prec = {"bf16": N.GPT2_BF16, "fp32": N.GPT2_FP32, "tf32": N.GPT2_TF32}[precision]
         nk = {"layernorm": N.GPT2_LAYERNORM, "rmsnorm": N.GPT2_RMSNORM}[norm]
         st = ct.c_int(0)
         h = N.lib.gpt2_build_norm(L, C, H, V, maxT, prec, nk, ct.byref(st))
@@ -65,6 +65,10 @@ class GPT2:
     def set_params(self, flat: np.ndarray):
         flat = np.ascontiguousarray(flat, dtype=np.float32)
         self._check(N.lib.gpt2_set_params(self.h, _ptr(flat), flat.size))
+
+    def init_params(self, seed: int = 42):
+        """The seeded initial parameters, drawn on the device (gpt2_init_params)."""
+        self._check(N.lib.gpt2_init_params(self.h, seed))
 
     def params(self) -> np.ndarray:
         out = np.empty(self.n, np.float32)

@@ -38,14 +38,21 @@ def bias_grad(dout: torch.Tensor) -> torch.Tensor:
 
 
 def matmul(A: torch.Tensor, B: torch.Tensor, a_kmajor=True, b_kmajor=True, out_f32=False,
-           bias=None, workspace_bytes: int = 64 << 20) -> torch.Tensor:
-    """D = A(m,k) B(n,k)^T.  A is (M,K) if a_kmajor else (K,M); B is (N,K) if b_kmajor else (K,N)."""
+           bias=None, workspace_bytes: int = 64 << 20, tf32: bool = False) -> torch.Tensor:
+    """D = A(m,k) B(n,k)^T.  A is (M,K) if a_kmajor else (K,M); B is (N,K) if b_kmajor else (K,N).
+    tf32: fp32 operands contracted on the tensor cores as TF32 (fp32 output)."""
     M, K = (A.shape if a_kmajor else A.shape[::-1])
     Nn, K2 = (B.shape if b_kmajor else B.shape[::-1])
     assert K == K2 and A.dtype == B.dtype
+    dt = N.GPT2_DT_TF32 if tf32 else _dt(A)
+    if tf32:
+        assert A.dtype == torch.float32
+        out_f32 = True
+        workspace_bytes = max(workspace_bytes,
+                              N.lib.gpt2_op_matmul_workspace(dt, M, Nn, K, int(a_kmajor), int(b_kmajor)))
     D = torch.empty(M, Nn, dtype=torch.float32 if out_f32 else A.dtype, device=A.device)
     ws = torch.empty(workspace_bytes, dtype=torch.uint8, device=A.device) if workspace_bytes else None
-    _check(N.lib.gpt2_op_matmul(_dt(A), M, Nn, K, A.data_ptr(), A.stride(0), int(a_kmajor), B.data_ptr(),
+    _check(N.lib.gpt2_op_matmul(dt, M, Nn, K, A.data_ptr(), A.stride(0), int(a_kmajor), B.data_ptr(),
                                 B.stride(0), int(b_kmajor), D.data_ptr(), D.stride(0), int(out_f32),
                                 None if bias is None else bias.data_ptr(),
                                 None if ws is None else ws.data_ptr(), workspace_bytes, _stream()))

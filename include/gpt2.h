@@ -59,9 +59,13 @@ enum gpt2_status {
 
 /* Arithmetic of the step.
  * GPT2_FP32: every tensor fp32, fp32 arithmetic everywhere (no TF32).
+ * GPT2_TF32: every tensor fp32; the matrix products (llm.c §1.5 matmul_forward, §1.6
+ *            matmul_backward) run on the tensor cores with their fp32 operands read as
+ *            TF32 (10-bit mantissa) and fp32 accumulation; everything else as GPT2_FP32.
+ *            Held to the bf16 tolerances, not the fp32 ones.
  * GPT2_BF16: bf16 activations and matrix operands, fp32 accumulation, fp32 master
  *            parameters, gradients and AdamW moments (mixed precision). */
-enum gpt2_precision { GPT2_FP32 = 0, GPT2_BF16 = 2 };
+enum gpt2_precision { GPT2_FP32 = 0, GPT2_TF32 = 1, GPT2_BF16 = 2 };
 
 /* Where the id arrays of gpt2_forward_async live. */
 enum gpt2_memory { GPT2_HOST = 0, GPT2_DEVICE = 1 };
@@ -92,6 +96,17 @@ void gpt2_free(gpt2_t* m);
 size_t gpt2_num_params(const gpt2_t* m);
 /* Vocabulary rows held on the device (V rounded up to a multiple of 128). */
 int gpt2_padded_vocab(const gpt2_t* m);
+
+/* Seeded initial parameters, drawn on the device (the listing's random_u32 / random_f32,
+ * llm.c §1.33-§1.34, run as 65,536 xorshift64* lanes, lane j seeded with
+ * splitmix64(seed + j); draw i of a tensor from lane i % 65536, whole rounds per tensor):
+ * wte, wpe, qkvw, fcw ~ N(0, 0.02) and attprojw, fcprojw ~ N(0, 0.02/sqrt(2L)) by
+ * Box-Muller in double (u1 >= 1e-7) rounded once to fp32, drawn in that order; LayerNorm
+ * gains 1; biases, shifts and padded vocabulary rows 0.  Refreshes the bf16 weight copy;
+ * the AdamW moments are left as they are.  The values equal those of the seeded input
+ * generator the tests use (gpt_train_step_arena_b300.synth.init_params) up to the
+ * last-ulp rounding of the double log, cos and sin of the two sides.  Asynchronous. */
+int gpt2_init_params(gpt2_t* m, uint64_t seed);
 
 /* Copy n = gpt2_num_params() fp32 values in, or out, in the layout above.  set also
  * refreshes the bf16 weight copy.  Synchronising.  GPT2_ERR_ARG if n differs. */

@@ -23,7 +23,9 @@
 extern "C" {
 #endif
 
-enum gpt2_dtype { GPT2_DT_F32 = 0, GPT2_DT_BF16 = 1 };
+/* GPT2_DT_TF32 (gpt2_op_matmul only): fp32 operands and output, contracted on the tensor
+ * cores with the operands read as TF32 and fp32 accumulation. */
+enum gpt2_dtype { GPT2_DT_F32 = 0, GPT2_DT_BF16 = 1, GPT2_DT_TF32 = 2 };
 
 const char* gpt2_op_last_error(void);
 
@@ -70,6 +72,11 @@ size_t gpt2_op_bias_grad_noalloc_max_floats(void);
 int gpt2_op_matmul(int dtype, int M, int N, int K, const void* A, long long lda, int a_kmajor,
                    const void* B, long long ldb, int b_kmajor, void* D, long long ldd, int d_f32,
                    const float* bias, void* workspace, size_t workspace_bytes, void* stream);
+/* Workspace bytes gpt2_op_matmul can use for this product: split-K partial sums (optional:
+ * with less, the product is not split) and, for GPT2_DT_TF32, K-major copies of the
+ * operands given M- or N-major (required; the workspace must then be 256-byte aligned).
+ * With GPT2_DT_TF32, D is always fp32 (d_f32 is ignored). */
+size_t gpt2_op_matmul_workspace(int dtype, int M, int N, int K, int a_kmajor, int b_kmajor);
 
 /* The same product with the epilogues the training step fuses into it (llm.c §1.5
  * matmul_forward with §1.11 residual_forward or §1.9 gelu_forward; §1.6 with §1.10

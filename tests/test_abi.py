@@ -60,5 +60,5 @@ def test_build_rejects_bad_arguments_before_touching_the_device():
     assert st.value == N.GPT2_ERR_ARG and b"norm" in N.lib.gpt2_last_build_error()
     assert not N.lib.gpt2_build_norm(1, 16, 5, 27, 16, N.GPT2_FP32, N.GPT2_RMSNORM, ct.byref(st))  # C % H
     assert st.value == N.GPT2_ERR_ARG
-    assert not N.lib.gpt2_build_ex(1, 16, 4, 27, 16, 1, ct.byref(st))                 # unknown precision
+    assert not N.lib.gpt2_build_ex(1, 16, 4, 27, 16, 3, ct.byref(st))                 # unknown precision
     assert st.value == N.GPT2_ERR_ARG
