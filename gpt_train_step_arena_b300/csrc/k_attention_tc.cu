@@ -34,7 +34,7 @@ namespace atc {
 using namespace tc;
 
 constexpr int HS = 64, BQ = 128, BKV = 128, NTH = 192;
-constexpr int NTH_BWD = 320;  // backward: TMA warp, MMA warp, 8 softmax warps
+constexpr int NTH_BWD = 576;  // backward: TMA warp, MMA warp, two softmax groups of 8 warps
 constexpr int TILE = 128 * 64 * 2;  // 16 KB: 128 rows of one head, 128-byte rows
 constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 3 * TILE, OFF_P = 5 * TILE, OFF_BAR = 7 * TILE;
 constexpr uint32_t TMEM_COLS = 256, TM_S = 0, TM_O = 128;
@@ -333,77 +333,100 @@ __global__ void __launch_bounds__(NTH, 2)
 // ------------------------------------------------------------------ backward
 // llm.c §1.8 attention_backward, without atomics and without the (T, T) buffers: P is
 // rebuilt from the forward's log-sum-exp L and D = rowsum(dO * O), dS = P * (dP - D).
-// Two kernels of one template, 320 threads (TMA warp, MMA warp, 8 softmax warps: two per
-// tensor-memory lane quarter, each taking 32 of a half's 64 columns), two CTAs per SM:
-//   DQ = true   (query-major, runs first): the CTA owns 128 queries of one head and
-//               streams K_j and V_j for j <= the query tile.  Its softmax threads first
-//               compute D for their own rows (and store it for the other kernel); then
-//               S = Q K^T, dP = dO V^T, dS = P (dP - D), dQ += dS K.
-//   DQ = false  (key-major): the CTA owns 128 keys and streams Q_i and dO_i for i >= the
-//               key tile; S^T = K Q^T, dP^T = V dO^T, P^T and dS^T = P^T (dP^T - D) with
-//               L and D of the query columns staged in shared memory; dV += P^T dO,
-//               dK += dS^T Q.
-// Each streamed 128-row tile is processed in two 64-column halves through one tensor-
-// memory buffer (S at column 0, dP at 64); P and dS are written back (bf16) over the
-// columns each thread read and are the A operand of the accumulation products, which the
-// tensor core runs before the next half's S and dP overwrite the buffer.  A CTA's chain
-// (products -> softmax -> products) is serial; the second CTA on the SM fills the gaps:
-// one CTA per SM issues these 64-column products at about 85 clocks each, two reach
-// about 58 (the tensor core's own rate is 45-48).
-// Tensor memory (256 columns): the half buffer at 0-127, dQ (or dV) at 128, dK at 192; the
-// query-major CTA's own rows Q and dO (A operands of S and dP) at 192 and 224.  The key-
-// major CTA keeps K and V in shared memory instead.
+// Two persistent kernels of one template, one CTA per SM, 576 threads (a TMA warp, an MMA
+// warp, two softmax groups of 8 warps), each CTA looping over work items (a 128-row tile
+// of one (b, h)), heaviest first:
+//   DQ = true   (query-major, runs first): an item is 128 queries; it streams K_j and V_j
+//               for j <= the query tile: S = Q K^T, dP = dO V^T, dS = P (dP - D),
+//               dQ += dS K.  D of the item's rows is computed here and stored for the
+//               other kernel.
+//   DQ = false  (key-major): an item is 128 keys; it streams Q_i and dO_i for i >= the key
+//               tile, with L and D of the tile's queries copied next to them: S^T = K Q^T,
+//               dP^T = V dO^T, P^T and dS^T = P^T (dP^T - D); dV += P^T dO, dK += dS^T Q.
+// The item's own rows (Q and dO, or K and V) come by TMA into shared memory and are moved
+// by the first softmax group into tensor memory, where they are the A operand of S and
+// dP; P and dS are written back there as the A operand of the accumulation products, so
+// every MMA reads only its B operand from shared memory (64-column MMAs with A in shared
+// memory measured twice as long).  Each streamed 128-row tile is processed as two
+// 64-column halves; half g goes to tensor-memory buffer g % 2 (S at its column 0, dP at
+// 64) and to softmax group g % 2, whose 8 warps take 32 columns of a row each.  The MMA
+// warp keeps two halves' S and dP ahead of the softmax, and the work of consecutive items
+// overlaps: the TMA warp streams the next item's tiles as stages free up, the first group
+// moves the next item's rows into the second row buffer before the current item's
+// accumulators are drained, and the next item's S and dP start as soon as its rows are
+// in; only its first accumulation waits for the drain.
+// Tensor memory (512 columns): buffers at 0 and 128; accumulators at 256 (dQ, or dV) and
+// 320 (dK); two row buffers of 64 columns (the two A operands, 32 packed columns each) at
+// 384 and 448, by item parity.
+constexpr int BW_NS = 4;  // streamed-tile stages
 struct BwdBars {
-    uint64_t row_full, st_full[2], st_empty[2], sdp_full, pds_full, stats[2], acc_done, drain;
+    uint64_t rt_full, rt_empty, rows_full[2], st_full[BW_NS], st_empty[BW_NS], sdp_full[2], pds_full[2], acc_done,
+        acc_free, drain;
     uint32_t tmem_slot;
     int abort;
 };
-constexpr int B_ROWS = 0;                 // key-major: K, V tiles (32 KB)
-constexpr int B_ST = 2 * TILE;            // streamed stages: 2 x (A 16 KB + B 16 KB)
-constexpr int B_STATS = B_ST + 4 * TILE;  // key-major: L, D of 2 x 128 query columns
-constexpr int B_BAR = B_STATS + 2 * 2 * 128 * 4;
-constexpr int BWD_SMEM = B_BAR + (int)sizeof(BwdBars);
-constexpr uint32_t TB_COLS = 256, TB_ACC1 = 128, TB_ACC2 = 192, TB_RA = 192, TB_RB = 224;
+constexpr int BW_ST = 0;                                // stages: A 16 KB + B 16 KB each
+constexpr int BW_RT = BW_ST + BW_NS * 2 * TILE;         // the item's row tiles: Q|K, dO|V, O (query-major)
+constexpr int BW_STATS = BW_RT + 3 * TILE;              // key-major: per stage L[128], D[128] (raw L)
+constexpr int BW_RSTAT = BW_STATS + BW_NS * 2 * 128 * 4;  // query-major: the item's L slice [128] (raw)
+constexpr int BW_LD = BW_RSTAT + 128 * 4;               // query-major: [2 row sets][L2 128, D 128]
+constexpr int BW_BAR = BW_LD + 2 * 2 * 128 * 4;
+constexpr int BWD_SMEM = BW_BAR + (int)sizeof(BwdBars);
+constexpr uint32_t TB_COLS = 512, TB_ACC = 256, TB_ACC2 = 320, TB_ROWS = 384;
+
+struct BwdItem {
+    int rt, bh, b, h, row0, r0, st0, nst;
+};
+G2_DEV BwdItem bwd_item(bool dq, int w, int nbh, int ntiles, int T, int NH) {
+    BwdItem it;
+    const int rank = w / nbh;  // items of the heaviest row tile first
+    it.bh = w % nbh;
+    it.rt = dq ? ntiles - 1 - rank : rank;
+    it.b = it.bh / NH;
+    it.h = it.bh % NH;
+    it.row0 = it.b * T;
+    it.r0 = it.rt * 128;
+    it.st0 = dq ? 0 : it.rt;
+    it.nst = dq ? it.rt + 1 : ntiles - it.rt;
+    return it;
+}
 
 template <bool DQ>
-__global__ void __launch_bounds__(NTH_BWD, 2)
+__global__ void __launch_bounds__(NTH_BWD, 1)
     attn_bwd_tc_k(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-                  bf16* dqkv, const bf16* qkv, const bf16* dout, const bf16* outp, const float* lse, float* Dbuf,
-                  int T, int C, int NH, int* flags) {
+                  const __grid_constant__ CUtensorMap tm_o, bf16* dqkv, const float* lse, float* Dbuf, int T, int C,
+                  int NH, int nbh, int* flags) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    BwdBars* bar = reinterpret_cast<BwdBars*>(smem + B_BAR);
+    BwdBars* bar = reinterpret_cast<BwdBars*>(smem + BW_BAR);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (smem_u32(smem) & 1023) {
         if (threadIdx.x == 0 && flags) atomicOr(flags, G2_FLAG_TIMEOUT);
         return;
     }
-    const int ntiles_t = gridDim.x;
-    // the row tile: queries (heaviest = last first) or keys (heaviest = first first)
-    const int rt = DQ ? ntiles_t - 1 - (int)blockIdx.x : (int)blockIdx.x;
-    const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
-    const int row0 = b * T, r0 = rt * 128;
-    // streamed tiles: keys 0..rt (DQ) or queries rt..ntiles_t-1 (key-major)
-    const int st0 = DQ ? 0 : rt, nst = DQ ? rt + 1 : ntiles_t - rt;
-    const int xa_st = DQ ? C + h * HS : h * HS;      // K or Q (qkv map)
-    const int xb_st = DQ ? 2 * C + h * HS : h * HS;  // V (qkv map) or dO (its own map)
-    const CUtensorMap* map_b_st = DQ ? &tm_qkv : &tm_do;
+    const int ntiles = (T + 127) / 128, nitems = ntiles * nbh;
+    const uint32_t rt_bytes = (DQ ? 3 : 2) * TILE;
 
     if (threadIdx.x == 0) {
         bar->abort = 0;
-        mbar_init(&bar->row_full, DQ ? 8 : 1);  // softmax warps' tensor-memory rows, or TMA
+        mbar_init(&bar->rt_full, 1);
+        mbar_init(&bar->rt_empty, 8);       // the first group's warps, done with the row tiles
         for (int i = 0; i < 2; i++) {
+            mbar_init(&bar->rows_full[i], 8);  // the first group's warps: rows in tensor memory
+            mbar_init(&bar->sdp_full[i], 1);
+            mbar_init(&bar->pds_full[i], 8);
+        }
+        for (int i = 0; i < BW_NS; i++) {
             mbar_init(&bar->st_full[i], 1);
             mbar_init(&bar->st_empty[i], 1);
-            mbar_init(&bar->stats[i], 256);
         }
-        mbar_init(&bar->sdp_full, 1);
-        mbar_init(&bar->pds_full, 8);
         mbar_init(&bar->acc_done, 1);
+        mbar_init(&bar->acc_free, DQ ? 8 : 16);  // the warps that drain accumulators
         mbar_init(&bar->drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_async_smem();
         tma_prefetch_desc(&tm_qkv);
         tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_o);
     }
     if (warp == 1) tmem_alloc(&bar->tmem_slot, TB_COLS);
     tc_fence_before();
@@ -413,219 +436,281 @@ __global__ void __launch_bounds__(NTH_BWD, 2)
     volatile int* abort_flag = &bar->abort;
 
     if (warp == 0) {
-        // ---------------- TMA producer: the key-major CTA's K and V, then the streamed tiles
-        if (lane == 0) {
-            if (!DQ) {
-                mbar_expect_tx(&bar->row_full, 2 * TILE);
-                tma_load_2d(&tm_qkv, &bar->row_full, smem + B_ROWS, C + h * HS, row0 + r0);
-                tma_load_2d(&tm_qkv, &bar->row_full, smem + B_ROWS + TILE, 2 * C + h * HS, row0 + r0);
+        // ---------------- TMA producer: per item its row tiles, then its streamed tiles
+        // through the stage ring (lane 0 issues; all lanes copy statistics that a bulk
+        // copy cannot take: a ragged last tile or an unaligned slice)
+        int nt = 0;  // streamed tiles issued so far (stage ring position)
+        int iss_st[BW_NS];
+        for (int i = 0; i < BW_NS; i++) iss_st[i] = -1;
+        int iss_rt = -1;
+        bool ok = true;
+        for (int w = blockIdx.x, k = 0; ok && w < nitems; w += gridDim.x, k++) {
+            const BwdItem it = bwd_item(DQ, w, nbh, ntiles, T, NH);
+            const int xa = DQ ? C + it.h * HS : it.h * HS;      // streamed K or Q
+            const int xb = DQ ? 2 * C + it.h * HS : it.h * HS;  // streamed V (qkv) or dO (dout map)
+            const CUtensorMap* mb = DQ ? &tm_qkv : &tm_do;
+            // the item's rows, once the first group has released the previous item's
+            bool wt = true;
+            if (lane == 0) wt = mbar_wait(&bar->rt_empty, (k & 1) ^ 1, abort_flag, flags);
+            if (!__shfl_sync(0xffffffffu, wt, 0)) {
+                ok = false;
+                break;
             }
-            for (int n = 2; n < nst; n++) {
-                tma_prefetch_l2(&tm_qkv, xa_st, row0 + (st0 + n) * 128);
-                tma_prefetch_l2(map_b_st, xb_st, row0 + (st0 + n) * 128);
+            const size_t lrow = (size_t)it.bh * T + it.r0;  // first L of the item's rows
+            // a bulk copy needs a whole tile inside T and 16-byte aligned addresses
+            const bool rt_bulk = DQ && it.r0 + 128 <= T && ((uintptr_t)(lse + lrow) & 15) == 0;
+            if (DQ && !rt_bulk) {
+                float* rs = reinterpret_cast<float*>(smem + BW_RSTAT);
+                for (int i = lane; i < 128; i += 32) rs[i] = it.r0 + i < T ? lse[lrow + i] : INFINITY;
+                __syncwarp();
             }
-            int issued[2] = {-1, -1};
-            bool ok = true;
-            for (int n = 0; n < nst; n++) {
-                const int s = n & 1;
-                const uint32_t ph = (n >> 1) & 1;
-                if (!mbar_wait(&bar->st_empty[s], ph ^ 1, abort_flag, flags)) {
+            if (lane == 0) {
+                mbar_expect_tx(&bar->rt_full, rt_bytes + (rt_bulk ? 512u : 0u));
+                if (DQ) {
+                    tma_load_2d(&tm_qkv, &bar->rt_full, smem + BW_RT, it.h * HS, it.row0 + it.r0);          // Q
+                    tma_load_2d(&tm_do, &bar->rt_full, smem + BW_RT + TILE, it.h * HS, it.row0 + it.r0);    // dO
+                    tma_load_2d(&tm_o, &bar->rt_full, smem + BW_RT + 2 * TILE, it.h * HS, it.row0 + it.r0); // O
+                    if (rt_bulk) bulk_load_1d(smem + BW_RSTAT, lse + lrow, 512, &bar->rt_full);
+                } else {
+                    tma_load_2d(&tm_qkv, &bar->rt_full, smem + BW_RT, C + it.h * HS, it.row0 + it.r0);        // K
+                    tma_load_2d(&tm_qkv, &bar->rt_full, smem + BW_RT + TILE, 2 * C + it.h * HS, it.row0 + it.r0);  // V
+                }
+                iss_rt = k & 1;
+                for (int n = BW_NS; n < it.nst; n++) {
+                    tma_prefetch_l2(&tm_qkv, xa, it.row0 + (it.st0 + n) * 128);
+                    tma_prefetch_l2(mb, xb, it.row0 + (it.st0 + n) * 128);
+                }
+            }
+            for (int n = 0; n < it.nst; n++, nt++) {
+                const int s = nt % BW_NS;
+                const uint32_t ph = (nt / BW_NS) & 1;
+                bool w2 = true;
+                if (lane == 0) w2 = mbar_wait(&bar->st_empty[s], ph ^ 1, abort_flag, flags);
+                if (!__shfl_sync(0xffffffffu, w2, 0)) {
                     ok = false;
                     break;
                 }
-                mbar_expect_tx(&bar->st_full[s], 2 * TILE);
-                uint8_t* st = smem + B_ST + s * 2 * TILE;
-                tma_load_2d(&tm_qkv, &bar->st_full[s], st, xa_st, row0 + (st0 + n) * 128);
-                tma_load_2d(map_b_st, &bar->st_full[s], st + TILE, xb_st, row0 + (st0 + n) * 128);
-                issued[s] = (int)ph;
-            }
-            if (!ok) {
-                unsigned long long t0 = globaltimer();
-                if (!DQ) {
-                    while (!mbar_try_wait(&bar->row_full, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+                const int q0 = (it.st0 + n) * 128;
+                const size_t qrow = (size_t)it.bh * T + q0;
+                const bool st_bulk = !DQ && q0 + 128 <= T && ((uintptr_t)(lse + qrow) & 15) == 0 &&
+                                     ((uintptr_t)(Dbuf + qrow) & 15) == 0;
+                float* Ls = reinterpret_cast<float*>(smem + BW_STATS) + s * 256;
+                if (!DQ && !st_bulk) {
+                    // L and D of the tile's queries; absent ones get L = +inf (P = 0)
+                    for (int i = lane; i < 128; i += 32) {
+                        Ls[i] = q0 + i < T ? lse[qrow + i] : INFINITY;
+                        Ls[128 + i] = q0 + i < T ? Dbuf[qrow + i] : 0.f;
                     }
+                    __syncwarp();  // the statistics are written before lane 0 arrives
                 }
-                for (int s = 0; s < 2; s++) {
-                    if (issued[s] < 0) continue;
-                    t0 = globaltimer();
-                    while (!mbar_try_wait(&bar->st_full[s], (uint32_t)issued[s]) && globaltimer() - t0 < TIMEOUT_NS) {
+                if (lane == 0) {
+                    mbar_expect_tx(&bar->st_full[s], 2 * TILE + (st_bulk ? 1024u : 0u));
+                    uint8_t* st = smem + BW_ST + s * 2 * TILE;
+                    tma_load_2d(&tm_qkv, &bar->st_full[s], st, xa, it.row0 + q0);
+                    tma_load_2d(mb, &bar->st_full[s], st + TILE, xb, it.row0 + q0);
+                    if (st_bulk) {
+                        bulk_load_1d(Ls, lse + qrow, 512, &bar->st_full[s]);
+                        bulk_load_1d(Ls + 128, Dbuf + qrow, 512, &bar->st_full[s]);
                     }
+                    iss_st[s] = (int)ph;
+                }
+            }
+        }
+        if (!ok && lane == 0) {  // wait (bounded) for the copies still in flight before leaving
+            unsigned long long t0 = globaltimer();
+            if (iss_rt >= 0) {
+                while (!mbar_try_wait(&bar->rt_full, (uint32_t)iss_rt) && globaltimer() - t0 < TIMEOUT_NS) {
+                }
+            }
+            for (int s = 0; s < BW_NS; s++) {
+                if (iss_st[s] < 0) continue;
+                t0 = globaltimer();
+                while (!mbar_try_wait(&bar->st_full[s], (uint32_t)iss_st[s]) && globaltimer() - t0 < TIMEOUT_NS) {
                 }
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
+        // ---------------- MMA issuer: the whole warp runs the loop converged, one elected
+        // lane issues (see umma_bf16_ts_w)
+        {
             constexpr uint32_t ID_SDP = make_idesc(64, false, false);  // N = 64 streamed rows
             constexpr uint32_t ID_ACC = make_idesc(HS, false, true);   // N = 64, streamed operand MN-major
             const uint32_t sbase = smem_u32(smem);
-            const int nhalves = 2 * nst;
-            bool ok = mbar_wait(&bar->row_full, 0, abort_flag, flags);
-            bool issued_any = false;
-            // S and dP of half g (tile g/2, columns 64 (g%2) ..): A = the CTA's rows (tensor
-            // memory, or shared memory for K and V), B = the streamed rows of the half
-            auto issue_sdp = [&](int g) -> bool {
-                const int n = g >> 1, hh = g & 1, s = n & 1;
-                if (hh == 0 && !mbar_wait(&bar->st_full[s], (n >> 1) & 1, abort_flag, flags)) return false;
-                tc_fence_after();
-                const uint32_t sA = sbase + B_ST + s * 2 * TILE + hh * 8192, sB = sA + TILE;
-#pragma unroll
-                for (int k = 0; k < HS / 16; k++) {
-                    const uint64_t bd = sdesc(sA + k * 32, 16, 1024);
-                    if (DQ)
-                        umma_bf16_ts(tmem, tmem + TB_RA + k * 8, bd, ID_SDP, k > 0 ? 1u : 0u);
-                    else
-                        umma_bf16(tmem, sdesc(sbase + B_ROWS + k * 32, 16, 1024), bd, ID_SDP, k > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int k = 0; k < HS / 16; k++) {
-                    const uint64_t bd = sdesc(sB + k * 32, 16, 1024);
-                    if (DQ)
-                        umma_bf16_ts(tmem + 64, tmem + TB_RB + k * 8, bd, ID_SDP, k > 0 ? 1u : 0u);
-                    else
-                        umma_bf16(tmem + 64, sdesc(sbase + B_ROWS + TILE + k * 32, 16, 1024), bd, ID_SDP,
-                                  k > 0 ? 1u : 0u);
-                }
-                umma_commit(&bar->sdp_full);
-                issued_any = true;
-                return true;
+            bool ok = true, issued_any = false;
+            // every lane waits; a failure in any lane fails the warp
+            auto wait_all = [&](uint64_t* b, uint32_t par) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(b, par, abort_flag, flags));
             };
-            if (ok) ok = issue_sdp(0);
-            for (int g = 0; ok && g < nhalves; g++) {
-                const int n = g >> 1, hh = g & 1, s = n & 1;
-                if (!mbar_wait(&bar->pds_full, g & 1, abort_flag, flags)) {
+            int nt = 0;  // streamed tiles before this item
+            for (int w = blockIdx.x, k = 0; ok && w < nitems; w += gridDim.x, k++) {
+                const BwdItem it = bwd_item(DQ, w, nbh, ntiles, T, NH);
+                const int nh = 2 * it.nst;
+                const uint32_t rows = tmem + TB_ROWS + (uint32_t)(k & 1) * 64;
+                if (!wait_all(&bar->rows_full[k & 1], (k >> 1) & 1)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                // accumulation of half g: A = P or dS in tensor memory (column group c of the
-                // half at 32c, 16 columns = 32 rows of the contraction each), B = the
-                // streamed rows of the half read N-major (64 hs wide)
-                const uint32_t sA = sbase + B_ST + s * 2 * TILE + hh * 8192, sB = sA + TILE;
+                // S and dP of half g (tile g/2, its 64 rows from 64 (g%2)) into buffer g%2:
+                // A = the item's rows in tensor memory, B = the half's rows (K-major)
+                auto issue_sdp = [&](int g) -> bool {
+                    const int tn = nt + (g >> 1), hh = g & 1, s = tn % BW_NS;
+                    const uint32_t buf = tmem + (uint32_t)(g & 1) * 128;
+                    if (hh == 0 && !wait_all(&bar->st_full[s], (tn / BW_NS) & 1)) return false;
+                    tc_fence_after();
+                    const uint32_t sA = sbase + BW_ST + s * 2 * TILE + hh * 8192, sB = sA + TILE;
 #pragma unroll
-                for (int k = 0; k < 64 / 16; k++) {
-                    const uint32_t acc = (g > 0 || k > 0) ? 1u : 0u;
-                    const uint32_t a_off = (k >> 1) * 32 + (k & 1) * 8;
-                    const uint64_t bA = sdesc(sA + k * 2048, 8192, 1024);
-                    if (DQ) {
-                        umma_bf16_ts(tmem + TB_ACC1, tmem + 64 + a_off, bA, ID_ACC, acc);  // dQ += dS K
-                    } else {
-                        const uint64_t bB = sdesc(sB + k * 2048, 8192, 1024);
-                        umma_bf16_ts(tmem + TB_ACC1, tmem + a_off, bB, ID_ACC, acc);       // dV += P^T dO
-                        umma_bf16_ts(tmem + TB_ACC2, tmem + 64 + a_off, bA, ID_ACC, acc);  // dK += dS^T Q
+                    for (int kk = 0; kk < HS / 16; kk++)
+                        umma_bf16_ts_w(buf, rows + kk * 8, sdesc(sA + kk * 32, 16, 1024), ID_SDP, kk > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < HS / 16; kk++)
+                        umma_bf16_ts_w(buf + 64, rows + 32 + kk * 8, sdesc(sB + kk * 32, 16, 1024), ID_SDP,
+                                       kk > 0 ? 1u : 0u);
+                    umma_commit_w(&bar->sdp_full[g & 1]);
+                    issued_any = true;
+                    return true;
+                };
+                // the half counter of sdp_full / pds_full phases runs on across items: every
+                // item has an even number of halves, so half g of any item uses buffer g % 2
+                const int G = 2 * nt;
+                ok = issue_sdp(0) && issue_sdp(1);
+                for (int g = 0; ok && g < nh; g++) {
+                    const int tn = nt + (g >> 1), hh = g & 1, s = tn % BW_NS;
+                    if (!wait_all(&bar->pds_full[g & 1], ((G + g) >> 1) & 1) ||
+                        (g == 0 && k > 0 && !wait_all(&bar->acc_free, (k - 1) & 1))) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    // accumulation of half g: A = P or dS in the buffer (8 packed columns = 16
+                    // rows of the contraction per MMA), B = the half's rows read N-major
+                    const uint32_t buf = tmem + (uint32_t)(g & 1) * 128;
+                    const uint32_t sA = sbase + BW_ST + s * 2 * TILE + hh * 8192, sB = sA + TILE;
+#pragma unroll
+                    for (int kk = 0; kk < 64 / 16; kk++) {
+                        const uint32_t acc = (g > 0 || kk > 0) ? 1u : 0u;
+                        const uint32_t a_off = (kk >> 1) * 32 + (kk & 1) * 8;  // column group kk/2, packed 8 (kk%2)
+                        const uint64_t bA = sdesc(sA + kk * 2048, 8192, 1024);
+                        if (DQ) {
+                            umma_bf16_ts_w(tmem + TB_ACC, buf + 64 + a_off, bA, ID_ACC, acc);  // dQ += dS K
+                        } else {
+                            const uint64_t bB = sdesc(sB + kk * 2048, 8192, 1024);
+                            umma_bf16_ts_w(tmem + TB_ACC, buf + a_off, bB, ID_ACC, acc);        // dV += P^T dO
+                            umma_bf16_ts_w(tmem + TB_ACC2, buf + 64 + a_off, bA, ID_ACC, acc);  // dK += dS^T Q
+                        }
+                    }
+                    if (hh == 1) umma_commit_w(&bar->st_empty[s]);  // both halves of the tile are done with it
+                    if (g == nh - 1) umma_commit_w(&bar->acc_done);
+                    // the buffer of half g+2 is that of half g, whose accumulation was issued just now
+                    if (g + 2 < nh && !issue_sdp(g + 2)) ok = false;
                 }
-                issued_any = true;
-                if (hh == 1) umma_commit(&bar->st_empty[s]);
-                if (g == nhalves - 1) umma_commit(&bar->acc_done);
-                // the next half's S and dP follow this accumulation on the tensor core
-                if (g + 1 < nhalves && !issue_sdp(g + 1)) ok = false;
+                nt += it.nst;
             }
             if (!ok && issued_any) {
-                umma_commit(&bar->drain);
-                unsigned long long t0 = globaltimer();
-                while (!mbar_try_wait(&bar->drain, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+                umma_commit_w(&bar->drain);
+                if (lane == 0) {
+                    unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(&bar->drain, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+                    }
                 }
+                __syncwarp();
             }
         }
     } else {
-        // ---------------- softmax warps 2..9: thread = row of the CTA's tile; warps 2-5
-        // take columns 0-31 of each half, warps 6-9 columns 32-63
-        const int quarter = warp & 3, r = quarter * 32 + lane, sub = (warp - 2) >> 2;
-        const int grow = r0 + r;  // query (DQ) or key position of this thread's row
+        // ---------------- softmax groups: warps 2-9 take the first 64 columns of every
+        // streamed tile (even halves), warps 10-17 the second (odd halves); thread = row,
+        // sub = which 32 of the half's 64 columns
+        const int grp = (warp - 2) >> 3, sub = ((warp - 2) >> 2) & 1;
+        const int quarter = warp & 3, r = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = LOG2E / sqrtf((float)HS);
-        float L2_row = 0.f, D_row = 0.f;
-        float* Ls = reinterpret_cast<float*>(smem + B_STATS);  // [2][128] (key-major only)
-        float* Dsm = Ls + 2 * 128;
-        float nL = 0.f, nD = 0.f;  // key-major: this thread's query column of the next tile
-        if (DQ) {
-            // this row's Q (group 0) or dO (group 1) into tensor memory: the A operands of S
-            // and dP, 64 bf16 = 32 packed columns
-            {
-                uint32_t rv[32];
-                const bf16* src = sub == 0 ? qkv + (size_t)(row0 + grow) * 3 * C + h * HS
-                                           : dout + (size_t)(row0 + grow) * C + h * HS;
-#pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    const uint4 u = grow < T ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0, 0, 0, 0);
-                    rv[4 * i] = u.x;
-                    rv[4 * i + 1] = u.y;
-                    rv[4 * i + 2] = u.z;
-                    rv[4 * i + 3] = u.w;
-                }
-                tmem_st32u(tmem + lane_off + (sub == 0 ? TB_RA : TB_RB), rv);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar->row_full);
-            }
-            // D = rowsum(dO * O) for this row (both column groups need it; group 0 stores
-            // it for the key-major kernel)
-            if (grow < T) {
-                const bf16* dor = dout + (size_t)(row0 + grow) * C + h * HS;
-                const bf16* orr = outp + (size_t)(row0 + grow) * C + h * HS;
-                float acc = 0.f;
-#pragma unroll
-                for (int i = 0; i < HS; i += 8) {
-                    float a8[8], c8[8];
-                    Vec8<bf16>::load(dor + i, a8);
-                    Vec8<bf16>::load(orr + i, c8);
-#pragma unroll
-                    for (int e = 0; e < 8; e++) acc += a8[e] * c8[e];
-                }
-                D_row = acc;
-                if (sub == 0) Dbuf[(size_t)bh * T + grow] = acc;
-                L2_row = lse[(size_t)bh * T + grow] * LOG2E;
-            }
-        } else if (sub == 0) {
-            const int q = st0 * 128 + r;
-            nL = q < T ? lse[(size_t)bh * T + q] * LOG2E : INFINITY;  // absent queries: P = 0
-            nD = q < T ? Dbuf[(size_t)bh * T + q] : 0.f;
-        }
+        float* LDs = reinterpret_cast<float*>(smem + BW_LD);  // [set][L2 | D][128]
         bool ok = true;
-        for (int n = 0; n < nst && ok; n++) {
-            const int slot = n & 1;
-            if (!DQ) {
-                // column group 0 writes one query column's L and D each; everyone waits
-                // (bounded) until all have: slot n&1 was last read in tile n-2, which every
-                // thread finished before arriving for tile n-1
+        // The first group moves item k's rows into row buffer k%2 (and, query-major, computes
+        // L and D of the rows), then releases the row tiles and announces the rows.
+        auto prep_rows = [&](int w, int k) -> bool {
+            const BwdItem it = bwd_item(DQ, w, nbh, ntiles, T, NH);
+            bool okp = mbar_wait(&bar->rt_full, k & 1, abort_flag, flags);
+            if (!__all_sync(0xffffffffu, okp)) return false;
+            const uint8_t* src = smem + BW_RT + sub * TILE + r * 128;  // row r of tile sub, 128-byte swizzle
+            uint32_t rv[32];
+#pragma unroll
+            for (int c = 0; c < 8; c++) {
+                const uint4 u = *reinterpret_cast<const uint4*>(src + ((c ^ (r & 7)) << 4));
+                rv[4 * c] = u.x;
+                rv[4 * c + 1] = u.y;
+                rv[4 * c + 2] = u.z;
+                rv[4 * c + 3] = u.w;
+            }
+            tmem_st32u(tmem + lane_off + TB_ROWS + (uint32_t)(k & 1) * 64 + sub * 32, rv);
+            if (DQ) {
+                // D = rowsum(dO * O) of row r from the staged rows (both subs of the row
+                // compute it: no exchange, so no barrier a stalled warp could hold up)
+                const uint8_t* dor = smem + BW_RT + TILE + r * 128;
+                const uint8_t* orr = smem + BW_RT + 2 * TILE + r * 128;
+                float D = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    float a8[8], c8[8];
+                    Vec8<bf16>::load(reinterpret_cast<const bf16*>(dor + ((c ^ (r & 7)) << 4)), a8);
+                    Vec8<bf16>::load(reinterpret_cast<const bf16*>(orr + ((c ^ (r & 7)) << 4)), c8);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) D += a8[e] * c8[e];
+                }
+                const float Lraw = reinterpret_cast<const float*>(smem + BW_RSTAT)[r];
+                const int q = it.r0 + r;
                 if (sub == 0) {
-                    Ls[slot * 128 + r] = nL;
-                    Dsm[slot * 128 + r] = nD;
-                }
-                mbar_arrive(&bar->stats[slot]);
-                ok = mbar_wait(&bar->stats[slot], (n >> 1) & 1, abort_flag, flags);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                if (sub == 0 && n + 1 < nst) {
-                    const int q = (st0 + n + 1) * 128 + r;
-                    nL = q < T ? lse[(size_t)bh * T + q] * LOG2E : INFINITY;
-                    nD = q < T ? Dbuf[(size_t)bh * T + q] : 0.f;
+                    float* ld = LDs + (k & 1) * 256;
+                    ld[r] = q < T ? Lraw * LOG2E : INFINITY;  // rows past T: P = 0
+                    ld[128 + r] = q < T ? D : 0.f;
+                    if (q < T) Dbuf[(size_t)it.bh * T + q] = D;
                 }
             }
-            const bool diag = (st0 + n) == rt;
-            for (int hh = 0; hh < 2; hh++) {
-                const int g = 2 * n + hh;
-                ok = mbar_wait(&bar->sdp_full, g & 1, abort_flag, flags);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bar->rt_empty);
+                mbar_arrive(&bar->rows_full[k & 1]);
+            }
+            return true;
+        };
+        if (grp == 0 && blockIdx.x < nitems) ok = prep_rows(blockIdx.x, 0);
+        int nt = 0;
+        for (int w = blockIdx.x, k = 0; w < nitems; w += gridDim.x, k++) {
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const BwdItem it = bwd_item(DQ, w, nbh, ntiles, T, NH);
+            const int nh = 2 * it.nst, G = 2 * nt;
+            float L2_row = INFINITY, D_row = 0.f;  // query-major: this row's L (log2 units) and D
+            if (DQ) {
+                ok = mbar_wait(&bar->rows_full[k & 1], (k >> 1) & 1, abort_flag, flags);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                L2_row = LDs[(k & 1) * 256 + r];
+                D_row = LDs[(k & 1) * 256 + 128 + r];
+            }
+            for (int g = grp; g < nh; g += 2) {
+                const int n = g >> 1, tn = nt + n, s = tn % BW_NS;
+                ok = mbar_wait(&bar->sdp_full[g & 1], ((G + g) >> 1) & 1, abort_flag, flags);
+                // key-major: the stage's statistics (already complete; the wait orders the reads)
+                if (!DQ && ok) ok = mbar_wait(&bar->st_full[s], (tn / BW_NS) & 1, abort_flag, flags);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const bool diag = (it.st0 + n) == it.rt;
+                const uint32_t tb = tmem + lane_off + (uint32_t)(g & 1) * 128 + sub * 32;
+                const float* Ls = reinterpret_cast<const float*>(smem + BW_STATS) + s * 256 + grp * 64 + sub * 32;
+                const float* Ds = Ls + 128;
                 // 32 columns in two rounds of 16: S and dP in, P and dS (8 packed columns
                 // each) written back over the first half of what this thread read
 #pragma unroll
                 for (int rd = 0; rd < 2; rd++) {
-                    uint32_t sv[16], dv[16];
-                    const uint32_t tS = tmem + lane_off + sub * 32 + rd * 16;
-                    tmem_ld16_raw(tS, sv);
-                    tmem_ld16_raw(tS + 64, dv);
-                    tmem_wait_ld();
+                    uint32_t v[32];  // [0, 16) S, [16, 32) dP
+                    tmem_ld16_raw(tb + rd * 16, v);
+                    tmem_ld16_raw(tb + 64 + rd * 16, v + 16);
+                    tmem_wait_ld_tied32(v);
                     uint32_t pk[8], dk[8];
-                    const int cbase = hh * 64 + sub * 32 + rd * 16;  // column within the streamed tile
+                    const int cbase = grp * 64 + sub * 32 + rd * 16;  // column within the streamed tile
 #pragma unroll
                     for (int c4 = 0; c4 < 16; c4 += 4) {
                         float Lc[4], Dc[4];
@@ -636,9 +721,9 @@ __global__ void __launch_bounds__(NTH_BWD, 2)
                                 Dc[e] = D_row;
                             }
                         } else {
-                            const float4 l4 = *reinterpret_cast<const float4*>(Ls + slot * 128 + cbase + c4);
-                            const float4 d4 = *reinterpret_cast<const float4*>(Dsm + slot * 128 + cbase + c4);
-                            Lc[0] = l4.x; Lc[1] = l4.y; Lc[2] = l4.z; Lc[3] = l4.w;
+                            const float4 l4 = *reinterpret_cast<const float4*>(Ls + rd * 16 + c4);
+                            const float4 d4 = *reinterpret_cast<const float4*>(Ds + rd * 16 + c4);
+                            Lc[0] = l4.x * LOG2E; Lc[1] = l4.y * LOG2E; Lc[2] = l4.z * LOG2E; Lc[3] = l4.w * LOG2E;
                             Dc[0] = d4.x; Dc[1] = d4.y; Dc[2] = d4.z; Dc[3] = d4.w;
                         }
                         float pv[4], dsv[4];
@@ -647,51 +732,59 @@ __global__ void __launch_bounds__(NTH_BWD, 2)
                             const int c = cbase + c4 + e;
                             // causal: key <= query; DQ rows are queries, key-major rows are keys
                             const bool vis = !diag || (DQ ? c <= r : r <= c);
-                            const float pr = vis ? ex2(fmaf(__uint_as_float(sv[c4 + e]), sl2, -Lc[e])) : 0.f;
+                            const float pr = vis ? ex2(fmaf(__uint_as_float(v[c4 + e]), sl2, -Lc[e])) : 0.f;
                             pv[e] = pr;
-                            dsv[e] = pr * (__uint_as_float(dv[c4 + e]) - Dc[e]);
+                            dsv[e] = pr * (__uint_as_float(v[16 + c4 + e]) - Dc[e]);
                         }
                         pk[c4 >> 1] = pack_bf16x2(pv[0], pv[1]);
                         pk[(c4 >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
                         dk[c4 >> 1] = pack_bf16x2(dsv[0], dsv[1]);
                         dk[(c4 >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
                     }
-                    // packed columns 8 rd .. 8 rd + 7 of this group's 16 (all already read)
-                    const uint32_t tP = tmem + lane_off + sub * 32 + rd * 8;
-                    if (!DQ) tmem_st8(tP, pk);
-                    tmem_st8(tP + 64, dk);
+                    // packed columns 8 rd .. 8 rd + 7 of this thread's 32: already read
+                    if (!DQ) tmem_st8(tb + 8 * rd, pk);
+                    tmem_st8(tb + 64 + 8 * rd, dk);
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar->pds_full);
+                if (lane == 0) mbar_arrive(&bar->pds_full[g & 1]);
             }
-        }
-        if (ok) {
-            ok = mbar_wait(&bar->acc_done, 0, abort_flag, flags);
-            if (__all_sync(0xffffffffu, ok)) {
-                tc_fence_after();
+            if (!__all_sync(0xffffffffu, ok)) break;
+            // the next item's rows go into the other row buffer now (its S and dP can start
+            // while this item's accumulators drain); that buffer's last reader was the item
+            // before this one, all of whose products completed before its drain
+            if (grp == 0 && w + (int)gridDim.x < nitems) {
+                ok = prep_rows(w + gridDim.x, k + 1);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            ok = mbar_wait(&bar->acc_done, k & 1, abort_flag, flags);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            // DQ: group 0 stores dQ (32 columns per sub); key-major: group 0 dV, group 1 dK
+            if (!DQ || grp == 0) {
+                const int grow = it.r0 + r;
                 const float scale = 1.0f / sqrtf((float)HS);
-                bf16* base = dqkv + (size_t)(row0 + grow) * 3 * C + h * HS;
-                // DQ: group g stores dQ columns 32g..32g+31; key-major: group 0 dV, group 1 dK
-                const int ncol = DQ ? 32 : 64;
-                bf16* dst = DQ ? base + sub * 32 : (sub ? base + C : base + 2 * C);
-                const float mul = (DQ || sub) ? scale : 1.0f;
-                const uint32_t t0 = tmem + lane_off + (DQ ? TB_ACC1 + sub * 32 : (sub ? TB_ACC2 : TB_ACC1));
-                for (int c0 = 0; c0 < ncol; c0 += 32) {
-                    float a[32];
-                    tmem_ld32(t0 + c0, a);
-                    if (grow < T) {
+                bf16* base = dqkv + (size_t)(it.row0 + grow) * 3 * C + it.h * HS;
+                bf16* dst = DQ ? base : (grp ? base + C : base + 2 * C);
+                const float mul = (DQ || grp) ? scale : 1.0f;
+                const uint32_t t0 = tmem + lane_off + (DQ ? TB_ACC : (grp ? TB_ACC2 : TB_ACC)) + sub * 32;
+                float a[32];
+                tmem_ld32(t0, a);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->acc_free);  // the accumulator columns are read
+                if (grow < T) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 8) {
-                            float y[8];
+                    for (int i = 0; i < 32; i += 8) {
+                        float y[8];
 #pragma unroll
-                            for (int e = 0; e < 8; e++) y[e] = a[i + e] * mul;
-                            Vec8<bf16>::store(dst + c0 + i, y);
-                        }
+                        for (int e = 0; e < 8; e++) y[e] = a[i + e] * mul;
+                        Vec8<bf16>::store(dst + sub * 32 + i, y);
                     }
                 }
             }
+            nt += it.nst;
         }
     }
     tc_fence_before();
@@ -726,11 +819,12 @@ cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, 
 
 cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv, const void* out, const float* lse,
                                   int B, int T, int C, int NH, float* Dbuf, int* flags, cudaStream_t s) {
-    CUtensorMap tq, td;
+    CUtensorMap tq, td, to;
     if (((uintptr_t)dout & 15) || ((uintptr_t)out & 15) || ((uintptr_t)dqkv & 15) || (C % 8))
         return cudaErrorNotSupported;
     if (!tc::make_map(&tq, qkv, 3ull * C, (uint64_t)B * T, 3ull * C, 64, 128) ||
-        !tc::make_map(&td, dout, (uint64_t)C, (uint64_t)B * T, (uint64_t)C, 64, 128))
+        !tc::make_map(&td, dout, (uint64_t)C, (uint64_t)B * T, (uint64_t)C, 64, 128) ||
+        !tc::make_map(&to, out, (uint64_t)C, (uint64_t)B * T, (uint64_t)C, 64, 128))
         return cudaErrorNotSupported;
     static bool attr_done = false;
     if (!attr_done) {
@@ -742,13 +836,20 @@ cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv,
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    dim3 grid((T + 127) / 128, B * NH);
-    if (grid.y > 65535) return cudaErrorInvalidValue;
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 148;
+    }
+    const int nbh = B * NH, items = ((T + 127) / 128) * nbh;
+    const int grid = items < sms ? items : sms;  // persistent: one CTA per SM
     // the query-major kernel also writes D = rowsum(dO * O), which the key-major one reads
-    G2_LAUNCH atc::attn_bwd_tc_k<true><<<grid, atc::NTH_BWD, atc::BWD_SMEM, s>>>(
-        tq, td, (bf16*)dqkv, (const bf16*)qkv, (const bf16*)dout, (const bf16*)out, lse, Dbuf, T, C, NH, flags);
-    G2_LAUNCH atc::attn_bwd_tc_k<false><<<grid, atc::NTH_BWD, atc::BWD_SMEM, s>>>(
-        tq, td, (bf16*)dqkv, (const bf16*)qkv, (const bf16*)dout, (const bf16*)out, lse, Dbuf, T, C, NH, flags);
+    G2_LAUNCH atc::attn_bwd_tc_k<true><<<grid, atc::NTH_BWD, atc::BWD_SMEM, s>>>(tq, td, to, (bf16*)dqkv, lse, Dbuf, T,
+                                                                                 C, NH, nbh, flags);
+    G2_LAUNCH atc::attn_bwd_tc_k<false><<<grid, atc::NTH_BWD, atc::BWD_SMEM, s>>>(tq, td, to, (bf16*)dqkv, lse, Dbuf,
+                                                                                  T, C, NH, nbh, flags);
     return cudaGetLastError();
 }
 

@@ -138,6 +138,10 @@ G2_DEV void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* b
                  "l"((uint64_t)src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
+// Barrier `id` (1..15) among `nthreads` threads of the CTA (whole warps).
+G2_DEV void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 G2_DEV void tma_prefetch_desc(const CUtensorMap* tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tm) : "memory");
 }
@@ -177,6 +181,41 @@ G2_DEV void umma_commit(uint64_t* bar) {
                  : "memory");
 }
 
+// Warp-converged issue: every lane of the warp runs the issue loop (so the operands are
+// warp-uniform values) and one lane, picked by elect.sync inside the same asm block,
+// issues.  Measured on this GPU: 64-column MMAs with A in tensor memory issue at 35 clocks
+// each this way, 49 from a branch that one lane runs alone.
+G2_DEV bool elect_one() {
+    uint32_t p = 0;
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+    return p != 0;
+}
+G2_DEV void umma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+G2_DEV void umma_bf16_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+G2_DEV void umma_commit_w(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
 // 32 consecutive fp32 columns of this thread's accumulator lane.
 G2_DEV void tmem_ld32(uint32_t taddr, float* v) {
     uint32_t r[32];
@@ -210,6 +249,14 @@ G2_DEV void tmem_ld32_raw(uint32_t taddr, uint32_t* r) {
         : "r"(taddr));
 }
 G2_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The same wait, naming the 32 registers the outstanding loads write: their uses cannot
+// be scheduled before it (with the plain wait only the asm order protects them).
+G2_DEV void tmem_wait_ld_tied32(uint32_t* r) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]),"+r"(r[1]),"+r"(r[2]),"+r"(r[3]),"+r"(r[4]),"+r"(r[5]),"+r"(r[6]),"+r"(r[7]),"+r"(r[8]),"+r"(r[9]),"+r"(r[10]),"+r"(r[11]),"+r"(r[12]),"+r"(r[13]),"+r"(r[14]),"+r"(r[15]),"+r"(r[16]),"+r"(r[17]),"+r"(r[18]),"+r"(r[19]),"+r"(r[20]),"+r"(r[21]),"+r"(r[22]),"+r"(r[23]),"+r"(r[24]),"+r"(r[25]),"+r"(r[26]),"+r"(r[27]),"+r"(r[28]),"+r"(r[29]),"+r"(r[30]),"+r"(r[31])
+                 :
+                 : "memory");
+}
 
 // 32 consecutive fp32 columns of this thread's lane from registers.
 G2_DEV void tmem_st32(uint32_t taddr, const float* v) {
