@@ -152,19 +152,22 @@ __global__ void __launch_bounds__(NTH, 2)
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
+        // ---------------- MMA issuer: the whole warp runs the loop converged, one elected
+        // lane issues (see umma_bf16_w)
+        {
+            auto wait_all = [&](uint64_t* b, uint32_t par) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(b, par, abort_flag, flags));
+            };
             constexpr uint32_t ID_S = make_idesc(BKV, false, false);  // S: N = 128 keys
             constexpr uint32_t ID_PV = make_idesc(HS, false, true);   // O: N = 64, V is MN-major
             const uint32_t sQ = smem_u32(smem + OFF_Q), sP = smem_u32(smem + OFF_P);
-            bool ok = mbar_wait(&bar->q_full, 0, abort_flag, flags);
+            bool ok = wait_all(&bar->q_full, 0);
             bool issued_any = false;
             for (int j = 0; ok && j <= nkv; j++) {
                 if (j < nkv) {
                     // S_j once K_j has landed and the softmax has read S_{j-1} out
                     const int s = j & 1;
-                    if (!mbar_wait(&bar->k_full[s], (j >> 1) & 1, abort_flag, flags) ||
-                        (j > 0 && !mbar_wait(&bar->s_free, (j - 1) & 1, abort_flag, flags))) {
+                    if (!wait_all(&bar->k_full[s], (j >> 1) & 1) || (j > 0 && !wait_all(&bar->s_free, (j - 1) & 1))) {
                         ok = false;
                         break;
                     }
@@ -172,16 +175,15 @@ __global__ void __launch_bounds__(NTH, 2)
                     const uint32_t sK = smem_u32(smem + OFF_K + s * TILE);
 #pragma unroll
                     for (int k = 0; k < HS / 16; k++)
-                        umma_bf16(tmem + TM_S, sdesc(sQ + k * 32, 16, 1024), sdesc(sK + k * 32, 16, 1024), ID_S,
+                        umma_bf16_w(tmem + TM_S, sdesc(sQ + k * 32, 16, 1024), sdesc(sK + k * 32, 16, 1024), ID_S,
                                   k > 0 ? 1u : 0u);
-                    umma_commit(&bar->s_full);
-                    umma_commit(&bar->k_empty[s]);
+                    umma_commit_w(&bar->s_full);
+                    umma_commit_w(&bar->k_empty[s]);
                     issued_any = true;
                 }
                 // P_{j-1} V_{j-1} once the softmax has written P_{j-1}
                 if (j > 0) {
-                    if (!mbar_wait(&bar->p_full, (j - 1) & 1, abort_flag, flags) ||
-                        !mbar_wait(&bar->v_full[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, flags)) {
+                    if (!wait_all(&bar->p_full, (j - 1) & 1) || !wait_all(&bar->v_full[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
                         ok = false;
                         break;
                     }
@@ -195,18 +197,21 @@ __global__ void __launch_bounds__(NTH, 2)
                         // keys [16k, 16k+16): 64-key block k/4 of P, 32 bytes per step inside it
                         const uint64_t ad = sdesc(sP + (k >> 2) * TILE + (k & 3) * 32, 16, 1024);
                         const uint64_t bd = sdesc(sV + k * 16 * 128, 8192, 1024);
-                        umma_bf16(tmem + TM_O, ad, bd, ID_PV, (pj > 0 || k > 0) ? 1u : 0u);
+                        umma_bf16_w(tmem + TM_O, ad, bd, ID_PV, (pj > 0 || k > 0) ? 1u : 0u);
                     }
-                    umma_commit(&bar->o_done);
-                    umma_commit(&bar->v_empty[ps]);
+                    umma_commit_w(&bar->o_done);
+                    umma_commit_w(&bar->v_empty[ps]);
                     issued_any = true;
                 }
             }
             if (!ok && issued_any) {
-                umma_commit(&bar->drain);
-                unsigned long long t0 = globaltimer();
-                while (!mbar_try_wait(&bar->drain, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+                umma_commit_w(&bar->drain);
+                if (lane == 0) {
+                    unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(&bar->drain, 0) && globaltimer() - t0 < TIMEOUT_NS) {
+                    }
                 }
+                __syncwarp();
             }
         }
     } else {
