@@ -57,6 +57,31 @@ def flops_per_token(c, Vp):
     return 6.0 * (12 * L * C * C + Vp * C) + 3.0 * 2.0 * C * (T + 1) * L
 
 
+def measure_tf32_peak():
+    """Dense TF32 matmul throughput of this GPU (TFLOP/s): torch fp32 8192^3 with TF32
+    allowed, best of 10 after warm-up, CUDA events."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    n = 8192
+    g = torch.Generator(device="cuda").manual_seed(0)
+    a = torch.randn(n, n, device="cuda", generator=g)
+    b = torch.randn(n, n, device="cuda", generator=g)
+    for _ in range(3):
+        torch.matmul(a, b)
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    torch.backends.cuda.matmul.allow_tf32 = prev
+    del a, b
+    return 2.0 * n ** 3 / (best / 1e3) / 1e12
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -223,7 +248,7 @@ def run_reference(args, rank, world):
         return
     from gpt_train_step_arena_b300 import synth
     cfg = dict(synth.WORKLOADS[args.workload])
-    T_s = args.cpu_tokens
+    T_s = min(args.cpu_tokens, cfg["T"])
     m, inp, tgt, cores = oracle_sample(cfg, T_s, norm=args.norm)
     hp = (cfg["lr"], cfg["b1"], cfg["b2"], cfg["eps"], cfg["wd"])
     for i in range(args.warmup):
@@ -250,12 +275,18 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def config_block(cfg, workload, norm="layernorm"):
+PRECISION_TEXT = {"bf16": "bf16 mixed (fp32 master/AdamW)", "tf32": "fp32 tensors, TF32 tensor-core matmuls",
+                  "fp32": "strict fp32"}
+
+
+def config_block(cfg, workload, norm="layernorm", precision="bf16"):
     Vp = (cfg["V"] + 127) // 128 * 128
     if norm != "layernorm":
         workload = f"{workload}_{norm}"   # the microGPT variant of the same shapes
+    if precision != "bf16":
+        workload = f"{workload}_{precision}"
     return {"workload": workload, "norm": norm, "L": cfg["L"], "C": cfg["C"], "H": cfg["NH"], "V": cfg["V"], "Vp": Vp,
-            "B": cfg["B"], "T": cfg["T"], "precision": "bf16 mixed (fp32 master/AdamW)",
+            "B": cfg["B"], "T": cfg["T"], "precision": PRECISION_TEXT[precision],
             "lr": cfg["lr"], "wd": cfg["wd"],
             "l2": "no flush: every step streams > 10 GB of activations and weights, far above the 126 MB L2"}
 
@@ -276,7 +307,7 @@ def run_ours(args, rank, world, local):
     stream = synth.token_stream(cfg, steps=W + 2 * K, seed=1337 + rank)
     batches = [synth.batch(stream, s, B, T) for s in range(W + 2 * K)]
 
-    g = GPT2(L, C, NH, V, maxT, precision="bf16", norm=args.norm)
+    g = GPT2(L, C, NH, V, maxT, precision=args.precision, norm=args.norm)
     g.set_params(params)
     s = torch.cuda.Stream()
     g.set_stream(s.cuda_stream)
@@ -356,13 +387,15 @@ def run_ours(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        m, inp, tgt, cores = oracle_sample(cfg, args.cpu_tokens, norm=args.norm)
+        T_s = min(args.cpu_tokens, cfg["T"])
+        m, inp, tgt, cores = oracle_sample(cfg, T_s, norm=args.norm)
         t_fb, t_adam = oracle_step_time(m, inp, tgt, hp, 1)
-        cpu = dict({"value": extrapolated_tokens_per_s(cfg, args.cpu_tokens, t_fb, t_adam), "unit": "tokens/s",
+        cpu = dict({"value": extrapolated_tokens_per_s(cfg, T_s, t_fb, t_adam), "unit": "tokens/s",
                     "cores": cores, "kind": "oracle",
-                    "sample": cpu_sample_text(args.workload, args.cpu_tokens, t_fb, t_adam)}, **cpu_host_info())
+                    "sample": cpu_sample_text(args.workload, T_s, t_fb, t_adam)}, **cpu_host_info())
         del m
 
+    tf32_peak = measure_tf32_peak() if args.precision == "tf32" and rank == 0 else None
     if rank != 0:
         return
     pk = _peaks()
@@ -396,12 +429,17 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": DATA, "config": config_block(cfg, args.workload, args.norm),
-        "mfu": {"algorithmic_flops_per_token": fpt,
-                "vs_measured_burst": value / world * fpt / (pk["bf16"] * 1e12),
-                "vs_measured_sustained": value / world * fpt / (pk["bf16_sus"] * 1e12),
-                "peak": "the 40% target is judged against the measured dense bf16 burst peak (cuBLAS, "
-                        "MEASURED_PEAKS.json), the larger of the two measured figures"},
+        "dtype": args.precision, "data": DATA, "config": config_block(cfg, args.workload, args.norm, args.precision),
+        "mfu": ({"algorithmic_flops_per_token": fpt,
+                 "vs_measured_burst": value / world * fpt / (pk["bf16"] * 1e12),
+                 "vs_measured_sustained": value / world * fpt / (pk["bf16_sus"] * 1e12),
+                 "peak": "the 40% target is judged against the measured dense bf16 burst peak (cuBLAS, "
+                         "MEASURED_PEAKS.json), the larger of the two measured figures"}
+                if args.precision == "bf16" else
+                {"algorithmic_flops_per_token": fpt,
+                 "tf32_peak_tflops": tf32_peak,
+                 "vs_tf32_peak": (value / world * fpt / (tf32_peak * 1e12)) if tf32_peak else None,
+                 "peak": "dense TF32 peak measured in this run (cuBLAS fp32 8192^3 with TF32 allowed, best of 10)"}),
         "roofline": roofline,
         "kernels": kernels,
         "cpu_baseline": cpu,
@@ -583,6 +621,9 @@ def main():
     ap.add_argument("--gen-tokens", type=int, default=40)
     ap.add_argument("--norm", choices=["layernorm", "rmsnorm"], default="layernorm",
                     help="rmsnorm: the microGPT variant (every LayerNorm replaced by RMSNorm)")
+    ap.add_argument("--precision", choices=["bf16", "tf32", "fp32"], default="bf16",
+                    help="train mode: tf32 = fp32 tensors with TF32 tensor-core matmuls (MFU against a TF32 peak "
+                         "measured in the same run)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=128,
                     help="positions of the oracle's CPU sample (both arms), B=1")

@@ -47,6 +47,7 @@ SIGNATURES = {
     "gpt2_profile_enable": (I, [P, I]),
     "gpt2_profile_reset": (I, [P]),
     "gpt2_profile_read": (I, [P, I, ct.POINTER(ct.c_double), ct.POINTER(ct.c_double), ct.POINTER(U64)]),
+    "gpt2_check_bounded_wait": (I, [P, ct.c_uint]),
     "gpt2_set_stream": (I, [P, P]),
     "gpt2_sync": (I, [P]),
     "gpt2_last_status": (I, [P]),

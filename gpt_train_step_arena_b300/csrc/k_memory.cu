@@ -15,6 +15,24 @@ namespace g2 {
 
 static inline unsigned cdiv(size_t a, size_t b) { return (unsigned)((a + b - 1) / b); }
 
+// ------------------------------------------------------------------ bounded-wait check
+// One thread waits, through the library's bounded wait with a limit of limit_ns, on an
+// mbarrier that nothing arrives at; no copy or MMA is in flight.  The wait gives up,
+// raises G2_FLAG_TIMEOUT in *flags and the kernel returns.
+__global__ void bounded_wait_check_k(int* flags, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    tc::mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tc::mbar_wait_limit(&bar, 0, &abort_flag, flags, limit_ns);
+}
+cudaError_t bounded_wait_check(int* flags, unsigned long long limit_ns, cudaStream_t s) {
+    G2_LAUNCH bounded_wait_check_k<<<1, 32, 0, s>>>(flags, limit_ns);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ ids check
 __global__ void check_ids_k(const int32_t* ids, int M, int V, int* flags, int bit) {
     int i = blockIdx.x * blockDim.x + threadIdx.x;

@@ -17,6 +17,11 @@ enum ActType { ACT_F32 = 0, ACT_BF16 = 1 };
 void count_launches(unsigned n);
 uint64_t launches_total();
 
+// ---- diagnostics ------------------------------------------------------------------
+// A one-thread kernel whose bounded mbarrier wait (limit limit_ns) expires: sets
+// G2_FLAG_TIMEOUT in *flags and returns.
+cudaError_t bounded_wait_check(int* flags, unsigned long long limit_ns, cudaStream_t s);
+
 // ---- token ids (llm.c §1.23 validation) --------------------------------------
 cudaError_t check_ids(const int32_t* ids, int M, int V, int* flags, int flag_bit, cudaStream_t s);
 

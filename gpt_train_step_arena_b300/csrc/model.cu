@@ -680,6 +680,22 @@ extern "C" int gpt2_update(gpt2_t* m, float lr, float b1, float b2, float eps, f
     return GPT2_OK;
 }
 
+// ------------------------------------------------------------------ diagnostics
+extern "C" int gpt2_check_bounded_wait(gpt2_t* m, unsigned timeout_us) {
+    if (!m) return GPT2_ERR_ARG;
+    if (!m->aarena) return fail(m, GPT2_ERR_STATE, "the check uses the activation arena's flags: run a forward first");
+    if (timeout_us < 1 || timeout_us > 1000000) return fail(m, GPT2_ERR_ARG, "timeout_us must be in [1, 1e6]");
+    int hflag = 0;
+    CK(cudaMemsetAsync(m->flags, 0, 64, m->stream));
+    CK(bounded_wait_check(m->flags, 1000ull * timeout_us, m->stream));
+    CK(cudaMemcpyAsync(&hflag, m->flags, 4, cudaMemcpyDeviceToHost, m->stream));
+    CK(cudaStreamSynchronize(m->stream));
+    CK(cudaMemsetAsync(m->flags, 0, 64, m->stream));  // the handle's next forward starts clean
+    if (hflag & G2_FLAG_TIMEOUT)
+        return fail(m, GPT2_ERR_TIMEOUT, "a device-side wait gave up (kernel reported a timeout)");
+    return fail(m, GPT2_ERR_STATE, "the bounded wait did not report a timeout");
+}
+
 // ------------------------------------------------------------------ profiling
 extern "C" int gpt2_profile_enable(gpt2_t* m, int on) {
     if (!m) return GPT2_ERR_ARG;

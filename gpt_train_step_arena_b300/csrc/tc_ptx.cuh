@@ -60,21 +60,26 @@ G2_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
 }
 
 // Bounded wait on phase `parity`.  Returns false (and raises the CTA-wide abort and
-// the global timeout flag) if it does not complete within TIMEOUT_NS, or if another
-// role of the CTA has already aborted.
-G2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* flags) {
+// the global timeout flag) if it does not complete within limit_ns, or if another role
+// of the CTA has already aborted.
+G2_DEV bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* flags,
+                            unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = globaltimer();
     while (true) {
         for (int i = 0; i < 16; i++)
             if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > TIMEOUT_NS) {
+        if (globaltimer() - t0 > limit_ns) {
             *abort_flag = 1;
             if (flags) atomicOr(flags, G2_FLAG_TIMEOUT);
             return false;
         }
     }
+}
+// The same with the library's limit (about 2 s).
+G2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* flags) {
+    return mbar_wait_limit(bar, parity, abort_flag, flags, TIMEOUT_NS);
 }
 
 G2_DEV void tma_load_2d(const CUtensorMap* tm, uint64_t* bar, void* dst, int x, int y) {

@@ -198,6 +198,15 @@ int gpt2_profile_enable(gpt2_t* m, int on);
 int gpt2_profile_reset(gpt2_t* m);
 int gpt2_profile_read(gpt2_t* m, int kernel_class, double* ms, double* work, uint64_t* calls);
 
+/* Diagnostic of the device-side bounded waits every tensor-core kernel uses: runs, on the
+ * handle's stream, a one-thread kernel that waits on an mbarrier nothing arrives at, with
+ * the wait's limit shortened to timeout_us microseconds (1..1e6), no copy or MMA in
+ * flight.  The wait gives up, raises the device timeout flag and returns; the call
+ * synchronises, clears the flag and returns GPT2_ERR_TIMEOUT (the status any call that
+ * reads the flags reports after a real timeout).  The handle stays usable.  Needs a
+ * prior forward (the flags live in the activation arena): GPT2_ERR_STATE otherwise. */
+int gpt2_check_bounded_wait(gpt2_t* m, unsigned timeout_us);
+
 /* Run subsequent work on `stream` (a cudaStream_t; NULL = legacy default stream). */
 int gpt2_set_stream(gpt2_t* m, void* stream);
 /* Wait for all queued work; returns a gpt2_status for any pending CUDA error. */

@@ -280,3 +280,36 @@ def test_rmsnorm_variant_gpt2_124m_small(G, precision):
         assert rel_l2(r["logits"], r["ref_logits"]) <= tol["logits"]
     assert_grads_close(r["grads"], r["ref_grads"], L, C, V, maxT, tol["grads"])
 
+
+
+def test_bounded_wait_expiry_reports_timeout_and_handle_stays_usable(G):
+    """A device wait that nothing completes gives up after its limit, raises the timeout
+    flag, and the host reports GPT2_ERR_TIMEOUT; the handle then trains on exactly as a
+    fresh one does."""
+    import time
+    from gpt_train_step_arena_b300 import _native as N
+    L, C, NH, V, maxT = cfg_shape("tiny")
+    params = synth.init_params(L, C, V, maxT, seed=3)
+    inp, tgt = synth.batch(synth.zipf_stream(V, 2 * 16 + 1, seed=4), 0, 2, 16)
+    g = G(L, C, NH, V, maxT, precision="bf16")
+    assert N.lib.gpt2_check_bounded_wait(g.h, 1000) == N.GPT2_ERR_STATE     # no forward yet
+    g.set_params(params)
+    g.forward(inp, tgt)
+    t0 = time.perf_counter()
+    rc = N.lib.gpt2_check_bounded_wait(g.h, 20000)                           # 20 ms limit
+    elapsed = time.perf_counter() - t0
+    assert rc == N.GPT2_ERR_TIMEOUT, rc
+    assert b"timeout" in N.lib.gpt2_last_error(g.h)
+    assert 0.015 <= elapsed < 5.0, elapsed                                   # it waited, then gave up
+    # still usable: one step equals the same step on a fresh handle
+    g.set_params(params)
+    loss = g.forward(inp, tgt)
+    g.backward()
+    grads = g.grads()
+    g.close()
+    f = G(L, C, NH, V, maxT, precision="bf16")
+    f.set_params(params)
+    assert f.forward(inp, tgt) == loss
+    f.backward()
+    assert np.array_equal(f.grads(), grads)
+    f.close()
