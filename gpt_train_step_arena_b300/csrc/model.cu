@@ -53,7 +53,8 @@ struct gpt2 {
     size_t abytes;
     int B, T;
     int32_t *tok, *tgt;
-    int* flags;
+    int* flags;   // [0]: bad ids / non-finite loss of the current forward (cleared by each forward)
+    int* tflags;  // G2_FLAG_TIMEOUT of any kernel since it was last reported (kept until reported)
     float *loss, *losses;
     char *res, *res2, *ln1, *qkv, *atty, *ln2, *fch, *fchg, *lnf, *logits;
     float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd, *lnf_mean, *lnf_rstd, *lse;
@@ -174,7 +175,7 @@ static cudaError_t gemm_fwd(gpt2* m, int M, int N, int K, const void* X, const v
     a.bias = bias; a.R = R; a.ldr = N;
     a.D2 = Y2; a.ldd2 = N;
     a.epi = Y2 ? EPI_GELU : EPI_STORE;
-    a.flags = m->flags;
+    a.flags = m->tflags;
     tf32_args(m, a);
     return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
 }
@@ -188,7 +189,7 @@ static cudaError_t gemm_dgrad(gpt2* m, int M, int N, int K, const void* dY, cons
     a.D = dX; a.ldd = K; a.d_f32 = 0;
     a.P = P; a.ldp = K;
     a.epi = P ? EPI_GELU_BWD : EPI_STORE;
-    a.flags = m->flags;
+    a.flags = m->tflags;
     tf32_args(m, a);
     return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
 }
@@ -200,7 +201,7 @@ static cudaError_t gemm_wgrad(gpt2* m, int M, int N, int K, const void* dY, cons
     a.B = X; a.sBn = 1; a.sBk = K;
     a.D = dW; a.ldd = K; a.d_f32 = 1;
     a.epi = EPI_STORE;
-    a.flags = m->flags;
+    a.flags = m->tflags;
     tf32_args(m, a);
     return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
 }
@@ -430,7 +431,7 @@ static int alloc_acts(gpt2* m, int B, int T) {
     m->aarena = base;
     m->abytes = total;
     m->B = B; m->T = T;
-    m->tok = (int32_t*)tok; m->tgt = (int32_t*)tgt; m->flags = (int*)flags;
+    m->tok = (int32_t*)tok; m->tgt = (int32_t*)tgt; m->flags = (int*)flags; m->tflags = (int*)flags + 1;
     m->loss = (float*)loss; m->losses = (float*)losses;
     m->res = (char*)res; m->res2 = (char*)res2; m->ln1 = (char*)ln1; m->qkv = (char*)qkv;
     m->atty = (char*)atty; m->ln2 = (char*)ln2; m->fch = (char*)fch; m->fchg = (char*)fchg;
@@ -474,7 +475,7 @@ static int forward_impl(gpt2* m, const int32_t* tokens, const int32_t* targets, 
     cudaMemcpyKind kind = where == GPT2_DEVICE ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
     CK(cudaMemcpyAsync(m->tok, tokens, M * 4, kind, s));
     if (targets) CK(cudaMemcpyAsync(m->tgt, targets, M * 4, kind, s));
-    CK(cudaMemsetAsync(m->flags, 0, 64, s));
+    CK(cudaMemsetAsync(m->flags, 0, sizeof(int), s));  // timeouts (tflags) stay until reported
     OP(GPT2_K_ENCODER, 4.0 * M, check_ids(m->tok, (int)M, V, m->flags, G2_FLAG_BAD_TOKEN, s));
     if (targets) OP(GPT2_K_ENCODER, 4.0 * M, check_ids(m->tgt, (int)M, V, m->flags, G2_FLAG_BAD_TARGET, s));
     // gathered token rows + position rows + output
@@ -499,7 +500,7 @@ static int forward_impl(gpt2* m, const int32_t* tokens, const int32_t* targets, 
            gemm_fwd(m, (int)M, 3 * C, C, ln1, pw(m, P_QKVW, (size_t)l * 3 * C * C),
                     pf(m, m->params, P_QKVB) + l * 3 * C, qkv, nullptr, nullptr));
         OP(GPT2_K_ATTN_FWD, attn_fwd_flops(m),
-           attention_forward(m->at, atty, m->lse + l * M * NH, qkv, B, T, C, NH, s, m->flags));
+           attention_forward(m->at, atty, m->lse + l * M * NH, qkv, B, T, C, NH, s, m->tflags));
         OP(GPT2_K_GEMM, gemm_flops(M, C, C),
            gemm_fwd(m, (int)M, C, C, atty, pw(m, P_APW, (size_t)l * C * C),
                     pf(m, m->params, P_APB) + l * C, res2, res_in, nullptr));
@@ -548,11 +549,13 @@ extern "C" int gpt2_read_loss(gpt2_t* m, float* out) {
     int hflags[2] = {0, 0};
     float loss = -1.0f;
     if (m->loss_valid) CK(cudaMemcpyAsync(&loss, m->loss, 4, cudaMemcpyDeviceToHost, m->stream));
-    CK(cudaMemcpyAsync(hflags, m->flags, 4, cudaMemcpyDeviceToHost, m->stream));
+    CK(cudaMemcpyAsync(hflags, m->flags, 8, cudaMemcpyDeviceToHost, m->stream));
     CK(cudaStreamSynchronize(m->stream));
     *out = loss;
-    if (hflags[0] & G2_FLAG_TIMEOUT)
+    if ((hflags[0] | hflags[1]) & G2_FLAG_TIMEOUT) {
+        CK(cudaMemsetAsync(m->flags, 0, 8, m->stream));  // reported once
         return fail(m, GPT2_ERR_TIMEOUT, "a device-side wait gave up (kernel reported a timeout)");
+    }
     if (hflags[0] & G2_FLAG_BAD_TOKEN)
         return fail(m, GPT2_ERR_TOKEN, "an input id is outside [0, %d)", m->V);
     if (hflags[0] & G2_FLAG_BAD_TARGET)
@@ -636,7 +639,7 @@ extern "C" int gpt2_backward(gpt2_t* m) {
         // attention
         OP(GPT2_K_ATTN_BWD, 2.0 * attn_fwd_flops(m),
            attention_backward(m->at, m->dqkv, m->datty, qkv, atty, m->lse + l * M * NH, B, T, C, NH,
-                              m->attD, s, m->flags));
+                              m->attD, s, m->tflags));
         // qkv: qkv = ln1 . Wqkv^T + bqkv
         OP(GPT2_K_GEMM, gemm_flops(M, C, 3 * C),
            gemm_dgrad(m, (int)M, 3 * C, C, m->dqkv, pw(m, P_QKVW, (size_t)l * 3 * C * C), m->dln, nullptr));
@@ -686,11 +689,11 @@ extern "C" int gpt2_check_bounded_wait(gpt2_t* m, unsigned timeout_us) {
     if (!m->aarena) return fail(m, GPT2_ERR_STATE, "the check uses the activation arena's flags: run a forward first");
     if (timeout_us < 1 || timeout_us > 1000000) return fail(m, GPT2_ERR_ARG, "timeout_us must be in [1, 1e6]");
     int hflag = 0;
-    CK(cudaMemsetAsync(m->flags, 0, 64, m->stream));
-    CK(bounded_wait_check(m->flags, 1000ull * timeout_us, m->stream));
-    CK(cudaMemcpyAsync(&hflag, m->flags, 4, cudaMemcpyDeviceToHost, m->stream));
+    CK(cudaMemsetAsync(m->tflags, 0, sizeof(int), m->stream));
+    CK(bounded_wait_check(m->tflags, 1000ull * timeout_us, m->stream));
+    CK(cudaMemcpyAsync(&hflag, m->tflags, 4, cudaMemcpyDeviceToHost, m->stream));
     CK(cudaStreamSynchronize(m->stream));
-    CK(cudaMemsetAsync(m->flags, 0, 64, m->stream));  // the handle's next forward starts clean
+    CK(cudaMemsetAsync(m->tflags, 0, sizeof(int), m->stream));  // reported here: the handle starts clean
     if (hflag & G2_FLAG_TIMEOUT)
         return fail(m, GPT2_ERR_TIMEOUT, "a device-side wait gave up (kernel reported a timeout)");
     return fail(m, GPT2_ERR_STATE, "the bounded wait did not report a timeout");

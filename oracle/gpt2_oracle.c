@@ -675,12 +675,11 @@ OR_EXPORT void or_zero_grad(OracleModel* m) {
  * last forward had no targets, -3 on allocation failure. */
 OR_EXPORT int or_backward(OracleModel* m) {
     if (!m->amem || !m->have_targets) return -1;
-    if (!m->gmem) {
-        m->gmem = carve_params(&m->g, m->psize);
-        m->gamem = carve_acts(&m->ga, m->asize);
-        if (!m->gmem || !m->gamem) return -3;
-        or_zero_grad(m);
-    }
+    /* gradient buffers on first use (the activation gradients again after
+     * or_release_acts, which frees them with the activations); calloc leaves them zero */
+    if (!m->gmem) m->gmem = carve_params(&m->g, m->psize);
+    if (!m->gamem) m->gamem = carve_acts(&m->ga, m->asize);
+    if (!m->gmem || !m->gamem) return -3;
     const int B = m->B, T = m->T, V = m->V, L = m->L, NH = m->NH, C = m->C;
     const size_t BTC = (size_t)B * T * C, BT = (size_t)B * T, BNTT = (size_t)B * NH * T * T;
     Params p = m->p, g = m->g;

@@ -313,3 +313,27 @@ def test_bounded_wait_expiry_reports_timeout_and_handle_stays_usable(G):
     f.backward()
     assert np.array_equal(f.grads(), grads)
     f.close()
+
+
+@pytest.mark.parametrize("precision", ["bf16", "tf32"])
+def test_split_k_weight_gradients_whole_step(G, precision):
+    """1,024 tokens per step on the tiny model: every weight-gradient product is split over
+    K (4 splits of 256 tokens each) and summed in the kernel by the last split to finish, on
+    one shared workspace holding products of different sizes, twice in a row."""
+    L, C, NH, V, maxT = cfg_shape("tiny")
+    params = synth.init_params(L, C, V, maxT, seed=21)
+    stream = synth.zipf_stream(V, 2 * 32 * 32 + 1, seed=22)
+    o = Oracle(L, C, NH, V, maxT)
+    g = G(L, C, NH, V, maxT, precision=precision)
+    g.set_params(params)
+    o.set_params(params)
+    for step in range(2):
+        inp, tgt = synth.batch(stream, step, 32, 32)
+        ref = o.forward(inp, tgt)
+        o.backward()
+        loss = g.forward(inp, tgt)
+        g.backward()
+        assert abs(loss - ref) <= 1e-2 * ref
+        assert_grads_close(g.grads(), o.grads(), L, C, V, maxT, 3e-2)
+        o.release_acts()
+    g.close()
