@@ -18,6 +18,7 @@ static const int ATT_MAX_HS = 256;
 
 template <typename T>
 __global__ void attn_fwd_simt_k(T* out, float* lse, const T* qkv, int B, int Tn, int C, int NH) {
+    G2_PDL_ENTRY();
     __shared__ float s_q[8][ATT_MAX_HS];
     int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     long long gid = (long long)blockIdx.x * 8 + warp;  // ((b*NH + h)*T + t)
@@ -74,6 +75,7 @@ __global__ void attn_fwd_simt_k(T* out, float* lse, const T* qkv, int B, int Tn,
 // D[b,h,t] = sum_d dO[b,t,h,d] * O[b,t,h,d]
 template <typename T>
 __global__ void attn_bwd_dot_k(float* D, const T* dout, const T* out, int B, int Tn, int C, int NH) {
+    G2_PDL_ENTRY();
     int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     long long gid = (long long)blockIdx.x * 8 + warp;
     if (gid >= (long long)B * NH * Tn) return;
@@ -91,6 +93,7 @@ __global__ void attn_bwd_dot_k(float* D, const T* dout, const T* out, int B, int
 template <typename T>
 __global__ void attn_bwd_dq_simt_k(T* dqkv, const T* dout, const T* qkv, const float* lse,
                                    const float* D, int B, int Tn, int C, int NH) {
+    G2_PDL_ENTRY();
     __shared__ float s_q[8][ATT_MAX_HS];
     __shared__ float s_do[8][ATT_MAX_HS];
     int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -149,6 +152,7 @@ __global__ void attn_bwd_dq_simt_k(T* dqkv, const T* dout, const T* qkv, const f
 template <typename T>
 __global__ void attn_bwd_dkv_simt_k(T* dqkv, const T* dout, const T* qkv, const float* lse,
                                     const float* D, int B, int Tn, int C, int NH) {
+    G2_PDL_ENTRY();
     __shared__ float s_k[8][ATT_MAX_HS];
     __shared__ float s_v[8][ATT_MAX_HS];
     int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -221,9 +225,9 @@ cudaError_t attention_forward_simt(ActType at, void* out, float* lse, const void
     long long n = (long long)B * NH * T;
     if (n <= 0) return cudaSuccess;
     if (at == ACT_BF16)
-        G2_LAUNCH attn_fwd_simt_k<bf16><<<rows8(n), 256, 0, s>>>((bf16*)out, lse, (const bf16*)qkv, B, T, C, NH);
+        ::g2::launch_k(attn_fwd_simt_k<bf16>, rows8(n), 256, 0, s, (bf16*)out, lse, (const bf16*)qkv, B, T, C, NH);
     else
-        G2_LAUNCH attn_fwd_simt_k<float><<<rows8(n), 256, 0, s>>>((float*)out, lse, (const float*)qkv, B, T, C, NH);
+        ::g2::launch_k(attn_fwd_simt_k<float>, rows8(n), 256, 0, s, (float*)out, lse, (const float*)qkv, B, T, C, NH);
     return cudaGetLastError();
 }
 
@@ -232,9 +236,9 @@ cudaError_t attention_bwd_dot(ActType at, float* D, const void* dout, const void
     long long n = (long long)B * NH * T;
     if (n <= 0) return cudaSuccess;
     if (at == ACT_BF16)
-        G2_LAUNCH attn_bwd_dot_k<bf16><<<rows8(n), 256, 0, s>>>(D, (const bf16*)dout, (const bf16*)out, B, T, C, NH);
+        ::g2::launch_k(attn_bwd_dot_k<bf16>, rows8(n), 256, 0, s, D, (const bf16*)dout, (const bf16*)out, B, T, C, NH);
     else
-        G2_LAUNCH attn_bwd_dot_k<float><<<rows8(n), 256, 0, s>>>(D, (const float*)dout, (const float*)out, B, T, C, NH);
+        ::g2::launch_k(attn_bwd_dot_k<float>, rows8(n), 256, 0, s, D, (const float*)dout, (const float*)out, B, T, C, NH);
     return cudaGetLastError();
 }
 
@@ -245,16 +249,16 @@ cudaError_t attention_backward_simt(ActType at, void* dqkv, const void* dout, co
     long long n = (long long)B * NH * T;
     if (n <= 0) return cudaSuccess;
     if (at == ACT_BF16) {
-        G2_LAUNCH attn_bwd_dot_k<bf16><<<rows8(n), 256, 0, s>>>(Dbuf, (const bf16*)dout, (const bf16*)out, B, T, C, NH);
-        G2_LAUNCH attn_bwd_dq_simt_k<bf16><<<rows8(n), 256, 0, s>>>((bf16*)dqkv, (const bf16*)dout,
+        ::g2::launch_k(attn_bwd_dot_k<bf16>, rows8(n), 256, 0, s, Dbuf, (const bf16*)dout, (const bf16*)out, B, T, C, NH);
+        ::g2::launch_k(attn_bwd_dq_simt_k<bf16>, rows8(n), 256, 0, s, (bf16*)dqkv, (const bf16*)dout,
                                                           (const bf16*)qkv, lse, Dbuf, B, T, C, NH);
-        G2_LAUNCH attn_bwd_dkv_simt_k<bf16><<<rows8(n), 256, 0, s>>>((bf16*)dqkv, (const bf16*)dout,
+        ::g2::launch_k(attn_bwd_dkv_simt_k<bf16>, rows8(n), 256, 0, s, (bf16*)dqkv, (const bf16*)dout,
                                                            (const bf16*)qkv, lse, Dbuf, B, T, C, NH);
     } else {
-        G2_LAUNCH attn_bwd_dot_k<float><<<rows8(n), 256, 0, s>>>(Dbuf, (const float*)dout, (const float*)out, B, T, C, NH);
-        G2_LAUNCH attn_bwd_dq_simt_k<float><<<rows8(n), 256, 0, s>>>((float*)dqkv, (const float*)dout,
+        ::g2::launch_k(attn_bwd_dot_k<float>, rows8(n), 256, 0, s, Dbuf, (const float*)dout, (const float*)out, B, T, C, NH);
+        ::g2::launch_k(attn_bwd_dq_simt_k<float>, rows8(n), 256, 0, s, (float*)dqkv, (const float*)dout,
                                                            (const float*)qkv, lse, Dbuf, B, T, C, NH);
-        G2_LAUNCH attn_bwd_dkv_simt_k<float><<<rows8(n), 256, 0, s>>>((float*)dqkv, (const float*)dout,
+        ::g2::launch_k(attn_bwd_dkv_simt_k<float>, rows8(n), 256, 0, s, (float*)dqkv, (const float*)dout,
                                                             (const float*)qkv, lse, Dbuf, B, T, C, NH);
     }
     return cudaGetLastError();

@@ -64,6 +64,7 @@ G2_DEV uint32_t pack_bf16x2(float lo, float hi) {
 __global__ void __launch_bounds__(NTH, 2)
     attn_fwd_tc_k(const __grid_constant__ CUtensorMap tm_qkv, bf16* out, float* lse, int T, int C, int NH,
                   int* flags) {
+    G2_PDL_ENTRY();
     extern __shared__ __align__(1024) uint8_t smem[];
     FwdBars* bar = reinterpret_cast<FwdBars*>(smem + OFF_BAR);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -401,6 +402,7 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
     attn_bwd_tc_k(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_o, bf16* dqkv, const float* lse, float* Dbuf, int T, int C,
                   int NH, int nbh, int* flags) {
+    G2_PDL_ENTRY();
     extern __shared__ __align__(1024) uint8_t smem[];
     BwdBars* bar = reinterpret_cast<BwdBars*>(smem + BW_BAR);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -818,7 +820,7 @@ cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, 
     }
     dim3 grid((T + atc::BQ - 1) / atc::BQ, B * NH);
     if (grid.y > 65535) return cudaErrorInvalidValue;
-    G2_LAUNCH atc::attn_fwd_tc_k<<<grid, atc::NTH, atc::FWD_SMEM, s>>>(tm, (bf16*)out, lse, T, C, NH, flags);
+    ::g2::launch_k(atc::attn_fwd_tc_k, grid, atc::NTH, atc::FWD_SMEM, s, tm, (bf16*)out, lse, T, C, NH, flags);
     return cudaGetLastError();
 }
 
@@ -851,9 +853,9 @@ cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv,
     const int nbh = B * NH, items = ((T + 127) / 128) * nbh;
     const int grid = items < sms ? items : sms;  // persistent: one CTA per SM
     // the query-major kernel also writes D = rowsum(dO * O), which the key-major one reads
-    G2_LAUNCH atc::attn_bwd_tc_k<true><<<grid, atc::NTH_BWD, atc::BWD_SMEM, s>>>(tq, td, to, (bf16*)dqkv, lse, Dbuf, T,
+    ::g2::launch_k(atc::attn_bwd_tc_k<true>, grid, atc::NTH_BWD, atc::BWD_SMEM, s, tq, td, to, (bf16*)dqkv, lse, Dbuf, T,
                                                                                  C, NH, nbh, flags);
-    G2_LAUNCH atc::attn_bwd_tc_k<false><<<grid, atc::NTH_BWD, atc::BWD_SMEM, s>>>(tq, td, to, (bf16*)dqkv, lse, Dbuf,
+    ::g2::launch_k(atc::attn_bwd_tc_k<false>, grid, atc::NTH_BWD, atc::BWD_SMEM, s, tq, td, to, (bf16*)dqkv, lse, Dbuf,
                                                                                   T, C, NH, nbh, flags);
     return cudaGetLastError();
 }

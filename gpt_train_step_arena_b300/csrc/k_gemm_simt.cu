@@ -13,6 +13,7 @@ static const int SB_M = 64, SB_N = 64, SB_K = 16;
 
 template <typename T>
 __global__ void __launch_bounds__(256) gemm_simt_k(GemmArgs a) {
+    G2_PDL_ENTRY();
     __shared__ float As[SB_K][SB_M + 4];
     __shared__ float Bs[SB_K][SB_N + 4];
     const T* A = (const T*)a.A;
@@ -88,9 +89,9 @@ cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t s) {
     dim3 grid((a.N + SB_N - 1) / SB_N, (a.M + SB_M - 1) / SB_M);
     if (grid.y > 65535) return cudaErrorInvalidValue;
     if (a.in_type == ACT_BF16)
-        G2_LAUNCH gemm_simt_k<bf16><<<grid, 256, 0, s>>>(a);
+        ::g2::launch_k(gemm_simt_k<bf16>, grid, 256, 0, s, a);
     else
-        G2_LAUNCH gemm_simt_k<float><<<grid, 256, 0, s>>>(a);
+        ::g2::launch_k(gemm_simt_k<float>, grid, 256, 0, s, a);
     return cudaGetLastError();
 }
 

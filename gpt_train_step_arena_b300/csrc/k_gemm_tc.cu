@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                    const __grid_constant__ CUtensorMap tmX, const Params p) {
+    G2_PDL_ENTRY();
     using CF = Cfg<BN, BMT, EPI>;
     using EO = EpiOut<EPI>;
     using OT = OperandT<TF>;
@@ -515,6 +516,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
 
 // Fixed-order sum of the split-K partials: out[i] = sum_s ws[s][i].
 __global__ void splitk_reduce_k(float* out, long long ldo, const float* ws, int M, int N, int splits) {
+    G2_PDL_ENTRY();
     size_t n = (size_t)M * N;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         float a = 0.f;
@@ -529,6 +531,7 @@ __global__ void splitk_reduce_k(float* out, long long ldo, const float* ws, int 
 // unrounded v (as the fused GELU epilogue does).
 __global__ void splitk_epilogue_k(void* D, long long ldd, int d_f32, const float* ws, int M, int N, int splits,
                                   const float* bias, const bf16* R, long long ldr, bf16* D2, long long ldd2) {
+    G2_PDL_ENTRY();
     size_t n = (size_t)M * N;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         float a = 0.f;
@@ -568,7 +571,7 @@ static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const 
         attr_done = true;
     }
     int grid = std::min(p.num_units, num_sms());
-    G2_LAUNCH kern<<<grid, CF::THREADS, CF::SMEM_BYTES, s>>>(ta, tb, td, td2, tx, p);
+    ::g2::launch_k(kern, grid, CF::THREADS, CF::SMEM_BYTES, s, ta, tb, td, td2, tx, p);
     return cudaGetLastError();
 }
 
@@ -790,7 +793,7 @@ static cudaError_t gemm_tc_tf32(const GemmArgs& a, float* ws, size_t ws_bytes, i
         if (e != cudaSuccess) return e;
         size_t n = (size_t)a.M * a.N;
         unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
-        G2_LAUNCH splitk_reduce_k<<<blocks, 256, 0, s>>>((float*)a.D, a.ldd, ws, a.M, a.N, splits);
+        ::g2::launch_k(splitk_reduce_k, blocks, 256, 0, s, (float*)a.D, a.ldd, ws, a.M, a.N, splits);
         return cudaGetLastError();
     }
     return BN == 256 ? launch_tf32<256, E_STORE_F32>(bmt, mp, p, s) : launch_tf32<128, E_STORE_F32>(bmt, mp, p, s);
@@ -885,11 +888,11 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
         size_t n = (size_t)a.M * a.N;
         unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
         if (skinny)
-            G2_LAUNCH splitk_epilogue_k<<<blocks, 256, 0, s>>>(
+            ::g2::launch_k(splitk_epilogue_k, blocks, 256, 0, s, 
                 a.D, a.ldd, a.d_f32, ws, a.M, a.N, splits, a.bias, (const bf16*)a.R, a.ldr,
                 a.epi == EPI_GELU ? (bf16*)a.D2 : nullptr, a.ldd2);
         else
-            G2_LAUNCH splitk_reduce_k<<<blocks, 256, 0, s>>>((float*)a.D, a.ldd, ws, a.M, a.N, splits);
+            ::g2::launch_k(splitk_reduce_k, blocks, 256, 0, s, (float*)a.D, a.ldd, ws, a.M, a.N, splits);
         return cudaGetLastError();
     }
     switch (a.epi) {

@@ -28,6 +28,7 @@ static inline unsigned grid_for(size_t n, int threads) {
 template <typename T>
 __global__ void gen_embed_k(T* x, const int32_t* ids, const T* wte, const T* wpe, int B, int n, int t0,
                             int maxT, int C, const int* dstate) {
+    G2_PDL_ENTRY();
     if (dstate) t0 = dstate[0];
     const size_t total = (size_t)B * n * C;
     for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
@@ -43,6 +44,7 @@ __global__ void gen_embed_k(T* x, const int32_t* ids, const T* wte, const T* wpe
 // kv[b, t0+i, :] = the key and value parts of qkv row b*n + i.
 template <typename T>
 __global__ void gen_kv_append_k(T* kv, const T* qkv, int B, int n, int t0, int maxT, int C, const int* dstate) {
+    G2_PDL_ENTRY();
     if (dstate) t0 = dstate[0];
     const size_t C2 = 2 * (size_t)C, total = (size_t)B * n * C2;
     for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
@@ -75,6 +77,7 @@ constexpr int GA_THREADS = 128;
 template <typename T>
 __global__ void __launch_bounds__(GA_THREADS) gen_attn_k(T* out, const T* qkv, const T* kv, int n, int t0,
                                                          int maxT, int C, int NH, const int* dstate) {
+    G2_PDL_ENTRY();
     extern __shared__ float gsh[];  // q[hs] | scores[t0 + n] | red[32] | part[GA_THREADS]
     if (dstate) t0 = dstate[0];
     const int hs = C / NH;
@@ -131,6 +134,7 @@ __global__ void __launch_bounds__(GA_THREADS) gen_attn_k(T* out, const T* qkv, c
 // last[b] = x[b*n + n-1]
 template <typename T>
 __global__ void gen_last_rows_k(T* last, const T* x, int B, int n, int C) {
+    G2_PDL_ENTRY();
     const size_t total = (size_t)B * C;
     for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
         const size_t b = e / C, c = e - b * C;
@@ -152,6 +156,7 @@ template <typename T>
 __global__ void __launch_bounds__(GS_THREADS) gen_sample_k(int32_t* ids, int32_t* out, const T* logits, int V, int Vp,
                                                            float temperature, const float* coins, int step,
                                                            int n_new, int t_next, int maxT, const int* dstate) {
+    G2_PDL_ENTRY();
     if (dstate) {
         t_next = dstate[0] + 1;
         step = dstate[1];
@@ -241,6 +246,7 @@ __global__ void __launch_bounds__(GS_THREADS) gen_sample_k(int32_t* ids, int32_t
 
 // End of a one-token step: the next step extends the following position.
 __global__ void gen_advance_k(int* dstate) {
+    G2_PDL_ENTRY();
     if (threadIdx.x == 0 && blockIdx.x == 0) {
         dstate[0] += 1;
         dstate[1] += 1;
@@ -252,10 +258,10 @@ cudaError_t gen_embed(ActType at, void* x, const int32_t* ids, const void* wte, 
                       int maxT, int C, const int* dstate, cudaStream_t s) {
     const unsigned g = grid_for((size_t)B * n * C, 256);
     if (at == ACT_BF16)
-        G2_LAUNCH gen_embed_k<bf16><<<g, 256, 0, s>>>((bf16*)x, ids, (const bf16*)wte, (const bf16*)wpe, B, n, t0,
+        ::g2::launch_k(gen_embed_k<bf16>, g, 256, 0, s, (bf16*)x, ids, (const bf16*)wte, (const bf16*)wpe, B, n, t0,
                                                      maxT, C, dstate);
     else
-        G2_LAUNCH gen_embed_k<float><<<g, 256, 0, s>>>((float*)x, ids, (const float*)wte, (const float*)wpe, B, n,
+        ::g2::launch_k(gen_embed_k<float>, g, 256, 0, s, (float*)x, ids, (const float*)wte, (const float*)wpe, B, n,
                                                       t0, maxT, C, dstate);
     return cudaGetLastError();
 }
@@ -264,9 +270,9 @@ cudaError_t gen_kv_append(ActType at, void* kv, const void* qkv, int B, int n, i
                           const int* dstate, cudaStream_t s) {
     const unsigned g = grid_for((size_t)B * n * 2 * C, 256);
     if (at == ACT_BF16)
-        G2_LAUNCH gen_kv_append_k<bf16><<<g, 256, 0, s>>>((bf16*)kv, (const bf16*)qkv, B, n, t0, maxT, C, dstate);
+        ::g2::launch_k(gen_kv_append_k<bf16>, g, 256, 0, s, (bf16*)kv, (const bf16*)qkv, B, n, t0, maxT, C, dstate);
     else
-        G2_LAUNCH gen_kv_append_k<float><<<g, 256, 0, s>>>((float*)kv, (const float*)qkv, B, n, t0, maxT, C,
+        ::g2::launch_k(gen_kv_append_k<float>, g, 256, 0, s, (float*)kv, (const float*)qkv, B, n, t0, maxT, C,
                                                            dstate);
     return cudaGetLastError();
 }
@@ -293,10 +299,10 @@ cudaError_t gen_attention(ActType at, void* out, const void* qkv, const void* kv
     }
     dim3 g((unsigned)(B * NH), (unsigned)n);
     if (at == ACT_BF16)
-        G2_LAUNCH gen_attn_k<bf16><<<g, GA_THREADS, smem, s>>>((bf16*)out, (const bf16*)qkv, (const bf16*)kv, n, t0,
+        ::g2::launch_k(gen_attn_k<bf16>, g, GA_THREADS, smem, s, (bf16*)out, (const bf16*)qkv, (const bf16*)kv, n, t0,
                                                               maxT, C, NH, dstate);
     else
-        G2_LAUNCH gen_attn_k<float><<<g, GA_THREADS, smem, s>>>((float*)out, (const float*)qkv, (const float*)kv, n,
+        ::g2::launch_k(gen_attn_k<float>, g, GA_THREADS, smem, s, (float*)out, (const float*)qkv, (const float*)kv, n,
                                                                t0, maxT, C, NH, dstate);
     return cudaGetLastError();
 }
@@ -304,9 +310,9 @@ cudaError_t gen_attention(ActType at, void* out, const void* qkv, const void* kv
 cudaError_t gen_last_rows(ActType at, void* last, const void* x, int B, int n, int C, cudaStream_t s) {
     const unsigned g = grid_for((size_t)B * C, 256);
     if (at == ACT_BF16)
-        G2_LAUNCH gen_last_rows_k<bf16><<<g, 256, 0, s>>>((bf16*)last, (const bf16*)x, B, n, C);
+        ::g2::launch_k(gen_last_rows_k<bf16>, g, 256, 0, s, (bf16*)last, (const bf16*)x, B, n, C);
     else
-        G2_LAUNCH gen_last_rows_k<float><<<g, 256, 0, s>>>((float*)last, (const float*)x, B, n, C);
+        ::g2::launch_k(gen_last_rows_k<float>, g, 256, 0, s, (float*)last, (const float*)x, B, n, C);
     return cudaGetLastError();
 }
 
@@ -314,16 +320,16 @@ cudaError_t gen_sample(ActType at, int32_t* ids, int32_t* out, const void* logit
                        float temperature, const float* coins, int step, int n_new, int t_next, int maxT,
                        const int* dstate, cudaStream_t s) {
     if (at == ACT_BF16)
-        G2_LAUNCH gen_sample_k<bf16><<<B, GS_THREADS, 0, s>>>(ids, out, (const bf16*)logits, V, Vp, temperature,
+        ::g2::launch_k(gen_sample_k<bf16>, B, GS_THREADS, 0, s, ids, out, (const bf16*)logits, V, Vp, temperature,
                                                              coins, step, n_new, t_next, maxT, dstate);
     else
-        G2_LAUNCH gen_sample_k<float><<<B, GS_THREADS, 0, s>>>(ids, out, (const float*)logits, V, Vp, temperature,
+        ::g2::launch_k(gen_sample_k<float>, B, GS_THREADS, 0, s, ids, out, (const float*)logits, V, Vp, temperature,
                                                               coins, step, n_new, t_next, maxT, dstate);
     return cudaGetLastError();
 }
 
 cudaError_t gen_advance(int* dstate, cudaStream_t s) {
-    G2_LAUNCH gen_advance_k<<<1, 32, 0, s>>>(dstate);
+    ::g2::launch_k(gen_advance_k, 1, 32, 0, s, dstate);
     return cudaGetLastError();
 }
 

@@ -43,6 +43,7 @@ G2_DEV double unit(uint32_t u) { return (double)(u >> 8) * (1.0 / 16777216.0); }
 // Thread p owns lanes 2p and 2p+1: the two draws of pair j = round * PAIRS + p of every
 // normal tensor, so its outputs 2j, 2j+1 sit next to those of threads p-1 and p+1.
 __global__ void __launch_bounds__(256) init_normal_k(float* params, InitPlan plan, uint64_t seed) {
+    G2_PDL_ENTRY();
     const int p = blockIdx.x * blockDim.x + threadIdx.x;
     if (p >= PAIRS) return;
     uint64_t s0 = splitmix64(seed + 2ull * p), s1 = splitmix64(seed + 2ull * p + 1);
@@ -66,6 +67,7 @@ __global__ void __launch_bounds__(256) init_normal_k(float* params, InitPlan pla
 }
 
 __global__ void fill_k(float* p, size_t n, float v) {
+    G2_PDL_ENTRY();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
         p[i] = v;
 }
@@ -77,9 +79,9 @@ cudaError_t init_params_device(float* params, const InitPlan& plan, const float*
     for (int i = 0; i < n_ones; i++) {
         if (!ones_n[i]) continue;
         const unsigned blocks = (unsigned)std::min<size_t>((ones_n[i] + 255) / 256, 1024);
-        G2_LAUNCH fill_k<<<blocks, 256, 0, s>>>(const_cast<float*>(ones[i]), ones_n[i], 1.0f);
+        ::g2::launch_k(fill_k, blocks, 256, 0, s, const_cast<float*>(ones[i]), ones_n[i], 1.0f);
     }
-    G2_LAUNCH init_normal_k<<<PAIRS / 256, 256, 0, s>>>(params, plan, seed);
+    ::g2::launch_k(init_normal_k, PAIRS / 256, 256, 0, s, params, plan, seed);
     return cudaGetLastError();
 }
 

@@ -20,6 +20,7 @@ static inline unsigned cdiv(size_t a, size_t b) { return (unsigned)((a + b - 1) 
 // mbarrier that nothing arrives at; no copy or MMA is in flight.  The wait gives up,
 // raises G2_FLAG_TIMEOUT in *flags and the kernel returns.
 __global__ void bounded_wait_check_k(int* flags, unsigned long long limit_ns) {
+    G2_PDL_ENTRY();
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
     if (threadIdx.x != 0) return;
@@ -29,18 +30,19 @@ __global__ void bounded_wait_check_k(int* flags, unsigned long long limit_ns) {
     tc::mbar_wait_limit(&bar, 0, &abort_flag, flags, limit_ns);
 }
 cudaError_t bounded_wait_check(int* flags, unsigned long long limit_ns, cudaStream_t s) {
-    G2_LAUNCH bounded_wait_check_k<<<1, 32, 0, s>>>(flags, limit_ns);
+    ::g2::launch_k(bounded_wait_check_k, 1, 32, 0, s, flags, limit_ns);
     return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ ids check
 __global__ void check_ids_k(const int32_t* ids, int M, int V, int* flags, int bit) {
+    G2_PDL_ENTRY();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < M && (unsigned)ids[i] >= (unsigned)V) atomicOr(flags, bit);
 }
 cudaError_t check_ids(const int32_t* ids, int M, int V, int* flags, int bit, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
-    G2_LAUNCH check_ids_k<<<cdiv(M, 256), 256, 0, s>>>(ids, M, V, flags, bit);
+    ::g2::launch_k(check_ids_k, cdiv(M, 256), 256, 0, s, ids, M, V, flags, bit);
     return cudaGetLastError();
 }
 
@@ -50,6 +52,7 @@ cudaError_t check_ids(const int32_t* ids, int M, int V, int* flags, int bit, cud
 template <typename T>
 __global__ void encoder_fwd_k(T* out, const int32_t* tok, const T* wte, const T* wpe, int M,
                               int Tn, int C, int V, int* flags) {
+    G2_PDL_ENTRY();
     int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (row >= M) return;
     int id = tok[row];
@@ -83,10 +86,10 @@ cudaError_t encoder_forward(ActType at, void* out, const int32_t* tok, const voi
     int M = B * T;
     if (M <= 0) return cudaSuccess;
     if (at == ACT_BF16)
-        G2_LAUNCH encoder_fwd_k<bf16><<<cdiv(M, 8), 256, 0, s>>>((bf16*)out, tok, (const bf16*)wte,
+        ::g2::launch_k(encoder_fwd_k<bf16>, cdiv(M, 8), 256, 0, s, (bf16*)out, tok, (const bf16*)wte,
                                                         (const bf16*)wpe, M, T, C, V, flags);
     else
-        G2_LAUNCH encoder_fwd_k<float><<<cdiv(M, 8), 256, 0, s>>>((float*)out, tok, (const float*)wte,
+        ::g2::launch_k(encoder_fwd_k<float>, cdiv(M, 8), 256, 0, s, (float*)out, tok, (const float*)wte,
                                                          (const float*)wpe, M, T, C, V, flags);
     return cudaGetLastError();
 }
@@ -95,6 +98,7 @@ cudaError_t encoder_forward(ActType at, void* out, const int32_t* tok, const voi
 // llm.c §1.2, position half: dwpe[t,c] = sum over b (ascending) of dout[b,t,c].
 template <typename T>
 __global__ void encoder_bwd_wpe_k(float* dwpe, const T* dout, int B, int Tn, int C, int maxT) {
+    G2_PDL_ENTRY();
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (size_t)maxT * C) return;
     int t = (int)(i / C), c = (int)(i % C);
@@ -107,9 +111,9 @@ cudaError_t encoder_backward_wpe(ActType at, float* dwpe, const void* dout, int 
                                  int maxT, cudaStream_t s) {
     size_t n = (size_t)maxT * C;
     if (at == ACT_BF16)
-        G2_LAUNCH encoder_bwd_wpe_k<bf16><<<cdiv(n, 256), 256, 0, s>>>(dwpe, (const bf16*)dout, B, T, C, maxT);
+        ::g2::launch_k(encoder_bwd_wpe_k<bf16>, cdiv(n, 256), 256, 0, s, dwpe, (const bf16*)dout, B, T, C, maxT);
     else
-        G2_LAUNCH encoder_bwd_wpe_k<float><<<cdiv(n, 256), 256, 0, s>>>(dwpe, (const float*)dout, B, T, C, maxT);
+        ::g2::launch_k(encoder_bwd_wpe_k<float>, cdiv(n, 256), 256, 0, s, dwpe, (const float*)dout, B, T, C, maxT);
     return cudaGetLastError();
 }
 
@@ -144,6 +148,7 @@ void encoder_bwd_scratch_carve(EncoderBwdScratch* sc, void* base, int M, int V, 
 }
 
 __global__ void enc_hist_k(int* chunk_cnt, const int32_t* tok, int M, int V) {
+    G2_PDL_ENTRY();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= M) return;
     int id = tok[i];
@@ -153,6 +158,7 @@ __global__ void enc_hist_k(int* chunk_cnt, const int32_t* tok, int M, int V) {
 // Per token: prefix over chunks (in place: chunk_cnt becomes exclusive chunk prefix)
 // and total count.
 __global__ void enc_chunk_prefix_k(int* chunk_cnt, int* cnt, int nchunks, int V) {
+    G2_PDL_ENTRY();
     int k = blockIdx.x * blockDim.x + threadIdx.x;
     if (k >= V) return;
     int run = 0;
@@ -175,6 +181,7 @@ __global__ void enc_chunk_prefix_k(int* chunk_cnt, int* cnt, int nchunks, int V)
 // thread totals, a running offset carries from tile to tile).  Integer sums: exact.
 constexpr int ENC_SCAN_T = 1024, ENC_SCAN_PER = 8;
 __global__ void __launch_bounds__(ENC_SCAN_T) enc_scan_k(const int* cnt, int* start, int* item_start, int V) {
+    G2_PDL_ENTRY();
     __shared__ int s_cnt[ENC_SCAN_T * ENC_SCAN_PER];
     __shared__ int s_a[32], s_b[32];
     static_assert(ENC_SCAN_T == 1024, "one warp scans the 32 warp totals");
@@ -251,6 +258,7 @@ __global__ void __launch_bounds__(ENC_SCAN_T) enc_scan_k(const int* cnt, int* st
 // One block per chunk: stable destination of every position of the chunk.
 __global__ void enc_rank_k(int* perm, const int32_t* tok, const int* start, const int* chunk_pref,
                            int M, int V) {
+    G2_PDL_ENTRY();
     __shared__ int s_tok[ENC_CHUNK];
     int c = blockIdx.x, base = c * ENC_CHUNK, n = min(ENC_CHUNK, M - base);
     for (int i = threadIdx.x; i < n; i += blockDim.x) s_tok[i] = tok[base + i];
@@ -265,6 +273,7 @@ __global__ void enc_rank_k(int* perm, const int32_t* tok, const int* start, cons
 }
 
 __global__ void enc_items_k(int* item_tok, const int* cnt, const int* item_start, int V) {
+    G2_PDL_ENTRY();
     int k = blockIdx.x * blockDim.x + threadIdx.x;
     if (k >= V) return;
     int n = (cnt[k] + ENC_SEG - 1) / ENC_SEG;
@@ -277,6 +286,7 @@ template <typename T>
 __global__ void enc_seg_k(float* dwte, float* partial, const T* dout, const int* perm,
                           const int* cnt, const int* start, const int* item_start,
                           const int* item_tok, const int* n_items, int C) {
+    G2_PDL_ENTRY();
     int item = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (item >= *n_items) return;
     int k = item_tok[item];
@@ -326,6 +336,7 @@ template <typename T, int NJ>
 __global__ void enc_seg_vec_k(float* dwte, float* partial, const T* dout, const int* perm, const int* cnt,
                               const int* start, const int* item_start, const int* item_tok, const int* n_items,
                               int C) {
+    G2_PDL_ENTRY();
     int item = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (item >= *n_items) return;
     int k = item_tok[item];
@@ -380,6 +391,7 @@ __global__ void enc_seg_vec_k(float* dwte, float* partial, const T* dout, const 
 // else one column per lane in steps of 32.
 __global__ void enc_fix_k(float* dwte, const float* partial, const int* cnt, const int* item_start,
                           int V, int C) {
+    G2_PDL_ENTRY();
     int k = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (k >= V || cnt[k] <= ENC_SEG) return;
     int i0 = item_start[k], i1 = item_start[k + 1];
@@ -417,31 +429,31 @@ cudaError_t encoder_backward_wte(ActType at, float* dwte, const void* dout, cons
     int nch = enc_nchunks(M);
     cudaError_t e = cudaMemsetAsync(sc->chunk_cnt, 0, (size_t)nch * V * sizeof(int), s);
     if (e != cudaSuccess) return e;
-    G2_LAUNCH enc_hist_k<<<cdiv(M, 256), 256, 0, s>>>(sc->chunk_cnt, tok, M, V);
-    G2_LAUNCH enc_chunk_prefix_k<<<cdiv(V, 256), 256, 0, s>>>(sc->chunk_cnt, sc->cnt, nch, V);
-    G2_LAUNCH enc_scan_k<<<1, ENC_SCAN_T, 0, s>>>(sc->cnt, sc->start, sc->item_start, V);
-    G2_LAUNCH enc_rank_k<<<nch, 1024, 0, s>>>(sc->perm, tok, sc->start, sc->chunk_cnt, M, V);
-    G2_LAUNCH enc_items_k<<<cdiv(V, 256), 256, 0, s>>>(sc->item_tok, sc->cnt, sc->item_start, V);
+    ::g2::launch_k(enc_hist_k, cdiv(M, 256), 256, 0, s, sc->chunk_cnt, tok, M, V);
+    ::g2::launch_k(enc_chunk_prefix_k, cdiv(V, 256), 256, 0, s, sc->chunk_cnt, sc->cnt, nch, V);
+    ::g2::launch_k(enc_scan_k, 1, ENC_SCAN_T, 0, s, sc->cnt, sc->start, sc->item_start, V);
+    ::g2::launch_k(enc_rank_k, nch, 1024, 0, s, sc->perm, tok, sc->start, sc->chunk_cnt, M, V);
+    ::g2::launch_k(enc_items_k, cdiv(V, 256), 256, 0, s, sc->item_tok, sc->cnt, sc->item_start, V);
     // Grid covers the maximum item count; the live count is read on the device.
     const int nj = (C % 8 == 0) ? (C + 255) / 256 : 0;
     if (at == ACT_BF16 && nj >= 1 && nj <= 4) {
 #define G2_SEGV(NJ)                                                                                          \
     case NJ:                                                                                                 \
-        G2_LAUNCH enc_seg_vec_k<bf16, NJ><<<cdiv(sc->max_items, 8), 256, 0, s>>>(                            \
+        ::g2::launch_k(enc_seg_vec_k<bf16, NJ>, cdiv(sc->max_items, 8), 256, 0, s,                             \
             dwte, sc->partial, (const bf16*)dout, sc->perm, sc->cnt, sc->start, sc->item_start, sc->item_tok, \
             sc->item_start + V, C);                                                                          \
         break;
         switch (nj) { G2_SEGV(1) G2_SEGV(2) G2_SEGV(3) G2_SEGV(4) }
 #undef G2_SEGV
     } else if (at == ACT_BF16)
-        G2_LAUNCH enc_seg_k<bf16><<<cdiv(sc->max_items, 8), 256, 0, s>>>(
+        ::g2::launch_k(enc_seg_k<bf16>, cdiv(sc->max_items, 8), 256, 0, s, 
             dwte, sc->partial, (const bf16*)dout, sc->perm, sc->cnt, sc->start, sc->item_start,
             sc->item_tok, sc->item_start + V, C);
     else
-        G2_LAUNCH enc_seg_k<float><<<cdiv(sc->max_items, 8), 256, 0, s>>>(
+        ::g2::launch_k(enc_seg_k<float>, cdiv(sc->max_items, 8), 256, 0, s, 
             dwte, sc->partial, (const float*)dout, sc->perm, sc->cnt, sc->start, sc->item_start,
             sc->item_tok, sc->item_start + V, C);
-    G2_LAUNCH enc_fix_k<<<dim3(cdiv(V, 8), cdiv(C, 256)), 256, 0, s>>>(dwte, sc->partial, sc->cnt, sc->item_start,
+    ::g2::launch_k(enc_fix_k, dim3(cdiv(V, 8), cdiv(C, 256)), 256, 0, s, dwte, sc->partial, sc->cnt, sc->item_start,
                                                                         V, C);
     return cudaGetLastError();
 }
@@ -455,6 +467,7 @@ cudaError_t encoder_backward_wte(ActType at, float* dwte, const void* dout, cons
 template <typename T, int NV>
 __global__ void ln_fwd_vec_k(T* out, float* mean, float* rstd, const T* inp, const float* w,
                              const float* b, int M, int C, int rms) {
+    G2_PDL_ENTRY();
     int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (row >= M) return;
     const T* x = inp + (size_t)row * C;
@@ -503,6 +516,7 @@ constexpr int LNT_ROWS = 32, LNT_STAGES = 3, LNT_THREADS = 288;
 template <int NV, bool RMS>
 __global__ void __launch_bounds__(LNT_THREADS, 1) ln_fwd_tma_k(bf16* out, float* mean, float* rstd, const bf16* inp,
                                                                const float* w, const float* b, int M, int C) {
+    G2_PDL_ENTRY();
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tile_bytes = LNT_ROWS * C * 2;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + LNT_STAGES * tile_bytes);
@@ -615,7 +629,7 @@ static cudaError_t ln_fwd_tma_launch_t(bf16* out, float* mean, float* rstd, cons
         attr_done = true;
     }
     const int ntiles = (M + LNT_ROWS - 1) / LNT_ROWS;
-    G2_LAUNCH ln_fwd_tma_k<NV, RMS><<<std::min(ntiles, sm_count()), LNT_THREADS, smem, s>>>(out, mean, rstd, inp, w,
+    ::g2::launch_k(ln_fwd_tma_k<NV, RMS>, std::min(ntiles, sm_count()), LNT_THREADS, smem, s, out, mean, rstd, inp, w,
                                                                                            b, M, C);
     return cudaGetLastError();
 }
@@ -630,6 +644,7 @@ static cudaError_t ln_fwd_tma_launch(bf16* out, float* mean, float* rstd, const 
 template <typename T>
 __global__ void ln_fwd_gen_k(T* out, float* mean, float* rstd, const T* inp, const float* w,
                              const float* b, int M, int C, int rms) {
+    G2_PDL_ENTRY();
     int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (row >= M) return;
     const T* x = inp + (size_t)row * C;
@@ -657,13 +672,13 @@ static void ln_fwd_launch(T* out, float* mean, float* rstd, const T* inp, const 
     unsigned g = cdiv(M, 8);
     const bool aligned = (((uintptr_t)w | (uintptr_t)b) & 15) == 0;
     switch (C % 256 == 0 && aligned ? C / 256 : 0) {
-        case 1: count_launches(1); ln_fwd_vec_k<T, 1><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
-        case 2: count_launches(1); ln_fwd_vec_k<T, 2><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
-        case 3: count_launches(1); ln_fwd_vec_k<T, 3><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
-        case 4: count_launches(1); ln_fwd_vec_k<T, 4><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
-        case 5: count_launches(1); ln_fwd_vec_k<T, 5><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
-        case 6: count_launches(1); ln_fwd_vec_k<T, 6><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
-        default: count_launches(1); ln_fwd_gen_k<T><<<g, 256, 0, s>>>(out, mean, rstd, inp, w, b, M, C, rms); break;
+        case 1: ::g2::launch_k(ln_fwd_vec_k<T, 1>, g, 256, 0, s, out, mean, rstd, inp, w, b, M, C, rms); break;
+        case 2: ::g2::launch_k(ln_fwd_vec_k<T, 2>, g, 256, 0, s, out, mean, rstd, inp, w, b, M, C, rms); break;
+        case 3: ::g2::launch_k(ln_fwd_vec_k<T, 3>, g, 256, 0, s, out, mean, rstd, inp, w, b, M, C, rms); break;
+        case 4: ::g2::launch_k(ln_fwd_vec_k<T, 4>, g, 256, 0, s, out, mean, rstd, inp, w, b, M, C, rms); break;
+        case 5: ::g2::launch_k(ln_fwd_vec_k<T, 5>, g, 256, 0, s, out, mean, rstd, inp, w, b, M, C, rms); break;
+        case 6: ::g2::launch_k(ln_fwd_vec_k<T, 6>, g, 256, 0, s, out, mean, rstd, inp, w, b, M, C, rms); break;
+        default: ::g2::launch_k(ln_fwd_gen_k<T>, g, 256, 0, s, out, mean, rstd, inp, w, b, M, C, rms); break;
     }
 }
 
@@ -712,6 +727,7 @@ template <typename T, int NV, bool OUTSUM>
 __global__ void __launch_bounds__(128) ln_bwd_vec_k(T* dres, float* part, const T* dout, const T* inp,
                                                     const float* w, const float* mean,
                                                     const float* rstd, int M, int C, int rms) {
+    G2_PDL_ENTRY();
     constexpr int NS = OUTSUM ? 3 : 2;
     __shared__ float sh[4][NS][NV * 256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -796,6 +812,7 @@ template <int NV, bool OUTSUM, bool RMS>
 __global__ void __launch_bounds__(LNT_THREADS, 1)
     ln_bwd_tma_k(bf16* dres, float* part, const bf16* dout, const bf16* inp, const float* w, const float* mean,
                  const float* rstd, int M, int C) {
+    G2_PDL_ENTRY();
     extern __shared__ __align__(1024) uint8_t smem[];
     const int sub_bytes = LNB_ROWS * C * 2;  // one tensor's rows of a tile
     const int stage_bytes = 3 * sub_bytes;
@@ -949,6 +966,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) ln_bwd_k(T* dres, float* part, const T* dout, const T* inp,
                                                 const float* w, const float* mean,
                                                 const float* rstd, int M, int C, int rms) {
+    G2_PDL_ENTRY();
     extern __shared__ float sh[];  // [8 warps][2][C]
     int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float* my_dw = sh + (size_t)warp * 2 * C;
@@ -1001,6 +1019,7 @@ __global__ void __launch_bounds__(256) ln_bwd_k(T* dres, float* part, const T* d
 // warp order.  One block per 32 columns.
 __global__ void __launch_bounds__(1024) colreduce_k(float* out0, float* out1, float* out2, const float* part,
                                                     int n, int N) {
+    G2_PDL_ENTRY();
     __shared__ float sh[32][33];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + lane;
@@ -1029,7 +1048,7 @@ __global__ void __launch_bounds__(1024) colreduce_k(float* out0, float* out1, fl
 static cudaError_t colreduce(float* out0, float* out1, float* out2, const float* part, int n, int N,
                              cudaStream_t s) {
     dim3 g(cdiv(N, 32), out2 ? 3 : out1 ? 2 : 1);
-    G2_LAUNCH colreduce_k<<<g, 1024, 0, s>>>(out0, out1, out2, part, n, N);
+    ::g2::launch_k(colreduce_k, g, 1024, 0, s, out0, out1, out2, part, n, N);
     return cudaGetLastError();
 }
 
@@ -1045,7 +1064,7 @@ static cudaError_t ln_bwd_tma_launch_t(bf16* dres, float* part, const bf16* dout
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    G2_LAUNCH ln_bwd_tma_k<NV, OUTSUM, RMS><<<grid, LNT_THREADS, smem, s>>>(dres, part, dout, inp, w, mean, rstd, M,
+    ::g2::launch_k(ln_bwd_tma_k<NV, OUTSUM, RMS>, grid, LNT_THREADS, smem, s, dres, part, dout, inp, w, mean, rstd, M,
                                                                              C);
     return cudaGetLastError();
 }
@@ -1088,10 +1107,10 @@ static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, float* dres_sum,
 #define G2_LNB_CASE(NVV)                                                                                  \
     case NVV:                                                                                             \
         if (dres_sum)                                                                                     \
-            G2_LAUNCH ln_bwd_vec_k<T, NVV, true><<<LNB_VEC_SUM_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, \
+            ::g2::launch_k(ln_bwd_vec_k<T, NVV, true>, LNB_VEC_SUM_BLOCKS, 128, 0, s, dres, part, dout, inp, w, mean, \
                                                                                    rstd, M, C, rms);      \
         else                                                                                              \
-            G2_LAUNCH ln_bwd_vec_k<T, NVV, false><<<LNB_VEC_BLOCKS, 128, 0, s>>>(dres, part, dout, inp, w, mean, \
+            ::g2::launch_k(ln_bwd_vec_k<T, NVV, false>, LNB_VEC_BLOCKS, 128, 0, s, dres, part, dout, inp, w, mean, \
                                                                                 rstd, M, C, rms);         \
         break;
         switch (nv) {
@@ -1104,7 +1123,7 @@ static cudaError_t ln_bwd_launch(T* dres, float* dw, float* db, float* dres_sum,
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(ln_bwd_k<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    G2_LAUNCH ln_bwd_k<T><<<LNB_BLOCKS, 256, smem, s>>>(dres, part, dout, inp, w, mean, rstd, M, C, rms);
+    ::g2::launch_k(ln_bwd_k<T>, LNB_BLOCKS, 256, smem, s, dres, part, dout, inp, w, mean, rstd, M, C, rms);
     cudaError_t e = colreduce(dw, db, nullptr, part, LNB_BLOCKS, C, s);
     if (e != cudaSuccess || !dres_sum) return e;
     // the generic kernel keeps no third sum: column-sum the updated rows separately
@@ -1132,6 +1151,7 @@ size_t colsum_partial_floats(int M, int N) { return (size_t)cdiv(M, CS_ROWS) * N
 
 template <typename T>
 __global__ void __launch_bounds__(256) colsum_part_k(float* part, const T* X, int M, int N) {
+    G2_PDL_ENTRY();
     __shared__ float sh[8][256];
     int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int col = blockIdx.x * 256 + lane * 8;
@@ -1185,9 +1205,9 @@ cudaError_t colsum(ActType at, float* out, const void* X, int M, int N, float* p
     if (nrb > 0) {
         dim3 g(cdiv(N, 256), nrb);
         if (at == ACT_BF16)
-            G2_LAUNCH colsum_part_k<bf16><<<g, 256, 0, s>>>(part, (const bf16*)X, M, N);
+            ::g2::launch_k(colsum_part_k<bf16>, g, 256, 0, s, part, (const bf16*)X, M, N);
         else
-            G2_LAUNCH colsum_part_k<float><<<g, 256, 0, s>>>(part, (const float*)X, M, N);
+            ::g2::launch_k(colsum_part_k<float>, g, 256, 0, s, part, (const float*)X, M, N);
     }
     if (nrb == 0) return cudaMemsetAsync(out, 0, (size_t)N * sizeof(float), s);
     return colreduce(out, nullptr, nullptr, part, nrb, N, s);
@@ -1202,6 +1222,7 @@ template <typename T>
 __global__ void __launch_bounds__(1024) softmax_xent_k(T* logits, float* losses,
                                                        const int32_t* targets, int V, int Vp,
                                                        float dloss, int* flags) {
+    G2_PDL_ENTRY();
     __shared__ float red[32];
     __shared__ float bcast;
     int row = blockIdx.x;
@@ -1334,6 +1355,7 @@ G2_DEV void merge_ms(float& m, float& s, float m2, float s2) {
 __global__ void __launch_bounds__(XE_THREADS) softmax_xent_bf16_k(bf16* logits, float* losses,
                                                                   const int32_t* targets, int V, int Vp,
                                                                   float dloss, int* flags) {
+    G2_PDL_ENTRY();
     __shared__ float red_m[XE_THREADS / 32], red_s[XE_THREADS / 32];
     __shared__ float bcast;
     const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1414,20 +1436,21 @@ cudaError_t softmax_xent(ActType at, void* logits, float* losses, const int32_t*
                          int V, int Vp, float dloss, int* flags, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
     if (at == ACT_BF16 && Vp % 8 == 0 && (((uintptr_t)logits) & 15) == 0) {
-        G2_LAUNCH softmax_xent_bf16_k<<<M, XE_THREADS, 0, s>>>((bf16*)logits, losses, targets, V, Vp, dloss,
+        ::g2::launch_k(softmax_xent_bf16_k, M, XE_THREADS, 0, s, (bf16*)logits, losses, targets, V, Vp, dloss,
                                                                flags);
         return cudaGetLastError();
     }
     if (at == ACT_BF16)
-        G2_LAUNCH softmax_xent_k<bf16><<<M, 1024, 0, s>>>((bf16*)logits, losses, targets, V, Vp, dloss, flags);
+        ::g2::launch_k(softmax_xent_k<bf16>, M, 1024, 0, s, (bf16*)logits, losses, targets, V, Vp, dloss, flags);
     else
-        G2_LAUNCH softmax_xent_k<float><<<M, 1024, 0, s>>>((float*)logits, losses, targets, V, Vp, dloss, flags);
+        ::g2::launch_k(softmax_xent_k<float>, M, 1024, 0, s, (float*)logits, losses, targets, V, Vp, dloss, flags);
     return cudaGetLastError();
 }
 
 // Single block; thread i sums x[i], x[i+1024], ... then a fixed tree.  Also flags a
 // non-finite mean.
 __global__ void mean_k(float* out, const float* x, int n) {
+    G2_PDL_ENTRY();
     __shared__ float sh[1024];
     float a = 0.f;
     for (int i = threadIdx.x; i < n; i += 1024) a += x[i];
@@ -1440,7 +1463,7 @@ __global__ void mean_k(float* out, const float* x, int n) {
     if (threadIdx.x == 0) out[0] = n > 0 ? sh[0] / (float)n : 0.f;
 }
 cudaError_t mean_fixed_order(float* out, const float* x, int n, cudaStream_t s) {
-    G2_LAUNCH mean_k<<<1, 1024, 0, s>>>(out, x, n);
+    ::g2::launch_k(mean_k, 1, 1024, 0, s, out, x, n);
     return cudaGetLastError();
 }
 
@@ -1462,6 +1485,7 @@ G2_DEV void adamw_one(float& p, float g, float& m, float& v, float lr, float b1,
 __global__ void adamw_k(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
                         float* __restrict__ v, bf16* __restrict__ shadow, size_t n4, float lr,
                         float b1, float b2, float eps, float wd, float c1, float c2) {
+    G2_PDL_ENTRY();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
          i += (size_t)gridDim.x * blockDim.x) {
         float4 P = reinterpret_cast<float4*>(p)[i];
@@ -1489,6 +1513,7 @@ __global__ void adamw_k(float* __restrict__ p, const float* __restrict__ g, floa
 __global__ void adamw_tail_k(float* p, const float* g, float* m, float* v, bf16* shadow,
                              size_t from, size_t n, float lr, float b1, float b2, float eps,
                              float wd, float c1, float c2) {
+    G2_PDL_ENTRY();
     size_t i = from + threadIdx.x;
     if (i >= n) return;
     adamw_one(p[i], g[i], m[i], v[i], lr, b1, b2, eps, wd, c1, c2);
@@ -1503,21 +1528,22 @@ cudaError_t adamw(float* p, const float* g, float* m, float* v, bf16* shadow, si
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         unsigned blocks = (unsigned)std::min<size_t>(cdiv(n4, 256), (size_t)sms * 8);
-        G2_LAUNCH adamw_k<<<blocks, 256, 0, s>>>(p, g, m, v, shadow, n4, lr, b1, b2, eps, wd, c1, c2);
+        ::g2::launch_k(adamw_k, blocks, 256, 0, s, p, g, m, v, shadow, n4, lr, b1, b2, eps, wd, c1, c2);
     }
     if (n4 * 4 < n)
-        G2_LAUNCH adamw_tail_k<<<1, 32, 0, s>>>(p, g, m, v, shadow, n4 * 4, n, lr, b1, b2, eps, wd, c1, c2);
+        ::g2::launch_k(adamw_tail_k, 1, 32, 0, s, p, g, m, v, shadow, n4 * 4, n, lr, b1, b2, eps, wd, c1, c2);
     return cudaGetLastError();
 }
 
 __global__ void cast_k(bf16* out, const float* in, size_t n) {
+    G2_PDL_ENTRY();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (size_t)gridDim.x * blockDim.x)
         out[i] = __float2bfloat16_rn(in[i]);
 }
 cudaError_t cast_f32_to_bf16(bf16* out, const float* in, size_t n, cudaStream_t s) {
     if (!n) return cudaSuccess;
-    G2_LAUNCH cast_k<<<(unsigned)std::min<size_t>(cdiv(n, 256), 148 * 16), 256, 0, s>>>(out, in, n);
+    ::g2::launch_k(cast_k, (unsigned)std::min<size_t>(cdiv(n, 256), 148 * 16), 256, 0, s, out, in, n);
     return cudaGetLastError();
 }
 

@@ -18,6 +18,7 @@ namespace {
 // through shared memory (padded against bank conflicts), reads and writes coalesced.
 __global__ void __launch_bounds__(256) transpose_f32_k(float* out, const float* in, int rows, int cols,
                                                         long long ld_in) {
+    G2_PDL_ENTRY();
     __shared__ float t[32][33];
     const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
@@ -35,6 +36,7 @@ __global__ void __launch_bounds__(256) transpose_f32_k(float* out, const float* 
 // mode 0: D += R; mode 1: D2 = gelu(D); mode 2: D *= gelu'(P)
 __global__ void tf32_epilogue_k(float* D, long long ldd, int M, int N, const float* R, long long ldr, float* D2,
                                 long long ldd2, const float* P, long long ldp, int mode) {
+    G2_PDL_ENTRY();
     const size_t n = (size_t)M * N;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const size_t m = i / N, c = i % N;
@@ -66,7 +68,7 @@ cudaError_t gemm_dispatch_tf32(const GemmArgs& a0, float* ws, size_t ws_bytes, c
         const size_t bytes = (size_t)rows_out * K * 4;
         if (!pk || left < bytes) return false;
         dim3 g((rows_out + 31) / 32, (K + 31) / 32);
-        G2_LAUNCH transpose_f32_k<<<g, 256, 0, s>>>(pk, (const float*)src, K, rows_out, ld_in);
+        ::g2::launch_k(transpose_f32_k, g, 256, 0, s, pk, (const float*)src, K, rows_out, ld_in);
         *dst = pk;
         const size_t adv = (bytes + 255) / 256 * 256;
         pk = (float*)((char*)pk + adv);
@@ -100,13 +102,13 @@ cudaError_t gemm_dispatch_tf32(const GemmArgs& a0, float* ws, size_t ws_bytes, c
     if (e != cudaSuccess) return e;
     const size_t n = (size_t)a0.M * a0.N;
     if (a0.epi == EPI_STORE && a0.R)
-        G2_LAUNCH tf32_epilogue_k<<<grid_for(n), 256, 0, s>>>((float*)a0.D, a0.ldd, a0.M, a0.N, (const float*)a0.R,
+        ::g2::launch_k(tf32_epilogue_k, grid_for(n), 256, 0, s, (float*)a0.D, a0.ldd, a0.M, a0.N, (const float*)a0.R,
                                                              a0.ldr, nullptr, 0, nullptr, 0, 0);
     else if (a0.epi == EPI_GELU)
-        G2_LAUNCH tf32_epilogue_k<<<grid_for(n), 256, 0, s>>>((float*)a0.D, a0.ldd, a0.M, a0.N, nullptr, 0,
+        ::g2::launch_k(tf32_epilogue_k, grid_for(n), 256, 0, s, (float*)a0.D, a0.ldd, a0.M, a0.N, nullptr, 0,
                                                              (float*)a0.D2, a0.ldd2, nullptr, 0, 1);
     else if (a0.epi == EPI_GELU_BWD)
-        G2_LAUNCH tf32_epilogue_k<<<grid_for(n), 256, 0, s>>>((float*)a0.D, a0.ldd, a0.M, a0.N, nullptr, 0, nullptr,
+        ::g2::launch_k(tf32_epilogue_k, grid_for(n), 256, 0, s, (float*)a0.D, a0.ldd, a0.M, a0.N, nullptr, 0, nullptr,
                                                              0, (const float*)a0.P, a0.ldp, 2);
     else
         return cudaSuccess;

@@ -14,6 +14,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -25,6 +26,13 @@
 #include "kernels.h"
 
 namespace g2 {
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* v = getenv("G2_PDL");
+        return v && v[0] == '1';
+    }();
+    return on;
+}
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 uint64_t launches_total() { return g_launches.load(std::memory_order_relaxed); }
