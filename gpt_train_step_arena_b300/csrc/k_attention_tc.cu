@@ -246,13 +246,20 @@ __global__ void __launch_bounds__(NTH, 2)
                 for (int i = 0; i < BKV; i++)
                     if (i > r) sv[i] = __float_as_uint(-INFINITY);
             }
-            float m8[8];
+            // row maximum: a tree of three-input maxima (43 + 15 + 5 + 2 + 1 instructions)
+            float t43[43];
 #pragma unroll
-            for (int e = 0; e < 8; e++) m8[e] = __uint_as_float(sv[e]);
+            for (int i = 0; i < 42; i++)
+                t43[i] = max3f(__uint_as_float(sv[3 * i]), __uint_as_float(sv[3 * i + 1]), __uint_as_float(sv[3 * i + 2]));
+            t43[42] = fmaxf(__uint_as_float(sv[126]), __uint_as_float(sv[127]));
+            float t15[15];
 #pragma unroll
-            for (int i = 8; i < BKV; i++) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sv[i]));
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
+            for (int i = 0; i < 14; i++) t15[i] = max3f(t43[3 * i], t43[3 * i + 1], t43[3 * i + 2]);
+            t15[14] = t43[42];
+            const float t5[5] = {max3f(t15[0], t15[1], t15[2]), max3f(t15[3], t15[4], t15[5]),
+                                 max3f(t15[6], t15[7], t15[8]), max3f(t15[9], t15[10], t15[11]),
+                                 max3f(t15[12], t15[13], t15[14])};
+            const float mx = max3f(max3f(t5[0], t5[1], t5[2]), t5[3], t5[4]) * sl2;
             bool resc = false;
             float corr = 1.f;
             if (j == 0) {
@@ -263,19 +270,20 @@ __global__ void __launch_bounds__(NTH, 2)
                 l *= corr;
                 resc = true;
             }
-            // P = 2^(s * sl2 - m) packed to bf16 in registers (S dies as P grows)
-            const float mneg = -m_used;
-            float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            // P = 2^(s * sl2 - m) packed to bf16 in registers (S dies as P grows); the scale
+            // and the row sum run two columns per instruction
+            const float2 sl2x2 = make_float2(sl2, sl2), mneg = make_float2(-m_used, -m_used);
+            float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             uint32_t pk[BKV / 2];
 #pragma unroll
             for (int i = 0; i < BKV; i += 2) {
-                const float p0 = ex2(fmaf(__uint_as_float(sv[i]), sl2, mneg));
-                const float p1 = ex2(fmaf(__uint_as_float(sv[i + 1]), sl2, mneg));
-                l8[i & 7] += p0;
-                l8[(i & 7) + 1] += p1;
-                pk[i >> 1] = pack_bf16x2(p0, p1);
+                const float2 a = fma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sl2x2, mneg);
+                const float2 p = make_float2(ex2(a.x), ex2(a.y));
+                l4[(i >> 1) & 3] = add2(l4[(i >> 1) & 3], p);
+                pk[i >> 1] = pack_bf16x2(p.x, p.y);
             }
-            l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+            const float2 l2 = add2(add2(l4[0], l4[1]), add2(l4[2], l4[3]));
+            l += l2.x + l2.y;
             if (j > 0) {
                 // O and the P buffer are free once P_{j-1} V_{j-1} has completed
                 ok = mbar_wait(&bar->o_done, (j - 1) & 1, abort_flag, flags);
@@ -720,33 +728,35 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
                     const int cbase = grp * 64 + sub * 32 + rd * 16;  // column within the streamed tile
 #pragma unroll
                     for (int c4 = 0; c4 < 16; c4 += 4) {
-                        float Lc[4], Dc[4];
+                        // this column pair's -L (log2 units) and D
+                        float2 nL[2], Dc[2];
                         if (DQ) {
-#pragma unroll
-                            for (int e = 0; e < 4; e++) {
-                                Lc[e] = L2_row;
-                                Dc[e] = D_row;
-                            }
+                            nL[0] = nL[1] = make_float2(-L2_row, -L2_row);
+                            Dc[0] = Dc[1] = make_float2(D_row, D_row);
                         } else {
                             const float4 l4 = *reinterpret_cast<const float4*>(Ls + rd * 16 + c4);
                             const float4 d4 = *reinterpret_cast<const float4*>(Ds + rd * 16 + c4);
-                            Lc[0] = l4.x * LOG2E; Lc[1] = l4.y * LOG2E; Lc[2] = l4.z * LOG2E; Lc[3] = l4.w * LOG2E;
-                            Dc[0] = d4.x; Dc[1] = d4.y; Dc[2] = d4.z; Dc[3] = d4.w;
+                            const float2 nl2e = make_float2(-LOG2E, -LOG2E);
+                            nL[0] = mul2(make_float2(l4.x, l4.y), nl2e);
+                            nL[1] = mul2(make_float2(l4.z, l4.w), nl2e);
+                            Dc[0] = make_float2(d4.x, d4.y);
+                            Dc[1] = make_float2(d4.z, d4.w);
                         }
-                        float pv[4], dsv[4];
 #pragma unroll
-                        for (int e = 0; e < 4; e++) {
-                            const int c = cbase + c4 + e;
-                            // causal: key <= query; DQ rows are queries, key-major rows are keys
-                            const bool vis = !diag || (DQ ? c <= r : r <= c);
-                            const float pr = vis ? ex2(fmaf(__uint_as_float(v[c4 + e]), sl2, -Lc[e])) : 0.f;
-                            pv[e] = pr;
-                            dsv[e] = pr * (__uint_as_float(v[16 + c4 + e]) - Dc[e]);
+                        for (int h = 0; h < 2; h++) {
+                            const int e = c4 + 2 * h;
+                            const float2 a = fma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                  make_float2(sl2, sl2), nL[h]);
+                            float2 p = make_float2(ex2(a.x), ex2(a.y));
+                            if (diag) {  // causal: key <= query; DQ rows are queries, key-major rows are keys
+                                const int c = cbase + e;
+                                if (!(DQ ? c <= r : r <= c)) p.x = 0.f;
+                                if (!(DQ ? c + 1 <= r : r <= c + 1)) p.y = 0.f;
+                            }
+                            const float2 ds = mul2(p, sub2(make_float2(__uint_as_float(v[16 + e]), __uint_as_float(v[17 + e])), Dc[h]));
+                            pk[e >> 1] = pack_bf16x2(p.x, p.y);
+                            dk[e >> 1] = pack_bf16x2(ds.x, ds.y);
                         }
-                        pk[c4 >> 1] = pack_bf16x2(pv[0], pv[1]);
-                        pk[(c4 >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
-                        dk[c4 >> 1] = pack_bf16x2(dsv[0], dsv[1]);
-                        dk[(c4 >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
                     }
                     // packed columns 8 rd .. 8 rd + 7 of this thread's 32: already read
                     if (!DQ) tmem_st8(tb + 8 * rd, pk);

@@ -507,18 +507,22 @@ __global__ void ln_fwd_vec_k(T* out, float* mean, float* rstd, const T* inp, con
     }
 }
 
-// bf16 rows streamed through shared memory: one CTA per SM; warp 0 copies tiles of 32
-// consecutive rows (one contiguous bulk copy each) into a 3-stage ring, warps 1-8
-// normalise 4 rows of each tile from shared memory and store them.  Keeps up to three
-// tiles (3 x 32 rows) in flight per SM without holding them in registers.
-constexpr int LNT_ROWS = 32, LNT_STAGES = 3, LNT_THREADS = 288;
+// bf16 rows streamed through shared memory: one CTA per SM; warp 0 copies tiles of 30
+// consecutive rows (one contiguous bulk copy each) into a 3-stage ring, warps 1-15
+// normalise 2 rows of each tile from shared memory and store them.  Keeps up to three
+// tiles (3 x 30 rows) in flight per SM without holding them in registers.  The pass is
+// bound by the latency of each row's two reductions, not by bytes: 15 compute warps (a
+// 512-thread block keeps 128 registers per thread) and sums formed as trees of two-wide
+// adds keep the chains short.
+constexpr int LNT_STAGES = 3, LNT_THREADS = 288;
+constexpr int LNF_WARPS = 15, LNF_ROWS = 2 * LNF_WARPS, LNF_THREADS = 32 * (LNF_WARPS + 1);
 
 template <int NV, bool RMS>
-__global__ void __launch_bounds__(LNT_THREADS, 1) ln_fwd_tma_k(bf16* out, float* mean, float* rstd, const bf16* inp,
+__global__ void __launch_bounds__(LNF_THREADS, 1) ln_fwd_tma_k(bf16* out, float* mean, float* rstd, const bf16* inp,
                                                                const float* w, const float* b, int M, int C) {
     G2_PDL_ENTRY();
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int tile_bytes = LNT_ROWS * C * 2;
+    const int tile_bytes = LNF_ROWS * C * 2;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + LNT_STAGES * tile_bytes);
     uint64_t* empty = full + LNT_STAGES;
     int* abort_p = reinterpret_cast<int*>(empty + LNT_STAGES);
@@ -526,74 +530,86 @@ __global__ void __launch_bounds__(LNT_THREADS, 1) ln_fwd_tma_k(bf16* out, float*
     if (threadIdx.x == 0) {
         for (int i = 0; i < LNT_STAGES; i++) {
             tc::mbar_init(&full[i], 1);
-            tc::mbar_init(&empty[i], 8);
+            tc::mbar_init(&empty[i], LNF_WARPS);
         }
         *abort_p = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     volatile int* abort_flag = abort_p;
-    const int ntiles = (M + LNT_ROWS - 1) / LNT_ROWS;
+    const int ntiles = (M + LNF_ROWS - 1) / LNF_ROWS;
     if (warp == 0) {
         if (lane == 0) {
             int it = 0;
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x, it++) {
                 const int s = it % LNT_STAGES;
                 if (!tc::mbar_wait(&empty[s], ((it / LNT_STAGES) & 1) ^ 1, abort_flag, nullptr)) break;
-                const int rows = min(LNT_ROWS, M - t * LNT_ROWS);
+                const int rows = min(LNF_ROWS, M - t * LNF_ROWS);
                 const uint32_t bytes = (uint32_t)rows * C * 2;
                 tc::mbar_expect_tx(&full[s], bytes);
-                tc::bulk_load_1d(smem + s * tile_bytes, inp + (size_t)t * LNT_ROWS * C, bytes, &full[s]);
+                tc::bulk_load_1d(smem + s * tile_bytes, inp + (size_t)t * LNF_ROWS * C, bytes, &full[s]);
             }
         }
     } else {
-        // warps 1..8: rows (warp - 1) + 8 i of each tile
-        float wv[NV][8], bv[NV][8];
+        // warps 1..15: rows (warp - 1) + 15 i of each tile; lane owns 8 consecutive columns
+        // of each 256-column slab j, held as 4 pairs
+        float2 wv[NV][4], bv[NV][4];
 #pragma unroll
         for (int j = 0; j < NV; j++) {
-            Vec8<float>::load(w + j * 256 + lane * 8, wv[j]);
-            if (RMS) {
+            float t8[8];
+            Vec8<float>::load(w + j * 256 + lane * 8, t8);
 #pragma unroll
-                for (int i = 0; i < 8; i++) bv[j][i] = 0.f;
-            } else {
-                Vec8<float>::load(b + j * 256 + lane * 8, bv[j]);
-            }
+            for (int i = 0; i < 4; i++) wv[j][i] = make_float2(t8[2 * i], t8[2 * i + 1]);
+            if (!RMS) Vec8<float>::load(b + j * 256 + lane * 8, t8);
+#pragma unroll
+            for (int i = 0; i < 4; i++) bv[j][i] = RMS ? make_float2(0.f, 0.f) : make_float2(t8[2 * i], t8[2 * i + 1]);
         }
         int it = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, it++) {
             const int s = it % LNT_STAGES;
             const bool ok = tc::mbar_wait(&full[s], (it / LNT_STAGES) & 1, abort_flag, nullptr);
             if (!__all_sync(0xffffffffu, ok)) break;
-            const int rows = min(LNT_ROWS, M - t * LNT_ROWS);
+            const int rows = min(LNF_ROWS, M - t * LNF_ROWS);
             const bf16* tile = reinterpret_cast<const bf16*>(smem + s * tile_bytes);
-            for (int r = warp - 1; r < rows; r += 8) {
-                const bf16* x = tile + (size_t)r * C;
-                float v[NV][8];
-                float sum = 0.f;
+            for (int r = warp - 1; r < rows; r += LNF_WARPS) {
+                const uint4* x = reinterpret_cast<const uint4*>(tile + (size_t)r * C);
+                float2 v[NV][4];
 #pragma unroll
                 for (int j = 0; j < NV; j++) {
-                    Vec8<bf16>::load(x + j * 256 + lane * 8, v[j]);
+                    const uint4 u = x[j * 32 + lane];
+                    const uint32_t q4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                    for (int i = 0; i < 8; i++) sum += v[j][i];
+                    for (int i = 0; i < 4; i++) v[j][i] = make_float2(bf16_lo(q4[i]), bf16_hi(q4[i]));
                 }
-                const float m = RMS ? 0.f : warp_sum(sum) / C;
-                float q = 0.f;
+                float m = 0.f;
+                if (!RMS) {
+                    float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int j = 0; j < NV; j++)
-#pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        float d = v[j][i] - m;
-                        q += d * d;
-                    }
-                const float rs = 1.0f / sqrtf(warp_sum(q) / C + 1e-5f);
-                const int row = t * LNT_ROWS + r;
-                bf16* o = out + (size_t)row * C;
+                    for (int j = 0; j < NV; j++) a = add2(a, add2(add2(v[j][0], v[j][1]), add2(v[j][2], v[j][3])));
+                    m = warp_sum(a.x + a.y) / C;
+                }
+                // d = v - m in place, then the sum of squares
+                const float2 nm = make_float2(-m, -m);
+                float2 q = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int j = 0; j < NV; j++) {
-                    float y[8];
 #pragma unroll
-                    for (int i = 0; i < 8; i++) y[i] = (v[j][i] - m) * rs * wv[j][i] + bv[j][i];
-                    Vec8<bf16>::store(o + j * 256 + lane * 8, y);
+                    for (int i = 0; i < 4; i++) v[j][i] = add2(v[j][i], nm);
+                    q = fma2(v[j][0], v[j][0], fma2(v[j][1], v[j][1], fma2(v[j][2], v[j][2], fma2(v[j][3], v[j][3], q))));
+                }
+                const float rs = 1.0f / sqrtf(warp_sum(q.x + q.y) / C + 1e-5f);
+                const float2 rs2 = make_float2(rs, rs);
+                const int row = t * LNF_ROWS + r;
+                uint4* o = reinterpret_cast<uint4*>(out + (size_t)row * C);
+#pragma unroll
+                for (int j = 0; j < NV; j++) {
+                    uint32_t p[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const float2 y = fma2(mul2(v[j][i], rs2), wv[j][i], bv[j][i]);
+                        p[i] = pack_bf16x2_rn(y.x, y.y);
+                    }
+                    o[j * 32 + lane] = make_uint4(p[0], p[1], p[2], p[3]);
                 }
                 if (lane == 0) {
                     if (mean) mean[row] = m;
@@ -620,16 +636,16 @@ static int sm_count() {
 template <int NV, bool RMS>
 static cudaError_t ln_fwd_tma_launch_t(bf16* out, float* mean, float* rstd, const bf16* inp, const float* w,
                                        const float* b, int M, int C, cudaStream_t s) {
-    const int smem = LNT_STAGES * LNT_ROWS * C * 2 + 256;
+    const int smem = LNT_STAGES * LNF_ROWS * C * 2 + 256;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(ln_fwd_tma_k<NV, RMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             LNT_STAGES * LNT_ROWS * (NV * 256) * 2 + 256);
+                                             LNT_STAGES * LNF_ROWS * (NV * 256) * 2 + 256);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    const int ntiles = (M + LNT_ROWS - 1) / LNT_ROWS;
-    ::g2::launch_k(ln_fwd_tma_k<NV, RMS>, std::min(ntiles, sm_count()), LNT_THREADS, smem, s, out, mean, rstd, inp, w,
+    const int ntiles = (M + LNF_ROWS - 1) / LNF_ROWS;
+    ::g2::launch_k(ln_fwd_tma_k<NV, RMS>, std::min(ntiles, sm_count()), LNF_THREADS, smem, s, out, mean, rstd, inp, w,
                                                                                            b, M, C);
     return cudaGetLastError();
 }
@@ -832,13 +848,15 @@ __global__ void __launch_bounds__(LNT_THREADS, 1)
     volatile int* abort_flag = abort_p;
     const int ntiles = (M + LNB_ROWS - 1) / LNB_ROWS;
     constexpr int NS = OUTSUM ? 3 : 2;
-    float aw[NV][8], ab[NV][8], ar[OUTSUM ? NV : 1][8];
+    // per-column sums of this lane's 8 columns of each slab j, as 4 pairs: n*dout (dw),
+    // dout (db) and, with OUTSUM, the stored new dres
+    float2 aw[NV][4], ab[NV][4], ar[OUTSUM ? NV : 1][4];
 #pragma unroll
     for (int j = 0; j < NV; j++)
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            aw[j][i] = ab[j][i] = 0.f;
-            if (OUTSUM) ar[OUTSUM ? j : 0][i] = 0.f;
+        for (int i = 0; i < 4; i++) {
+            aw[j][i] = ab[j][i] = make_float2(0.f, 0.f);
+            if (OUTSUM) ar[OUTSUM ? j : 0][i] = make_float2(0.f, 0.f);
         }
     if (warp == 0) {
         if (lane == 0) {
@@ -857,9 +875,15 @@ __global__ void __launch_bounds__(LNT_THREADS, 1)
             }
         }
     } else {
-        float wv[NV][8];
+        float2 wv[NV][4];
 #pragma unroll
-        for (int j = 0; j < NV; j++) Vec8<float>::load(w + j * 256 + lane * 8, wv[j]);
+        for (int j = 0; j < NV; j++) {
+            float t8[8];
+            Vec8<float>::load(w + j * 256 + lane * 8, t8);
+#pragma unroll
+            for (int i = 0; i < 4; i++) wv[j][i] = make_float2(t8[2 * i], t8[2 * i + 1]);
+        }
+        auto wpair = [&](int j, int i) { return wv[j][i]; };
         // the row statistics of this warp's rows (warp - 1 and warp + 7) are loaded one
         // tile ahead, so no row starts with a dependent global load
         constexpr int RPW = LNB_ROWS / 8;
@@ -892,44 +916,57 @@ __global__ void __launch_bounds__(LNT_THREADS, 1)
                 const int r = warp - 1 + 8 * ri;
                 if (r >= rows) break;
                 const int row = t * LNB_ROWS + r;
-                const bf16* d = reinterpret_cast<const bf16*>(st) + (size_t)r * C;
-                const bf16* x = reinterpret_cast<const bf16*>(st + sub_bytes) + (size_t)r * C;
-                const bf16* dr_in = reinterpret_cast<const bf16*>(st + 2 * sub_bytes) + (size_t)r * C;
-                float dv[NV][8], xv[NV][8];
+                const uint4* d = reinterpret_cast<const uint4*>(st + (size_t)r * C * 2);
+                const uint4* x = reinterpret_cast<const uint4*>(st + sub_bytes + (size_t)r * C * 2);
+                const uint4* dr_in = reinterpret_cast<const uint4*>(st + 2 * sub_bytes + (size_t)r * C * 2);
+                const float rs = cr[ri];
+                const float2 rs2 = make_float2(rs, rs), nmr = make_float2(-cm[ri] * rs, -cm[ri] * rs);
+                // n = (x - mean) rstd (kept in xv), g = w dout (dout kept packed in dk);
+                // row sums of g and g n
+                float2 xv[NV][4];
+                uint32_t dk[NV][4];
+                float2 sg = make_float2(0.f, 0.f), sgn = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int j = 0; j < NV; j++) {
-                    Vec8<bf16>::load(d + j * 256 + lane * 8, dv[j]);
-                    Vec8<bf16>::load(x + j * 256 + lane * 8, xv[j]);
-                }
-                const float m = cm[ri], rs = cr[ri];
-                float gm = 0.f, gnm = 0.f;
+                    const uint4 ud = d[j * 32 + lane], ux = x[j * 32 + lane];
+                    const uint32_t wx[4] = {ux.x, ux.y, ux.z, ux.w};
+                    dk[j][0] = ud.x;
+                    dk[j][1] = ud.y;
+                    dk[j][2] = ud.z;
+                    dk[j][3] = ud.w;
+                    float2 g[4];
 #pragma unroll
-                for (int j = 0; j < NV; j++)
-#pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        const float n = (xv[j][i] - m) * rs;
+                    for (int i = 0; i < 4; i++) {
+                        const float2 dd = make_float2(bf16_lo(dk[j][i]), bf16_hi(dk[j][i]));
+                        const float2 n = fma2(make_float2(bf16_lo(wx[i]), bf16_hi(wx[i])), rs2, nmr);
+                        g[i] = mul2(wpair(j, i), dd);
+                        if (!RMS) ab[j][i] = add2(ab[j][i], dd);
+                        aw[j][i] = fma2(n, dd, aw[j][i]);
                         xv[j][i] = n;
-                        const float g = wv[j][i] * dv[j][i];
-                        gm += g;
-                        gnm += g * n;
-                        if (!RMS) ab[j][i] += dv[j][i];
-                        aw[j][i] += n * dv[j][i];
-                        dv[j][i] = g;
                     }
-                gm = RMS ? 0.f : warp_sum(gm) / C;
-                gnm = warp_sum(gnm) / C;
-                bf16* dr_out = dres + (size_t)row * C;
+                    sg = add2(sg, add2(add2(g[0], g[1]), add2(g[2], g[3])));
+                    sgn = fma2(g[0], xv[j][0], fma2(g[1], xv[j][1], fma2(g[2], xv[j][2], fma2(g[3], xv[j][3], sgn))));
+                }
+                const float gm = RMS ? 0.f : warp_sum(sg.x + sg.y) / C;
+                const float gnm = warp_sum(sgn.x + sgn.y) / C;
+                const float2 ngm = make_float2(-gm, -gm), ngnm = make_float2(-gnm, -gnm);
+                uint4* dr_out = reinterpret_cast<uint4*>(dres + (size_t)row * C);
 #pragma unroll
                 for (int j = 0; j < NV; j++) {
-                    float o[8];
-                    Vec8<bf16>::load(dr_in + j * 256 + lane * 8, o);
+                    const uint4 uo = dr_in[j * 32 + lane];
+                    const uint32_t wo[4] = {uo.x, uo.y, uo.z, uo.w};
+                    uint32_t po[4];
 #pragma unroll
-                    for (int i = 0; i < 8; i++) o[i] += (dv[j][i] - gm - xv[j][i] * gnm) * rs;
-                    Vec8<bf16>::store(dr_out + j * 256 + lane * 8, o);
-                    if (OUTSUM) {
-#pragma unroll
-                        for (int i = 0; i < 8; i++) ar[OUTSUM ? j : 0][i] += to_f(from_f<bf16>(o[i]));
+                    for (int i = 0; i < 4; i++) {
+                        // dres += (g - gm - n gnm) rstd
+                        const float2 g = mul2(wpair(j, i), make_float2(bf16_lo(dk[j][i]), bf16_hi(dk[j][i])));
+                        const float2 v = fma2(xv[j][i], ngnm, add2(g, ngm));
+                        const float2 o = fma2(v, rs2, make_float2(bf16_lo(wo[i]), bf16_hi(wo[i])));
+                        po[i] = pack_bf16x2_rn(o.x, o.y);
+                        if (OUTSUM)  // the column sums of dres as stored
+                            ar[OUTSUM ? j : 0][i] = add2(ar[OUTSUM ? j : 0][i], make_float2(bf16_lo(po[i]), bf16_hi(po[i])));
                     }
+                    dr_out[j * 32 + lane] = make_uint4(po[0], po[1], po[2], po[3]);
                 }
             }
             __syncwarp();
@@ -943,11 +980,19 @@ __global__ void __launch_bounds__(LNT_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < NV; j++)
 #pragma unroll
-            for (int i = 0; i < 8; i++) {
-                const int c = j * 256 + lane * 8 + i;
-                sh[((warp - 1) * NS + 0) * C + c] = aw[j][i];
-                sh[((warp - 1) * NS + 1) * C + c] = ab[j][i];
-                if (OUTSUM) sh[((warp - 1) * NS + 2) * C + c] = ar[OUTSUM ? j : 0][i];
+            for (int i = 0; i < 4; i++) {
+                const int c = j * 256 + lane * 8 + 2 * i;
+                float* s0 = sh + ((warp - 1) * NS + 0) * C + c;
+                float* s1 = sh + ((warp - 1) * NS + 1) * C + c;
+                s0[0] = aw[j][i].x;
+                s0[1] = aw[j][i].y;
+                s1[0] = ab[j][i].x;
+                s1[1] = ab[j][i].y;
+                if (OUTSUM) {
+                    float* s2 = sh + ((warp - 1) * NS + 2) * C + c;
+                    s2[0] = ar[OUTSUM ? j : 0][i].x;
+                    s2[1] = ar[OUTSUM ? j : 0][i].y;
+                }
             }
     }
     __syncthreads();
@@ -1308,48 +1353,69 @@ __global__ void __launch_bounds__(1024) softmax_xent_k(T* logits, float* losses,
 
 // bf16 rows, Vp a multiple of 8, in two passes over the row with one block per row.
 // Pass 1 streams the row from memory; each thread keeps a running maximum m of its
-// columns and the sum s of 2^((x - m) log2 e), rescaling s when a chunk of 8 columns
-// raises m; the block then merges the (m, s) pairs in a fixed tree.  Pass 2 reads the
-// row again -- an L2 hit, it was read microseconds earlier -- and overwrites it with
-// (softmax - onehot) * dloss.  Exponentials are exp2f of pre-scaled arguments.
+// columns (held as mL = m log2 e) and the sum s of 2^(x log2 e - mL), rescaling s when a
+// group of 32 columns raises m; the block then merges the (mL, s) pairs in a fixed tree
+// into lse2 = log2 of the row's sum of exp.  Pass 2 reads the row again -- an L2 hit, it
+// was read microseconds earlier -- and overwrites it with (softmax - onehot) * dloss,
+// dloss > 0 folded into the exponent: softmax * dloss = 2^(x log2 e - (lse2 - log2 dloss)).
+// The pass is bound by issue slots rather than bytes, so the full 8-column chunks take a
+// branch-free body: the hardware 2^x, three-input maxima and two-wide fp32 FMA / add.
 constexpr int XE_THREADS = 512;
 constexpr float XE_LOG2E = 1.4426950408889634f;
 constexpr float XE_LN2 = 0.6931471805599453f;
 
+// 8 bf16 columns of a 16-byte chunk as fp32
 G2_DEV void unpack8(const uint4& u, float* v) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-        float2 t = __bfloat1622float2(h[i]);
-        v[2 * i] = t.x;
-        v[2 * i + 1] = t.y;
+        v[2 * i] = bf16_lo(w[i]);
+        v[2 * i + 1] = bf16_hi(w[i]);
     }
 }
 
-// fold 8 columns (the first nvalid real) into the running (m, s)
-template <bool FULL>
-G2_DEV void xe_fold(const uint4& u, int nvalid, float& m, float& s) {
+// s += 2^(v log2 e - mL) over n (even) columns, two at a time
+template <int N>
+G2_DEV void xe_accum(const float* v, float mL, float2& s) {
+    const float2 l2 = make_float2(XE_LOG2E, XE_LOG2E), nm = make_float2(-mL, -mL);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+        const float2 a = fma2(make_float2(v[i], v[i + 1]), l2, nm);
+        s = add2(s, make_float2(ex2_ftz(a.x), ex2_ftz(a.y)));
+    }
+}
+
+// raise the running maximum to cm (>= m) and rescale s to it
+G2_DEV void xe_raise(float cm, float& m, float& mL, float2& s) {
+    if (cm > m) {  // m = -inf at the start: the factor is 0 and s stays 0
+        const float c = ex2_ftz((m - cm) * XE_LOG2E);
+        s.x *= c;
+        s.y *= c;
+        m = cm;
+        mL = m * XE_LOG2E;
+    }
+}
+
+// the ragged chunk: its first nvalid columns are real
+G2_DEV void xe_fold_part(const uint4& u, int nvalid, float& m, float& mL, float2& s) {
     float v[8];
     unpack8(u, v);
-    float cm = -INFINITY;
+    float cm = m;
 #pragma unroll
     for (int i = 0; i < 8; i++)
-        if (FULL || i < nvalid) cm = fmaxf(cm, v[i]);
-    if (cm > m) {
-        s *= exp2f((m - cm) * XE_LOG2E);  // m = -inf at the start: s stays 0
-        m = cm;
-    }
-    const float ml = m * XE_LOG2E;
+        if (i < nvalid) cm = fmaxf(cm, v[i]);
+    xe_raise(cm, m, mL, s);
 #pragma unroll
     for (int i = 0; i < 8; i++)
-        if (FULL || i < nvalid) s += exp2f(fmaf(v[i], XE_LOG2E, -ml));
+        if (i < nvalid) s.x += ex2_ftz(fmaf(v[i], XE_LOG2E, -mL));
 }
 
-G2_DEV void merge_ms(float& m, float& s, float m2, float s2) {
-    float mn = fmaxf(m, m2);
+// merge (mL2, s2) into (mL, s): both relative to their own scaled maximum
+G2_DEV void merge_ms(float& mL, float& s, float mL2, float s2) {
+    const float mn = fmaxf(mL, mL2);
     if (mn == -INFINITY) return;  // both empty
-    s = s * exp2f((m - mn) * XE_LOG2E) + s2 * exp2f((m2 - mn) * XE_LOG2E);
-    m = mn;
+    s = s * ex2_ftz(mL - mn) + s2 * ex2_ftz(mL2 - mn);
+    mL = mn;
 }
 
 __global__ void __launch_bounds__(XE_THREADS) softmax_xent_bf16_k(bf16* logits, float* losses,
@@ -1367,29 +1433,37 @@ __global__ void __launch_bounds__(XE_THREADS) softmax_xent_bf16_k(bf16* logits, 
     float x_tg = 0.f;
     if (tid == 0 && ok) x_tg = __bfloat162float(x[tg]);
 
-    float m = -INFINITY, s = 0.f;
+    float m = -INFINITY, mL = -INFINITY;
+    float2 s2 = make_float2(0.f, 0.f);
     int k = tid;
     for (; k + 3 * XE_THREADS < nfull; k += 4 * XE_THREADS) {
-        uint4 u[4];
+        float v[32];
 #pragma unroll
-        for (int j = 0; j < 4; j++) u[j] = xv[k + j * XE_THREADS];
+        for (int j = 0; j < 4; j++) unpack8(xv[k + j * XE_THREADS], v + 8 * j);
+        float t[11];
 #pragma unroll
-        for (int j = 0; j < 4; j++) xe_fold<true>(u[j], 8, m, s);
+        for (int i = 0; i < 10; i++) t[i] = max3f(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+        t[10] = max3f(v[30], v[31], m);
+        const float cm = max3f(max3f(t[0], t[1], t[2]), max3f(t[3], t[4], t[5]), max3f(t[6], t[7], max3f(t[8], t[9], t[10])));
+        xe_raise(cm, m, mL, s2);
+        xe_accum<32>(v, mL, s2);
     }
-    for (; k < nreal; k += XE_THREADS) {
-        uint4 u = xv[k];
-        if (k < nfull)
-            xe_fold<true>(u, 8, m, s);
-        else
-            xe_fold<false>(u, V - k * 8, m, s);
+    for (; k < nfull; k += XE_THREADS) {
+        float v[8];
+        unpack8(xv[k], v);
+        const float cm = max3f(max3f(v[0], v[1], v[2]), max3f(v[3], v[4], v[5]), max3f(v[6], v[7], m));
+        xe_raise(cm, m, mL, s2);
+        xe_accum<8>(v, mL, s2);
     }
+    if (k < nreal) xe_fold_part(xv[k], V - k * 8, m, mL, s2);  // the one ragged chunk
+    float s = s2.x + s2.y;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        merge_ms(m, s, m2, s2);
+        const float mL2 = __shfl_xor_sync(0xffffffffu, mL, o), sb = __shfl_xor_sync(0xffffffffu, s, o);
+        merge_ms(mL, s, mL2, sb);
     }
     if (lane == 0) {
-        red_m[warp] = m;
+        red_m[warp] = mL;
         red_s[warp] = s;
     }
     __syncthreads();
@@ -1398,10 +1472,10 @@ __global__ void __launch_bounds__(XE_THREADS) softmax_xent_bf16_k(bf16* logits, 
         float ss = lane < XE_THREADS / 32 ? red_s[lane] : 0.f;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            float m2 = __shfl_xor_sync(0xffffffffu, mm, o), s2 = __shfl_xor_sync(0xffffffffu, ss, o);
-            merge_ms(mm, ss, m2, s2);
+            const float m2 = __shfl_xor_sync(0xffffffffu, mm, o), sb = __shfl_xor_sync(0xffffffffu, ss, o);
+            merge_ms(mm, ss, m2, sb);
         }
-        if (lane == 0) bcast = mm * XE_LOG2E + log2f(ss);  // log2 of the row's sum of exp
+        if (lane == 0) bcast = mm + log2f(ss);  // log2 of the row's sum of exp
     }
     __syncthreads();  // also orders the read of x[tg] before pass 2 overwrites it
     const float lse2 = bcast;
@@ -1409,25 +1483,47 @@ __global__ void __launch_bounds__(XE_THREADS) softmax_xent_bf16_k(bf16* logits, 
         if (!ok && flags) atomicOr(flags, G2_FLAG_BAD_TARGET);
         losses[row] = ok ? lse2 * XE_LN2 - x_tg : 0.f;
     }
+    const float off = lse2 - log2f(dloss);
+    const float2 l2 = make_float2(XE_LOG2E, XE_LOG2E), noff = make_float2(-off, -off);
     const int k_t = ok ? tg >> 3 : -1, e_t = tg & 7;
     uint4* xo = reinterpret_cast<uint4*>(x);
-    for (k = tid; k < nch; k += XE_THREADS) {
-        uint4 u = __ldcs(xv + k);
-        float v[8];
-        unpack8(u, v);
-        uint4 o;
-        __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+    for (k = tid; k < nfull; k += XE_THREADS) {
+        const uint4 u = __ldcs(xv + k);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        float g[8];
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            const int c0 = k * 8 + 2 * i;
-            float g0 = c0 < V ? exp2f(fmaf(v[2 * i], XE_LOG2E, -lse2)) * dloss : 0.f;
-            float g1 = c0 + 1 < V ? exp2f(fmaf(v[2 * i + 1], XE_LOG2E, -lse2)) * dloss : 0.f;
-            if (k == k_t) {
-                g0 -= e_t == 2 * i ? dloss : 0.f;
-                g1 -= e_t == 2 * i + 1 ? dloss : 0.f;
-            }
-            oh[i] = __floats2bfloat162_rn(g0, g1);
+            const float2 a = fma2(make_float2(bf16_lo(w[i]), bf16_hi(w[i])), l2, noff);
+            g[2 * i] = ex2_ftz(a.x);
+            g[2 * i + 1] = ex2_ftz(a.y);
         }
+        if (k == k_t) {
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                if (i == e_t) g[i] -= dloss;
+        }
+        uint4 o;
+        o.x = pack_bf16x2_rn(g[0], g[1]);
+        o.y = pack_bf16x2_rn(g[2], g[3]);
+        o.z = pack_bf16x2_rn(g[4], g[5]);
+        o.w = pack_bf16x2_rn(g[6], g[7]);
+        __stcs(xo + k, o);
+    }
+    // the ragged chunk and the padding columns
+    for (k = nfull + tid; k < nch; k += XE_THREADS) {
+        const uint4 u = __ldcs(xv + k);
+        float v[8], g[8];
+        unpack8(u, v);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const int c = k * 8 + i;
+            g[i] = c < V ? ex2_ftz(fmaf(v[i], XE_LOG2E, -off)) - (c == tg && ok ? dloss : 0.f) : 0.f;
+        }
+        uint4 o;
+        o.x = pack_bf16x2_rn(g[0], g[1]);
+        o.y = pack_bf16x2_rn(g[2], g[3]);
+        o.z = pack_bf16x2_rn(g[4], g[5]);
+        o.w = pack_bf16x2_rn(g[6], g[7]);
         __stcs(xo + k, o);
     }
 }
@@ -1435,7 +1531,8 @@ __global__ void __launch_bounds__(XE_THREADS) softmax_xent_bf16_k(bf16* logits, 
 cudaError_t softmax_xent(ActType at, void* logits, float* losses, const int32_t* targets, int M,
                          int V, int Vp, float dloss, int* flags, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
-    if (at == ACT_BF16 && Vp % 8 == 0 && (((uintptr_t)logits) & 15) == 0) {
+    // the fast kernel folds log2(dloss) into the exponent: dloss must be positive and finite
+    if (at == ACT_BF16 && Vp % 8 == 0 && (((uintptr_t)logits) & 15) == 0 && dloss > 0.f && dloss < INFINITY) {
         ::g2::launch_k(softmax_xent_bf16_k, M, XE_THREADS, 0, s, (bf16*)logits, losses, targets, V, Vp, dloss,
                                                                flags);
         return cudaGetLastError();
