@@ -14,8 +14,9 @@ size_t gemm_tc_workspace_bytes(int M, int N, int K);
 size_t gemm_tc_skinny_workspace_bytes(int M, int N, int K);
 // flags (may be null): G2_FLAG_TIMEOUT is OR-ed in if a bounded wait expires.
 cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, cudaStream_t s);
-// Tile-height override for every later product (128 or 256; anything else: chosen per
-// shape); returns the previous setting.  Products with a staged epilogue input ignore it.
+// Tile override for every later product (128 or 256 rows on one SM, 2 for two-SM CTA
+// pairs; anything else: chosen per shape); returns the previous setting.  Products with a
+// staged epilogue input never take 256-row tiles on one SM.
 int gemm_tc_force_tile_rows(int rows);
 // "rows=.. cols=.. splits=.. a=k|mn b=k|mn epi=.." of the last launch ("none" before any).
 void gemm_tc_last_variant(char* out, size_t n);

@@ -76,7 +76,9 @@ struct Params {
     int* flags;
 };
 
-template <int BN, int BMT, int EPI>
+// PAIR: the tile is computed by a cluster of two CTAs on two SMs (cta_group::2): each CTA
+// holds 128 rows of A and BN/2 rows of B per stage and receives its 128 accumulator rows.
+template <int BN, int BMT, int EPI, bool PAIR = false>
 struct Cfg {
     static constexpr int HALVES = BMT / BM;                 // 128-row accumulator halves per tile
     // The GELU' epilogue (FC-projection input gradient) is latency-bound with one epilogue
@@ -84,12 +86,16 @@ struct Cfg {
     // each draining half of the tile's columns, with one staged-input buffer each so the
     // pipeline keeps three stages (measured: 186 -> 162 us per layer at B=32, T=1024;
     // two input buffers and two stages: 189 us).  The residual epilogue gains nothing.
-    static constexpr int COLSPLIT = (HALVES == 1 && EPI == E_GELU_BWD) ? 2 : 1;
+    // Pair tiles finish a K = 768 mainloop in about 6,000 clocks, so their bias + GELU and
+    // residual epilogues get the column split too.
+    static constexpr int COLSPLIT =
+        (HALVES == 1 && (EPI == E_GELU_BWD || (PAIR && (EPI == E_GELU || EPI == E_STORE_RES)))) ? 2 : 1;
     static constexpr int EPI_WARPS = 4 * HALVES * COLSPLIT;  // per 32-lane quarter, per half, per column part
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;     // + TMA warp + MMA warp
     static constexpr int NIN = COLSPLIT == 2 ? 1 : 2;       // staged-input buffers per warp
     static constexpr int A_BYTES = BMT * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;     // rows of B this CTA stages
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     // each epilogue warp stages 32 rows x 128 bytes per output for the TMA store
     // output staging: two sets on 128-row tiles (a chunk's stores need not have finished
@@ -200,16 +206,22 @@ G2_DEV void stage_row(uint8_t* buf, int lane, const float* v) {
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int BN, int BMT, bool A_MN, bool B_MN, int EPI, bool TF = false>
-__global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
+template <int BN, int BMT, bool A_MN, bool B_MN, int EPI, bool TF = false, bool PAIR = false>
+__global__ void __launch_bounds__(Cfg<BN, BMT, EPI, PAIR>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                    const __grid_constant__ CUtensorMap tmX, const Params p) {
     G2_PDL_ENTRY();
-    using CF = Cfg<BN, BMT, EPI>;
+    using CF = Cfg<BN, BMT, EPI, PAIR>;
     using EO = EpiOut<EPI>;
     using OT = OperandT<TF>;
     static_assert(!TF || (!A_MN && !B_MN), "TF32 products take K-major operands only");
+    static_assert(!PAIR || (BMT == BM && !TF && BN == 256), "CTA pairs: 128 rows per CTA, bf16, BN = 256");
+    // a work unit covers TILE_M rows: a CTA pair splits them 128 / 128 by cluster rank
+    constexpr int TILE_M = PAIR ? 2 * BM : BMT;
+    const uint32_t rank = PAIR ? cluster_rank() : 0u;
+    const int u0 = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+    const int ustep = PAIR ? (int)num_clusters_x() : (int)gridDim.x;
     constexpr int S = CF::STAGES, NB = CF::ACC_BUFS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -227,13 +239,15 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         s_abort = 0;
+        // a pair's leader: both CTAs' epilogue warps release an accumulator
+        const bool lead = PAIR && rank == 0;
         for (int i = 0; i < S; i++) {
             mbar_init(&full_bar[i], 1);
             mbar_init(&empty_bar[i], 1);
         }
         for (int i = 0; i < NB; i++) {
             mbar_init(&tfull_bar[i], 1);
-            mbar_init(&tempty_bar[i], CF::EPI_WARPS);
+            mbar_init(&tempty_bar[i], lead ? 2 * CF::EPI_WARPS : CF::EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
         for (int i = 0; i < 2 * CF::EPI_WARPS; i++) mbar_init(&in_bar[i], 1);
@@ -243,22 +257,32 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmD);
     }
-    if (warp == 1) tmem_alloc(tmem_slot, CF::TMEM_COLS);
+    if (warp == 1) {
+        if constexpr (PAIR)
+            tmem_alloc_pair(tmem_slot, CF::TMEM_COLS);
+        else
+            tmem_alloc(tmem_slot, CF::TMEM_COLS);
+    }
     tc_fence_before();
-    __syncthreads();
+    if (PAIR)
+        cluster_sync();  // both CTAs' barriers and tensor memory exist before any cross-CTA signal
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     volatile int* abort_flag = &s_abort;
 
     if (warp == 0) {
-        // ---------------- TMA producer
+        // ---------------- TMA producer (a pair: each CTA loads its halves; both halves of a
+        // stage complete on the leader's barrier, which expects the bytes of both)
         if (lane == 0) {
+            const uint32_t lead_full = PAIR ? mapa_rank(smem_u32(full_bar), 0) : 0u;
             int stage = 0;
             uint32_t phase = 0;
             int issued_phase[S];
             for (int i = 0; i < S; i++) issued_phase[i] = -1;
             bool ok = true;
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+            for (int u = u0; u < p.num_units && ok; u += ustep) {
                 int mb, nb, sp;
                 unit_coords(p, u, mb, nb, sp);
                 int kb0 = sp * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
@@ -269,21 +293,27 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
                     }
                     uint8_t* sa = smem + stage * CF::STAGE_BYTES;
                     uint8_t* sb = sa + CF::A_BYTES;
-                    mbar_expect_tx(&full_bar[stage], CF::STAGE_BYTES);
+                    if (!PAIR || rank == 0) mbar_expect_tx(&full_bar[stage], (PAIR ? 2 : 1) * CF::STAGE_BYTES);
                     const int k0 = kb * OT::BKE;
+                    const int arow = mb * TILE_M + (int)rank * BM;           // this CTA's A rows
+                    const int bcol = nb * BN + (int)rank * CF::B_ROWS;      // and its B rows (N)
+                    auto load = [&](const CUtensorMap* tm, void* dst, int x, int y) {
+                        if constexpr (PAIR)
+                            tma_load_2d_pair(tm, lead_full + (uint32_t)stage * 8u, dst, x, y);
+                        else
+                            tma_load_2d(tm, &full_bar[stage], dst, x, y);
+                    };
                     if (!A_MN) {
-                        tma_load_2d(&tmA, &full_bar[stage], sa, k0, mb * BMT);
+                        load(&tmA, sa, k0, arow);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BMT / 64; j++)
-                            tma_load_2d(&tmA, &full_bar[stage], sa + j * 64 * BK * 2, mb * BMT + 64 * j, k0);
+                        for (int j = 0; j < BMT / 64; j++) load(&tmA, sa + j * 64 * BK * 2, arow + 64 * j, k0);
                     }
                     if (!B_MN) {
-                        tma_load_2d(&tmB, &full_bar[stage], sb, k0, nb * BN);
+                        load(&tmB, sb, k0, bcol);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; j++)
-                            tma_load_2d(&tmB, &full_bar[stage], sb + j * 64 * BK * 2, nb * BN + 64 * j, k0);
+                        for (int j = 0; j < CF::B_ROWS / 64; j++) load(&tmB, sb + j * 64 * BK * 2, bcol + 64 * j, k0);
                     }
                     issued_phase[stage] = (int)phase;
                     if (++stage == S) {
@@ -292,8 +322,9 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
                     }
                 }
             }
-            if (!ok) {
-                // drain: wait (bounded) for every load still in flight before returning
+            if (!ok && (!PAIR || rank == 0)) {
+                // drain: wait (bounded) for every load still in flight before returning (the
+                // leader's barriers also count the second CTA's loads)
                 for (int i = 0; i < S; i++) {
                     if (issued_phase[i] < 0) continue;
                     unsigned long long t0 = globaltimer();
@@ -301,19 +332,36 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
                            globaltimer() - t0 < TIMEOUT_NS) {
                     }
                 }
+            } else if (!ok) {
+                // the second CTA cannot observe its loads: give those issued time to land
+                const unsigned long long t0 = globaltimer();
+                while (globaltimer() - t0 < 100000ull) {
+                }
             }
         }
+    } else if (warp == 1 && PAIR && rank != 0) {
+        // ---------------- the pair's second CTA issues no MMAs
     } else if (warp == 1) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer (the leader of a pair issues for both CTAs)
         if (lane == 0) {
-            constexpr uint32_t IDESC = TF ? make_idesc_tf32(BN) : make_idesc(BN, A_MN, B_MN);
+            constexpr uint32_t IDESC = TF ? make_idesc_tf32(BN) : make_idesc(BN, A_MN, B_MN, PAIR ? 2 * BM : BM);
+            // completion of the MMAs issued so far, as an arrive on this CTA's barrier and, for
+            // a pair, on the same barrier of the second CTA
+            auto commit_both = [&](uint64_t* b) {
+                if constexpr (PAIR) {
+                    umma_commit_pair(smem_u32(b));
+                    umma_commit_pair(mapa_rank(smem_u32(b), 1));
+                } else {
+                    umma_commit(b);
+                }
+            };
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
             bool issued_any = false;
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+            for (int u = u0; u < p.num_units && ok; u += ustep) {
                 int mb, nb, sp;
                 unit_coords(p, u, mb, nb, sp);
                 int kb0 = sp * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
@@ -348,21 +396,23 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
                                 bd = sdesc(sb + k * UMMA_K * 128, 64 * BK * 2, 1024);
                             // K-major: the k-th MMA's operands start 32 bytes further along the
                             // 128-byte row (16 bf16 or 8 fp32)
-                            if (TF)
+                            if constexpr (TF)
                                 umma_tf32(d_tmem + hh * BN, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                            else if constexpr (PAIR)
+                                umma_bf16_pair(d_tmem + hh * BN, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
                             else
                                 umma_bf16(d_tmem + hh * BN, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
                         }
                     }
                     issued_any = true;
-                    umma_commit(&empty_bar[stage]);
+                    commit_both(&empty_bar[stage]);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                umma_commit(&tfull_bar[acc]);
+                commit_both(&tfull_bar[acc]);
                 if (++acc == NB) {
                     acc = 0;
                     acc_phase ^= 1;
@@ -370,7 +420,10 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
             }
             if (!ok && issued_any) {
                 // drain: all MMAs issued so far complete before this commit arrives
-                umma_commit(drain_bar);
+                if constexpr (PAIR)
+                    umma_commit_pair(smem_u32(drain_bar));
+                else
+                    umma_commit(drain_bar);
                 unsigned long long t0 = globaltimer();
                 while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < TIMEOUT_NS) {
                 }
@@ -415,10 +468,10 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
             }
             __syncwarp();
         };
-        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        for (int u = u0; u < p.num_units; u += ustep) {
             int mb, nb, sp;
             unit_coords(p, u, mb, nb, sp);
-            const int gm = mb * BMT + row_in_tile;
+            const int gm = mb * TILE_M + (int)rank * BM + row_in_tile;
             const int gm0 = gm - lane;  // first row of this warp's 32
             constexpr int NCH = BN / EO::CW / CF::COLSPLIT;  // chunks of this warp
             if (EO::IN) {
@@ -499,7 +552,12 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+            if (lane == 0) {  // a pair's accumulator is free once both CTAs have read theirs
+                if (PAIR && rank != 0)
+                    mbar_arrive_remote(mapa_rank(smem_u32(&tempty_bar[acc]), 0));
+                else
+                    mbar_arrive(&tempty_bar[acc]);
+            }
             if (++acc == NB) {
                 acc = 0;
                 acc_phase ^= 1;
@@ -510,8 +568,14 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI>::THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // neither CTA leaves while the other may still signal it
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, CF::TMEM_COLS);
+    if (warp == 1) {
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, CF::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, CF::TMEM_COLS);
+    }
 }
 
 // Fixed-order sum of the split-K partials: out[i] = sum_s ws[s][i].
@@ -559,19 +623,63 @@ static int num_sms() {
     return n;
 }
 
-template <int BN, int BMT, bool A_MN, bool B_MN, int EPI, bool TF = false>
+// Tile mode of a bf16 product: 128- or 256-row tiles on one SM each, or TILE_PAIR: 256-row
+// tiles computed by a cluster of two CTAs (128 rows each, cta_group::2).
+constexpr int TILE_PAIR = 2;
+
+// Clusters of two CTAs of the pair kernel that can be resident at once (0: pairs are not
+// available), from the occupancy calculator on one representative instantiation: every
+// pair instantiation takes the whole shared memory of its SM.
+static int pair_max_clusters() {
+    static int n = -1;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        using CF = Cfg<256, 128, E_STORE, true>;
+        auto kern = gemm_tc_kernel<256, 128, false, false, E_STORE, false, true>;
+        int v = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * num_sms());
+            cfg.blockDim = dim3(CF::THREADS);
+            cfg.dynamicSmemBytes = CF::SMEM_BYTES;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&v, kern, &cfg) != cudaSuccess) {
+                v = 0;
+                cudaGetLastError();
+            }
+        } else {
+            cudaGetLastError();
+        }
+        n = v;
+    });
+    return n;
+}
+
+template <int BN, int BMT, bool A_MN, bool B_MN, int EPI, bool TF = false, bool PAIR = false>
 static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
                             const CUtensorMap& td2, const CUtensorMap& tx, const Params& p, cudaStream_t s) {
-    using CF = Cfg<BN, BMT, EPI>;
-    auto kern = gemm_tc_kernel<BN, BMT, A_MN, B_MN, EPI, TF>;
+    using CF = Cfg<BN, BMT, EPI, PAIR>;
+    auto kern = gemm_tc_kernel<BN, BMT, A_MN, B_MN, EPI, TF, PAIR>;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    int grid = std::min(p.num_units, num_sms());
-    ::g2::launch_k(kern, grid, CF::THREADS, CF::SMEM_BYTES, s, ta, tb, td, td2, tx, p);
+    if constexpr (PAIR) {
+        const int clusters = std::min(p.num_units, pair_max_clusters());
+        if (clusters < 1) return cudaErrorNotSupported;
+        ::g2::launch_k_cluster(kern, 2 * clusters, CF::THREADS, CF::SMEM_BYTES, s, 2u, ta, tb, td, td2, tx, p);
+    } else {
+        int grid = std::min(p.num_units, num_sms());
+        ::g2::launch_k(kern, grid, CF::THREADS, CF::SMEM_BYTES, s, ta, tb, td, td2, tx, p);
+    }
     return cudaGetLastError();
 }
 
@@ -581,6 +689,16 @@ struct Maps {
 
 template <int BN, int EPI>
 static cudaError_t launch_layout(int bmt, bool a_mn, bool b_mn, const Maps& m, const Params& p, cudaStream_t s) {
+    if (bmt == TILE_PAIR) {
+        if constexpr (BN == 256) {
+            if (!a_mn && !b_mn) return launch_t<BN, 128, false, false, EPI, false, true>(m.a, m.b, m.d, m.d2, m.x, p, s);
+            if (!a_mn && b_mn) return launch_t<BN, 128, false, true, EPI, false, true>(m.a, m.b, m.d, m.d2, m.x, p, s);
+            if (a_mn && b_mn) return launch_t<BN, 128, true, true, EPI, false, true>(m.a, m.b, m.d, m.d2, m.x, p, s);
+            return launch_t<BN, 128, true, false, EPI, false, true>(m.a, m.b, m.d, m.d2, m.x, p, s);
+        } else {
+            return cudaErrorNotSupported;
+        }
+    }
     if (bmt == 256) {
         if (!a_mn && !b_mn) return launch_t<BN, 256, false, false, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
         if (!a_mn && b_mn) return launch_t<BN, 256, false, true, EPI>(m.a, m.b, m.d, m.d2, m.x, p, s);
@@ -632,14 +750,33 @@ static char g_variant[128] = "none";
 static int tile_rows(int M, int N, int K, int BN, bool staged_input = false) {
     if (staged_input) return 128;
     const int forced = g_force_rows.load(std::memory_order_relaxed);
-    if (forced) return forced;
+    if (forced == 128 || forced == 256) return forced;
     const long long tiles128 = (long long)((M + 127) / 128) * ((N + BN - 1) / BN);
     const bool long_k = K >= 2048 && tiles128 >= 4LL * num_sms();
     const bool very_many_tiles = tiles128 >= 64LL * num_sms();  // e.g. the LM head forward
     return (long_k || very_many_tiles) ? 256 : 128;
 }
 
-int gemm_tc_force_tile_rows(int rows) { return g_force_rows.exchange(rows == 128 || rows == 256 ? rows : 0); }
+int gemm_tc_force_tile_rows(int rows) {
+    return g_force_rows.exchange(rows == 128 || rows == 256 || rows == TILE_PAIR ? rows : 0);
+}
+
+// Tile mode of a bf16 product.  CTA pairs (256-row tiles, 128 rows and half of B per SM:
+// 32 KB of operands per SM per 512 clocks of tensor work, against 48 KB for a 128-row tile
+// on one SM, with the accumulator still double-buffered) for the forward layout (A and B
+// K-major) with 256-column tiles and more than one row tile: measured at B=32, T=1024 they
+// beat the best one-SM tiles by 2-5% (QKV 91 -> 87 us, LM head 1.80 -> 1.70 ms, bias +
+// GELU 153 -> 150 us, residual 46.1 -> 45.2 us); on the input- and weight-gradient
+// layouts they tie or lose (LM-head gradients 1.57 / 1.45 ms on 256-row tiles against
+// 1.71 / 1.55 ms).  The forced setting when given; one-SM tiles when pairs cannot launch.
+static int tile_mode(int M, int N, int K, int BN, bool staged_input, bool skinny, bool fwd_layout) {
+    const int forced = g_force_rows.load(std::memory_order_relaxed);
+    const bool pair_ok = BN == 256 && !skinny && M > 128 && pair_max_clusters() > 0;
+    if (forced == TILE_PAIR) return pair_ok ? TILE_PAIR : tile_rows(M, N, K, BN, staged_input);
+    if (forced) return tile_rows(M, N, K, BN, staged_input);
+    if (pair_ok && fwd_layout) return TILE_PAIR;
+    return tile_rows(M, N, K, BN, staged_input);
+}
 
 void gemm_tc_note_variant(const char* v) {
     std::lock_guard<std::mutex> lk(g_variant_mu);
@@ -653,9 +790,8 @@ void gemm_tc_last_variant(char* out, size_t n) {
 
 // Split-K plan for a product with few output tiles and a long K (bke: elements per K
 // block, 64 for bf16 operands, 32 for fp32 ones).
-static void plan(int M, int N, int K, int BN, int& splits, int& kb_per, int bke = BK) {
-    const int bmt = tile_rows(M, N, K, BN);
-    int tiles = ((M + bmt - 1) / bmt) * ((N + BN - 1) / BN);
+static void plan(int M, int N, int K, int BN, int rows, int& splits, int& kb_per, int bke = BK) {
+    int tiles = ((M + rows - 1) / rows) * ((N + BN - 1) / BN);
     int num_kb = (K + bke - 1) / bke;
     int sms = num_sms();
     splits = 1;
@@ -694,11 +830,16 @@ size_t gemm_tc_skinny_workspace_bytes(int M, int N, int K) {
 }
 
 size_t gemm_tc_workspace_bytes(int M, int N, int K) {
-    int BN = N > 128 ? 256 : 128, splits, kb_per;
-    plan(M, N, K, BN, splits, kb_per);
-    size_t b = splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
-    plan(M, N, K, BN, splits, kb_per, 32);  // the same product with fp32 (TF32) operands
-    return std::max(b, splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0);
+    // the most splits any tile height or operand type can plan
+    const int BN = N > 128 ? 256 : 128;
+    size_t b = 0;
+    for (int rows : {128, 256})
+        for (int bke : {BK, 32}) {
+            int splits, kb_per;
+            plan(M, N, K, BN, rows, splits, kb_per, bke);
+            if (splits > 1) b = std::max(b, (size_t)splits * M * N * sizeof(float));
+        }
+    return b;
 }
 
 // TF32 products (fp32 operands): both operands K-major, rows 16-byte aligned, fp32
@@ -756,7 +897,7 @@ static cudaError_t gemm_tc_tf32(const GemmArgs& a, float* ws, size_t ws_bytes, i
     p.tiles_n = (a.N + BN - 1) / BN;
     p.num_kb = (a.K + BKE - 1) / BKE;
     int splits = 1, kb_per = p.num_kb;
-    if (!a.bias) plan(a.M, a.N, a.K, BN, splits, kb_per, BKE);
+    if (!a.bias) plan(a.M, a.N, a.K, BN, bmt, splits, kb_per, BKE);
     if (splits > 1 && (!ws || ws_bytes < (size_t)splits * a.M * a.N * sizeof(float) || a.N % 4)) {
         splits = 1;
         kb_per = p.num_kb;
@@ -805,30 +946,32 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
     const bool skinny = a.skinny_split && a.M <= 128 && a.epi != EPI_GELU_BWD;
     const int BN = skinny ? skinny_bn(a.M, a.N) : (a.N > 128 ? 256 : 128);
     const bool staged_in = a.epi == EPI_GELU_BWD || (a.epi == EPI_STORE && a.R && !a.d_f32);
-    const int bmt = tile_rows(a.M, a.N, a.K, BN, staged_in);
+    const int bmt = tile_mode(a.M, a.N, a.K, BN, staged_in, skinny, !a_mn && !b_mn);
+    const int unit_rows = bmt == 128 ? 128 : 256;  // rows of a work unit (a pair: 128 per SM)
+    const int a_box = bmt == 256 ? 256 : 128, b_box = bmt == TILE_PAIR ? BN / 2 : BN;
     Maps mp;
     bool ok;
     if (!a_mn)
-        ok = make_map(&mp.a, a.A, a.K, a.M, a.sAm, BK, bmt);
+        ok = make_map(&mp.a, a.A, a.K, a.M, a.sAm, BK, a_box);
     else
         ok = make_map(&mp.a, a.A, a.M, a.K, a.sAk, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
     if (!b_mn)
-        ok = make_map(&mp.b, a.B, a.K, a.N, a.sBn, BK, BN);
+        ok = make_map(&mp.b, a.B, a.K, a.N, a.sBn, BK, b_box);
     else
         ok = make_map(&mp.b, a.B, a.N, a.K, a.sBk, 64, BK);
     if (!ok) return cudaErrorInvalidValue;
 
     Params p{};
     p.M = a.M; p.N = a.N; p.K = a.K;
-    p.tiles_m = (a.M + bmt - 1) / bmt;
+    p.tiles_m = (a.M + unit_rows - 1) / unit_rows;
     p.tiles_n = (a.N + BN - 1) / BN;
     p.num_kb = (a.K + BK - 1) / BK;
     int splits = 1, kb_per = p.num_kb;
     if (skinny)
         plan_skinny(a.M, a.N, a.K, BN, splits, kb_per);
     else if (a.epi == EPI_STORE && a.d_f32 && !a.bias && !a.R)
-        plan(a.M, a.N, a.K, BN, splits, kb_per);
+        plan(a.M, a.N, a.K, BN, unit_rows, splits, kb_per);
     if (splits > 1 && (!ws || ws_bytes < (size_t)splits * a.M * a.N * sizeof(float))) {
         splits = 1;
         kb_per = p.num_kb;
@@ -876,9 +1019,12 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
     {
         static const char* epi_names[] = {"store", "gelu", "gelu_bwd"};
         std::lock_guard<std::mutex> lk(g_variant_mu);
-        snprintf(g_variant, sizeof g_variant, "rows=%d cols=%d splits=%d a=%s b=%s epi=%s%s%s", bmt, BN, splits,
+        char pairs[32] = "";
+        if (bmt == TILE_PAIR) snprintf(pairs, sizeof pairs, " clusters=%d", pair_max_clusters());
+        snprintf(g_variant, sizeof g_variant, "rows=%s cols=%d splits=%d a=%s b=%s epi=%s%s%s%s",
+                 bmt == TILE_PAIR ? "pair256" : (bmt == 256 ? "256" : "128"), BN, splits,
                  a_mn ? "mn" : "k", b_mn ? "mn" : "k", epi_names[a.epi], a.d_f32 ? " f32" : "",
-                 staged_in && a.epi == EPI_STORE ? " residual" : "");
+                 staged_in && a.epi == EPI_STORE ? " residual" : "", pairs);
     }
     cudaError_t e;
     if (splits > 1) {

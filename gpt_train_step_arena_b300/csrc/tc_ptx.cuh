@@ -81,6 +81,34 @@ G2_DEV bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort_
 G2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* flags) {
     return mbar_wait_limit(bar, parity, abort_flag, flags, TIMEOUT_NS);
 }
+// Non-blocking test of phase `parity`.
+G2_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// As mbar_wait, but polling without ever suspending the thread: for barriers completed
+// by another SM of the cluster, whose arrivals need not wake a suspended waiter early.
+G2_DEV bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* flags) {
+    if (mbar_test_wait(bar, parity)) return true;
+    unsigned long long t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 64; i++)
+            if (mbar_test_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > TIMEOUT_NS) {
+            *abort_flag = 1;
+            if (flags) atomicOr(flags, G2_FLAG_TIMEOUT);
+            return false;
+        }
+    }
+}
 
 G2_DEV void tma_load_2d(const CUtensorMap* tm, uint64_t* bar, void* dst, int x, int y) {
     asm volatile(
@@ -183,6 +211,54 @@ G2_DEV void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t 
 G2_DEV void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
+                 : "memory");
+}
+
+// ---- CTA pairs (cta_group::2): a cluster of two CTAs on two SMs shares each MMA.  The
+// leader (rank 0) issues M = 256 products whose A rows 0-127 and B rows (N) 0-N/2 come
+// from its own shared memory and the rest from the peer's, at the same offsets; each CTA's
+// tensor memory receives its own 128 accumulator rows.  Every tcgen05 instruction of such
+// a kernel carries cta_group::2.
+// The shared::cluster address of the same shared variable in CTA `rank` of the cluster.
+G2_DEV uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+// One arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
+G2_DEV void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Collective: one warp of each CTA of the pair; both receive the same address.
+G2_DEV void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+                 : "memory");
+}
+G2_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+G2_DEV void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+// Tile load into this CTA's shared memory whose completion (complete_tx) goes to the
+// mbarrier at a shared::cluster address of either CTA of the pair: both CTAs' halves of a
+// stage are counted on the leader's barrier.
+G2_DEV void tma_load_2d_pair(const CUtensorMap* tm, uint32_t cluster_bar, void* dst, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%3, "
+        "%4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)tm), "r"(cluster_bar), "r"(x), "r"(y)
+        : "memory");
+}
+// Completion of the pair's MMAs issued so far, as one arrive on the mbarrier at a
+// shared::cluster address (this CTA's or the peer's).
+G2_DEV void umma_commit_pair(uint32_t cluster_addr) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
 

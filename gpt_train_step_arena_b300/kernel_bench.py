@@ -42,7 +42,12 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller device footprint)")
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--tile-rows", type=int, default=0,
+                    help="force the tensor-core GEMM's tiles: 128, 256 or 2 (two-SM pairs); 0: per shape")
     args = ap.parse_args()
+    if args.tile_rows:
+        from . import _native as N_
+        N_.lib.gpt2_op_gemm_force_tile_rows(args.tile_rows)
     c = dict(synth.WORKLOADS[args.workload])
     if args.batch:
         c["B"] = args.batch
@@ -144,7 +149,8 @@ def main():
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.reps
     rate = work / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
-    print(json.dumps({"op": args.op, "workload": args.workload, "B": c["B"], "ms": ms, unit: rate}))
+    print(json.dumps({"op": args.op, "workload": args.workload, "B": c["B"], "ms": ms, unit: rate,
+                      "variant": ops.gemm_last_variant()}))
 
 
 if __name__ == "__main__":

@@ -188,7 +188,8 @@ def encoder_backward(dwte: torch.Tensor, dout: torch.Tensor, tokens: torch.Tenso
 
 
 class gemm_tile_rows:
-    """Context manager: force the tensor-core GEMM's tile height (128 or 256) inside."""
+    """Context manager: force the tensor-core GEMM's tiles inside: 128 or 256 rows on one
+    SM, or 2 for 256-row tiles computed by a cluster of two CTAs on two SMs."""
 
     def __init__(self, rows: int):
         self.rows = rows

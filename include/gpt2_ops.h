@@ -184,10 +184,12 @@ int gpt2_op_encoder_backward(int dtype, float* dwte, float* dwpe, const void* do
 
 /* Tile height of the tensor-core matrix product, a test and tuning hook: rows = 128 or
  * 256 makes every later bf16 tensor-core product of the process use tiles of that many
- * rows, any other value restores the choice per shape (the default); returns the
- * previous setting.  Products whose epilogue reads a staged input (residual, GELU')
- * always use 128-row tiles.  Not synchronised with work in flight: set it between
- * launches. */
+ * rows on one SM each; rows = 2 makes it use 256-row tiles computed by clusters of two
+ * CTAs on two SMs (128 rows and half of each B tile per SM; products with 128-column
+ * tiles or a single row tile keep the per-shape choice); any other value restores the
+ * choice per shape (the default); returns the previous setting.  Products whose epilogue
+ * reads a staged input (residual, GELU') never use 256-row tiles on one SM.  Not
+ * synchronised with work in flight: set it between launches. */
 int gpt2_op_gemm_force_tile_rows(int rows);
 /* The kernel variant of the last matrix product launched by this process, as
  * "rows=R cols=N splits=S a=k|mn b=k|mn epi=...", or "simt" when the last product took

@@ -2,10 +2,11 @@
 against the CPU oracle (or, for products, the exact fp64 contraction of the operands the
 kernel sees):
 
-* the tensor-core GEMM with 256-row tiles (two 128-row accumulator halves sharing each
-  B stage), which the per-shape choice takes for the LM head and the long-K input
-  gradients at B=32, T=1024: forced on small ragged shapes in every operand layout, and
-  reached naturally on an LM-head-sized forward product;
+* the tensor-core GEMM with 256-row tiles on one SM (two 128-row accumulator halves
+  sharing each B stage), which the per-shape choice takes for the LM-head gradients and
+  the long-K input gradients at B=32, T=1024: forced on small ragged shapes in every
+  operand layout; and the 256-row tiles on CTA pairs that it takes for the forward
+  products, reached naturally on an LM-head-sized forward product;
 * the encoder backward's long buckets (positions of one id split into segments summed in
   a second pass) and its multi-chunk ranking, at M = 32,768 Zipf(1.1) ids over the GPT-2
   vocabulary, where id 0 alone holds thousands of positions;
@@ -93,10 +94,10 @@ def test_matmul_256_row_tiles_bias(torch_cuda):
     assert _rel(_np(D), _np(A) @ _np(W).T + _np(b)) <= 8e-3
 
 
-def test_matmul_lm_head_size_takes_256_row_tiles(torch_cuda):
+def test_matmul_lm_head_size_takes_pair_tiles(torch_cuda):
     """LM-head forward shape (M = 6272 rows, Vp = 50304, C = 768): the per-shape choice
-    itself picks 256-row tiles; rows sampled across every row tile and the ragged last
-    one are checked against the fp64 product."""
+    itself picks 256-row tiles on CTA pairs; rows sampled across every row tile and the
+    ragged last one are checked against the fp64 product."""
     torch = torch_cuda
     from gpt_train_step_arena_b300 import ops
     M, N, K = 6272, 50304, 768
@@ -105,7 +106,7 @@ def test_matmul_lm_head_size_takes_256_row_tiles(torch_cuda):
     W = _to(torch, (rng.normal(size=(N, K)) * 0.02).astype(np.float32), torch.bfloat16)
     D = ops.matmul(A, W)
     variant = ops.gemm_last_variant()
-    assert variant.startswith("rows=256"), variant
+    assert variant.startswith("rows=pair256"), variant
     rows = np.unique(np.concatenate([np.arange(0, M, 97), [M - 1, M - 2, 255, 256, 511]]))
     got = _np(D[torch.from_numpy(rows).to("cuda")])
     want = _np(A[torch.from_numpy(rows).to("cuda")]) @ _np(W).T
