@@ -1487,8 +1487,8 @@ __global__ void __launch_bounds__(XE_THREADS) softmax_xent_bf16_k(bf16* logits, 
     const float2 l2 = make_float2(XE_LOG2E, XE_LOG2E), noff = make_float2(-off, -off);
     const int k_t = ok ? tg >> 3 : -1, e_t = tg & 7;
     uint4* xo = reinterpret_cast<uint4*>(x);
-    for (k = tid; k < nfull; k += XE_THREADS) {
-        const uint4 u = __ldcs(xv + k);
+    // one full chunk: (softmax - onehot) * dloss, packed back to bf16
+    auto grad_chunk = [&](const uint4& u, int kc) {
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
         float g[8];
 #pragma unroll
@@ -1497,7 +1497,7 @@ __global__ void __launch_bounds__(XE_THREADS) softmax_xent_bf16_k(bf16* logits, 
             g[2 * i] = ex2_ftz(a.x);
             g[2 * i + 1] = ex2_ftz(a.y);
         }
-        if (k == k_t) {
+        if (kc == k_t) {
 #pragma unroll
             for (int i = 0; i < 8; i++)
                 if (i == e_t) g[i] -= dloss;
@@ -1507,8 +1507,17 @@ __global__ void __launch_bounds__(XE_THREADS) softmax_xent_bf16_k(bf16* logits, 
         o.y = pack_bf16x2_rn(g[2], g[3]);
         o.z = pack_bf16x2_rn(g[4], g[5]);
         o.w = pack_bf16x2_rn(g[6], g[7]);
-        __stcs(xo + k, o);
+        __stcs(xo + kc, o);
+    };
+    // four chunks' loads in flight per thread, as in the first pass
+    for (k = tid; k + 3 * XE_THREADS < nfull; k += 4 * XE_THREADS) {
+        uint4 u[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) u[j] = __ldcs(xv + k + j * XE_THREADS);
+#pragma unroll
+        for (int j = 0; j < 4; j++) grad_chunk(u[j], k + j * XE_THREADS);
     }
+    for (; k < nfull; k += XE_THREADS) grad_chunk(__ldcs(xv + k), k);
     // the ragged chunk and the padding columns
     for (k = nfull + tid; k < nch; k += XE_THREADS) {
         const uint4 u = __ldcs(xv + k);

@@ -81,35 +81,6 @@ G2_DEV bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort_
 G2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* flags) {
     return mbar_wait_limit(bar, parity, abort_flag, flags, TIMEOUT_NS);
 }
-// Non-blocking test of phase `parity`.
-G2_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// As mbar_wait, but polling without ever suspending the thread: for barriers completed
-// by another SM of the cluster, whose arrivals need not wake a suspended waiter early.
-G2_DEV bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* flags) {
-    if (mbar_test_wait(bar, parity)) return true;
-    unsigned long long t0 = globaltimer();
-    while (true) {
-        for (int i = 0; i < 64; i++)
-            if (mbar_test_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > TIMEOUT_NS) {
-            *abort_flag = 1;
-            if (flags) atomicOr(flags, G2_FLAG_TIMEOUT);
-            return false;
-        }
-    }
-}
-
 G2_DEV void tma_load_2d(const CUtensorMap* tm, uint64_t* bar, void* dst, int x, int y) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
