@@ -6,25 +6,27 @@
 // t2 <= t of q.k / sqrt(hs), times v.  Only the row log-sum-exp is kept for the
 // backward, not the (T, T) probabilities.
 //
-// One CTA per (128-query tile, b, h), two CTAs resident per SM, 192 threads:
-//   warp 0     TMA: the Q tile once, then K_j and V_j (128 keys x 64 bf16 each) into
-//              two-stage rings, read straight from the (B, T, 3C) qkv buffer; a K stage
+// Persistent: two CTAs per SM, each looping over work items (a 128-query tile of one
+// (b, h), heaviest first), 192 threads:
+//   warp 0     TMA: each item's Q tile into one of two Q buffers (the next item's Q
+//              loads while the current item runs), then K_j and V_j (128 keys x 64 bf16)
+//              into two-stage rings, straight from the (B, T, 3C) qkv buffer; a K stage
 //              is refilled once its S product is done, a V stage once its PV product is;
-//              all of the CTA's K and V tiles are prefetched into L2 at the start.
+//              each item's K and V tiles are prefetched into L2 when it starts.
 //   warp 1     owns 256 columns of tensor memory (S: 128 x 128 fp32 at column 0,
-//              O: 128 x 64 fp32 at column 128); one lane issues S = Q K_j^T and
-//              O += P_{j-1} V_{j-1} (tcgen05.mma kind::f16, M = 128).
+//              O: 128 x 64 fp32 at column 128, P: 128 x 128 bf16 packed at column 192);
+//              one lane issues S = Q K_j^T and O += P_{j-1} V_{j-1} (tcgen05.mma
+//              kind::f16, M = 128; P read from tensor memory), tile after tile across
+//              items, so an item's last PV runs behind the next item's first S.
 //   warps 2-5  softmax, one query row per thread: the row max of S_j (tcgen05.ld),
-//              P_j = 2^(s * log2e / sqrt(hs) - m) rounded to bf16 into shared memory
-//              (the A operand of the PV product, K-major with the 128-byte swizzle),
-//              the running sum l, and a rescale of O in tensor memory when the row max
-//              grows by more than 2^8 (lazy rescaling: the result is unchanged, the
-//              stale max only lets terms reach 2^8).  At the end: O / l and the row
-//              log-sum-exp, natural-log units.
-// S_{j+1} is issued as soon as the softmax has released S_j, so the product P_j V_j
-// and the next S overlap the softmax; the second resident CTA fills the remaining
-// gaps.  Every mbarrier wait is bounded; on expiry the kernel raises the timeout flag,
-// drains what it issued and returns.
+//              P_j = 2^(s * log2e / sqrt(hs) - m) rounded to bf16 into tensor memory
+//              (tcgen05.st), the running sum l, and a rescale of O in tensor memory when
+//              the row max grows by more than 2^8 (lazy rescaling: the result is
+//              unchanged, the stale max only lets terms reach 2^8).  At the end of an
+//              item: O / l and the row log-sum-exp, natural-log units; then O is released
+//              for the next item's first PV.
+// Every mbarrier wait is bounded; on expiry the kernel raises the timeout flag, drains
+// what it issued and returns.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
@@ -36,16 +38,28 @@ using namespace tc;
 constexpr int HS = 64, BQ = 128, BKV = 128, NTH = 192;
 constexpr int NTH_BWD = 576;  // backward: TMA warp, MMA warp, two softmax groups of 8 warps
 constexpr int TILE = 128 * 64 * 2;  // 16 KB: 128 rows of one head, 128-byte rows
-constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 3 * TILE, OFF_P = 5 * TILE, OFF_BAR = 7 * TILE;
-constexpr uint32_t TMEM_COLS = 256, TM_S = 0, TM_O = 128;
+constexpr int OFF_Q = 0, OFF_K = 2 * TILE, OFF_V = 4 * TILE, OFF_BAR = 6 * TILE;  // Q, K, V: 2 buffers each
+constexpr uint32_t TMEM_COLS = 256, TM_S = 0, TM_O = 128, TM_P = 192;
 constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
 constexpr float RESCALE_LOG2 = 8.0f;
 
 struct FwdBars {
-    uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full, s_free, p_full, o_done, drain;
+    uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2], s_full, s_free, p_full, o_done,
+        o_free, drain;
     uint32_t tmem_slot;
     int abort;
 };
+// Work item w: query tile qt of (b, h) = bh, heaviest tiles first.
+struct FwdItem {
+    int qt, bh, nkv;
+};
+G2_DEV FwdItem fwd_item(int w, int nbh, int ntq) {
+    FwdItem it;
+    it.qt = ntq - 1 - w / nbh;
+    it.bh = w % nbh;
+    it.nkv = it.qt + 1;
+    return it;
+}
 constexpr int FWD_SMEM = OFF_BAR + (int)sizeof(FwdBars);
 
 // 2^x, the hardware approximation (relative error about 2^-22; results below 2^-126
@@ -62,7 +76,7 @@ G2_DEV uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __global__ void __launch_bounds__(NTH, 2)
-    attn_fwd_tc_k(const __grid_constant__ CUtensorMap tm_qkv, bf16* out, float* lse, int T, int C, int NH,
+    attn_fwd_tc_k(const __grid_constant__ CUtensorMap tm_qkv, bf16* out, float* lse, int T, int C, int NH, int nbh,
                   int* flags) {
     G2_PDL_ENTRY();
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -74,14 +88,13 @@ __global__ void __launch_bounds__(NTH, 2)
         if (threadIdx.x == 0 && flags) atomicOr(flags, G2_FLAG_TIMEOUT);
         return;
     }
-    const int nqt = gridDim.x, qt = nqt - 1 - (int)blockIdx.x;  // heaviest query tiles first
-    const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
-    const int q0 = qt * BQ, nkv = qt + 1, row0 = b * T;
+    const int ntq = (T + BQ - 1) / BQ, nitems = ntq * nbh;
 
     if (threadIdx.x == 0) {
         bar->abort = 0;
-        mbar_init(&bar->q_full, 1);
         for (int i = 0; i < 2; i++) {
+            mbar_init(&bar->q_full[i], 1);
+            mbar_init(&bar->q_empty[i], 1);
             mbar_init(&bar->k_full[i], 1);
             mbar_init(&bar->k_empty[i], 1);
             mbar_init(&bar->v_full[i], 1);
@@ -91,6 +104,7 @@ __global__ void __launch_bounds__(NTH, 2)
         mbar_init(&bar->s_free, 4);
         mbar_init(&bar->p_full, 4);
         mbar_init(&bar->o_done, 1);
+        mbar_init(&bar->o_free, 4);
         mbar_init(&bar->drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_async_smem();
@@ -104,107 +118,129 @@ __global__ void __launch_bounds__(NTH, 2)
     volatile int* abort_flag = &bar->abort;
 
     if (warp == 0) {
-        // ---------------- TMA producer
+        // ---------------- TMA producer: per item its Q (buffer k % 2, free once the item
+        // two back has issued its last S), then its K and V tiles through the rings; the
+        // ring position g counts tiles over all of this CTA's items
         if (lane == 0) {
-            mbar_expect_tx(&bar->q_full, TILE);
-            tma_load_2d(&tm_qkv, &bar->q_full, smem + OFF_Q, h * HS, row0 + q0);
-            // every K and V tile this CTA will read, into L2 ahead of the loads
-            for (int j = 2; j < nkv; j++) {
-                tma_prefetch_l2(&tm_qkv, C + h * HS, row0 + j * BKV);
-                tma_prefetch_l2(&tm_qkv, 2 * C + h * HS, row0 + j * BKV);
-            }
-            // K_j goes as soon as S_{j-2} has consumed its stage, V_j once P_{j-2} V_{j-2} has
-            int issued_k[2] = {-1, -1}, issued_v[2] = {-1, -1};
+            int issued_q[2] = {-1, -1}, issued_k[2] = {-1, -1}, issued_v[2] = {-1, -1};
             bool ok = true;
-            for (int j = 0; j < nkv; j++) {
-                const int s = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                if (!mbar_wait(&bar->k_empty[s], ph ^ 1, abort_flag, flags)) {
+            int g = 0;
+            for (int w = blockIdx.x, k = 0; ok && w < nitems; w += gridDim.x, k++) {
+                const FwdItem it = fwd_item(w, nbh, ntq);
+                const int row0 = (it.bh / NH) * T, h = it.bh % NH;
+                const int qb = k & 1;
+                const uint32_t qph = (k >> 1) & 1;
+                if (!mbar_wait(&bar->q_empty[qb], qph ^ 1, abort_flag, flags)) {
                     ok = false;
                     break;
                 }
-                mbar_expect_tx(&bar->k_full[s], TILE);
-                tma_load_2d(&tm_qkv, &bar->k_full[s], smem + OFF_K + s * TILE, C + h * HS, row0 + j * BKV);
-                issued_k[s] = (int)ph;
-                if (!mbar_wait(&bar->v_empty[s], ph ^ 1, abort_flag, flags)) {
-                    ok = false;
-                    break;
+                mbar_expect_tx(&bar->q_full[qb], TILE);
+                tma_load_2d(&tm_qkv, &bar->q_full[qb], smem + OFF_Q + qb * TILE, h * HS, row0 + it.qt * BQ);
+                issued_q[qb] = (int)qph;
+                // the item's K and V tiles past the first two, into L2 ahead of their loads
+                for (int j = 2; j < it.nkv; j++) {
+                    tma_prefetch_l2(&tm_qkv, C + h * HS, row0 + j * BKV);
+                    tma_prefetch_l2(&tm_qkv, 2 * C + h * HS, row0 + j * BKV);
                 }
-                mbar_expect_tx(&bar->v_full[s], TILE);
-                tma_load_2d(&tm_qkv, &bar->v_full[s], smem + OFF_V + s * TILE, 2 * C + h * HS, row0 + j * BKV);
-                issued_v[s] = (int)ph;
+                for (int j = 0; j < it.nkv; j++, g++) {
+                    const int s = g & 1;
+                    const uint32_t ph = (g >> 1) & 1;
+                    if (!mbar_wait(&bar->k_empty[s], ph ^ 1, abort_flag, flags)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&bar->k_full[s], TILE);
+                    tma_load_2d(&tm_qkv, &bar->k_full[s], smem + OFF_K + s * TILE, C + h * HS, row0 + j * BKV);
+                    issued_k[s] = (int)ph;
+                    if (!mbar_wait(&bar->v_empty[s], ph ^ 1, abort_flag, flags)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&bar->v_full[s], TILE);
+                    tma_load_2d(&tm_qkv, &bar->v_full[s], smem + OFF_V + s * TILE, 2 * C + h * HS, row0 + j * BKV);
+                    issued_v[s] = (int)ph;
+                }
             }
             if (!ok) {  // wait (bounded) for the copies still in flight before leaving
-                unsigned long long t0 = globaltimer();
-                while (!mbar_try_wait(&bar->q_full, 0) && globaltimer() - t0 < TIMEOUT_NS) {
-                }
+                auto drain = [&](uint64_t* b, int parity) {
+                    if (parity < 0) return;
+                    const unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(b, (uint32_t)parity) && globaltimer() - t0 < TIMEOUT_NS) {
+                    }
+                };
+#pragma unroll
                 for (int s = 0; s < 2; s++) {
-                    if (issued_k[s] >= 0) {
-                        t0 = globaltimer();
-                        while (!mbar_try_wait(&bar->k_full[s], (uint32_t)issued_k[s]) && globaltimer() - t0 < TIMEOUT_NS) {
-                        }
-                    }
-                    if (issued_v[s] >= 0) {
-                        t0 = globaltimer();
-                        while (!mbar_try_wait(&bar->v_full[s], (uint32_t)issued_v[s]) && globaltimer() - t0 < TIMEOUT_NS) {
-                        }
-                    }
+                    drain(&bar->q_full[s], issued_q[s]);
+                    drain(&bar->k_full[s], issued_k[s]);
+                    drain(&bar->v_full[s], issued_v[s]);
                 }
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer: the whole warp runs the loop converged, one elected
-        // lane issues (see umma_bf16_w)
+        // lane issues (see umma_bf16_w); tiles are numbered g over all of this CTA's items
         {
             auto wait_all = [&](uint64_t* b, uint32_t par) -> bool {
                 return __all_sync(0xffffffffu, mbar_wait(b, par, abort_flag, flags));
             };
             constexpr uint32_t ID_S = make_idesc(BKV, false, false);  // S: N = 128 keys
             constexpr uint32_t ID_PV = make_idesc(HS, false, true);   // O: N = 64, V is MN-major
-            const uint32_t sQ = smem_u32(smem + OFF_Q), sP = smem_u32(smem + OFF_P);
-            bool ok = wait_all(&bar->q_full, 0);
-            bool issued_any = false;
-            for (int j = 0; ok && j <= nkv; j++) {
-                if (j < nkv) {
-                    // S_j once K_j has landed and the softmax has read S_{j-1} out
-                    const int s = j & 1;
-                    if (!wait_all(&bar->k_full[s], (j >> 1) & 1) || (j > 0 && !wait_all(&bar->s_free, (j - 1) & 1))) {
+            bool ok = true, issued_any = false;
+            // O += P_g V_g once the softmax has written P_g into tensor memory: 8 products of 16
+            // keys (8 packed columns of P each); an item's first one overwrites O, after the
+            // softmax has read out the item before's (o_free)
+            auto issue_pv = [&](int g, bool first, int k) -> bool {
+                if (!wait_all(&bar->p_full, g & 1) || !wait_all(&bar->v_full[g & 1], (g >> 1) & 1)) return false;
+                if (first && k > 0 && !wait_all(&bar->o_free, (k - 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t sV = smem_u32(smem + OFF_V + (g & 1) * TILE);
+#pragma unroll
+                for (int kk = 0; kk < BKV / 16; kk++)
+                    umma_bf16_ts_w(tmem + TM_O, tmem + TM_P + kk * 8, sdesc(sV + kk * 16 * 128, 8192, 1024), ID_PV,
+                                   (!first || kk > 0) ? 1u : 0u);
+                umma_commit_w(&bar->o_done);
+                umma_commit_w(&bar->v_empty[g & 1]);
+                return true;
+            };
+            int g = 0;                                        // S products issued so far
+            int pend_g = -1, pend_k = 0;                      // the tile whose PV is still to issue
+            bool pend_first = false;
+            for (int w = blockIdx.x, k = 0; ok && w < nitems; w += gridDim.x, k++) {
+                const FwdItem it = fwd_item(w, nbh, ntq);
+                const int qb = k & 1;
+                if (!wait_all(&bar->q_full[qb], (k >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sQ = smem_u32(smem + OFF_Q + qb * TILE);
+                for (int j = 0; j < it.nkv; j++, g++) {
+                    // S_g once K_g has landed and the softmax has read S_{g-1} out
+                    const int s = g & 1;
+                    if (!wait_all(&bar->k_full[s], (g >> 1) & 1) || (g > 0 && !wait_all(&bar->s_free, (g - 1) & 1))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sK = smem_u32(smem + OFF_K + s * TILE);
 #pragma unroll
-                    for (int k = 0; k < HS / 16; k++)
-                        umma_bf16_w(tmem + TM_S, sdesc(sQ + k * 32, 16, 1024), sdesc(sK + k * 32, 16, 1024), ID_S,
-                                  k > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < HS / 16; kk++)
+                        umma_bf16_w(tmem + TM_S, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK + kk * 32, 16, 1024), ID_S,
+                                    kk > 0 ? 1u : 0u);
                     umma_commit_w(&bar->s_full);
                     umma_commit_w(&bar->k_empty[s]);
+                    if (j == it.nkv - 1) umma_commit_w(&bar->q_empty[qb]);  // the item's Q is done with
                     issued_any = true;
-                }
-                // P_{j-1} V_{j-1} once the softmax has written P_{j-1}
-                if (j > 0) {
-                    if (!wait_all(&bar->p_full, (j - 1) & 1) || !wait_all(&bar->v_full[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+                    // the previous tile's PV (perhaps the item before's last) behind this S
+                    if (pend_g >= 0 && !issue_pv(pend_g, pend_first, pend_k)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                }
-                if (j > 0) {
-                    const int pj = j - 1, ps = pj & 1;
-                    const uint32_t sV = smem_u32(smem + OFF_V + ps * TILE);
-#pragma unroll
-                    for (int k = 0; k < BKV / 16; k++) {
-                        // keys [16k, 16k+16): 64-key block k/4 of P, 32 bytes per step inside it
-                        const uint64_t ad = sdesc(sP + (k >> 2) * TILE + (k & 3) * 32, 16, 1024);
-                        const uint64_t bd = sdesc(sV + k * 16 * 128, 8192, 1024);
-                        umma_bf16_w(tmem + TM_O, ad, bd, ID_PV, (pj > 0 || k > 0) ? 1u : 0u);
-                    }
-                    umma_commit_w(&bar->o_done);
-                    umma_commit_w(&bar->v_empty[ps]);
-                    issued_any = true;
+                    pend_g = g;
+                    pend_first = j == 0;
+                    pend_k = k;
                 }
             }
+            if (ok && pend_g >= 0 && !issue_pv(pend_g, pend_first, pend_k)) ok = false;
             if (!ok && issued_any) {
                 umma_commit_w(&bar->drain);
                 if (lane == 0) {
@@ -218,122 +254,131 @@ __global__ void __launch_bounds__(NTH, 2)
     } else {
         // ---------------- softmax warps 2..5
         const int quarter = warp & 3, r = quarter * 32 + lane;  // TMEM lane = row of the tile
-        const int q = q0 + r;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const float sl2 = LOG2E / sqrtf((float)HS);
-        uint8_t* prow = smem + OFF_P + r * 128;
-        float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < nkv; j++) {
-            ok = mbar_wait(&bar->s_full, j & 1, abort_flag, flags);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const bool diag = j == qt;
-            // the whole row of S_j into registers, then S is released for S_{j+1}
-            uint32_t sv[BKV];
-#pragma unroll
-            for (int c = 0; c < BKV / 32; c++) tmem_ld32_raw(lane_base + TM_S + c * 32, sv + c * 32);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->s_free);
-            // causal mask on the diagonal tile: key j*128 + i is visible to row r iff i <= r
-            if (diag) {
-#pragma unroll
-                for (int i = 0; i < BKV; i++)
-                    if (i > r) sv[i] = __float_as_uint(-INFINITY);
-            }
-            // row maximum: a tree of three-input maxima (43 + 15 + 5 + 2 + 1 instructions)
-            float t43[43];
-#pragma unroll
-            for (int i = 0; i < 42; i++)
-                t43[i] = max3f(__uint_as_float(sv[3 * i]), __uint_as_float(sv[3 * i + 1]), __uint_as_float(sv[3 * i + 2]));
-            t43[42] = fmaxf(__uint_as_float(sv[126]), __uint_as_float(sv[127]));
-            float t15[15];
-#pragma unroll
-            for (int i = 0; i < 14; i++) t15[i] = max3f(t43[3 * i], t43[3 * i + 1], t43[3 * i + 2]);
-            t15[14] = t43[42];
-            const float t5[5] = {max3f(t15[0], t15[1], t15[2]), max3f(t15[3], t15[4], t15[5]),
-                                 max3f(t15[6], t15[7], t15[8]), max3f(t15[9], t15[10], t15[11]),
-                                 max3f(t15[12], t15[13], t15[14])};
-            const float mx = max3f(max3f(t5[0], t5[1], t5[2]), t5[3], t5[4]) * sl2;
-            bool resc = false;
-            float corr = 1.f;
-            if (j == 0) {
-                m_used = mx;
-            } else if (mx > m_used + RESCALE_LOG2) {
-                corr = ex2(m_used - mx);
-                m_used = mx;
-                l *= corr;
-                resc = true;
-            }
-            // P = 2^(s * sl2 - m) packed to bf16 in registers (S dies as P grows); the scale
-            // and the row sum run two columns per instruction
-            const float2 sl2x2 = make_float2(sl2, sl2), mneg = make_float2(-m_used, -m_used);
-            float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            uint32_t pk[BKV / 2];
-#pragma unroll
-            for (int i = 0; i < BKV; i += 2) {
-                const float2 a = fma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sl2x2, mneg);
-                const float2 p = make_float2(ex2(a.x), ex2(a.y));
-                l4[(i >> 1) & 3] = add2(l4[(i >> 1) & 3], p);
-                pk[i >> 1] = pack_bf16x2(p.x, p.y);
-            }
-            const float2 l2 = add2(add2(l4[0], l4[1]), add2(l4[2], l4[3]));
-            l += l2.x + l2.y;
-            if (j > 0) {
-                // O and the P buffer are free once P_{j-1} V_{j-1} has completed
-                ok = mbar_wait(&bar->o_done, (j - 1) & 1, abort_flag, flags);
+        int g = 0;  // tiles over all of this CTA's items (the barriers' phase count)
+        for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+            const int qt = fwd_item(w, nbh, ntq).qt;
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j <= qt; j++, g++) {
+                ok = mbar_wait(&bar->s_full, g & 1, abort_flag, flags);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, resc)) {
+                const bool diag = j == qt;
+                // the whole row of S_g into registers, then S is released for S_{g+1}
+                uint32_t sv[BKV];
 #pragma unroll
-                    for (int c = 0; c < 2; c++) {
-                        float o[32];
-                        tmem_ld32(lane_base + TM_O + c * 32, o);
+                for (int c = 0; c < BKV / 32; c++) tmem_ld32_raw(lane_base + TM_S + c * 32, sv + c * 32);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->s_free);
+                // causal mask on the diagonal tile: key j*128 + i is visible to row r iff i <= r
+                if (diag) {
 #pragma unroll
-                        for (int i = 0; i < 32; i++) o[i] *= corr;
-                        tmem_st32(lane_base + TM_O + c * 32, o);
-                    }
-                    tmem_wait_st();
+                    for (int i = 0; i < BKV; i++)
+                        if (i > r) sv[i] = __float_as_uint(-INFINITY);
                 }
-            }
-            // 16-byte chunk ch (keys 8ch..8ch+7): 64-key block ch/8, chunk ch%8 of this row,
-            // XOR-swizzled by the row (the layout TMA's 128-byte swizzle produces)
+                // row maximum: a tree of three-input maxima (43 + 15 + 5 + 2 + 1 instructions)
+                float t43[43];
 #pragma unroll
-            for (int ch = 0; ch < BKV / 8; ch++)
-                *reinterpret_cast<uint4*>(prow + (ch >> 3) * TILE + (((ch & 7) ^ (r & 7)) << 4)) =
-                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            fence_async_smem();
+                for (int i = 0; i < 42; i++)
+                    t43[i] = max3f(__uint_as_float(sv[3 * i]), __uint_as_float(sv[3 * i + 1]),
+                                   __uint_as_float(sv[3 * i + 2]));
+                t43[42] = fmaxf(__uint_as_float(sv[126]), __uint_as_float(sv[127]));
+                float t15[15];
+#pragma unroll
+                for (int i = 0; i < 14; i++) t15[i] = max3f(t43[3 * i], t43[3 * i + 1], t43[3 * i + 2]);
+                t15[14] = t43[42];
+                const float t5[5] = {max3f(t15[0], t15[1], t15[2]), max3f(t15[3], t15[4], t15[5]),
+                                     max3f(t15[6], t15[7], t15[8]), max3f(t15[9], t15[10], t15[11]),
+                                     max3f(t15[12], t15[13], t15[14])};
+                const float mx = max3f(max3f(t5[0], t5[1], t5[2]), t5[3], t5[4]) * sl2;
+                bool resc = false;
+                float corr = 1.f;
+                if (j == 0) {
+                    m_used = mx;
+                } else if (mx > m_used + RESCALE_LOG2) {
+                    corr = ex2(m_used - mx);
+                    m_used = mx;
+                    l *= corr;
+                    resc = true;
+                }
+                // P = 2^(s * sl2 - m) packed to bf16 in registers (S dies as P grows); the
+                // scale and the row sum run two columns per instruction
+                const float2 sl2x2 = make_float2(sl2, sl2), mneg = make_float2(-m_used, -m_used);
+                float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                make_float2(0.f, 0.f)};
+                uint32_t pk[BKV / 2];
+#pragma unroll
+                for (int i = 0; i < BKV; i += 2) {
+                    const float2 a = fma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sl2x2, mneg);
+                    const float2 p = make_float2(ex2(a.x), ex2(a.y));
+                    l4[(i >> 1) & 3] = add2(l4[(i >> 1) & 3], p);
+                    pk[i >> 1] = pack_bf16x2(p.x, p.y);
+                }
+                const float2 l2 = add2(add2(l4[0], l4[1]), add2(l4[2], l4[3]));
+                l += l2.x + l2.y;
+                if (j > 0) {
+                    // O and the P columns are free once P_{g-1} V_{g-1} has completed (an
+                    // item's first tile: the item before's end already waited for it)
+                    ok = mbar_wait(&bar->o_done, (g - 1) & 1, abort_flag, flags);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+                        for (int c = 0; c < 2; c++) {
+                            float o[32];
+                            tmem_ld32(lane_base + TM_O + c * 32, o);
+#pragma unroll
+                            for (int i = 0; i < 32; i++) o[i] *= corr;
+                            tmem_st32(lane_base + TM_O + c * 32, o);
+                        }
+                    }
+                }
+                // P_g into tensor memory: key pair i of this row in column TM_P + i (the A
+                // operand of the PV product, 8 columns per 16 keys)
+                tmem_st32u(lane_base + TM_P, pk);
+                tmem_st32u(lane_base + TM_P + 32, pk + 32);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->p_full);
+            }
+            if (!ok) break;
+            // the item's O once its last PV is done; then O is free for the next item
+            ok = mbar_wait(&bar->o_done, (g - 1) & 1, abort_flag, flags);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float o[64];
+            tmem_ld32(lane_base + TM_O, o);
+            tmem_ld32(lane_base + TM_O + 32, o + 32);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->p_full);
-        }
-        if (ok) {
-            ok = mbar_wait(&bar->o_done, (nkv - 1) & 1, abort_flag, flags);
-            if (__all_sync(0xffffffffu, ok)) {
-                tc_fence_after();
-                float o[64];
-                tmem_ld32(lane_base + TM_O, o);
-                tmem_ld32(lane_base + TM_O + 32, o + 32);
-                if (q < T) {
-                    const float inv = 1.0f / l;
-                    bf16* dst = out + (size_t)(row0 + q) * C + h * HS;
+            if (lane == 0) mbar_arrive(&bar->o_free);
+            const int bh = w % nbh, q = qt * BQ + r;
+            if (q < T) {
+                const int row0 = (bh / NH) * T, h = bh % NH;
+                const float inv = 1.0f / l;
+                bf16* dst = out + (size_t)(row0 + q) * C + h * HS;
 #pragma unroll
-                    for (int i = 0; i < HS; i += 8) {
-                        float y[8];
+                for (int i = 0; i < HS; i += 8) {
+                    float y[8];
 #pragma unroll
-                        for (int e = 0; e < 8; e++) y[e] = o[i + e] * inv;
-                        Vec8<bf16>::store(dst + i, y);
-                    }
-                    lse[(size_t)bh * T + q] = (m_used + log2f(l)) * LN2;
+                    for (int e = 0; e < 8; e++) y[e] = o[i + e] * inv;
+                    Vec8<bf16>::store(dst + i, y);
                 }
+                lse[(size_t)bh * T + q] = (m_used + log2f(l)) * LN2;
             }
         }
     }
@@ -828,9 +873,16 @@ cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, 
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    dim3 grid((T + atc::BQ - 1) / atc::BQ, B * NH);
-    if (grid.y > 65535) return cudaErrorInvalidValue;
-    ::g2::launch_k(atc::attn_fwd_tc_k, grid, atc::NTH, atc::FWD_SMEM, s, tm, (bf16*)out, lse, T, C, NH, flags);
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 148;
+    }
+    const int nbh = B * NH, items = ((T + atc::BQ - 1) / atc::BQ) * nbh;
+    const int grid = items < 2 * sms ? items : 2 * sms;  // persistent: two CTAs per SM
+    ::g2::launch_k(atc::attn_fwd_tc_k, grid, atc::NTH, atc::FWD_SMEM, s, tm, (bf16*)out, lse, T, C, NH, nbh, flags);
     return cudaGetLastError();
 }
 
