@@ -53,6 +53,12 @@ struct FwdBars {
 struct FwdItem {
     int qt, bh, nkv;
 };
+// The k-th work item of CTA c among G persistent CTAs: items are listed heaviest first and
+// handed out in rounds of G whose direction alternates (a snake), so that every CTA's
+// total stays within one item of the mean.  Which CTA runs an item changes nothing in
+// its arithmetic.
+G2_DEV int item_of(int k, int c, int G) { return k * G + ((k & 1) ? G - 1 - c : c); }
+
 G2_DEV FwdItem fwd_item(int w, int nbh, int ntq) {
     FwdItem it;
     it.qt = ntq - 1 - w / nbh;
@@ -125,7 +131,8 @@ __global__ void __launch_bounds__(NTH, 2)
             int issued_q[2] = {-1, -1}, issued_k[2] = {-1, -1}, issued_v[2] = {-1, -1};
             bool ok = true;
             int g = 0;
-            for (int w = blockIdx.x, k = 0; ok && w < nitems; w += gridDim.x, k++) {
+            for (int k = 0, w = item_of(0, blockIdx.x, gridDim.x); ok && w < nitems;
+                 k++, w = item_of(k, blockIdx.x, gridDim.x)) {
                 const FwdItem it = fwd_item(w, nbh, ntq);
                 const int row0 = (it.bh / NH) * T, h = it.bh % NH;
                 const int qb = k & 1;
@@ -205,7 +212,8 @@ __global__ void __launch_bounds__(NTH, 2)
             int g = 0;                                        // S products issued so far
             int pend_g = -1, pend_k = 0;                      // the tile whose PV is still to issue
             bool pend_first = false;
-            for (int w = blockIdx.x, k = 0; ok && w < nitems; w += gridDim.x, k++) {
+            for (int k = 0, w = item_of(0, blockIdx.x, gridDim.x); ok && w < nitems;
+                 k++, w = item_of(k, blockIdx.x, gridDim.x)) {
                 const FwdItem it = fwd_item(w, nbh, ntq);
                 const int qb = k & 1;
                 if (!wait_all(&bar->q_full[qb], (k >> 1) & 1)) {
@@ -258,7 +266,8 @@ __global__ void __launch_bounds__(NTH, 2)
         const float sl2 = LOG2E / sqrtf((float)HS);
         bool ok = true;
         int g = 0;  // tiles over all of this CTA's items (the barriers' phase count)
-        for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+        for (int k = 0, w = item_of(0, blockIdx.x, gridDim.x); ok && w < nitems;
+             k++, w = item_of(k, blockIdx.x, gridDim.x)) {
             const int qt = fwd_item(w, nbh, ntq).qt;
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j <= qt; j++, g++) {
@@ -504,7 +513,8 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
         for (int i = 0; i < BW_NS; i++) iss_st[i] = -1;
         int iss_rt = -1;
         bool ok = true;
-        for (int w = blockIdx.x, k = 0; ok && w < nitems; w += gridDim.x, k++) {
+        for (int k = 0, w = item_of(0, blockIdx.x, gridDim.x); ok && w < nitems;
+             k++, w = item_of(k, blockIdx.x, gridDim.x)) {
             const BwdItem it = bwd_item(DQ, w, nbh, ntiles, T, NH);
             const int xa = DQ ? C + it.h * HS : it.h * HS;      // streamed K or Q
             const int xb = DQ ? 2 * C + it.h * HS : it.h * HS;  // streamed V (qkv) or dO (dout map)
@@ -602,7 +612,8 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
                 return __all_sync(0xffffffffu, mbar_wait(b, par, abort_flag, flags));
             };
             int nt = 0;  // streamed tiles before this item
-            for (int w = blockIdx.x, k = 0; ok && w < nitems; w += gridDim.x, k++) {
+            for (int k = 0, w = item_of(0, blockIdx.x, gridDim.x); ok && w < nitems;
+                 k++, w = item_of(k, blockIdx.x, gridDim.x)) {
                 const BwdItem it = bwd_item(DQ, w, nbh, ntiles, T, NH);
                 const int nh = 2 * it.nst;
                 const uint32_t rows = tmem + TB_ROWS + (uint32_t)(k & 1) * 64;
@@ -736,7 +747,8 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
         };
         if (grp == 0 && blockIdx.x < nitems) ok = prep_rows(blockIdx.x, 0);
         int nt = 0;
-        for (int w = blockIdx.x, k = 0; w < nitems; w += gridDim.x, k++) {
+        for (int k = 0, w = item_of(0, blockIdx.x, gridDim.x); w < nitems;
+             k++, w = item_of(k, blockIdx.x, gridDim.x)) {
             if (!__all_sync(0xffffffffu, ok)) break;
             const BwdItem it = bwd_item(DQ, w, nbh, ntiles, T, NH);
             const int nh = 2 * it.nst, G = 2 * nt;
@@ -816,8 +828,9 @@ __global__ void __launch_bounds__(NTH_BWD, 1)
             // the next item's rows go into the other row buffer now (its S and dP can start
             // while this item's accumulators drain); that buffer's last reader was the item
             // before this one, all of whose products completed before its drain
-            if (grp == 0 && w + (int)gridDim.x < nitems) {
-                ok = prep_rows(w + gridDim.x, k + 1);
+            const int w_next = item_of(k + 1, blockIdx.x, gridDim.x);
+            if (grp == 0 && w_next < nitems) {
+                ok = prep_rows(w_next, k + 1);
                 if (!__all_sync(0xffffffffu, ok)) break;
             }
             ok = mbar_wait(&bar->acc_done, k & 1, abort_flag, flags);
