@@ -1097,20 +1097,223 @@ static cudaError_t colreduce(float* out0, float* out1, float* out2, const float*
     return cudaGetLastError();
 }
 
+// bf16 backward, rows streamed through shared memory as in ln_bwd_tma_k (warp 0 copies
+// tiles of 16 rows of dout, x and dres into a 3-stage ring), computed in two phases per
+// tile by 12 warps.  Phase A, a warp per row: the row sums of g = w dout and g n, n = (x -
+// mean) rstd, kept with the row's mean and rstd in a small table (two, by tile parity).
+// Phase B, once every warp has filled the table (an mbarrier, bounded wait): thread t owns the 8 columns of chunk t % (C/8) and the
+// rows t / (C/8), + RG, ... of the tile; it writes dres += (g - mean(g) - n mean(g n))
+// rstd and keeps its columns' sums of n dout (dw), dout (db) and, with OUTSUM, of the
+// stored new dres in 24 registers (the one-phase kernel held 72 and fit only 8 warps).  At
+// the end the row groups' sums are added in order into one partial row per CTA
+// (part[k][blockIdx][C]), which colreduce_k adds in block order.
+constexpr int LNBC_WARPS = 12, LNBC_THREADS = 32 * (LNBC_WARPS + 1), LNBC_CT = 32 * LNBC_WARPS;
+
+template <int NV, bool OUTSUM, bool RMS>
+__global__ void __launch_bounds__(LNBC_THREADS, 1)
+    ln_bwd_cols_k(bf16* dres, float* part, const bf16* dout, const bf16* inp, const float* w, const float* mean,
+                  const float* rstd, int M, int C) {
+    G2_PDL_ENTRY();
+    constexpr int CH = 32 * NV, RG = LNBC_CT / CH;  // chunks of 8 columns; row groups
+    constexpr int NS = OUTSUM ? 3 : 2;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int sub_bytes = LNB_ROWS * C * 2;  // one tensor's rows of a tile
+    const int stage_bytes = 3 * sub_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + LNB_STAGES * stage_bytes);
+    uint64_t* empty = full + LNB_STAGES;
+    uint64_t* stats_bar = empty + LNB_STAGES;  // [2]: the row table of tile parity p is complete
+    int* abort_p = reinterpret_cast<int*>(stats_bar + 2);
+    float4* rowstat = reinterpret_cast<float4*>(smem + LNB_STAGES * stage_bytes + 128);  // [2][LNB_ROWS]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < LNB_STAGES; i++) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], LNBC_WARPS);
+        }
+        tc::mbar_init(&stats_bar[0], LNBC_WARPS);
+        tc::mbar_init(&stats_bar[1], LNBC_WARPS);
+        *abort_p = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    volatile int* abort_flag = abort_p;
+    const int ntiles = (M + LNB_ROWS - 1) / LNB_ROWS;
+    const int t = threadIdx.x - 32, ch = t % CH, rg = t / CH;  // phase B role (compute threads)
+    float2 aw[4], ab[4], ar[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) aw[i] = ab[i] = ar[i] = make_float2(0.f, 0.f);
+    if (warp == 0) {
+        if (lane == 0) {
+            int it = 0;
+            for (int tt = blockIdx.x; tt < ntiles; tt += gridDim.x, it++) {
+                const int s = it % LNB_STAGES;
+                if (!tc::mbar_wait(&empty[s], ((it / LNB_STAGES) & 1) ^ 1, abort_flag, nullptr)) break;
+                const int rows = min(LNB_ROWS, M - tt * LNB_ROWS);
+                const uint32_t bytes = (uint32_t)rows * C * 2;
+                const size_t off = (size_t)tt * LNB_ROWS * C;
+                uint8_t* st = smem + s * stage_bytes;
+                tc::mbar_expect_tx(&full[s], 3 * bytes);
+                tc::bulk_load_1d(st, dout + off, bytes, &full[s]);
+                tc::bulk_load_1d(st + sub_bytes, inp + off, bytes, &full[s]);
+                tc::bulk_load_1d(st + 2 * sub_bytes, dres + off, bytes, &full[s]);
+            }
+        }
+    } else {
+        const int wi = warp - 1;  // compute warp 0..11
+        // w for phase A (lane's 8 columns of each 256-column slab) and phase B (chunk ch)
+        float2 wa[NV][4], wb[4];
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            float t8[8];
+            Vec8<float>::load(w + j * 256 + lane * 8, t8);
+#pragma unroll
+            for (int i = 0; i < 4; i++) wa[j][i] = make_float2(t8[2 * i], t8[2 * i + 1]);
+        }
+        {
+            float t8[8];
+            Vec8<float>::load(w + ch * 8, t8);
+#pragma unroll
+            for (int i = 0; i < 4; i++) wb[i] = make_float2(t8[2 * i], t8[2 * i + 1]);
+        }
+        // the row statistics of this warp's phase-A rows (wi and wi + 12), one tile ahead
+        constexpr int RPW = (LNB_ROWS + LNBC_WARPS - 1) / LNBC_WARPS;
+        float nm[RPW], nr[RPW];
+        auto load_stats = [&](int tt) {
+#pragma unroll
+            for (int i = 0; i < RPW; i++) {
+                const int r = wi + LNBC_WARPS * i, row = tt * LNB_ROWS + r;
+                const bool v = tt < ntiles && r < LNB_ROWS && row < M;
+                nm[i] = (RMS || !v) ? 0.f : mean[row];
+                nr[i] = v ? rstd[row] : 0.f;
+            }
+        };
+        load_stats(blockIdx.x);
+        int it = 0;
+        for (int tt = blockIdx.x; tt < ntiles; tt += gridDim.x, it++) {
+            float cm[RPW], cr[RPW];
+#pragma unroll
+            for (int i = 0; i < RPW; i++) {
+                cm[i] = nm[i];
+                cr[i] = nr[i];
+            }
+            load_stats(tt + gridDim.x);
+            const int s = it % LNB_STAGES;
+            const bool ok = tc::mbar_wait(&full[s], (it / LNB_STAGES) & 1, abort_flag, nullptr);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const int rows = min(LNB_ROWS, M - tt * LNB_ROWS);
+            const uint8_t* st = smem + s * stage_bytes;
+            float4* rsb = rowstat + (it & 1) * LNB_ROWS;
+            // ---- phase A: a warp per row
+#pragma unroll
+            for (int i = 0; i < RPW; i++) {
+                const int r = wi + LNBC_WARPS * i;
+                if (r >= rows) break;
+                const uint4* d = reinterpret_cast<const uint4*>(st + (size_t)r * C * 2);
+                const uint4* x = reinterpret_cast<const uint4*>(st + sub_bytes + (size_t)r * C * 2);
+                const float rs = cr[i];
+                const float2 rs2 = make_float2(rs, rs), nmr = make_float2(-cm[i] * rs, -cm[i] * rs);
+                float2 sg = make_float2(0.f, 0.f), sgn = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < NV; j++) {
+                    const uint4 ud = d[j * 32 + lane], ux = x[j * 32 + lane];
+                    const uint32_t wd[4] = {ud.x, ud.y, ud.z, ud.w}, wx[4] = {ux.x, ux.y, ux.z, ux.w};
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const float2 n = fma2(make_float2(bf16_lo(wx[q]), bf16_hi(wx[q])), rs2, nmr);
+                        const float2 g = mul2(wa[j][q], make_float2(bf16_lo(wd[q]), bf16_hi(wd[q])));
+                        sg = add2(sg, g);
+                        sgn = fma2(g, n, sgn);
+                    }
+                }
+                const float gm = RMS ? 0.f : warp_sum(sg.x + sg.y) / C;
+                const float gnm = warp_sum(sgn.x + sgn.y) / C;
+                if (lane == 0) rsb[r] = make_float4(gm, gnm, cm[i], rs);
+            }
+            // every row's statistics are in the table (each use of a table is one phase of
+            // its barrier: parity (it / 2) % 2)
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&stats_bar[it & 1]);
+            const bool oks = tc::mbar_wait(&stats_bar[it & 1], (it >> 1) & 1, abort_flag, nullptr);
+            if (!__all_sync(0xffffffffu, oks)) break;
+            // ---- phase B: thread t, chunk ch, rows rg, rg + RG, ...
+            for (int r = rg; r < rows; r += RG) {
+                const float4 sr = rsb[r];
+                const float rs = sr.w;
+                const float2 rs2 = make_float2(rs, rs), nmr = make_float2(-sr.z * rs, -sr.z * rs);
+                const float2 ngm = make_float2(-sr.x, -sr.x), ngnm = make_float2(-sr.y, -sr.y);
+                const uint4 ud = *reinterpret_cast<const uint4*>(st + (size_t)r * C * 2 + ch * 16);
+                const uint4 ux = *reinterpret_cast<const uint4*>(st + sub_bytes + (size_t)r * C * 2 + ch * 16);
+                const uint4 uo = *reinterpret_cast<const uint4*>(st + 2 * sub_bytes + (size_t)r * C * 2 + ch * 16);
+                const uint32_t wd[4] = {ud.x, ud.y, ud.z, ud.w}, wx[4] = {ux.x, ux.y, ux.z, ux.w},
+                               wo[4] = {uo.x, uo.y, uo.z, uo.w};
+                uint32_t po[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const float2 dd = make_float2(bf16_lo(wd[q]), bf16_hi(wd[q]));
+                    const float2 n = fma2(make_float2(bf16_lo(wx[q]), bf16_hi(wx[q])), rs2, nmr);
+                    const float2 g = mul2(wb[q], dd);
+                    if (!RMS) ab[q] = add2(ab[q], dd);
+                    aw[q] = fma2(n, dd, aw[q]);
+                    // dres += (g - gm - n gnm) rstd
+                    const float2 v = fma2(n, ngnm, add2(g, ngm));
+                    const float2 o = fma2(v, rs2, make_float2(bf16_lo(wo[q]), bf16_hi(wo[q])));
+                    po[q] = pack_bf16x2_rn(o.x, o.y);
+                    if (OUTSUM) ar[q] = add2(ar[q], make_float2(bf16_lo(po[q]), bf16_hi(po[q])));
+                }
+                *reinterpret_cast<uint4*>(dres + ((size_t)tt * LNB_ROWS + r) * C + ch * 8) =
+                    make_uint4(po[0], po[1], po[2], po[3]);
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&empty[s]);
+        }
+    }
+    // every stage is consumed (or the loop gave up): reuse the ring for the block's sums
+    __syncthreads();
+    float* sh = reinterpret_cast<float*>(smem);  // [RG][NS][C]
+    if (warp >= 1) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int c = ch * 8 + 2 * q;
+            float* s0 = sh + (rg * NS + 0) * C + c;
+            float* s1 = sh + (rg * NS + 1) * C + c;
+            s0[0] = aw[q].x;
+            s0[1] = aw[q].y;
+            s1[0] = ab[q].x;
+            s1[1] = ab[q].y;
+            if (OUTSUM) {
+                float* s2 = sh + (rg * NS + 2) * C + c;
+                s2[0] = ar[q].x;
+                s2[1] = ar[q].y;
+            }
+        }
+    }
+    __syncthreads();
+    for (int k = 0; k < NS; k++) {
+        float* pk = part + (size_t)(k * gridDim.x + blockIdx.x) * C;
+        for (int c = threadIdx.x; c < C; c += blockDim.x) {
+            float a = 0.f;
+#pragma unroll
+            for (int g = 0; g < RG; g++) a += sh[(g * NS + k) * C + c];
+            pk[c] = a;
+        }
+    }
+}
+
 template <int NV, bool OUTSUM, bool RMS>
 static cudaError_t ln_bwd_tma_launch_t(bf16* dres, float* part, const bf16* dout, const bf16* inp, const float* w,
                                        const float* mean, const float* rstd, int M, int C, int grid, cudaStream_t s) {
-    const int smem = LNB_STAGES * 3 * LNB_ROWS * C * 2 + 256;
+    // the ring, its barriers (128 bytes) and two tables of 16 row statistics (512 bytes)
+    const int smem = LNB_STAGES * 3 * LNB_ROWS * C * 2 + 128 + 512;
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(ln_bwd_tma_k<NV, OUTSUM, RMS>,
+        cudaError_t e = cudaFuncSetAttribute(ln_bwd_cols_k<NV, OUTSUM, RMS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             LNB_STAGES * 3 * LNB_ROWS * (NV * 256) * 2 + 256);
+                                             LNB_STAGES * 3 * LNB_ROWS * (NV * 256) * 2 + 128 + 512);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    ::g2::launch_k(ln_bwd_tma_k<NV, OUTSUM, RMS>, grid, LNT_THREADS, smem, s, dres, part, dout, inp, w, mean, rstd, M,
-                                                                             C);
+    ::g2::launch_k(ln_bwd_cols_k<NV, OUTSUM, RMS>, grid, LNBC_THREADS, smem, s, dres, part, dout, inp, w, mean, rstd,
+                   M, C);
     return cudaGetLastError();
 }
 
