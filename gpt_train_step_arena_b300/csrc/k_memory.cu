@@ -514,7 +514,7 @@ __global__ void ln_fwd_vec_k(T* out, float* mean, float* rstd, const T* inp, con
 // bound by the latency of each row's two reductions, not by bytes: 15 compute warps (a
 // 512-thread block keeps 128 registers per thread) and sums formed as trees of two-wide
 // adds keep the chains short.
-constexpr int LNT_STAGES = 3, LNT_THREADS = 288;
+constexpr int LNT_STAGES = 3;
 constexpr int LNF_WARPS = 15, LNF_ROWS = 2 * LNF_WARPS, LNF_THREADS = 32 * (LNF_WARPS + 1);
 
 template <int NV, bool RMS>
@@ -815,197 +815,8 @@ __global__ void __launch_bounds__(128) ln_bwd_vec_k(T* dres, float* part, const 
     }
 }
 
-// bf16 backward with the rows streamed through shared memory: one CTA per SM; warp 0
-// copies tiles of 16 consecutive rows of dout, x and dres (three contiguous bulk copies)
-// into a 3-stage ring; warps 1-8 take 2 rows of each tile, update dres in global memory
-// and keep per-column sums of n*dout (dw), dout (db) and, with OUTSUM, of the stored new
-// dres in registers.  At the end each CTA writes one partial row per sum
-// (part[k][blockIdx][C]), which colreduce_k adds in block order: the summation order
-// depends on (M, C, grid) only.
+// bf16 backward tiles: 16 consecutive rows of dout, x and dres per stage, 3 stages.
 constexpr int LNB_ROWS = 16, LNB_STAGES = 3;
-
-template <int NV, bool OUTSUM, bool RMS>
-__global__ void __launch_bounds__(LNT_THREADS, 1)
-    ln_bwd_tma_k(bf16* dres, float* part, const bf16* dout, const bf16* inp, const float* w, const float* mean,
-                 const float* rstd, int M, int C) {
-    G2_PDL_ENTRY();
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int sub_bytes = LNB_ROWS * C * 2;  // one tensor's rows of a tile
-    const int stage_bytes = 3 * sub_bytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + LNB_STAGES * stage_bytes);
-    uint64_t* empty = full + LNB_STAGES;
-    int* abort_p = reinterpret_cast<int*>(empty + LNB_STAGES);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < LNB_STAGES; i++) {
-            tc::mbar_init(&full[i], 1);
-            tc::mbar_init(&empty[i], 8);
-        }
-        *abort_p = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    volatile int* abort_flag = abort_p;
-    const int ntiles = (M + LNB_ROWS - 1) / LNB_ROWS;
-    constexpr int NS = OUTSUM ? 3 : 2;
-    // per-column sums of this lane's 8 columns of each slab j, as 4 pairs: n*dout (dw),
-    // dout (db) and, with OUTSUM, the stored new dres
-    float2 aw[NV][4], ab[NV][4], ar[OUTSUM ? NV : 1][4];
-#pragma unroll
-    for (int j = 0; j < NV; j++)
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            aw[j][i] = ab[j][i] = make_float2(0.f, 0.f);
-            if (OUTSUM) ar[OUTSUM ? j : 0][i] = make_float2(0.f, 0.f);
-        }
-    if (warp == 0) {
-        if (lane == 0) {
-            int it = 0;
-            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, it++) {
-                const int s = it % LNB_STAGES;
-                if (!tc::mbar_wait(&empty[s], ((it / LNB_STAGES) & 1) ^ 1, abort_flag, nullptr)) break;
-                const int rows = min(LNB_ROWS, M - t * LNB_ROWS);
-                const uint32_t bytes = (uint32_t)rows * C * 2;
-                const size_t off = (size_t)t * LNB_ROWS * C;
-                uint8_t* st = smem + s * stage_bytes;
-                tc::mbar_expect_tx(&full[s], 3 * bytes);
-                tc::bulk_load_1d(st, dout + off, bytes, &full[s]);
-                tc::bulk_load_1d(st + sub_bytes, inp + off, bytes, &full[s]);
-                tc::bulk_load_1d(st + 2 * sub_bytes, dres + off, bytes, &full[s]);
-            }
-        }
-    } else {
-        float2 wv[NV][4];
-#pragma unroll
-        for (int j = 0; j < NV; j++) {
-            float t8[8];
-            Vec8<float>::load(w + j * 256 + lane * 8, t8);
-#pragma unroll
-            for (int i = 0; i < 4; i++) wv[j][i] = make_float2(t8[2 * i], t8[2 * i + 1]);
-        }
-        auto wpair = [&](int j, int i) { return wv[j][i]; };
-        // the row statistics of this warp's rows (warp - 1 and warp + 7) are loaded one
-        // tile ahead, so no row starts with a dependent global load
-        constexpr int RPW = LNB_ROWS / 8;
-        float nm[RPW], nr[RPW];
-        auto load_stats = [&](int t) {
-#pragma unroll
-            for (int i = 0; i < RPW; i++) {
-                const int row = t * LNB_ROWS + warp - 1 + 8 * i;
-                nm[i] = (RMS || t >= ntiles || row >= M) ? 0.f : mean[row];
-                nr[i] = (t >= ntiles || row >= M) ? 0.f : rstd[row];
-            }
-        };
-        load_stats(blockIdx.x);
-        int it = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, it++) {
-            float cm[RPW], cr[RPW];
-#pragma unroll
-            for (int i = 0; i < RPW; i++) {
-                cm[i] = nm[i];
-                cr[i] = nr[i];
-            }
-            load_stats(t + gridDim.x);
-            const int s = it % LNB_STAGES;
-            const bool ok = tc::mbar_wait(&full[s], (it / LNB_STAGES) & 1, abort_flag, nullptr);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            const int rows = min(LNB_ROWS, M - t * LNB_ROWS);
-            const uint8_t* st = smem + s * stage_bytes;
-#pragma unroll
-            for (int ri = 0; ri < RPW; ri++) {
-                const int r = warp - 1 + 8 * ri;
-                if (r >= rows) break;
-                const int row = t * LNB_ROWS + r;
-                const uint4* d = reinterpret_cast<const uint4*>(st + (size_t)r * C * 2);
-                const uint4* x = reinterpret_cast<const uint4*>(st + sub_bytes + (size_t)r * C * 2);
-                const uint4* dr_in = reinterpret_cast<const uint4*>(st + 2 * sub_bytes + (size_t)r * C * 2);
-                const float rs = cr[ri];
-                const float2 rs2 = make_float2(rs, rs), nmr = make_float2(-cm[ri] * rs, -cm[ri] * rs);
-                // n = (x - mean) rstd (kept in xv), g = w dout (dout kept packed in dk);
-                // row sums of g and g n
-                float2 xv[NV][4];
-                uint32_t dk[NV][4];
-                float2 sg = make_float2(0.f, 0.f), sgn = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int j = 0; j < NV; j++) {
-                    const uint4 ud = d[j * 32 + lane], ux = x[j * 32 + lane];
-                    const uint32_t wx[4] = {ux.x, ux.y, ux.z, ux.w};
-                    dk[j][0] = ud.x;
-                    dk[j][1] = ud.y;
-                    dk[j][2] = ud.z;
-                    dk[j][3] = ud.w;
-                    float2 g[4];
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const float2 dd = make_float2(bf16_lo(dk[j][i]), bf16_hi(dk[j][i]));
-                        const float2 n = fma2(make_float2(bf16_lo(wx[i]), bf16_hi(wx[i])), rs2, nmr);
-                        g[i] = mul2(wpair(j, i), dd);
-                        if (!RMS) ab[j][i] = add2(ab[j][i], dd);
-                        aw[j][i] = fma2(n, dd, aw[j][i]);
-                        xv[j][i] = n;
-                    }
-                    sg = add2(sg, add2(add2(g[0], g[1]), add2(g[2], g[3])));
-                    sgn = fma2(g[0], xv[j][0], fma2(g[1], xv[j][1], fma2(g[2], xv[j][2], fma2(g[3], xv[j][3], sgn))));
-                }
-                const float gm = RMS ? 0.f : warp_sum(sg.x + sg.y) / C;
-                const float gnm = warp_sum(sgn.x + sgn.y) / C;
-                const float2 ngm = make_float2(-gm, -gm), ngnm = make_float2(-gnm, -gnm);
-                uint4* dr_out = reinterpret_cast<uint4*>(dres + (size_t)row * C);
-#pragma unroll
-                for (int j = 0; j < NV; j++) {
-                    const uint4 uo = dr_in[j * 32 + lane];
-                    const uint32_t wo[4] = {uo.x, uo.y, uo.z, uo.w};
-                    uint32_t po[4];
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        // dres += (g - gm - n gnm) rstd
-                        const float2 g = mul2(wpair(j, i), make_float2(bf16_lo(dk[j][i]), bf16_hi(dk[j][i])));
-                        const float2 v = fma2(xv[j][i], ngnm, add2(g, ngm));
-                        const float2 o = fma2(v, rs2, make_float2(bf16_lo(wo[i]), bf16_hi(wo[i])));
-                        po[i] = pack_bf16x2_rn(o.x, o.y);
-                        if (OUTSUM)  // the column sums of dres as stored
-                            ar[OUTSUM ? j : 0][i] = add2(ar[OUTSUM ? j : 0][i], make_float2(bf16_lo(po[i]), bf16_hi(po[i])));
-                    }
-                    dr_out[j * 32 + lane] = make_uint4(po[0], po[1], po[2], po[3]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&empty[s]);
-        }
-    }
-    // every stage is consumed (or the loop gave up): reuse the ring for the block's sums
-    __syncthreads();
-    float* sh = reinterpret_cast<float*>(smem);  // [8 warps][NS][C]
-    if (warp >= 1) {
-#pragma unroll
-        for (int j = 0; j < NV; j++)
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const int c = j * 256 + lane * 8 + 2 * i;
-                float* s0 = sh + ((warp - 1) * NS + 0) * C + c;
-                float* s1 = sh + ((warp - 1) * NS + 1) * C + c;
-                s0[0] = aw[j][i].x;
-                s0[1] = aw[j][i].y;
-                s1[0] = ab[j][i].x;
-                s1[1] = ab[j][i].y;
-                if (OUTSUM) {
-                    float* s2 = sh + ((warp - 1) * NS + 2) * C + c;
-                    s2[0] = ar[OUTSUM ? j : 0][i].x;
-                    s2[1] = ar[OUTSUM ? j : 0][i].y;
-                }
-            }
-    }
-    __syncthreads();
-    for (int k = 0; k < NS; k++) {
-        float* pk = part + (size_t)(k * gridDim.x + blockIdx.x) * C;
-        for (int c = threadIdx.x; c < C; c += blockDim.x) {
-            float a = 0.f;
-#pragma unroll
-            for (int wi = 0; wi < 8; wi++) a += sh[(wi * NS + k) * C + c];
-            pk[c] = a;
-        }
-    }
-}
 
 template <typename T>
 __global__ void __launch_bounds__(256) ln_bwd_k(T* dres, float* part, const T* dout, const T* inp,
@@ -1097,9 +908,9 @@ static cudaError_t colreduce(float* out0, float* out1, float* out2, const float*
     return cudaGetLastError();
 }
 
-// bf16 backward, rows streamed through shared memory as in ln_bwd_tma_k (warp 0 copies
-// tiles of 16 rows of dout, x and dres into a 3-stage ring), computed in two phases per
-// tile by 12 warps.  Phase A, a warp per row: the row sums of g = w dout and g n, n = (x -
+// bf16 backward, rows streamed through shared memory: one CTA per SM; warp 0 copies tiles
+// of 16 rows of dout, x and dres (three contiguous bulk copies) into a 3-stage ring; they
+// are computed in two phases per tile by 12 warps.  Phase A, a warp per row: the row sums of g = w dout and g n, n = (x -
 // mean) rstd, kept with the row's mean and rstd in a small table (two, by tile parity).
 // Phase B, once every warp has filled the table (an mbarrier, bounded wait): thread t owns the 8 columns of chunk t % (C/8) and the
 // rows t / (C/8), + RG, ... of the tile; it writes dres += (g - mean(g) - n mean(g n))
