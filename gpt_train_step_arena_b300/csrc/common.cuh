@@ -208,6 +208,42 @@ G2_DEV float2 mul2(float2 a, float2 b) {
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
 }
+// GELU (tanh form) and its derivative on two values, for the GEMM epilogues.  With
+// r = 1 / (e + 1), e = 2^(2 log2(e) u) = e^{2u}, tanh(u) = 1 - 2r, so
+//   gelu(x)  = 0.5 x (1 + tanh u)                      = x (1 - r)
+//   gelu'(x) = 0.5 (1 + tanh u) + 0.5 x sech^2(u) u'   = (1 - r) (1 + 2 k x r (1 + 3 c x^2))
+// with u = k (x + c x^3), k = sqrt(2/pi), c = 0.044715 and sech^2 = 1 - tanh^2 = 4 r (1 - r):
+// the same exponential and reciprocal approximations as the scalar forms, in about half
+// the instructions (results differ from them by a few rounding steps, far below a bf16
+// rounding).  Saturation: e -> inf gives r = 0 (gelu = x, gelu' = 1); e -> 0 gives r = 1
+// (gelu = 0, gelu' = 0).
+G2_DEV float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+G2_DEV float2 gelu_r2(float2 x, float2& r) {  // r of both values (returned through r), x^2
+    constexpr float K2 = 2.0f * 1.4426950408889634f * 0.7978845608028654f;  // 2 log2(e) k
+    constexpr float C2 = K2 * 0.044715f;
+    const float2 x2 = mul2(x, x);
+    const float2 u = mul2(x, fma2(x2, make_float2(C2, C2), make_float2(K2, K2)));
+    r = make_float2(rcp_approx(ex2_ftz(u.x) + 1.0f), rcp_approx(ex2_ftz(u.y) + 1.0f));
+    return x2;
+}
+G2_DEV float2 gelu2(float2 x) {
+    float2 r;
+    gelu_r2(x, r);
+    return fma2(make_float2(-x.x, -x.y), r, x);  // x - x r
+}
+G2_DEV float2 gelu_grad2(float2 x) {
+    constexpr float K = 0.7978845608028654f, C = 0.044715f;
+    float2 r;
+    const float2 x2 = gelu_r2(x, r);
+    const float2 a = fma2(r, make_float2(-1.f, -1.f), make_float2(1.f, 1.f));                    // 1 - r
+    const float2 poly = fma2(x2, make_float2(6.f * K * C, 6.f * K * C), make_float2(2.f * K, 2.f * K));  // 2k (1 + 3c x^2)
+    const float2 b = fma2(mul2(x, r), poly, make_float2(1.f, 1.f));
+    return mul2(a, b);
+}
 // the two bf16 halves of a 32-bit word as fp32 (exact)
 G2_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 G2_DEV float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

@@ -160,7 +160,11 @@ G2_DEV void epilogue_math(const Params& p, float* v, const uint8_t* in_row_buf, 
         float x[CW];
         unstage_row_bf16(in_row_buf, lane, x);
 #pragma unroll
-        for (int i = 0; i < CW; i++) v[i] *= gelu_tanh_grad_fast(x[i]);
+        for (int i = 0; i < CW; i += 2) {
+            const float2 g = gelu_grad2(make_float2(x[i], x[i + 1]));
+            v[i] *= g.x;
+            v[i + 1] *= g.y;
+        }
         return;
     }
     if (p.bias) {
@@ -530,7 +534,11 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI, PAIR>::THREADS, 1)
                 stage_row<EO::F32>(stg, lane, v);
                 if (EPI == E_GELU) {
 #pragma unroll
-                    for (int i = 0; i < EO::CW; i++) v[i] = gelu_tanh_fast(v[i]);
+                    for (int i = 0; i < EO::CW; i += 2) {
+                        const float2 gl = gelu2(make_float2(v[i], v[i + 1]));
+                        v[i] = gl.x;
+                        v[i + 1] = gl.y;
+                    }
                     stage_row<false>(stg + 4096, lane, v);
                 }
                 fence_async_smem();
