@@ -598,6 +598,29 @@ __global__ void splitk_reduce_k(float* out, long long ldo, const float* ws, int 
     }
 }
 
+// The same sum four columns at a time (N and ldo multiples of 4, 16-byte aligned buffers,
+// M * N / 4 < 2^31): splits added in the same order from 0, so the result is bitwise that
+// of splitk_reduce_k, with one 32-bit division per four elements instead of a 64-bit one
+// per element.
+__global__ void splitk_reduce4_k(float* out, long long ldo, const float* ws, int M, int N, int splits) {
+    G2_PDL_ENTRY();
+    const int n4 = N / 4;
+    const unsigned nv = (unsigned)M * (unsigned)n4;
+    const size_t n = (size_t)M * N;
+    for (unsigned v = blockIdx.x * blockDim.x + threadIdx.x; v < nv; v += gridDim.x * blockDim.x) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < splits; sp++) {
+            const float4 b = reinterpret_cast<const float4*>(ws + (size_t)sp * n)[v];
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+        const unsigned m = v / (unsigned)n4, c = (v - m * (unsigned)n4) * 4u;
+        *reinterpret_cast<float4*>(out + (size_t)m * ldo + c) = a;
+    }
+}
+
 // The same sum with the forward epilogue of a split product: v = sum_s ws[s][m][n]
 // (+ bias[n]) (+ R[m,n]); D = v (bf16, or fp32 with d_f32); with D2, D2 = gelu(v) from the
 // unrounded v (as the fused GELU epilogue does).
@@ -629,6 +652,20 @@ static int num_sms() {
         if (n <= 0) n = 148;
     }
     return n;
+}
+
+// Launch of the fixed-order split-K sum: the four-column form where it applies.
+static void launch_splitk_reduce(float* out, long long ldo, const float* ws, int M, int N, int splits,
+                                 cudaStream_t s) {
+    const size_t n = (size_t)M * N;
+    const bool vec = (N % 4) == 0 && (ldo % 4) == 0 && (((uintptr_t)out | (uintptr_t)ws) & 15) == 0 &&
+                     n / 4 < (size_t)1 << 31;
+    const size_t work = vec ? n / 4 : n;
+    const unsigned blocks = (unsigned)std::min<size_t>((work + 255) / 256, (size_t)num_sms() * 8);
+    if (vec)
+        ::g2::launch_k(splitk_reduce4_k, blocks, 256, 0, s, out, ldo, ws, M, N, splits);
+    else
+        ::g2::launch_k(splitk_reduce_k, blocks, 256, 0, s, out, ldo, ws, M, N, splits);
 }
 
 // Tile mode of a bf16 product: 128- or 256-row tiles on one SM each, or TILE_PAIR: 256-row
@@ -940,9 +977,7 @@ static cudaError_t gemm_tc_tf32(const GemmArgs& a, float* ws, size_t ws_bytes, i
     if (splits > 1) {
         cudaError_t e = BN == 256 ? launch_tf32<256, E_PARTIAL>(bmt, mp, p, s) : launch_tf32<128, E_PARTIAL>(bmt, mp, p, s);
         if (e != cudaSuccess) return e;
-        size_t n = (size_t)a.M * a.N;
-        unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
-        ::g2::launch_k(splitk_reduce_k, blocks, 256, 0, s, (float*)a.D, a.ldd, ws, a.M, a.N, splits);
+        launch_splitk_reduce((float*)a.D, a.ldd, ws, a.M, a.N, splits, s);
         return cudaGetLastError();
     }
     return BN == 256 ? launch_tf32<256, E_STORE_F32>(bmt, mp, p, s) : launch_tf32<128, E_STORE_F32>(bmt, mp, p, s);
@@ -1046,7 +1081,7 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
                 a.D, a.ldd, a.d_f32, ws, a.M, a.N, splits, a.bias, (const bf16*)a.R, a.ldr,
                 a.epi == EPI_GELU ? (bf16*)a.D2 : nullptr, a.ldd2);
         else
-            ::g2::launch_k(splitk_reduce_k, blocks, 256, 0, s, (float*)a.D, a.ldd, ws, a.M, a.N, splits);
+            launch_splitk_reduce((float*)a.D, a.ldd, ws, a.M, a.N, splits, s);
         return cudaGetLastError();
     }
     switch (a.epi) {
