@@ -65,6 +65,9 @@ SIGNATURES = {
     "gpt2_op_matmul_workspace": (SZ, [I, I, I, I, I, I]),
     "gpt2_op_matmul_ex": (I, [I, I, I, I, P, ct.c_longlong, I, P, ct.c_longlong, I, P, ct.c_longlong, P, P,
                               ct.c_longlong, P, ct.c_longlong, P, ct.c_longlong, I, P, SZ, P]),
+    "gpt2_op_matmul_gelu_bwd_bias_grad_workspace": (SZ, [I, I]),
+    "gpt2_op_matmul_gelu_bwd_bias_grad": (I, [I, I, I, P, ct.c_longlong, I, P, ct.c_longlong, I, P, ct.c_longlong,
+                                              P, ct.c_longlong, P, P, SZ, P]),
     "gpt2_op_adamw": (I, [P, P, P, P, P, SZ, F, F, F, F, F, I, P]),
     "gpt2_op_attention_forward": (I, [I, P, P, P, I, I, I, I, P]),
     "gpt2_op_attention_backward": (I, [I, P, P, P, P, P, I, I, I, I, P, P]),

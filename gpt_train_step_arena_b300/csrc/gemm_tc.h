@@ -8,6 +8,9 @@ namespace g2 {
 // operands, or fp32 operands with tf32 set (then K-major only, fp32 output, store or bias
 // epilogue).
 bool gemm_tc_supported(const GemmArgs& a);
+// True when gemm_tc writes the per-32-row column sums of a GELU' product's output into
+// a.colsum_part (set, bf16, EPI_GELU_BWD, N even, 8-byte aligned, tensor-core path).
+bool gemm_tc_fuses_colsum(const GemmArgs& a);
 // Workspace the kernel wants for split-K partial sums of an fp32-output product.
 size_t gemm_tc_workspace_bytes(int M, int N, int K);
 // Workspace of a product with one row tile (M <= 128) launched with skinny_split set.

@@ -73,6 +73,7 @@ struct Params {
     const bf16* P;
     long long ldp;
     float* ws;  // split-K partials: [splits][M][N] fp32
+    float* cs_part;  // GELU' epilogue: column sums of the stored output per 32-row group, or null
     int* flags;
 };
 
@@ -552,6 +553,25 @@ __global__ void __launch_bounds__(Cfg<BN, BMT, EPI, PAIR>::THREADS, 1)
                     bulk_commit();
                     newest_set = set;
                 }
+                if constexpr (EPI == E_GELU_BWD) {
+                    // the bias gradient of this pre-activation: lane l reads columns 2l and
+                    // 2l + 1 of the warp's 32 staged rows (the stored bf16 values, 4-byte
+                    // words one row apart, conflict-free) and adds them in row order; the
+                    // TMA store reads the same buffer meanwhile.  Rows past M are zeros
+                    // (zero-filled operand and pre-activation rows).
+                    if (p.cs_part && gm0 < p.M && in_ok) {
+                        const uint8_t* colp = stg + ((lane & 3) << 2);
+                        float2 cs = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int r = 0; r < 32; r++) {
+                            const uint32_t w =
+                                *reinterpret_cast<const uint32_t*>(colp + r * 128 + ((((lane >> 2) ^ r) & 7) << 4));
+                            cs = add2(cs, make_float2(bf16_lo(w), bf16_hi(w)));
+                        }
+                        const int j = gn0 + 2 * lane;
+                        if (j < p.N) *reinterpret_cast<float2*>(p.cs_part + (size_t)(gm0 >> 5) * p.N + j) = cs;
+                    }
+                }
                 if (!in_ok) {
                     // a wait gave up: let the loads already issued land before leaving
                     drain_in();
@@ -922,6 +942,11 @@ bool gemm_tc_supported(const GemmArgs& a) {
     return true;
 }
 
+bool gemm_tc_fuses_colsum(const GemmArgs& a) {
+    return a.colsum_part && a.epi == EPI_GELU_BWD && a.in_type == ACT_BF16 && !a.d_f32 && (a.N % 2) == 0 &&
+           ((uintptr_t)a.colsum_part & 7) == 0 && gemm_tc_supported(a);
+}
+
 // D (fp32) = A . B^T (+ bias) with fp32 operands read as TF32.
 static cudaError_t gemm_tc_tf32(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, cudaStream_t s) {
     const int BN = a.N > 128 ? 256 : 128;
@@ -1028,6 +1053,7 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
     p.D2 = (bf16*)a.D2; p.ldd2 = a.ldd2;
     p.P = (const bf16*)a.P; p.ldp = a.ldp;
     p.ws = ws;
+    p.cs_part = gemm_tc_fuses_colsum(a) ? a.colsum_part : nullptr;
     p.flags = flags ? flags : fallback_flag();
 
     // output maps for the TMA stores: 32-row boxes of 128 bytes (64 bf16 or 32 fp32)
@@ -1064,10 +1090,10 @@ cudaError_t gemm_tc(const GemmArgs& a, float* ws, size_t ws_bytes, int* flags, c
         std::lock_guard<std::mutex> lk(g_variant_mu);
         char pairs[32] = "";
         if (bmt == TILE_PAIR) snprintf(pairs, sizeof pairs, " clusters=%d", pair_max_clusters());
-        snprintf(g_variant, sizeof g_variant, "rows=%s cols=%d splits=%d a=%s b=%s epi=%s%s%s%s",
+        snprintf(g_variant, sizeof g_variant, "rows=%s cols=%d splits=%d a=%s b=%s epi=%s%s%s%s%s",
                  bmt == TILE_PAIR ? "pair256" : (bmt == 256 ? "256" : "128"), BN, splits,
                  a_mn ? "mn" : "k", b_mn ? "mn" : "k", epi_names[a.epi], a.d_f32 ? " f32" : "",
-                 staged_in && a.epi == EPI_STORE ? " residual" : "", pairs);
+                 staged_in && a.epi == EPI_STORE ? " residual" : "", p.cs_part ? " colsum" : "", pairs);
     }
     cudaError_t e;
     if (splits > 1) {

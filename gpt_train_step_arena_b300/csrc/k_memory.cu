@@ -908,6 +908,12 @@ static cudaError_t colreduce(float* out0, float* out1, float* out2, const float*
     return cudaGetLastError();
 }
 
+cudaError_t colsum_reduce(float* out, const float* part, int n, int N, cudaStream_t s) {
+    if (N <= 0) return cudaSuccess;
+    if (n <= 0) return cudaMemsetAsync(out, 0, (size_t)N * sizeof(float), s);
+    return colreduce(out, nullptr, nullptr, part, n, N, s);
+}
+
 // bf16 backward, rows streamed through shared memory: one CTA per SM; warp 0 copies tiles
 // of 16 rows of dout, x and dres (three contiguous bulk copies) into a 3-stage ring; they
 // are computed in two phases per tile by 12 warps.  Phase A, a warp per row: the row sums of g = w dout and g n, n = (x -

@@ -66,6 +66,10 @@ cudaError_t layernorm_backward(ActType at, void* dres, float* dw, float* db, flo
 // ---- bias gradient: out[n] = sum_m X[m,n] (fixed order) --------------------------
 size_t colsum_partial_floats(int M, int N);
 cudaError_t colsum(ActType at, float* out, const void* X, int M, int N, float* part, cudaStream_t s);
+// out[c] = sum over i < n of part[i*N + c], rows added in a fixed order (the second pass
+// of colsum; also the sum of a product epilogue's per-row-group column sums); n = 0
+// writes zeros.
+cudaError_t colsum_reduce(float* out, const float* part, int n, int N, cudaStream_t s);
 
 // ---- fused softmax + cross-entropy forward and backward (llm.c §1.13-§1.15) -------
 // logits (M,Vp) is overwritten in place by dlogits = (softmax - onehot) * dloss over the
@@ -162,6 +166,10 @@ struct GemmArgs {
     int tf32;                   // fp32 operands: contract on the tensor cores as TF32 (else exact fp32)
     float* tws;                 // TF32: workspace for K-major copies of M/N-major operands, or null
     size_t tws_bytes;
+    // EPI_GELU_BWD on the bf16 tensor-core path (gemm_tc_fuses_colsum): the epilogue also
+    // writes the column sums of the stored bf16 output per 32-row group,
+    // colsum_part[ceil(M/32)][N] fp32 (8-byte aligned), for colsum_reduce to add up; or null
+    float* colsum_part;
 };
 cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t s);
 

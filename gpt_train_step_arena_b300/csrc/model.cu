@@ -187,9 +187,11 @@ static cudaError_t gemm_fwd(gpt2* m, int M, int N, int K, const void* X, const v
     tf32_args(m, a);
     return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
 }
-// dX[M,K] = dY[M,N] . W[N,K]  (optionally times gelu'(P))
+// dX[M,K] = dY[M,N] . W[N,K]  (optionally times gelu'(P)).  With cs_part, *cs_fused
+// tells whether the product's epilogue also wrote the per-32-row column sums of dX there
+// (the bias gradient's first pass).
 static cudaError_t gemm_dgrad(gpt2* m, int M, int N, int K, const void* dY, const void* W, void* dX,
-                              const void* P) {
+                              const void* P, float* cs_part = nullptr, bool* cs_fused = nullptr) {
     GemmArgs a{};
     a.M = M; a.N = K; a.K = N; a.in_type = m->at;
     a.A = dY; a.sAm = N; a.sAk = 1;
@@ -198,7 +200,9 @@ static cudaError_t gemm_dgrad(gpt2* m, int M, int N, int K, const void* dY, cons
     a.P = P; a.ldp = K;
     a.epi = P ? EPI_GELU_BWD : EPI_STORE;
     a.flags = m->tflags;
+    a.colsum_part = cs_part;
     tf32_args(m, a);
+    if (cs_fused) *cs_fused = cs_part && gemm_tc_fuses_colsum(a);
     return gemm_dispatch(a, m->gemm_ws, m->gemm_ws_bytes, m->stream);
 }
 // dW[N,K] (fp32, overwritten) = dY[M,N]^T . X[M,K]
@@ -397,7 +401,9 @@ static int alloc_acts(gpt2* m, int B, int T) {
         *attD, *lnp, *csp, *enc, *ws, *tws;
     size_t ln_part = ln_bwd_partial_floats(m->C) * 4;
     size_t maxN = std::max<size_t>(4 * C, (size_t)m->Vp);
-    size_t cs_part = colsum_partial_floats((int)M, (int)maxN) * 4;
+    // column-sum partials: the bias-gradient pass's row blocks, or the GELU' product's
+    // 32-row groups over the 4C hidden columns
+    size_t cs_part = std::max(colsum_partial_floats((int)M, (int)maxN), (M + 31) / 32 * 4 * C) * 4;
     size_t enc_bytes = encoder_bwd_scratch_bytes((int)M, m->V, m->C);
     m->gemm_ws_bytes = gemm_workspace_bytes((int)M, m->C, m->Vp, m->L);
     // TF32: the largest set of operand copies of one product (the LM-head weight gradient
@@ -620,8 +626,11 @@ extern "C" int gpt2_backward(gpt2_t* m) {
         char* fch = act(m, m->fch, l * 4 * MC);
         char* fchg = act(m, m->fchg, l * 4 * MC);
         // fcproj: res_out = fchg . Wfp^T + bfp + res2   (dres = d res_out)
+        // (its epilogue also sums the columns of dfch per 32 rows: the fc bias gradient)
+        bool fcb_fused = false;
         OP(GPT2_K_GEMM, gemm_flops(M, 4 * C, C),
-           gemm_dgrad(m, (int)M, C, 4 * C, m->dres, pw(m, P_FPW, (size_t)l * 4 * C * C), m->dfch, fch));
+           gemm_dgrad(m, (int)M, C, 4 * C, m->dres, pw(m, P_FPW, (size_t)l * 4 * C * C), m->dfch, fch,
+                      m->cs_part, &fcb_fused));
         OP(GPT2_K_GEMM, gemm_flops(C, 4 * C, M),
            gemm_wgrad(m, (int)M, C, 4 * C, m->dres, fchg, pf(m, g, P_FPW) + (size_t)l * 4 * C * C));
         // (the fcproj bias gradient, the column sum of dres, came out of the layernorm
@@ -631,8 +640,12 @@ extern "C" int gpt2_backward(gpt2_t* m) {
            gemm_dgrad(m, (int)M, 4 * C, C, m->dfch, pw(m, P_FCW, (size_t)l * 4 * C * C), m->dln, nullptr));
         OP(GPT2_K_GEMM, gemm_flops(4 * C, C, M),
            gemm_wgrad(m, (int)M, 4 * C, C, m->dfch, ln2, pf(m, g, P_FCW) + (size_t)l * 4 * C * C));
-        OP(GPT2_K_BIAS_GRAD, cs_bytes(4 * C),
-           colsum(m->at, pf(m, g, P_FCB) + l * 4 * C, m->dfch, (int)M, 4 * C, m->cs_part, s));
+        if (fcb_fused)
+            OP(GPT2_K_BIAS_GRAD, 4.0 * ((M + 31) / 32 + 1) * 4 * C,
+               colsum_reduce(pf(m, g, P_FCB) + l * 4 * C, m->cs_part, (int)((M + 31) / 32), 4 * C, s));
+        else
+            OP(GPT2_K_BIAS_GRAD, cs_bytes(4 * C),
+               colsum(m->at, pf(m, g, P_FCB) + l * 4 * C, m->dfch, (int)M, 4 * C, m->cs_part, s));
         // ln2 (dres becomes d res2)
         OP(GPT2_K_LAYERNORM, ln_bwd_bytes,
            layernorm_backward(m->at, m->dres, pf(m, g, P_LN2W) + l * C, pf(m, g, P_LN2B) + l * C,

@@ -1,4 +1,5 @@
 // C ABI of include/gpt2_ops.h: argument checks and one launcher call each.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -128,6 +129,45 @@ extern "C" int gpt2_op_matmul_ex(int dtype, int M, int N, int K, const void* A, 
     if (!gemm_tc_path(a)) return op_fail(GPT2_ERR_ARG, "matmul_ex: layout or alignment outside the fused path");
     return op_cuda(gemm_dispatch(a, (float*)workspace, workspace ? workspace_bytes : 0, (cudaStream_t)stream),
                    "matmul_ex");
+}
+
+extern "C" size_t gpt2_op_matmul_gelu_bwd_bias_grad_workspace(int M, int N) {
+    if (M <= 0 || N <= 0) return 0;
+    const size_t groups = (size_t)((M + 31) / 32) * N;
+    return std::max(groups, colsum_partial_floats(M, N)) * sizeof(float);
+}
+
+extern "C" int gpt2_op_matmul_gelu_bwd_bias_grad(int M, int N, int K, const void* A, long long lda, int a_kmajor,
+                                                 const void* B, long long ldb, int b_kmajor, void* D, long long ldd,
+                                                 const void* P, long long ldp, float* dbias, void* workspace,
+                                                 size_t workspace_bytes, void* stream) {
+    if (M < 0 || N < 0 || K < 0) return op_fail(GPT2_ERR_ARG, "gelu_bwd_bias_grad: negative size");
+    if (N == 0) return GPT2_OK;
+    if (!dbias) return op_fail(GPT2_ERR_ARG, "gelu_bwd_bias_grad: null dbias");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (M == 0) return op_cuda(cudaMemsetAsync(dbias, 0, (size_t)N * sizeof(float), s), "gelu_bwd_bias_grad");
+    if (!A || !B || !D || !P || !workspace) return op_fail(GPT2_ERR_ARG, "gelu_bwd_bias_grad: null pointer");
+    const size_t need = gpt2_op_matmul_gelu_bwd_bias_grad_workspace(M, N);
+    if (workspace_bytes < need || ((uintptr_t)workspace & 7))
+        return op_fail(GPT2_ERR_ARG, "gelu_bwd_bias_grad: workspace of %zu bytes (8-byte aligned) needed, %zu given",
+                       need, workspace_bytes);
+    GemmArgs a{};
+    a.M = M; a.N = N; a.K = K; a.in_type = ACT_BF16;
+    a.A = A;
+    if (a_kmajor) { a.sAm = lda; a.sAk = 1; } else { a.sAm = 1; a.sAk = lda; }
+    a.B = B;
+    if (b_kmajor) { a.sBn = ldb; a.sBk = 1; } else { a.sBn = 1; a.sBk = ldb; }
+    a.D = D; a.ldd = ldd; a.d_f32 = 0;
+    a.P = P; a.ldp = ldp;
+    a.epi = EPI_GELU_BWD;
+    a.colsum_part = (float*)workspace;
+    if (!gemm_tc_path(a)) return op_fail(GPT2_ERR_ARG, "gelu_bwd_bias_grad: layout or alignment outside the fused path");
+    const bool fused = gemm_tc_fuses_colsum(a);
+    if (!fused && ldd != N) return op_fail(GPT2_ERR_ARG, "gelu_bwd_bias_grad: odd N needs ldd == N");
+    int rc = op_cuda(gemm_dispatch(a, nullptr, 0, s), "gelu_bwd_bias_grad");
+    if (rc) return rc;
+    if (fused) return op_cuda(colsum_reduce(dbias, (const float*)workspace, (M + 31) / 32, N, s), "gelu_bwd_bias_grad");
+    return op_cuda(colsum(ACT_BF16, dbias, D, M, N, (float*)workspace, s), "gelu_bwd_bias_grad");
 }
 
 extern "C" int gpt2_op_adamw(float* p, const float* g, float* m, float* v, void* shadow, size_t n,

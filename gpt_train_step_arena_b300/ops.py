@@ -162,6 +162,22 @@ def linear_fused(A: torch.Tensor, W: torch.Tensor, epilogue: int, bias=None, R=N
     return (D, D2) if D2 is not None else D
 
 
+def linear_gelu_bwd_bias_grad(A: torch.Tensor, W: torch.Tensor, P: torch.Tensor, b_kmajor=False):
+    """bf16 D = (A . W) * gelu'(P) (W (K,N), or W (N,K) with b_kmajor) and dbias = the
+    column sums of the stored D (fp32).  Returns (D, dbias)."""
+    M, K = A.shape
+    Nn = W.shape[0] if b_kmajor else W.shape[1]
+    D = torch.empty(M, Nn, dtype=A.dtype, device=A.device)
+    dbias = torch.empty(Nn, dtype=torch.float32, device=A.device)
+    wsb = N.lib.gpt2_op_matmul_gelu_bwd_bias_grad_workspace(M, Nn)
+    ws = torch.empty(max(wsb, 8), dtype=torch.uint8, device=A.device)
+    _check(N.lib.gpt2_op_matmul_gelu_bwd_bias_grad(M, Nn, K, A.data_ptr(), A.stride(0), 1, W.data_ptr(),
+                                                   W.stride(0), int(b_kmajor), D.data_ptr(), D.stride(0),
+                                                   P.data_ptr(), P.stride(0), dbias.data_ptr(), ws.data_ptr(),
+                                                   ws.numel(), _stream()))
+    return D, dbias
+
+
 def encoder_forward(tokens: torch.Tensor, wte: torch.Tensor, wpe: torch.Tensor, flags=None):
     """tokens (B,T) int32, wte (V,C), wpe (>=T,C) -> out (B,T,C) like wte."""
     B, T = tokens.shape

@@ -93,6 +93,24 @@ int gpt2_op_matmul_ex(int dtype, int M, int N, int K, const void* A, long long l
                       const void* R, long long ldr, void* D2, long long ldd2, const void* P, long long ldp,
                       int epilogue, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The FC layer's pre-activation gradient and its bias gradient in one call (llm.c §1.6
+ * matmul_backward: dbias[o] = sum over positions of dout[., o]; §1.10 gelu_backward),
+ * bf16 only:
+ *   D[m,n] = (A.B^T)[m,n] * gelu_tanh'(P[m,n])     as gpt2_op_matmul_ex with GPT2_EPI_GELU_BWD
+ *   dbias[n] = sum over 0 <= m < M of D[m,n]        fp32, overwritten, over the stored bf16 D
+ * The product's epilogue sums each 32-row group's columns into the workspace and a
+ * fixed-order pass adds the groups (should the epilogue not take it, a separate column-sum
+ * pass reads D, which then needs ldd == N).  Sums are in a fixed order, so two calls give
+ * bitwise equal results.  workspace: device memory of at least
+ * gpt2_op_matmul_gelu_bwd_bias_grad_workspace(M, N) bytes, 8-byte aligned.  Returns
+ * GPT2_ERR_ARG (nothing launched) for null pointers, a layout the fused path cannot take
+ * (as gpt2_op_matmul_ex) or a short workspace; M = 0 writes dbias = 0. */
+size_t gpt2_op_matmul_gelu_bwd_bias_grad_workspace(int M, int N);
+int gpt2_op_matmul_gelu_bwd_bias_grad(int M, int N, int K, const void* A, long long lda, int a_kmajor,
+                                      const void* B, long long ldb, int b_kmajor, void* D, long long ldd,
+                                      const void* P, long long ldp, float* dbias, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
 /* AdamW over n fp32 elements (llm.c §1.26 gpt2_update), in place on p, m, v; g is read.
  * shadow_bf16 (n bfloat16, may be NULL) receives the rounded updated parameters.
  * t >= 1 counts updates. */
