@@ -21,7 +21,9 @@ by RMSNorm, page "microGPT 3D", lesson 04).
 --impl reference times the CPU oracle (test infrastructure, plain C, all host cores)
 on bounded samples of the same workload, rank 0 only: fwd+bwd on B=1,T=--cpu-tokens
 positions plus one AdamW over all parameters per step, extrapolated to the step's B*T
-positions.  The same sample gives the `cpu_baseline` of the default arm.
+positions (workloads of at most 4096 tokens per step are timed in full).  The same
+sample gives the `cpu_baseline` of the default arm; --cpu-variants adds the double and
+float oracles on one thread and on every core.
 """
 from __future__ import annotations
 
@@ -55,6 +57,14 @@ def flops_per_token(c, Vp):
     3 * 2 * C * (T+1) * L (QK^T and PV over t2 <= t; backward = 2x forward)."""
     L, C, T = c["L"], c["C"], c["T"]
     return 6.0 * (12 * L * C * C + Vp * C) + 3.0 * 2.0 * C * (T + 1) * L
+
+
+def palm_flops_per_token(c, Vp):
+    """The PaLM-paper convention, reported beside the algorithmic count: 6 N + 12 L C T
+    per token, N = every parameter (the padded wte included)."""
+    from gpt_train_step_arena_b300 import synth
+    n = sum(synth.param_sizes(c["L"], c["C"], Vp, c["maxT"]))
+    return 6.0 * n + 12.0 * c["L"] * c["C"] * c["T"]
 
 
 def measure_tf32_peak():
@@ -198,17 +208,32 @@ def cpu_model() -> str:
     return "unknown"
 
 
-def oracle_sample(cfg, T_sample, stream_seed=1337, norm="layernorm"):
-    """The CPU oracle set up for one bounded sample of the workload: the full model, on
-    B=1, T=T_sample (the first T_sample positions of row 0 of step 0)."""
+FULL_STEP_TOKENS = 4096  # workloads up to this many tokens per step are timed in full
+
+
+def sample_shape(cfg, cpu_tokens):
+    """(B, T) of the oracle's CPU sample: the whole step for small workloads, else the
+    first cpu_tokens positions of row 0 (B=1)."""
+    if cfg["B"] * cfg["T"] <= FULL_STEP_TOKENS:
+        return cfg["B"], cfg["T"]
+    return 1, min(cpu_tokens, cfg["T"])
+
+
+def oracle_sample(cfg, B_s, T_s, stream_seed=1337, norm="layernorm", variant="f64"):
+    """The CPU oracle set up for one bounded sample of the workload: the full model on the
+    first B_s x T_s positions of step 0 (B_s = 1: the first T_s positions of row 0)."""
     from gpt_train_step_arena_b300 import synth
     from oracle.oracle import Model, cpu_threads
     L, C, NH, V, maxT = cfg["L"], cfg["C"], cfg["NH"], cfg["V"], cfg["maxT"]
     params = synth.init_params(L, C, V, maxT, seed=42)
     stream = synth.token_stream(cfg, steps=1, seed=stream_seed)
-    inp = stream[:T_sample].reshape(1, T_sample)
-    tgt = stream[1:T_sample + 1].reshape(1, T_sample)
-    m = Model(L, C, NH, V, maxT, norm=norm)
+    if B_s == 1:
+        inp = stream[:T_s].reshape(1, T_s)
+        tgt = stream[1:T_s + 1].reshape(1, T_s)
+    else:
+        assert T_s == cfg["T"], "a multi-row sample takes whole rows"
+        inp, tgt = synth.batch(stream, 0, B_s, T_s)
+    m = Model(L, C, NH, V, maxT, variant=variant, norm=norm)
     m.set_params(params)
     return m, inp, tgt, cpu_threads()
 
@@ -223,18 +248,53 @@ def oracle_step_time(m, inp, tgt, hp, t):
     return t1 - t0, time.perf_counter() - t1
 
 
-def extrapolated_tokens_per_s(cfg, T_s, t_fb, t_adam):
-    """Tokens/s of the full step extrapolated from the sample: the step's B*T positions cost
-    B*T/T_s times the sample's fwd+bwd, plus one AdamW over all parameters."""
+def extrapolated_tokens_per_s(cfg, sample_tokens, t_fb, t_adam):
+    """Tokens/s of the full step from the sample: the step's B*T positions cost
+    B*T/sample_tokens times the sample's fwd+bwd, plus one AdamW over all parameters
+    (exact when the sample is the whole step)."""
     BT = cfg["B"] * cfg["T"]
-    return BT / (BT / T_s * t_fb + t_adam)
+    return BT / (BT / sample_tokens * t_fb + t_adam)
 
 
-def cpu_sample_text(workload, T_s, t_fb, t_adam):
+def cpu_sample_text(workload, B_s, T_s, t_fb, t_adam, variant="f64", threads="OpenMP on the host cores"):
+    if B_s > 1:
+        return (f"full step: fwd+bwd of the {workload} model on its B={B_s},T={T_s} batch of step 0 "
+                f"({t_fb:.3g} s) plus one AdamW over all parameters ({t_adam:.3g} s); {variant} oracle, {threads}")
     return (f"extrapolated: fwd+bwd of the full {workload} model on B=1,T={T_s} (the first {T_s} positions of "
-            f"row 0 of step 0; {t_fb:.2f} s) scaled to the step's B*T positions, plus one AdamW over all "
-            f"parameters ({t_adam:.2f} s); f64 oracle, OpenMP on the host cores. Per-token attention work "
+            f"row 0 of step 0; {t_fb:.3g} s) scaled to the step's B*T positions, plus one AdamW over all "
+            f"parameters ({t_adam:.3g} s); {variant} oracle, {threads}. Per-token attention work "
             f"grows with T, so at T=1024 the oracle's step costs a few percent more per token than this")
+
+
+def cpu_leg(cfg, workload, norm, cpu_tokens, hp, t=1, variant="f64", threads=0):
+    """The oracle timed on one sample step: (tokens/s of the whole step, threads used, sample text).
+    threads: 0 = the OpenMP default (every host core or OMP_NUM_THREADS), else that many."""
+    from oracle.oracle import set_threads
+    B_s, T_s = sample_shape(cfg, cpu_tokens)
+    m, inp, tgt, cores = oracle_sample(cfg, B_s, T_s, norm=norm, variant=variant)
+    prev = set_threads(0, variant)
+    used = set_threads(threads if threads > 0 else cores, variant)
+    try:
+        t_fb, t_adam = oracle_step_time(m, inp, tgt, hp, t)
+    finally:
+        set_threads(prev, variant)
+    del m
+    text = cpu_sample_text(workload, B_s, T_s, t_fb, t_adam, variant,
+                           "one thread" if used == 1 else f"OpenMP, {used} threads")
+    return extrapolated_tokens_per_s(cfg, B_s * T_s, t_fb, t_adam), used, text
+
+
+def cpu_variants(cfg, workload, norm, cpu_tokens, hp):
+    """The double and float oracles, each on one thread and on every host core, on the same
+    sample (one step each, after one untimed step)."""
+    from oracle.oracle import cpu_threads
+    out = []
+    for variant in ("f64", "f32"):
+        for threads in (1, cpu_threads()):
+            cpu_leg(cfg, workload, norm, cpu_tokens, hp, 1, variant, threads)   # untimed: page in, warm caches
+            v, used, text = cpu_leg(cfg, workload, norm, cpu_tokens, hp, 2, variant, threads)
+            out.append({"oracle": variant, "threads": used, "value": v, "unit": "tokens/s", "sample": text})
+    return out
 
 
 def cpu_host_info():
@@ -248,8 +308,8 @@ def run_reference(args, rank, world):
         return
     from gpt_train_step_arena_b300 import synth
     cfg = dict(synth.WORKLOADS[args.workload])
-    T_s = min(args.cpu_tokens, cfg["T"])
-    m, inp, tgt, cores = oracle_sample(cfg, T_s, norm=args.norm)
+    B_s, T_s = sample_shape(cfg, args.cpu_tokens)
+    m, inp, tgt, cores = oracle_sample(cfg, B_s, T_s, norm=args.norm)
     hp = (cfg["lr"], cfg["b1"], cfg["b2"], cfg["eps"], cfg["wd"])
     for i in range(args.warmup):
         oracle_step_time(m, inp, tgt, hp, i + 1)
@@ -260,8 +320,8 @@ def run_reference(args, rank, world):
         t_adam += b
     t_fb /= args.steps
     t_adam /= args.steps
-    value = extrapolated_tokens_per_s(cfg, T_s, t_fb, t_adam)
-    sample = cpu_sample_text(args.workload, T_s, t_fb, t_adam)
+    value = extrapolated_tokens_per_s(cfg, B_s * T_s, t_fb, t_adam)
+    sample = cpu_sample_text(args.workload, B_s, T_s, t_fb, t_adam)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -272,6 +332,9 @@ def run_reference(args, rank, world):
                               "sample": sample}, **cpu_host_info()),
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    if args.cpu_variants:
+        del m
+        line["cpu_variants"] = cpu_variants(cfg, args.workload, args.norm, args.cpu_tokens, hp)
     print(json.dumps(line), flush=True)
 
 
@@ -387,13 +450,12 @@ def run_ours(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        T_s = min(args.cpu_tokens, cfg["T"])
-        m, inp, tgt, cores = oracle_sample(cfg, T_s, norm=args.norm)
-        t_fb, t_adam = oracle_step_time(m, inp, tgt, hp, 1)
-        cpu = dict({"value": extrapolated_tokens_per_s(cfg, T_s, t_fb, t_adam), "unit": "tokens/s",
-                    "cores": cores, "kind": "oracle",
-                    "sample": cpu_sample_text(args.workload, T_s, t_fb, t_adam)}, **cpu_host_info())
-        del m
+        v_cpu, cores, text = cpu_leg(cfg, args.workload, args.norm, args.cpu_tokens, hp)
+        cpu = dict({"value": v_cpu, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": text},
+                   **cpu_host_info())
+    cpu_var = None
+    if rank == 0 and world == 1 and args.cpu_variants:
+        cpu_var = cpu_variants(cfg, args.workload, args.norm, args.cpu_tokens, hp)
 
     tf32_peak = measure_tf32_peak() if args.precision == "tf32" and rank == 0 else None
     if rank != 0:
@@ -401,6 +463,7 @@ def run_ours(args, rank, world, local):
     pk = _peaks()
     Vp = g.Vp
     fpt = flops_per_token(cfg, Vp)
+    palm = palm_flops_per_token(cfg, Vp)
     ms_step = max_ms / K
     tokens = world * K * B * T
     value = tokens / (max_ms / 1000.0)
@@ -433,6 +496,8 @@ def run_ours(args, rank, world, local):
         "mfu": ({"algorithmic_flops_per_token": fpt,
                  "vs_measured_burst": value / world * fpt / (pk["bf16"] * 1e12),
                  "vs_measured_sustained": value / world * fpt / (pk["bf16_sus"] * 1e12),
+                 "palm_flops_per_token": palm,
+                 "palm_vs_measured_burst": value / world * palm / (pk["bf16"] * 1e12),
                  "peak": "the 40% target is judged against the measured dense bf16 burst peak (cuBLAS, "
                          "MEASURED_PEAKS.json), the larger of the two measured figures"}
                 if args.precision == "bf16" else
@@ -443,6 +508,7 @@ def run_ours(args, rank, world, local):
         "roofline": roofline,
         "kernels": kernels,
         "cpu_baseline": cpu,
+        **({"cpu_variants": cpu_var} if cpu_var else {}),
         "e2e": {"value": world * K * B * T / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 8, "clocks": clk_e2e},
         "gpu_launches": launches,
@@ -626,7 +692,11 @@ def main():
                          "measured in the same run)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=128,
-                    help="positions of the oracle's CPU sample (both arms), B=1")
+                    help="positions of the oracle's CPU sample (both arms), B=1, for workloads of more than "
+                         f"{FULL_STEP_TOKENS} tokens per step (smaller ones are timed in full)")
+    ap.add_argument("--cpu-variants", action="store_true",
+                    help="also time the double and float oracles on one thread and on every host core "
+                         "(cpu_variants; minutes at the 124M shapes)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

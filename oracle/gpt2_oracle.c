@@ -38,6 +38,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #ifdef ORACLE_REAL_FLOAT
 typedef float real;
@@ -821,3 +824,17 @@ OR_EXPORT void or_free(OracleModel* m) {
 }
 
 OR_EXPORT int or_real_bytes(void) { return (int)sizeof(real); }
+
+/* Threads of the OpenMP loops for later calls (n <= 0 keeps the setting); returns the
+ * count now in force (1 without OpenMP).  No result depends on it: every parallel loop
+ * gives each thread its own outputs (rows, output channels or (b, h) pairs), each
+ * computed in the listing's order. */
+OR_EXPORT int or_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}

@@ -59,6 +59,7 @@ def _lib(variant: str):
             "or_update": (i, [P, R, R, R, R, R, i]),
             "or_free": (None, [P]),
             "or_real_bytes": (i, []),
+            "or_set_threads": (i, [i]),
             "or_release_acts": (None, [P]),
             "or_sample_mult": (i, [P, i, R]),
             "or_generate": (i, [P, P, i, i, i, R, P, P]),
@@ -348,6 +349,12 @@ class Model:
             raise ValueError(f"or_generate failed with code {rc}")
         self.B = self.T = None
         return out
+
+
+def set_threads(n: int, variant: str = "f64") -> int:
+    """Threads of the oracle's OpenMP loops from now on (n <= 0 keeps them); returns the
+    count in force.  Results do not depend on it."""
+    return int(_lib(variant).or_set_threads(int(n)))
 
 
 def cpu_threads() -> int:

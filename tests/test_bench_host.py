@@ -46,3 +46,60 @@ def test_config_block_names_the_workload():
     blk = bench.config_block(c, "gpt2_124m")
     assert blk["workload"] == "gpt2_124m" and blk["B"] == 32 and blk["T"] == 1024 and blk["Vp"] == 50304
     assert bench.config_block(c, "gpt2_124m", "rmsnorm")["workload"] == "gpt2_124m_rmsnorm"
+
+
+def test_palm_flops_per_token_closed_form():
+    """6 N + 12 L C T with N = 12 L C^2 + 13 L C + (Vp + maxT) C + 2 C, the GPT-2
+    parameter count (per layer: qkv 3C^2 + 3C, attention projection C^2 + C, two
+    LayerNorms 4C, fc 4C^2 + 4C, fc projection 4C^2 + C; then wte, wpe and the final
+    LayerNorm): 0.860 GFLOP per token for GPT-2 124M at T = 1024."""
+    c = synth.WORKLOADS["gpt2_124m"]
+    L, C, T, maxT, Vp = c["L"], c["C"], c["T"], c["maxT"], 50304
+    n = 12 * L * C * C + 13 * L * C + (Vp + maxT) * C + 2 * C
+    assert n == 124_475_904
+    assert bench.palm_flops_per_token(c, Vp) == 6 * n + 12 * L * C * T == 860_101_632
+
+
+def test_cpu_sample_shape_and_extrapolation():
+    tiny, big = synth.WORKLOADS["tiny"], synth.WORKLOADS["gpt2_124m"]
+    assert bench.sample_shape(tiny, 128) == (tiny["B"], tiny["T"])    # timed in full
+    assert bench.sample_shape(big, 128) == (1, 128)
+    assert bench.sample_shape(big, 4096) == (1, 1024)
+    # a whole-step sample is not scaled: B*T tokens in t_fb + t_adam seconds
+    BT = tiny["B"] * tiny["T"]
+    assert bench.extrapolated_tokens_per_s(tiny, BT, 2.0, 1.0) == BT / 3.0
+    # B*T / 128 samples of fwd+bwd plus one AdamW
+    assert bench.extrapolated_tokens_per_s(big, 128, 0.5, 2.0) == 32768 / (256 * 0.5 + 2.0)
+
+
+def test_oracle_threads_change_no_result():
+    """The oracle's OpenMP loops give each thread its own outputs: one thread and several
+    give bitwise the same loss and gradients."""
+    import numpy as np
+    from oracle.oracle import Model, set_threads
+    c = synth.WORKLOADS["tiny"]
+    L, C, NH, V, maxT = c["L"], c["C"], c["NH"], c["V"], c["maxT"]
+    params = synth.init_params(L, C, V, maxT, seed=42)
+    inp, tgt = synth.batch(synth.token_stream(c, steps=1), 0, c["B"], c["T"])
+    prev = set_threads(0)
+    out = []
+    try:
+        for n in (1, 4):
+            assert set_threads(n) == n
+            m = Model(L, C, NH, V, maxT)
+            m.set_params(params)
+            loss = m.forward(inp, tgt)
+            m.backward()
+            out.append((loss, m.grads()))
+    finally:
+        set_threads(prev)
+    assert out[0][0] == out[1][0]
+    assert np.array_equal(out[0][1], out[1][1])
+
+
+def test_cpu_leg_one_thread_full_tiny_step():
+    c = synth.WORKLOADS["tiny"]
+    hp = (c["lr"], c["b1"], c["b2"], c["eps"], c["wd"])
+    v, used, text = bench.cpu_leg(c, "tiny", "layernorm", 128, hp, variant="f32", threads=1)
+    assert v > 0 and used == 1
+    assert text.startswith("full step") and "f32 oracle, one thread" in text
