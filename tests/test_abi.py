@@ -62,3 +62,30 @@ def test_build_rejects_bad_arguments_before_touching_the_device():
     assert st.value == N.GPT2_ERR_ARG
     assert not N.lib.gpt2_build_ex(1, 16, 4, 27, 16, 3, ct.byref(st))                 # unknown precision
     assert st.value == N.GPT2_ERR_ARG
+
+
+def test_gelu_bwd_bias_grad_rejects_bad_arguments_on_the_host():
+    """gpt2_op_matmul_gelu_bwd_bias_grad checks sizes, pointers and the workspace before
+    any CUDA call (no GPU needed); N = 0 is an empty call."""
+    from gpt_train_step_arena_b300 import _native as N
+    f = N.lib.gpt2_op_matmul_gelu_bwd_bias_grad
+    M, Nn, K = 300, 520, 448
+    need = N.lib.gpt2_op_matmul_gelu_bwd_bias_grad_workspace(M, Nn)
+    # the larger of ceil(M/32) x N group sums and the column-sum pass's partials, fp32
+    assert need >= ((M + 31) // 32) * Nn * 4
+    assert N.lib.gpt2_op_matmul_gelu_bwd_bias_grad_workspace(0, Nn) == 0
+    p = 4096   # never dereferenced: every call below stops at an argument check
+    args = dict(A=p, lda=K, ak=1, B=p, ldb=Nn, bk=0, D=p, ldd=Nn, P=p, ldp=Nn, db=p, ws=p, wsb=need)
+
+    def call(M=M, Nn=Nn, K=K, **kw):
+        a = dict(args, **kw)
+        return f(M, Nn, K, a["A"], a["lda"], a["ak"], a["B"], a["ldb"], a["bk"], a["D"], a["ldd"], a["P"],
+                 a["ldp"], a["db"], a["ws"], a["wsb"], None)
+
+    assert call(M=-1) == N.GPT2_ERR_ARG
+    assert call(Nn=0) == N.GPT2_OK
+    assert call(db=None) == N.GPT2_ERR_ARG
+    assert call(P=None) == N.GPT2_ERR_ARG
+    assert call(ws=None) == N.GPT2_ERR_ARG
+    assert call(wsb=need - 4) == N.GPT2_ERR_ARG and b"workspace" in N.lib.gpt2_op_last_error()
+    assert call(ws=p + 4) == N.GPT2_ERR_ARG      # not 8-byte aligned
