@@ -268,12 +268,13 @@ def cpu_sample_text(workload, B_s, T_s, t_fb, t_adam, variant="f64", threads="Op
 
 def cpu_leg(cfg, workload, norm, cpu_tokens, hp, t=1, variant="f64", threads=0):
     """The oracle timed on one sample step: (tokens/s of the whole step, threads used, sample text).
-    threads: 0 = the OpenMP default (every host core or OMP_NUM_THREADS), else that many."""
+    threads: 0 = the OpenMP default (the cores this process may run on, or OMP_NUM_THREADS),
+    else that many."""
     from oracle.oracle import set_threads
     B_s, T_s = sample_shape(cfg, cpu_tokens)
-    m, inp, tgt, cores = oracle_sample(cfg, B_s, T_s, norm=norm, variant=variant)
+    m, inp, tgt, _ = oracle_sample(cfg, B_s, T_s, norm=norm, variant=variant)
     prev = set_threads(0, variant)
-    used = set_threads(threads if threads > 0 else cores, variant)
+    used = set_threads(threads, variant) if threads > 0 else prev
     try:
         t_fb, t_adam = oracle_step_time(m, inp, tgt, hp, t)
     finally:
@@ -287,10 +288,9 @@ def cpu_leg(cfg, workload, norm, cpu_tokens, hp, t=1, variant="f64", threads=0):
 def cpu_variants(cfg, workload, norm, cpu_tokens, hp):
     """The double and float oracles, each on one thread and on every host core, on the same
     sample (one step each, after one untimed step)."""
-    from oracle.oracle import cpu_threads
     out = []
     for variant in ("f64", "f32"):
-        for threads in (1, cpu_threads()):
+        for threads in (1, 0):
             cpu_leg(cfg, workload, norm, cpu_tokens, hp, 1, variant, threads)   # untimed: page in, warm caches
             v, used, text = cpu_leg(cfg, workload, norm, cpu_tokens, hp, 2, variant, threads)
             out.append({"oracle": variant, "threads": used, "value": v, "unit": "tokens/s", "sample": text})
